@@ -1,0 +1,277 @@
+"""CSA2 CPU oracle (fp64 C, loaded through ctypes) -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg may import this package.  The CUDA library never links it, and
+it imports nothing from the CUDA package.  See ``csa2_oracle.h`` for the
+sources, readings and canonical layouts.
+
+Every numpy-level function below marshals arrays and calls the C code; no
+arithmetic of the method is done here.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIBDIR = os.path.join(_HERE, "_lib")
+_LIB = os.path.join(_LIBDIR, "libcsa2_oracle.so")
+_SRC = os.path.join(_HERE, "csa2_oracle.c")
+_lock = threading.Lock()
+_lib = None
+
+CACHE_FP4 = 0
+CACHE_BF16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, no FP contraction so x86 and Arm agree)."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "csa2_oracle.h"))):
+        return _LIB
+    tmp = _LIB + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = C.CDLL(_LIB)
+            vp, i, d = C.c_void_p, C.c_int, C.c_double
+            L.orc_bf16_value.restype = d
+            L.orc_bf16_value.argtypes = [C.c_uint16]
+            L.orc_bf16_round.restype = C.c_uint16
+            L.orc_bf16_round.argtypes = [d]
+            L.orc_e2m1_value.restype = d
+            L.orc_e2m1_value.argtypes = [i]
+            L.orc_e4m3_value.restype = d
+            L.orc_e4m3_value.argtypes = [i]
+            L.orc_e4m3_nearest_code.restype = i
+            L.orc_e4m3_nearest_code.argtypes = [d]
+            L.orc_e2m1_nearest_code.restype = i
+            L.orc_e2m1_nearest_code.argtypes = [d, d]
+            L.orc_fp4_encode.argtypes = [vp, i, vp, vp]
+            L.orc_fp4_decode.argtypes = [vp, vp, i, vp]
+            L.orc_compress.restype = i
+            L.orc_compress.argtypes = [i, i, i, i, i, i, d, i, vp, vp, vp, vp, i,
+                                       vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.orc_index_topk.restype = i
+            L.orc_index_topk.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i, i, i,
+                                         vp, vp, vp, vp]
+            L.orc_attend.restype = i
+            L.orc_attend.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, i, vp, i, vp, vp, vp,
+                                     i, d, vp, vp]
+            L.orc_attend_dense.restype = i
+            L.orc_attend_dense.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, i, vp, vp, vp,
+                                           i, d, vp]
+            L.orc_threads.restype = i
+            _lib = L
+    return _lib
+
+
+def threads() -> int:
+    return lib().orc_threads()
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- codecs ----
+
+def bf16_value(bits: int) -> float:
+    return lib().orc_bf16_value(int(bits))
+
+
+def bf16_round(x: float) -> int:
+    return lib().orc_bf16_round(float(x))
+
+
+def e2m1_value(code: int) -> float:
+    return lib().orc_e2m1_value(int(code))
+
+
+def e4m3_value(byte: int) -> float:
+    return lib().orc_e4m3_value(int(byte))
+
+
+def e4m3_nearest_code(y: float) -> int:
+    return lib().orc_e4m3_nearest_code(float(y))
+
+
+def e2m1_nearest_code(x: float, scale: float) -> int:
+    return lib().orc_e2m1_nearest_code(float(x), float(scale))
+
+
+def fp4_encode(x: np.ndarray):
+    """x [..., C] fp64 -> (codes [..., C/2] u8, scales [..., C/16] u8)."""
+    x = _c(x, np.float64)
+    Cn = x.shape[-1]
+    rows = x.reshape(-1, Cn)
+    codes = np.zeros((rows.shape[0], Cn // 2), np.uint8)
+    scales = np.zeros((rows.shape[0], Cn // 16), np.uint8)
+    L = lib()
+    for n in range(rows.shape[0]):
+        L.orc_fp4_encode(_p(rows[n]), Cn, _p(codes[n]), _p(scales[n]))
+    return codes.reshape(x.shape[:-1] + (Cn // 2,)), scales.reshape(x.shape[:-1] + (Cn // 16,))
+
+
+def fp4_decode(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    Cn = codes.shape[-1] * 2
+    cr = codes.reshape(-1, Cn // 2)
+    sr = scales.reshape(-1, Cn // 16)
+    out = np.zeros((cr.shape[0], Cn), np.float64)
+    L = lib()
+    for n in range(cr.shape[0]):
+        L.orc_fp4_decode(_p(cr[n]), _p(sr[n]), Cn, _p(out[n]))
+    return out.reshape(codes.shape[:-1] + (Cn,))
+
+
+# ------------------------------------------------------------- the path ----
+
+class Cache:
+    """Canonical (unpaged) cache of B sequences x n_cap entries of `channels`."""
+
+    def __init__(self, B: int, n_cap: int, channels: int, dtype: str):
+        self.B, self.n_cap, self.channels, self.dtype = B, n_cap, channels, dtype
+        if dtype == "fp4":
+            self.codes = np.zeros((B, n_cap, channels // 2), np.uint8)
+            self.scales = np.zeros((B, n_cap, channels // 16), np.uint8)
+            self.bf16 = None
+        elif dtype == "bf16":
+            self.codes = self.scales = None
+            self.bf16 = np.zeros((B, n_cap, channels), np.uint16)
+        else:
+            raise ValueError(dtype)
+
+    @property
+    def dtype_code(self) -> int:
+        return CACHE_FP4 if self.dtype == "fp4" else CACHE_BF16
+
+    def values(self) -> np.ndarray:
+        """Decoded fp64 entries [B][n_cap][channels]."""
+        if self.dtype == "fp4":
+            return fp4_decode(self.codes, self.scales)
+        return (self.bf16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def compress(x, pos0, w, w_idx, main: Cache, idx: Cache, r: int, theta: float, rope_dims: int = 64,
+             diagnostics: bool = False):
+    """a1: merge + RoPE + encode into `main`, then project + encode into `idx`.
+    x [B][T][D] bf16 bits, pos0 [B] int64, w [r][D] fp32, w_idx [D][Ci] bf16 bits."""
+    x = _c(x, np.uint16)
+    pos0 = _c(pos0, np.int64)
+    w = _c(w, np.float32)
+    w_idx = _c(w_idx, np.uint16)
+    B, T, D = x.shape
+    Ci = w_idx.shape[1]
+    M = T // r
+    diag = {}
+    if diagnostics:
+        for k, n in (("pre_main", D), ("mag_main", D), ("pre_idx", Ci), ("mag_idx", Ci)):
+            diag[k] = np.zeros((B, M, n), np.float64)
+    rc = lib().orc_compress(B, T, D, Ci, rope_dims, r, float(theta), main.dtype_code,
+                            _p(x), _p(pos0), _p(w), _p(w_idx), main.n_cap,
+                            _p(main.codes), _p(main.scales), _p(main.bf16),
+                            _p(idx.codes), _p(idx.scales), _p(idx.bf16),
+                            _p(diag.get("pre_main")), _p(diag.get("mag_main")),
+                            _p(diag.get("pre_idx")), _p(diag.get("mag_idx")))
+    if rc != 0:
+        raise ValueError("orc_compress rejected its arguments (%d)" % rc)
+    return diag
+
+
+def index_topk(idx: Cache, n_entries, q_idx, q_pos, r: int, k: int, head_w=None, hsi_blocks: int = 0,
+               hsi_block: int = 8, pool=None, want_pool: bool = False, want_scores: bool = False):
+    """a3-a6.  q_idx [B][Tq][H][Ci] bf16 bits, q_pos [B][Tq] int64.
+    Returns (topk [B][Tq][k] int32, pool [B][Tq][hsi_blocks] or None, scores or None)."""
+    q_idx = _c(q_idx, np.uint16)
+    B, Tq, H, Ci = q_idx.shape
+    n_entries = _c(n_entries, np.int32)
+    q_pos = _c(q_pos, np.int64)
+    hw = None if head_w is None else _c(head_w, np.float32)
+    pl = None if pool is None else _c(pool, np.int32)
+    topk = np.zeros((B, Tq, k), np.int32)
+    pool_out = np.zeros((B, Tq, hsi_blocks), np.int32) if want_pool else None
+    scores = np.zeros((B, Tq, idx.n_cap), np.float64) if want_scores else None
+    rc = lib().orc_index_topk(B, Tq, H, Ci, r, idx.dtype_code, idx.n_cap, _p(idx.codes),
+                              _p(idx.scales), _p(idx.bf16), _p(n_entries), _p(q_idx), _p(hw),
+                              _p(q_pos), k, hsi_blocks, hsi_block, _p(pl), _p(topk), _p(pool_out),
+                              _p(scores))
+    if rc != 0:
+        raise ValueError("orc_index_topk rejected its arguments (%d)" % rc)
+    return topk, pool_out, scores
+
+
+def attend(main: Cache, n_entries, q, topk, swa, swa_len, swa_pos0, q_pos, window: int, scale: float,
+           want_lse: bool = False):
+    """a7.  q [B][Tq][Hm][D] bf16 bits, topk [B][Tq][k], swa [B][S][D] bf16 bits.
+    Returns out [B][Tq][Hm][D] fp64 (and lse [B][Tq][Hm])."""
+    q = _c(q, np.uint16)
+    B, Tq, Hm, D = q.shape
+    topk = _c(topk, np.int32)
+    k = topk.shape[-1]
+    swa = _c(swa, np.uint16)
+    S = swa.shape[1]
+    out = np.zeros((B, Tq, Hm, D), np.float64)
+    lse = np.zeros((B, Tq, Hm), np.float64) if want_lse else None
+    rc = lib().orc_attend(B, Tq, Hm, D, main.dtype_code, main.n_cap, _p(main.codes), _p(main.scales),
+                          _p(main.bf16), _p(_c(n_entries, np.int32)), _p(q), _p(topk), k, _p(swa), S,
+                          _p(_c(swa_len, np.int32)), _p(_c(swa_pos0, np.int64)), _p(_c(q_pos, np.int64)),
+                          window, float(scale), _p(out), _p(lse))
+    if rc != 0:
+        raise ValueError("orc_attend rejected its arguments (%d)" % rc)
+    return (out, lse) if want_lse else out
+
+
+def attend_dense(main: Cache, n_entries, q, swa, swa_len, swa_pos0, q_pos, r: int, window: int,
+                 scale: float):
+    q = _c(q, np.uint16)
+    B, Tq, Hm, D = q.shape
+    swa = _c(swa, np.uint16)
+    S = swa.shape[1]
+    out = np.zeros((B, Tq, Hm, D), np.float64)
+    rc = lib().orc_attend_dense(B, Tq, Hm, D, r, main.dtype_code, main.n_cap, _p(main.codes),
+                                _p(main.scales), _p(main.bf16), _p(_c(n_entries, np.int32)), _p(q),
+                                _p(swa), S, _p(_c(swa_len, np.int32)), _p(_c(swa_pos0, np.int64)),
+                                _p(_c(q_pos, np.int64)), window, float(scale), _p(out))
+    if rc != 0:
+        raise ValueError("orc_attend_dense rejected its arguments (%d)" % rc)
+    return out
+
+
+# ------------------------------------------------------ cross-layer modes ----
+
+def layer_modes(schedule):
+    """a8: for a [(layer, mode)] schedule, map each layer to (mode, index source
+    layer).  A Reuse layer reads the top-k of the latest earlier Full/Reindex
+    layer; Full/Reindex layers publish their own."""
+    out, latest = {}, None
+    for layer, mode in schedule:
+        if mode in ("full", "reindex"):
+            latest = layer
+            out[layer] = (mode, layer)
+        elif mode == "reuse":
+            if latest is None:
+                raise ValueError("Reuse layer %d has no earlier indexing layer" % layer)
+            out[layer] = (mode, latest)
+        else:
+            raise ValueError(mode)
+    return out

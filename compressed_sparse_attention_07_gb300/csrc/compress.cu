@@ -1,0 +1,129 @@
+// a1 -- CSA2 compressor: merge r tokens per entry with per-channel weights,
+// RoPE at the entry's last covered position, encode into the paged main
+// cache, project the stored entry to indexer K and encode that too.
+// (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.3.1 and sec. 2.4.4; 36kr "CSA2",
+// "FP4 and Bounded Replay".)  One CTA per new entry; this step moves a few KB
+// per entry, so it is latency-bound and kept simple.
+#include "internal.h"
+
+namespace csa2 {
+namespace {
+
+template <int kDtype>
+__global__ void __launch_bounds__(256) compress_kernel(int T, int r, double theta, const uint16_t* __restrict__ x,
+                                                       const int64_t* __restrict__ pos0,
+                                                       const float* __restrict__ merge_w,
+                                                       const uint16_t* __restrict__ w_idx, CacheView mc,
+                                                       CacheView ic, int32_t* n_entries, int32_t* status) {
+  __shared__ float e_s[kDim];          // the stored (decoded) entry
+  __shared__ float kpart[2][kIdxDim];  // projection halves
+  const int m = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  const int64_t j = pos0[b] / r + m;
+
+  // merge: thread t owns channels 2t and 2t+1
+  float v0 = 0.0f, v1 = 0.0f;
+  for (int i = 0; i < r; ++i) {
+    const uint16_t* xr = x + ((int64_t)b * T + (int64_t)m * r + i) * kDim;
+    uint32_t pair = __ldg(reinterpret_cast<const uint32_t*>(xr) + t);
+    float x0 = __uint_as_float(pair << 16), x1 = __uint_as_float(pair & 0xFFFF0000u);
+    float w0 = __ldg(merge_w + i * kDim + 2 * t), w1 = __ldg(merge_w + i * kDim + 2 * t + 1);
+    v0 = (i == 0) ? w0 * x0 : fmaf(w0, x0, v0);
+    v1 = (i == 0) ? w1 * x1 : fmaf(w1, x1, v1);
+  }
+  // RoPE on the pair (2t, 2t+1) for the first 64 channels; angle in fp64
+  if (t < kRope / 2) {
+    double p = (double)(r * j + r - 1);
+    double ang = p * pow(theta, -2.0 * t / kRope);
+    double sd, cd;
+    sincos(ang, &sd, &cd);
+    float c = (float)cd, s = (float)sd;
+    float a = v0, bb = v1;
+    v0 = fmaf(a, c, -(bb * s));
+    v1 = fmaf(a, s, bb * c);
+  }
+
+  const int64_t page = page_of(mc, b, j, status);
+  const int slot = (int)(j % kPage);
+  if (kDtype == CSA2_CACHE_FP4) {
+    float amax = fmaxf(fabsf(v0), fabsf(v1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    int sc = e4m3_scale_code(amax);
+    float s = e4m3_pos(sc);
+    uint32_t c0 = e2m1_code(v0, s), c1 = e2m1_code(v1, s);
+    if (page >= 0) {
+      mc.data[page * kMainFp4Data + slot * (kDim / 2) + t] = (uint8_t)(c0 | (c1 << 4));
+      if ((t & 7) == 0) mc.scales[page * kMainFp4Scales + slot * (kDim / 16) + (t >> 3)] = (uint8_t)sc;
+    }
+    e_s[2 * t] = e2m1_to_float(c0) * s;
+    e_s[2 * t + 1] = e2m1_to_float(c1) * s;
+  } else {
+    __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
+    uint32_t packed = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+    if (page >= 0)
+      reinterpret_cast<uint32_t*>(mc.data + page * kMainBf16Data + slot * (kDim * 2))[t] = packed;
+    e_s[2 * t] = __bfloat162float(h0);
+    e_s[2 * t + 1] = __bfloat162float(h1);
+  }
+  __syncthreads();
+
+  // indexer K = stored entry . W_idx; two halves of the channel sum
+  {
+    const int k = t & (kIdxDim - 1), half = t >> 7;
+    float acc = 0.0f;
+    const int c0 = half * (kDim / 2);
+#pragma unroll 8
+    for (int c = c0; c < c0 + kDim / 2; ++c)
+      acc = fmaf(e_s[c], bf16_bits_to_float(__ldg(w_idx + c * kIdxDim + k)), acc);
+    kpart[half][k] = acc;
+  }
+  __syncthreads();
+  if (t < kIdxDim) {
+    const float kv = kpart[0][t] + kpart[1][t];
+    const int64_t ipage = page_of(ic, b, j, status);
+    if (kDtype == CSA2_CACHE_FP4) {
+      float amax = fabsf(kv);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      int sc = e4m3_scale_code(amax);
+      uint32_t code = e2m1_code(kv, e4m3_pos(sc));
+      uint32_t hi = __shfl_xor_sync(0xffffffffu, code, 1);
+      if (ipage >= 0 && (t & 1) == 0) {
+        int bi = t >> 1;  // byte index 0..63 -> 16-byte chunk bi/16
+        ic.data[ipage * kIdxFp4Data + ((bi >> 4) * kPage + slot) * 16 + (bi & 15)] = (uint8_t)(code | (hi << 4));
+      }
+      if (ipage >= 0 && (t & 15) == 0) ic.scales[ipage * kIdxFp4Scales + slot * (kIdxDim / 16) + (t >> 4)] = (uint8_t)sc;
+    } else {
+      uint16_t h = __bfloat16_as_ushort(__float2bfloat16_rn(kv));
+      if (ipage >= 0) {
+        int byte = 2 * t;  // chunk byte/16
+        *reinterpret_cast<uint16_t*>(ic.data + ipage * kIdxBf16Data + ((byte >> 4) * kPage + slot) * 16 +
+                                     (byte & 15)) = h;
+      }
+    }
+  }
+  if (m == gridDim.x - 1 && t == 0) n_entries[b] = (int32_t)(j + 1);
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const csa2_cfg& cfg, int B, int T, const uint16_t* x, const int64_t* pos0,
+                            const float* merge_w, const uint16_t* w_idx, const csa2_cache& main_c,
+                            const csa2_cache& idx_c, int32_t* n_entries, int32_t* status,
+                            cudaStream_t stream) {
+  const int M = T / cfg.ratio;
+  if (M == 0 || B == 0) return cudaSuccess;
+  dim3 grid(M, B);
+  if (cfg.cache_dtype == CSA2_CACHE_FP4)
+    compress_kernel<CSA2_CACHE_FP4><<<grid, 256, 0, stream>>>(T, cfg.ratio, cfg.rope_theta, x, pos0, merge_w,
+                                                              w_idx, view_of(main_c), view_of(idx_c),
+                                                              n_entries, status);
+  else
+    compress_kernel<CSA2_CACHE_BF16><<<grid, 256, 0, stream>>>(T, cfg.ratio, cfg.rope_theta, x, pos0, merge_w,
+                                                               w_idx, view_of(main_c), view_of(idx_c),
+                                                               n_entries, status);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

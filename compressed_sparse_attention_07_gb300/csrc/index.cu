@@ -1,0 +1,371 @@
+// a3..a6 -- CSA2 lightweight indexer: per-query scores over the visible
+// indexer-K entries (or over an HSI pool), HSI block maxima, and exact
+// top-k selection with the (score desc, id asc) order.
+// (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.3.1, 2.3.2, 2.3.4; 36kr "CSA2".)
+#include <algorithm>
+
+#include "internal.h"
+
+namespace csa2 {
+namespace {
+
+constexpr int kScoreThreads = 128;  // one entry per thread
+constexpr int kSelThreads = 1024;   // one CTA selects for one query
+constexpr uint32_t kInvalid = 0xFFFFFFFFu;  // score bit pattern of a non-candidate
+
+// Decoded indexer-K entry (128 channels) of sequence b, slot j, into registers.
+template <int kDtype>
+__device__ __forceinline__ bool load_idx_entry(const CacheView& ic, int b, int64_t j, float (&kv)[kIdxDim],
+                                               int32_t* status) {
+  const int64_t page = page_of(ic, b, j, status);
+  if (page < 0) return false;
+  const int slot = (int)(j % kPage);
+  if (kDtype == CSA2_CACHE_FP4) {
+    const uint8_t* base = ic.data + page * kIdxFp4Data;
+    uint2 sc = __ldg(reinterpret_cast<const uint2*>(ic.scales + page * kIdxFp4Scales + slot * 8));
+    uint32_t sw[2] = {sc.x, sc.y};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (c * kPage + slot) * 16));
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+          const int ch = c * 32 + q * 8 + n;  // channel
+          const int g = ch >> 4;
+          float s = e4m3_to_float((sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+          kv[ch] = e2m1_to_float((w[q] >> (4 * n)) & 15u) * s;
+        }
+      }
+    }
+  } else {
+    const uint8_t* base = ic.data + page * kIdxBf16Data;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (c * kPage + slot) * 16));
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        kv[c * 8 + 2 * q] = __uint_as_float(w[q] << 16);
+        kv[c * 8 + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+      }
+    }
+  }
+  return true;
+}
+
+// s = sum_h w_h ReLU(q_h . K) with q in shared memory (fp32), -0 folded to +0.
+__device__ __forceinline__ float index_score(const float (*qs)[kIdxDim], const float* hw, const float (&kv)[kIdxDim]) {
+  float acc = 0.0f;
+#pragma unroll 1
+  for (int h = 0; h < kIdxHeads; ++h) {
+    float d = 0.0f;
+    const float4* q4 = reinterpret_cast<const float4*>(qs[h]);
+#pragma unroll
+    for (int c = 0; c < kIdxDim / 4; ++c) {
+      float4 q = q4[c];
+      d = fmaf(q.x, kv[4 * c], d);
+      d = fmaf(q.y, kv[4 * c + 1], d);
+      d = fmaf(q.z, kv[4 * c + 2], d);
+      d = fmaf(q.w, kv[4 * c + 3], d);
+    }
+    acc = fmaf(hw[h], fmaxf(d, 0.0f), acc);
+  }
+  return acc + 0.0f;
+}
+
+__device__ __forceinline__ void load_query(int qi, const uint16_t* q_idx, const float* head_w,
+                                           float (*qs)[kIdxDim], float* hw) {
+  const uint16_t* qp = q_idx + (int64_t)qi * kIdxHeads * kIdxDim;
+  for (int i = threadIdx.x; i < kIdxHeads * kIdxDim; i += blockDim.x)
+    qs[i / kIdxDim][i % kIdxDim] = bf16_bits_to_float(__ldg(qp + i));
+  if (threadIdx.x < kIdxHeads) hw[threadIdx.x] = head_w ? __ldg(head_w + (int64_t)qi * kIdxHeads + threadIdx.x) : 1.0f;
+  __syncthreads();
+}
+
+// Full: every visible entry.  scores [chunk][max_entries], bmax [chunk][ceil(max_entries/8)].
+template <int kDtype>
+__global__ void __launch_bounds__(kScoreThreads) score_full_kernel(int q0, int Tq, int r, const uint16_t* __restrict__ q_idx,
+                                                                   const float* __restrict__ head_w,
+                                                                   const int64_t* __restrict__ q_pos, CacheView ic,
+                                                                   const int32_t* __restrict__ n_entries,
+                                                                   int64_t max_entries, float* scores, float* bmax,
+                                                                   int32_t* status) {
+  __shared__ __align__(16) float qs[kIdxHeads][kIdxDim];
+  __shared__ float hw[kIdxHeads];
+  const int qi = q0 + blockIdx.y, b = qi / Tq;
+  const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
+  const int64_t j0 = (int64_t)blockIdx.x * kScoreThreads;
+  if (j0 >= nv) return;
+  load_query(qi, q_idx, head_w, qs, hw);
+  const int64_t j = j0 + threadIdx.x;
+  float s = -INFINITY;
+  if (j < nv) {
+    float kv[kIdxDim];
+    if (load_idx_entry<kDtype>(ic, b, j, kv, status)) s = index_score(qs, hw, kv);
+    scores[(int64_t)blockIdx.y * max_entries + j] = s;
+  }
+  if (bmax) {
+    float m = s;
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    if ((threadIdx.x & 7) == 0 && j < nv) bmax[(int64_t)blockIdx.y * ((max_entries + 7) / 8) + j / 8] = m;
+  }
+}
+
+// Reindex: the visible entries of the pool's blocks; position p -> block
+// pool[p / 8], entry block * 8 + p % 8.  scores [chunk][n_blocks * 8].
+template <int kDtype>
+__global__ void __launch_bounds__(kScoreThreads) score_pool_kernel(int q0, int Tq, int r, int n_blocks,
+                                                                   const uint16_t* __restrict__ q_idx,
+                                                                   const float* __restrict__ head_w,
+                                                                   const int64_t* __restrict__ q_pos, CacheView ic,
+                                                                   const int32_t* __restrict__ n_entries,
+                                                                   int64_t max_entries, const int32_t* __restrict__ pool,
+                                                                   float* scores, int32_t* status) {
+  __shared__ __align__(16) float qs[kIdxHeads][kIdxDim];
+  __shared__ float hw[kIdxHeads];
+  const int qi = q0 + blockIdx.y, b = qi / Tq;
+  const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
+  load_query(qi, q_idx, head_w, qs, hw);
+  const int64_t p = (int64_t)blockIdx.x * kScoreThreads + threadIdx.x;
+  const int64_t npos = (int64_t)n_blocks * kHsiBlock;
+  if (p >= npos) return;
+  const int32_t blk = __ldg(pool + (int64_t)qi * n_blocks + p / kHsiBlock);
+  float s = __uint_as_float(kInvalid);
+  if (blk >= 0) {
+    const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
+    if ((int64_t)blk * kHsiBlock >= max_entries) {
+      if (p % kHsiBlock == 0) report(status, CSA2_ERR_BAD_INDEX);
+    } else if (j < nv) {
+      float kv[kIdxDim];
+      if (load_idx_entry<kDtype>(ic, b, j, kv, status)) s = index_score(qs, hw, kv);
+    }
+  }
+  scores[(int64_t)blockIdx.y * npos + p] = s;
+}
+
+// ---------------------------------------------------------------- select ----
+
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if (u == kInvalid) return 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix sum over the CTA (kSelThreads threads); returns the total.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t w = warp_sums[lane];
+    uint32_t ws = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, ws, o);
+      if (lane >= o) ws += y;
+    }
+    warp_sums[lane] = ws - w;  // exclusive
+    if (lane == 31) warp_sums[32] = ws;
+  }
+  __syncthreads();
+  uint32_t res = warp_sums[wid] + x - v;
+  total = warp_sums[32];
+  __syncthreads();
+  return res;
+}
+
+// id emitted for position p
+struct IdMap {
+  const int32_t* pool;  // Reindex: pool row of this query; NULL: id = p
+  __device__ __forceinline__ int32_t operator()(int64_t p) const {
+    return pool ? pool[p / kHsiBlock] * kHsiBlock + (int32_t)(p % kHsiBlock) : (int32_t)p;
+  }
+};
+
+// Select the k largest keys among n positions of `vals` ((key desc, position
+// asc)); `forced` (>= 0) gets the largest key.  Writes ids ascending to out[k],
+// -1 padded.  Radix select (11/11/10-bit digits) then an ordered compaction.
+__device__ void block_select(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out) {
+  __shared__ uint32_t hist[2048];
+  __shared__ uint32_t warp_sums[33];
+  __shared__ uint32_t sh_krem, sh_digit;
+  auto key_at = [&](int64_t p) -> uint32_t { return p == forced ? 0xFFFFFFFFu : order_key(vals[p]); };
+
+  // count valid candidates
+  uint32_t cnt = 0;
+  for (int64_t p = threadIdx.x; p < n; p += kSelThreads) cnt += key_at(p) != 0u;
+  uint32_t nvalid;
+  block_exclusive_scan(cnt, warp_sums, nvalid);
+
+  uint32_t T = 0, krem = 0;  // select key > T, plus the first krem keys == T
+  if (nvalid > (uint32_t)k) {
+    uint32_t prefix = 0, pmask = 0;
+    krem = (uint32_t)k;
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+      const int sh = shifts[pass];
+      const uint32_t dmask = (1u << widths[pass]) - 1u;
+      for (int i = threadIdx.x; i < 2048; i += kSelThreads) hist[i] = 0;
+      __syncthreads();
+      for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
+        uint32_t kk = key_at(p);
+        if (kk != 0u && (kk & pmask) == prefix) atomicAdd(&hist[(kk >> sh) & dmask], 1u);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        // lane L owns bins [2048 - 64(L+1), 2048 - 64L): scan from the top
+        const int lane = threadIdx.x;
+        uint32_t s = 0;
+        for (int i = 0; i < 64; ++i) s += hist[2047 - 64 * lane - i];
+        uint32_t incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        uint32_t excl = incl - s;  // keys in higher bins than this lane's chunk
+        const uint32_t kr = (pass == 0) ? (uint32_t)k : sh_krem;
+        if (excl < kr && incl >= kr) {
+          uint32_t above = excl;
+          for (int i = 0; i < 64; ++i) {
+            int d = 2047 - 64 * lane - i;
+            if (above + hist[d] >= kr) {
+              sh_digit = (uint32_t)d;
+              sh_krem = kr - above;
+              break;
+            }
+            above += hist[d];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= sh_digit << sh;
+      pmask |= dmask << sh;
+      __syncthreads();
+    }
+    T = prefix;
+    krem = sh_krem;
+  }
+
+  // ordered compaction: thread t scans the contiguous segment [t*seg, (t+1)*seg)
+  const int64_t seg = (n + kSelThreads - 1) / kSelThreads;
+  const int64_t lo = (int64_t)threadIdx.x * seg, hi = lo + seg < n ? lo + seg : n;
+  uint32_t gt = 0, eq = 0;
+  for (int64_t p = lo; p < hi; ++p) {
+    uint32_t kk = key_at(p);
+    gt += kk > T;
+    eq += (kk == T) && (T != 0u);
+  }
+  uint32_t eq_total;
+  uint32_t eq_before = block_exclusive_scan(eq, warp_sums, eq_total);
+  uint32_t take = krem > eq_before ? min(krem - eq_before, eq) : 0u;
+  uint32_t total;
+  uint32_t off = block_exclusive_scan(gt + take, warp_sums, total);
+  for (int64_t p = lo; p < hi && off < (uint32_t)k; ++p) {
+    uint32_t kk = key_at(p);
+    if (kk > T) {
+      out[off++] = idmap(p);
+    } else if (kk == T && T != 0u && take > 0) {
+      out[off++] = idmap(p);
+      --take;
+    }
+  }
+  for (uint32_t i = total + threadIdx.x; i < (uint32_t)k; i += kSelThreads) out[i] = -1;
+}
+
+// blockIdx.y == 0: entry top-k; == 1: HSI block pool (Full) .
+__global__ void __launch_bounds__(kSelThreads) select_kernel(int q0, int Tq, int r, int k, int n_blocks, int64_t max_entries,
+                                                             const int64_t* __restrict__ q_pos,
+                                                             const int32_t* __restrict__ n_entries,
+                                                             const int32_t* __restrict__ pool, const float* scores,
+                                                             const float* bmax, int64_t score_stride,
+                                                             int32_t* topk_out, int32_t* pool_out) {
+  const int qc = blockIdx.x, qi = q0 + qc, b = qi / Tq;
+  const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
+  if (blockIdx.y == 0) {
+    const float* v = scores + (int64_t)qc * score_stride;
+    if (pool) {
+      block_select(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks},
+                   topk_out + (int64_t)qi * k);
+    } else {
+      block_select(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k);
+    }
+  } else {
+    const int64_t nb = (nv + kHsiBlock - 1) / kHsiBlock;
+    const float* v = bmax + (int64_t)qc * ((max_entries + 7) / 8);
+    block_select(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks);
+  }
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex) {
+  if (reindex) return align256((size_t)cfg.hsi_blocks * kHsiBlock * sizeof(float));
+  size_t b = align256((size_t)max_entries * sizeof(float));
+  if (cfg.hsi_blocks > 0) b += align256((size_t)((max_entries + 7) / 8) * sizeof(float));
+  return b;
+}
+
+cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx,
+                              const float* head_w, const int64_t* q_pos, const csa2_cache& idx_c,
+                              const int32_t* n_entries, int max_entries, const int32_t* pool,
+                              int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
+                              int32_t* status, cudaStream_t stream) {
+  const int Q = B * Tq;
+  if (Q == 0) return cudaSuccess;
+  const bool reindex = pool != nullptr;
+  const size_t per_q = index_query_ws_bytes(cfg, max_entries, reindex);
+  const int chunk = (int)std::min<size_t>((size_t)Q, ws_bytes / per_q);
+  if (chunk < 1) return cudaErrorInvalidValue;
+  float* scores = static_cast<float*>(ws);
+  const int64_t stride = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
+  float* bmax = (!reindex && pool_out) ? reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                                                    align256((size_t)chunk * stride * sizeof(float)))
+                                       : nullptr;
+  const CacheView iv = view_of(idx_c);
+  for (int q0 = 0; q0 < Q; q0 += chunk) {
+    const int nq = std::min(chunk, Q - q0);
+    if (reindex) {
+      dim3 g((unsigned)((stride + kScoreThreads - 1) / kScoreThreads), nq);
+      if (cfg.cache_dtype == CSA2_CACHE_FP4)
+        score_pool_kernel<CSA2_CACHE_FP4><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, cfg.hsi_blocks, q_idx, head_w,
+                                                                          q_pos, iv, n_entries, max_entries, pool,
+                                                                          scores, status);
+      else
+        score_pool_kernel<CSA2_CACHE_BF16><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, cfg.hsi_blocks, q_idx, head_w,
+                                                                           q_pos, iv, n_entries, max_entries, pool,
+                                                                           scores, status);
+    } else {
+      dim3 g((unsigned)((max_entries + kScoreThreads - 1) / kScoreThreads), nq);
+      if (cfg.cache_dtype == CSA2_CACHE_FP4)
+        score_full_kernel<CSA2_CACHE_FP4><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, q_idx, head_w, q_pos, iv,
+                                                                          n_entries, max_entries, scores, bmax, status);
+      else
+        score_full_kernel<CSA2_CACHE_BF16><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, q_idx, head_w, q_pos, iv,
+                                                                           n_entries, max_entries, scores, bmax, status);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 sg(nq, (!reindex && pool_out) ? 2 : 1);
+    select_kernel<<<sg, kSelThreads, 0, stream>>>(q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, max_entries, q_pos,
+                                                  n_entries, pool, scores, bmax, stride, topk_out, pool_out);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace csa2

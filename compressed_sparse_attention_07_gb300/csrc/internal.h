@@ -1,0 +1,39 @@
+// Internal launcher declarations shared by the CSA2 translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+#include "csa2_device.cuh"
+
+namespace csa2 {
+
+inline CacheView view_of(const csa2_cache& c) {
+  return CacheView{static_cast<uint8_t*>(c.data), static_cast<uint8_t*>(c.scales), c.block_table,
+                   c.max_pages, c.num_pages};
+}
+
+cudaError_t launch_compress(const csa2_cfg& cfg, int B, int T, const uint16_t* x, const int64_t* pos0,
+                            const float* merge_w, const uint16_t* w_idx, const csa2_cache& main_c,
+                            const csa2_cache& idx_c, int32_t* n_entries, int32_t* status,
+                            cudaStream_t stream);
+
+// Per-query workspace bytes of the indexer (scores + HSI block maxima).
+size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex);
+
+cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx,
+                              const float* head_w, const int64_t* q_pos, const csa2_cache& idx_c,
+                              const int32_t* n_entries, int max_entries, const int32_t* pool,
+                              int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
+                              int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q, const csa2_cache& main_c,
+                          const int32_t* n_entries, const int32_t* topk, const uint16_t* swa, int S,
+                          const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos,
+                          float scale, float* out, float* lse, int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_gather_dequant(const csa2_cache& c, int cache_dtype, int B, int n, const int32_t* ids,
+                                  float* out, int32_t* status, cudaStream_t stream);
+
+}  // namespace csa2

@@ -1,0 +1,93 @@
+"""Test-side conversion between the oracle's canonical (unpaged) caches and the
+library's paged device caches, written from the layout documented in
+include/csa2.h.  Index shuffling only: no arithmetic of the method."""
+import numpy as np
+import torch
+
+import compressed_sparse_attention_07_gb300 as csa
+
+PAGE = 64
+
+
+def dev(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """numpy -> device tensor; uint16 bit patterns travel as int16."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(device)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    a = t.detach().cpu().numpy()
+    return a.view(np.uint16) if a.dtype == np.int16 else a
+
+
+def page_order(seed: int, n: int) -> np.ndarray:
+    """A seeded permutation of the page pool (fragmented page tables)."""
+    return np.random.default_rng(seed).permutation(n)
+
+
+def _pad_entries(a: np.ndarray, cap: int) -> np.ndarray:
+    B, N = a.shape[:2]
+    if N == cap:
+        return a
+    out = np.zeros((B, cap) + a.shape[2:], a.dtype)
+    out[:, :N] = a
+    return out
+
+
+def _page_bytes(cache: csa.PagedCache, canon_codes: np.ndarray, canon_scales):
+    """Canonical [B][cap][...] -> per-page byte rows in block-table order."""
+    B, mp = cache.batch, cache.max_pages
+    C_ = cache.channels
+    codes = _pad_entries(canon_codes, cache.capacity)
+    if cache.cache_dtype == csa.CACHE_FP4:
+        cb = codes.reshape(B, mp, PAGE, C_ // 2)
+        if C_ == 128:  # 16-byte chunk c of slot s at (c*64 + s)*16
+            cb = cb.reshape(B, mp, PAGE, 4, 16).transpose(0, 1, 3, 2, 4)
+        sb = _pad_entries(canon_scales, cache.capacity).reshape(B, mp, PAGE * (C_ // 16))
+        return cb.reshape(B * mp, -1), sb.reshape(B * mp, -1)
+    vb = codes.view(np.uint8).reshape(B, mp, PAGE, C_ * 2)
+    if C_ == 128:
+        vb = vb.reshape(B, mp, PAGE, 16, 16).transpose(0, 1, 3, 2, 4)
+    return vb.reshape(B * mp, -1), None
+
+
+def upload(cache: csa.PagedCache, ocache) -> None:
+    """Copy an oracle.Cache (canonical) into the paged device cache."""
+    if cache.cache_dtype == csa.CACHE_FP4:
+        d, s = _page_bytes(cache, ocache.codes, ocache.scales)
+    else:
+        d, s = _page_bytes(cache, ocache.bf16, None)
+    bt = cache.block_table.flatten().long()
+    cache.data[bt] = torch.from_numpy(np.ascontiguousarray(d)).to(cache.data.device)
+    if s is not None:
+        cache.scales[bt] = torch.from_numpy(np.ascontiguousarray(s)).to(cache.data.device)
+
+
+def download(cache: csa.PagedCache, n: int):
+    """Paged device cache -> canonical arrays of the first n entries per sequence:
+    (codes [B][n][C/2], scales [B][n][C/16]) for FP4, (values [B][n][C] uint16, None) for BF16."""
+    B, mp, C_ = cache.batch, cache.max_pages, cache.channels
+    bt = cache.block_table.flatten().long()
+    d = cache.data[bt].cpu().numpy()
+    if cache.cache_dtype == csa.CACHE_FP4:
+        cb = d.reshape(B, mp, -1)
+        if C_ == 128:
+            cb = cb.reshape(B, mp, 4, PAGE, 16).transpose(0, 1, 3, 2, 4)
+        codes = np.ascontiguousarray(cb).reshape(B, mp * PAGE, C_ // 2)[:, :n]
+        s = cache.scales[bt].cpu().numpy().reshape(B, mp * PAGE, C_ // 16)[:, :n]
+        return codes, s
+    vb = d.reshape(B, mp, -1)
+    if C_ == 128:
+        vb = vb.reshape(B, mp, 16, PAGE, 16).transpose(0, 1, 3, 2, 4)
+    vals = np.ascontiguousarray(vb).reshape(B, mp * PAGE, C_ * 2).view(np.uint16)[:, :n]
+    return vals, None
+
+
+def cache_pair(B, capacity, channels, dtype: str, seed: int):
+    """A paged device cache with a shuffled page table."""
+    cd = csa.CACHE_FP4 if dtype == "fp4" else csa.CACHE_BF16
+    mp = -(-capacity // PAGE)
+    order = page_order(seed, B * mp + 3)[: B * mp]
+    return csa.PagedCache(B, capacity, channels, cd, page_order=order, spare_pages=3)

@@ -1,0 +1,99 @@
+"""Comparison rules shared by the GPU parity tests (test code only).
+
+- FP4 / bf16 dequantisation: bit-exact.
+- Encoded codes from the compressor: bit-exact, except where the oracle's
+  pre-encoding value lies within the rounding-error bound of an fp32
+  evaluation of a decision boundary.  The bound is margin * M, with M the sum
+  of |terms| that formed the value (returned by the oracle): 2^-19 M for the
+  merged / rotated entry (at most ~10 fp32 roundings of terms of size M),
+  2^-14 M for indexer K (a 512-term fp32 sum).  Excused positions are counted
+  and reported; an entry whose stored main codes differ excuses its indexer K.
+- Top-k: bit-exact on integer-valued inputs (exact scores); otherwise set
+  equality up to near-ties: every id in the symmetric difference must have an
+  oracle score within 1e-5 relative of the oracle's k-th score.
+- Attention: per (token, head) row, max|o - o*| / max|o*| <= 2e-2.
+"""
+import numpy as np
+
+import oracle
+
+MAIN_MARGIN = 2.0 ** -19
+IDX_MARGIN = 2.0 ** -14
+NEAR_TIE = 1e-5
+ATT_TOL = 2e-2
+
+_E4 = np.array([oracle.e4m3_value(c) for c in range(127)])
+_SCALE_T = 3.0 * (_E4[:-1] + _E4[1:])  # 6 * midpoints, increasing
+_E2M1_MID = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def fp4_code_mismatches(gpu_codes, gpu_scales, ora_codes, ora_scales, pre, mag, margin):
+    """Returns (n_unexcused, n_excused, bad_entry_mask [..., entries])."""
+    C = pre.shape[-1]
+    G = C // 16
+    lead = pre.shape[:-1]
+    pre_g = pre.reshape(lead + (G, 16))
+    mag_g = mag.reshape(lead + (G, 16))
+    amax = np.abs(pre_g).max(-1)
+    tol_a = margin * mag_g.max(-1)
+    near_scale = (np.abs(amax[..., None] - _SCALE_T) <= tol_a[..., None]).any(-1)
+
+    def nib(codes):
+        lo, hi = codes & 15, codes >> 4
+        return np.stack([lo, hi], -1).reshape(lead + (C,))
+
+    gc, oc = nib(gpu_codes), nib(ora_codes)
+    s = np.vectorize(oracle.e4m3_value)(ora_scales.astype(int)) if ora_scales.size else ora_scales
+    s_el = np.repeat(s, 16, axis=-1)
+    near_code = (np.abs(np.abs(pre)[..., None] - s_el[..., None] * _E2M1_MID) <= (margin * mag)[..., None]).any(-1)
+    near_code |= np.repeat(near_scale, 16, axis=-1)
+    scale_bad = gpu_scales != ora_scales
+    code_bad = gc != oc
+    unexcused = int((scale_bad & ~near_scale).sum() + (code_bad & ~near_code).sum())
+    excused = int((scale_bad & near_scale).sum() + (code_bad & near_code).sum())
+    bad_entry = scale_bad.any(-1) | code_bad.any(-1)
+    return unexcused, excused, bad_entry
+
+
+def bf16_mismatches(gpu_vals, ora_vals, pre, mag, margin):
+    g = (gpu_vals.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    o = (ora_vals.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    diff = gpu_vals != ora_vals
+    mid = (g + o) / 2
+    near = np.abs(pre - mid) <= margin * mag
+    one_ulp = np.abs(gpu_vals.astype(np.int64) - ora_vals.astype(np.int64)) <= 1
+    unexcused = int((diff & ~(near & one_ulp)).sum())
+    excused = int((diff & near & one_ulp).sum())
+    return unexcused, excused, diff.any(-1)
+
+
+def topk_mismatch(gpu_ids, ora_ids, ora_scores, k, exact: bool):
+    """Number of query rows whose top-k differs beyond the rules above."""
+    bad = 0
+    for qi in range(gpu_ids.shape[0]):
+        g, o = gpu_ids[qi], ora_ids[qi]
+        if exact:
+            bad += not np.array_equal(g, o)
+            continue
+        gs, os_ = set(g[g >= 0].tolist()), set(o[o >= 0].tolist())
+        if len(gs) != len(os_) or (g >= 0).sum() != len(gs):
+            bad += 1
+            continue
+        diff = gs ^ os_
+        if not diff:
+            continue
+        s = ora_scores[qi]
+        kth = np.sort(s[np.isfinite(s)])[::-1][min(k, np.isfinite(s).sum()) - 1]
+        ok = all(abs(s[j] - kth) <= NEAR_TIE * abs(kth) for j in diff)
+        bad += not ok
+    return bad
+
+
+def attention_rel_err(out, ref):
+    """max over (token, head) rows of max|o - o*| / max|o*|."""
+    o = out.reshape(-1, out.shape[-1]).astype(np.float64)
+    r = ref.reshape(-1, ref.shape[-1])
+    num = np.abs(o - r).max(-1)
+    den = np.abs(r).max(-1)
+    den = np.where(den == 0, 1.0, den)
+    return float((num / den).max())

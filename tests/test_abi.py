@@ -1,0 +1,145 @@
+"""Host-side checks of the C ABI: the library builds and exports every symbol
+declared in include/*.h, page sizes follow the documented layout, and bad
+arguments are rejected before any launch (no GPU needed: every call below
+fails validation, so nothing is launched)."""
+import ctypes as C
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import compressed_sparse_attention_07_gb300 as csa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names += re.findall(r"CSA2_API\s+[\w\s\*]+?\b(csa2_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = csa.load()
+    names = _declared()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_page_bytes_follow_layout():
+    lib = csa.load()
+    assert lib.csa2_page_bytes(512, csa.CACHE_FP4, 0) == 64 * 256
+    assert lib.csa2_page_bytes(512, csa.CACHE_FP4, 1) == 64 * 32
+    assert lib.csa2_page_bytes(128, csa.CACHE_FP4, 0) == 64 * 64
+    assert lib.csa2_page_bytes(128, csa.CACHE_FP4, 1) == 64 * 8
+    assert lib.csa2_page_bytes(512, csa.CACHE_BF16, 0) == 64 * 1024
+    assert lib.csa2_page_bytes(512, csa.CACHE_BF16, 1) == 0
+    # 288 B per main entry and 72 B per indexer entry in FP4
+    assert (lib.csa2_page_bytes(512, 0, 0) + lib.csa2_page_bytes(512, 0, 1)) // 64 == 288
+    assert (lib.csa2_page_bytes(128, 0, 0) + lib.csa2_page_bytes(128, 0, 1)) // 64 == 72
+
+
+def test_status_strings():
+    for code in (0, 1, 2, 3, 4, 16, 17, 18):
+        assert csa.status_string(code) != "unknown status"
+    assert csa.status_string(999) == "unknown status"
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _fake_cache(channels, dtype=csa.CACHE_FP4):
+    return csa._CacheDesc(FAKE, FAKE if dtype == csa.CACHE_FP4 else None, FAKE, 4, 8, channels, 0)
+
+
+def test_validation_rejects_before_launch():
+    lib = csa.load()
+    cfg = csa.Cfg(ratio=2)
+    m, i = _fake_cache(512), _fake_cache(128)
+    # no configuration
+    assert lib.csa2_compress(None, 1, 2, FAKE, FAKE, FAKE, FAKE, C.byref(m), C.byref(i), FAKE, None, None) == 1
+    # unsupported model size
+    bad = csa.Cfg(ratio=2)
+    bad.dim = 256
+    assert lib.csa2_compress(C.byref(bad), 1, 2, FAKE, FAKE, FAKE, FAKE, C.byref(m), C.byref(i), FAKE, None,
+                             None) == 2
+    bad = csa.Cfg(ratio=3)
+    assert lib.csa2_attend(C.byref(bad), 1, 1, FAKE, C.byref(m), FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 1.0, FAKE,
+                           None, None, None) == 2
+    # T not a multiple of r
+    assert lib.csa2_compress(C.byref(cfg), 1, 3, FAKE, FAKE, FAKE, FAKE, C.byref(m), C.byref(i), FAKE, None,
+                             None) == 1
+    # wrong channel count for the indexer cache
+    assert lib.csa2_compress(C.byref(cfg), 1, 2, FAKE, FAKE, FAKE, FAKE, C.byref(m), C.byref(m), FAKE, None,
+                             None) == 1
+    # workspace too small for one query
+    need = lib.csa2_index_workspace_bytes(C.byref(cfg), 1, 1, 256, 0)
+    assert need >= 256 * 4
+    assert lib.csa2_index_topk(C.byref(cfg), 1, 1, FAKE, None, FAKE, C.byref(i), FAKE, 256, None, FAKE, None, FAKE,
+                               need - 1, None, None) == 4
+    # more entries than the cache can hold
+    assert lib.csa2_index_topk(C.byref(cfg), 1, 1, FAKE, None, FAKE, C.byref(i), FAKE, 4 * 64 + 1, None, FAKE, None,
+                               FAKE, 1 << 30, None, None) == 4
+    # pool and pool_out together, or HSI outputs without HSI blocks
+    hcfg = csa.Cfg(ratio=1, hsi_blocks=16)
+    assert lib.csa2_index_topk(C.byref(hcfg), 1, 1, FAKE, None, FAKE, C.byref(i), FAKE, 256, FAKE, FAKE, FAKE, FAKE,
+                               1 << 30, None, None) == 1
+    assert lib.csa2_index_topk(C.byref(cfg), 1, 1, FAKE, None, FAKE, C.byref(i), FAKE, 256, None, FAKE, FAKE, FAKE,
+                               1 << 30, None, None) == 1
+    # unaligned workspace
+    assert lib.csa2_index_topk(C.byref(cfg), 1, 1, FAKE, None, FAKE, C.byref(i), FAKE, 256, None, FAKE, None,
+                               FAKE + 4, 1 << 30, None, None) == 1
+    # window rows required when window > 0
+    assert lib.csa2_attend(C.byref(cfg), 1, 1, FAKE, C.byref(m), FAKE, FAKE, None, 0, None, None, FAKE, 1.0, FAKE,
+                           None, None, None) == 1
+    # NaN scale
+    assert lib.csa2_attend(C.byref(cfg), 1, 1, FAKE, C.byref(m), FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE,
+                           float("nan"), FAKE, None, None, None) == 1
+    # Reindex without a pool
+    st = csa._GroupState(m, i, FAKE, 256, 0, FAKE, None, FAKE, 1 << 30, None)
+    io = csa._LayerIO()
+    assert lib.csa2_layer(C.byref(hcfg), csa.MODE_REINDEX, C.byref(st), C.byref(io), None) == 1
+    assert lib.csa2_layer(C.byref(hcfg), 7, C.byref(st), C.byref(io), None) == 1
+    # empty batches are a no-op
+    assert lib.csa2_compress(C.byref(cfg), 0, 2, None, None, None, None, None, None, None, None, None) == 0
+
+
+def test_paged_round_trip_on_host():
+    """upload / download through the documented layout (CPU tensors)."""
+    import oracle
+    import synth
+    from tests import _paged
+
+    for dtype, chans in (("fp4", 512), ("fp4", 128), ("bf16", 512), ("bf16", 128)):
+        cd = csa.CACHE_FP4 if dtype == "fp4" else csa.CACHE_BF16
+        order = _paged.page_order(1, 3 * 3 + 2)[:9]
+        pc = csa.PagedCache(3, 150, chans, cd, device="cpu", page_order=order, spare_pages=2)
+        oc = oracle.Cache(3, 150, chans, dtype)
+        g = synth.rng(1, "rt")
+        if dtype == "fp4":
+            oc.codes[:], oc.scales[:] = g.integers(0, 256, oc.codes.shape), g.integers(0, 256, oc.scales.shape)
+        else:
+            oc.bf16[:] = g.integers(0, 65536, oc.bf16.shape)
+        _paged.upload(pc, oc)
+        a, b = _paged.download(pc, 150)
+        if dtype == "fp4":
+            np.testing.assert_array_equal(a, oc.codes)
+            np.testing.assert_array_equal(b, oc.scales)
+            # spot-check the documented address of one entry
+            bj, j = 2, 131
+            page = int(pc.block_table[bj, j // 64])
+            slot = j % 64
+            if chans == 512:
+                got = pc.data[page, slot * 256:(slot + 1) * 256].numpy()
+            else:
+                got = np.concatenate([pc.data[page, (c * 64 + slot) * 16:(c * 64 + slot + 1) * 16].numpy()
+                                      for c in range(4)])
+            np.testing.assert_array_equal(got, oc.codes[bj, j])
+        else:
+            np.testing.assert_array_equal(a, oc.bf16)

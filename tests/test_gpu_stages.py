@@ -1,0 +1,295 @@
+"""GPU-vs-oracle parity of each stage of the CSA2 path through the C ABI, at
+sizes the oracle finishes in seconds that still span several tiles, pages
+and ragged tails."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import compressed_sparse_attention_07_gb300 as csa
+import oracle
+import synth
+from tests import _paged
+from tests import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+D, CI, H, HM = 512, 128, 32, 64
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ------------------------------------------------------------- dequant ----
+
+@pytest.mark.parametrize("channels", [512, 128])
+def test_dequant_bit_exact_every_code_and_scale(channels):
+    """Every E2M1 code under every finite E4M3 scale decodes exactly."""
+    B, n = 2, 254
+    oc = oracle.Cache(B, n, channels, "fp4")
+    codes = np.arange(channels // 2 * n * B, dtype=np.int64) % 256
+    oc.codes[:] = codes.reshape(oc.codes.shape).astype(np.uint8)
+    sc = np.arange(channels // 16 * n * B) % 254
+    sc = np.where(sc >= 127, sc + 1, sc)  # skip 0x7F (NaN), keep 0x80..0xFE
+    oc.scales[:] = sc.reshape(oc.scales.shape).astype(np.uint8)
+    pc = _paged.cache_pair(B, n, channels, "fp4", seed=3)
+    _paged.upload(pc, oc)
+    ids = torch.from_numpy(np.stack([np.arange(n), np.arange(n)[::-1]]).astype(np.int32)).cuda()
+    out = torch.empty((B, n, channels), dtype=torch.float32, device="cuda")
+    st = _status()
+    csa.gather_dequant(pc, ids, out, status=st)
+    want = oc.values()
+    want[1] = want[1][::-1]
+    got = out.cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+    assert int(st.item()) == 0
+
+
+def test_dequant_bf16_and_bad_page_status():
+    oc = oracle.Cache(1, 100, 512, "bf16")
+    oc.bf16[:] = synth.normal_bf16(synth.rng(5, "c"), oc.bf16.shape)
+    pc = _paged.cache_pair(1, 100, 512, "bf16", seed=5)
+    _paged.upload(pc, oc)
+    ids = torch.arange(100, dtype=torch.int32, device="cuda").reshape(1, 100)
+    out = torch.empty((1, 100, 512), dtype=torch.float32, device="cuda")
+    csa.gather_dequant(pc, ids, out)
+    np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), oc.values()[0:1])
+    # a block-table entry outside the pool is reported and the row reads as zeros
+    pc.block_table[0, 1] = pc.num_pages + 5
+    st = _status()
+    csa.gather_dequant(pc, ids, out, status=st)
+    assert int(st.item()) == 16  # CSA2_ERR_BAD_PAGE
+    assert (out[0, 64:100] == 0).all()
+
+
+# ------------------------------------------------------------ compress ----
+
+def _compress_case(B, T, r, dtype, pos0, seed, theta=1e4, capacity=None):
+    x = synth.normal_bf16(synth.rng(seed, "x"), (B, T, D))
+    w = synth.merge_weights(synth.rng(seed, "w"), r, D)
+    w_idx = synth.normal_bf16(synth.rng(seed, "w_idx"), (D, CI), std=1 / math.sqrt(D))
+    pos0 = np.asarray(pos0, np.int64)
+    M = T // r
+    cap = capacity or int(pos0.max() // r + M)
+    om, oi = oracle.Cache(B, cap, D, dtype), oracle.Cache(B, cap, CI, dtype)
+    diag = oracle.compress(x, pos0, w, w_idx, om, oi, r, theta, diagnostics=True)
+    cfg = csa.Cfg(ratio=r, cache_dtype=csa.CACHE_FP4 if dtype == "fp4" else csa.CACHE_BF16, rope_theta=theta)
+    pm, pi = _paged.cache_pair(B, cap, D, dtype, seed), _paged.cache_pair(B, cap, CI, dtype, seed + 1)
+    n_ent = torch.zeros(B, dtype=torch.int32, device="cuda")
+    st = _status()
+    csa.compress(cfg, _paged.dev(x), _paged.dev(pos0), _paged.dev(w), _paged.dev(w_idx), pm, pi, n_ent, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert n_ent.cpu().tolist() == [int(p // r + M) for p in pos0]
+    return om, oi, pm, pi, diag, cap
+
+
+def _check_compress(om, oi, pm, pi, diag, pos0, r, M, dtype):
+    B = len(pos0)
+    gm, gms = _paged.download(pm, pm.capacity)
+    gi, gis = _paged.download(pi, pi.capacity)
+    rows = [np.arange(p // r, p // r + M) for p in pos0]
+    tot_exc = 0
+    for b in range(B):
+        j = rows[b]
+        if dtype == "fp4":
+            u, e, bad = P.fp4_code_mismatches(gm[b, j], gms[b, j], om.codes[b, j], om.scales[b, j],
+                                              diag["pre_main"][b], diag["mag_main"][b], P.MAIN_MARGIN)
+            assert u == 0, "main codes differ away from decision boundaries"
+            ok = ~bad
+            u2, e2, _ = P.fp4_code_mismatches(gi[b, j][ok], gis[b, j][ok], oi.codes[b, j][ok], oi.scales[b, j][ok],
+                                              diag["pre_idx"][b][ok], diag["mag_idx"][b][ok], P.IDX_MARGIN)
+        else:
+            u, e, bad = P.bf16_mismatches(gm[b, j], om.bf16[b, j], diag["pre_main"][b], diag["mag_main"][b],
+                                          P.MAIN_MARGIN)
+            assert u == 0
+            ok = ~bad
+            u2, e2, _ = P.bf16_mismatches(gi[b, j][ok], oi.bf16[b, j][ok], diag["pre_idx"][b][ok],
+                                          diag["mag_idx"][b][ok], P.IDX_MARGIN)
+        assert u2 == 0, "indexer K codes differ away from decision boundaries"
+        tot_exc += e + e2
+    return tot_exc
+
+
+@pytest.mark.parametrize("dtype,r,T,pos0,theta", [
+    ("fp4", 2, 2, [0, 130, 4094], 1e4),            # decode: one pair per sequence
+    ("fp4", 2, 256, [0, 1048576], 1e4),            # prefill chunk, far positions
+    ("fp4", 1, 1, [5, 262143, 64], 1.6e5),         # decoder decode step
+    ("fp4", 1, 200, [0, 777], 1.6e5),              # ragged page tails
+    ("bf16", 2, 64, [0, 2048], 1e4),
+    ("bf16", 1, 3, [10, 100], 1.6e5),
+])
+def test_compress_matches_oracle(dtype, r, T, pos0, theta):
+    B = len(pos0)
+    om, oi, pm, pi, diag, cap = _compress_case(B, T, r, dtype, pos0, seed=11 + T, theta=theta)
+    exc = _check_compress(om, oi, pm, pi, diag, pos0, r, T // r, dtype)
+    print("compress %s r=%d T=%d: %d near-boundary codes excused" % (dtype, r, T, exc))
+
+
+# --------------------------------------------------------------- index ----
+
+def _idx_caches(B, N, dtype, seed, integer=False, dup=False):
+    oc = oracle.Cache(B, N, CI, dtype)
+    g = synth.rng(seed, "idx")
+    for b in range(B):
+        if dtype == "fp4":
+            oc.codes[b], oc.scales[b] = synth.integer_fp4_bytes(g, N, CI) if integer else synth.fp4_bytes(g, N, CI)
+        else:
+            oc.bf16[b] = synth.integer_bf16(g, (N, CI)) if integer else synth.normal_bf16(g, (N, CI))
+    if dup:  # repeat a few entries so that ties straddle the k-th place
+        pick = synth.rng(seed, "dup").integers(0, 40, size=(B, N))
+        for b in range(B):
+            if dtype == "fp4":
+                oc.codes[b], oc.scales[b] = oc.codes[b][pick[b]], oc.scales[b][pick[b]]
+            else:
+                oc.bf16[b] = oc.bf16[b][pick[b]]
+    pc = _paged.cache_pair(B, N, CI, dtype, seed)
+    _paged.upload(pc, oc)
+    return oc, pc
+
+
+def _run_index(cfg, pc, q_idx, q_pos, n_ent, N, head_w=None, pool=None, want_pool=False, ws_queries=None):
+    B, Tq = q_idx.shape[:2]
+    k = cfg.topk
+    topk = torch.full((B, Tq, k), -7, dtype=torch.int32, device="cuda")
+    pool_out = torch.full((B, Tq, cfg.hsi_blocks), -7, dtype=torch.int32, device="cuda") if want_pool else None
+    per_q = csa.index_workspace_bytes(cfg, 1, 1, N, reindex=pool is not None)
+    nq = B * Tq if ws_queries is None else ws_queries
+    ws = torch.empty(per_q * nq, dtype=torch.uint8, device="cuda")
+    st = _status()
+    csa.index_topk(cfg, _paged.dev(q_idx), _paged.dev(q_pos), pc, _paged.dev(n_ent), N, topk, ws,
+                   head_w=None if head_w is None else _paged.dev(head_w),
+                   pool=None if pool is None else _paged.dev(pool), pool_out=pool_out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return topk.cpu().numpy(), (pool_out.cpu().numpy() if want_pool else None)
+
+
+@pytest.mark.parametrize("dtype", ["fp4", "bf16"])
+def test_index_topk_integer_mode_bit_exact(dtype):
+    """Integer q and integer-valued K make every score exact: the top-k
+    (lowest id on ties) and the HSI pool must match bit for bit, including
+    chunked workspaces, ragged n_entries and short contexts."""
+    B, N, k, nb = 3, 3000, 512, 64
+    oc, pc = _idx_caches(B, N, dtype, seed=21, integer=True, dup=True)
+    q_idx = synth.integer_bf16(synth.rng(21, "q"), (B, 2, H, CI), -1, 1)
+    q_pos = np.array([[2999, 1500], [2999, 2999], [300, 2999]], np.int64)
+    n_ent = np.array([3000, 2457, 200], np.int32)
+    cfg = csa.Cfg(ratio=1, cache_dtype=csa.CACHE_FP4 if dtype == "fp4" else csa.CACHE_BF16, topk=k, hsi_blocks=nb)
+    g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True, ws_queries=2)
+    o_top, o_pool, s = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, want_pool=True,
+                                         want_scores=True)
+    np.testing.assert_array_equal(g_top, o_top)
+    np.testing.assert_array_equal(g_pool, o_pool)
+    ties = 0
+    for b in range(B):
+        for t in range(2):
+            v = np.sort(s[b, t][np.isfinite(s[b, t])])[::-1]
+            ties += len(v) > k and v[k - 1] == v[k]
+    assert ties > 0
+
+
+def test_index_topk_random_fp4_with_head_weights_and_ratio2():
+    B, N, k = 2, 2500, 512
+    oc, pc = _idx_caches(B, N, "fp4", seed=22)
+    q_idx = synth.normal_bf16(synth.rng(22, "q"), (B, 3, H, CI))
+    hw = synth.rng(22, "hw").uniform(0.0, 2.0, size=(B, 3, H)).astype(np.float32)
+    q_pos = np.array([[4999, 2000, 1], [4999, 1100, 700]], np.int64)
+    n_ent = np.array([2500, 2500], np.int32)
+    cfg = csa.Cfg(ratio=2, topk=k)
+    g_top, _ = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, head_w=hw)
+    o_top, _, s = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=2, k=k, head_w=hw, want_scores=True)
+    assert P.topk_mismatch(g_top.reshape(-1, k), o_top.reshape(-1, k), s.reshape(B * 3, -1), k, exact=False) == 0
+    assert (g_top[0, 2] >= 0).sum() == 1 and g_top[0, 2, 0] == 0  # t = 1 sees entry 0 only
+
+
+def test_reindex_over_pool_matches_oracle():
+    B, N, k, nb = 2, 4000, 64, 40
+    oc, pc = _idx_caches(B, N, "fp4", seed=23, integer=True, dup=True)
+    q_idx = synth.integer_bf16(synth.rng(23, "q"), (B, 1, H, CI), -1, 1)
+    q_pos = np.array([[3999], [3500]], np.int64)
+    n_ent = np.array([4000, 4000], np.int32)
+    g = synth.rng(23, "pool")
+    pool = np.full((B, 1, nb), -1, np.int32)
+    for b in range(B):
+        blocks = np.sort(g.choice(500, size=nb - 3, replace=False))
+        pool[b, 0, :nb - 3] = blocks
+    cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=nb)
+    g_top, _ = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, pool=pool)
+    o_top, _, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, pool=pool)
+    np.testing.assert_array_equal(g_top, o_top)
+
+
+# -------------------------------------------------------------- attend ----
+
+def _main_caches(B, N, dtype, seed):
+    oc = oracle.Cache(B, N, D, dtype)
+    g = synth.rng(seed, "main")
+    for b in range(B):
+        if dtype == "fp4":
+            oc.codes[b], oc.scales[b] = synth.fp4_bytes(g, N, D)
+        else:
+            oc.bf16[b] = synth.normal_bf16(g, (N, D))
+    pc = _paged.cache_pair(B, N, D, dtype, seed)
+    _paged.upload(pc, oc)
+    return oc, pc
+
+
+@pytest.mark.parametrize("dtype", ["fp4", "bf16"])
+def test_attend_matches_oracle(dtype):
+    """Decode and banded-window prefill queries, -1 padded top-k, a window
+    clipped at the sequence start and a short window buffer."""
+    B, N, Tq, k, W = 3, 700, 3, 512, 128
+    oc, pc = _main_caches(B, N, dtype, seed=31)
+    g = synth.rng(31, "ids")
+    topk = np.full((B, Tq, k), -1, np.int32)
+    for b in range(B):
+        for t in range(Tq):
+            n = [512, 300, 0][(b + t) % 3]
+            topk[b, t, :n] = np.sort(g.choice(N, size=n, replace=False))
+    q = synth.normal_bf16(synth.rng(31, "q"), (B, Tq, HM, D))
+    S = 200
+    swa = synth.normal_bf16(synth.rng(31, "swa"), (B, S, D))
+    swa_pos0 = np.array([0, 1000, 5000], np.int64)
+    swa_len = np.array([150, 200, 60], np.int32)
+    q_pos = np.array([[3, 100, 149], [1199, 1130, 1050], [5059, 5100, 4990]], np.int64)
+    n_ent = np.array([N, N, N], np.int32)
+    scale = 1 / math.sqrt(D)
+    cfg = csa.Cfg(ratio=2, cache_dtype=csa.CACHE_FP4 if dtype == "fp4" else csa.CACHE_BF16, topk=k, window=W)
+    out = torch.empty((B, Tq, HM, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, Tq, HM), dtype=torch.float32, device="cuda")
+    st = _status()
+    csa.attend(cfg, _paged.dev(q), pc, _paged.dev(n_ent), _paged.dev(topk), _paged.dev(swa), _paged.dev(swa_len),
+               _paged.dev(swa_pos0), _paged.dev(q_pos), out, lse=lse, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_out, o_lse = oracle.attend(oc, n_ent, q, topk, swa, swa_len, swa_pos0, q_pos, W, scale, want_lse=True)
+    err = P.attention_rel_err(out.cpu().numpy(), o_out)
+    assert err <= P.ATT_TOL, err
+    lg = lse.cpu().numpy()
+    fin = np.isfinite(o_lse)
+    assert np.array_equal(np.isfinite(lg), fin)
+    np.testing.assert_allclose(lg[fin], o_lse[fin], rtol=0, atol=1e-3)
+    print("attend %s: max row rel err %.3g" % (dtype, err))
+
+
+def test_attend_reports_out_of_range_ids():
+    B, N = 1, 100
+    oc, pc = _main_caches(B, N, "fp4", seed=32)
+    topk = np.array([[[3, 50, 99, 100, -1]]], np.int32)  # 100 is past the last entry
+    q = synth.normal_bf16(synth.rng(32, "q"), (1, 1, HM, D))
+    swa = synth.normal_bf16(synth.rng(32, "swa"), (1, 4, D))
+    cfg = csa.Cfg(ratio=1, topk=5, window=4)
+    out = torch.empty((1, 1, HM, D), dtype=torch.float32, device="cuda")
+    st = _status()
+    csa.attend(cfg, _paged.dev(q), pc, _paged.dev(np.array([N], np.int32)), _paged.dev(topk), _paged.dev(swa),
+               _paged.dev(np.array([4], np.int32)), _paged.dev(np.array([96], np.int64)),
+               _paged.dev(np.array([[99]], np.int64)), out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 17  # CSA2_ERR_BAD_INDEX
+    want = oracle.attend(oc, np.array([N]), q, np.array([[[3, 50, 99, -1, -1]]], np.int32), swa,
+                         np.array([4], np.int32), np.array([96]), np.array([[99]]), 4, 1 / math.sqrt(D))
+    assert P.attention_rel_err(out.cpu().numpy(), want) <= P.ATT_TOL

@@ -1,0 +1,417 @@
+"""CSA2 benchmark: query-tokens/s of one CSA2 step on synthetic inputs.
+
+A step is one pass of the whole path over one batch: the compressor on the
+step's new tokens, the indexer with top-k (and the HSI pool / Reindex on
+decoder workloads), and sparse attention over top-k plus the window.  The
+default workload is the batch-8 decode step at 32768 tokens of context with
+2:1 compression into an FP4 cache (16384 entries per sequence).
+
+Timing: W warm-up steps, then K timed steps; before each step a 256 MiB
+buffer is written so that the step starts with a cold L2 (the inputs are
+smaller than L2), and each step is bracketed by CUDA events on the launching
+stream (per-stage events give the per-kernel durations used for the
+roofline).  Under torchrun every rank runs its own batch (weak scaling, no
+data-path collective); rank 0 prints one JSON line with the max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "CSA2 sparse-attention query-tokens/s at 1 GB300; achieved HBM GB/s vs peak"
+UNIT = "query-tokens/s"
+DEFAULT_WORKLOAD = "decode_b8_ctx32768_r2_fp4"
+FLUSH_BYTES = 256 << 20
+# algorithmic bytes per unit (hot-path scope table): indexer 72 B per visible
+# FP4 entry per query (256 B per bf16 entry); attention 512 x 288 + 128 x 1024
+# + Q 65536 + fp32 out 131072 + ids 2048 B per query token; compressor
+# r x 1024 B in + 360 B out per entry.
+IDX_ENTRY_BYTES = {"fp4": 72, "bf16": 256}
+MAIN_ENTRY_BYTES = {"fp4": 288, "bf16": 1024}
+
+
+def attend_query_bytes(cache, topk=512, window=128):
+    return topk * MAIN_ENTRY_BYTES[cache] + window * 1024 + 64 * 512 * 2 + 64 * 512 * 4 + topk * 4
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks ----
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            self.path = os.path.join("/tmp", "csa2_clocks_%d_%d.csv" % (os.getpid(), self.index))
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- workload ----
+
+class DecodeStep:
+    """One decode step of one CSA2 layer in Full mode: compress the step's
+    r new tokens per sequence (one entry), index the whole visible cache
+    (plus the HSI pool on the decoder Full layer), attend over top-k and the
+    window.  The cache prefix holds seeded random FP4 bytes (or N(0,1) bf16)."""
+
+    def __init__(self, wl: synth.Workload, device, seed_offset=0):
+        import torch
+        import compressed_sparse_attention_07_gb300 as csa
+        self.torch, self.csa, self.wl = torch, csa, wl
+        B, r = wl.batch, wl.ratio
+        self.B = B
+        self.N = wl.ctx // r
+        cd = csa.CACHE_FP4 if wl.cache == "fp4" else csa.CACHE_BF16
+        self.cfg = csa.Cfg(ratio=r, cache_dtype=cd, topk=wl.topk, window=wl.window,
+                           hsi_blocks=wl.hsi_blocks if wl.hsi else 0, rope_theta=wl.theta)
+        seed = wl.seed + seed_offset
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.main = csa.PagedCache(B, self.N, 512, cd, device=device)
+        self.idx = csa.PagedCache(B, self.N, 128, cd, device=device)
+        for c in (self.main, self.idx):
+            if cd == csa.CACHE_FP4:
+                c.data.random_(0, 256, generator=g)
+                c.scales.random_(0x20, 0x3D, generator=g)
+            else:
+                v = torch.randn(c.data.numel() // 2, generator=g, device=device, dtype=torch.float32)
+                c.data.view(torch.int16).copy_(v.to(torch.bfloat16).view(torch.int16).view(c.data.shape[0], -1))
+        ctx = wl.ctx
+        s = seed
+        self.h = {
+            "x": synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512)),
+            "pos0": np.full(B, ctx - r, np.int64),
+            "q": synth.normal_bf16(synth.rng(s, "q"), (B, 1, 64, 512)),
+            "q_idx": synth.normal_bf16(synth.rng(s, "q_idx"), (B, 1, 32, 128)),
+            "swa": synth.normal_bf16(synth.rng(s, "swa"), (B, wl.window, 512)),
+            "swa_len": np.full(B, wl.window, np.int32),
+            "swa_pos0": np.full(B, ctx - wl.window, np.int64),
+            "q_pos": np.full((B, 1), ctx - 1, np.int64),
+        }
+        self.merge_w = torch.from_numpy(synth.merge_weights(synth.rng(s, "w"), r, 512)).to(device)
+        self.w_idx = torch.from_numpy(synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512)).view(
+            np.int16)).to(device)
+        self.d = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)).to(device)
+                  for k, v in self.h.items()}
+        self.n_entries = torch.full((B,), self.N - 1, dtype=torch.int32, device=device)
+        self.topk = torch.empty((B, 1, wl.topk), dtype=torch.int32, device=device)
+        self.pool = torch.empty((B, 1, wl.hsi_blocks), dtype=torch.int32, device=device) if wl.hsi else None
+        self.ws = torch.empty(csa.index_workspace_bytes(self.cfg, B, 1, self.N), dtype=torch.uint8, device=device)
+        self.out = torch.empty((B, 1, 64, 512), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.stages = ["compress", "index_topk", "attend"]
+        self.launches_per_step = 4  # compress, score, select, attend
+        eb = IDX_ENTRY_BYTES[wl.cache]
+        self.stage_bytes = {"compress": B * (r * 1024 + (288 + 72 if wl.cache == "fp4" else 1280)),
+                            "index_topk": B * self.N * eb,
+                            "attend": B * attend_query_bytes(wl.cache, wl.topk, wl.window)}
+        self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_full_kernel + select_kernel",
+                              "attend": "attend_kernel"}
+        self.units = B
+
+    def inputs_host(self):
+        return {k: v for k, v in self.h.items()}
+
+    def step(self, events=None, d=None):
+        csa, d = self.csa, (d or self.d)
+        ev = events or [None] * 4
+        if ev[0] is not None:
+            ev[0].record()
+        csa.compress(self.cfg, d["x"], d["pos0"], self.merge_w, self.w_idx, self.main, self.idx, self.n_entries,
+                     status=self.status)
+        if ev[1] is not None:
+            ev[1].record()
+        csa.index_topk(self.cfg, d["q_idx"], d["q_pos"], self.idx, self.n_entries, self.N, self.topk, self.ws,
+                       pool_out=self.pool, status=self.status)
+        if ev[2] is not None:
+            ev[2].record()
+        csa.attend(self.cfg, d["q"], self.main, self.n_entries, self.topk, d["swa"], d["swa_len"], d["swa_pos0"],
+                   d["q_pos"], self.out, status=self.status)
+        if ev[3] is not None:
+            ev[3].record()
+        return self.out
+
+
+def make_step(name, device, seed_offset=0):
+    wl = synth.WORKLOADS[name]
+    if wl.tq == 1 and not wl.layers:
+        return DecodeStep(wl, device, seed_offset)
+    raise SystemExit("workload %s is not wired into the benchmark yet" % name)
+
+
+# ------------------------------------------------------------- cpu oracle ----
+
+class OracleStep:
+    """The CPU oracle running the same step (compress the new pair, index,
+    attend) for all B sequences on its own seeded random cache."""
+
+    def __init__(self, wl: synth.Workload):
+        import oracle
+        self.oracle, self.wl = oracle, wl
+        B, r, N = wl.batch, wl.ratio, wl.ctx // wl.ratio
+        self.N = N
+        self.main = oracle.Cache(B, N, 512, wl.cache)
+        self.idx = oracle.Cache(B, N, 128, wl.cache)
+        g = synth.rng(wl.seed, "oracle_cache")
+        for c in (self.main, self.idx):
+            if wl.cache == "fp4":
+                for b in range(B):
+                    c.codes[b], c.scales[b] = synth.fp4_bytes(g, N, c.channels)
+            else:
+                c.bf16[:] = synth.normal_bf16(g, c.bf16.shape)
+        s = wl.seed
+        ctx = wl.ctx
+        self.x = synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512))
+        self.pos0 = np.full(B, ctx - r, np.int64)
+        self.w = synth.merge_weights(synth.rng(s, "w"), r, 512)
+        self.w_idx = synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512))
+        self.q = synth.normal_bf16(synth.rng(s, "q"), (B, 1, 64, 512))
+        self.q_idx = synth.normal_bf16(synth.rng(s, "q_idx"), (B, 1, 32, 128))
+        self.swa = synth.normal_bf16(synth.rng(s, "swa"), (B, wl.window, 512))
+        self.q_pos = np.full((B, 1), ctx - 1, np.int64)
+        self.n_ent = np.full(B, N, np.int32)
+        self.units = B
+        self.cores = min(oracle.threads(), B)
+
+    def step(self):
+        o, wl = self.oracle, self.wl
+        o.compress(self.x, self.pos0, self.w, self.w_idx, self.main, self.idx, wl.ratio, wl.theta)
+        topk, pool, _ = o.index_topk(self.idx, self.n_ent, self.q_idx, self.q_pos, wl.ratio, wl.topk,
+                                     hsi_blocks=wl.hsi_blocks if wl.hsi else 0, want_pool=wl.hsi)
+        return o.attend(self.main, self.n_ent, self.q, topk, self.swa, np.full(wl.batch, wl.window, np.int32),
+                        np.full(wl.batch, wl.ctx - wl.window, np.int64), self.q_pos, wl.window, 1 / math.sqrt(512))
+
+
+def cpu_baseline(wl, seconds: float):
+    st = OracleStep(wl)
+    st.step()  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        st.step()
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n * st.units / dt, "unit": UNIT, "cores": st.cores, "kind": "oracle",
+            "sample": "%d full steps of %s (%d query tokens each: compress + index over %d entries + attend), "
+                      "fp64 C oracle, OpenMP over query tokens" % (n, wl.name, st.units, st.N)}
+
+
+# -------------------------------------------------------------------- main ----
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, ws, rank):
+    """The oracle as it stands, on the host cores, on this arm's workload."""
+    wl = synth.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    st = OracleStep(wl)
+    for _ in range(args.warmup):
+        st.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.step()
+    dt = time.perf_counter() - t0
+    v = args.steps * st.units / dt
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name}, "impl": "reference",
+            "cpu_baseline": {"value": v, "unit": UNIT, "kind": "oracle", "cores": st.cores,
+                             "sample": "%d full steps of %s on the host cores" % (args.steps, wl.name)},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        barrier(ws)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    step = make_step(args.workload, dev, seed_offset=rank)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    nst = len(step.stages)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step.step()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0, "device status %d" % int(step.status.item())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        step.step(events=evs[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(ws)
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[nst]) for e in evs]
+    stage_ms = {s: statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, s in enumerate(step.stages)}
+    total_ms = max_over_ranks(sum(step_ms), ws)
+    ms_per_step = total_ms / args.steps
+    value = ws * step.units * args.steps / (total_ms / 1e3)
+
+    # end to end through the Python API with host buffers: H2D of the step's
+    # inputs from pinned memory, the step, D2H of the attention output
+    hin = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory()
+           for k, v in step.inputs_host().items()}
+    hout = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in hin.items()}
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = hout.numel() * hout.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    for k in range(e2e_steps):
+        flush.fill_(k & 0xFF)
+        e2e_ev[k][0].record()
+        for name, t in hin.items():
+            dbuf[name].copy_(t, non_blocking=True)
+        out = step.step(d=dbuf)
+        hout.copy_(out, non_blocking=True)
+        e2e_ev[k][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), ws) / e2e_steps
+    assert int(step.status.item()) == 0
+
+    hbm, tflops, src = peaks()
+    dom = max(stage_ms, key=stage_ms.get)
+    ach = step.stage_bytes[dom] / (stage_ms[dom] / 1e3) / 1e9
+    roof = {"bound": "hbm", "kernel": step.stage_kernels[dom], "achieved": ach, "peak": hbm, "unit": "GB/s",
+            "frac": ach / hbm, "traffic": None,
+            "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "of fallback",
+            "algorithmic_bytes_per_launch": step.stage_bytes[dom], "launch_ms": stage_ms[dom]}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(step.wl, args.cpu_seconds)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": step.wl.name, "batch_per_gpu": step.B, "ctx": step.wl.ctx,
+                           "entries": step.N, "cache": step.wl.cache, "topk": step.wl.topk,
+                           "window": step.wl.window, "hsi": step.wl.hsi,
+                           "l2": "flushed before every step (256 MiB write)"},
+                "stage_ms": stage_ms, "wall_s": wall,
+                "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": ws * step.units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "gpu_launches": step.launches_per_step * args.steps, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    barrier(ws)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

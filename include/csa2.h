@@ -166,6 +166,30 @@ CSA2_API int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const u
                     const int64_t* q_pos, float scale, float* out, float* lse, int32_t* status,
                     void* stream);
 
+/* csa2_index_topk without a caller-provided workspace, for callers that
+ * cannot allocate device memory (a serving engine or plugin host that owns
+ * all device memory in its own pool and offers no allocator, or a decode loop
+ * that must not pay for cudaMalloc's device synchronisation).  The write-ups
+ * have no counterpart to this call: it only changes where the scratch lives.
+ * Same arguments, rules and results as csa2_index_topk; the scores and HSI
+ * block maxima go to one static device array of
+ * csa2_index_static_scratch_bytes() bytes (8 MiB) built into the library,
+ * present on every GPU that loads it until the process exits.  One query's
+ * scratch (about 4 B per entry, 4.5 B with HSI) must fit, else
+ * CSA2_ERR_CAPACITY before any launch; larger batches run in chunks.
+ * Allocates nothing.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress), so make that first call before any stream
+ * capture.  Calls share the array and keep the previous call's contents
+ * (nothing needs clearing); calls that overlap on the GPU race, so order them
+ * on one stream. */
+CSA2_API int32_t csa2_index_topk_static(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q_idx,
+                                        const float* head_w, const int64_t* q_pos, const csa2_cache* idx_cache,
+                                        const int32_t* n_entries, int32_t max_entries, const int32_t* pool,
+                                        int32_t* topk_out, int32_t* pool_out, int32_t* status, void* stream);
+
+/* Size in bytes of the static scratch array behind csa2_index_topk_static. */
+CSA2_API size_t csa2_index_static_scratch_bytes(void);
+
 /* Decode entries of a cache to fp32: out[b][i][c] = value of entry
  * ids[b][i] of sequence b (ids < 0 give zeros).  ids [B][n]; out
  * [B][n][channels].  Exact for both cache formats. */

@@ -162,8 +162,8 @@ class DecodeStep:
         self.stage_bytes = {"compress": B * (r * 1024 + (288 + 72 if wl.cache == "fp4" else 1280)),
                             "index_topk": B * self.N * eb,
                             "attend": B * attend_query_bytes(wl.cache, wl.topk, wl.window)}
-        self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_full_kernel + select_kernel",
-                              "attend": "attend_kernel"}
+        self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_tc_kernel + select_kernel",
+                              "attend": "attend_tc_kernel"}
         self.units = B
 
     def inputs_host(self):

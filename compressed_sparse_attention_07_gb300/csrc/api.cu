@@ -16,8 +16,8 @@ bool cfg_supported(const csa2_cfg* c, int32_t* err) {
     return false;
   }
   if (c->dim != kDim || c->rope_dims != kRope || c->n_heads != kHeads || c->idx_heads != kIdxHeads ||
-      c->idx_dim != kIdxDim || c->hsi_block != kHsiBlock || c->topk < 1 || c->topk > 2048 || c->window < 0 ||
-      c->window > 1024 || (c->ratio != 1 && c->ratio != 2) || c->hsi_blocks < 0 || c->hsi_blocks > 4096) {
+      c->idx_dim != kIdxDim || c->hsi_block != kHsiBlock || c->topk < 1 || c->topk > 1024 || c->window < 0 ||
+      c->window > 512 || !attend_tc_supported(c->topk, c->window) || (c->ratio != 1 && c->ratio != 2) || c->hsi_blocks < 0 || c->hsi_blocks > 4096) {
     *err = CSA2_ERR_UNSUPPORTED;
     return false;
   }
@@ -39,6 +39,18 @@ int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ER
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
+
+int csa2::num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
 
 extern "C" {
 

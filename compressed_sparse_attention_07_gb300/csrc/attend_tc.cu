@@ -1,0 +1,501 @@
+// a7 -- CSA2 sparse attention on the tensor cores.
+//
+// For one query token and a group of HG heads: rows E = the selected main-KV
+// entries followed by the window rows; logits l = scale * q_h . c_e; one
+// softmax per head over E; out_h = sum_e p_e c_e, the same 512-channel latent
+// serving as key and value (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.2.2 and
+// sec. 3.3.1; 36kr "CSA2").
+//
+// Rows are processed in tiles of 128 (top-k tiles, then window tiles, each
+// padded to 128 rows) and 128-channel chunks:
+//  - warp 4 gathers rows into a shared-memory staging ring with 1-D bulk
+//    copies: whole FP4 rows (256 B codes + 32 B scales) per top-k tile,
+//    256-byte bf16 chunks per window (or bf16-cache) tile and chunk;
+//  - warps 0-3 (thread r <-> row r of the tile) decode their row chunk to
+//    f16 into a K-major [128 rows x 128 channels] tile C;
+//  - phase A: thread 0 issues S^T[tile] += C . Q_chunk^T (M = 128 rows,
+//    N = HG heads) into TMEM for every tile;
+//  - softmax: exact two-pass per head over all rows from TMEM, P^T (f16) to
+//    shared memory (over the Q tile, which phase A no longer needs);
+//  - phase B: the rows are gathered and decoded again and
+//    O^T[chunk] += C^T . P^T[tile] (M = 128 channels, A read MN-major from the
+//    same C tile, N = HG heads) accumulates in TMEM;
+//  - epilogue: O^T / row sums -> fp32 out (coalesced), natural-log LSE.
+// FP4 values are exact in f16; bf16 Q / window rows are converted to f16
+// (exact for magnitudes in [2^-17, 65504]); accumulation is fp32.
+#include <algorithm>
+
+#include "internal.h"
+#include "tc.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kCons = 128;
+constexpr int kThreads = kCons + 32;
+constexpr uint32_t kSpin = 1u << 26;
+constexpr int kStageRow = 304;                 // staged FP4 row: 256 codes + 32 scales + pad (bank spread)
+constexpr int kStageRowChunk = 272;            // staged bf16 row chunk: 256 + pad
+constexpr int kStageBytes = 128 * kStageRow;   // 38912
+constexpr int kStages = 2;
+constexpr int kCBytes = 128 * 128 * 2;         // decoded f16 tile chunk
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttArgs {
+  int Tq, k, W, S;
+  int tiles_main, tiles_win;
+  const uint16_t* q;
+  CacheView mc;
+  const int32_t* n_entries;
+  int64_t capacity;
+  const int32_t* topk;
+  const uint16_t* swa;
+  const int32_t* swa_len;
+  const int64_t* swa_pos0;
+  const int64_t* q_pos;
+  float scale;
+  float* out;
+  float* lse;
+  int32_t* status;
+};
+
+__device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
+
+__device__ __forceinline__ uint32_t f16x2_from_f32(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return f16x2_from_f32(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t f16x2_scale(uint32_t sbyte) {
+  uint32_t r;
+  uint16_t pair = (uint16_t)(sbyte | (sbyte << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  return r;
+}
+
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Row source of slot i (tiles padded to 128): >= 0 main entry id,
+// <= -2 window row (-2 - row in swa), -1 empty.
+__device__ __forceinline__ int32_t slot_source(const AttArgs& a, int qi, int b, int i) {
+  const int kp = a.tiles_main * 128;
+  if (i < kp) {
+    if (i >= a.k) return -1;
+    const int32_t id = __ldg(a.topk + (int64_t)qi * a.k + i);
+    if (id < 0) return -1;
+    if (id >= __ldg(a.n_entries + b) || id >= a.capacity) {
+      report(a.status, CSA2_ERR_BAD_INDEX);
+      return -1;
+    }
+    return id;
+  }
+  const int w = i - kp;
+  if (w >= a.W) return -1;
+  const int64_t pos = __ldg(a.q_pos + qi) - a.W + 1 + w;
+  const int64_t p0 = __ldg(a.swa_pos0 + b);
+  int64_t len = __ldg(a.swa_len + b);
+  len = len < a.S ? len : a.S;
+  if (pos < 0 || pos < p0 || pos >= p0 + len) return -1;
+  return (int32_t)(-2 - (pos - p0));
+}
+
+template <int kDtype, int HG>
+__global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
+  constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
+  const int n_tiles = a.tiles_main + a.tiles_win;
+  const int nslot = n_tiles * 128;
+  const int n_chunks = n_tiles * 4;                            // per phase
+  const int units_main = kMainFp4 ? a.tiles_main : 4 * a.tiles_main;
+  const int units_phase = units_main + 4 * a.tiles_win;
+  const int tmem_cols = [&] {
+    int need = n_tiles * HG > 4 * HG ? n_tiles * HG : 4 * HG;
+    int c = 32;
+    while (c < need) c <<= 1;
+    return c;
+  }();
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stage = smem;                                        // kStages x kStageBytes
+  uint8_t* ctile = stage + kStages * kStageBytes;               // 2 x kCBytes
+  uint8_t* qp = ctile + 2 * kCBytes;                            // Q tile, later P^T
+  const int qp_bytes = max(HG * kDim * 2, nslot * HG * 2);
+  int32_t* src = reinterpret_cast<int32_t*>(qp + qp_bytes);     // [nslot]
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], cdone[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  __shared__ float red[4][HG];
+  __shared__ float m_s[HG], inv_s[HG];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hg = blockIdx.x, qi = blockIdx.y, b = qi / a.Tq;
+
+  // ---- set-up: row sources, Q (f16, K-major [HG][512]), barriers, TMEM
+  for (int i = tid; i < nslot; i += kThreads) src[i] = slot_source(a, qi, b, i);
+  for (int i = tid; i < HG * kDim / 2; i += kThreads) {
+    const int h = (2 * i) / kDim, kk = (2 * i) % kDim;
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.q + ((int64_t)qi * kHeads + hg * HG + h) * kDim) + kk / 2);
+    *reinterpret_cast<uint32_t*>(qp + tc::kmajor_off(h, kk, kDim)) = bf16x2_to_f16x2(w);
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full_bar[s], 1);
+      tc::mbar_init(&empty_bar[s], kCons);
+    }
+    tc::mbar_init(&cdone[0], 1);
+    tc::mbar_init(&cdone[1], 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    for (int u = 0; u < 2 * units_phase; ++u) {
+      const int s = u % kStages;
+      const int up = u % units_phase;
+      int t, c;  // tile, chunk (-1: whole FP4 rows)
+      if (up < units_main) {
+        t = kMainFp4 ? up : up / 4;
+        c = kMainFp4 ? -1 : up % 4;
+      } else {
+        t = a.tiles_main + (up - units_main) / 4;
+        c = (up - units_main) % 4;
+      }
+      // bytes of this unit
+      uint32_t bytes = 0;
+      for (int rr = lane; rr < 128; rr += 32) {
+        const int32_t sidx = src[t * 128 + rr];
+        if (sidx >= 0) {
+          if (page_of(a.mc, b, sidx, nullptr) >= 0) bytes += (c < 0) ? 288u : 256u;
+        } else if (sidx <= -2) {
+          bytes += 256u;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(&empty_bar[s], ((u / kStages) & 1) ^ 1, kSpin) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          report(a.status, CSA2_ERR_TIMEOUT);
+          atomicExch(&abort_flag, 1);
+        }
+        break;
+      }
+      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+      if (lane == 0) tc::mbar_arrive_expect_tx(&full_bar[s], bytes);
+      __syncwarp();
+      uint8_t* slot = stage + s * kStageBytes;
+      for (int rr = lane; rr < 128; rr += 32) {
+        const int32_t sidx = src[t * 128 + rr];
+        if (sidx >= 0) {
+          const int64_t page = page_of(a.mc, b, sidx, a.status);
+          if (page < 0) continue;
+          const int sl = sidx % kPage;
+          if (c < 0) {
+            tc::bulk_g2s(slot + rr * kStageRow, a.mc.data + page * kMainFp4Data + sl * (kDim / 2), 256, &full_bar[s]);
+            tc::bulk_g2s(slot + rr * kStageRow + 256, a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16), 32,
+                         &full_bar[s]);
+          } else {
+            tc::bulk_g2s(slot + rr * kStageRowChunk, a.mc.data + page * kMainBf16Data + sl * (kDim * 2) + 256 * c, 256,
+                         &full_bar[s]);
+          }
+        } else if (sidx <= -2) {
+          const int64_t row = -2 - (int64_t)sidx;
+          tc::bulk_g2s(slot + rr * kStageRowChunk, a.swa + ((int64_t)b * a.S + row) * kDim + 128 * c, 256, &full_bar[s]);
+        }
+      }
+      ++issued;
+    }
+    if (lane == 0)
+      for (int u = (issued > kStages ? issued - kStages : 0); u < issued; ++u)
+        if (!tc::mbar_wait(&full_bar[u % kStages], (u / kStages) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int r = tid;                 // row of the tile / TMEM lane / channel in the epilogue
+  const uint32_t lane_base = 32 * warp;
+  constexpr uint32_t kIdescS = tc::idesc_f16(128, HG, false, false, false, false);
+  constexpr uint32_t kIdescO = tc::idesc_f16(128, HG, false, false, true, false);
+  int last_issued = -1, waited = -1;
+  bool aborted = false;
+  for (int n = 0; n < 2 * n_chunks; ++n) {
+    const int ph = n / n_chunks, t = (n % n_chunks) / 4, c = n % 4;
+    const bool fp4_tile = kMainFp4 && t < a.tiles_main;
+    const int up = (t < a.tiles_main) ? (kMainFp4 ? t : 4 * t + c) : units_main + 4 * (t - a.tiles_main) + c;
+    const int u = ph * units_phase + up;
+    const int s = u % kStages;
+    const bool first = !fp4_tile || c == 0, last = !fp4_tile || c == 3;
+
+    if (ph == 1 && n == n_chunks) {
+      // ---------------- softmax over all rows (phase A complete)
+      const int e = n - 1;
+      const bool ok = tc::mbar_wait(&cdone[e & 1], (e >> 1) & 1, kSpin);
+      waited = e;
+      if (!ok) atomicExch(&abort_flag, 1);
+      tc::fence_after_sync();
+      const float sc2 = a.scale * kLog2e;
+      float m[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) m[h] = -INFINITY;
+      for (int tt = 0; tt < n_tiles; ++tt) {
+        const bool valid = src[tt * 128 + r] != -1;
+#pragma unroll
+        for (int h0 = 0; h0 < HG; h0 += 16) {
+          uint32_t v[16];
+          tc::tmem_ld16(tc::taddr(tb, lane_base, tt * HG + h0), v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (valid) m[h0 + j] = fmaxf(m[h0 + j], __uint_as_float(v[j]) * sc2);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], o));
+      }
+      if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < HG; ++h) red[warp][h] = m[h];
+      named_sync();
+      if (r < HG) m_s[r] = fmaxf(fmaxf(red[0][r], red[1][r]), fmaxf(red[2][r], red[3][r]));
+      named_sync();
+      float sum[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        m[h] = m_s[h];
+        sum[h] = 0.0f;
+      }
+      for (int tt = 0; tt < n_tiles; ++tt) {
+        const bool valid = src[tt * 128 + r] != -1;
+        const int row = tt * 128 + r;
+#pragma unroll
+        for (int h0 = 0; h0 < HG; h0 += 16) {
+          uint32_t v[16];
+          tc::tmem_ld16(tc::taddr(tb, lane_base, tt * HG + h0), v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int h = h0 + j;
+            float p = 0.0f;
+            if (valid && m[h] != -INFINITY) p = exp2f(__uint_as_float(v[j]) * sc2 - m[h]);
+            sum[h] += p;
+            *reinterpret_cast<__half*>(qp + tc::kmajor_off(h, row, nslot)) = __float2half_rn(p);
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], o);
+      }
+      if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < HG; ++h) red[warp][h] = sum[h];
+      named_sync();
+      if (r < HG) {
+        const float tot = red[0][r] + red[1][r] + red[2][r] + red[3][r];
+        inv_s[r] = tot > 0.0f ? 1.0f / tot : 0.0f;
+        if (a.lse)
+          a.lse[(int64_t)qi * kHeads + hg * HG + r] =
+              tot > 0.0f ? (m_s[r] + log2f(tot)) * 0.6931471805599453f : -INFINITY;
+      }
+      tc::fence_async_smem();
+    }
+
+    // ---------------- decode row chunk (t, c) into C tile n % 2
+    if (n >= 2) {  // the MMAs that read this C tile two chunks ago must be done
+      const int e = n - 2;
+      if (e > waited) {
+        if (!tc::mbar_wait(&cdone[e & 1], (e >> 1) & 1, kSpin)) atomicExch(&abort_flag, 1);
+        waited = e;
+      }
+    }
+    if (first && !tc::mbar_wait(&full_bar[s], (u / kStages) & 1, kSpin)) atomicExch(&abort_flag, 1);
+    {
+      uint8_t* ct = ctile + (n & 1) * kCBytes;
+      const uint8_t* slot = stage + s * kStageBytes;
+      const int32_t sidx = src[t * 128 + r];
+      uint32_t av[64];
+      if (sidx == -1) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) av[j] = 0u;
+      } else if (fp4_tile) {
+        const uint8_t* row = slot + r * kStageRow;
+        const uint2 scw = *reinterpret_cast<const uint2*>(row + 256 + 8 * c);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 cw = *reinterpret_cast<const uint4*>(row + 64 * c + 16 * q4);
+          const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int g = 2 * q4 + (q >> 1);  // 16-channel group within the chunk
+            const uint32_t s2 = f16x2_scale(((g < 4 ? scw.x : scw.y) >> (8 * (g & 3))) & 0xFFu);
+            uint32_t h4[4];
+            e2m1x8_to_f16x2(w4[q], h4);
+#pragma unroll
+            for (int by = 0; by < 4; ++by) av[16 * q4 + 4 * q + by] = hmul2(h4[by], s2);
+          }
+        }
+      } else {
+        const uint8_t* row = slot + r * kStageRowChunk;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * j);
+          av[4 * j] = bf16x2_to_f16x2(v.x);
+          av[4 * j + 1] = bf16x2_to_f16x2(v.y);
+          av[4 * j + 2] = bf16x2_to_f16x2(v.z);
+          av[4 * j + 3] = bf16x2_to_f16x2(v.w);
+        }
+      }
+      if (last) tc::mbar_arrive(&empty_bar[s]);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 8 * j, 128)) =
+            make_uint4(av[4 * j], av[4 * j + 1], av[4 * j + 2], av[4 * j + 3]);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    named_sync();
+    tc::fence_after_sync();
+    if (*reinterpret_cast<volatile int*>(&abort_flag)) {
+      aborted = true;
+      break;
+    }
+    if (tid == 0) {
+      const uint32_t cbase = tc::smem_u32(ctile + (n & 1) * kCBytes);
+      if (ph == 0) {
+        // S^T[t] (+)= C[128 rows x 128 ch] . Q[:, chunk c]^T
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = tc::sdesc(cbase + ks * 256, 128, 2048);
+          const uint64_t bd = tc::sdesc(tc::smem_u32(qp) + (c * 16 + ks * 2) * 128, 128, kDim * 16);
+          tc::mma_ss(tb + t * HG, ad, bd, kIdescS, (c > 0 || ks > 0) ? 1u : 0u);
+        }
+      } else {
+        // O^T[chunk c] (+)= C^T[128 ch x 128 rows] . P^T[tile t]
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = tc::sdesc(cbase + ks * 2 * 2048, 2048, 128);
+          const uint64_t bd = tc::sdesc(tc::smem_u32(qp) + (t * 16 + ks * 2) * 128, 128, nslot * 16);
+          tc::mma_ss(tb + c * HG, ad, bd, kIdescO, (t > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      tc::mma_commit(&cdone[n & 1]);
+    }
+    last_issued = n;
+  }
+
+  // ---------------- epilogue: O^T -> out
+  if (last_issued > waited) {
+    const bool ok = tc::mbar_wait(&cdone[last_issued & 1], (last_issued >> 1) & 1, kSpin);
+    if (!ok) {
+      report(a.status, CSA2_ERR_TIMEOUT);
+      aborted = true;
+    }
+  }
+  tc::fence_after_sync();
+  if (!aborted) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int h0 = 0; h0 < HG; h0 += 16) {
+        uint32_t v[16];
+        tc::tmem_ld16(tc::taddr(tb, lane_base, c * HG + h0), v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int h = h0 + j;
+          a.out[((int64_t)qi * kHeads + hg * HG + h) * kDim + c * 128 + r] = __uint_as_float(v[j]) * inv_s[h];
+        }
+      }
+    }
+  } else if (r == 0) {
+    report(a.status, CSA2_ERR_TIMEOUT);
+  }
+  tc::fence_before_sync();
+  named_sync();
+  if (warp == 0) tc::tmem_dealloc(tb, tmem_cols);
+}
+
+template <int kDtype, int HG>
+size_t att_smem(int n_tiles) {
+  const int nslot = n_tiles * 128;
+  return (size_t)kStages * kStageBytes + 2 * kCBytes + std::max(HG * kDim * 2, nslot * HG * 2) + nslot * 4;
+}
+
+template <int kDtype, int HG>
+cudaError_t launch_hg(const AttArgs& a, int Q, cudaStream_t stream) {
+  const size_t smem = att_smem<kDtype, HG>(a.tiles_main + a.tiles_win);
+  auto kern = attend_tc_kernel<kDtype, HG>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  kern<<<dim3(kHeads / HG, Q), kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+constexpr size_t kSmemLimit = 227 * 1024;
+
+template <int kDtype>
+cudaError_t launch_dtype(const AttArgs& a, int Q, int num_sms, cudaStream_t stream) {
+  const int nt = a.tiles_main + a.tiles_win;
+  // widest head group that fits TMEM (512 columns) and shared memory, preferring
+  // more CTAs when there are few query tokens
+  const bool few = (int64_t)Q * 2 < 2 * num_sms;
+  const bool fit64 = nt * 64 <= 512 && att_smem<kDtype, 64>(nt) <= kSmemLimit;
+  const bool fit32 = nt * 32 <= 512 && att_smem<kDtype, 32>(nt) <= kSmemLimit;
+  if (!few && fit64) return launch_hg<kDtype, 64>(a, Q, stream);
+  if ((int64_t)Q * 4 >= 2 * num_sms && fit32) return launch_hg<kDtype, 32>(a, Q, stream);
+  if (nt * 16 <= 512 && att_smem<kDtype, 16>(nt) <= kSmemLimit) return launch_hg<kDtype, 16>(a, Q, stream);
+  return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace
+
+bool attend_tc_supported(int topk, int window) {
+  const int nt = (topk + 127) / 128 + (window + 127) / 128;
+  return nt * 16 <= 512 && att_smem<CSA2_CACHE_FP4, 16>(nt) <= kSmemLimit;
+}
+
+cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q, const csa2_cache& main_c,
+                          const int32_t* n_entries, const int32_t* topk, const uint16_t* swa, int S,
+                          const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos,
+                          float scale, float* out, float* lse, int32_t* status, cudaStream_t stream) {
+  const int Q = B * Tq;
+  if (Q == 0) return cudaSuccess;
+  AttArgs a{Tq, cfg.topk, cfg.window, S, (cfg.topk + 127) / 128, (cfg.window + 127) / 128, q, view_of(main_c),
+            n_entries, (int64_t)main_c.max_pages * kPage, topk, swa, swa_len, swa_pos0, q_pos, scale, out, lse,
+            status};
+  if (cfg.cache_dtype == CSA2_CACHE_FP4) return launch_dtype<CSA2_CACHE_FP4>(a, Q, num_sms(), stream);
+  return launch_dtype<CSA2_CACHE_BF16>(a, Q, num_sms(), stream);
+}
+
+}  // namespace csa2

@@ -4,19 +4,26 @@
 // (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.3.1 and sec. 2.4.4; 36kr "CSA2",
 // "FP4 and Bounded Replay".)  One CTA per new entry; this step moves a few KB
 // per entry, so it is latency-bound and kept simple.
+#include <cmath>
+
 #include "internal.h"
 
 namespace csa2 {
 namespace {
 
+// RoPE inverse frequencies theta^(-2i/64), formed on the host in fp64.
+struct RopeFreqs {
+  double f[kRope / 2];
+};
+
 template <int kDtype>
-__global__ void __launch_bounds__(256) compress_kernel(int T, int r, double theta, const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs rf, const uint16_t* __restrict__ x,
                                                        const int64_t* __restrict__ pos0,
                                                        const float* __restrict__ merge_w,
                                                        const uint16_t* __restrict__ w_idx, CacheView mc,
                                                        CacheView ic, int32_t* n_entries, int32_t* status) {
   __shared__ float e_s[kDim];          // the stored (decoded) entry
-  __shared__ float kpart[2][kIdxDim];  // projection halves
+  __shared__ float kpart[8][kIdxDim];  // projection partial sums, 8 row slices
   const int m = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
   const int64_t j = pos0[b] / r + m;
 
@@ -30,13 +37,16 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, double thet
     v0 = (i == 0) ? w0 * x0 : fmaf(w0, x0, v0);
     v1 = (i == 0) ? w1 * x1 : fmaf(w1, x1, v1);
   }
-  // RoPE on the pair (2t, 2t+1) for the first 64 channels; angle in fp64
+  // RoPE on the pair (2t, 2t+1) for the first 64 channels: the angle p * f is
+  // formed and reduced modulo 2 pi in fp64 (Cody-Waite, 2 pi split so that
+  // k * hi is exact), then rotated with fp32 sincos of the reduced angle.
   if (t < kRope / 2) {
-    double p = (double)(r * j + r - 1);
-    double ang = p * pow(theta, -2.0 * t / kRope);
-    double sd, cd;
-    sincos(ang, &sd, &cd);
-    float c = (float)cd, s = (float)sd;
+    const double ang = (double)(r * j + r - 1) * rf.f[t];
+    const double kk = rint(ang * 0.15915494309189535);      // 1 / (2 pi)
+    double red = fma(-kk, 6.28318530717958623, ang);          // 2 pi, high part
+    red = fma(-kk, 2.4492935982947064e-16, red);              // 2 pi, low part
+    float s, c;
+    sincosf((float)red, &s, &c);
     float a = v0, bb = v1;
     v0 = fmaf(a, c, -(bb * s));
     v1 = fmaf(a, s, bb * c);
@@ -68,19 +78,30 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, double thet
   }
   __syncthreads();
 
-  // indexer K = stored entry . W_idx; two halves of the channel sum
+  // indexer K = stored entry . W_idx: thread t owns columns 4*(t%32)..+3 over
+  // the 64-row slice t/32 (64 independent 8-byte loads in flight, each warp
+  // reading whole 256-byte rows); the 8 slice sums are added in slice order.
   {
-    const int k = t & (kIdxDim - 1), half = t >> 7;
-    float acc = 0.0f;
-    const int c0 = half * (kDim / 2);
-#pragma unroll 8
-    for (int c = c0; c < c0 + kDim / 2; ++c)
-      acc = fmaf(e_s[c], bf16_bits_to_float(__ldg(w_idx + c * kIdxDim + k)), acc);
-    kpart[half][k] = acc;
+    const int kg = t & 31, rs = t >> 5;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const uint2* w2 = reinterpret_cast<const uint2*>(w_idx) + kg;  // row c at + c * 32
+#pragma unroll 16
+    for (int c = rs * 64; c < rs * 64 + 64; ++c) {
+      const uint2 wv = __ldg(w2 + c * (kIdxDim / 4));
+      const float e = e_s[c];
+      acc[0] = fmaf(e, __uint_as_float(wv.x << 16), acc[0]);
+      acc[1] = fmaf(e, __uint_as_float(wv.x & 0xFFFF0000u), acc[1]);
+      acc[2] = fmaf(e, __uint_as_float(wv.y << 16), acc[2]);
+      acc[3] = fmaf(e, __uint_as_float(wv.y & 0xFFFF0000u), acc[3]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) kpart[rs][4 * kg + q] = acc[q];
   }
   __syncthreads();
   if (t < kIdxDim) {
-    const float kv = kpart[0][t] + kpart[1][t];
+    float kv = kpart[0][t];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) kv += kpart[q][t];
     const int64_t ipage = page_of(ic, b, j, status);
     if (kDtype == CSA2_CACHE_FP4) {
       float amax = fabsf(kv);
@@ -115,12 +136,14 @@ cudaError_t launch_compress(const csa2_cfg& cfg, int B, int T, const uint16_t* x
   const int M = T / cfg.ratio;
   if (M == 0 || B == 0) return cudaSuccess;
   dim3 grid(M, B);
+  RopeFreqs rf;
+  for (int i = 0; i < kRope / 2; ++i) rf.f[i] = std::pow(cfg.rope_theta, -2.0 * i / kRope);
   if (cfg.cache_dtype == CSA2_CACHE_FP4)
-    compress_kernel<CSA2_CACHE_FP4><<<grid, 256, 0, stream>>>(T, cfg.ratio, cfg.rope_theta, x, pos0, merge_w,
+    compress_kernel<CSA2_CACHE_FP4><<<grid, 256, 0, stream>>>(T, cfg.ratio, rf, x, pos0, merge_w,
                                                               w_idx, view_of(main_c), view_of(idx_c),
                                                               n_entries, status);
   else
-    compress_kernel<CSA2_CACHE_BF16><<<grid, 256, 0, stream>>>(T, cfg.ratio, cfg.rope_theta, x, pos0, merge_w,
+    compress_kernel<CSA2_CACHE_BF16><<<grid, 256, 0, stream>>>(T, cfg.ratio, rf, x, pos0, merge_w,
                                                                w_idx, view_of(main_c), view_of(idx_c),
                                                                n_entries, status);
   return cudaGetLastError();

@@ -84,37 +84,6 @@ __device__ __forceinline__ void load_query(int qi, const uint16_t* q_idx, const 
   __syncthreads();
 }
 
-// Full: every visible entry.  scores [chunk][max_entries], bmax [chunk][ceil(max_entries/8)].
-template <int kDtype>
-__global__ void __launch_bounds__(kScoreThreads) score_full_kernel(int q0, int Tq, int r, const uint16_t* __restrict__ q_idx,
-                                                                   const float* __restrict__ head_w,
-                                                                   const int64_t* __restrict__ q_pos, CacheView ic,
-                                                                   const int32_t* __restrict__ n_entries,
-                                                                   int64_t max_entries, float* scores, float* bmax,
-                                                                   int32_t* status) {
-  __shared__ __align__(16) float qs[kIdxHeads][kIdxDim];
-  __shared__ float hw[kIdxHeads];
-  const int qi = q0 + blockIdx.y, b = qi / Tq;
-  const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
-  const int64_t j0 = (int64_t)blockIdx.x * kScoreThreads;
-  if (j0 >= nv) return;
-  load_query(qi, q_idx, head_w, qs, hw);
-  const int64_t j = j0 + threadIdx.x;
-  float s = -INFINITY;
-  if (j < nv) {
-    float kv[kIdxDim];
-    if (load_idx_entry<kDtype>(ic, b, j, kv, status)) s = index_score(qs, hw, kv);
-    scores[(int64_t)blockIdx.y * max_entries + j] = s;
-  }
-  if (bmax) {
-    float m = s;
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-    if ((threadIdx.x & 7) == 0 && j < nv) bmax[(int64_t)blockIdx.y * ((max_entries + 7) / 8) + j / 8] = m;
-  }
-}
-
 // Reindex: the visible entries of the pool's blocks; position p -> block
 // pool[p / 8], entry block * 8 + p % 8.  scores [chunk][n_blocks * 8].
 template <int kDtype>
@@ -349,13 +318,9 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
                                                                            q_pos, iv, n_entries, max_entries, pool,
                                                                            scores, status);
     } else {
-      dim3 g((unsigned)((max_entries + kScoreThreads - 1) / kScoreThreads), nq);
-      if (cfg.cache_dtype == CSA2_CACHE_FP4)
-        score_full_kernel<CSA2_CACHE_FP4><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, q_idx, head_w, q_pos, iv,
-                                                                          n_entries, max_entries, scores, bmax, status);
-      else
-        score_full_kernel<CSA2_CACHE_BF16><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, q_idx, head_w, q_pos, iv,
-                                                                           n_entries, max_entries, scores, bmax, status);
+      cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, scores, bmax,
+                                      status, num_sms(), stream);
+      if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

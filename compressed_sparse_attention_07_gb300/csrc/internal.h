@@ -19,6 +19,15 @@ cudaError_t launch_compress(const csa2_cfg& cfg, int B, int T, const uint16_t* x
                             const csa2_cache& idx_c, int32_t* n_entries, int32_t* status,
                             cudaStream_t stream);
 
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms();
+
+// Tensor-core indexer scores (Full mode) for queries [q0, q0 + nq).
+cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
+                            const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
+                            int64_t max_entries, float* scores, float* bmax, int32_t* status, int num_sms,
+                            cudaStream_t stream);
+
 // Per-query workspace bytes of the indexer (scores + HSI block maxima).
 size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex);
 
@@ -32,6 +41,9 @@ cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q,
                           const int32_t* n_entries, const int32_t* topk, const uint16_t* swa, int S,
                           const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos,
                           float scale, float* out, float* lse, int32_t* status, cudaStream_t stream);
+
+// Whether the attention kernel fits top-k + window rows (TMEM and shared memory).
+bool attend_tc_supported(int topk, int window);
 
 cudaError_t launch_gather_dequant(const csa2_cache& c, int cache_dtype, int B, int n, const int32_t* ids,
                                   float* out, int32_t* status, cudaStream_t stream);

@@ -23,7 +23,7 @@
  *    skipped.  No call aborts the process or raises across the ABI.
  *  - Sizes fixed by the model and accepted only at these values: dim 512,
  *    rope_dims 64, n_heads 64, idx_heads 32, idx_dim 128, hsi_block 8.
- *    topk (1..2048), window (0..1024), ratio (1 or 2), hsi_blocks (0..4096)
+ *    topk (1..1024), window (0..512), ratio (1 or 2), hsi_blocks (0..4096)
  *    and rope_theta are free.
  *
  * Paged cache layout (a build choice; the pages never mention paging).  A

@@ -293,3 +293,49 @@ def test_attend_reports_out_of_range_ids():
     want = oracle.attend(oc, np.array([N]), q, np.array([[[3, 50, 99, -1, -1]]], np.int32), swa,
                          np.array([4], np.int32), np.array([96]), np.array([[99]]), 4, 1 / math.sqrt(D))
     assert P.attention_rel_err(out.cpu().numpy(), want) <= P.ATT_TOL
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_index_prefill_queries_share_tiles(integer):
+    """Prefill-shaped indexing: 8 consecutive causal queries of one sequence
+    (four per CTA on the tensor-core path) over a cache of many tiles, r = 2,
+    with HSI blocks; exact on integer inputs, near-tie tolerant otherwise."""
+    B, N, k, nb = 1, 9000, 512, 256
+    oc, pc = _idx_caches(B, N, "fp4", seed=24, integer=integer, dup=integer)
+    g = synth.rng(24, "q")
+    Tq = 8
+    q_idx = synth.integer_bf16(g, (B, Tq, H, CI), -1, 1) if integer else synth.normal_bf16(g, (B, Tq, H, CI))
+    q_pos = (2 * N - Tq + np.arange(Tq)).reshape(1, Tq).astype(np.int64)  # last 8 positions: ragged visibility
+    q_pos[0, :3] = [1, 200, 5001]
+    n_ent = np.array([N], np.int32)
+    cfg = csa.Cfg(ratio=2, topk=k, hsi_blocks=nb)
+    g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+    o_top, o_pool, s = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=2, k=k, hsi_blocks=nb, hsi_block=8,
+                                         want_pool=True, want_scores=True)
+    if integer:
+        np.testing.assert_array_equal(g_top, o_top)
+        np.testing.assert_array_equal(g_pool, o_pool)
+    else:
+        assert P.topk_mismatch(g_top.reshape(Tq, k), o_top.reshape(Tq, k), s.reshape(Tq, -1), k, exact=False) == 0
+        for t in range(Tq):  # pools may differ only by near-tied block maxima
+            gp, op = set(g_pool[0, t][g_pool[0, t] >= 0]), set(o_pool[0, t][o_pool[0, t] >= 0])
+            if gp != op:
+                nv = (q_pos[0, t] - 1) // 2 + 1
+                bm = [s[0, t, 8 * b_:min(8 * b_ + 8, nv)].max() for b_ in range((nv + 7) // 8)]
+                kth = sorted(bm, reverse=True)[nb - 1]
+                assert all(abs(bm[b_] - kth) <= P.NEAR_TIE * abs(kth) for b_ in gp ^ op)
+
+
+def test_index_long_cache_many_tiles_per_cta():
+    """One decode query per sequence over 40000 entries: each CTA walks many
+    tiles through the shared-memory ring (wrap-around of every stage)."""
+    B, N, k = 2, 40000, 512
+    oc, pc = _idx_caches(B, N, "fp4", seed=25, integer=True, dup=True)
+    q_idx = synth.integer_bf16(synth.rng(25, "q"), (B, 1, H, CI), -1, 1)
+    q_pos = np.array([[N - 1], [31000]], np.int64)
+    n_ent = np.array([N, 35000], np.int32)
+    cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=2048)
+    g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+    o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=2048, want_pool=True)
+    np.testing.assert_array_equal(g_top, o_top)
+    np.testing.assert_array_equal(g_pool, o_pool)

@@ -8,11 +8,12 @@
 //
 // Rows are processed in tiles of 128 (top-k tiles, then window tiles, each
 // padded to 128 rows) and 128-channel chunks:
-//  - warp 4 gathers rows into a shared-memory staging ring with 1-D bulk
-//    copies: whole FP4 rows (256 B codes + 32 B scales) per top-k tile,
-//    256-byte bf16 chunks per window (or bf16-cache) tile and chunk;
-//  - warps 0-3 (thread r <-> row r of the tile) decode their row chunk to
-//    f16 into a K-major [128 rows x 128 channels] tile C;
+//  - thread r of the CTA owns row r of every tile: it gathers that row into
+//    a shared-memory staging ring with 16-byte cp.async copies, several units
+//    ahead (whole FP4 rows, 256 B codes + 32 B scales, per top-k tile;
+//    256-byte bf16 chunks per window or bf16-cache tile and chunk), then
+//    decodes its row chunk to f16 into a K-major [128 rows x 128 channels]
+//    tile C;
 //  - phase A: thread 0 issues S^T[tile] += C . Q_chunk^T (M = 128 rows,
 //    N = HG heads) into TMEM for every tile;
 //  - softmax: exact two-pass per head over all rows from TMEM, P^T (f16) to
@@ -32,12 +33,11 @@ namespace csa2 {
 namespace {
 
 constexpr int kCons = 128;
-constexpr int kThreads = kCons + 32;
+constexpr int kThreads = kCons;
 constexpr uint32_t kSpin = 1u << 26;
 constexpr int kStageRow = 304;                 // staged FP4 row: 256 codes + 32 scales + pad (bank spread)
 constexpr int kStageRowChunk = 272;            // staged bf16 row chunk: 256 + pad
 constexpr int kStageBytes = 128 * kStageRow;   // 38912
-constexpr int kStages = 2;
 constexpr int kCBytes = 128 * 128 * 2;         // decoded f16 tile chunk
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -58,6 +58,13 @@ struct AttArgs {
   float* lse;
   int32_t* status;
 };
+
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
 
@@ -92,8 +99,10 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return r;
 }
 
-// Row source of slot i (tiles padded to 128): >= 0 main entry id,
-// <= -2 window row (-2 - row in swa), -1 empty.
+// Row source of slot i (tiles padded to 128), page already resolved:
+// >= 0 main entry at page * 64 + slot of the page pool, <= -2 window row
+// (-2 - row in swa), -1 empty.  Resolving the block table once here keeps
+// dependent global loads off the gather path.
 __device__ __forceinline__ int32_t slot_source(const AttArgs& a, int qi, int b, int i) {
   const int kp = a.tiles_main * 128;
   if (i < kp) {
@@ -104,7 +113,9 @@ __device__ __forceinline__ int32_t slot_source(const AttArgs& a, int qi, int b, 
       report(a.status, CSA2_ERR_BAD_INDEX);
       return -1;
     }
-    return id;
+    const int64_t page = page_of(a.mc, b, id, a.status);
+    if (page < 0) return -1;
+    return (int32_t)(page * kPage + id % kPage);
   }
   const int w = i - kp;
   if (w >= a.W) return -1;
@@ -116,7 +127,7 @@ __device__ __forceinline__ int32_t slot_source(const AttArgs& a, int qi, int b, 
   return (int32_t)(-2 - (pos - p0));
 }
 
-template <int kDtype, int HG>
+template <int kDtype, int HG, int kStages>
 __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   const int n_tiles = a.tiles_main + a.tiles_win;
@@ -137,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
   uint8_t* qp = ctile + 2 * kCBytes;                            // Q tile, later P^T
   const int qp_bytes = max(HG * kDim * 2, nslot * HG * 2);
   int32_t* src = reinterpret_cast<int32_t*>(qp + qp_bytes);     // [nslot]
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], cdone[2];
+  __shared__ __align__(8) uint64_t cdone[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ float red[4][HG];
@@ -154,10 +165,6 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
     *reinterpret_cast<uint32_t*>(qp + tc::kmajor_off(h, kk, kDim)) = bf16x2_to_f16x2(w);
   }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&full_bar[s], 1);
-      tc::mbar_init(&empty_bar[s], kCons);
-    }
     tc::mbar_init(&cdone[0], 1);
     tc::mbar_init(&cdone[1], 1);
     abort_flag = 0;
@@ -173,11 +180,11 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
   tc::fence_after_sync();
   const uint32_t tb = tmem_base;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    int issued = 0;
-    for (int u = 0; u < 2 * units_phase; ++u) {
-      const int s = u % kStages;
+  // Gather this thread's row of staging unit u (2 phases x units_phase units)
+  // into ring slot u % kStages; one commit group per unit, empty or not.
+  const int total_units = 2 * units_phase;
+  auto gather = [&](int u) {
+    if (u < total_units) {
       const int up = u % units_phase;
       int t, c;  // tile, chunk (-1: whole FP4 rows)
       if (up < units_main) {
@@ -187,58 +194,36 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
         t = a.tiles_main + (up - units_main) / 4;
         c = (up - units_main) % 4;
       }
-      // bytes of this unit
-      uint32_t bytes = 0;
-      for (int rr = lane; rr < 128; rr += 32) {
-        const int32_t sidx = src[t * 128 + rr];
-        if (sidx >= 0) {
-          if (page_of(a.mc, b, sidx, nullptr) >= 0) bytes += (c < 0) ? 288u : 256u;
-        } else if (sidx <= -2) {
-          bytes += 256u;
-        }
-      }
+      uint8_t* slot = stage + (u % kStages) * kStageBytes;
+      const int32_t sidx = src[t * 128 + tid];
+      if (sidx >= 0) {
+        const int64_t page = sidx / kPage;
+        const int sl = sidx % kPage;
+        if (c < 0) {
+          const uint8_t* g = a.mc.data + page * kMainFp4Data + sl * (kDim / 2);
+          const uint8_t* gs = a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16);
+          uint8_t* d = slot + tid * kStageRow;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-      int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait(&empty_bar[s], ((u / kStages) & 1) ^ 1, kSpin) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) {
-          report(a.status, CSA2_ERR_TIMEOUT);
-          atomicExch(&abort_flag, 1);
+          for (int j = 0; j < 16; ++j) cp16(d + 16 * j, g + 16 * j);
+          cp16(d + 256, gs);
+          cp16(d + 272, gs + 16);
+        } else {
+          const uint8_t* g = a.mc.data + page * kMainBf16Data + sl * (kDim * 2) + 256 * c;
+          uint8_t* d = slot + tid * kStageRowChunk;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cp16(d + 16 * j, g + 16 * j);
         }
-        break;
+      } else if (sidx <= -2) {
+        const uint16_t* g = a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx)) * kDim + 128 * c;
+        uint8_t* d = slot + tid * kStageRowChunk;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) cp16(d + 16 * j, g + 8 * j);
       }
-      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
-      if (lane == 0) tc::mbar_arrive_expect_tx(&full_bar[s], bytes);
-      __syncwarp();
-      uint8_t* slot = stage + s * kStageBytes;
-      for (int rr = lane; rr < 128; rr += 32) {
-        const int32_t sidx = src[t * 128 + rr];
-        if (sidx >= 0) {
-          const int64_t page = page_of(a.mc, b, sidx, a.status);
-          if (page < 0) continue;
-          const int sl = sidx % kPage;
-          if (c < 0) {
-            tc::bulk_g2s(slot + rr * kStageRow, a.mc.data + page * kMainFp4Data + sl * (kDim / 2), 256, &full_bar[s]);
-            tc::bulk_g2s(slot + rr * kStageRow + 256, a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16), 32,
-                         &full_bar[s]);
-          } else {
-            tc::bulk_g2s(slot + rr * kStageRowChunk, a.mc.data + page * kMainBf16Data + sl * (kDim * 2) + 256 * c, 256,
-                         &full_bar[s]);
-          }
-        } else if (sidx <= -2) {
-          const int64_t row = -2 - (int64_t)sidx;
-          tc::bulk_g2s(slot + rr * kStageRowChunk, a.swa + ((int64_t)b * a.S + row) * kDim + 128 * c, 256, &full_bar[s]);
-        }
-      }
-      ++issued;
     }
-    if (lane == 0)
-      for (int u = (issued > kStages ? issued - kStages : 0); u < issued; ++u)
-        if (!tc::mbar_wait(&full_bar[u % kStages], (u / kStages) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
-    return;
-  }
+    cp_commit();
+  };
+#pragma unroll
+  for (int u = 0; u < kStages - 1; ++u) gather(u);
 
   // -------------------------------------------------------------- consumers
   const int r = tid;                 // row of the tile / TMEM lane / channel in the epilogue
@@ -253,7 +238,13 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
     const int up = (t < a.tiles_main) ? (kMainFp4 ? t : 4 * t + c) : units_main + 4 * (t - a.tiles_main) + c;
     const int u = ph * units_phase + up;
     const int s = u % kStages;
-    const bool first = !fp4_tile || c == 0, last = !fp4_tile || c == 3;
+    const bool first = !fp4_tile || c == 0;
+    if (first) {
+      // keep kStages - 1 units in flight; unit u's copies (this thread's own
+      // row) are complete once at most kStages - 1 newer groups are pending
+      gather(u + kStages - 1);
+      cp_wait<kStages - 1>();
+    }
 
     if (ph == 1 && n == n_chunks) {
       // ---------------- softmax over all rows (phase A complete)
@@ -340,7 +331,6 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
         waited = e;
       }
     }
-    if (first && !tc::mbar_wait(&full_bar[s], (u / kStages) & 1, kSpin)) atomicExch(&abort_flag, 1);
     {
       uint8_t* ct = ctile + (n & 1) * kCBytes;
       const uint8_t* slot = stage + s * kStageBytes;
@@ -377,7 +367,6 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
           av[4 * j + 3] = bf16x2_to_f16x2(v.w);
         }
       }
-      if (last) tc::mbar_arrive(&empty_bar[s]);
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 8 * j, 128)) =
@@ -416,6 +405,7 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
   }
 
   // ---------------- epilogue: O^T -> out
+  cp_wait<0>();  // no copies into this CTA's shared memory outlive it
   if (last_issued > waited) {
     const bool ok = tc::mbar_wait(&cdone[last_issued & 1], (last_issued >> 1) & 1, kSpin);
     if (!ok) {
@@ -448,21 +438,28 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
 }
 
 template <int kDtype, int HG>
-size_t att_smem(int n_tiles) {
+size_t att_smem(int n_tiles, int stages = 2) {
   const int nslot = n_tiles * 128;
-  return (size_t)kStages * kStageBytes + 2 * kCBytes + std::max(HG * kDim * 2, nslot * HG * 2) + nslot * 4;
+  return (size_t)stages * kStageBytes + 2 * kCBytes + std::max(HG * kDim * 2, nslot * HG * 2) + nslot * 4;
 }
 
-template <int kDtype, int HG>
-cudaError_t launch_hg(const AttArgs& a, int Q, cudaStream_t stream) {
-  const size_t smem = att_smem<kDtype, HG>(a.tiles_main + a.tiles_win);
-  auto kern = attend_tc_kernel<kDtype, HG>;
+template <int kDtype, int HG, int kStages>
+cudaError_t launch_hgs(const AttArgs& a, int Q, cudaStream_t stream) {
+  const size_t smem = att_smem<kDtype, HG>(a.tiles_main + a.tiles_win, kStages);
+  auto kern = attend_tc_kernel<kDtype, HG, kStages>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   kern<<<dim3(kHeads / HG, Q), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kSmemLimit = 225 * 1024;  // dynamic, leaving room for static shared memory
+
+template <int kDtype, int HG>
+cudaError_t launch_hg(const AttArgs& a, int Q, cudaStream_t stream) {
+  // three staging units in flight when they fit, else two
+  if (att_smem<kDtype, HG>(a.tiles_main + a.tiles_win, 3) <= kSmemLimit) return launch_hgs<kDtype, HG, 3>(a, Q, stream);
+  return launch_hgs<kDtype, HG, 2>(a, Q, stream);
+}
 
 template <int kDtype>
 cudaError_t launch_dtype(const AttArgs& a, int Q, int num_sms, cudaStream_t stream) {

@@ -12,6 +12,7 @@ namespace {
 constexpr int kScoreThreads = 128;  // one entry per thread
 constexpr int kSelThreads = 1024;   // one CTA selects for one query
 constexpr uint32_t kInvalid = 0xFFFFFFFFu;  // score bit pattern of a non-candidate
+constexpr int64_t kSelSmemKeys = 48 * 1024;  // keys held in shared memory (192 KB)
 
 // Decoded indexer-K entry (128 channels) of sequence b, slot j, into registers.
 template <int kDtype>
@@ -164,15 +165,23 @@ struct IdMap {
 // Select the k largest keys among n positions of `vals` ((key desc, position
 // asc)); `forced` (>= 0) gets the largest key.  Writes ids ascending to out[k],
 // -1 padded.  Radix select (11/11/10-bit digits) then an ordered compaction.
-__device__ void block_select(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out) {
+// skeys: shared-memory copy of the n keys when it fits (every pass after the
+// first then reads shared memory), else nullptr (every pass reads vals).
+__device__ void block_select(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
+                             uint32_t* skeys) {
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t warp_sums[33];
   __shared__ uint32_t sh_krem, sh_digit;
-  auto key_at = [&](int64_t p) -> uint32_t { return p == forced ? 0xFFFFFFFFu : order_key(vals[p]); };
+  auto gkey = [&](int64_t p) -> uint32_t { return p == forced ? 0xFFFFFFFFu : order_key(vals[p]); };
+  auto key_at = [&](int64_t p) -> uint32_t { return skeys ? skeys[p] : gkey(p); };
 
-  // count valid candidates
+  // count valid candidates (and stage the keys)
   uint32_t cnt = 0;
-  for (int64_t p = threadIdx.x; p < n; p += kSelThreads) cnt += key_at(p) != 0u;
+  for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
+    const uint32_t kk = gkey(p);
+    if (skeys) skeys[p] = kk;
+    cnt += kk != 0u;
+  }
   uint32_t nvalid;
   block_exclusive_scan(cnt, warp_sums, nvalid);
 
@@ -255,25 +264,28 @@ __device__ void block_select(const float* vals, int64_t n, int k, int64_t forced
 
 // blockIdx.y == 0: entry top-k; == 1: HSI block pool (Full) .
 __global__ void __launch_bounds__(kSelThreads) select_kernel(int q0, int Tq, int r, int k, int n_blocks, int64_t max_entries,
+                                                             int64_t smem_keys,
                                                              const int64_t* __restrict__ q_pos,
                                                              const int32_t* __restrict__ n_entries,
                                                              const int32_t* __restrict__ pool, const float* scores,
                                                              const float* bmax, int64_t score_stride,
                                                              int32_t* topk_out, int32_t* pool_out) {
+  extern __shared__ uint32_t skeys_dyn[];
   const int qc = blockIdx.x, qi = q0 + qc, b = qi / Tq;
   const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
+  auto keys_for = [&](int64_t n) -> uint32_t* { return n <= smem_keys ? skeys_dyn : nullptr; };
   if (blockIdx.y == 0) {
     const float* v = scores + (int64_t)qc * score_stride;
     if (pool) {
       block_select(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks},
-                   topk_out + (int64_t)qi * k);
+                   topk_out + (int64_t)qi * k, keys_for((int64_t)n_blocks * kHsiBlock));
     } else {
-      block_select(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k);
+      block_select(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k, keys_for(nv));
     }
   } else {
     const int64_t nb = (nv + kHsiBlock - 1) / kHsiBlock;
     const float* v = bmax + (int64_t)qc * ((max_entries + 7) / 8);
-    block_select(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks);
+    block_select(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks, keys_for(nb));
   }
 }
 
@@ -324,9 +336,15 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // keys staged in shared memory when the largest candidate list fits
+    const int64_t n_max = reindex ? stride : (int64_t)max_entries;
+    const int64_t smem_keys = std::min<int64_t>(n_max, kSelSmemKeys);
     dim3 sg(nq, (!reindex && pool_out) ? 2 : 1);
-    select_kernel<<<sg, kSelThreads, 0, stream>>>(q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, max_entries, q_pos,
-                                                  n_entries, pool, scores, bmax, stride, topk_out, pool_out);
+    const size_t sel_smem = (size_t)smem_keys * sizeof(uint32_t);
+    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
+    select_kernel<<<sg, kSelThreads, sel_smem, stream>>>(q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, max_entries,
+                                                         smem_keys, q_pos, n_entries, pool, scores, bmax, stride,
+                                                         topk_out, pool_out);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

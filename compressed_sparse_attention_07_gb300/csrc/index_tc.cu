@@ -24,6 +24,7 @@ namespace {
 constexpr int kConsumers = 128;
 constexpr int kThreads = kConsumers + 32;
 constexpr uint32_t kSpin = 1u << 26;
+constexpr int kMaxTilesPerCta = 512;
 
 template <int kDtype>
 struct TileFmt {
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
   __shared__ __align__(8) uint64_t full_bar[S], empty_bar[S], mma_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ int32_t ptab[2 * kMaxTilesPerCta];  // resolved pages of this CTA's tiles
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int g0 = a.q0 + blockIdx.y * QPC;   // first query of the group (same sequence)
@@ -116,6 +118,10 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
   }
   for (int i = tid; i < QPC * kIdxHeads; i += kThreads)
     hw[i / kIdxHeads][i % kIdxHeads] = a.head_w ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;
+  for (int i = tid; i < 2 * n_my; i += kThreads) {
+    const int64_t p = 2 * t_begin + i;  // logical page
+    ptab[i] = (p * kPage < nv_max) ? (int32_t)page_of(a.ic, b, p * kPage, a.status) : -1;
+  }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&full_bar[s], 1);
@@ -149,16 +155,12 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
         }
         if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
         uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
-        const int64_t tile = t_begin + i;
         uint32_t bytes = 0;
         int64_t pages[2] = {-1, -1};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int64_t p = 2 * tile + h;  // logical page
-          if (p * kPage < nv_max) {
-            pages[h] = page_of(a.ic, b, p * kPage, a.status);
-            if (pages[h] >= 0) bytes += F::kPageData + F::kPageScales;
-          }
+          pages[h] = ptab[2 * i + h];
+          if (pages[h] >= 0) bytes += F::kPageData + F::kPageScales;
         }
         tc::mbar_arrive_expect_tx(&full_bar[s], bytes);
 #pragma unroll
@@ -314,7 +316,7 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   const int64_t tiles = (max_entries + 127) / 128;
   // enough CTAs for a few waves, at least 4 tiles each
   const int64_t want = std::max<int64_t>(1, (int64_t)(qpc == 1 ? 4 : 2) * num_sms / std::max(groups, 1));
-  int64_t per = std::max<int64_t>(4, (tiles + want - 1) / want);
+  int64_t per = std::min<int64_t>(kMaxTilesPerCta, std::max<int64_t>(4, (tiles + want - 1) / want));
   const int splits = (int)((tiles + per - 1) / per);
   ScoreArgs a{q0, Tq, cfg.ratio, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
               scores, bmax, status};

@@ -32,8 +32,7 @@
 namespace csa2 {
 namespace {
 
-constexpr int kCons = 128;
-constexpr int kThreads = kCons;
+constexpr int kThreads = 512;  // four threads per row of a 128-row tile
 constexpr uint32_t kSpin = 1u << 26;
 constexpr int kStageRow = 304;                 // staged FP4 row: 256 codes + 32 scales + pad (bank spread)
 constexpr int kStageRowChunk = 272;            // staged bf16 row chunk: 256 + pad
@@ -66,7 +65,6 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
 
 __device__ __forceinline__ uint32_t f16x2_from_f32(float lo, float hi) {
   uint32_t r;
@@ -128,8 +126,9 @@ __device__ __forceinline__ int32_t slot_source(const AttArgs& a, int qi, int b, 
 }
 
 template <int kDtype, int HG, int kStages>
-__global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
+  constexpr int CPT = HG / 4;  // TMEM columns (heads) per thread in softmax / epilogue
   const int n_tiles = a.tiles_main + a.tiles_win;
   const int nslot = n_tiles * 128;
   const int n_chunks = n_tiles * 4;                            // per phase
@@ -155,14 +154,19 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
   __shared__ float m_s[HG], inv_s[HG];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127;         // row of the tile (TMEM lane); channel in the epilogue
+  const int p = tid >> 7;          // quarter of the row chunk / column group
+  const int quad = warp & 3;       // TMEM lane quadrant this warp may access
+  const uint32_t lane_base = 32 * quad;
   const int hg = blockIdx.x, qi = blockIdx.y, b = qi / a.Tq;
 
   // ---- set-up: row sources, Q (f16, K-major [HG][512]), barriers, TMEM
   for (int i = tid; i < nslot; i += kThreads) src[i] = slot_source(a, qi, b, i);
-  for (int i = tid; i < HG * kDim / 2; i += kThreads) {
-    const int h = (2 * i) / kDim, kk = (2 * i) % kDim;
-    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(a.q + ((int64_t)qi * kHeads + hg * HG + h) * kDim) + kk / 2);
-    *reinterpret_cast<uint32_t*>(qp + tc::kmajor_off(h, kk, kDim)) = bf16x2_to_f16x2(w);
+  for (int i = tid; i < HG * kDim / 8; i += kThreads) {
+    const int h = (8 * i) / kDim, kk = (8 * i) % kDim;
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)qi * kHeads + hg * HG + h) * kDim + kk));
+    *reinterpret_cast<uint4*>(qp + tc::kmajor_off(h, kk, kDim)) =
+        make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
   }
   if (tid == 0) {
     tc::mbar_init(&cdone[0], 1);
@@ -180,8 +184,9 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
   tc::fence_after_sync();
   const uint32_t tb = tmem_base;
 
-  // Gather this thread's row of staging unit u (2 phases x units_phase units)
-  // into ring slot u % kStages; one commit group per unit, empty or not.
+  // Gather quarter p of row r of staging unit u (2 phases x units_phase units)
+  // into ring slot u % kStages with 16-byte cp.async copies; one commit group
+  // per unit, empty or not.
   const int total_units = 2 * units_phase;
   auto gather = [&](int u) {
     if (u < total_units) {
@@ -195,29 +200,27 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
         c = (up - units_main) % 4;
       }
       uint8_t* slot = stage + (u % kStages) * kStageBytes;
-      const int32_t sidx = src[t * 128 + tid];
+      const int32_t sidx = src[t * 128 + r];
       if (sidx >= 0) {
         const int64_t page = sidx / kPage;
         const int sl = sidx % kPage;
         if (c < 0) {
           const uint8_t* g = a.mc.data + page * kMainFp4Data + sl * (kDim / 2);
-          const uint8_t* gs = a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16);
-          uint8_t* d = slot + tid * kStageRow;
+          uint8_t* d = slot + r * kStageRow;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) cp16(d + 16 * j, g + 16 * j);
-          cp16(d + 256, gs);
-          cp16(d + 272, gs + 16);
+          for (int j = p; j < 16; j += 4) cp16(d + 16 * j, g + 16 * j);
+          if (p < 2) cp16(d + 256 + 16 * p, a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16) + 16 * p);
         } else {
           const uint8_t* g = a.mc.data + page * kMainBf16Data + sl * (kDim * 2) + 256 * c;
-          uint8_t* d = slot + tid * kStageRowChunk;
+          uint8_t* d = slot + r * kStageRowChunk;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) cp16(d + 16 * j, g + 16 * j);
+          for (int j = p; j < 16; j += 4) cp16(d + 16 * j, g + 16 * j);
         }
       } else if (sidx <= -2) {
         const uint16_t* g = a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx)) * kDim + 128 * c;
-        uint8_t* d = slot + tid * kStageRowChunk;
+        uint8_t* d = slot + r * kStageRowChunk;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) cp16(d + 16 * j, g + 8 * j);
+        for (int j = p; j < 16; j += 4) cp16(d + 16 * j, g + 8 * j);
       }
     }
     cp_commit();
@@ -225,9 +228,6 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
 #pragma unroll
   for (int u = 0; u < kStages - 1; ++u) gather(u);
 
-  // -------------------------------------------------------------- consumers
-  const int r = tid;                 // row of the tile / TMEM lane / channel in the epilogue
-  const uint32_t lane_base = 32 * warp;
   constexpr uint32_t kIdescS = tc::idesc_f16(128, HG, false, false, false, false);
   constexpr uint32_t kIdescO = tc::idesc_f16(128, HG, false, false, true, false);
   int last_issued = -1, waited = -1;
@@ -238,13 +238,6 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
     const int up = (t < a.tiles_main) ? (kMainFp4 ? t : 4 * t + c) : units_main + 4 * (t - a.tiles_main) + c;
     const int u = ph * units_phase + up;
     const int s = u % kStages;
-    const bool first = !fp4_tile || c == 0;
-    if (first) {
-      // keep kStages - 1 units in flight; unit u's copies (this thread's own
-      // row) are complete once at most kStages - 1 newer groups are pending
-      gather(u + kStages - 1);
-      cp_wait<kStages - 1>();
-    }
 
     if (ph == 1 && n == n_chunks) {
       // ---------------- softmax over all rows (phase A complete)
@@ -254,76 +247,77 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
       if (!ok) atomicExch(&abort_flag, 1);
       tc::fence_after_sync();
       const float sc2 = a.scale * kLog2e;
-      float m[HG];
+      float m[CPT];
 #pragma unroll
-      for (int h = 0; h < HG; ++h) m[h] = -INFINITY;
+      for (int j = 0; j < CPT; ++j) m[j] = -INFINITY;
       for (int tt = 0; tt < n_tiles; ++tt) {
         const bool valid = src[tt * 128 + r] != -1;
+        uint32_t v[CPT];
+        tc::tmem_ld_n<CPT>(tc::taddr(tb, lane_base, tt * HG + p * CPT), v);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int h0 = 0; h0 < HG; h0 += 16) {
-          uint32_t v[16];
-          tc::tmem_ld16(tc::taddr(tb, lane_base, tt * HG + h0), v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (valid) m[h0 + j] = fmaxf(m[h0 + j], __uint_as_float(v[j]) * sc2);
-        }
+        for (int j = 0; j < CPT; ++j)
+          if (valid) m[j] = fmaxf(m[j], __uint_as_float(v[j]) * sc2);
       }
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
+      for (int j = 0; j < CPT; ++j) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], o));
+        for (int o = 16; o > 0; o >>= 1) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], o));
       }
       if (lane == 0)
 #pragma unroll
-        for (int h = 0; h < HG; ++h) red[warp][h] = m[h];
-      named_sync();
-      if (r < HG) m_s[r] = fmaxf(fmaxf(red[0][r], red[1][r]), fmaxf(red[2][r], red[3][r]));
-      named_sync();
-      float sum[HG];
+        for (int j = 0; j < CPT; ++j) red[quad][p * CPT + j] = m[j];
+      __syncthreads();
+      if (tid < HG) m_s[tid] = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
+      __syncthreads();
+      float sum[CPT];
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        m[h] = m_s[h];
-        sum[h] = 0.0f;
+      for (int j = 0; j < CPT; ++j) {
+        m[j] = m_s[p * CPT + j];
+        sum[j] = 0.0f;
       }
       for (int tt = 0; tt < n_tiles; ++tt) {
         const bool valid = src[tt * 128 + r] != -1;
         const int row = tt * 128 + r;
+        uint32_t v[CPT];
+        tc::tmem_ld_n<CPT>(tc::taddr(tb, lane_base, tt * HG + p * CPT), v);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int h0 = 0; h0 < HG; h0 += 16) {
-          uint32_t v[16];
-          tc::tmem_ld16(tc::taddr(tb, lane_base, tt * HG + h0), v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int h = h0 + j;
-            float p = 0.0f;
-            if (valid && m[h] != -INFINITY) p = exp2f(__uint_as_float(v[j]) * sc2 - m[h]);
-            sum[h] += p;
-            *reinterpret_cast<__half*>(qp + tc::kmajor_off(h, row, nslot)) = __float2half_rn(p);
-          }
+        for (int j = 0; j < CPT; ++j) {
+          float pr = 0.0f;
+          if (valid && m[j] != -INFINITY) pr = exp2f(__uint_as_float(v[j]) * sc2 - m[j]);
+          sum[j] += pr;
+          *reinterpret_cast<__half*>(qp + tc::kmajor_off(p * CPT + j, row, nslot)) = __float2half_rn(pr);
         }
       }
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
+      for (int j = 0; j < CPT; ++j) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], o);
+        for (int o = 16; o > 0; o >>= 1) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], o);
       }
+      __syncthreads();  // everyone has read red (maxima) before it is reused
       if (lane == 0)
 #pragma unroll
-        for (int h = 0; h < HG; ++h) red[warp][h] = sum[h];
-      named_sync();
-      if (r < HG) {
-        const float tot = red[0][r] + red[1][r] + red[2][r] + red[3][r];
-        inv_s[r] = tot > 0.0f ? 1.0f / tot : 0.0f;
+        for (int j = 0; j < CPT; ++j) red[quad][p * CPT + j] = sum[j];
+      __syncthreads();
+      if (tid < HG) {
+        const float tot = red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
+        inv_s[tid] = tot > 0.0f ? 1.0f / tot : 0.0f;
         if (a.lse)
-          a.lse[(int64_t)qi * kHeads + hg * HG + r] =
-              tot > 0.0f ? (m_s[r] + log2f(tot)) * 0.6931471805599453f : -INFINITY;
+          a.lse[(int64_t)qi * kHeads + hg * HG + tid] =
+              tot > 0.0f ? (m_s[tid] + log2f(tot)) * 0.6931471805599453f : -INFINITY;
       }
       tc::fence_async_smem();
     }
 
-    // ---------------- decode row chunk (t, c) into C tile n % 2
+    if (!fp4_tile || c == 0) {
+      // unit u: this thread's copies done, then everyone's (barrier); the
+      // barrier also frees the slot of unit u - 1 for the next refill
+      cp_wait<kStages - 2>();
+      __syncthreads();
+      gather(u + kStages - 1);
+    }
+    // ---------------- decode quarter p of row chunk (t, c) into C tile n % 2
     if (n >= 2) {  // the MMAs that read this C tile two chunks ago must be done
       const int e = n - 2;
       if (e > waited) {
@@ -335,31 +329,27 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
       uint8_t* ct = ctile + (n & 1) * kCBytes;
       const uint8_t* slot = stage + s * kStageBytes;
       const int32_t sidx = src[t * 128 + r];
-      uint32_t av[64];
+      uint32_t av[16];
       if (sidx == -1) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) av[j] = 0u;
+        for (int j = 0; j < 16; ++j) av[j] = 0u;
       } else if (fp4_tile) {
         const uint8_t* row = slot + r * kStageRow;
-        const uint2 scw = *reinterpret_cast<const uint2*>(row + 256 + 8 * c);
+        const uint32_t sc2b = *reinterpret_cast<const uint16_t*>(row + 256 + 8 * c + 2 * p);  // groups 2p, 2p+1
+        const uint4 cw = *reinterpret_cast<const uint4*>(row + 64 * c + 16 * p);
+        const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+        const uint32_t s_lo = f16x2_scale(sc2b & 0xFFu), s_hi = f16x2_scale(sc2b >> 8);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 cw = *reinterpret_cast<const uint4*>(row + 64 * c + 16 * q4);
-          const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+        for (int q = 0; q < 4; ++q) {
+          uint32_t h4[4];
+          e2m1x8_to_f16x2(w4[q], h4);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int g = 2 * q4 + (q >> 1);  // 16-channel group within the chunk
-            const uint32_t s2 = f16x2_scale(((g < 4 ? scw.x : scw.y) >> (8 * (g & 3))) & 0xFFu);
-            uint32_t h4[4];
-            e2m1x8_to_f16x2(w4[q], h4);
-#pragma unroll
-            for (int by = 0; by < 4; ++by) av[16 * q4 + 4 * q + by] = hmul2(h4[by], s2);
-          }
+          for (int by = 0; by < 4; ++by) av[4 * q + by] = hmul2(h4[by], q < 2 ? s_lo : s_hi);
         }
       } else {
-        const uint8_t* row = slot + r * kStageRowChunk;
+        const uint8_t* row = slot + r * kStageRowChunk + 64 * p;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 4; ++j) {
           const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * j);
           av[4 * j] = bf16x2_to_f16x2(v.x);
           av[4 * j + 1] = bf16x2_to_f16x2(v.y);
@@ -368,13 +358,13 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
         }
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 8 * j, 128)) =
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 32 * p + 8 * j, 128)) =
             make_uint4(av[4 * j], av[4 * j + 1], av[4 * j + 2], av[4 * j + 3]);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
-    named_sync();
+    __syncthreads();
     tc::fence_after_sync();
     if (*reinterpret_cast<volatile int*>(&abort_flag)) {
       aborted = true;
@@ -408,32 +398,26 @@ __global__ void __launch_bounds__(kThreads) attend_tc_kernel(AttArgs a) {
   cp_wait<0>();  // no copies into this CTA's shared memory outlive it
   if (last_issued > waited) {
     const bool ok = tc::mbar_wait(&cdone[last_issued & 1], (last_issued >> 1) & 1, kSpin);
-    if (!ok) {
-      report(a.status, CSA2_ERR_TIMEOUT);
-      aborted = true;
-    }
+    if (!ok) aborted = true;
   }
   tc::fence_after_sync();
   if (!aborted) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
+      uint32_t v[CPT];
+      tc::tmem_ld_n<CPT>(tc::taddr(tb, lane_base, c * HG + p * CPT), v);
+      tc::tmem_wait_ld();
 #pragma unroll
-      for (int h0 = 0; h0 < HG; h0 += 16) {
-        uint32_t v[16];
-        tc::tmem_ld16(tc::taddr(tb, lane_base, c * HG + h0), v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int h = h0 + j;
-          a.out[((int64_t)qi * kHeads + hg * HG + h) * kDim + c * 128 + r] = __uint_as_float(v[j]) * inv_s[h];
-        }
+      for (int j = 0; j < CPT; ++j) {
+        const int h = p * CPT + j;
+        a.out[((int64_t)qi * kHeads + hg * HG + h) * kDim + c * 128 + r] = __uint_as_float(v[j]) * inv_s[h];
       }
     }
-  } else if (r == 0) {
+  } else if (tid == 0) {
     report(a.status, CSA2_ERR_TIMEOUT);
   }
   tc::fence_before_sync();
-  named_sync();
+  __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, tmem_cols);
 }
 

@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
   __shared__ float kpart[8][kIdxDim];  // projection partial sums, 8 row slices
   const int m = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
   const int64_t j = pos0[b] / r + m;
+  // both block-table lookups early, off the critical path of the projection
+  const int64_t page = page_of(mc, b, j, status);
+  const int64_t ipage = page_of(ic, b, j, status);
 
   // merge: thread t owns channels 2t and 2t+1
   float v0 = 0.0f, v1 = 0.0f;
@@ -52,7 +55,6 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
     v1 = fmaf(a, s, bb * c);
   }
 
-  const int64_t page = page_of(mc, b, j, status);
   const int slot = (int)(j % kPage);
   if (kDtype == CSA2_CACHE_FP4) {
     float amax = fmaxf(fabsf(v0), fabsf(v1));
@@ -83,16 +85,19 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
   // reading whole 256-byte rows); the 8 slice sums are added in slice order.
   {
     const int kg = t & 31, rs = t >> 5;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const uint2* w2 = reinterpret_cast<const uint2*>(w_idx) + kg;  // row c at + c * 32
-#pragma unroll 16
-    for (int c = rs * 64; c < rs * 64 + 64; ++c) {
-      const uint2 wv = __ldg(w2 + c * (kIdxDim / 4));
-      const float e = e_s[c];
-      acc[0] = fmaf(e, __uint_as_float(wv.x << 16), acc[0]);
-      acc[1] = fmaf(e, __uint_as_float(wv.x & 0xFFFF0000u), acc[1]);
-      acc[2] = fmaf(e, __uint_as_float(wv.y << 16), acc[2]);
-      acc[3] = fmaf(e, __uint_as_float(wv.y & 0xFFFF0000u), acc[3]);
+    // all 64 row loads are issued before the first use (independent requests)
+    uint2 wv[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) wv[i] = __ldg(w2 + (rs * 64 + i) * (kIdxDim / 4));
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float e = e_s[rs * 64 + i];
+      acc[0] = fmaf(e, __uint_as_float(wv[i].x << 16), acc[0]);
+      acc[1] = fmaf(e, __uint_as_float(wv[i].x & 0xFFFF0000u), acc[1]);
+      acc[2] = fmaf(e, __uint_as_float(wv[i].y << 16), acc[2]);
+      acc[3] = fmaf(e, __uint_as_float(wv[i].y & 0xFFFF0000u), acc[3]);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) kpart[rs][4 * kg + q] = acc[q];
@@ -102,7 +107,6 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
     float kv = kpart[0][t];
 #pragma unroll
     for (int q = 1; q < 8; ++q) kv += kpart[q][t];
-    const int64_t ipage = page_of(ic, b, j, status);
     if (kDtype == CSA2_CACHE_FP4) {
       float amax = fabsf(kv);
 #pragma unroll

@@ -198,7 +198,13 @@ __device__ void block_select(const float* vals, int64_t n, int k, int64_t forced
       __syncthreads();
       for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
         uint32_t kk = key_at(p);
-        if (kk != 0u && (kk & pmask) == prefix) atomicAdd(&hist[(kk >> sh) & dmask], 1u);
+        const bool in = kk != 0u && (kk & pmask) == prefix;
+        // keys crowd into few digits: one shared-memory atomic per distinct
+        // digit per warp instead of one per key
+        const uint32_t d = in ? ((kk >> sh) & dmask) : 0xFFFFFFFFu;
+        const uint32_t active = __activemask();
+        const uint32_t peers = __match_any_sync(active, d);
+        if (in && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[d], (uint32_t)__popc(peers));
       }
       __syncthreads();
       if (threadIdx.x < 32) {

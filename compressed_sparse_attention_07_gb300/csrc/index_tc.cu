@@ -109,12 +109,20 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
   const int n_my = (int)(t_end - t_begin);
 
   // ---- set-up: Q_idx (f16 or bf16) into the B tile, head weights, barriers, TMEM
-  for (int i = tid; i < kN * kIdxDim; i += kThreads) {
-    const int row = i / kIdxDim, k = i % kIdxDim;  // row = q*32 + h
-    const uint16_t v = __ldg(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim + (row % kIdxHeads) * kIdxDim + k);
-    uint16_t o = v;
-    if (!kBf16) o = __half_as_ushort(__float2half_rn(bf16_bits_to_float(v)));
-    *reinterpret_cast<uint16_t*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = o;
+  for (int i = tid; i < kN * kIdxDim / 8; i += kThreads) {
+    const int row = (8 * i) / kIdxDim, k = (8 * i) % kIdxDim;  // row = q*32 + h; 8 channels per load
+    uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
+                                                   (row % kIdxHeads) * kIdxDim + k));
+    if (!kBf16) {
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+        w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = v;
   }
   for (int i = tid; i < QPC * kIdxHeads; i += kThreads)
     hw[i / kIdxHeads][i % kIdxHeads] = a.head_w ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;

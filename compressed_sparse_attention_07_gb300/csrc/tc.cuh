@@ -107,6 +107,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t a, uint32_t (&r)[16]) {
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(a));
 }
+__device__ __forceinline__ void tmem_ld8(uint32_t a, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(a));
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t a, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+// n (4, 8 or 16) consecutive columns of this warp's 32 lanes.
+template <int n>
+__device__ __forceinline__ void tmem_ld_n(uint32_t a, uint32_t (&r)[n]) {
+  if constexpr (n == 16) tmem_ld16(a, r);
+  else if constexpr (n == 8) tmem_ld8(a, r);
+  else tmem_ld4(a, r);
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st16(uint32_t a, const uint32_t (&r)[16]) {

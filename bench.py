@@ -50,11 +50,12 @@ def attend_query_bytes(cache, topk=512, window=128):
 
 
 def peaks():
+    """(HBM GB/s, sustained bf16 TFLOP/s, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
-    return 6800.0, 1900.0, "fallback"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1700.0, "fallback"
 
 
 # ------------------------------------------------------------------ clocks ----
@@ -105,36 +106,66 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workload ----
 
-class DecodeStep:
-    """One decode step of one CSA2 layer in Full mode: compress the step's
-    r new tokens per sequence (one entry), index the whole visible cache
-    (plus the HSI pool on the decoder Full layer), attend over top-k and the
-    window.  The cache prefix holds seeded random FP4 bytes (or N(0,1) bf16)."""
+def _dev(a, device):
+    import torch
+    a = np.ascontiguousarray(a)
+    return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(device)
+
+
+def _fill_cache(c, cd, g, device):
+    """Seeded random cache contents: uniform FP4 codes with E4M3 scales in
+    0x20..0x3C, or N(0,1) bf16 values (same distribution as the tests)."""
+    import torch
+    import compressed_sparse_attention_07_gb300 as csa
+    if cd == csa.CACHE_FP4:
+        c.data.random_(0, 256, generator=g)
+        c.scales.random_(0x20, 0x3D, generator=g)
+    else:
+        v = torch.randn(c.data.numel() // 2, generator=g, device=device, dtype=torch.float32)
+        c.data.view(torch.int16).copy_(v.to(torch.bfloat16).view(torch.int16).view(c.data.shape[0], -1))
+
+
+class StepBase:
+    """Common pieces: config, caches with a seeded random prefix, step inputs
+    on the device and as host arrays (for the end-to-end leg)."""
 
     def __init__(self, wl: synth.Workload, device, seed_offset=0):
         import torch
         import compressed_sparse_attention_07_gb300 as csa
-        self.torch, self.csa, self.wl = torch, csa, wl
-        B, r = wl.batch, wl.ratio
-        self.B = B
-        self.N = wl.ctx // r
-        cd = csa.CACHE_FP4 if wl.cache == "fp4" else csa.CACHE_BF16
-        self.cfg = csa.Cfg(ratio=r, cache_dtype=cd, topk=wl.topk, window=wl.window,
+        self.torch, self.csa, self.wl, self.device = torch, csa, wl, device
+        self.cd = csa.CACHE_FP4 if wl.cache == "fp4" else csa.CACHE_BF16
+        self.cfg = csa.Cfg(ratio=wl.ratio, cache_dtype=self.cd, topk=wl.topk, window=wl.window,
                            hsi_blocks=wl.hsi_blocks if wl.hsi else 0, rope_theta=wl.theta)
-        seed = wl.seed + seed_offset
-        g = torch.Generator(device=device)
-        g.manual_seed(seed)
-        self.main = csa.PagedCache(B, self.N, 512, cd, device=device)
-        self.idx = csa.PagedCache(B, self.N, 128, cd, device=device)
+        self.seed = wl.seed + seed_offset
+        self.B = wl.batch
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def make_caches(self, capacity):
+        g = self.torch.Generator(device=self.device)
+        g.manual_seed(self.seed)
+        self.main = self.csa.PagedCache(self.B, capacity, 512, self.cd, device=self.device)
+        self.idx = self.csa.PagedCache(self.B, capacity, 128, self.cd, device=self.device)
         for c in (self.main, self.idx):
-            if cd == csa.CACHE_FP4:
-                c.data.random_(0, 256, generator=g)
-                c.scales.random_(0x20, 0x3D, generator=g)
-            else:
-                v = torch.randn(c.data.numel() // 2, generator=g, device=device, dtype=torch.float32)
-                c.data.view(torch.int16).copy_(v.to(torch.bfloat16).view(torch.int16).view(c.data.shape[0], -1))
+            _fill_cache(c, self.cd, g, self.device)
+
+    def upload(self):
+        self.d = {k: _dev(v, self.device) for k, v in self.h.items()}
+
+    def inputs_host(self):
+        return self.h
+
+
+class DecodeStep(StepBase):
+    """One decode step of one CSA2 layer in Full mode: compress the step's r
+    new tokens per sequence (one entry), index the whole visible cache (plus
+    the HSI pool on the decoder Full layer), attend over top-k and window."""
+
+    def __init__(self, wl, device, seed_offset=0):
+        super().__init__(wl, device, seed_offset)
+        torch, csa, B, r, s = self.torch, self.csa, self.B, wl.ratio, self.seed
+        self.N = wl.ctx // r
+        self.make_caches(self.N)
         ctx = wl.ctx
-        s = seed
         self.h = {
             "x": synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512)),
             "pos0": np.full(B, ctx - r, np.int64),
@@ -145,17 +176,14 @@ class DecodeStep:
             "swa_pos0": np.full(B, ctx - wl.window, np.int64),
             "q_pos": np.full((B, 1), ctx - 1, np.int64),
         }
-        self.merge_w = torch.from_numpy(synth.merge_weights(synth.rng(s, "w"), r, 512)).to(device)
-        self.w_idx = torch.from_numpy(synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512)).view(
-            np.int16)).to(device)
-        self.d = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)).to(device)
-                  for k, v in self.h.items()}
+        self.upload()
+        self.merge_w = _dev(synth.merge_weights(synth.rng(s, "w"), r, 512), device)
+        self.w_idx = _dev(synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512)), device)
         self.n_entries = torch.full((B,), self.N - 1, dtype=torch.int32, device=device)
         self.topk = torch.empty((B, 1, wl.topk), dtype=torch.int32, device=device)
         self.pool = torch.empty((B, 1, wl.hsi_blocks), dtype=torch.int32, device=device) if wl.hsi else None
         self.ws = torch.empty(csa.index_workspace_bytes(self.cfg, B, 1, self.N), dtype=torch.uint8, device=device)
         self.out = torch.empty((B, 1, 64, 512), dtype=torch.float32, device=device)
-        self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.stages = ["compress", "index_topk", "attend"]
         self.launches_per_step = 4  # compress, score, select, attend
         eb = IDX_ENTRY_BYTES[wl.cache]
@@ -165,9 +193,7 @@ class DecodeStep:
         self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_tc_kernel + select_kernel",
                               "attend": "attend_tc_kernel"}
         self.units = B
-
-    def inputs_host(self):
-        return {k: v for k, v in self.h.items()}
+        self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N}
 
     def step(self, events=None, d=None):
         csa, d = self.csa, (d or self.d)
@@ -189,23 +215,149 @@ class DecodeStep:
         return self.out
 
 
+class PrefillStep(StepBase):
+    """One prefill chunk of Tq query tokens appended to a long context: the
+    compressor on the chunk's tokens, causal indexing of every chunk token
+    over the prefix plus the chunk's own entries, attention with the banded
+    window (rows t-W+1..t of the chunk and the prefix tail)."""
+
+    def __init__(self, wl, device, seed_offset=0):
+        super().__init__(wl, device, seed_offset)
+        torch, csa, B, r, s = self.torch, self.csa, self.B, wl.ratio, self.seed
+        Tq, ctx, W = wl.tq, wl.ctx, wl.window
+        self.N = (ctx + Tq) // r
+        self.make_caches(self.N)
+        S = W - 1 + Tq
+        self.h = {
+            "x": synth.normal_bf16(synth.rng(s, "x_chunk"), (B, Tq, 512)),
+            "pos0": np.full(B, ctx, np.int64),
+            "q": synth.normal_bf16(synth.rng(s, "q"), (B, Tq, 64, 512)),
+            "q_idx": synth.normal_bf16(synth.rng(s, "q_idx"), (B, Tq, 32, 128)),
+            "swa": synth.normal_bf16(synth.rng(s, "swa"), (B, S, 512)),
+            "swa_len": np.full(B, S, np.int32),
+            "swa_pos0": np.full(B, ctx - (W - 1), np.int64),
+            "q_pos": np.tile(ctx + np.arange(Tq, dtype=np.int64), (B, 1)),
+        }
+        self.upload()
+        self.merge_w = _dev(synth.merge_weights(synth.rng(s, "w"), r, 512), device)
+        self.w_idx = _dev(synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512)), device)
+        self.n_entries = torch.full((B,), ctx // r, dtype=torch.int32, device=device)
+        self.topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device=device)
+        per_q = csa.index_workspace_bytes(self.cfg, 1, 1, self.N)
+        self.ws = torch.empty(per_q * min(B * Tq, 512), dtype=torch.uint8, device=device)
+        self.out = torch.empty((B, Tq, 64, 512), dtype=torch.float32, device=device)
+        self.stages = ["compress", "index_topk", "attend"]
+        chunks = -(-B * Tq // 512)
+        self.launches_per_step = 1 + 2 * chunks + 1
+        pairs = sum(min((ctx + t - (r - 1)) // r + 1, self.N) for t in range(Tq)) * B
+        self.stage_bytes = {"compress": B * (Tq // r) * (r * 1024 + 360),
+                            "index_topk": B * self.N * IDX_ENTRY_BYTES[wl.cache] + B * Tq * (8192 + 2048),
+                            "attend": B * Tq * attend_query_bytes(wl.cache, wl.topk, wl.window)}
+        self.stage_flops = {"index_topk": pairs * 8192, "attend": B * Tq * 4 * 64 * 512 * (wl.topk + wl.window)}
+        self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_tc_kernel + select_kernel",
+                              "attend": "attend_tc_kernel"}
+        self.units = B * Tq
+        self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "query_tokens": Tq, "entries": self.N,
+                          "index_pairs": pairs}
+
+    step = DecodeStep.step
+
+
+class GroupStep(StepBase):
+    """One decode step through a cross-layer group of decoder layers: layer
+    20 Full (compress the new token, full indexing with the HSI pool), layers
+    24/28/32/36 Reindex over the pool, the other fifteen Reuse; every layer
+    has its own query, indexer query and window rows."""
+
+    def __init__(self, wl, device, seed_offset=0):
+        super().__init__(wl, device, seed_offset)
+        torch, csa, B, r, s = self.torch, self.csa, self.B, wl.ratio, self.seed
+        ctx = wl.ctx
+        self.N = ctx // r
+        self.make_caches(self.N)
+        self.layers = list(wl.layers)
+        self.h = {
+            "x": synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512)),
+            "pos0": np.full(B, ctx - r, np.int64),
+            "swa_len": np.full(B, wl.window, np.int32),
+            "swa_pos0": np.full(B, ctx - wl.window, np.int64),
+            "q_pos": np.full((B, 1), ctx - 1, np.int64),
+        }
+        for layer, mode in self.layers:
+            ls = s * 1000 + layer
+            self.h["q%d" % layer] = synth.normal_bf16(synth.rng(ls, "q"), (B, 1, 64, 512))
+            self.h["swa%d" % layer] = synth.normal_bf16(synth.rng(ls, "swa"), (B, wl.window, 512))
+            if mode != "reuse":
+                self.h["q_idx%d" % layer] = synth.normal_bf16(synth.rng(ls, "q_idx"), (B, 1, 32, 128))
+        self.upload()
+        self.merge_w = _dev(synth.merge_weights(synth.rng(s, "w"), r, 512), device)
+        self.w_idx = _dev(synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512)), device)
+        self.n_entries = torch.full((B,), self.N - 1, dtype=torch.int32, device=device)
+        topk = torch.empty((B, 1, wl.topk), dtype=torch.int32, device=device)
+        pool = torch.empty((B, 1, wl.hsi_blocks), dtype=torch.int32, device=device)
+        ws = torch.empty(max(csa.index_workspace_bytes(self.cfg, B, 1, self.N),
+                             csa.index_workspace_bytes(self.cfg, B, 1, self.N, reindex=True)),
+                         dtype=torch.uint8, device=device)
+        self.state = csa.GroupState(self.main, self.idx, self.n_entries, self.N, topk, pool, ws, self.status)
+        self.outs = {l: torch.empty((B, 1, 64, 512), dtype=torch.float32, device=device) for l, _ in self.layers}
+        self.out = self.outs[self.layers[-1][0]]
+        self.stages = ["L%d_%s" % (l, m) for l, m in self.layers]
+        self.launches_per_step = sum({"full": 4, "reindex": 3, "reuse": 1}[m] for _, m in self.layers)
+        att = B * attend_query_bytes(wl.cache, wl.topk, wl.window)
+        self.stage_bytes = {}
+        for l, m in self.layers:
+            extra = {"full": B * (self.N * 72 + r * 1024 + 360), "reindex": B * wl.hsi_blocks * 8 * 72,
+                     "reuse": 0}[m]
+            self.stage_bytes["L%d_%s" % (l, m)] = att + extra
+        self.stage_kernels = {st: {"full": "compress + score_tc + select + attend_tc",
+                                   "reindex": "score_pool + select + attend_tc", "reuse": "attend_tc"}[st.split("_")[1]]
+                              for st in self.stages}
+        self.units = B
+        self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N, "layers": len(self.layers),
+                          "unit": "query token through the 20-layer group"}
+
+    def step(self, events=None, d=None):
+        csa, d = self.csa, (d or self.d)
+        ev = events or [None] * (len(self.layers) + 1)
+        if ev[0] is not None:
+            ev[0].record()
+        mode_of = {"full": csa.MODE_FULL, "reindex": csa.MODE_REINDEX, "reuse": csa.MODE_REUSE}
+        for i, (l, m) in enumerate(self.layers):
+            kw = {}
+            if m == "full":
+                kw = dict(x=d["x"], pos0=d["pos0"], merge_w=self.merge_w, w_idx=self.w_idx)
+            csa.layer(self.cfg, mode_of[m], self.state, d["q_pos"], d["q%d" % l], d["swa%d" % l], d["swa_len"],
+                      d["swa_pos0"], self.outs[l], q_idx=d.get("q_idx%d" % l), **kw)
+            if ev[i + 1] is not None:
+                ev[i + 1].record()
+        return self.out
+
+
 def make_step(name, device, seed_offset=0):
     wl = synth.WORKLOADS[name]
-    if wl.tq == 1 and not wl.layers:
-        return DecodeStep(wl, device, seed_offset)
-    raise SystemExit("workload %s is not wired into the benchmark yet" % name)
+    if wl.layers:
+        return GroupStep(wl, device, seed_offset)
+    if wl.tq > 1:
+        return PrefillStep(wl, device, seed_offset)
+    return DecodeStep(wl, device, seed_offset)
 
 
 # ------------------------------------------------------------- cpu oracle ----
 
 class OracleStep:
-    """The CPU oracle running the same step (compress the new pair, index,
-    attend) for all B sequences on its own seeded random cache."""
+    """The CPU oracle on a bounded sample of the same workload, with its own
+    seeded random cache: decode -- up to 4 sequences through the step
+    (compress, index, attend); decoder group -- one sequence through all 20
+    layers; prefill -- the chunk's compressor and 4 query rows."""
 
     def __init__(self, wl: synth.Workload):
         import oracle
         self.oracle, self.wl = oracle, wl
-        B, r, N = wl.batch, wl.ratio, wl.ctx // wl.ratio
+        r = wl.ratio
+        self.prefill = wl.tq > 1
+        self.B = 1 if (wl.layers or self.prefill) else min(wl.batch, 4)
+        B = self.B
+        N = (wl.ctx + wl.tq) // r if self.prefill else wl.ctx // r
         self.N = N
         self.main = oracle.Cache(B, N, 512, wl.cache)
         self.idx = oracle.Cache(B, N, 128, wl.cache)
@@ -216,32 +368,69 @@ class OracleStep:
                     c.codes[b], c.scales[b] = synth.fp4_bytes(g, N, c.channels)
             else:
                 c.bf16[:] = synth.normal_bf16(g, c.bf16.shape)
-        s = wl.seed
-        ctx = wl.ctx
-        self.x = synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512))
-        self.pos0 = np.full(B, ctx - r, np.int64)
+        s, ctx = wl.seed, wl.ctx
         self.w = synth.merge_weights(synth.rng(s, "w"), r, 512)
         self.w_idx = synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512))
-        self.q = synth.normal_bf16(synth.rng(s, "q"), (B, 1, 64, 512))
-        self.q_idx = synth.normal_bf16(synth.rng(s, "q_idx"), (B, 1, 32, 128))
-        self.swa = synth.normal_bf16(synth.rng(s, "swa"), (B, wl.window, 512))
-        self.q_pos = np.full((B, 1), ctx - 1, np.int64)
-        self.n_ent = np.full(B, N, np.int32)
-        self.units = B
-        self.cores = min(oracle.threads(), B)
+        if self.prefill:
+            rows = np.array([0, 2047, 2048, wl.tq - 1], np.int64)
+            self.x = synth.normal_bf16(synth.rng(s, "x_chunk"), (1, wl.tq, 512))
+            self.pos0 = np.array([ctx], np.int64)
+            self.q = synth.normal_bf16(synth.rng(s, "q"), (1, wl.tq, 64, 512))[:, rows]
+            self.q_idx = synth.normal_bf16(synth.rng(s, "q_idx"), (1, wl.tq, 32, 128))[:, rows]
+            S = wl.window - 1 + wl.tq
+            self.swa = synth.normal_bf16(synth.rng(s, "swa"), (1, S, 512))
+            self.swa_len, self.swa_pos0 = np.array([S], np.int32), np.array([ctx - wl.window + 1], np.int64)
+            self.q_pos = (ctx + rows).reshape(1, -1)
+            self.n_ent = np.array([N], np.int32)
+            self.units = len(rows)
+            self.sample = "4 query rows (0, 2047, 2048, last) of the %d-token chunk plus its compressor" % wl.tq
+        else:
+            self.x = synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512))
+            self.pos0 = np.full(B, ctx - r, np.int64)
+            self.q_pos = np.full((B, 1), ctx - 1, np.int64)
+            self.swa_len, self.swa_pos0 = np.full(B, wl.window, np.int32), np.full(B, ctx - wl.window, np.int64)
+            self.n_ent = np.full(B, N, np.int32)
+            if wl.layers:
+                self.per_layer = []
+                for layer, mode in wl.layers:
+                    ls = s * 1000 + layer
+                    self.per_layer.append((layer, mode,
+                                           synth.normal_bf16(synth.rng(ls, "q"), (1, 1, 64, 512)),
+                                           synth.normal_bf16(synth.rng(ls, "swa"), (1, wl.window, 512)),
+                                           synth.normal_bf16(synth.rng(ls, "q_idx"), (1, 1, 32, 128))))
+                self.units = 1
+                self.sample = "1 sequence through the %d-layer group" % len(wl.layers)
+            else:
+                self.q = synth.normal_bf16(synth.rng(s, "q"), (B, 1, 64, 512))
+                self.q_idx = synth.normal_bf16(synth.rng(s, "q_idx"), (B, 1, 32, 128))
+                self.swa = synth.normal_bf16(synth.rng(s, "swa"), (B, wl.window, 512))
+                self.units = B
+                self.sample = "%d sequences of the step (compress + index over %d entries + attend)" % (B, N)
+        self.cores = min(oracle.threads(), max(self.units, 1))
 
     def step(self):
         o, wl = self.oracle, self.wl
+        sc = 1 / math.sqrt(512)
         o.compress(self.x, self.pos0, self.w, self.w_idx, self.main, self.idx, wl.ratio, wl.theta)
-        topk, pool, _ = o.index_topk(self.idx, self.n_ent, self.q_idx, self.q_pos, wl.ratio, wl.topk,
-                                     hsi_blocks=wl.hsi_blocks if wl.hsi else 0, want_pool=wl.hsi)
-        return o.attend(self.main, self.n_ent, self.q, topk, self.swa, np.full(wl.batch, wl.window, np.int32),
-                        np.full(wl.batch, wl.ctx - wl.window, np.int64), self.q_pos, wl.window, 1 / math.sqrt(512))
+        if self.prefill or not wl.layers:
+            topk, _, _ = o.index_topk(self.idx, self.n_ent, self.q_idx, self.q_pos, wl.ratio, wl.topk,
+                                      hsi_blocks=wl.hsi_blocks if wl.hsi else 0, want_pool=wl.hsi)
+            return o.attend(self.main, self.n_ent, self.q, topk, self.swa, self.swa_len, self.swa_pos0, self.q_pos,
+                            wl.window, sc)
+        topk = pool = None
+        for layer, mode, q, swa, q_idx in self.per_layer:
+            if mode == "full":
+                topk, pool, _ = o.index_topk(self.idx, self.n_ent, q_idx, self.q_pos, wl.ratio, wl.topk,
+                                             hsi_blocks=wl.hsi_blocks, want_pool=True)
+            elif mode == "reindex":
+                topk, _, _ = o.index_topk(self.idx, self.n_ent, q_idx, self.q_pos, wl.ratio, wl.topk,
+                                          hsi_blocks=wl.hsi_blocks, pool=pool)
+            out = o.attend(self.main, self.n_ent, q, topk, swa, self.swa_len, self.swa_pos0, self.q_pos, wl.window, sc)
+        return out
 
 
 def cpu_baseline(wl, seconds: float):
     st = OracleStep(wl)
-    st.step()  # warm
     t0 = time.perf_counter()
     n = 0
     while True:
@@ -251,8 +440,7 @@ def cpu_baseline(wl, seconds: float):
             break
     dt = time.perf_counter() - t0
     return {"value": n * st.units / dt, "unit": UNIT, "cores": st.cores, "kind": "oracle",
-            "sample": "%d full steps of %s (%d query tokens each: compress + index over %d entries + attend), "
-                      "fp64 C oracle, OpenMP over query tokens" % (n, wl.name, st.units, st.N)}
+            "sample": "%d runs of %s: %s; fp64 C oracle, OpenMP over query tokens" % (n, wl.name, st.sample)}
 
 
 # -------------------------------------------------------------------- main ----
@@ -304,7 +492,7 @@ def run_reference(args, ws, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name}, "impl": "reference",
             "cpu_baseline": {"value": v, "unit": UNIT, "kind": "oracle", "cores": st.cores,
-                             "sample": "%d full steps of %s on the host cores" % (args.steps, wl.name)},
+                             "sample": "%d runs of %s: %s" % (args.steps, wl.name, st.sample)},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -383,24 +571,35 @@ def main():
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), ws) / e2e_steps
     assert int(step.status.item()) == 0
 
-    hbm, tflops, src = peaks()
+    hbm, tflops_sus, src = peaks()
     dom = max(stage_ms, key=stage_ms.get)
-    ach = step.stage_bytes[dom] / (stage_ms[dom] / 1e3) / 1e9
-    roof = {"bound": "hbm", "kernel": step.stage_kernels[dom], "achieved": ach, "peak": hbm, "unit": "GB/s",
-            "frac": ach / hbm, "traffic": None,
-            "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "of fallback",
-            "algorithmic_bytes_per_launch": step.stage_bytes[dom], "launch_ms": stage_ms[dom]}
+    flops = getattr(step, "stage_flops", {}).get(dom)
+    if flops is not None:
+        # prefill contractions: against the tensor-core peak (f16 operands have
+        # the bf16 rate; the sustained figure, the kernel runs inside a long step)
+        ach = flops / (stage_ms[dom] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": step.stage_kernels[dom], "achieved": ach, "peak": tflops_sus,
+                "unit": "TFLOP/s", "frac": ach / tflops_sus, "traffic": None,
+                "peak_source": ("of measured (MEASURED_PEAKS.json bf16_tflops_sustained, f16 = bf16 rate)"
+                                if src == "measured" else "of fallback"),
+                "algorithmic_flops_per_launch": flops, "launch_ms": stage_ms[dom]}
+    else:
+        ach = step.stage_bytes[dom] / (stage_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": step.stage_kernels[dom], "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "traffic": None,
+                "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "of fallback",
+                "algorithmic_bytes_per_launch": step.stage_bytes[dom], "launch_ms": stage_ms[dom]}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(step.wl, args.cpu_seconds)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": step.wl.name, "batch_per_gpu": step.B, "ctx": step.wl.ctx,
-                           "entries": step.N, "cache": step.wl.cache, "topk": step.wl.topk,
-                           "window": step.wl.window, "hsi": step.wl.hsi,
-                           "l2": "flushed before every step (256 MiB write)"},
+                "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+                "config": dict({"workload": step.wl.name}, **step.cfg_extra,
+                               **{"cache": step.wl.cache, "topk": step.wl.topk, "window": step.wl.window,
+                                  "hsi": step.wl.hsi, "operands": "f16 tensor-core operands, fp32 accumulate",
+                                  "l2": "flushed before every step (256 MiB write)"}),
                 "stage_ms": stage_ms, "wall_s": wall,
                 "roofline": roof, "cpu_baseline": cpu,
                 "e2e": {"value": ws * step.units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -175,55 +175,77 @@ __device__ void block_select(const float* vals, int64_t n, int k, int64_t forced
   auto gkey = [&](int64_t p) -> uint32_t { return p == forced ? 0xFFFFFFFFu : order_key(vals[p]); };
   auto key_at = [&](int64_t p) -> uint32_t { return skeys ? skeys[p] : gkey(p); };
 
-  // count valid candidates (and stage the keys)
-  uint32_t cnt = 0;
+  // count valid candidates (and stage the keys); range of the valid keys
+  __shared__ uint32_t sh_min[32], sh_max[32];
+  uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
     const uint32_t kk = gkey(p);
     if (skeys) skeys[p] = kk;
-    cnt += kk != 0u;
+    if (kk != 0u) {
+      ++cnt;
+      kmin = min(kmin, kk);
+      kmax = max(kmax, kk);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    sh_min[threadIdx.x >> 5] = kmin;
+    sh_max[threadIdx.x >> 5] = kmax;
   }
   uint32_t nvalid;
-  block_exclusive_scan(cnt, warp_sums, nvalid);
+  block_exclusive_scan(cnt, warp_sums, nvalid);  // (its barriers also publish sh_min / sh_max)
+  kmin = sh_min[0];
+  kmax = sh_max[0];
+  for (int w = 1; w < kSelThreads / 32; ++w) {
+    kmin = min(kmin, sh_min[w]);
+    kmax = max(kmax, sh_max[w]);
+  }
 
   uint32_t T = 0, krem = 0;  // select key > T, plus the first krem keys == T
   if (nvalid > (uint32_t)k) {
-    uint32_t prefix = 0, pmask = 0;
+    // Radix select on x = key - kmin, from the top significant bit of the
+    // range down, at most 11 bits per pass: binning relative to the range
+    // spreads the keys over the bins even when they share their top bits.
+    const uint32_t range = kmax - kmin;
+    const int nbits = range ? 32 - __clz(range) : 0;
+    uint32_t prefix = 0;  // the fixed top bits of x
+    int fixed = 0;
     krem = (uint32_t)k;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int sh = shifts[pass];
-      const uint32_t dmask = (1u << widths[pass]) - 1u;
+    while (fixed < nbits) {
+      const int w = min(11, nbits - fixed);
+      const int sh = nbits - fixed - w;
+      const uint32_t dmask = (1u << w) - 1u;
       for (int i = threadIdx.x; i < 2048; i += kSelThreads) hist[i] = 0;
       __syncthreads();
       for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
-        uint32_t kk = key_at(p);
-        const bool in = kk != 0u && (kk & pmask) == prefix;
-        // keys crowd into few digits: one shared-memory atomic per distinct
-        // digit per warp instead of one per key
-        const uint32_t d = in ? ((kk >> sh) & dmask) : 0xFFFFFFFFu;
-        const uint32_t active = __activemask();
-        const uint32_t peers = __match_any_sync(active, d);
-        if (in && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+        const uint32_t kk = key_at(p);
+        if (kk == 0u) continue;
+        const uint32_t x = kk - kmin;
+        const uint32_t top = (sh + w >= 32) ? 0u : (x >> (sh + w));
+        if (top == prefix) atomicAdd(&hist[(x >> sh) & dmask], 1u);
       }
       __syncthreads();
       if (threadIdx.x < 32) {
         // lane L owns bins [2048 - 64(L+1), 2048 - 64L): scan from the top
         const int lane = threadIdx.x;
-        uint32_t s = 0;
-        for (int i = 0; i < 64; ++i) s += hist[2047 - 64 * lane - i];
-        uint32_t incl = s;
+        uint32_t sacc = 0;
+        for (int i = 0; i < 64; ++i) sacc += hist[2047 - 64 * lane - i];
+        uint32_t incl = sacc;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        uint32_t excl = incl - s;  // keys in higher bins than this lane's chunk
-        const uint32_t kr = (pass == 0) ? (uint32_t)k : sh_krem;
+        const uint32_t excl = incl - sacc;  // keys in higher bins than this lane's chunk
+        const uint32_t kr = (fixed == 0) ? (uint32_t)k : sh_krem;
         if (excl < kr && incl >= kr) {
           uint32_t above = excl;
           for (int i = 0; i < 64; ++i) {
-            int d = 2047 - 64 * lane - i;
+            const int d = 2047 - 64 * lane - i;
             if (above + hist[d] >= kr) {
               sh_digit = (uint32_t)d;
               sh_krem = kr - above;
@@ -234,12 +256,12 @@ __device__ void block_select(const float* vals, int64_t n, int k, int64_t forced
         }
       }
       __syncthreads();
-      prefix |= sh_digit << sh;
-      pmask |= dmask << sh;
+      prefix = (prefix << w) | sh_digit;
+      fixed += w;
+      krem = sh_krem;
       __syncthreads();
     }
-    T = prefix;
-    krem = sh_krem;
+    T = kmin + prefix;
   }
 
   // ordered compaction: thread t scans the contiguous segment [t*seg, (t+1)*seg)

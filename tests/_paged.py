@@ -91,3 +91,28 @@ def cache_pair(B, capacity, channels, dtype: str, seed: int):
     mp = -(-capacity // PAGE)
     order = page_order(seed, B * mp + 3)[: B * mp]
     return csa.PagedCache(B, capacity, channels, cd, page_order=order, spare_pages=3)
+
+
+def upload_seq(cache: csa.PagedCache, b: int, ocache, ob: int = 0) -> None:
+    """Copy sequence ob of an oracle.Cache into sequence b of the paged cache."""
+    mp = cache.max_pages
+    C_ = cache.channels
+    n = ocache.n_cap
+    one = type(ocache)(1, cache.capacity, C_, ocache.dtype)
+    if ocache.dtype == "fp4":
+        one.codes[0, :n], one.scales[0, :n] = ocache.codes[ob], ocache.scales[ob]
+    else:
+        one.bf16[0, :n] = ocache.bf16[ob]
+    view = csa.PagedCache.__new__(csa.PagedCache)
+    view.batch, view.channels, view.cache_dtype = 1, C_, cache.cache_dtype
+    view.max_pages, view.capacity, view.num_pages = mp, cache.capacity, cache.num_pages
+    view.data, view.scales = cache.data, cache.scales
+    view.block_table = cache.block_table[b:b + 1]
+    if ocache.dtype == "fp4":
+        d, s = _page_bytes(view, one.codes, one.scales)
+    else:
+        d, s = _page_bytes(view, one.bf16, None)
+    bt = view.block_table.flatten().long()
+    cache.data[bt] = torch.from_numpy(np.ascontiguousarray(d)).to(cache.data.device)
+    if s is not None:
+        cache.scales[bt] = torch.from_numpy(np.ascontiguousarray(s)).to(cache.data.device)

@@ -23,6 +23,7 @@ NEAR_TIE = 1e-5
 ATT_TOL = 2e-2
 
 _E4 = np.array([oracle.e4m3_value(c) for c in range(127)])
+_E4_ALL = np.array([oracle.e4m3_value(c) for c in range(256)])  # byte -> value (NaN for 0x7F / 0xFF)
 _SCALE_T = 3.0 * (_E4[:-1] + _E4[1:])  # 6 * midpoints, increasing
 _E2M1_MID = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
 
@@ -43,7 +44,7 @@ def fp4_code_mismatches(gpu_codes, gpu_scales, ora_codes, ora_scales, pre, mag, 
         return np.stack([lo, hi], -1).reshape(lead + (C,))
 
     gc, oc = nib(gpu_codes), nib(ora_codes)
-    s = np.vectorize(oracle.e4m3_value)(ora_scales.astype(int)) if ora_scales.size else ora_scales
+    s = _E4_ALL[ora_scales.astype(np.int64)]
     s_el = np.repeat(s, 16, axis=-1)
     near_code = (np.abs(np.abs(pre)[..., None] - s_el[..., None] * _E2M1_MID) <= (margin * mag)[..., None]).any(-1)
     near_code |= np.repeat(near_scale, 16, axis=-1)

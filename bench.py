@@ -243,6 +243,7 @@ class PrefillStep(StepBase):
         self.w_idx = _dev(synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512)), device)
         self.n_entries = torch.full((B,), ctx // r, dtype=torch.int32, device=device)
         self.topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device=device)
+        self.pool = None
         per_q = csa.index_workspace_bytes(self.cfg, 1, 1, self.N)
         self.ws = torch.empty(per_q * min(B * Tq, 512), dtype=torch.uint8, device=device)
         self.out = torch.empty((B, Tq, 64, 512), dtype=torch.float32, device=device)

@@ -57,14 +57,17 @@ def fp4_code_mismatches(gpu_codes, gpu_scales, ora_codes, ora_scales, pre, mag, 
 
 
 def bf16_mismatches(gpu_vals, ora_vals, pre, mag, margin):
+    """A bf16 code is excused when the GPU value is the rounding of some value
+    within the fp32 evaluation bound of the oracle's pre-rounding value:
+    |g - pre| <= margin * M + ulp(g) (covers sign flips of values that cancel
+    to near zero)."""
     g = (gpu_vals.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    o = (ora_vals.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     diff = gpu_vals != ora_vals
-    mid = (g + o) / 2
-    near = np.abs(pre - mid) <= margin * mag
-    one_ulp = np.abs(gpu_vals.astype(np.int64) - ora_vals.astype(np.int64)) <= 1
-    unexcused = int((diff & ~(near & one_ulp)).sum())
-    excused = int((diff & near & one_ulp).sum())
+    ulp = np.ldexp(1.0, np.frexp(np.abs(g))[1] - 8)
+    ulp = np.maximum(ulp, np.ldexp(1.0, -133))
+    near = np.abs(g - pre) <= margin * mag + ulp
+    unexcused = int((diff & ~near).sum())
+    excused = int((diff & near).sum())
     return unexcused, excused, diff.any(-1)
 
 

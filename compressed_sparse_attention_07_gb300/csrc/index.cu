@@ -11,8 +11,9 @@ namespace {
 
 constexpr int kScoreThreads = 128;  // one entry per thread
 constexpr int kSelThreads = 1024;   // one CTA selects for one query
-constexpr uint32_t kInvalid = 0xFFFFFFFFu;  // score bit pattern of a non-candidate
-constexpr int64_t kSelSmemKeys = 48 * 1024;  // keys held in shared memory (192 KB)
+constexpr uint32_t kInvalid = kScoreInvalid;
+constexpr int kHistBins = 8192;    // linear bins over a query's key range
+constexpr int kCandMax = 16384;    // candidates sorted in shared memory
 
 // Decoded indexer-K entry (128 channels) of sequence b, slot j, into registers.
 template <int kDtype>
@@ -94,7 +95,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_pool_kernel(int q0, int T
                                                                    const int64_t* __restrict__ q_pos, CacheView ic,
                                                                    const int32_t* __restrict__ n_entries,
                                                                    int64_t max_entries, const int32_t* __restrict__ pool,
-                                                                   float* scores, int32_t* status) {
+                                                                   float* scores, uint32_t* kmin, uint32_t* kmax,
+                                                                   int32_t* status) {
   __shared__ __align__(16) float qs[kIdxHeads][kIdxDim];
   __shared__ float hw[kIdxHeads];
   const int qi = q0 + blockIdx.y, b = qi / Tq;
@@ -102,28 +104,25 @@ __global__ void __launch_bounds__(kScoreThreads) score_pool_kernel(int q0, int T
   load_query(qi, q_idx, head_w, qs, hw);
   const int64_t p = (int64_t)blockIdx.x * kScoreThreads + threadIdx.x;
   const int64_t npos = (int64_t)n_blocks * kHsiBlock;
-  if (p >= npos) return;
-  const int32_t blk = __ldg(pool + (int64_t)qi * n_blocks + p / kHsiBlock);
   float s = __uint_as_float(kInvalid);
-  if (blk >= 0) {
-    const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
-    if ((int64_t)blk * kHsiBlock >= max_entries) {
-      if (p % kHsiBlock == 0) report(status, CSA2_ERR_BAD_INDEX);
-    } else if (j < nv) {
-      float kv[kIdxDim];
-      if (load_idx_entry<kDtype>(ic, b, j, kv, status)) s = index_score(qs, hw, kv);
+  if (p < npos) {
+    const int32_t blk = __ldg(pool + (int64_t)qi * n_blocks + p / kHsiBlock);
+    if (blk >= 0) {
+      const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
+      if ((int64_t)blk * kHsiBlock >= max_entries) {
+        if (p % kHsiBlock == 0) report(status, CSA2_ERR_BAD_INDEX);
+      } else if (j < nv) {
+        float kv[kIdxDim];
+        if (load_idx_entry<kDtype>(ic, b, j, kv, status)) s = index_score(qs, hw, kv);
+      }
     }
+    scores[(int64_t)blockIdx.y * npos + p] = s;
   }
-  scores[(int64_t)blockIdx.y * npos + p] = s;
+  const uint32_t key = order_key(s);
+  fold_key_range(key ? key : 0xFFFFFFFFu, key, kmin + blockIdx.y, kmax + blockIdx.y);
 }
 
 // ---------------------------------------------------------------- select ----
-
-__device__ __forceinline__ uint32_t order_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if (u == kInvalid) return 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // Exclusive prefix sum over the CTA (kSelThreads threads); returns the total.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t& total) {
@@ -290,30 +289,149 @@ __device__ void block_select(const float* vals, int64_t n, int k, int64_t forced
   for (uint32_t i = total + threadIdx.x; i < (uint32_t)k; i += kSelThreads) out[i] = -1;
 }
 
-// blockIdx.y == 0: entry top-k; == 1: HSI block pool (Full) .
-__global__ void __launch_bounds__(kSelThreads) select_kernel(int q0, int Tq, int r, int k, int n_blocks, int64_t max_entries,
-                                                             int64_t smem_keys,
-                                                             const int64_t* __restrict__ q_pos,
-                                                             const int32_t* __restrict__ n_entries,
-                                                             const int32_t* __restrict__ pool, const float* scores,
-                                                             const float* bmax, int64_t score_stride,
-                                                             int32_t* topk_out, int32_t* pool_out) {
-  extern __shared__ uint32_t skeys_dyn[];
+// Bitonic sort of P (a power of two) 64-bit keys in shared memory, descending
+// or ascending; every thread of the CTA calls it.
+__device__ void bitonic_sort(unsigned long long* a, int P, bool descending) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += kSelThreads) {
+        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+        const bool up = ((lo & size) == 0) != descending;  // this pair sorts ascending
+        const unsigned long long x = a[lo], y = a[hi];
+        if ((x > y) == up) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Top-k of one query from its scores in global memory in two passes:
+// (1) histogram over kHistBins linear bins of the key range [kmin, kmax]
+// recorded by the scoring kernel -> the bin holding the k-th key; (2) gather
+// every key in that bin or above, as (key << 32 | ~position), sort them
+// descending in shared memory -- the first k are the selection by (score
+// desc, position asc) -- then sort the chosen positions ascending.  The
+// forced position (HSI's latest block) always takes a slot.  Falls back to
+// the radix select when more than kCandMax keys tie into the threshold bin.
+__device__ void select_two_pass(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
+                                uint32_t kmin, uint32_t kmax, uint32_t* hist, unsigned long long* cand) {
+  __shared__ uint32_t sh_tb, sh_above, sh_total, sh_count;
+  const bool any = kmin <= kmax;
+  const uint32_t range = any ? kmax - kmin : 0u;
+  const int nbits = range ? 32 - __clz(range) : 0;
+  const int sh = nbits > 13 ? nbits - 13 : 0;
+  const bool has_forced = forced >= 0 && forced < n;
+  const uint32_t kk_need = (uint32_t)k - (has_forced ? 1u : 0u);
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) hist[i] = 0;
+  if (threadIdx.x == 0) sh_count = 0;
+  __syncthreads();
+  if (any) {
+    for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
+      if (p == forced) continue;
+      const uint32_t kk = order_key(vals[p]);
+      if (kk != 0u) atomicAdd(&hist[(kk - kmin) >> sh], 1u);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    // lane L owns bins [8192 - 256(L+1), 8192 - 256L): counts from the top
+    const int lane = threadIdx.x;
+    uint32_t sacc = 0;
+    for (int i = 0; i < 256; ++i) sacc += hist[kHistBins - 1 - 256 * lane - i];
+    uint32_t incl = sacc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    const uint32_t excl = incl - sacc;
+    if (lane == 0) {
+      sh_total = total;
+      sh_tb = 0;
+      sh_above = 0;
+    }
+    __syncwarp();
+    if (total > kk_need && excl < kk_need && incl >= kk_need) {
+      uint32_t above = excl;
+      for (int i = 0; i < 256; ++i) {
+        const int d = kHistBins - 1 - 256 * lane - i;
+        if (above + hist[d] >= kk_need) {
+          sh_tb = (uint32_t)d;
+          sh_above = above;
+          break;
+        }
+        above += hist[d];
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t tb = sh_tb;
+  const uint32_t cand_n = (sh_total > kk_need ? sh_above + hist[tb] : sh_total) + (has_forced ? 1u : 0u);
+  if (cand_n > (uint32_t)kCandMax) {
+    block_select(vals, n, k, forced, idmap, out, nullptr);
+    return;
+  }
+  // (2) gather the candidates
+  for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
+    unsigned long long ck = 0ull;
+    if (p == forced) {
+      ck = (0xFFFFFFFFull << 32) | (0xFFFFFFFFu - (uint32_t)p);
+    } else if (any) {
+      const uint32_t kk = order_key(vals[p]);
+      if (kk != 0u && ((kk - kmin) >> sh) >= tb) ck = ((unsigned long long)kk << 32) | (0xFFFFFFFFu - (uint32_t)p);
+    }
+    if (ck) cand[atomicAdd(&sh_count, 1u)] = ck;
+  }
+  __syncthreads();
+  const int C = (int)sh_count;
+  int P = 1;
+  while (P < C) P <<= 1;
+  for (int i = C + threadIdx.x; i < P; i += kSelThreads) cand[i] = 0ull;
+  __syncthreads();
+  bitonic_sort(cand, P, true);
+  const int m = C < k ? C : k;
+  // chosen positions, ascending
+  int P2 = 1;
+  while (P2 < m) P2 <<= 1;
+  for (int i = threadIdx.x; i < P2; i += kSelThreads) {
+    const unsigned long long v = (i < m) ? (unsigned long long)(0xFFFFFFFFu - (uint32_t)(cand[i] & 0xFFFFFFFFull))
+                                         : ~0ull;
+    cand[kCandMax + i] = v;
+  }
+  __syncthreads();
+  bitonic_sort(cand + kCandMax, P2, false);
+  for (int i = threadIdx.x; i < k; i += kSelThreads) out[i] = i < m ? idmap((int64_t)cand[kCandMax + i]) : -1;
+}
+
+// blockIdx.y == 0: entry top-k (Full or Reindex); == 1: HSI block pool (Full).
+__global__ void __launch_bounds__(kSelThreads) select2_kernel(int q0, int Tq, int r, int k, int n_blocks,
+                                                              int64_t max_entries, const int64_t* __restrict__ q_pos,
+                                                              const int32_t* __restrict__ n_entries,
+                                                              const int32_t* __restrict__ pool, const float* scores,
+                                                              const float* bmax, int64_t score_stride,
+                                                              const uint32_t* kmin, const uint32_t* kmax,
+                                                              int32_t* topk_out, int32_t* pool_out) {
+  extern __shared__ __align__(16) unsigned long long sel_smem[];
+  unsigned long long* cand = sel_smem;                                    // [2 * kCandMax]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem + 2 * kCandMax);  // [kHistBins]
   const int qc = blockIdx.x, qi = q0 + qc, b = qi / Tq;
   const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
-  auto keys_for = [&](int64_t n) -> uint32_t* { return n <= smem_keys ? skeys_dyn : nullptr; };
+  const uint32_t lo = kmin[qc], hi = kmax[qc];
   if (blockIdx.y == 0) {
     const float* v = scores + (int64_t)qc * score_stride;
-    if (pool) {
-      block_select(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks},
-                   topk_out + (int64_t)qi * k, keys_for((int64_t)n_blocks * kHsiBlock));
-    } else {
-      block_select(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k, keys_for(nv));
-    }
+    if (pool)
+      select_two_pass(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks},
+                      topk_out + (int64_t)qi * k, lo, hi, hist, cand);
+    else
+      select_two_pass(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k, lo, hi, hist, cand);
   } else {
     const int64_t nb = (nv + kHsiBlock - 1) / kHsiBlock;
     const float* v = bmax + (int64_t)qc * ((max_entries + 7) / 8);
-    block_select(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks, keys_for(nb));
+    select_two_pass(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks, lo, hi, hist, cand);
   }
 }
 
@@ -321,11 +439,13 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
+// Per query: scores (Full: max_entries, Reindex: pool positions), HSI block
+// maxima (Full with HSI), and the [min, max] key range (8 bytes, padded).
 size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex) {
-  if (reindex) return align256((size_t)cfg.hsi_blocks * kHsiBlock * sizeof(float));
+  if (reindex) return align256((size_t)cfg.hsi_blocks * kHsiBlock * sizeof(float)) + 512;
   size_t b = align256((size_t)max_entries * sizeof(float));
   if (cfg.hsi_blocks > 0) b += align256((size_t)((max_entries + 7) / 8) * sizeof(float));
-  return b;
+  return b + 512;
 }
 
 cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx,
@@ -341,38 +461,42 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
   if (chunk < 1) return cudaErrorInvalidValue;
   float* scores = static_cast<float*>(ws);
   const int64_t stride = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
-  float* bmax = (!reindex && pool_out) ? reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                                                    align256((size_t)chunk * stride * sizeof(float)))
-                                       : nullptr;
+  char* cur = static_cast<char*>(ws) + align256((size_t)chunk * stride * sizeof(float));
+  float* bmax = nullptr;
+  if (!reindex && pool_out) {
+    bmax = reinterpret_cast<float*>(cur);
+    cur += align256((size_t)chunk * ((max_entries + 7) / 8) * sizeof(float));
+  }
+  uint32_t* kmin = reinterpret_cast<uint32_t*>(cur);
+  uint32_t* kmax = reinterpret_cast<uint32_t*>(cur + align256((size_t)chunk * sizeof(uint32_t)));
   const CacheView iv = view_of(idx_c);
   for (int q0 = 0; q0 < Q; q0 += chunk) {
     const int nq = std::min(chunk, Q - q0);
+    cudaMemsetAsync(kmin, 0xFF, (size_t)nq * sizeof(uint32_t), stream);  // empty ranges
+    cudaMemsetAsync(kmax, 0x00, (size_t)nq * sizeof(uint32_t), stream);
     if (reindex) {
       dim3 g((unsigned)((stride + kScoreThreads - 1) / kScoreThreads), nq);
       if (cfg.cache_dtype == CSA2_CACHE_FP4)
         score_pool_kernel<CSA2_CACHE_FP4><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, cfg.hsi_blocks, q_idx, head_w,
                                                                           q_pos, iv, n_entries, max_entries, pool,
-                                                                          scores, status);
+                                                                          scores, kmin, kmax, status);
       else
         score_pool_kernel<CSA2_CACHE_BF16><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, cfg.hsi_blocks, q_idx, head_w,
                                                                            q_pos, iv, n_entries, max_entries, pool,
-                                                                           scores, status);
+                                                                           scores, kmin, kmax, status);
     } else {
       cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, scores, bmax,
-                                      status, num_sms(), stream);
+                                      kmin, kmax, status, num_sms(), stream);
       if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // keys staged in shared memory when the largest candidate list fits
-    const int64_t n_max = reindex ? stride : (int64_t)max_entries;
-    const int64_t smem_keys = std::min<int64_t>(n_max, kSelSmemKeys);
     dim3 sg(nq, (!reindex && pool_out) ? 2 : 1);
-    const size_t sel_smem = (size_t)smem_keys * sizeof(uint32_t);
-    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
-    select_kernel<<<sg, kSelThreads, sel_smem, stream>>>(q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, max_entries,
-                                                         smem_keys, q_pos, n_entries, pool, scores, bmax, stride,
-                                                         topk_out, pool_out);
+    const size_t sel_smem = 2 * kCandMax * sizeof(unsigned long long) + kHistBins * sizeof(uint32_t);
+    cudaFuncSetAttribute(select2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
+    select2_kernel<<<sg, kSelThreads, sel_smem, stream>>>(q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, max_entries,
+                                                          q_pos, n_entries, pool, scores, bmax, stride, kmin, kmax,
+                                                          topk_out, pool_out);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -45,6 +45,8 @@ struct ScoreArgs {
   int tiles_per_cta;
   float* scores;   // [chunk][max_entries]
   float* bmax;     // [chunk][ceil(max_entries/8)] or null
+  uint32_t* kmin;  // [chunk] key range of each query's scores
+  uint32_t* kmax;
   int32_t* status;
 };
 
@@ -192,6 +194,12 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
   const int lane_base = 32 * warp;  // TMEM lanes of this warp
   int i = 0;
   int last_issued = -1, waited = -1;
+  uint32_t klo[QPC], khi[QPC];
+#pragma unroll
+  for (int q = 0; q < QPC; ++q) {
+    klo[q] = 0xFFFFFFFFu;
+    khi[q] = 0u;
+  }
   for (; i <= n_my; ++i) {
     if (i < n_my) {
       const int s = i % S;
@@ -280,7 +288,12 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
         s += 0.0f;
         if (j >= nv[q] || !ok) s = -INFINITY;
         const int qc = blockIdx.y * QPC + q;
-        if (j < nv[q]) a.scores[(int64_t)qc * a.max_entries + j] = s;
+        if (j < nv[q]) {
+          a.scores[(int64_t)qc * a.max_entries + j] = s;
+          const uint32_t kk = order_key(s);
+          klo[q] = min(klo[q], kk);
+          khi[q] = max(khi[q], kk);
+        }
         if (a.bmax) {
           float m = s;
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -291,6 +304,9 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
       }
     }
   }
+#pragma unroll
+  for (int q = 0; q < QPC; ++q)
+    fold_key_range(klo[q], khi[q], a.kmin + blockIdx.y * QPC + q, a.kmax + blockIdx.y * QPC + q);
   // after an abort, let the last issued MMAs finish before TMEM is released
   if (last_issued > waited) {
     if (!tc::mbar_wait(&mma_bar[last_issued & 1], (last_issued >> 1) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
@@ -317,8 +333,8 @@ static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaSt
 
 cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
                             const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
-                            int64_t max_entries, float* scores, float* bmax, int32_t* status, int num_sms,
-                            cudaStream_t stream) {
+                            int64_t max_entries, float* scores, float* bmax, uint32_t* kmin, uint32_t* kmax,
+                            int32_t* status, int num_sms, cudaStream_t stream) {
   const int qpc = (Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) ? 4 : 1;
   const int groups = nq / qpc;
   const int64_t tiles = (max_entries + 127) / 128;
@@ -327,7 +343,7 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   int64_t per = std::min<int64_t>(kMaxTilesPerCta, std::max<int64_t>(4, (tiles + want - 1) / want));
   const int splits = (int)((tiles + per - 1) / per);
   ScoreArgs a{q0, Tq, cfg.ratio, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
-              scores, bmax, status};
+              scores, bmax, kmin, kmax, status};
   if (cfg.cache_dtype == CSA2_CACHE_FP4)
     return qpc == 4 ? launch_one<CSA2_CACHE_FP4, 4>(a, groups, splits, stream)
                     : launch_one<CSA2_CACHE_FP4, 1>(a, groups, splits, stream);

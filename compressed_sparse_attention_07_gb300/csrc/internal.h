@@ -25,8 +25,8 @@ int num_sms();
 // Tensor-core indexer scores (Full mode) for queries [q0, q0 + nq).
 cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
                             const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
-                            int64_t max_entries, float* scores, float* bmax, int32_t* status, int num_sms,
-                            cudaStream_t stream);
+                            int64_t max_entries, float* scores, float* bmax, uint32_t* kmin, uint32_t* kmax,
+                            int32_t* status, int num_sms, cudaStream_t stream);
 
 // Per-query workspace bytes of the indexer (scores + HSI block maxima).
 size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex);

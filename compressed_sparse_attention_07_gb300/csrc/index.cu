@@ -13,7 +13,8 @@ constexpr int kScoreThreads = 128;  // one entry per thread
 constexpr int kSelThreads = 1024;   // one CTA selects for one query
 constexpr uint32_t kInvalid = kScoreInvalid;
 constexpr int kHistBins = 8192;    // linear bins over a query's key range
-constexpr int kCandMax = 16384;    // candidates sorted in shared memory
+constexpr int kCandMax = 8192;     // candidates sorted in shared memory
+constexpr int kSelOutMax = 4096;   // k of one selection (top-k <= 1024, HSI blocks <= 4096)
 
 // Decoded indexer-K entry (128 channels) of sequence b, slot j, into registers.
 template <int kDtype>
@@ -416,8 +417,8 @@ __global__ void __launch_bounds__(kSelThreads) select2_kernel(int q0, int Tq, in
                                                               const uint32_t* kmin, const uint32_t* kmax,
                                                               int32_t* topk_out, int32_t* pool_out) {
   extern __shared__ __align__(16) unsigned long long sel_smem[];
-  unsigned long long* cand = sel_smem;                                    // [2 * kCandMax]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem + 2 * kCandMax);  // [kHistBins]
+  unsigned long long* cand = sel_smem;                                             // [kCandMax + kSelOutMax]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem + kCandMax + kSelOutMax);  // [kHistBins]
   const int qc = blockIdx.x, qi = q0 + qc, b = qi / Tq;
   const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
   const uint32_t lo = kmin[qc], hi = kmax[qc];
@@ -492,7 +493,7 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 sg(nq, (!reindex && pool_out) ? 2 : 1);
-    const size_t sel_smem = 2 * kCandMax * sizeof(unsigned long long) + kHistBins * sizeof(uint32_t);
+    const size_t sel_smem = (kCandMax + kSelOutMax) * sizeof(unsigned long long) + kHistBins * sizeof(uint32_t);
     cudaFuncSetAttribute(select2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
     select2_kernel<<<sg, kSelThreads, sel_smem, stream>>>(q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, max_entries,
                                                           q_pos, n_entries, pool, scores, bmax, stride, kmin, kmax,

@@ -9,119 +9,10 @@
 namespace csa2 {
 namespace {
 
-constexpr int kScoreThreads = 128;  // one entry per thread
 constexpr int kSelThreads = 1024;   // one CTA selects for one query
-constexpr uint32_t kInvalid = kScoreInvalid;
 constexpr int kHistBins = 8192;    // linear bins over a query's key range
 constexpr int kCandMax = 8192;     // candidates sorted in shared memory
 constexpr int kSelOutMax = 4096;   // k of one selection (top-k <= 1024, HSI blocks <= 4096)
-
-// Decoded indexer-K entry (128 channels) of sequence b, slot j, into registers.
-template <int kDtype>
-__device__ __forceinline__ bool load_idx_entry(const CacheView& ic, int b, int64_t j, float (&kv)[kIdxDim],
-                                               int32_t* status) {
-  const int64_t page = page_of(ic, b, j, status);
-  if (page < 0) return false;
-  const int slot = (int)(j % kPage);
-  if (kDtype == CSA2_CACHE_FP4) {
-    const uint8_t* base = ic.data + page * kIdxFp4Data;
-    uint2 sc = __ldg(reinterpret_cast<const uint2*>(ic.scales + page * kIdxFp4Scales + slot * 8));
-    uint32_t sw[2] = {sc.x, sc.y};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (c * kPage + slot) * 16));
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-          const int ch = c * 32 + q * 8 + n;  // channel
-          const int g = ch >> 4;
-          float s = e4m3_to_float((sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
-          kv[ch] = e2m1_to_float((w[q] >> (4 * n)) & 15u) * s;
-        }
-      }
-    }
-  } else {
-    const uint8_t* base = ic.data + page * kIdxBf16Data;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (c * kPage + slot) * 16));
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        kv[c * 8 + 2 * q] = __uint_as_float(w[q] << 16);
-        kv[c * 8 + 2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-      }
-    }
-  }
-  return true;
-}
-
-// s = sum_h w_h ReLU(q_h . K) with q in shared memory (fp32), -0 folded to +0.
-__device__ __forceinline__ float index_score(const float (*qs)[kIdxDim], const float* hw, const float (&kv)[kIdxDim]) {
-  float acc = 0.0f;
-#pragma unroll 1
-  for (int h = 0; h < kIdxHeads; ++h) {
-    float d = 0.0f;
-    const float4* q4 = reinterpret_cast<const float4*>(qs[h]);
-#pragma unroll
-    for (int c = 0; c < kIdxDim / 4; ++c) {
-      float4 q = q4[c];
-      d = fmaf(q.x, kv[4 * c], d);
-      d = fmaf(q.y, kv[4 * c + 1], d);
-      d = fmaf(q.z, kv[4 * c + 2], d);
-      d = fmaf(q.w, kv[4 * c + 3], d);
-    }
-    acc = fmaf(hw[h], fmaxf(d, 0.0f), acc);
-  }
-  return acc + 0.0f;
-}
-
-__device__ __forceinline__ void load_query(int qi, const uint16_t* q_idx, const float* head_w,
-                                           float (*qs)[kIdxDim], float* hw) {
-  const uint16_t* qp = q_idx + (int64_t)qi * kIdxHeads * kIdxDim;
-  for (int i = threadIdx.x; i < kIdxHeads * kIdxDim; i += blockDim.x)
-    qs[i / kIdxDim][i % kIdxDim] = bf16_bits_to_float(__ldg(qp + i));
-  if (threadIdx.x < kIdxHeads) hw[threadIdx.x] = head_w ? __ldg(head_w + (int64_t)qi * kIdxHeads + threadIdx.x) : 1.0f;
-  __syncthreads();
-}
-
-// Reindex: the visible entries of the pool's blocks; position p -> block
-// pool[p / 8], entry block * 8 + p % 8.  scores [chunk][n_blocks * 8].
-template <int kDtype>
-__global__ void __launch_bounds__(kScoreThreads) score_pool_kernel(int q0, int Tq, int r, int n_blocks,
-                                                                   const uint16_t* __restrict__ q_idx,
-                                                                   const float* __restrict__ head_w,
-                                                                   const int64_t* __restrict__ q_pos, CacheView ic,
-                                                                   const int32_t* __restrict__ n_entries,
-                                                                   int64_t max_entries, const int32_t* __restrict__ pool,
-                                                                   float* scores, uint32_t* kmin, uint32_t* kmax,
-                                                                   int32_t* status) {
-  __shared__ __align__(16) float qs[kIdxHeads][kIdxDim];
-  __shared__ float hw[kIdxHeads];
-  const int qi = q0 + blockIdx.y, b = qi / Tq;
-  const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
-  load_query(qi, q_idx, head_w, qs, hw);
-  const int64_t p = (int64_t)blockIdx.x * kScoreThreads + threadIdx.x;
-  const int64_t npos = (int64_t)n_blocks * kHsiBlock;
-  float s = __uint_as_float(kInvalid);
-  if (p < npos) {
-    const int32_t blk = __ldg(pool + (int64_t)qi * n_blocks + p / kHsiBlock);
-    if (blk >= 0) {
-      const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
-      if ((int64_t)blk * kHsiBlock >= max_entries) {
-        if (p % kHsiBlock == 0) report(status, CSA2_ERR_BAD_INDEX);
-      } else if (j < nv) {
-        float kv[kIdxDim];
-        if (load_idx_entry<kDtype>(ic, b, j, kv, status)) s = index_score(qs, hw, kv);
-      }
-    }
-    scores[(int64_t)blockIdx.y * npos + p] = s;
-  }
-  const uint32_t key = order_key(s);
-  fold_key_range(key ? key : 0xFFFFFFFFu, key, kmin + blockIdx.y, kmax + blockIdx.y);
-}
 
 // ---------------------------------------------------------------- select ----
 
@@ -470,27 +361,12 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
   }
   uint32_t* kmin = reinterpret_cast<uint32_t*>(cur);
   uint32_t* kmax = reinterpret_cast<uint32_t*>(cur + align256((size_t)chunk * sizeof(uint32_t)));
-  const CacheView iv = view_of(idx_c);
   for (int q0 = 0; q0 < Q; q0 += chunk) {
     const int nq = std::min(chunk, Q - q0);
     cudaMemsetAsync(kmin, 0xFF, (size_t)nq * sizeof(uint32_t), stream);  // empty ranges
     cudaMemsetAsync(kmax, 0x00, (size_t)nq * sizeof(uint32_t), stream);
-    if (reindex) {
-      dim3 g((unsigned)((stride + kScoreThreads - 1) / kScoreThreads), nq);
-      if (cfg.cache_dtype == CSA2_CACHE_FP4)
-        score_pool_kernel<CSA2_CACHE_FP4><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, cfg.hsi_blocks, q_idx, head_w,
-                                                                          q_pos, iv, n_entries, max_entries, pool,
-                                                                          scores, kmin, kmax, status);
-      else
-        score_pool_kernel<CSA2_CACHE_BF16><<<g, kScoreThreads, 0, stream>>>(q0, Tq, cfg.ratio, cfg.hsi_blocks, q_idx, head_w,
-                                                                           q_pos, iv, n_entries, max_entries, pool,
-                                                                           scores, kmin, kmax, status);
-    } else {
-      cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, scores, bmax,
-                                      kmin, kmax, status, num_sms(), stream);
-      if (e != cudaSuccess) return e;
-    }
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, scores,
+                                    stride, bmax, kmin, kmax, status, num_sms(), stream);
     if (e != cudaSuccess) return e;
     dim3 sg(nq, (!reindex && pool_out) ? 2 : 1);
     const size_t sel_smem = (kCandMax + kSelOutMax) * sizeof(unsigned long long) + kHistBins * sizeof(uint32_t);

@@ -1,18 +1,25 @@
-// a3 / a5 -- CSA2 indexer scores on the tensor cores (Full mode).
+// a3 / a5 / a6 -- CSA2 indexer scores on the tensor cores.
 //
-// s_j = sum_h w_h ReLU(q_h . K_j) over the visible indexer-K entries
-// (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.3.1; 36kr "CSA2").  Per CTA: a
+// s_j = sum_h w_h ReLU(q_h . K_j) (DeepSeek-V4.1 Flash, hn.213312.xyz
+// sec. 2.3.1; 36kr "CSA2") for every visible indexer-K entry (Full) or for the
+// entries of an HSI pool (Reindex, hn.213312.xyz sec. 2.3.4).  Per CTA: a
 // range of 128-entry tiles of one group of QPC queries of one sequence.
-//  - warp 4 (one elected lane) streams whole cache pages into a shared-memory
-//    ring with 1-D bulk copies (two pages = one tile; mbarrier completion);
-//  - warps 0-3 (thread t <-> entry t of the tile <-> TMEM lane t) decode their
-//    entry (FP4 -> f16, exact; bf16 kept) straight into TMEM as the A operand;
-//  - thread 0 issues tcgen05.mma: D[128 entries x 32*QPC] += K_tile . Q^T with
-//    A from TMEM and Q_idx (f16 / bf16) from shared memory;
+//  - page mode (Full): warp 8 (one elected lane) streams whole cache pages,
+//    two per tile, into a shared-memory ring with 1-D bulk copies completing
+//    on mbarriers;
+//  - gather mode (Reindex): each thread gathers its own entry of the pool
+//    with cp.async into the same ring layout (block ids resolved to pages
+//    once at set-up);
+//  - two consumer warpgroups take alternate tiles; thread t of a warpgroup
+//    owns entry t of the tile and TMEM lane t: it decodes the entry (FP4 ->
+//    f16, exact; bf16 kept), stores it to its warpgroup's TMEM A buffer, and
+//    one thread issues tcgen05.mma D[128 x 32*QPC] = K_tile . Q^T with Q_idx
+//    (f16 / bf16) from shared memory;
 //  - the epilogue reads D back (one row per thread), forms the ReLU-weighted
-//    head sums, writes the scores and the 8-entry block maxima for HSI.
-// A and D are double-buffered in TMEM so that the MMA of tile i overlaps the
-// epilogue of tile i-1 and the decode of tile i+1.  Every wait is bounded.
+//    head sums, writes the scores, the 8-entry block maxima for HSI and folds
+//    the per-query key range used by the top-k selection.
+// A warpgroup decodes its next tile while its previous MMA runs, and the two
+// warpgroups interleave on the tensor core.  Every wait is bounded.
 #include <algorithm>
 
 #include "internal.h"
@@ -21,17 +28,19 @@
 namespace csa2 {
 namespace {
 
-constexpr int kConsumers = 128;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kWG = 2;                     // consumer warpgroups
+constexpr int kConsumers = 128 * kWG;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp (page mode)
+constexpr int kStages = 4;                 // ring slots; warpgroup g owns slots g, g + 2 in gather mode
 constexpr uint32_t kSpin = 1u << 26;
 constexpr int kMaxTilesPerCta = 512;
+constexpr int kMaxGatherTiles = 32;        // gather mode: resolved positions held in shared memory
 
 template <int kDtype>
 struct TileFmt {
   static constexpr int kPageData = (kDtype == CSA2_CACHE_FP4) ? kIdxFp4Data : kIdxBf16Data;
   static constexpr int kPageScales = (kDtype == CSA2_CACHE_FP4) ? kIdxFp4Scales : 0;
   static constexpr int kSlotBytes = 2 * (kPageData + kPageScales);
-  static constexpr int kStages = (kDtype == CSA2_CACHE_FP4) ? 4 : 2;
 };
 
 struct ScoreArgs {
@@ -43,9 +52,12 @@ struct ScoreArgs {
   const int32_t* n_entries;
   int64_t max_entries;
   int tiles_per_cta;
-  float* scores;   // [chunk][max_entries]
-  float* bmax;     // [chunk][ceil(max_entries/8)] or null
-  uint32_t* kmin;  // [chunk] key range of each query's scores
+  const int32_t* pool;  // gather mode: pool block ids [Q][n_blocks]
+  int n_blocks;
+  float* scores;        // [chunk][stride]
+  int64_t stride;
+  float* bmax;          // [chunk][ceil(max_entries/8)] or null
+  uint32_t* kmin;       // [chunk] key range of each query's scores
   uint32_t* kmax;
   int32_t* status;
 };
@@ -72,29 +84,42 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return r;
 }
 
-__device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int kDtype, int QPC>
-__global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
+// Barrier of one warpgroup (ids 1, 2) or of all consumers (id 3).
+__device__ __forceinline__ void wg_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 3, %0;" ::"n"(kConsumers) : "memory"); }
+
+template <int kDtype, int QPC, bool kGather>
+__global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(ScoreArgs a) {
   using F = TileFmt<kDtype>;
   constexpr int kN = 32 * QPC;                    // MMA N: QPC queries x 32 heads
   constexpr int kAcols = 64;                      // 128 channels of f16 pairs
-  constexpr int kTmemCols = (2 * kAcols + 2 * kN) <= 256 ? 256 : 512;
-  constexpr int S = F::kStages;
+  constexpr int kTmemCols = (kWG * kAcols + kWG * kN) <= 256 ? 256 : 512;
   constexpr bool kBf16 = (kDtype == CSA2_CACHE_BF16);
   constexpr uint32_t kIdesc = tc::idesc_f16(128, kN, kBf16, kBf16, false, false);
+  static_assert(!kGather || QPC == 1, "gather mode scores one query per CTA");
 
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* qtile = smem;                                   // [kN rows][128] K-major, 256*kN B
-  uint8_t* ring = smem + 256 * kN;                         // S slots
+  uint8_t* qtile = smem;                          // [kN rows][128] K-major, 256*kN B
+  uint8_t* ring = smem + 256 * kN;                // kStages slots
   __shared__ float hw[QPC][kIdxHeads];
-  __shared__ __align__(8) uint64_t full_bar[S], empty_bar[S], mma_bar[2];
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], mma_bar[kWG];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ int32_t ptab[2 * kMaxTilesPerCta];  // resolved pages of this CTA's tiles
+  __shared__ int32_t ptab[kGather ? 1 : 2 * kMaxTilesPerCta];     // page mode: pages of this CTA's tiles
+  __shared__ int32_t gtab[kGather ? kMaxGatherTiles * 128 : 1];   // gather mode: page*64+slot or -1
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int g0 = a.q0 + blockIdx.y * QPC;   // first query of the group (same sequence)
+  const int g0 = a.q0 + blockIdx.y * QPC;  // first query of the group (same sequence)
   const int b = g0 / a.Tq;
   int64_t nv[QPC];
   int64_t nv_max = 0;
@@ -104,13 +129,14 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
     nv[q] = visible_entries(a.q_pos[g0 + q], a.r, ne);
     nv_max = nv[q] > nv_max ? nv[q] : nv_max;
   }
-  const int64_t n_tiles = (nv_max + 127) / 128;
+  const int64_t npos = kGather ? (int64_t)a.n_blocks * kHsiBlock : nv_max;
+  const int64_t n_tiles = (npos + 127) / 128;
   const int64_t t_begin = (int64_t)blockIdx.x * a.tiles_per_cta;
   const int64_t t_end = t_begin + a.tiles_per_cta < n_tiles ? t_begin + a.tiles_per_cta : n_tiles;
   if (t_begin >= t_end) return;  // uniform: the whole CTA leaves before any barrier
   const int n_my = (int)(t_end - t_begin);
 
-  // ---- set-up: Q_idx (f16 or bf16) into the B tile, head weights, barriers, TMEM
+  // ---- set-up: Q_idx (f16 or bf16) into the B tile, head weights, pages, barriers, TMEM
   for (int i = tid; i < kN * kIdxDim / 8; i += kThreads) {
     const int row = (8 * i) / kIdxDim, k = (8 * i) % kIdxDim;  // row = q*32 + h; 8 channels per load
     uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
@@ -128,17 +154,36 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
   }
   for (int i = tid; i < QPC * kIdxHeads; i += kThreads)
     hw[i / kIdxHeads][i % kIdxHeads] = a.head_w ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;
-  for (int i = tid; i < 2 * n_my; i += kThreads) {
-    const int64_t p = 2 * t_begin + i;  // logical page
-    ptab[i] = (p * kPage < nv_max) ? (int32_t)page_of(a.ic, b, p * kPage, a.status) : -1;
+  if (kGather) {
+    for (int i = tid; i < n_my * 128; i += kThreads) {
+      const int64_t p = t_begin * 128 + i;  // pool position
+      int32_t e = -1;
+      if (p < npos) {
+        const int32_t blk = __ldg(a.pool + (int64_t)g0 * a.n_blocks + p / kHsiBlock);
+        if (blk >= 0) {
+          const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
+          if ((int64_t)blk * kHsiBlock >= a.max_entries) {
+            if (p % kHsiBlock == 0) report(a.status, CSA2_ERR_BAD_INDEX);
+          } else if (j < nv[0]) {
+            const int64_t page = page_of(a.ic, b, j, a.status);
+            if (page >= 0) e = (int32_t)(page * kPage + j % kPage);
+          }
+        }
+      }
+      gtab[i] = e;
+    }
+  } else {
+    for (int i = tid; i < 2 * n_my; i += kThreads) {
+      const int64_t p = 2 * t_begin + i;  // logical page
+      ptab[i] = (p * kPage < nv_max) ? (int32_t)page_of(a.ic, b, p * kPage, a.status) : -1;
+    }
   }
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&full_bar[s], 1);
-      tc::mbar_init(&empty_bar[s], kConsumers);
+      tc::mbar_init(&empty_bar[s], 128);
     }
-    tc::mbar_init(&mma_bar[0], 1);
-    tc::mbar_init(&mma_bar[1], 1);
+    for (int w = 0; w < kWG; ++w) tc::mbar_init(&mma_bar[w], 1);
     abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -152,13 +197,13 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
   tc::fence_after_sync();
   const uint32_t tb = tmem_base;
 
-  if (warp == 4) {
+  if (warp == kConsumers / 32) {
     // ------------------------------------------------------------ producer
-    if ((tid & 31) == 0) {
+    if (!kGather && (tid & 31) == 0) {
       int issued = 0;
       for (int i = 0; i < n_my; ++i) {
-        const int s = i % S;
-        if (!tc::mbar_wait(&empty_bar[s], ((i / S) & 1) ^ 1, kSpin)) {
+        const int s = i % kStages;
+        if (!tc::mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, kSpin)) {
           report(a.status, CSA2_ERR_TIMEOUT);
           atomicExch(&abort_flag, 1);
           break;
@@ -166,81 +211,164 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
         if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
         uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
         uint32_t bytes = 0;
-        int64_t pages[2] = {-1, -1};
+        int64_t pages[2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          pages[h] = ptab[2 * i + h];
-          if (pages[h] >= 0) bytes += F::kPageData + F::kPageScales;
+        for (int hh = 0; hh < 2; ++hh) {
+          pages[hh] = ptab[2 * i + hh];
+          if (pages[hh] >= 0) bytes += F::kPageData + F::kPageScales;
         }
         tc::mbar_arrive_expect_tx(&full_bar[s], bytes);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (pages[h] < 0) continue;
-          tc::bulk_g2s(slot + h * F::kPageData, a.ic.data + pages[h] * F::kPageData, F::kPageData, &full_bar[s]);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (pages[hh] < 0) continue;
+          tc::bulk_g2s(slot + hh * F::kPageData, a.ic.data + pages[hh] * F::kPageData, F::kPageData, &full_bar[s]);
           if (F::kPageScales)
-            tc::bulk_g2s(slot + 2 * F::kPageData + h * F::kPageScales, a.ic.scales + pages[h] * F::kPageScales,
+            tc::bulk_g2s(slot + 2 * F::kPageData + hh * F::kPageScales, a.ic.scales + pages[hh] * F::kPageScales,
                          F::kPageScales, &full_bar[s]);
         }
         ++issued;
       }
       // do not leave while copies into this CTA's shared memory are in flight
-      for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-        if (!tc::mbar_wait(&full_bar[i % S], (i / S) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
+      for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+        if (!tc::mbar_wait(&full_bar[i % kStages], (i / kStages) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  const int lane_base = 32 * warp;  // TMEM lanes of this warp
-  int i = 0;
-  int last_issued = -1, waited = -1;
+  const int g = warp >> 2;               // warpgroup: tiles g, g + 2, ...
+  const int lt = tid & 127;              // entry of the tile, TMEM lane
+  const uint32_t lane_base = 32 * (warp & 3);
+  const uint32_t acol = (uint32_t)(g * kAcols);
+  const uint32_t dcol = (uint32_t)(kWG * kAcols + g * kN);
+  const int n_own = n_my > g ? (n_my - g + 1) / 2 : 0;
   uint32_t klo[QPC], khi[QPC];
 #pragma unroll
   for (int q = 0; q < QPC; ++q) {
     klo[q] = 0xFFFFFFFFu;
     khi[q] = 0u;
   }
-  for (; i <= n_my; ++i) {
-    if (i < n_my) {
-      const int s = i % S;
-      const bool ok = tc::mbar_wait(&full_bar[s], (i / S) & 1, kSpin);
-      if (!ok) atomicExch(&abort_flag, 1);
-      uint32_t av[64];
+  const int h = lt >> 6, sl = lt & 63;  // where this entry sits in a tile's ring slot
+
+  // gather mode: copy this thread's entry of own tile u into its slot
+  auto gather = [&](int u) {
+    if (kGather && u < n_own) {
+      const int i = g + 2 * u;
+      uint8_t* slot = ring + (size_t)(i % kStages) * F::kSlotBytes;
+      const int32_t e = gtab[i * 128 + lt];
+      if (e >= 0) {
+        const int64_t page = e / kPage;
+        const int es = e % kPage;
+        if (kDtype == CSA2_CACHE_FP4) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            cp16(slot + h * kIdxFp4Data + (c * kPage + sl) * 16, a.ic.data + page * kIdxFp4Data + (c * kPage + es) * 16);
+          cp8(slot + 2 * kIdxFp4Data + h * kIdxFp4Scales + sl * 8, a.ic.scales + page * kIdxFp4Scales + es * 8);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            cp16(slot + h * kIdxBf16Data + (c * kPage + sl) * 16, a.ic.data + page * kIdxBf16Data + (c * kPage + es) * 16);
+        }
+      }
+    }
+    if (kGather) cp_commit();
+  };
+  gather(0);
+
+  int last_issued = -1, waited = -1;  // own tile counters
+  int u = 0;
+  for (; u <= n_own; ++u) {
+    const int i = g + 2 * u;  // CTA-local tile index
+    const bool have = u < n_own;
+    uint32_t av[64];
+    if (have) {
+      // ---- fetch tile i (own) and decode this thread's entry into registers
+      const int s = i % kStages;
+      if (kGather) {
+        gather(u + 1);
+        cp_wait<1>();
+      } else if (!tc::mbar_wait(&full_bar[s], (i / kStages) & 1, kSpin)) {
+        atomicExch(&abort_flag, 1);
+      }
       const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
-      const int h = tid >> 6, sl = tid & 63;
+      const bool present = !kGather || gtab[i * 128 + lt] >= 0;
       if (kDtype == CSA2_CACHE_FP4) {
         uint4 cw[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           cw[c] = *reinterpret_cast<const uint4*>(slot + h * kIdxFp4Data + (c * kPage + sl) * 16);
         const uint2 sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * kIdxFp4Scales + sl * 8);
-        tc::mbar_arrive(&empty_bar[s]);
+        if (!kGather) tc::mbar_arrive(&empty_bar[s]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint32_t w4[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int g = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
-            const uint32_t sb = ((g < 4 ? sc.x : sc.y) >> (8 * (g & 3))) & 0xFFu;
+            const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
+            const uint32_t sb = ((gg < 4 ? sc.x : sc.y) >> (8 * (gg & 3))) & 0xFFu;
             const uint32_t s2 = f16x2_scale(sb);
             uint32_t h4[4];
             e2m1x8_to_f16x2(w4[q], h4);
 #pragma unroll
-            for (int by = 0; by < 4; ++by) av[c * 16 + q * 4 + by] = hmul2(h4[by], s2);
+            for (int by = 0; by < 4; ++by) av[c * 16 + q * 4 + by] = present ? hmul2(h4[by], s2) : 0u;
           }
         }
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint4 v = *reinterpret_cast<const uint4*>(slot + h * kIdxBf16Data + (c * kPage + sl) * 16);
-          av[4 * c] = v.x;
-          av[4 * c + 1] = v.y;
-          av[4 * c + 2] = v.z;
-          av[4 * c + 3] = v.w;
+          av[4 * c] = present ? v.x : 0u;
+          av[4 * c + 1] = present ? v.y : 0u;
+          av[4 * c + 2] = present ? v.z : 0u;
+          av[4 * c + 3] = present ? v.w : 0u;
         }
-        tc::mbar_arrive(&empty_bar[s]);
+        if (!kGather) tc::mbar_arrive(&empty_bar[s]);
       }
-      const uint32_t acol = (uint32_t)((i & 1) * kAcols);
+    }
+    if (u >= 1) {
+      // ---- epilogue of own tile u-1 (its MMA ran while this tile was fetched)
+      const int e = u - 1, ie = g + 2 * e;
+      const bool ok = tc::mbar_wait(&mma_bar[g], e & 1, kSpin);
+      waited = e;
+      if (!ok) {
+        report(a.status, CSA2_ERR_TIMEOUT);
+        atomicExch(&abort_flag, 1);
+      }
+      tc::fence_after_sync();
+      const int64_t pos = (t_begin + ie) * 128 + lt;  // entry id (page mode) / pool position (gather mode)
+#pragma unroll
+      for (int q = 0; q < QPC; ++q) {
+        uint32_t d[32];
+        tc::tmem_ld32(tc::taddr(tb, lane_base, dcol + 32 * q), d);
+        tc::tmem_wait_ld();
+        float sc = 0.0f;
+#pragma unroll
+        for (int hh = 0; hh < kIdxHeads; ++hh) sc = fmaf(hw[q][hh], fmaxf(__uint_as_float(d[hh]), 0.0f), sc);
+        sc += 0.0f;
+        const int qc = blockIdx.y * QPC + q;
+        const bool valid = kGather ? (gtab[ie * 128 + lt] >= 0) : (pos < nv[q]);
+        if (!ok) sc = -INFINITY;
+        if (kGather) {
+          if (pos < npos) a.scores[(int64_t)qc * a.stride + pos] = valid ? sc : __uint_as_float(kScoreInvalid);
+        } else if (valid) {
+          a.scores[(int64_t)qc * a.stride + pos] = sc;
+        }
+        if (valid) {
+          const uint32_t kk = order_key(sc);
+          klo[q] = min(klo[q], kk);
+          khi[q] = max(khi[q], kk);
+        }
+        if (!kGather && a.bmax) {
+          float m = valid ? sc : -INFINITY;
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          if ((lt & 7) == 0 && valid) a.bmax[(int64_t)qc * ((a.max_entries + 7) / 8) + pos / 8] = m;
+        }
+      }
+    }
+    if (have) {
+      // ---- own A buffer is free (previous MMA done): store, sync, issue
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r16[16];
@@ -251,81 +379,42 @@ __global__ void __launch_bounds__(kThreads) score_tc_kernel(ScoreArgs a) {
       tc::tmem_wait_st();
     }
     tc::fence_before_sync();
-    named_sync();
+    wg_sync(g);
     tc::fence_after_sync();
-    if (*reinterpret_cast<volatile int*>(&abort_flag)) break;  // uniform after the barrier
-    if (i < n_my && tid == 0) {
-      const uint32_t acol = (uint32_t)((i & 1) * kAcols);
-      const uint32_t dcol = (uint32_t)(2 * kAcols + (i & 1) * kN);
+    if (*reinterpret_cast<volatile int*>(&abort_flag)) break;  // uniform within the warpgroup
+    if (have && lt == 0) {
 #pragma unroll
       for (int ks = 0; ks < kIdxDim / 16; ++ks) {
         const uint64_t bdesc = tc::sdesc(tc::smem_u32(qtile) + ks * 256, 128, kIdxDim * 16);
         tc::mma_ts(tb + dcol, tb + acol + ks * 8, bdesc, kIdesc, ks > 0);
       }
-      tc::mma_commit(&mma_bar[i & 1]);
+      tc::mma_commit(&mma_bar[g]);
     }
-    if (i < n_my) last_issued = i;
-    if (i >= 1) {
-      // epilogue of tile i-1
-      const int e = i - 1;
-      const bool ok = tc::mbar_wait(&mma_bar[e & 1], (e >> 1) & 1, kSpin);
-      waited = e;
-      if (!ok) {
-        report(a.status, CSA2_ERR_TIMEOUT);
-        atomicExch(&abort_flag, 1);
-      }
-      tc::fence_after_sync();
-      const int64_t j = (t_begin + e) * 128 + tid;
-      const uint32_t dcol = (uint32_t)(2 * kAcols + (e & 1) * kN);
-#pragma unroll
-      for (int q = 0; q < QPC; ++q) {
-        uint32_t d[32];
-        tc::tmem_ld32(tc::taddr(tb, lane_base, dcol + 32 * q), d);
-        tc::tmem_wait_ld();
-        float s = 0.0f;
-#pragma unroll
-        for (int hh = 0; hh < kIdxHeads; ++hh) s = fmaf(hw[q][hh], fmaxf(__uint_as_float(d[hh]), 0.0f), s);
-        s += 0.0f;
-        if (j >= nv[q] || !ok) s = -INFINITY;
-        const int qc = blockIdx.y * QPC + q;
-        if (j < nv[q]) {
-          a.scores[(int64_t)qc * a.max_entries + j] = s;
-          const uint32_t kk = order_key(s);
-          klo[q] = min(klo[q], kk);
-          khi[q] = max(khi[q], kk);
-        }
-        if (a.bmax) {
-          float m = s;
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-          if ((tid & 7) == 0 && j < nv[q]) a.bmax[(int64_t)qc * ((a.max_entries + 7) / 8) + j / 8] = m;
-        }
-      }
-    }
+    if (have) last_issued = u;
   }
+  if (kGather) cp_wait<0>();  // no copies into this CTA's shared memory outlive it
 #pragma unroll
   for (int q = 0; q < QPC; ++q)
     fold_key_range(klo[q], khi[q], a.kmin + blockIdx.y * QPC + q, a.kmax + blockIdx.y * QPC + q);
-  // after an abort, let the last issued MMAs finish before TMEM is released
+  // after an abort, let the last issued MMA finish before TMEM is released
   if (last_issued > waited) {
-    if (!tc::mbar_wait(&mma_bar[last_issued & 1], (last_issued >> 1) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
+    if (!tc::mbar_wait(&mma_bar[g], last_issued & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
   }
   tc::fence_before_sync();
-  named_sync();
+  consumers_sync();
   if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
 }
 
 }  // namespace
 
-template <int kDtype, int QPC>
+template <int kDtype, int QPC, bool kGather>
 static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaStream_t stream) {
   using F = TileFmt<kDtype>;
-  size_t smem = 256 * 32 * QPC + (size_t)F::kStages * F::kSlotBytes;
-  // at most two CTAs per SM: their TMEM (256 columns each) then always fits
-  const size_t min_smem = (QPC == 1) ? 80 * 1024 : 120 * 1024;
-  if (smem < min_smem) smem = min_smem;
-  auto kern = score_tc_kernel<kDtype, QPC>;
+  size_t smem = 256 * 32 * QPC + (size_t)kStages * F::kSlotBytes;
+  // never more CTAs on an SM than its 512 TMEM columns hold (a blocked
+  // allocation would only idle the SM): 256 columns -> 2 CTAs, 512 -> 1
+  smem = std::max<size_t>(smem, (32 * QPC * 2 + 128) <= 256 ? 76 * 1024 : 116 * 1024);
+  auto kern = score_tc_kernel<kDtype, QPC, kGather>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   kern<<<dim3(splits, groups), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
@@ -333,22 +422,27 @@ static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaSt
 
 cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
                             const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
-                            int64_t max_entries, float* scores, float* bmax, uint32_t* kmin, uint32_t* kmax,
-                            int32_t* status, int num_sms, cudaStream_t stream) {
-  const int qpc = (Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) ? 4 : 1;
+                            int64_t max_entries, const int32_t* pool, float* scores, int64_t stride, float* bmax,
+                            uint32_t* kmin, uint32_t* kmax, int32_t* status, int num_sms, cudaStream_t stream) {
+  const bool gather = pool != nullptr;
+  const int qpc = (!gather && Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) ? 4 : 1;
   const int groups = nq / qpc;
-  const int64_t tiles = (max_entries + 127) / 128;
-  // enough CTAs for a few waves, at least 4 tiles each
-  const int64_t want = std::max<int64_t>(1, (int64_t)(qpc == 1 ? 4 : 2) * num_sms / std::max(groups, 1));
-  int64_t per = std::min<int64_t>(kMaxTilesPerCta, std::max<int64_t>(4, (tiles + want - 1) / want));
+  const int64_t tiles = gather ? ((int64_t)cfg.hsi_blocks * kHsiBlock + 127) / 128 : (max_entries + 127) / 128;
+  // enough CTAs for a couple of waves, at least 4 tiles each
+  const int64_t want = std::max<int64_t>(1, (int64_t)(qpc == 1 ? 2 : 1) * num_sms / std::max(groups, 1));
+  const int64_t cap = gather ? kMaxGatherTiles : kMaxTilesPerCta;
+  const int64_t per = std::min<int64_t>(cap, std::max<int64_t>(4, (tiles + want - 1) / want));
   const int splits = (int)((tiles + per - 1) / per);
   ScoreArgs a{q0, Tq, cfg.ratio, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
-              scores, bmax, kmin, kmax, status};
-  if (cfg.cache_dtype == CSA2_CACHE_FP4)
-    return qpc == 4 ? launch_one<CSA2_CACHE_FP4, 4>(a, groups, splits, stream)
-                    : launch_one<CSA2_CACHE_FP4, 1>(a, groups, splits, stream);
-  return qpc == 4 ? launch_one<CSA2_CACHE_BF16, 4>(a, groups, splits, stream)
-                  : launch_one<CSA2_CACHE_BF16, 1>(a, groups, splits, stream);
+              pool, cfg.hsi_blocks, scores, stride, bmax, kmin, kmax, status};
+  if (cfg.cache_dtype == CSA2_CACHE_FP4) {
+    if (gather) return launch_one<CSA2_CACHE_FP4, 1, true>(a, groups, splits, stream);
+    return qpc == 4 ? launch_one<CSA2_CACHE_FP4, 4, false>(a, groups, splits, stream)
+                    : launch_one<CSA2_CACHE_FP4, 1, false>(a, groups, splits, stream);
+  }
+  if (gather) return launch_one<CSA2_CACHE_BF16, 1, true>(a, groups, splits, stream);
+  return qpc == 4 ? launch_one<CSA2_CACHE_BF16, 4, false>(a, groups, splits, stream)
+                  : launch_one<CSA2_CACHE_BF16, 1, false>(a, groups, splits, stream);
 }
 
 }  // namespace csa2

@@ -22,11 +22,12 @@ cudaError_t launch_compress(const csa2_cfg& cfg, int B, int T, const uint16_t* x
 // Streaming multiprocessors of the current device (cached per device).
 int num_sms();
 
-// Tensor-core indexer scores (Full mode) for queries [q0, q0 + nq).
+// Tensor-core indexer scores for queries [q0, q0 + nq): every visible entry
+// (pool == NULL) or the entries of each query's HSI pool.
 cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
                             const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
-                            int64_t max_entries, float* scores, float* bmax, uint32_t* kmin, uint32_t* kmax,
-                            int32_t* status, int num_sms, cudaStream_t stream);
+                            int64_t max_entries, const int32_t* pool, float* scores, int64_t stride, float* bmax,
+                            uint32_t* kmin, uint32_t* kmax, int32_t* status, int num_sms, cudaStream_t stream);
 
 // Per-query workspace bytes of the indexer (scores + HSI block maxima).
 size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex);

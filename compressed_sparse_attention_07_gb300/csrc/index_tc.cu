@@ -28,10 +28,15 @@
 namespace csa2 {
 namespace {
 
-constexpr int kWG = 2;                     // consumer warpgroups
-constexpr int kConsumers = 128 * kWG;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp (page mode)
-constexpr int kStages = 4;                 // ring slots; warpgroup g owns slots g, g + 2 in gather mode
+// Consumer warpgroups: four on single-query FP4 tiles (latency-bound decode
+// and epilogue), two otherwise (TMEM and shared-memory budget).
+template <int kDtype, int QPC>
+struct Shape {
+  static constexpr int kWG = (QPC == 1 && kDtype == CSA2_CACHE_FP4) ? 4 : 2;
+  static constexpr int kConsumers = 128 * kWG;
+  static constexpr int kThreads = kConsumers + 32;  // + one producer warp (page mode)
+  static constexpr int kStages = 2 * kWG;           // ring slots; warpgroup g owns slots g, g + kWG
+};
 constexpr uint32_t kSpin = 1u << 26;
 constexpr int kMaxTilesPerCta = 512;
 constexpr int kMaxGatherTiles = 32;        // gather mode: resolved positions held in shared memory
@@ -94,13 +99,17 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Barrier of one warpgroup (ids 1, 2) or of all consumers (id 3).
+// Barrier of one warpgroup (ids 1..4) or of all consumers (id 5).
 __device__ __forceinline__ void wg_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 3, %0;" ::"n"(kConsumers) : "memory"); }
+__device__ __forceinline__ void consumers_sync(int n) { asm volatile("bar.sync 5, %0;" ::"r"(n) : "memory"); }
 
 template <int kDtype, int QPC, bool kGather>
-__global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kernel(ScoreArgs a) {
   using F = TileFmt<kDtype>;
+  constexpr int kWG = Shape<kDtype, QPC>::kWG;
+  constexpr int kConsumers = Shape<kDtype, QPC>::kConsumers;
+  constexpr int kThreads = Shape<kDtype, QPC>::kThreads;
+  constexpr int kStages = Shape<kDtype, QPC>::kStages;
   constexpr int kN = 32 * QPC;                    // MMA N: QPC queries x 32 heads
   constexpr int kAcols = 64;                      // 128 channels of f16 pairs
   constexpr int kTmemCols = (kWG * kAcols + kWG * kN) <= 256 ? 256 : 512;
@@ -236,12 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(ScoreArgs a) {
   }
 
   // -------------------------------------------------------------- consumers
-  const int g = warp >> 2;               // warpgroup: tiles g, g + 2, ...
+  const int g = warp >> 2;               // warpgroup: tiles g, g + kWG, ...
   const int lt = tid & 127;              // entry of the tile, TMEM lane
   const uint32_t lane_base = 32 * (warp & 3);
   const uint32_t acol = (uint32_t)(g * kAcols);
   const uint32_t dcol = (uint32_t)(kWG * kAcols + g * kN);
-  const int n_own = n_my > g ? (n_my - g + 1) / 2 : 0;
+  const int n_own = n_my > g ? (n_my - g + kWG - 1) / kWG : 0;
   uint32_t klo[QPC], khi[QPC];
 #pragma unroll
   for (int q = 0; q < QPC; ++q) {
@@ -253,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(ScoreArgs a) {
   // gather mode: copy this thread's entry of own tile u into its slot
   auto gather = [&](int u) {
     if (kGather && u < n_own) {
-      const int i = g + 2 * u;
+      const int i = g + kWG * u;
       uint8_t* slot = ring + (size_t)(i % kStages) * F::kSlotBytes;
       const int32_t e = gtab[i * 128 + lt];
       if (e >= 0) {
@@ -278,56 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(ScoreArgs a) {
   int last_issued = -1, waited = -1;  // own tile counters
   int u = 0;
   for (; u <= n_own; ++u) {
-    const int i = g + 2 * u;  // CTA-local tile index
+    const int i = g + kWG * u;  // CTA-local tile index
     const bool have = u < n_own;
-    uint32_t av[64];
-    if (have) {
-      // ---- fetch tile i (own) and decode this thread's entry into registers
-      const int s = i % kStages;
-      if (kGather) {
-        gather(u + 1);
-        cp_wait<1>();
-      } else if (!tc::mbar_wait(&full_bar[s], (i / kStages) & 1, kSpin)) {
-        atomicExch(&abort_flag, 1);
-      }
-      const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
-      const bool present = !kGather || gtab[i * 128 + lt] >= 0;
-      if (kDtype == CSA2_CACHE_FP4) {
-        uint4 cw[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          cw[c] = *reinterpret_cast<const uint4*>(slot + h * kIdxFp4Data + (c * kPage + sl) * 16);
-        const uint2 sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * kIdxFp4Scales + sl * 8);
-        if (!kGather) tc::mbar_arrive(&empty_bar[s]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t w4[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
-            const uint32_t sb = ((gg < 4 ? sc.x : sc.y) >> (8 * (gg & 3))) & 0xFFu;
-            const uint32_t s2 = f16x2_scale(sb);
-            uint32_t h4[4];
-            e2m1x8_to_f16x2(w4[q], h4);
-#pragma unroll
-            for (int by = 0; by < 4; ++by) av[c * 16 + q * 4 + by] = present ? hmul2(h4[by], s2) : 0u;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(slot + h * kIdxBf16Data + (c * kPage + sl) * 16);
-          av[4 * c] = present ? v.x : 0u;
-          av[4 * c + 1] = present ? v.y : 0u;
-          av[4 * c + 2] = present ? v.z : 0u;
-          av[4 * c + 3] = present ? v.w : 0u;
-        }
-        if (!kGather) tc::mbar_arrive(&empty_bar[s]);
-      }
-    }
     if (u >= 1) {
-      // ---- epilogue of own tile u-1 (its MMA ran while this tile was fetched)
-      const int e = u - 1, ie = g + 2 * e;
+      // ---- epilogue of own tile u-1; afterwards the A and D buffers are free
+      const int e = u - 1, ie = g + kWG * e;
       const bool ok = tc::mbar_wait(&mma_bar[g], e & 1, kSpin);
       waited = e;
       if (!ok) {
@@ -368,13 +332,53 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(ScoreArgs a) {
       }
     }
     if (have) {
-      // ---- own A buffer is free (previous MMA done): store, sync, issue
+      // ---- fetch own tile i and decode this thread's entry straight into TMEM
+      const int s = i % kStages;
+      if (kGather) {
+        gather(u + 1);
+        cp_wait<1>();
+      } else if (!tc::mbar_wait(&full_bar[s], (i / kStages) & 1, kSpin)) {
+        atomicExch(&abort_flag, 1);
+      }
+      const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
+      const bool present = !kGather || gtab[i * 128 + lt] >= 0;
+      if (kDtype == CSA2_CACHE_FP4) {
+        uint4 cw[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r16[16];
+        for (int c = 0; c < 4; ++c)
+          cw[c] = *reinterpret_cast<const uint4*>(slot + h * kIdxFp4Data + (c * kPage + sl) * 16);
+        const uint2 sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * kIdxFp4Scales + sl * 8);
+        if (!kGather) tc::mbar_arrive(&empty_bar[s]);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) r16[j] = av[16 * c + j];
-        tc::tmem_st16(tc::taddr(tb, lane_base, acol + 16 * c), r16);
+        for (int c = 0; c < 4; ++c) {  // 32 channels -> 16 TMEM columns
+          const uint32_t w4[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
+          uint32_t r16[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
+            const uint32_t s2 = f16x2_scale(((gg < 4 ? sc.x : sc.y) >> (8 * (gg & 3))) & 0xFFu);
+            uint32_t h4[4];
+            e2m1x8_to_f16x2(w4[q], h4);
+#pragma unroll
+            for (int by = 0; by < 4; ++by) r16[q * 4 + by] = present ? hmul2(h4[by], s2) : 0u;
+          }
+          tc::tmem_st16(tc::taddr(tb, lane_base, acol + 16 * c), r16);
+        }
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t r16[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(slot + h * kIdxBf16Data + ((4 * c4 + c) * kPage + sl) * 16);
+            r16[4 * c] = present ? v.x : 0u;
+            r16[4 * c + 1] = present ? v.y : 0u;
+            r16[4 * c + 2] = present ? v.z : 0u;
+            r16[4 * c + 3] = present ? v.w : 0u;
+          }
+          tc::tmem_st16(tc::taddr(tb, lane_base, acol + 16 * c4), r16);
+        }
+        if (!kGather) tc::mbar_arrive(&empty_bar[s]);
       }
       tc::tmem_wait_st();
     }
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(ScoreArgs a) {
     if (!tc::mbar_wait(&mma_bar[g], last_issued & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
   }
   tc::fence_before_sync();
-  consumers_sync();
+  consumers_sync(kConsumers);
   if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
 }
 
@@ -410,13 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_kernel(ScoreArgs a) {
 template <int kDtype, int QPC, bool kGather>
 static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaStream_t stream) {
   using F = TileFmt<kDtype>;
-  size_t smem = 256 * 32 * QPC + (size_t)kStages * F::kSlotBytes;
-  // never more CTAs on an SM than its 512 TMEM columns hold (a blocked
-  // allocation would only idle the SM): 256 columns -> 2 CTAs, 512 -> 1
-  smem = std::max<size_t>(smem, (32 * QPC * 2 + 128) <= 256 ? 76 * 1024 : 116 * 1024);
+  using Sh = Shape<kDtype, QPC>;
+  size_t smem = 256 * 32 * QPC + (size_t)Sh::kStages * F::kSlotBytes;
+  // one CTA per SM: its TMEM allocation may take all 512 columns
+  smem = std::max<size_t>(smem, 116 * 1024);
   auto kern = score_tc_kernel<kDtype, QPC, kGather>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  kern<<<dim3(splits, groups), kThreads, smem, stream>>>(a);
+  kern<<<dim3(splits, groups), Sh::kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -421,6 +421,295 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
   if (warp == 0) tc::tmem_dealloc(tb, tmem_cols);
 }
 
+
+// ---------------------------------------------------------------------------
+// Tile-split variant for few query tokens (decode).  One CTA per (query
+// token, group of 16 heads, 128-row tile); the tiles of a query form a thread
+// block cluster.  Each CTA gathers and decodes only its tile, keeps the four
+// decoded 128-channel chunks in shared memory for both products, and computes
+// a partial softmax (max m_t, sum l_t per head) with O_t = sum_e e^(l-m_t) c_e.
+// The partials are merged through distributed shared memory: M = max_t m_t,
+// L = sum_t e^(m_t-M) l_t, out = sum_t e^(m_t-M) O_t / L, each CTA of the
+// cluster reducing one slice of the output (deterministic order over t).
+constexpr int kSplitHG = 16;
+constexpr int kSplitCPT = kSplitHG / 4;
+constexpr size_t kSplitSmem = 2 * (size_t)kStageBytes + 4 * (size_t)kCBytes + kSplitHG * kDim * 2 + kSplitHG * 128 * 2 +
+                              128 * 4 + 2 * kSplitHG * 4;
+
+template <int kDtype>
+__global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
+  constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
+  constexpr int HG = kSplitHG, CPT = kSplitCPT;
+  const int n_tiles = a.tiles_main + a.tiles_win;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stage = smem;                                   // 2 staging slots
+  uint8_t* ctile = stage + 2 * kStageBytes;                // 4 decoded chunks [128 rows x 128 ch] f16
+  uint8_t* qs = ctile + 4 * kCBytes;                       // Q [16 heads x 512] f16, K-major
+  uint8_t* pt = qs + HG * kDim * 2;                        // P^T [16 heads x 128 rows] f16, K-major
+  int32_t* src = reinterpret_cast<int32_t*>(pt + HG * 128 * 2);  // [128]
+  float* ml = reinterpret_cast<float*>(src + 128);         // m[16] (log2 domain), l[16]
+  float* ot = reinterpret_cast<float*>(ctile);             // after phase B: scaled O_t [512 ch][16 heads]
+  __shared__ __align__(8) uint64_t cdone;
+  __shared__ uint32_t tmem_base;
+  __shared__ float red[4][HG];
+  __shared__ float m_s[HG], alpha[HG];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127, p = tid >> 7, quad = warp & 3;
+  const uint32_t lane_base = 32 * quad;
+  const int t = (int)tc::cluster_rank();                   // tile of this CTA
+  const int hg = blockIdx.x / n_tiles, qi = blockIdx.y, b = qi / a.Tq;
+  const bool fp4_tile = kMainFp4 && t < a.tiles_main;
+  const int n_units = fp4_tile ? 1 : 4;
+
+  // ---- set-up: row sources of this tile, Q, barrier, TMEM (S^T 16 cols, O^T 4 x 16)
+  if (tid < 128) src[tid] = slot_source(a, qi, b, t * 128 + tid);
+  for (int i = tid; i < HG * kDim / 8; i += kThreads) {
+    const int h = (8 * i) / kDim, kk = (8 * i) % kDim;
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)qi * kHeads + hg * HG + h) * kDim + kk));
+    *reinterpret_cast<uint4*>(qs + tc::kmajor_off(h, kk, kDim)) =
+        make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+  }
+  if (tid == 0) {
+    tc::mbar_init(&cdone, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 128);
+    tc::tmem_relinquish();
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = tmem_base;
+
+  // quarter p of row r of unit u (whole FP4 rows, or 128-channel chunk u)
+  auto gather = [&](int u) {
+    if (u < n_units) {
+      uint8_t* slot = stage + (u & 1) * kStageBytes;
+      const int32_t sidx = src[r];
+      if (sidx >= 0) {
+        const int64_t page = sidx / kPage;
+        const int sl = sidx % kPage;
+        if (fp4_tile) {
+          const uint8_t* g = a.mc.data + page * kMainFp4Data + sl * (kDim / 2);
+          uint8_t* d = slot + r * kStageRow;
+#pragma unroll
+          for (int j = p; j < 16; j += 4) cp16(d + 16 * j, g + 16 * j);
+          if (p < 2) cp16(d + 256 + 16 * p, a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16) + 16 * p);
+        } else {
+          const uint8_t* g = a.mc.data + page * kMainBf16Data + sl * (kDim * 2) + 256 * u;
+          uint8_t* d = slot + r * kStageRowChunk;
+#pragma unroll
+          for (int j = p; j < 16; j += 4) cp16(d + 16 * j, g + 16 * j);
+        }
+      } else if (sidx <= -2) {
+        const uint16_t* g = a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx)) * kDim + 128 * u;
+        uint8_t* d = slot + r * kStageRowChunk;
+#pragma unroll
+        for (int j = p; j < 16; j += 4) cp16(d + 16 * j, g + 8 * j);
+      }
+    }
+    cp_commit();
+  };
+  gather(0);
+  gather(1);
+
+  // ---- phase A: decode chunk c into C[c], S^T += C[c] . Q_c^T
+  constexpr uint32_t kIdescS = tc::idesc_f16(128, HG, false, false, false, false);
+  constexpr uint32_t kIdescO = tc::idesc_f16(128, HG, false, false, true, false);
+  const int32_t sidx = src[r];
+  for (int c = 0; c < 4; ++c) {
+    const int u = fp4_tile ? 0 : c;
+    if (!fp4_tile || c == 0) {
+      cp_wait<1>();
+      __syncthreads();
+    }
+    const uint8_t* slot = stage + (u & 1) * kStageBytes;
+    uint32_t av[16];
+    if (sidx == -1) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) av[j] = 0u;
+    } else if (fp4_tile) {
+      const uint8_t* row = slot + r * kStageRow;
+      const uint32_t sc2b = *reinterpret_cast<const uint16_t*>(row + 256 + 8 * c + 2 * p);
+      const uint4 cw = *reinterpret_cast<const uint4*>(row + 64 * c + 16 * p);
+      const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+      const uint32_t s_lo = f16x2_scale(sc2b & 0xFFu), s_hi = f16x2_scale(sc2b >> 8);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t h4[4];
+        e2m1x8_to_f16x2(w4[q], h4);
+#pragma unroll
+        for (int by = 0; by < 4; ++by) av[4 * q + by] = hmul2(h4[by], q < 2 ? s_lo : s_hi);
+      }
+    } else {
+      const uint8_t* row = slot + r * kStageRowChunk + 64 * p;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * j);
+        av[4 * j] = bf16x2_to_f16x2(v.x);
+        av[4 * j + 1] = bf16x2_to_f16x2(v.y);
+        av[4 * j + 2] = bf16x2_to_f16x2(v.z);
+        av[4 * j + 3] = bf16x2_to_f16x2(v.w);
+      }
+    }
+    uint8_t* ct = ctile + c * kCBytes;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 32 * p + 8 * j, 128)) =
+          make_uint4(av[4 * j], av[4 * j + 1], av[4 * j + 2], av[4 * j + 3]);
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (!fp4_tile) gather(c + 2);  // every thread is done with the slot of unit c
+    if (tid == 0) {
+      const uint32_t cbase = tc::smem_u32(ct);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t ad = tc::sdesc(cbase + ks * 256, 128, 2048);
+        const uint64_t bd = tc::sdesc(tc::smem_u32(qs) + (c * 16 + ks * 2) * 128, 128, kDim * 16);
+        tc::mma_ss(tb, ad, bd, kIdescS, (c > 0 || ks > 0) ? 1u : 0u);
+      }
+      if (c == 3) tc::mma_commit(&cdone);
+    }
+  }
+  cp_wait<0>();
+  bool ok = tc::mbar_wait(&cdone, 0, kSpin);
+  tc::fence_after_sync();
+
+  // ---- partial softmax over this tile's rows
+  const float sc2 = a.scale * kLog2e;
+  const bool valid = sidx != -1;
+  float v[CPT];
+  {
+    uint32_t w[CPT];
+    tc::tmem_ld_n<CPT>(tc::taddr(tb, lane_base, p * CPT), w);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) v[j] = valid ? __uint_as_float(w[j]) * sc2 : -INFINITY;
+  }
+  float m[CPT];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    m[j] = v[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], o));
+  }
+  if (lane == 0)
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) red[quad][p * CPT + j] = m[j];
+  __syncthreads();
+  if (tid < HG) m_s[tid] = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
+  __syncthreads();
+  float sum[CPT];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const float mh = m_s[p * CPT + j];
+    const float pr = (valid && mh != -INFINITY) ? exp2f(v[j] - mh) : 0.0f;
+    *reinterpret_cast<__half*>(pt + tc::kmajor_off(p * CPT + j, r, 128)) = __float2half_rn(pr);
+    sum[j] = pr;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], o);
+  }
+  __syncthreads();  // red (maxima) read by every thread above
+  if (lane == 0)
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) red[quad][p * CPT + j] = sum[j];
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid < HG) {
+    ml[tid] = m_s[tid];
+    ml[HG + tid] = red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
+  }
+  // ---- phase B: O^T[c] = C[c]^T . P^T for the four chunks
+  if (tid == 0) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t cbase = tc::smem_u32(ctile + c * kCBytes);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t ad = tc::sdesc(cbase + ks * 2 * 2048, 2048, 128);
+        const uint64_t bd = tc::sdesc(tc::smem_u32(pt) + ks * 256, 128, 2048);
+        tc::mma_ss(tb + 32 + 16 * c, ad, bd, kIdescO, ks > 0 ? 1u : 0u);
+      }
+    }
+    tc::mma_commit(&cdone);
+  }
+  // ---- merge the tiles' (m, l): every CTA of the cluster has written its own
+  tc::cluster_sync();
+  const int n = n_tiles;
+  if (tid < HG) {
+    const uint32_t ml_addr = tc::smem_u32(ml);
+    float M = -INFINITY;
+    for (int k2 = 0; k2 < n; ++k2) M = fmaxf(M, tc::ld_dsmem(tc::map_rank(ml_addr + 4 * tid, k2)));
+    float L = 0.0f;
+    for (int k2 = 0; k2 < n; ++k2) {
+      const float mk = tc::ld_dsmem(tc::map_rank(ml_addr + 4 * tid, k2));
+      const float lk = tc::ld_dsmem(tc::map_rank(ml_addr + 4 * (HG + tid), k2));
+      if (mk != -INFINITY) L += exp2f(mk - M) * lk;
+    }
+    alpha[tid] = (L > 0.0f && ml[tid] != -INFINITY) ? exp2f(ml[tid] - M) / L : 0.0f;
+    if (t == 0 && a.lse)
+      a.lse[(int64_t)qi * kHeads + hg * HG + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  }
+  ok = tc::mbar_wait(&cdone, 1, kSpin) && ok;
+  tc::fence_after_sync();
+  __syncthreads();
+  // scaled O_t -> shared memory [channel][head] (the C tiles are no longer read)
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[CPT];
+    tc::tmem_ld_n<CPT>(tc::taddr(tb, lane_base, 32 + 16 * c + p * CPT), w);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) ot[(c * 128 + r) * HG + p * CPT + j] = ok ? __uint_as_float(w[j]) * alpha[p * CPT + j] : 0.0f;
+  }
+  if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
+  tc::cluster_sync();
+  // ---- this CTA's slice of the output: sum over the cluster's tiles
+  {
+    const int E = HG * kDim;
+    const int lo = t * E / n, hi = (t + 1) * E / n;
+    const uint32_t ot_addr = tc::smem_u32(ot);
+    for (int e = lo + tid; e < hi; e += kThreads) {
+      const int h = e / kDim, ch = e % kDim;
+      const uint32_t off = ot_addr + 4 * (ch * HG + h);
+      float acc = 0.0f;
+      for (int k2 = 0; k2 < n; ++k2) acc += tc::ld_dsmem(tc::map_rank(off, k2));
+      a.out[((int64_t)qi * kHeads + hg * HG + h) * kDim + ch] = acc;
+    }
+  }
+  tc::fence_before_sync();
+  tc::cluster_sync();  // peers may still be reading this CTA's shared memory until here
+  if (warp == 0) tc::tmem_dealloc(tb, 128);
+}
+
+template <int kDtype>
+cudaError_t launch_split(const AttArgs& a, int Q, cudaStream_t stream) {
+  const int n_tiles = a.tiles_main + a.tiles_win;
+  auto kern = attend_split_kernel<kDtype>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSplitSmem);
+  if (n_tiles > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_tiles * (kHeads / kSplitHG), Q);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSplitSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = n_tiles;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 template <int kDtype, int HG>
 size_t att_smem(int n_tiles, int stages = 2) {
   const int nslot = n_tiles * 128;
@@ -475,6 +764,15 @@ cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q,
   AttArgs a{Tq, cfg.topk, cfg.window, S, (cfg.topk + 127) / 128, (cfg.window + 127) / 128, q, view_of(main_c),
             n_entries, (int64_t)main_c.max_pages * kPage, topk, swa, swa_len, swa_pos0, q_pos, scale, out, lse,
             status};
+  // few query tokens: split the rows of every query over a cluster of CTAs
+  // (one per 128-row tile); many: one CTA per query and head group
+  const int n_tiles = a.tiles_main + a.tiles_win;
+  if ((int64_t)Q * 4 * n_tiles <= 8 * (int64_t)num_sms() && n_tiles <= 16) {
+    cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_split<CSA2_CACHE_FP4>(a, Q, stream)
+                                                      : launch_split<CSA2_CACHE_BF16>(a, Q, stream);
+    if (e == cudaSuccess) return e;
+    (void)cudaGetLastError();  // cluster shape not schedulable here: use the per-query kernel
+  }
   if (cfg.cache_dtype == CSA2_CACHE_FP4) return launch_dtype<CSA2_CACHE_FP4>(a, Q, num_sms(), stream);
   return launch_dtype<CSA2_CACHE_BF16>(a, Q, num_sms(), stream);
 }

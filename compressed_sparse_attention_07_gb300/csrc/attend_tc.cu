@@ -448,7 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
   uint8_t* pt = qs + HG * kDim * 2;                        // P^T [16 heads x 128 rows] f16, K-major
   int32_t* src = reinterpret_cast<int32_t*>(pt + HG * 128 * 2);  // [128]
   float* ml = reinterpret_cast<float*>(src + 128);         // m[16] (log2 domain), l[16]
-  float* ot = reinterpret_cast<float*>(ctile);             // after phase B: scaled O_t [512 ch][16 heads]
   __shared__ __align__(8) uint64_t cdone;
   __shared__ uint32_t tmem_base;
   __shared__ float red[4][HG];
@@ -640,19 +639,28 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
     }
     tc::mma_commit(&cdone);
   }
-  // ---- merge the tiles' (m, l): every CTA of the cluster has written its own
+  // ---- merge the tiles' (m, l); every CTA of the cluster has written its own,
+  // and every CTA is past its gathers, so the staging slots are free
   tc::cluster_sync();
   const int n = n_tiles;
   if (tid < HG) {
     const uint32_t ml_addr = tc::smem_u32(ml);
-    float M = -INFINITY;
-    for (int k2 = 0; k2 < n; ++k2) M = fmaxf(M, tc::ld_dsmem(tc::map_rank(ml_addr + 4 * tid, k2)));
-    float L = 0.0f;
-    for (int k2 = 0; k2 < n; ++k2) {
-      const float mk = tc::ld_dsmem(tc::map_rank(ml_addr + 4 * tid, k2));
-      const float lk = tc::ld_dsmem(tc::map_rank(ml_addr + 4 * (HG + tid), k2));
-      if (mk != -INFINITY) L += exp2f(mk - M) * lk;
+    float mk[16], lk[16];
+#pragma unroll
+    for (int k2 = 0; k2 < 16; ++k2) {
+      if (k2 < n) {
+        mk[k2] = tc::ld_dsmem(tc::map_rank(ml_addr + 4 * tid, k2));
+        lk[k2] = tc::ld_dsmem(tc::map_rank(ml_addr + 4 * (HG + tid), k2));
+      }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k2 = 0; k2 < 16; ++k2)
+      if (k2 < n) M = fmaxf(M, mk[k2]);
+    float L = 0.0f;
+#pragma unroll
+    for (int k2 = 0; k2 < 16; ++k2)
+      if (k2 < n && mk[k2] != -INFINITY) L += exp2f(mk[k2] - M) * lk[k2];
     alpha[tid] = (L > 0.0f && ml[tid] != -INFINITY) ? exp2f(ml[tid] - M) / L : 0.0f;
     if (t == 0 && a.lse)
       a.lse[(int64_t)qi * kHeads + hg * HG + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
@@ -660,32 +668,39 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
   ok = tc::mbar_wait(&cdone, 1, kSpin) && ok;
   tc::fence_after_sync();
   __syncthreads();
-  // scaled O_t -> shared memory [channel][head] (the C tiles are no longer read)
+  // ---- push the scaled partial output to the CTA owning each output slice:
+  // element e = head * 512 + channel belongs to CTA e / slice and lands in its
+  // staging area at [sender tile][e - owner start]
+  const int E = HG * kDim;
+  const int slice = (E + n - 1) / n;
+  const uint32_t recv = tc::smem_u32(stage);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t w[CPT];
     tc::tmem_ld_n<CPT>(tc::taddr(tb, lane_base, 32 + 16 * c + p * CPT), w);
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int j = 0; j < CPT; ++j) ot[(c * 128 + r) * HG + p * CPT + j] = ok ? __uint_as_float(w[j]) * alpha[p * CPT + j] : 0.0f;
+    for (int j = 0; j < CPT; ++j) {
+      const int h = p * CPT + j, e = h * kDim + c * 128 + r;
+      const int o = e / slice;
+      const float val = ok ? __uint_as_float(w[j]) * alpha[h] : 0.0f;
+      tc::st_dsmem(tc::map_rank(recv + 4 * (t * slice + (e - o * slice)), o), val);
+    }
   }
   if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
+  tc::fence_before_sync();
   tc::cluster_sync();
-  // ---- this CTA's slice of the output: sum over the cluster's tiles
+  // ---- this CTA's slice: sum the tiles' partials in tile order
   {
-    const int E = HG * kDim;
-    const int lo = t * E / n, hi = (t + 1) * E / n;
-    const uint32_t ot_addr = tc::smem_u32(ot);
+    const float* rv = reinterpret_cast<const float*>(stage);
+    const int lo = t * slice, hi = min(E, lo + slice);
     for (int e = lo + tid; e < hi; e += kThreads) {
-      const int h = e / kDim, ch = e % kDim;
-      const uint32_t off = ot_addr + 4 * (ch * HG + h);
       float acc = 0.0f;
-      for (int k2 = 0; k2 < n; ++k2) acc += tc::ld_dsmem(tc::map_rank(off, k2));
+      for (int k2 = 0; k2 < n; ++k2) acc += rv[k2 * slice + (e - lo)];
+      const int h = e / kDim, ch = e % kDim;
       a.out[((int64_t)qi * kHeads + hg * HG + h) * kDim + ch] = acc;
     }
   }
-  tc::fence_before_sync();
-  tc::cluster_sync();  // peers may still be reading this CTA's shared memory until here
   if (warp == 0) tc::tmem_dealloc(tb, 128);
 }
 

@@ -6,12 +6,16 @@ decoder workloads), and sparse attention over top-k plus the window.  The
 default workload is the batch-8 decode step at 32768 tokens of context with
 2:1 compression into an FP4 cache (16384 entries per sequence).
 
-Timing: W warm-up steps, then K timed steps; before each step a 256 MiB
-buffer is written so that the step starts with a cold L2 (the inputs are
-smaller than L2), and each step is bracketed by CUDA events on the launching
-stream (per-stage events give the per-kernel durations used for the
-roofline).  Under torchrun every rank runs its own batch (weak scaling, no
-data-path collective); rank 0 prints one JSON line with the max over ranks.
+Timing: W warm-up steps launched eagerly; then the step is captured once as a
+CUDA graph and K replays are timed, each bracketed by CUDA events on the
+launching stream.  Before every step a 256 MiB buffer is written so that the
+step starts with a cold L2 (the inputs are smaller than L2).  The per-stage
+durations used for the roofline come from one graph per stage replayed back
+to back after the same flush; the eager launch of the step through the Python
+API is timed too (eager_ms_per_step), and the end-to-end leg runs eagerly
+with the inputs copied from pinned host memory and the output copied back.
+Under torchrun every rank runs its own batch (weak scaling, no data-path
+collective); rank 0 prints one JSON line with the max over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 """
@@ -154,6 +158,19 @@ class StepBase:
     def inputs_host(self):
         return self.h
 
+    def step(self, events=None, d=None):
+        """Run the stages in order, recording events[i] before stage i and
+        events[-1] after the last."""
+        calls = self.calls(d or self.d)
+        ev = events or [None] * (len(calls) + 1)
+        if ev[0] is not None:
+            ev[0].record()
+        for i, c in enumerate(calls):
+            c()
+            if ev[i + 1] is not None:
+                ev[i + 1].record()
+        return self.out
+
 
 class DecodeStep(StepBase):
     """One decode step of one CSA2 layer in Full mode: compress the step's r
@@ -195,24 +212,16 @@ class DecodeStep(StepBase):
         self.units = B
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N}
 
-    def step(self, events=None, d=None):
-        csa, d = self.csa, (d or self.d)
-        ev = events or [None] * 4
-        if ev[0] is not None:
-            ev[0].record()
-        csa.compress(self.cfg, d["x"], d["pos0"], self.merge_w, self.w_idx, self.main, self.idx, self.n_entries,
-                     status=self.status)
-        if ev[1] is not None:
-            ev[1].record()
-        csa.index_topk(self.cfg, d["q_idx"], d["q_pos"], self.idx, self.n_entries, self.N, self.topk, self.ws,
-                       pool_out=self.pool, status=self.status)
-        if ev[2] is not None:
-            ev[2].record()
-        csa.attend(self.cfg, d["q"], self.main, self.n_entries, self.topk, d["swa"], d["swa_len"], d["swa_pos0"],
-                   d["q_pos"], self.out, status=self.status)
-        if ev[3] is not None:
-            ev[3].record()
-        return self.out
+    def calls(self, d):
+        csa, st = self.csa, self.status
+        return [
+            lambda: csa.compress(self.cfg, d["x"], d["pos0"], self.merge_w, self.w_idx, self.main, self.idx,
+                                 self.n_entries, status=st),
+            lambda: csa.index_topk(self.cfg, d["q_idx"], d["q_pos"], self.idx, self.n_entries, self.N, self.topk,
+                                   self.ws, pool_out=self.pool, status=st),
+            lambda: csa.attend(self.cfg, d["q"], self.main, self.n_entries, self.topk, d["swa"], d["swa_len"],
+                               d["swa_pos0"], d["q_pos"], self.out, status=st),
+        ]
 
 
 class PrefillStep(StepBase):
@@ -261,7 +270,7 @@ class PrefillStep(StepBase):
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "query_tokens": Tq, "entries": self.N,
                           "index_pairs": pairs}
 
-    step = DecodeStep.step
+    calls = DecodeStep.calls
 
 
 class GroupStep(StepBase):
@@ -317,21 +326,18 @@ class GroupStep(StepBase):
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N, "layers": len(self.layers),
                           "unit": "query token through the 20-layer group"}
 
-    def step(self, events=None, d=None):
-        csa, d = self.csa, (d or self.d)
-        ev = events or [None] * (len(self.layers) + 1)
-        if ev[0] is not None:
-            ev[0].record()
+    def calls(self, d):
+        csa = self.csa
         mode_of = {"full": csa.MODE_FULL, "reindex": csa.MODE_REINDEX, "reuse": csa.MODE_REUSE}
-        for i, (l, m) in enumerate(self.layers):
+        out = []
+        for l, m in self.layers:
             kw = {}
             if m == "full":
                 kw = dict(x=d["x"], pos0=d["pos0"], merge_w=self.merge_w, w_idx=self.w_idx)
-            csa.layer(self.cfg, mode_of[m], self.state, d["q_pos"], d["q%d" % l], d["swa%d" % l], d["swa_len"],
-                      d["swa_pos0"], self.outs[l], q_idx=d.get("q_idx%d" % l), **kw)
-            if ev[i + 1] is not None:
-                ev[i + 1].record()
-        return self.out
+            out.append(lambda l=l, m=m, kw=kw: csa.layer(
+                self.cfg, mode_of[m], self.state, d["q_pos"], d["q%d" % l], d["swa%d" % l], d["swa_len"],
+                d["swa_pos0"], self.outs[l], q_idx=d.get("q_idx%d" % l), **kw))
+        return out
 
 
 def make_step(name, device, seed_offset=0):
@@ -531,24 +537,62 @@ def main():
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0, "device status %d" % int(step.status.item())
 
+    # the step and each of its stages captured once as CUDA graphs (decode
+    # steps are a handful of short kernels: replaying a graph removes the
+    # host-side launch gaps between them)
+    calls = step.calls(step.d)
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        for c in calls:
+            c()
+    g_stage = []
+    for c in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            c()
+        g_stage.append(g)
+    for _ in range(2):
+        flush.fill_(2)
+        g_step.replay()
+    torch.cuda.synchronize()
+
     clocks = ClockSampler(local)
     clocks.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for k in range(args.steps):
         flush.fill_(k & 0xFF)
-        step.step(events=evs[k])
+        evs[k][0].record()
+        g_step.replay()
+        evs[k][1].record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(ws)
     clk = clocks.stop()
-    step_ms = [e[0].elapsed_time(e[nst]) for e in evs]
-    stage_ms = {s: statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, s in enumerate(step.stages)}
+    step_ms = [a.elapsed_time(b) for a, b in evs]
     total_ms = max_over_ranks(sum(step_ms), ws)
     ms_per_step = total_ms / args.steps
     value = ws * step.units * args.steps / (total_ms / 1e3)
+
+    # per-stage durations (stage graphs back to back after the flush) and
+    # the same step launched eagerly through the Python API
+    n_stage = min(args.steps, 50)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(n_stage)]
+    for k in range(n_stage):
+        flush.fill_(k & 0xFF)
+        for i, g in enumerate(g_stage):
+            sev[k][i].record()
+            g.replay()
+        sev[k][nst].record()
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(n_stage)]
+    for k in range(n_stage):
+        flush.fill_(k & 0xFF)
+        step.step(events=eev[k])
+    torch.cuda.synchronize()
+    stage_ms = {s: statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in sev) for i, s in enumerate(step.stages)}
+    eager_ms = statistics.fmean(e[0].elapsed_time(e[nst]) for e in eev)
 
     # end to end through the Python API with host buffers: H2D of the step's
     # inputs from pinned memory, the step, D2H of the attention output
@@ -600,8 +644,9 @@ def main():
                 "config": dict({"workload": step.wl.name}, **step.cfg_extra,
                                **{"cache": step.wl.cache, "topk": step.wl.topk, "window": step.wl.window,
                                   "hsi": step.wl.hsi, "operands": "f16 tensor-core operands, fp32 accumulate",
-                                  "l2": "flushed before every step (256 MiB write)"}),
-                "stage_ms": stage_ms, "wall_s": wall,
+                                  "l2": "flushed before every step (256 MiB write)",
+                                  "launch": "CUDA graph of the step, captured once and replayed per step"}),
+                "stage_ms": stage_ms, "eager_ms_per_step": eager_ms, "wall_s": wall,
                 "roofline": roof, "cpu_baseline": cpu,
                 "e2e": {"value": ws * step.units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

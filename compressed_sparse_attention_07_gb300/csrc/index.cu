@@ -10,36 +10,46 @@ namespace csa2 {
 namespace {
 
 constexpr int kSelThreads = 1024;   // one CTA selects for one query
-constexpr int kHistBins = 8192;    // linear bins over a query's key range
-constexpr int kCandMax = 8192;     // candidates sorted in shared memory
-constexpr int kSelOutMax = 4096;   // k of one selection (top-k <= 1024, HSI blocks <= 4096)
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kPer = 16;              // keys a lane holds per round
+constexpr int kRound = kSelThreads * kPer;  // positions per round; a warp covers 512 consecutive ones
+constexpr int kHistBins = 8192;       // linear bins over a query's key range
+constexpr int kDigitBins = 2048;      // refinement digit: 11 bits
+constexpr int kCandMax = 8192;        // keys of the threshold bin listed in shared memory
 
 // ---------------------------------------------------------------- select ----
 
-// Exclusive prefix sum over the CTA (kSelThreads threads); returns the total.
+struct SelShared {
+  uint32_t hist[kHistBins];
+  uint32_t cand[kCandMax];
+  uint32_t wa[kSelWarps + 1], wb[kSelWarps + 1];
+  uint32_t cut_bin, cut_above, cut_total, cand_n, carry_eq, carry_off;
+};
+
+// Exclusive prefix sum over the CTA; returns the total in `total`.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t& total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_sums[wid] = x;
   __syncthreads();
   if (wid == 0) {
-    uint32_t w = warp_sums[lane];
+    const uint32_t w = warp_sums[lane];
     uint32_t ws = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, ws, o);
+      const uint32_t y = __shfl_up_sync(0xffffffffu, ws, o);
       if (lane >= o) ws += y;
     }
-    warp_sums[lane] = ws - w;  // exclusive
+    warp_sums[lane] = ws - w;
     if (lane == 31) warp_sums[32] = ws;
   }
   __syncthreads();
-  uint32_t res = warp_sums[wid] + x - v;
+  const uint32_t res = warp_sums[wid] + x - v;
   total = warp_sums[32];
   __syncthreads();
   return res;
@@ -53,277 +63,235 @@ struct IdMap {
   }
 };
 
-// Select the k largest keys among n positions of `vals` ((key desc, position
-// asc)); `forced` (>= 0) gets the largest key.  Writes ids ascending to out[k],
-// -1 padded.  Radix select (11/11/10-bit digits) then an ordered compaction.
-// skeys: shared-memory copy of the n keys when it fits (every pass after the
-// first then reads shared memory), else nullptr (every pass reads vals).
-__device__ void block_select(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
-                             uint32_t* skeys) {
-  __shared__ uint32_t hist[2048];
-  __shared__ uint32_t warp_sums[33];
-  __shared__ uint32_t sh_krem, sh_digit;
-  auto gkey = [&](int64_t p) -> uint32_t { return p == forced ? 0xFFFFFFFFu : order_key(vals[p]); };
-  auto key_at = [&](int64_t p) -> uint32_t { return skeys ? skeys[p] : gkey(p); };
-
-  // count valid candidates (and stage the keys); range of the valid keys
-  __shared__ uint32_t sh_min[32], sh_max[32];
-  uint32_t cnt = 0, kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
-    const uint32_t kk = gkey(p);
-    if (skeys) skeys[p] = kk;
-    if (kk != 0u) {
-      ++cnt;
-      kmin = min(kmin, kk);
-      kmax = max(kmax, kk);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  if ((threadIdx.x & 31) == 0) {
-    sh_min[threadIdx.x >> 5] = kmin;
-    sh_max[threadIdx.x >> 5] = kmax;
-  }
-  uint32_t nvalid;
-  block_exclusive_scan(cnt, warp_sums, nvalid);  // (its barriers also publish sh_min / sh_max)
-  kmin = sh_min[0];
-  kmax = sh_max[0];
-  for (int w = 1; w < kSelThreads / 32; ++w) {
-    kmin = min(kmin, sh_min[w]);
-    kmax = max(kmax, sh_max[w]);
-  }
-
-  uint32_t T = 0, krem = 0;  // select key > T, plus the first krem keys == T
-  if (nvalid > (uint32_t)k) {
-    // Radix select on x = key - kmin, from the top significant bit of the
-    // range down, at most 11 bits per pass: binning relative to the range
-    // spreads the keys over the bins even when they share their top bits.
-    const uint32_t range = kmax - kmin;
-    const int nbits = range ? 32 - __clz(range) : 0;
-    uint32_t prefix = 0;  // the fixed top bits of x
-    int fixed = 0;
-    krem = (uint32_t)k;
-    while (fixed < nbits) {
-      const int w = min(11, nbits - fixed);
-      const int sh = nbits - fixed - w;
-      const uint32_t dmask = (1u << w) - 1u;
-      for (int i = threadIdx.x; i < 2048; i += kSelThreads) hist[i] = 0;
-      __syncthreads();
-      for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
-        const uint32_t kk = key_at(p);
-        if (kk == 0u) continue;
-        const uint32_t x = kk - kmin;
-        const uint32_t top = (sh + w >= 32) ? 0u : (x >> (sh + w));
-        if (top == prefix) atomicAdd(&hist[(x >> sh) & dmask], 1u);
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) {
-        // lane L owns bins [2048 - 64(L+1), 2048 - 64L): scan from the top
-        const int lane = threadIdx.x;
-        uint32_t sacc = 0;
-        for (int i = 0; i < 64; ++i) sacc += hist[2047 - 64 * lane - i];
-        uint32_t incl = sacc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t excl = incl - sacc;  // keys in higher bins than this lane's chunk
-        const uint32_t kr = (fixed == 0) ? (uint32_t)k : sh_krem;
-        if (excl < kr && incl >= kr) {
-          uint32_t above = excl;
-          for (int i = 0; i < 64; ++i) {
-            const int d = 2047 - 64 * lane - i;
-            if (above + hist[d] >= kr) {
-              sh_digit = (uint32_t)d;
-              sh_krem = kr - above;
-              break;
-            }
-            above += hist[d];
-          }
-        }
-      }
-      __syncthreads();
-      prefix = (prefix << w) | sh_digit;
-      fixed += w;
-      krem = sh_krem;
-      __syncthreads();
-    }
-    T = kmin + prefix;
-  }
-
-  // ordered compaction: thread t scans the contiguous segment [t*seg, (t+1)*seg)
-  const int64_t seg = (n + kSelThreads - 1) / kSelThreads;
-  const int64_t lo = (int64_t)threadIdx.x * seg, hi = lo + seg < n ? lo + seg : n;
-  uint32_t gt = 0, eq = 0;
-  for (int64_t p = lo; p < hi; ++p) {
-    uint32_t kk = key_at(p);
-    gt += kk > T;
-    eq += (kk == T) && (T != 0u);
-  }
-  uint32_t eq_total;
-  uint32_t eq_before = block_exclusive_scan(eq, warp_sums, eq_total);
-  uint32_t take = krem > eq_before ? min(krem - eq_before, eq) : 0u;
+// The bin, counting down from the top, where the running count reaches
+// `need` (>= 1): s.cut_bin, s.cut_above = keys in higher bins, s.cut_total =
+// all keys.  Thread t owns nbins/kSelThreads bins from the top.
+__device__ void find_cut(const uint32_t* hist, int nbins, uint32_t need, SelShared& s) {
+  const int per = nbins / kSelThreads;
+  const int top = nbins - 1 - per * (int)threadIdx.x;
+  uint32_t sum = 0;
+  for (int i = 0; i < per; ++i) sum += hist[top - i];
   uint32_t total;
-  uint32_t off = block_exclusive_scan(gt + take, warp_sums, total);
-  for (int64_t p = lo; p < hi && off < (uint32_t)k; ++p) {
-    uint32_t kk = key_at(p);
-    if (kk > T) {
-      out[off++] = idmap(p);
-    } else if (kk == T && T != 0u && take > 0) {
-      out[off++] = idmap(p);
-      --take;
-    }
-  }
-  for (uint32_t i = total + threadIdx.x; i < (uint32_t)k; i += kSelThreads) out[i] = -1;
-}
-
-// Bitonic sort of P (a power of two) 64-bit keys in shared memory, descending
-// or ascending; every thread of the CTA calls it.
-__device__ void bitonic_sort(unsigned long long* a, int P, bool descending) {
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < P / 2; i += kSelThreads) {
-        const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
-        const bool up = ((lo & size) == 0) != descending;  // this pair sorts ascending
-        const unsigned long long x = a[lo], y = a[hi];
-        if ((x > y) == up) {
-          a[lo] = y;
-          a[hi] = x;
-        }
+  const uint32_t excl = block_exclusive_scan(sum, s.wa, total);
+  if (excl < need && excl + sum >= need) {
+    uint32_t above = excl;
+    for (int i = 0; i < per; ++i) {
+      const uint32_t h = hist[top - i];
+      if (above + h >= need) {
+        s.cut_bin = (uint32_t)(top - i);
+        s.cut_above = above;
+        break;
       }
-      __syncthreads();
+      above += h;
     }
+  }
+  if (threadIdx.x == 0) s.cut_total = total;
+  __syncthreads();
+}
+
+// Keys of one round: lane l of warp w holds positions base + 512w + 32j + l
+// (j < kPer); 0 for positions past n and for the forced one.
+__device__ __forceinline__ void load_round(const float* vals, int64_t n, int64_t forced, int64_t base,
+                                           uint32_t (&key)[kPer]) {
+  const int64_t p0 = base + (threadIdx.x >> 5) * (32 * kPer) + (threadIdx.x & 31);
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int64_t p = p0 + 32 * j;
+    key[j] = (p < n && p != forced) ? order_key(vals[p]) : 0u;
   }
 }
 
-// Top-k of one query from its scores in global memory in two passes:
-// (1) histogram over kHistBins linear bins of the key range [kmin, kmax]
-// recorded by the scoring kernel -> the bin holding the k-th key; (2) gather
-// every key in that bin or above, as (key << 32 | ~position), sort them
-// descending in shared memory -- the first k are the selection by (score
-// desc, position asc) -- then sort the chosen positions ascending.  The
-// forced position (HSI's latest block) always takes a slot.  Falls back to
-// the radix select when more than kCandMax keys tie into the threshold bin.
-__device__ void select_two_pass(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
-                                uint32_t kmin, uint32_t kmax, uint32_t* hist, unsigned long long* cand) {
-  __shared__ uint32_t sh_tb, sh_above, sh_total, sh_count;
+// Select the k largest keys among n positions of `vals` by (key desc,
+// position asc); `forced` (>= 0) always takes a slot.  Writes the chosen ids
+// in ascending position order to out[k], -1 padded.
+//   1. histogram of the keys over kHistBins linear bins of the query's key
+//      range [kmin, kmax] (recorded by the scoring kernel) -> the bin where
+//      the count from the top reaches k;
+//   2. the keys of that bin are listed in shared memory and refined 11 bits
+//      at a time down to the exact threshold key T and the number krem of
+//      keys equal to T that still fit (the first krem by position);
+//   3. ordered compaction: warp ballots within 512-position runs, one scan
+//      over the warps per round.
+// Rounds of kRound positions; for n <= kRound the keys stay in registers
+// after the first read.
+__device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
+                            uint32_t kmin, uint32_t kmax, SelShared& s) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const bool has_forced = forced >= 0 && forced < n;
+  const uint32_t need = (uint32_t)k - (has_forced ? 1u : 0u);
   const bool any = kmin <= kmax;
   const uint32_t range = any ? kmax - kmin : 0u;
   const int nbits = range ? 32 - __clz(range) : 0;
   const int sh = nbits > 13 ? nbits - 13 : 0;
-  const bool has_forced = forced >= 0 && forced < n;
-  const uint32_t kk_need = (uint32_t)k - (has_forced ? 1u : 0u);
-  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) hist[i] = 0;
-  if (threadIdx.x == 0) sh_count = 0;
-  __syncthreads();
-  if (any) {
-    for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
-      if (p == forced) continue;
-      const uint32_t kk = order_key(vals[p]);
-      if (kk != 0u) atomicAdd(&hist[(kk - kmin) >> sh], 1u);
+  const bool resident = n <= kRound;
+  auto bin_of = [&](uint32_t kk) -> uint32_t {
+    const uint32_t x = kk > kmin ? kk - kmin : 0u;
+    return min(x >> sh, (uint32_t)(kHistBins - 1));
+  };
+  uint32_t key[kPer];
+
+  uint32_t T = 0xFFFFFFFFu, krem = 0;  // select key > T, then the first krem keys == T
+  if (need > 0 && any) {
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
+    if (threadIdx.x == 0) s.cand_n = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < n; base += kRound) {
+      load_round(vals, n, forced, base, key);
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (key[j]) atomicAdd(&s.hist[bin_of(key[j])], 1u);
+    }
+    __syncthreads();
+    find_cut(s.hist, kHistBins, need, s);
+    if (s.cut_total <= need) {
+      T = 0;  // every valid key
+    } else {
+      const uint32_t tb = s.cut_bin;
+      const uint32_t c = s.hist[tb];
+      uint32_t prefix = tb;
+      int rem = sh;
+      krem = need - s.cut_above;
+      const bool listed = c <= (uint32_t)kCandMax;
+      __syncthreads();  // every thread has read the cut and hist[tb]
+      if (rem > 0 && listed) {
+        for (int64_t base = 0; base < n; base += kRound) {
+          if (!resident) load_round(vals, n, forced, base, key);
+#pragma unroll
+          for (int j = 0; j < kPer; ++j) {
+            const bool m = key[j] != 0u && bin_of(key[j]) == tb;
+            const uint32_t bal = __ballot_sync(0xffffffffu, m);
+            if (!bal) continue;
+            uint32_t at = 0;
+            if (lane == 0) at = atomicAdd(&s.cand_n, (uint32_t)__popc(bal));
+            at = __shfl_sync(0xffffffffu, at, 0);
+            if (m) s.cand[at + __popc(bal & ((1u << lane) - 1u))] = key[j] - kmin;
+          }
+        }
+        __syncthreads();
+      }
+      while (rem > 0) {
+        const int w = rem < 11 ? rem : 11;
+        const int s2 = rem - w;
+        const uint32_t dmask = (1u << w) - 1u;
+        for (int i = threadIdx.x; i < kDigitBins; i += kSelThreads) s.hist[i] = 0;
+        __syncthreads();
+        if (listed) {
+          const uint32_t cn = s.cand_n;
+          for (uint32_t i = threadIdx.x; i < cn; i += kSelThreads) {
+            const uint32_t x = s.cand[i];
+            if ((x >> rem) == prefix) atomicAdd(&s.hist[(x >> s2) & dmask], 1u);
+          }
+        } else {
+          for (int64_t base = 0; base < n; base += kRound) {
+            if (!resident) load_round(vals, n, forced, base, key);
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+              const uint32_t x = key[j] - kmin;
+              if (key[j] != 0u && key[j] >= kmin && (x >> rem) == prefix) atomicAdd(&s.hist[(x >> s2) & dmask], 1u);
+            }
+          }
+        }
+        __syncthreads();
+        find_cut(s.hist, kDigitBins, krem, s);
+        krem -= s.cut_above;
+        prefix = (prefix << w) | s.cut_bin;
+        rem = s2;
+        __syncthreads();
+      }
+      T = kmin + prefix;
     }
   }
+
+  // ordered compaction
+  if (threadIdx.x == 0) {
+    s.carry_eq = 0;
+    s.carry_off = 0;
+  }
   __syncthreads();
-  if (threadIdx.x < 32) {
-    // lane L owns bins [8192 - 256(L+1), 8192 - 256L): counts from the top
-    const int lane = threadIdx.x;
-    uint32_t sacc = 0;
-    for (int i = 0; i < 256; ++i) sacc += hist[kHistBins - 1 - 256 * lane - i];
-    uint32_t incl = sacc;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int64_t base = 0; base < n; base += kRound) {
+    if (!resident || !(need > 0 && any)) load_round(vals, n, forced, base, key);
+    const int64_t p0 = base + wid * (32 * kPer) + lane;
+    uint32_t gt = 0, eq = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+    for (int j = 0; j < kPer; ++j) {
+      gt += __popc(__ballot_sync(0xffffffffu, key[j] > T || p0 + 32 * j == forced));
+      eq += __popc(__ballot_sync(0xffffffffu, key[j] == T && T != 0u));
     }
-    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-    const uint32_t excl = incl - sacc;
     if (lane == 0) {
-      sh_total = total;
-      sh_tb = 0;
-      sh_above = 0;
+      s.wa[wid] = gt;
+      s.wb[wid] = eq;
     }
-    __syncwarp();
-    if (total > kk_need && excl < kk_need && incl >= kk_need) {
-      uint32_t above = excl;
-      for (int i = 0; i < 256; ++i) {
-        const int d = kHistBins - 1 - 256 * lane - i;
-        if (above + hist[d] >= kk_need) {
-          sh_tb = (uint32_t)d;
-          sh_above = above;
-          break;
-        }
-        above += hist[d];
+    __syncthreads();
+    if (wid == 0) {
+      const uint32_t g = s.wa[lane], e = s.wb[lane];
+      uint32_t ie = e;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, ie, o);
+        if (lane >= o) ie += y;
+      }
+      const uint32_t e_before = s.carry_eq + ie - e;
+      const uint32_t take = krem > e_before ? min(krem - e_before, e) : 0u;
+      const uint32_t v = g + take;
+      uint32_t iv = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, iv, o);
+        if (lane >= o) iv += y;
+      }
+      const uint32_t off = s.carry_off + iv - v;
+      __syncwarp();
+      s.wa[lane] = off;
+      s.wb[lane] = e_before;
+      if (lane == 31) {
+        s.carry_eq += ie;
+        s.carry_off += iv;
       }
     }
-  }
-  __syncthreads();
-  const uint32_t tb = sh_tb;
-  const uint32_t cand_n = (sh_total > kk_need ? sh_above + hist[tb] : sh_total) + (has_forced ? 1u : 0u);
-  if (cand_n > (uint32_t)kCandMax) {
-    block_select(vals, n, k, forced, idmap, out, nullptr);
-    return;
-  }
-  // (2) gather the candidates
-  for (int64_t p = threadIdx.x; p < n; p += kSelThreads) {
-    unsigned long long ck = 0ull;
-    if (p == forced) {
-      ck = (0xFFFFFFFFull << 32) | (0xFFFFFFFFu - (uint32_t)p);
-    } else if (any) {
-      const uint32_t kk = order_key(vals[p]);
-      if (kk != 0u && ((kk - kmin) >> sh) >= tb) ck = ((unsigned long long)kk << 32) | (0xFFFFFFFFu - (uint32_t)p);
+    __syncthreads();
+    uint32_t off = s.wa[wid], e_run = s.wb[wid];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int64_t p = p0 + 32 * j;
+      const bool is_eq = key[j] == T && T != 0u;
+      const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
+      const bool sel = key[j] > T || p == forced || (is_eq && e_run + __popc(be & lt) < krem);
+      const uint32_t bs = __ballot_sync(0xffffffffu, sel);
+      const uint32_t o = off + __popc(bs & lt);
+      if (sel && o < (uint32_t)k) out[o] = idmap(p);
+      off += __popc(bs);
+      e_run += __popc(be);
     }
-    if (ck) cand[atomicAdd(&sh_count, 1u)] = ck;
+    __syncthreads();
   }
-  __syncthreads();
-  const int C = (int)sh_count;
-  int P = 1;
-  while (P < C) P <<= 1;
-  for (int i = C + threadIdx.x; i < P; i += kSelThreads) cand[i] = 0ull;
-  __syncthreads();
-  bitonic_sort(cand, P, true);
-  const int m = C < k ? C : k;
-  // chosen positions, ascending
-  int P2 = 1;
-  while (P2 < m) P2 <<= 1;
-  for (int i = threadIdx.x; i < P2; i += kSelThreads) {
-    const unsigned long long v = (i < m) ? (unsigned long long)(0xFFFFFFFFu - (uint32_t)(cand[i] & 0xFFFFFFFFull))
-                                         : ~0ull;
-    cand[kCandMax + i] = v;
-  }
-  __syncthreads();
-  bitonic_sort(cand + kCandMax, P2, false);
-  for (int i = threadIdx.x; i < k; i += kSelThreads) out[i] = i < m ? idmap((int64_t)cand[kCandMax + i]) : -1;
+  for (uint32_t i = s.carry_off + threadIdx.x; i < (uint32_t)k; i += kSelThreads) out[i] = -1;
 }
 
 // blockIdx.y == 0: entry top-k (Full or Reindex); == 1: HSI block pool (Full).
-__global__ void __launch_bounds__(kSelThreads) select2_kernel(int q0, int Tq, int r, int k, int n_blocks,
-                                                              int64_t max_entries, const int64_t* __restrict__ q_pos,
-                                                              const int32_t* __restrict__ n_entries,
-                                                              const int32_t* __restrict__ pool, const float* scores,
-                                                              const float* bmax, int64_t score_stride,
-                                                              const uint32_t* kmin, const uint32_t* kmax,
-                                                              int32_t* topk_out, int32_t* pool_out) {
-  extern __shared__ __align__(16) unsigned long long sel_smem[];
-  unsigned long long* cand = sel_smem;                                             // [kCandMax + kSelOutMax]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(sel_smem + kCandMax + kSelOutMax);  // [kHistBins]
+__global__ void __launch_bounds__(kSelThreads) select_kernel(int q0, int Tq, int r, int k, int n_blocks,
+                                                             int64_t max_entries, const int64_t* __restrict__ q_pos,
+                                                             const int32_t* __restrict__ n_entries,
+                                                             const int32_t* __restrict__ pool, const float* scores,
+                                                             const float* bmax, int64_t score_stride,
+                                                             const uint32_t* kmin, const uint32_t* kmax,
+                                                             int32_t* topk_out, int32_t* pool_out) {
+  extern __shared__ __align__(16) unsigned char sel_raw[];
+  SelShared& s = *reinterpret_cast<SelShared*>(sel_raw);
   const int qc = blockIdx.x, qi = q0 + qc, b = qi / Tq;
   const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
   const uint32_t lo = kmin[qc], hi = kmax[qc];
   if (blockIdx.y == 0) {
     const float* v = scores + (int64_t)qc * score_stride;
     if (pool)
-      select_two_pass(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks},
-                      topk_out + (int64_t)qi * k, lo, hi, hist, cand);
+      select_topk(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks},
+                  topk_out + (int64_t)qi * k, lo, hi, s);
     else
-      select_two_pass(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k, lo, hi, hist, cand);
+      select_topk(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k, lo, hi, s);
   } else {
     const int64_t nb = (nv + kHsiBlock - 1) / kHsiBlock;
     const float* v = bmax + (int64_t)qc * ((max_entries + 7) / 8);
-    select_two_pass(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks, lo, hi, hist, cand);
+    select_topk(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks, lo, hi, s);
   }
 }
 
@@ -369,11 +337,11 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
                                     stride, bmax, kmin, kmax, status, num_sms(), stream);
     if (e != cudaSuccess) return e;
     dim3 sg(nq, (!reindex && pool_out) ? 2 : 1);
-    const size_t sel_smem = (kCandMax + kSelOutMax) * sizeof(unsigned long long) + kHistBins * sizeof(uint32_t);
-    cudaFuncSetAttribute(select2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
-    select2_kernel<<<sg, kSelThreads, sel_smem, stream>>>(q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, max_entries,
-                                                          q_pos, n_entries, pool, scores, bmax, stride, kmin, kmax,
-                                                          topk_out, pool_out);
+    const size_t sel_smem = sizeof(SelShared);
+    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
+    select_kernel<<<sg, kSelThreads, sel_smem, stream>>>(q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, max_entries,
+                                                         q_pos, n_entries, pool, scores, bmax, stride, kmin, kmax,
+                                                         topk_out, pool_out);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -206,6 +206,32 @@ def test_index_topk_random_fp4_with_head_weights_and_ratio2():
     assert (g_top[0, 2] >= 0).sum() == 1 and g_top[0, 2, 0] == 0  # t = 1 sees entry 0 only
 
 
+def test_select_threshold_bin_beyond_shared_list_and_single_slots():
+    """19500 copies of one indexer row among 500 random rows: fewer than k
+    keys lie above the copies' key, so the k-th place falls inside a bin of
+    more than 8192 equal keys (refined over the scores themselves, the first
+    ids win); hsi_blocks = 1 keeps only the forced latest block and topk = 1
+    the single best entry."""
+    B, N = 1, 20000
+    oc = oracle.Cache(B, N, CI, "fp4")
+    oc.codes[0], oc.scales[0] = synth.integer_fp4_bytes(synth.rng(26, "idx"), N, CI)
+    oc.codes[0, 500:], oc.scales[0, 500:] = oc.codes[0, 7], oc.scales[0, 7]
+    pc = _paged.cache_pair(B, N, CI, "fp4", 26)
+    _paged.upload(pc, oc)
+    q_idx = synth.integer_bf16(synth.rng(26, "q"), (B, 2, H, CI), -1, 1)
+    q_pos = np.array([[N - 1, 12345]], np.int64)
+    n_ent = np.array([N], np.int32)
+    for k, nb in ((512, 1), (1, 3)):
+        cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=nb)
+        g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+        o_top, o_pool, s = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, want_pool=True,
+                                             want_scores=True)
+        np.testing.assert_array_equal(g_top, o_top)
+        np.testing.assert_array_equal(g_pool, o_pool)
+    v = s[0, 0][np.isfinite(s[0, 0])]
+    assert (v > v[600]).sum() < 512 and v.max() - v.min() >= 1.0  # the case the test is for
+
+
 def test_reindex_over_pool_matches_oracle():
     B, N, k, nb = 2, 4000, 64, 40
     oc, pc = _idx_caches(B, N, "fp4", seed=23, integer=True, dup=True)

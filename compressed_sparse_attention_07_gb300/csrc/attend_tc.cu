@@ -704,6 +704,318 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
   if (warp == 0) tc::tmem_dealloc(tb, 128);
 }
 
+// ---------------------------------------------------------------------------
+// Row-tile variant for every head at once (at most six 128-row tiles per
+// query: top-k <= 512 with window <= 256, or similar).  One CTA per (query
+// token, 128-row tile), the query's tiles forming a cluster.  Each row is
+// read once: thread (r, p) loads quarter p of row r (one 128-channel chunk)
+// straight into registers, decodes it and stores it to the K-major chunk
+// tile C[p]; then
+//   S^T[128 rows x 64 heads]  = sum_c C[c] . Q_c^T       (M 128, N 64, K 512)
+//   partial softmax per head over the tile's rows: m_t, l_t, P = 2^(s - m_t)
+//   O_t^T[c] = C[c]^T . P^T                            (M 128, N 64, K 128)
+// and the tiles are merged through distributed shared memory:
+// M = max_t m_t, L = sum_t 2^(m_t - M) l_t, out = sum_t 2^(m_t - M) O_t / L;
+// chunk c of the output is summed, in tile order, by the CTA of rank c % n.
+constexpr int kAllHeads = 64;
+constexpr size_t kRowQBytes = (size_t)kAllHeads * kDim * 2;   // 65536
+constexpr size_t kRowCBytes = 4 * (size_t)kCBytes;            // 131072
+constexpr size_t kRowPBytes = (size_t)kAllHeads * 128 * 2;    // 16384
+constexpr size_t kRowSmem = kRowQBytes + kRowCBytes + kRowPBytes + 128 * 4 + 2 * kAllHeads * 4;
+constexpr int kRowMaxTiles = 6;                               // receive area n * ceil(4/n) * 32 KB <= 192 KB
+
+// Reduce v[16] over the 32 lanes of a warp (op = max or +): afterwards lane l
+// holds the result for entry l >> 1.  Each step hands half of the entries
+// still held to the partner lane, 8 + 4 + 2 + 1 + 1 shuffles in all.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(const float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
+  float a8[8], a4[4], a2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float keep = b4 ? v[8 + i] : v[i], send = b4 ? v[i] : v[8 + i];
+    a8[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b3 ? a8[4 + i] : a8[i], send = b3 ? a8[i] : a8[4 + i];
+    a4[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b2 ? a4[2 + i] : a4[i], send = b2 ? a4[i] : a4[2 + i];
+    a2[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  const float keep = b1 ? a2[1] : a2[0], send = b1 ? a2[0] : a2[1];
+  float a1 = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+}
+
+template <int kDtype>
+__global__ void __launch_bounds__(kThreads, 1) attend_rows_kernel(AttArgs a) {
+  constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
+  const int n = a.tiles_main + a.tiles_win;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* qs = smem;                                     // Q [64 heads x 512] f16, K-major
+  uint8_t* ctile = qs + kRowQBytes;                       // C[4]: [128 rows x 128 ch] f16, K-major
+  uint8_t* pt = ctile + kRowCBytes;                       // P^T [64 heads x 128 rows] f16, K-major
+  float* ml = reinterpret_cast<float*>(pt + kRowPBytes + 128 * 4);  // m[64] (log2 domain), l[64]
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ float red_m[4][kAllHeads], red_s[4][kAllHeads];
+  __shared__ float mx[kAllHeads], alpha[kAllHeads];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127, p = tid >> 7, quad = warp & 3;
+  const uint32_t lane_base = 32 * quad;
+  const int t = (int)tc::cluster_rank();
+  const int qi = blockIdx.y, b = qi / a.Tq;
+  const bool fp4_tile = kMainFp4 && t < a.tiles_main;
+
+  // ---- loads: Q (16 bytes x 8 per thread), then quarter p of row r
+  uint4 qv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = tid + kThreads * i, h = idx >> 6, kk = (idx & 63) * 8;
+    qv[i] = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)qi * kHeads + h) * kDim + kk));
+  }
+  const int32_t sidx = slot_source(a, qi, b, t * 128 + r);
+  uint4 raw[16];
+  uint2 sc = make_uint2(0u, 0u);
+  if (sidx >= 0) {
+    const int64_t page = sidx / kPage;
+    const int sl = sidx % kPage;
+    if (fp4_tile) {
+      const uint4* g = reinterpret_cast<const uint4*>(a.mc.data + page * kMainFp4Data + sl * (kDim / 2) + 64 * p);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) raw[j] = __ldg(g + j);
+      sc = __ldg(reinterpret_cast<const uint2*>(a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16) + 8 * p));
+    } else {
+      const uint4* g = reinterpret_cast<const uint4*>(a.mc.data + page * kMainBf16Data + sl * (kDim * 2) + 256 * p);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) raw[j] = __ldg(g + j);
+    }
+  } else if (sidx <= -2) {
+    const uint4* g = reinterpret_cast<const uint4*>(a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx)) * kDim + 128 * p);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) raw[j] = __ldg(g + j);
+  }
+
+  // ---- set-up while the rows arrive: Q to f16, barrier, TMEM (S^T 64 + O^T 4 x 64 columns)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = tid + kThreads * i, h = idx >> 6, kk = (idx & 63) * 8;
+    *reinterpret_cast<uint4*>(qs + tc::kmajor_off(h, kk, kDim)) =
+        make_uint4(bf16x2_to_f16x2(qv[i].x), bf16x2_to_f16x2(qv[i].y), bf16x2_to_f16x2(qv[i].z),
+                   bf16x2_to_f16x2(qv[i].w));
+  }
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+
+  // ---- decode chunk p of row r into C[p]
+  uint8_t* ct = ctile + p * kCBytes;
+  if (sidx == -1) {
+#pragma unroll
+    for (int m = 0; m < 16; ++m) *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 8 * m, 128)) = make_uint4(0, 0, 0, 0);
+  } else if (fp4_tile) {
+    const uint32_t sw[2] = {sc.x, sc.y};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // 16 code bytes = 32 channels, two scale groups
+      const uint32_t sb = (sw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+      const uint32_t s_lo = f16x2_scale(sb & 0xFFu), s_hi = f16x2_scale(sb >> 8);
+      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t h4[4];
+        e2m1x8_to_f16x2(w4[q], h4);
+        const uint32_t s2 = q < 2 ? s_lo : s_hi;
+        *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 32 * j + 8 * q, 128)) =
+            make_uint4(hmul2(h4[0], s2), hmul2(h4[1], s2), hmul2(h4[2], s2), hmul2(h4[3], s2));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+      *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 8 * m, 128)) =
+          make_uint4(bf16x2_to_f16x2(raw[m].x), bf16x2_to_f16x2(raw[m].y), bf16x2_to_f16x2(raw[m].z),
+                     bf16x2_to_f16x2(raw[m].w));
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = tmem_base;
+
+  // ---- S^T = sum_c C[c] . Q_c^T
+  constexpr uint32_t kIdescS = tc::idesc_f16(128, kAllHeads, false, false, false, false);
+  constexpr uint32_t kIdescO = tc::idesc_f16(128, kAllHeads, false, false, true, false);
+  if (tid == 0) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t cbase = tc::smem_u32(ctile + c * kCBytes);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t ad = tc::sdesc(cbase + ks * 256, 128, 2048);
+        const uint64_t bd = tc::sdesc(tc::smem_u32(qs) + (c * 16 + ks * 2) * 128, 128, kDim * 16);
+        tc::mma_ss(tb, ad, bd, kIdescS, (c > 0 || ks > 0) ? 1u : 0u);
+      }
+    }
+    tc::mma_commit(&bar);
+  }
+  bool ok = tc::mbar_wait(&bar, 0, kSpin);
+  tc::fence_after_sync();
+
+  // ---- partial softmax over the tile's rows (thread: row r, heads 16p..16p+15)
+  const float sc2 = a.scale * kLog2e;
+  const bool valid = sidx != -1;
+  float v[16];
+  {
+    uint32_t w[16];
+    tc::tmem_ld16(tc::taddr(tb, lane_base, 16 * p), w);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = valid ? __uint_as_float(w[j]) * sc2 : -INFINITY;
+  }
+  {
+    const float wm = warp_reduce16<true>(v);
+    if ((lane & 1) == 0) red_m[quad][16 * p + (lane >> 1)] = wm;
+  }
+  __syncthreads();
+  if (tid < kAllHeads) mx[tid] = fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]), fmaxf(red_m[2][tid], red_m[3][tid]));
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float mh = mx[16 * p + j];
+    v[j] = (valid && mh != -INFINITY) ? exp2f(v[j] - mh) : 0.0f;
+    *reinterpret_cast<__half*>(pt + tc::kmajor_off(16 * p + j, r, 128)) = __float2half_rn(v[j]);
+  }
+  {
+    const float ws = warp_reduce16<false>(v);
+    if ((lane & 1) == 0) red_s[quad][16 * p + (lane >> 1)] = ws;
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid < kAllHeads) {
+    ml[tid] = mx[tid];
+    ml[kAllHeads + tid] = red_s[0][tid] + red_s[1][tid] + red_s[2][tid] + red_s[3][tid];
+  }
+
+  // ---- O^T[c] = C[c]^T . P^T
+  if (tid == 0) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t cbase = tc::smem_u32(ctile + c * kCBytes);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t ad = tc::sdesc(cbase + ks * 2 * 2048, 2048, 128);
+        const uint64_t bd = tc::sdesc(tc::smem_u32(pt) + ks * 256, 128, 2048);
+        tc::mma_ss(tb + kAllHeads + kAllHeads * c, ad, bd, kIdescO, ks > 0 ? 1u : 0u);
+      }
+    }
+    tc::mma_commit(&bar);
+  }
+  ok = tc::mbar_wait(&bar, 1, kSpin) && ok;
+  tc::fence_after_sync();
+  float o[4][16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[16];
+    tc::tmem_ld16(tc::taddr(tb, lane_base, kAllHeads + kAllHeads * c + 16 * p), w);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[c][j] = __uint_as_float(w[j]);
+  }
+  tc::fence_before_sync();
+  // every CTA of the cluster: (m, l) written, products finished, shared memory free
+  tc::cluster_sync();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tb, 512);
+  if (tid < kAllHeads) {
+    const uint32_t ml_addr = tc::smem_u32(ml);
+    float mk[kRowMaxTiles], lk[kRowMaxTiles];
+#pragma unroll
+    for (int k2 = 0; k2 < kRowMaxTiles; ++k2) {
+      mk[k2] = k2 < n ? tc::ld_dsmem(tc::map_rank(ml_addr + 4 * tid, k2)) : -INFINITY;
+      lk[k2] = k2 < n ? tc::ld_dsmem(tc::map_rank(ml_addr + 4 * (kAllHeads + tid), k2)) : 0.0f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k2 = 0; k2 < kRowMaxTiles; ++k2) M = fmaxf(M, mk[k2]);
+    float L = 0.0f;
+#pragma unroll
+    for (int k2 = 0; k2 < kRowMaxTiles; ++k2)
+      if (mk[k2] != -INFINITY) L += exp2f(mk[k2] - M) * lk[k2];
+    const float mt = ml[tid];
+    alpha[tid] = (ok && L > 0.0f && mt != -INFINITY) ? exp2f(mt - M) / L : 0.0f;
+    if (t == 0 && a.lse)
+      a.lse[(int64_t)qi * kHeads + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  }
+  if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
+  __syncthreads();
+  // ---- push the scaled partial output: chunk c goes to rank c % n, slot c / n,
+  // at [sender tile][slot][head][channel]
+  const int spo = (4 + n - 1) / n;
+  const uint32_t recv = tc::smem_u32(smem);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t dst = tc::map_rank(recv, c % n) + 4u * (uint32_t)(((t * spo + c / n) * kAllHeads + 16 * p) * 128 + r);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) tc::st_dsmem(dst + 4u * 128u * j, o[c][j] * alpha[16 * p + j]);
+  }
+  tc::cluster_sync();
+  // ---- this CTA's chunks: sum the tiles' partials in tile order
+  const float* rv = reinterpret_cast<const float*>(smem);
+  for (int s2 = 0; s2 < spo; ++s2) {
+    const int c = s2 * n + t;
+    if (c >= 4) break;
+    for (int e = tid; e < kAllHeads * 128; e += kThreads) {
+      float acc = 0.0f;
+      for (int k2 = 0; k2 < n; ++k2) acc += rv[(k2 * spo + s2) * kAllHeads * 128 + e];
+      const int h = e >> 7, ch = e & 127;
+      a.out[((int64_t)qi * kHeads + h) * kDim + c * 128 + ch] = acc;
+    }
+  }
+}
+
+template <int kDtype>
+cudaError_t launch_rows(const AttArgs& a, int Q, cudaStream_t stream) {
+  const int n_tiles = a.tiles_main + a.tiles_win;
+  auto kern = attend_rows_kernel<kDtype>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRowSmem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_tiles, Q);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kRowSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = n_tiles;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // whether this cluster shape can be scheduled at all, asked once per shape
+  static int schedulable[kRowMaxTiles + 1] = {};  // 0 unknown, 1 yes, -1 no
+  if (schedulable[n_tiles] == 0) {
+    int clusters = 0;
+    const bool yes = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters >= 1;
+    (void)cudaGetLastError();
+    schedulable[n_tiles] = yes ? 1 : -1;
+  }
+  if (schedulable[n_tiles] < 0) return cudaErrorNotSupported;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 template <int kDtype>
 cudaError_t launch_split(const AttArgs& a, int Q, cudaStream_t stream) {
   const int n_tiles = a.tiles_main + a.tiles_win;
@@ -779,9 +1091,14 @@ cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q,
   AttArgs a{Tq, cfg.topk, cfg.window, S, (cfg.topk + 127) / 128, (cfg.window + 127) / 128, q, view_of(main_c),
             n_entries, (int64_t)main_c.max_pages * kPage, topk, swa, swa_len, swa_pos0, q_pos, scale, out, lse,
             status};
-  // few query tokens: split the rows of every query over a cluster of CTAs
-  // (one per 128-row tile); many: one CTA per query and head group
+  // up to six row tiles: one CTA per (query, tile) for every head, the
+  // query's tiles in one cluster; more: split by head groups
   const int n_tiles = a.tiles_main + a.tiles_win;
+  if (n_tiles <= kRowMaxTiles) {
+    cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_rows<CSA2_CACHE_FP4>(a, Q, stream)
+                                                      : launch_rows<CSA2_CACHE_BF16>(a, Q, stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if ((int64_t)Q * 4 * n_tiles <= 8 * (int64_t)num_sms() && n_tiles <= 16) {
     cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_split<CSA2_CACHE_FP4>(a, Q, stream)
                                                       : launch_split<CSA2_CACHE_BF16>(a, Q, stream);

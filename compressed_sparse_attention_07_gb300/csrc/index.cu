@@ -20,42 +20,29 @@ constexpr int kCandMax = 8192;        // keys of the threshold bin listed in sha
 
 // ---------------------------------------------------------------- select ----
 
+constexpr int kRankMax = 512;  // threshold-bin candidates ranked directly (else refined by digits)
+
 struct SelShared {
+  uint32_t keys[kRound];       // this CTA's keys of the current round (slots: kslot)
   uint32_t hist[kHistBins];    // this CTA's histogram (the cluster's peers read it)
   uint32_t merged[kHistBins];  // the cluster's histogram
-  uint32_t cand[kCandMax];
-  uint32_t wa[kSelWarps + 1], wb[kSelWarps + 1];
-  uint32_t cut_bin, cut_above, cut_total, cand_n, carry_eq, carry_off, grand;
+  uint32_t cand[kCandMax];     // this CTA's keys of the threshold bin, minus kmin (peers read them)
+  uint32_t all[kRankMax];      // the cluster's threshold-bin keys
+  uint32_t part[kSelThreads];  // bin sums per thread (find_cut)
+  uint32_t wsum[kSelWarps + 1];
+  uint32_t cut_bin, cut_above, cut_total, cand_n, c_all, t_x, t_krem, carry_eq, carry_gt, grand;
   uint32_t tot_gt, tot_eq;     // this CTA's counts for the compaction (peers read them)
+  uint32_t peer_off[9];
 };
 
-// Exclusive prefix sum over the CTA; returns the total in `total`.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t& total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  uint32_t x = v;
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
   }
-  if (lane == 31) warp_sums[wid] = x;
-  __syncthreads();
-  if (wid == 0) {
-    const uint32_t w = warp_sums[lane];
-    uint32_t ws = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, ws, o);
-      if (lane >= o) ws += y;
-    }
-    warp_sums[lane] = ws - w;
-    if (lane == 31) warp_sums[32] = ws;
-  }
-  __syncthreads();
-  const uint32_t res = warp_sums[wid] + x - v;
-  total = warp_sums[32];
-  __syncthreads();
-  return res;
+  return v;
 }
 
 // id emitted for position p
@@ -68,27 +55,47 @@ struct IdMap {
 
 // The bin, counting down from the top, where the running count reaches
 // `need` (>= 1): s.cut_bin, s.cut_above = keys in higher bins, s.cut_total =
-// all keys.  Thread t owns nbins/kSelThreads bins from the top.
+// all keys (the cut is set only when cut_total >= need).  Every thread sums
+// nbins/kSelThreads bins (thread t from the top); warp 0 then finds the
+// 32-thread group, the thread and the bin with three warp scans.
 __device__ void find_cut(const uint32_t* hist, int nbins, uint32_t need, SelShared& s) {
   const int per = nbins / kSelThreads;
-  const int top = nbins - 1 - per * (int)threadIdx.x;
-  uint32_t sum = 0;
-  for (int i = 0; i < per; ++i) sum += hist[top - i];
-  uint32_t total;
-  const uint32_t excl = block_exclusive_scan(sum, s.wa, total);
-  if (excl < need && excl + sum >= need) {
-    uint32_t above = excl;
-    for (int i = 0; i < per; ++i) {
-      const uint32_t h = hist[top - i];
-      if (above + h >= need) {
-        s.cut_bin = (uint32_t)(top - i);
-        s.cut_above = above;
-        break;
-      }
-      above += h;
-    }
+  const int t = threadIdx.x, lane = t & 31;
+  {
+    const int top = nbins - 1 - per * t;
+    uint32_t sum = 0;
+    for (int i = 0; i < per; ++i) sum += hist[top - i];
+    s.part[t] = sum;
   }
-  if (threadIdx.x == 0) s.cut_total = total;
+  __syncthreads();
+  if (t < 32) {
+    uint32_t acc = 0;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) acc += s.part[32 * lane + i];
+    const uint32_t incl = warp_incl_scan(acc), excl = incl - acc;
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    const uint32_t g = __ballot_sync(0xffffffffu, excl < need && incl >= need);
+    if (g) {
+      const int G = __ffs(g) - 1;
+      uint32_t above = __shfl_sync(0xffffffffu, excl, G);
+      const uint32_t pv = s.part[32 * G + lane];
+      const uint32_t pi = warp_incl_scan(pv);
+      const uint32_t h = __ballot_sync(0xffffffffu, above + pi - pv < need && above + pi >= need);
+      const int P = __ffs(h) - 1;
+      above += __shfl_sync(0xffffffffu, pi - pv, P);
+      const int top = nbins - 1 - per * (32 * G + P);
+      const uint32_t hv = lane < per ? hist[top - lane] : 0u;
+      const uint32_t hi = warp_incl_scan(hv);
+      const uint32_t hb = __ballot_sync(0xffffffffu, lane < per && above + hi - hv < need && above + hi >= need);
+      const int Bn = __ffs(hb) - 1;
+      const uint32_t ab = __shfl_sync(0xffffffffu, hi - hv, Bn);
+      if (lane == 0) {
+        s.cut_bin = (uint32_t)(top - Bn);
+        s.cut_above = above + ab;
+      }
+    }
+    if (lane == 0) s.cut_total = total;
+  }
   __syncthreads();
 }
 
@@ -119,20 +126,12 @@ __device__ __forceinline__ float ld_score(const float* p) {
   return v;
 }
 
-// Keys of one round of the range [lo, hi): lane l of warp w holds positions
-// lo + base + 512w + 32j + l (j < kPer); 0 past hi and at the forced one.
-// The loads are issued together and the values stay in registers.
-__device__ __forceinline__ void load_round(const float* vals, int64_t lo, int64_t hi, int64_t forced, int64_t base,
-                                           uint32_t (&key)[kPer]) {
-  const int64_t p0 = lo + base + (threadIdx.x >> 5) * (32 * kPer) + (threadIdx.x & 31);
-  float v[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int64_t p = p0 + 32 * j;
-    v[j] = p < hi ? ld_score(vals + p) : __uint_as_float(kScoreInvalid);
-  }
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) key[j] = (p0 + 32 * j == forced) ? 0u : order_key(v[j]);
+// Shared-memory slot of key i of a round: 16-byte units are XOR-swizzled so
+// that both the coalesced pattern (thread t, key t + 1024j) and one thread
+// reading the 16 consecutive keys of its own range hit distinct banks.
+__device__ __forceinline__ int kslot(int i) {
+  const int u = i >> 2;
+  return ((u ^ ((u >> 3) & 7)) << 2) | (i & 3);
 }
 
 // Select the k largest keys among n positions of `vals` by (key desc,
@@ -143,14 +142,16 @@ __device__ __forceinline__ void load_round(const float* vals, int64_t lo, int64_
 //      range [kmin, kmax] (recorded by the scoring kernel), summed over the
 //      cluster through distributed shared memory -> the bin where the count
 //      from the top reaches k;
-//   2. the keys of that bin are listed in shared memory and refined 11 bits
-//      at a time (cluster-summed digit histograms) down to the exact
+//   2. the keys of that bin are listed; when there are at most kRankMax of
+//      them in the cluster, each one's rank among them gives the exact
 //      threshold key T and the number krem of keys equal to T that still fit
-//      (the first krem by position);
+//      (the first krem by position); more are refined 11 bits at a time
+//      (cluster-summed digit histograms);
 //   3. ordered compaction: each CTA starts after the selections of the lower
-//      ranks; within a CTA, warp ballots over 512-position runs and one scan
-//      over the warps per round.
-// A range of at most kRound positions stays in registers after one read.
+//      ranks; thread t owns 16 consecutive positions of a round, offsets from
+//      warp scans and one scan over the warps.
+// Keys are staged in shared memory a round of kRound positions at a time; a
+// range of at most kRound positions is read from global memory once.
 __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
                             uint32_t kmin, uint32_t kmax, SelShared& s, int cs, int rk) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -163,31 +164,54 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
   int64_t L = (n + cs - 1) / cs;
   L = (L + 511) & ~(int64_t)511;
   const int64_t lo = min(n, (int64_t)rk * L), hi = min(n, lo + L);
-  // a CTA's round layout spans kRound positions from lo, past hi when L < kRound:
-  // only the CTA whose range holds the forced position may count it
-  forced = (forced >= lo && forced < hi) ? forced : -1;
+  forced = (forced >= lo && forced < hi) ? forced : -1;  // only the CTA whose range holds it
   const bool resident = L <= kRound;
   const bool ranked = need > 0 && any;
+  const uint32_t lt = (1u << lane) - 1u;
   auto bin_of = [&](uint32_t kk) -> uint32_t {
     const uint32_t x = kk > kmin ? kk - kmin : 0u;
     return min(x >> sh, (uint32_t)(kHistBins - 1));
   };
-  uint32_t key[kPer];
+  // stage round `base`: position lo + base + i -> s.keys[kslot(i)] (0 past hi
+  // and at the forced position), every load issued before the first is
+  // used; optionally histogram the keys on the way
+  auto load = [&](int64_t base, bool count) {
+    float v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int64_t p = lo + base + threadIdx.x + kSelThreads * j;
+      v[j] = p < hi ? ld_score(vals + p) : __uint_as_float(kScoreInvalid);
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = threadIdx.x + kSelThreads * j;
+      const uint32_t kk = (lo + base + i == forced) ? 0u : order_key(v[j]);
+      s.keys[kslot(i)] = kk;
+      if (count && kk) atomicAdd(&s.hist[bin_of(kk)], 1u);
+    }
+  };
+  // make round `base` the staged one (a no-op for a resident range)
+  auto stage = [&](int64_t base) {
+    if (resident) return;
+    __syncthreads();
+    load(base, false);
+    __syncthreads();
+  };
 
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
   if (threadIdx.x == 0) {
     s.cand_n = 0;
     s.tot_gt = 0;
     s.tot_eq = 0;
+    s.carry_gt = 0;
+    s.carry_eq = 0;
   }
   __syncthreads();
   uint32_t T = 0xFFFFFFFFu, krem = 0;  // select key > T, then the first krem keys == T
   if (ranked) {
     for (int64_t base = 0; base < L; base += kRound) {
-      load_round(vals, lo, hi, forced, base, key);
-#pragma unroll
-      for (int j = 0; j < kPer; ++j)
-        if (key[j]) atomicAdd(&s.hist[bin_of(key[j])], 1u);
+      if (base > 0) __syncthreads();
+      load(base, true);
     }
     csync(cs);
     const uint32_t* H = s.hist;
@@ -207,17 +231,66 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
       const bool listed = s.hist[tb] <= (uint32_t)kCandMax;  // this CTA's share of the bin
       if (rem > 0 && listed) {
         for (int64_t base = 0; base < L; base += kRound) {
-          if (!resident) load_round(vals, lo, hi, forced, base, key);
-#pragma unroll
+          stage(base);
+#pragma unroll 4
           for (int j = 0; j < kPer; ++j) {
-            const bool m = key[j] != 0u && bin_of(key[j]) == tb;
+            const uint32_t kk = s.keys[kslot(threadIdx.x + kSelThreads * j)];
+            const bool m = kk != 0u && bin_of(kk) == tb;
             const uint32_t bal = __ballot_sync(0xffffffffu, m);
             if (!bal) continue;
             uint32_t at = 0;
             if (lane == 0) at = atomicAdd(&s.cand_n, (uint32_t)__popc(bal));
             at = __shfl_sync(0xffffffffu, at, 0);
-            if (m) s.cand[at + __popc(bal & ((1u << lane) - 1u))] = key[j] - kmin;
+            if (m) s.cand[at + __popc(bal & lt)] = kk - kmin;
           }
+        }
+      }
+      if (rem > 0) {
+        // the cluster's count of threshold-bin keys (all CTAs agree on `small`)
+        csync(cs);
+        if (threadIdx.x == 0) {
+          uint32_t c = 0, ok = 1;
+          for (int r = 0; r < cs; ++r) {
+            s.peer_off[r] = c;
+            const uint32_t cr = cs > 1 ? tc::ld_dsmem_u32(tc::map_rank(tc::smem_u32(&s.cand_n), r)) : s.cand_n;
+            const uint32_t hr = cs > 1 ? tc::ld_dsmem_u32(tc::map_rank(tc::smem_u32(&s.hist[tb]), r)) : s.hist[tb];
+            ok &= cr == hr;  // every CTA listed its share
+            c += hr;
+          }
+          s.peer_off[cs] = c;
+          s.c_all = ok ? c : 0xFFFFFFFFu;
+        }
+        __syncthreads();
+        const uint32_t c_all = s.c_all;
+        if (c_all <= (uint32_t)kRankMax) {
+          const uint32_t* C = s.cand;
+          if (cs > 1) {
+            for (uint32_t i = threadIdx.x; i < c_all; i += kSelThreads) {
+              int r = 0;
+              while (i >= s.peer_off[r + 1]) ++r;
+              s.all[i] = tc::ld_dsmem_u32(tc::map_rank(tc::smem_u32(&s.cand[i - s.peer_off[r]]), r));
+            }
+            C = s.all;
+            __syncthreads();
+          }
+          // rank of each candidate among the threshold-bin keys
+          for (uint32_t i = threadIdx.x; i < c_all; i += kSelThreads) {
+            const uint32_t x = C[i];
+            uint32_t gt = 0, eq = 0;
+            for (uint32_t j = 0; j < c_all; ++j) {
+              const uint32_t y = C[j];
+              gt += y > x;
+              eq += y == x;
+            }
+            if (gt < krem && krem <= gt + eq) {  // the same x and counts for every such i
+              s.t_x = x;
+              s.t_krem = krem - gt;
+            }
+          }
+          __syncthreads();
+          prefix = s.t_x;
+          krem = s.t_krem;
+          rem = 0;
         }
       }
       while (rem > 0) {
@@ -235,11 +308,11 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
           }
         } else {
           for (int64_t base = 0; base < L; base += kRound) {
-            if (!resident) load_round(vals, lo, hi, forced, base, key);
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-              const uint32_t x = key[j] - kmin;
-              if (key[j] != 0u && key[j] >= kmin && (x >> rem) == prefix) atomicAdd(&s.hist[(x >> s2) & dmask], 1u);
+            stage(base);
+#pragma unroll 1
+            for (int i = threadIdx.x; i < kRound; i += kSelThreads) {
+              const uint32_t kk = s.keys[kslot(i)], x = kk - kmin;
+              if (kk != 0u && kk >= kmin && (x >> rem) == prefix) atomicAdd(&s.hist[(x >> s2) & dmask], 1u);
             }
           }
         }
@@ -257,106 +330,105 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
       }
       T = kmin + prefix;
     }
+  } else if (resident) {
+    load(0, false);
+    __syncthreads();
   }
 
-  // ---- ordered compaction
-  const uint32_t lt = (1u << lane) - 1u;
-  // this CTA's counts of keys above T (and the forced position) and equal to T
-  {
+  // ---- ordered compaction: in a round, thread t owns keys 16t .. 16t + 15
+  auto sel_gt = [&](uint32_t kk, int64_t p) { return kk > T || p == forced; };
+  auto sel_eq = [&](uint32_t kk) { return kk == T && T != 0u; };
+  if (cs > 1) {
+    // this CTA's keys above T (and the forced position) and equal to T
     uint32_t gt = 0, eq = 0;
     for (int64_t base = 0; base < L; base += kRound) {
-      if (!resident || !ranked) load_round(vals, lo, hi, forced, base, key);
-      const int64_t p0 = lo + base + wid * (32 * kPer) + lane;
-#pragma unroll
+      stage(base);
+#pragma unroll 4
       for (int j = 0; j < kPer; ++j) {
-        gt += __popc(__ballot_sync(0xffffffffu, key[j] > T || p0 + 32 * j == forced));
-        eq += __popc(__ballot_sync(0xffffffffu, key[j] == T && T != 0u));
+        const int i = threadIdx.x + kSelThreads * j;
+        const uint32_t kk = s.keys[kslot(i)];
+        gt += sel_gt(kk, lo + base + i);
+        eq += sel_eq(kk);
       }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o);
+      eq += __shfl_xor_sync(0xffffffffu, eq, o);
     }
     if (lane == 0) {
       atomicAdd(&s.tot_gt, gt);
       atomicAdd(&s.tot_eq, eq);
     }
-  }
-  csync(cs);
-  if (threadIdx.x == 0) {
-    // ranks in order: equal keys before this CTA, outputs before it, all outputs
-    const uint32_t tg = tc::smem_u32(&s.tot_gt), te = tc::smem_u32(&s.tot_eq);
-    uint32_t ce = 0, co = 0, ce_me = 0, co_me = 0;
-    for (int r = 0; r < cs; ++r) {
-      const uint32_t g = cs > 1 ? tc::ld_dsmem_u32(tc::map_rank(tg, r)) : s.tot_gt;
-      const uint32_t e = cs > 1 ? tc::ld_dsmem_u32(tc::map_rank(te, r)) : s.tot_eq;
-      if (r == rk) {
-        ce_me = ce;
-        co_me = co;
+    csync(cs);
+    if (threadIdx.x == 0) {
+      // the keys above T and equal to T in lower ranks
+      const uint32_t tg = tc::smem_u32(&s.tot_gt), te = tc::smem_u32(&s.tot_eq);
+      uint32_t g_all = 0, e_all = 0;
+      for (int r = 0; r < cs; ++r) {
+        if (r == rk) {
+          s.carry_gt = g_all;
+          s.carry_eq = e_all;
+        }
+        g_all += tc::ld_dsmem_u32(tc::map_rank(tg, r));
+        e_all += tc::ld_dsmem_u32(tc::map_rank(te, r));
       }
-      const uint32_t take = krem > ce ? min(krem - ce, e) : 0u;
-      co += g + take;
-      ce += e;
     }
-    s.carry_eq = ce_me;
-    s.carry_off = co_me;
-    s.grand = co;
+    csync(cs);  // no CTA reads another's shared memory after this
   }
-  csync(cs);  // no CTA reads another's shared memory after this
   for (int64_t base = 0; base < L; base += kRound) {
-    if (!resident || !ranked) load_round(vals, lo, hi, forced, base, key);
-    const int64_t p0 = lo + base + wid * (32 * kPer) + lane;
+    stage(base);
+    uint32_t kk[kPer];
+#pragma unroll
+    for (int m = 0; m < kPer / 4; ++m) {
+      const uint4 v4 = *reinterpret_cast<const uint4*>(s.keys + kslot(kPer * threadIdx.x + 4 * m));
+      kk[4 * m] = v4.x;
+      kk[4 * m + 1] = v4.y;
+      kk[4 * m + 2] = v4.z;
+      kk[4 * m + 3] = v4.w;
+    }
+    const int64_t p0 = lo + base + kPer * threadIdx.x;
     uint32_t gt = 0, eq = 0;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      gt += __popc(__ballot_sync(0xffffffffu, key[j] > T || p0 + 32 * j == forced));
-      eq += __popc(__ballot_sync(0xffffffffu, key[j] == T && T != 0u));
+    for (int m = 0; m < kPer; ++m) {
+      gt += sel_gt(kk[m], p0 + m);
+      eq += sel_eq(kk[m]);
     }
-    if (lane == 0) {
-      s.wa[wid] = gt;
-      s.wb[wid] = eq;
-    }
+    const uint32_t v = gt | (eq << 16);
+    const uint32_t incl = warp_incl_scan(v);
+    if (lane == 31) s.wsum[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-      const uint32_t g = s.wa[lane], e = s.wb[lane];
-      uint32_t ie = e;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, ie, o);
-        if (lane >= o) ie += y;
-      }
-      const uint32_t e_before = s.carry_eq + ie - e;
-      const uint32_t take = krem > e_before ? min(krem - e_before, e) : 0u;
-      const uint32_t v = g + take;
-      uint32_t iv = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, iv, o);
-        if (lane >= o) iv += y;
-      }
-      const uint32_t off = s.carry_off + iv - v;
+      const uint32_t ws = s.wsum[lane], wi = warp_incl_scan(ws);
       __syncwarp();
-      s.wa[lane] = off;
-      s.wb[lane] = e_before;
-      if (lane == 31) {
-        s.carry_eq += ie;
-        s.carry_off += iv;
+      s.wsum[lane] = wi - ws;
+      if (lane == 31) s.wsum[kSelWarps] = wi;
+    }
+    __syncthreads();
+    const uint32_t before = s.wsum[wid] + incl - v;
+    uint32_t E = s.carry_eq + (before >> 16);
+    uint32_t off = s.carry_gt + (before & 0xFFFFu) + min(krem, E);
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      bool take = sel_gt(kk[m], p0 + m);
+      if (!take && sel_eq(kk[m])) take = E++ < krem;
+      if (take) {
+        if (off < (uint32_t)k) out[off] = idmap(p0 + m);
+        ++off;
       }
     }
-    __syncthreads();
-    uint32_t off = s.wa[wid], e_run = s.wb[wid];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int64_t p = p0 + 32 * j;
-      const bool is_eq = key[j] == T && T != 0u;
-      const uint32_t be = __ballot_sync(0xffffffffu, is_eq);
-      const bool sel = key[j] > T || p == forced || (is_eq && e_run + __popc(be & lt) < krem);
-      const uint32_t bs = __ballot_sync(0xffffffffu, sel);
-      const uint32_t o = off + __popc(bs & lt);
-      if (sel && o < (uint32_t)k) out[o] = idmap(p);
-      off += __popc(bs);
-      e_run += __popc(be);
+    __syncthreads();  // every thread has read the carries and the warp offsets
+    if (threadIdx.x == 0) {
+      s.carry_gt += s.wsum[kSelWarps] & 0xFFFFu;
+      s.carry_eq += s.wsum[kSelWarps] >> 16;
     }
-    __syncthreads();
   }
-  if (rk == cs - 1)
-    for (uint32_t i = s.grand + threadIdx.x; i < (uint32_t)k; i += kSelThreads) out[i] = -1;
+  // the last rank pads after every selection of the cluster
+  if (rk == cs - 1) {
+    __syncthreads();
+    const uint32_t total = s.carry_gt + min(krem, s.carry_eq);
+    for (uint32_t i = total + threadIdx.x; i < (uint32_t)k; i += kSelThreads) out[i] = -1;
+  }
 }
 
 // grid (cs, queries, selections), clusters of cs CTAs along x.  Selection 0:

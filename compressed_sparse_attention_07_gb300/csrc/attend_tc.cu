@@ -26,6 +26,9 @@
 // (exact for magnitudes in [2^-17, 65504]); accumulation is fp32.
 #include <algorithm>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "internal.h"
 #include "tc.cuh"
 
@@ -754,15 +757,16 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16]) {
 }
 
 template <int kDtype>
-__global__ void __launch_bounds__(kThreads, 1) attend_rows_kernel(AttArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    attend_rows_kernel(AttArgs a, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w) {
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   const int n = a.tiles_main + a.tiles_win;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* qs = smem;                                     // Q [64 heads x 512] f16, K-major
-  uint8_t* ctile = qs + kRowQBytes;                       // C[4]: [128 rows x 128 ch] f16, K-major
+  uint8_t* ctile = qs + kRowQBytes;                       // C [128 rows x 512 ch] f16, K-major
   uint8_t* pt = ctile + kRowCBytes;                       // P^T [64 heads x 128 rows] f16, K-major
   float* ml = reinterpret_cast<float*>(pt + kRowPBytes + 128 * 4);  // m[64] (log2 domain), l[64]
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar, tbar;
   __shared__ uint32_t tmem_base;
   __shared__ float red_m[4][kAllHeads], red_s[4][kAllHeads];
   __shared__ float mx[kAllHeads], alpha[kAllHeads];
@@ -773,14 +777,27 @@ __global__ void __launch_bounds__(kThreads, 1) attend_rows_kernel(AttArgs a) {
   const int t = (int)tc::cluster_rank();
   const int qi = blockIdx.y, b = qi / a.Tq;
   const bool fp4_tile = kMainFp4 && t < a.tiles_main;
+  const bool win_tile = t >= a.tiles_main;
 
-  // ---- loads: Q (16 bytes x 8 per thread), then quarter p of row r
-  uint4 qv[8];
+  // ---- Q (and the window tile: consecutive rows of the window buffer) by
+  // tensor copies straight into the K-major operand layout: a box of
+  // 8 elements x 8 rows x 64 16-byte units is one 8-row group (8 KB)
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_init(&tbar, 1);
+    tc::fence_mbar_init();
+    tc::mbar_arrive_expect_tx(&tbar, (uint32_t)(kRowQBytes + (win_tile ? kRowCBytes : 0)));
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int idx = tid + kThreads * i, h = idx >> 6, kk = (idx & 63) * 8;
-    qv[i] = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)qi * kHeads + h) * kDim + kk));
+    for (int g = 0; g < kAllHeads / 8; ++g) tc::tma_load_3d(qs + g * 8192, &tm_q, 0, qi * kHeads + 8 * g, 0, &tbar);
+    if (win_tile) {
+      const int w0 = (t - a.tiles_main) * 128;
+      const int row0 = (int)((int64_t)b * a.S + (__ldg(a.q_pos + qi) - a.W + 1 + w0) - __ldg(a.swa_pos0 + b));
+#pragma unroll 4
+      for (int g = 0; g < 16; ++g) tc::tma_load_3d(ctile + g * 8192, &tm_w, 0, row0 + 8 * g, 0, &tbar);
+    }
   }
+  __syncthreads();  // the barriers are initialised before anyone waits on them
+  // ---- main-cache rows: quarter p of row r straight into registers
   const int32_t sidx = slot_source(a, qi, b, t * 128 + r);
   uint4 raw[16];
   uint2 sc = make_uint2(0u, 0u);
@@ -797,35 +814,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_rows_kernel(AttArgs a) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) raw[j] = __ldg(g + j);
     }
-  } else if (sidx <= -2) {
-    const uint4* g = reinterpret_cast<const uint4*>(a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx)) * kDim + 128 * p);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) raw[j] = __ldg(g + j);
-  }
-
-  // ---- set-up while the rows arrive: Q to f16, barrier, TMEM (S^T 64 + O^T 4 x 64 columns)
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int idx = tid + kThreads * i, h = idx >> 6, kk = (idx & 63) * 8;
-    *reinterpret_cast<uint4*>(qs + tc::kmajor_off(h, kk, kDim)) =
-        make_uint4(bf16x2_to_f16x2(qv[i].x), bf16x2_to_f16x2(qv[i].y), bf16x2_to_f16x2(qv[i].z),
-                   bf16x2_to_f16x2(qv[i].w));
-  }
-  if (tid == 0) {
-    tc::mbar_init(&bar, 1);
-    tc::fence_mbar_init();
   }
   if (warp == 0) {
     tc::tmem_alloc(&tmem_base, 512);
     tc::tmem_relinquish();
   }
 
-  // ---- decode chunk p of row r into C[p]
-  uint8_t* ct = ctile + p * kCBytes;
-  if (sidx == -1) {
-#pragma unroll
-    for (int m = 0; m < 16; ++m) *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 8 * m, 128)) = make_uint4(0, 0, 0, 0);
-  } else if (fp4_tile) {
+  // ---- decode quarter p of row r (channels 128p..128p+127) into C
+  if (fp4_tile && sidx >= 0) {
     const uint32_t sw[2] = {sc.x, sc.y};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {  // 16 code bytes = 32 channels, two scale groups
@@ -837,16 +833,39 @@ __global__ void __launch_bounds__(kThreads, 1) attend_rows_kernel(AttArgs a) {
         uint32_t h4[4];
         e2m1x8_to_f16x2(w4[q], h4);
         const uint32_t s2 = q < 2 ? s_lo : s_hi;
-        *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 32 * j + 8 * q, 128)) =
+        *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(r, 128 * p + 32 * j + 8 * q, kDim)) =
             make_uint4(hmul2(h4[0], s2), hmul2(h4[1], s2), hmul2(h4[2], s2), hmul2(h4[3], s2));
       }
     }
-  } else {
+  } else if (!win_tile && sidx >= 0) {
 #pragma unroll
     for (int m = 0; m < 16; ++m)
-      *reinterpret_cast<uint4*>(ct + tc::kmajor_off(r, 8 * m, 128)) =
+      *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(r, 128 * p + 8 * m, kDim)) =
           make_uint4(bf16x2_to_f16x2(raw[m].x), bf16x2_to_f16x2(raw[m].y), bf16x2_to_f16x2(raw[m].z),
                      bf16x2_to_f16x2(raw[m].w));
+  } else if (!win_tile) {
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+      *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(r, 128 * p + 8 * m, kDim)) = make_uint4(0, 0, 0, 0);
+  }
+  // ---- the tensor copies: bf16 -> f16 in place (window rows outside the
+  // window or the buffer are zeroed)
+  bool ok = tc::mbar_wait(&tbar, 0, kSpin);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint4* u = reinterpret_cast<uint4*>(qs) + tid + kThreads * i;
+    const uint4 w = *u;
+    *u = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+  }
+  if (win_tile) {
+#pragma unroll 4
+    for (int m = 0; m < 16; ++m) {
+      uint4* u = reinterpret_cast<uint4*>(ctile + tc::kmajor_off(r, 128 * p + 8 * m, kDim));
+      const uint4 w = *u;
+      *u = sidx == -1 ? make_uint4(0, 0, 0, 0)
+                      : make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                                   bf16x2_to_f16x2(w.w));
+    }
   }
   tc::fence_async_smem();
   tc::fence_before_sync();
@@ -854,23 +873,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_rows_kernel(AttArgs a) {
   tc::fence_after_sync();
   const uint32_t tb = tmem_base;
 
-  // ---- S^T = sum_c C[c] . Q_c^T
+  // ---- S^T = sum over 16-channel steps of C . Q^T
   constexpr uint32_t kIdescS = tc::idesc_f16(128, kAllHeads, false, false, false, false);
   constexpr uint32_t kIdescO = tc::idesc_f16(128, kAllHeads, false, false, true, false);
-  if (tid == 0) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t cbase = tc::smem_u32(ctile + c * kCBytes);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ad = tc::sdesc(cbase + ks * 256, 128, 2048);
-        const uint64_t bd = tc::sdesc(tc::smem_u32(qs) + (c * 16 + ks * 2) * 128, 128, kDim * 16);
-        tc::mma_ss(tb, ad, bd, kIdescS, (c > 0 || ks > 0) ? 1u : 0u);
-      }
+  if (tid == 0 && ok) {
+#pragma unroll 4
+    for (int ks = 0; ks < kDim / 16; ++ks) {
+      const uint64_t ad = tc::sdesc(tc::smem_u32(ctile) + ks * 256, 128, kDim * 16);
+      const uint64_t bd = tc::sdesc(tc::smem_u32(qs) + ks * 256, 128, kDim * 16);
+      tc::mma_ss(tb, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
     }
-    tc::mma_commit(&bar);
   }
-  bool ok = tc::mbar_wait(&bar, 0, kSpin);
+  if (tid == 0) tc::mma_commit(&bar);
+  ok = tc::mbar_wait(&bar, 0, kSpin) && ok;
   tc::fence_after_sync();
 
   // ---- partial softmax over the tile's rows (thread: row r, heads 16p..16p+15)
@@ -910,16 +925,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_rows_kernel(AttArgs a) {
     ml[kAllHeads + tid] = red_s[0][tid] + red_s[1][tid] + red_s[2][tid] + red_s[3][tid];
   }
 
-  // ---- O^T[c] = C[c]^T . P^T
+  // ---- O^T[c] = C[:, chunk c]^T . P^T (C read MN-major: 8-row groups 8 KB apart)
   if (tid == 0) {
+    if (ok) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t cbase = tc::smem_u32(ctile + c * kCBytes);
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t cbase = tc::smem_u32(ctile) + c * 16 * 128;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t ad = tc::sdesc(cbase + ks * 2 * 2048, 2048, 128);
-        const uint64_t bd = tc::sdesc(tc::smem_u32(pt) + ks * 256, 128, 2048);
-        tc::mma_ss(tb + kAllHeads + kAllHeads * c, ad, bd, kIdescO, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = tc::sdesc(cbase + ks * 2 * (kDim * 16), kDim * 16, 128);
+          const uint64_t bd = tc::sdesc(tc::smem_u32(pt) + ks * 256, 128, 2048);
+          tc::mma_ss(tb + kAllHeads + kAllHeads * c, ad, bd, kIdescO, ks > 0 ? 1u : 0u);
+        }
       }
     }
     tc::mma_commit(&bar);
@@ -987,9 +1004,41 @@ __global__ void __launch_bounds__(kThreads, 1) attend_rows_kernel(AttArgs a) {
   }
 }
 
+// Tensor map over rows of 512 bf16 channels viewed as (8 elements, rows,
+// 64 16-byte units) with strides (row bytes, 16 bytes): a box of 8 x 8 x 64
+// lands as one 8-row group of the K-major interleaved operand layout.
+static bool encode_rows_map(CUtensorMap* tm, const void* base, uint64_t rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (rows == 0 || ((uintptr_t)base & 15u)) return false;
+  const cuuint64_t dims[3] = {8, rows, kDim / 8};
+  const cuuint64_t strides[2] = {kDim * 2, 16};
+  const cuuint32_t box[3] = {8, 8, kDim / 8};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int kDtype>
-cudaError_t launch_rows(const AttArgs& a, int Q, cudaStream_t stream) {
+cudaError_t launch_rows(const AttArgs& a, int Q, int B, cudaStream_t stream) {
   const int n_tiles = a.tiles_main + a.tiles_win;
+  CUtensorMap tm_q, tm_w;
+  if (!encode_rows_map(&tm_q, a.q, (uint64_t)Q * kHeads)) return cudaErrorNotSupported;
+  if (a.tiles_win > 0) {
+    if (!encode_rows_map(&tm_w, a.swa, (uint64_t)B * a.S)) return cudaErrorNotSupported;
+  } else {
+    tm_w = tm_q;  // not read
+  }
   auto kern = attend_rows_kernel<kDtype>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRowSmem);
   cudaLaunchConfig_t cfg = {};
@@ -1013,7 +1062,7 @@ cudaError_t launch_rows(const AttArgs& a, int Q, cudaStream_t stream) {
     schedulable[n_tiles] = yes ? 1 : -1;
   }
   if (schedulable[n_tiles] < 0) return cudaErrorNotSupported;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return cudaLaunchKernelEx(&cfg, kern, a, tm_q, tm_w);
 }
 
 template <int kDtype>
@@ -1095,8 +1144,8 @@ cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q,
   // query's tiles in one cluster; more: split by head groups
   const int n_tiles = a.tiles_main + a.tiles_win;
   if (n_tiles <= kRowMaxTiles) {
-    cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_rows<CSA2_CACHE_FP4>(a, Q, stream)
-                                                      : launch_rows<CSA2_CACHE_BF16>(a, Q, stream);
+    cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_rows<CSA2_CACHE_FP4>(a, Q, B, stream)
+                                                      : launch_rows<CSA2_CACHE_BF16>(a, Q, B, stream);
     if (e != cudaErrorNotSupported) return e;
   }
   if ((int64_t)Q * 4 * n_tiles <= 8 * (int64_t)num_sms() && n_tiles <= 16) {

@@ -25,6 +25,15 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
   __shared__ float e_s[kDim];          // the stored (decoded) entry
   __shared__ float kpart[8][kIdxDim];  // projection partial sums, 8 row slices
   const int m = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  // the W_idx rows this thread needs (64 independent 8-byte loads), issued
+  // first: they depend on nothing, so their latency overlaps the merge
+  const int kg = t & 31, rs = t >> 5;
+  uint2 wv[64];
+  {
+    const uint2* w2 = reinterpret_cast<const uint2*>(w_idx) + kg;  // row c at + c * 32
+#pragma unroll
+    for (int i = 0; i < 64; ++i) wv[i] = __ldg(w2 + (rs * 64 + i) * (kIdxDim / 4));
+  }
   const int64_t j = pos0[b] / r + m;
   // both block-table lookups early, off the critical path of the projection
   const int64_t page = page_of(mc, b, j, status);
@@ -81,15 +90,9 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
   __syncthreads();
 
   // indexer K = stored entry . W_idx: thread t owns columns 4*(t%32)..+3 over
-  // the 64-row slice t/32 (64 independent 8-byte loads in flight, each warp
-  // reading whole 256-byte rows); the 8 slice sums are added in slice order.
+  // the 64-row slice t/32 (each warp reads whole 256-byte rows); the 8 slice
+  // sums are added in slice order.
   {
-    const int kg = t & 31, rs = t >> 5;
-    const uint2* w2 = reinterpret_cast<const uint2*>(w_idx) + kg;  // row c at + c * 32
-    // all 64 row loads are issued before the first use (independent requests)
-    uint2 wv[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) wv[i] = __ldg(w2 + (rs * 64 + i) * (kIdxDim / 4));
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int i = 0; i < 64; ++i) {

@@ -8,6 +8,8 @@ namespace {
 template <int kDtype>
 __global__ void __launch_bounds__(128) gather_dequant_kernel(CacheView c, int channels, int n, const int32_t* ids,
                                                              float* out, int32_t* status) {
+  griddep_wait();
+  griddep_launch();
   const int i = blockIdx.x, b = blockIdx.y;
   const int32_t id = ids[(int64_t)b * n + i];
   float* o = out + ((int64_t)b * n + i) * channels;
@@ -46,10 +48,10 @@ cudaError_t launch_gather_dequant(const csa2_cache& c, int cache_dtype, int B, i
   if (B == 0 || n == 0) return cudaSuccess;
   dim3 grid(n, B);
   if (cache_dtype == CSA2_CACHE_FP4)
-    gather_dequant_kernel<CSA2_CACHE_FP4><<<grid, 128, 0, stream>>>(view_of(c), c.channels, n, ids, out, status);
-  else
-    gather_dequant_kernel<CSA2_CACHE_BF16><<<grid, 128, 0, stream>>>(view_of(c), c.channels, n, ids, out, status);
-  return cudaGetLastError();
+    return launch_k(gather_dequant_kernel<CSA2_CACHE_FP4>, grid, dim3(128), 0, stream, 0, view_of(c), c.channels, n,
+                    ids, out, status);
+  return launch_k(gather_dequant_kernel<CSA2_CACHE_BF16>, grid, dim3(128), 0, stream, 0, view_of(c), c.channels, n,
+                  ids, out, status);
 }
 
 }  // namespace csa2

@@ -26,9 +26,6 @@
 // (exact for magnitudes in [2^-17, 65504]); accumulation is fp32.
 #include <algorithm>
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "internal.h"
 #include "tc.cuh"
 
@@ -130,6 +127,8 @@ __device__ __forceinline__ int32_t slot_source(const AttArgs& a, int qi, int b, 
 
 template <int kDtype, int HG, int kStages>
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
+  griddep_wait();  // before any global read or tensor-memory allocation
+  griddep_launch();
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   constexpr int CPT = HG / 4;  // TMEM columns (heads) per thread in softmax / epilogue
   const int n_tiles = a.tiles_main + a.tiles_win;
@@ -441,6 +440,8 @@ constexpr size_t kSplitSmem = 2 * (size_t)kStageBytes + 4 * (size_t)kCBytes + kS
 
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
+  griddep_wait();  // before any global read or tensor-memory allocation
+  griddep_launch();
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   constexpr int HG = kSplitHG, CPT = kSplitCPT;
   const int n_tiles = a.tiles_main + a.tiles_win;
@@ -725,7 +726,7 @@ constexpr size_t kRowQBytes = (size_t)kAllHeads * kDim * 2;   // 65536
 constexpr size_t kRowCBytes = 4 * (size_t)kCBytes;            // 131072
 constexpr size_t kRowPBytes = (size_t)kAllHeads * 128 * 2;    // 16384
 constexpr size_t kRowSmem = kRowQBytes + kRowCBytes + kRowPBytes + 128 * 4 + 2 * kAllHeads * 4;
-constexpr int kRowMaxTiles = 6;                               // receive area n * ceil(4/n) * 32 KB <= 192 KB
+constexpr int kRowMaxTiles = 6;  // receive area n * ceil(4/n) * 32 KB <= 192 KB
 
 // Reduce v[16] over the 32 lanes of a warp (op = max or +): afterwards lane l
 // holds the result for entry l >> 1.  Each step hands half of the entries
@@ -758,15 +759,18 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16]) {
 
 template <int kDtype>
 __global__ void __launch_bounds__(kThreads, 1)
-    attend_rows_kernel(AttArgs a, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w) {
+    attend_rows_kernel(AttArgs a) {
+  griddep_wait();  // before any global read or tensor-memory allocation
+  griddep_launch();
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   const int n = a.tiles_main + a.tiles_win;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* qs = smem;                                     // Q [64 heads x 512] f16, K-major
   uint8_t* ctile = qs + kRowQBytes;                       // C [128 rows x 512 ch] f16, K-major
   uint8_t* pt = ctile + kRowCBytes;                       // P^T [64 heads x 128 rows] f16, K-major
+  int32_t* srcs = reinterpret_cast<int32_t*>(pt + kRowPBytes);      // row sources [128]
   float* ml = reinterpret_cast<float*>(pt + kRowPBytes + 128 * 4);  // m[64] (log2 domain), l[64]
-  __shared__ __align__(8) uint64_t bar, tbar;
+  __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tmem_base;
   __shared__ float red_m[4][kAllHeads], red_s[4][kAllHeads];
   __shared__ float mx[kAllHeads], alpha[kAllHeads];
@@ -777,94 +781,88 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t = (int)tc::cluster_rank();
   const int qi = blockIdx.y, b = qi / a.Tq;
   const bool fp4_tile = kMainFp4 && t < a.tiles_main;
-  const bool win_tile = t >= a.tiles_main;
 
-  // ---- Q (and the window tile: consecutive rows of the window buffer) by
-  // tensor copies straight into the K-major operand layout: a box of
-  // 8 elements x 8 rows x 64 16-byte units is one 8-row group (8 KB)
+  // ---- loads, coalesced: warp w fills the 8-row group w of C (and half of
+  // the 8-head group w % 8 of Q); lane l takes row 8w + l % 8 and 16-byte
+  // units 4k + l / 8, so each row is read in 64-byte runs and every warp-wide
+  // store covers whole 128-byte core-matrix rows
+  const int rl = lane & 7, uq = lane >> 3;
+  const int rho = 8 * warp + rl;
+  const int32_t sidx_l = slot_source(a, qi, b, t * 128 + rho);
+  uint4 qv[8];
+  {
+    const int h = 8 * (warp & 7) + rl, u0 = 32 * (warp >> 3);
+    const uint4* g = reinterpret_cast<const uint4*>(a.q + ((int64_t)qi * kHeads + h) * kDim);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) qv[k] = __ldg(g + u0 + 4 * k + uq);
+  }
+  uint4 raw[16];
+  uint32_t scl[4];
+  if (sidx_l >= 0) {
+    const int64_t page = sidx_l / kPage;
+    const int sl = sidx_l % kPage;
+    if (fp4_tile) {
+      const uint4* g = reinterpret_cast<const uint4*>(a.mc.data + page * kMainFp4Data + sl * (kDim / 2));
+      const uint16_t* gs = reinterpret_cast<const uint16_t*>(a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        raw[k] = __ldg(g + 4 * k + uq);
+        scl[k] = __ldg(gs + 4 * k + uq);
+      }
+    } else {
+      const uint4* g = reinterpret_cast<const uint4*>(a.mc.data + page * kMainBf16Data + sl * (kDim * 2));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) raw[k] = __ldg(g + 4 * k + uq);
+    }
+  } else if (sidx_l <= -2) {
+    const uint4* g = reinterpret_cast<const uint4*>(a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx_l)) * kDim);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) raw[k] = __ldg(g + 4 * k + uq);
+  }
+  if (uq == 0) srcs[rho] = sidx_l;
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
-    tc::mbar_init(&tbar, 1);
     tc::fence_mbar_init();
-    tc::mbar_arrive_expect_tx(&tbar, (uint32_t)(kRowQBytes + (win_tile ? kRowCBytes : 0)));
-#pragma unroll
-    for (int g = 0; g < kAllHeads / 8; ++g) tc::tma_load_3d(qs + g * 8192, &tm_q, 0, qi * kHeads + 8 * g, 0, &tbar);
-    if (win_tile) {
-      const int w0 = (t - a.tiles_main) * 128;
-      const int row0 = (int)((int64_t)b * a.S + (__ldg(a.q_pos + qi) - a.W + 1 + w0) - __ldg(a.swa_pos0 + b));
-#pragma unroll 4
-      for (int g = 0; g < 16; ++g) tc::tma_load_3d(ctile + g * 8192, &tm_w, 0, row0 + 8 * g, 0, &tbar);
-    }
-  }
-  __syncthreads();  // the barriers are initialised before anyone waits on them
-  // ---- main-cache rows: quarter p of row r straight into registers
-  const int32_t sidx = slot_source(a, qi, b, t * 128 + r);
-  uint4 raw[16];
-  uint2 sc = make_uint2(0u, 0u);
-  if (sidx >= 0) {
-    const int64_t page = sidx / kPage;
-    const int sl = sidx % kPage;
-    if (fp4_tile) {
-      const uint4* g = reinterpret_cast<const uint4*>(a.mc.data + page * kMainFp4Data + sl * (kDim / 2) + 64 * p);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) raw[j] = __ldg(g + j);
-      sc = __ldg(reinterpret_cast<const uint2*>(a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16) + 8 * p));
-    } else {
-      const uint4* g = reinterpret_cast<const uint4*>(a.mc.data + page * kMainBf16Data + sl * (kDim * 2) + 256 * p);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) raw[j] = __ldg(g + j);
-    }
   }
   if (warp == 0) {
     tc::tmem_alloc(&tmem_base, 512);
     tc::tmem_relinquish();
   }
-
-  // ---- decode quarter p of row r (channels 128p..128p+127) into C
-  if (fp4_tile && sidx >= 0) {
-    const uint32_t sw[2] = {sc.x, sc.y};
+  {
+    const int h = 8 * (warp & 7) + rl, u0 = 32 * (warp >> 3);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // 16 code bytes = 32 channels, two scale groups
-      const uint32_t sb = (sw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-      const uint32_t s_lo = f16x2_scale(sb & 0xFFu), s_hi = f16x2_scale(sb >> 8);
-      const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<uint4*>(qs + tc::kmajor_off(h, 8 * (u0 + 4 * k + uq), kDim)) =
+          make_uint4(bf16x2_to_f16x2(qv[k].x), bf16x2_to_f16x2(qv[k].y), bf16x2_to_f16x2(qv[k].z),
+                     bf16x2_to_f16x2(qv[k].w));
+  }
+  // ---- decode into C: FP4 code chunk q = 4k + l/8 (32 channels, two scale
+  // groups) -> units 4q..4q+3; bf16 unit u = 4k + l/8 -> unit u
+  if (fp4_tile) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t h4[4];
-        e2m1x8_to_f16x2(w4[q], h4);
-        const uint32_t s2 = q < 2 ? s_lo : s_hi;
-        *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(r, 128 * p + 32 * j + 8 * q, kDim)) =
-            make_uint4(hmul2(h4[0], s2), hmul2(h4[1], s2), hmul2(h4[2], s2), hmul2(h4[3], s2));
+    for (int k = 0; k < 4; ++k) {
+      const int q = 4 * k + uq;
+      const uint32_t s_lo = f16x2_scale(scl[k] & 0xFFu), s_hi = f16x2_scale((scl[k] >> 8) & 0xFFu);
+      const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (sidx_l >= 0) {
+          uint32_t h4[4];
+          e2m1x8_to_f16x2(w4[i], h4);
+          const uint32_t s2 = i < 2 ? s_lo : s_hi;
+          o = make_uint4(hmul2(h4[0], s2), hmul2(h4[1], s2), hmul2(h4[2], s2), hmul2(h4[3], s2));
+        }
+        *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 32 * q + 8 * i, kDim)) = o;
       }
     }
-  } else if (!win_tile && sidx >= 0) {
+  } else {
 #pragma unroll
-    for (int m = 0; m < 16; ++m)
-      *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(r, 128 * p + 8 * m, kDim)) =
-          make_uint4(bf16x2_to_f16x2(raw[m].x), bf16x2_to_f16x2(raw[m].y), bf16x2_to_f16x2(raw[m].z),
-                     bf16x2_to_f16x2(raw[m].w));
-  } else if (!win_tile) {
-#pragma unroll
-    for (int m = 0; m < 16; ++m)
-      *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(r, 128 * p + 8 * m, kDim)) = make_uint4(0, 0, 0, 0);
-  }
-  // ---- the tensor copies: bf16 -> f16 in place (window rows outside the
-  // window or the buffer are zeroed)
-  bool ok = tc::mbar_wait(&tbar, 0, kSpin);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint4* u = reinterpret_cast<uint4*>(qs) + tid + kThreads * i;
-    const uint4 w = *u;
-    *u = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
-  }
-  if (win_tile) {
-#pragma unroll 4
-    for (int m = 0; m < 16; ++m) {
-      uint4* u = reinterpret_cast<uint4*>(ctile + tc::kmajor_off(r, 128 * p + 8 * m, kDim));
-      const uint4 w = *u;
-      *u = sidx == -1 ? make_uint4(0, 0, 0, 0)
-                      : make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
-                                   bf16x2_to_f16x2(w.w));
+    for (int k = 0; k < 16; ++k) {
+      const uint4 o = sidx_l == -1 ? make_uint4(0, 0, 0, 0)
+                                   : make_uint4(bf16x2_to_f16x2(raw[k].x), bf16x2_to_f16x2(raw[k].y),
+                                                bf16x2_to_f16x2(raw[k].z), bf16x2_to_f16x2(raw[k].w));
+      *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 8 * (4 * k + uq), kDim)) = o;
     }
   }
   tc::fence_async_smem();
@@ -872,6 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = tmem_base;
+  const int32_t sidx = srcs[r];  // the row this thread reads from TMEM below
+  bool ok = true;
 
   // ---- S^T = sum over 16-channel steps of C . Q^T
   constexpr uint32_t kIdescS = tc::idesc_f16(128, kAllHeads, false, false, false, false);
@@ -980,65 +980,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
   __syncthreads();
   // ---- push the scaled partial output: chunk c goes to rank c % n, slot c / n,
-  // at [sender tile][slot][head][channel]
+  // at [sender tile][slot][head][channel] (a warp's stores are 128 contiguous
+  // bytes); the CTA's own chunk is written to its shared memory directly
   const int spo = (4 + n - 1) / n;
   const uint32_t recv = tc::smem_u32(smem);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const uint32_t dst = tc::map_rank(recv, c % n) + 4u * (uint32_t)(((t * spo + c / n) * kAllHeads + 16 * p) * 128 + r);
+    const int owner = c % n;
+    const uint32_t e0 = (uint32_t)(((t * spo + c / n) * kAllHeads + 16 * p) * 128 + r);
+    if (owner == t) {
+      float* dst = reinterpret_cast<float*>(smem) + e0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) tc::st_dsmem(dst + 4u * 128u * j, o[c][j] * alpha[16 * p + j]);
+      for (int j = 0; j < 16; ++j) dst[128 * j] = o[c][j] * alpha[16 * p + j];
+    } else {
+      const uint32_t dst = tc::map_rank(recv, owner) + 4u * e0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tc::st_dsmem(dst + 4u * 128u * j, o[c][j] * alpha[16 * p + j]);
+    }
   }
   tc::cluster_sync();
-  // ---- this CTA's chunks: sum the tiles' partials in tile order
+  // ---- this CTA's chunks: sum the tiles' partials in tile order, four
+  // channels per thread, 16-byte stores along the channels
   const float* rv = reinterpret_cast<const float*>(smem);
   for (int s2 = 0; s2 < spo; ++s2) {
     const int c = s2 * n + t;
     if (c >= 4) break;
-    for (int e = tid; e < kAllHeads * 128; e += kThreads) {
-      float acc = 0.0f;
-      for (int k2 = 0; k2 < n; ++k2) acc += rv[(k2 * spo + s2) * kAllHeads * 128 + e];
-      const int h = e >> 7, ch = e & 127;
-      a.out[((int64_t)qi * kHeads + h) * kDim + c * 128 + ch] = acc;
+    for (int e = tid; e < kAllHeads * 32; e += kThreads) {
+      const int h = e >> 5, ch4 = 4 * (e & 31);
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int k2 = 0; k2 < n; ++k2) {
+        const float4 v4 = *reinterpret_cast<const float4*>(rv + ((k2 * spo + s2) * kAllHeads + h) * 128 + ch4);
+        acc.x += v4.x;
+        acc.y += v4.y;
+        acc.z += v4.z;
+        acc.w += v4.w;
+      }
+      *reinterpret_cast<float4*>(a.out + ((int64_t)qi * kHeads + h) * kDim + c * 128 + ch4) = acc;
     }
   }
-}
-
-// Tensor map over rows of 512 bf16 channels viewed as (8 elements, rows,
-// 64 16-byte units) with strides (row bytes, 16 bytes): a box of 8 x 8 x 64
-// lands as one 8-row group of the K-major interleaved operand layout.
-static bool encode_rows_map(CUtensorMap* tm, const void* base, uint64_t rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-  if (!enc) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn) {
-      (void)cudaGetLastError();
-      return false;
-    }
-    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  if (rows == 0 || ((uintptr_t)base & 15u)) return false;
-  const cuuint64_t dims[3] = {8, rows, kDim / 8};
-  const cuuint64_t strides[2] = {kDim * 2, 16};
-  const cuuint32_t box[3] = {8, 8, kDim / 8};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int kDtype>
-cudaError_t launch_rows(const AttArgs& a, int Q, int B, cudaStream_t stream) {
+cudaError_t launch_rows(const AttArgs& a, int Q, cudaStream_t stream) {
   const int n_tiles = a.tiles_main + a.tiles_win;
-  CUtensorMap tm_q, tm_w;
-  if (!encode_rows_map(&tm_q, a.q, (uint64_t)Q * kHeads)) return cudaErrorNotSupported;
-  if (a.tiles_win > 0) {
-    if (!encode_rows_map(&tm_w, a.swa, (uint64_t)B * a.S)) return cudaErrorNotSupported;
-  } else {
-    tm_w = tm_q;  // not read
-  }
   auto kern = attend_rows_kernel<kDtype>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRowSmem);
   cudaLaunchConfig_t cfg = {};
@@ -1062,7 +1046,7 @@ cudaError_t launch_rows(const AttArgs& a, int Q, int B, cudaStream_t stream) {
     schedulable[n_tiles] = yes ? 1 : -1;
   }
   if (schedulable[n_tiles] < 0) return cudaErrorNotSupported;
-  return cudaLaunchKernelEx(&cfg, kern, a, tm_q, tm_w);
+  return launch_k(kern, cfg.gridDim, cfg.blockDim, kRowSmem, stream, n_tiles, a);
 }
 
 template <int kDtype>
@@ -1071,19 +1055,7 @@ cudaError_t launch_split(const AttArgs& a, int Q, cudaStream_t stream) {
   auto kern = attend_split_kernel<kDtype>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSplitSmem);
   if (n_tiles > 8) cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_tiles * (kHeads / kSplitHG), Q);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSplitSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = n_tiles;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return launch_k(kern, dim3(n_tiles * (kHeads / kSplitHG), Q), dim3(kThreads), kSplitSmem, stream, n_tiles, a);
 }
 
 template <int kDtype, int HG>
@@ -1097,8 +1069,7 @@ cudaError_t launch_hgs(const AttArgs& a, int Q, cudaStream_t stream) {
   const size_t smem = att_smem<kDtype, HG>(a.tiles_main + a.tiles_win, kStages);
   auto kern = attend_tc_kernel<kDtype, HG, kStages>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  kern<<<dim3(kHeads / HG, Q), kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_k(kern, dim3(kHeads / HG, Q), dim3(kThreads), smem, stream, 0, a);
 }
 
 constexpr size_t kSmemLimit = 225 * 1024;  // dynamic, leaving room for static shared memory
@@ -1144,8 +1115,8 @@ cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q,
   // query's tiles in one cluster; more: split by head groups
   const int n_tiles = a.tiles_main + a.tiles_win;
   if (n_tiles <= kRowMaxTiles) {
-    cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_rows<CSA2_CACHE_FP4>(a, Q, B, stream)
-                                                      : launch_rows<CSA2_CACHE_BF16>(a, Q, B, stream);
+    cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_rows<CSA2_CACHE_FP4>(a, Q, stream)
+                                                      : launch_rows<CSA2_CACHE_BF16>(a, Q, stream);
     if (e != cudaErrorNotSupported) return e;
   }
   if ((int64_t)Q * 4 * n_tiles <= 8 * (int64_t)num_sms() && n_tiles <= 16) {

@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
 #pragma unroll
     for (int i = 0; i < 64; ++i) wv[i] = __ldg(w2 + (rs * 64 + i) * (kIdxDim / 4));
   }
+  griddep_wait();  // the previous kernel may still read the cache pages written below
+  griddep_launch();
   const int64_t j = pos0[b] / r + m;
   // both block-table lookups early, off the critical path of the projection
   const int64_t page = page_of(mc, b, j, status);
@@ -146,14 +148,10 @@ cudaError_t launch_compress(const csa2_cfg& cfg, int B, int T, const uint16_t* x
   RopeFreqs rf;
   for (int i = 0; i < kRope / 2; ++i) rf.f[i] = std::pow(cfg.rope_theta, -2.0 * i / kRope);
   if (cfg.cache_dtype == CSA2_CACHE_FP4)
-    compress_kernel<CSA2_CACHE_FP4><<<grid, 256, 0, stream>>>(T, cfg.ratio, rf, x, pos0, merge_w,
-                                                              w_idx, view_of(main_c), view_of(idx_c),
-                                                              n_entries, status);
-  else
-    compress_kernel<CSA2_CACHE_BF16><<<grid, 256, 0, stream>>>(T, cfg.ratio, rf, x, pos0, merge_w,
-                                                               w_idx, view_of(main_c), view_of(idx_c),
-                                                               n_entries, status);
-  return cudaGetLastError();
+    return launch_k(compress_kernel<CSA2_CACHE_FP4>, grid, dim3(256), 0, stream, 0, T, cfg.ratio, rf, x, pos0, merge_w,
+                    w_idx, view_of(main_c), view_of(idx_c), n_entries, status);
+  return launch_k(compress_kernel<CSA2_CACHE_BF16>, grid, dim3(256), 0, stream, 0, T, cfg.ratio, rf, x, pos0, merge_w,
+                  w_idx, view_of(main_c), view_of(idx_c), n_entries, status);
 }
 
 }  // namespace csa2

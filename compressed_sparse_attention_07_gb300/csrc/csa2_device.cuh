@@ -114,25 +114,17 @@ __device__ __forceinline__ uint32_t e2m1_code(float x, float s) {
 // Score bit pattern marking a non-candidate position (a NaN never produced
 // by the scoring) and the monotone unsigned key of a score: larger score ->
 // larger key; the non-candidate pattern maps to key 0.
+// Programmatic dependent launch: wait until the previous kernel on the
+// stream has completed and its writes are visible; let the next kernel's
+// grid be scheduled (it waits for this one in turn).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 constexpr uint32_t kScoreInvalid = 0xFFFFFFFFu;
 __device__ __forceinline__ uint32_t order_key(float v) {
   const uint32_t u = __float_as_uint(v);
   if (u == kScoreInvalid) return 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Fold a key into a query's [min, max] key range kept in global memory
-// (warp-reduced first: one pair of atomics per warp).
-__device__ __forceinline__ void fold_key_range(uint32_t lo, uint32_t hi, uint32_t* kmin, uint32_t* kmax) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-  }
-  if ((threadIdx.x & 31) == 0 && lo <= hi) {
-    atomicMin(kmin, lo);
-    atomicMax(kmax, hi);
-  }
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {

@@ -439,14 +439,41 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
                                                                 const int32_t* __restrict__ n_entries,
                                                                 const int32_t* __restrict__ pool, const float* scores,
                                                                 const float* bmax, int64_t score_stride,
-                                                                const uint32_t* kmin, const uint32_t* kmax,
+                                                                const uint32_t* krange, int kr_stride, int n_slots,
                                                                 int32_t* topk_out, int32_t* pool_out) {
+  griddep_wait();  // the scores are the previous kernel's output
+  griddep_launch();
   extern __shared__ __align__(16) unsigned char sel_raw[];
   SelShared& s = *reinterpret_cast<SelShared*>(sel_raw);
+  __shared__ uint32_t r_lo, r_hi;
   const int cs = (int)tc::cluster_size(), rk = (int)tc::cluster_rank();
   const int qc = blockIdx.y, qi = q0 + qc, b = qi / Tq;
   const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
-  const uint32_t lo = kmin[qc], hi = kmax[qc];
+  // the query's key range: the scoring CTAs' slots reduced
+  if (threadIdx.x == 0) {
+    r_lo = 0xFFFFFFFFu;
+    r_hi = 0u;
+  }
+  __syncthreads();
+  {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    const uint32_t* kr = krange + (int64_t)qc * kr_stride * 2;
+    for (int i = threadIdx.x; i < n_slots; i += kSelThreads) {
+      lo = min(lo, kr[2 * i]);
+      hi = max(hi, kr[2 * i + 1]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if ((threadIdx.x & 31) == 0 && lo <= hi) {
+      atomicMin(&r_lo, lo);
+      atomicMax(&r_hi, hi);
+    }
+  }
+  __syncthreads();
+  const uint32_t lo = r_lo, hi = r_hi;
   if (blockIdx.z == 0) {
     const float* v = scores + (int64_t)qc * score_stride;
     if (pool)
@@ -466,12 +493,17 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 }  // namespace
 
 // Per query: scores (Full: max_entries, Reindex: pool positions), HSI block
-// maxima (Full with HSI), and the [min, max] key range (8 bytes, padded).
+// maxima (Full with HSI), and the scoring CTAs' key-range slots (8 bytes each).
+static int64_t score_tiles(const csa2_cfg& cfg, int max_entries, bool reindex) {
+  return reindex ? ((int64_t)cfg.hsi_blocks * kHsiBlock + 127) / 128 : ((int64_t)max_entries + 127) / 128;
+}
+
 size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex) {
-  if (reindex) return align256((size_t)cfg.hsi_blocks * kHsiBlock * sizeof(float)) + 512;
+  const size_t slots = align256((size_t)score_range_slots(score_tiles(cfg, max_entries, reindex)) * 8);
+  if (reindex) return align256((size_t)cfg.hsi_blocks * kHsiBlock * sizeof(float)) + slots;
   size_t b = align256((size_t)max_entries * sizeof(float));
   if (cfg.hsi_blocks > 0) b += align256((size_t)((max_entries + 7) / 8) * sizeof(float));
-  return b + 512;
+  return b + slots;
 }
 
 cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx,
@@ -493,38 +525,24 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
     bmax = reinterpret_cast<float*>(cur);
     cur += align256((size_t)chunk * ((max_entries + 7) / 8) * sizeof(float));
   }
-  uint32_t* kmin = reinterpret_cast<uint32_t*>(cur);
-  uint32_t* kmax = reinterpret_cast<uint32_t*>(cur + align256((size_t)chunk * sizeof(uint32_t)));
+  uint32_t* krange = reinterpret_cast<uint32_t*>(cur);
+  const int kr_stride = score_range_slots(score_tiles(cfg, max_entries, reindex));
+  // one CTA per kRound positions of the longest selection, up to a cluster of 8
+  const int64_t n_max = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
+  int cs = 1;
+  while (cs < 8 && (int64_t)cs * kRound < n_max) cs <<= 1;
+  const size_t sel_smem = sizeof(SelShared);
+  cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
   for (int q0 = 0; q0 < Q; q0 += chunk) {
     const int nq = std::min(chunk, Q - q0);
-    cudaMemsetAsync(kmin, 0xFF, (size_t)nq * sizeof(uint32_t), stream);  // empty ranges
-    cudaMemsetAsync(kmax, 0x00, (size_t)nq * sizeof(uint32_t), stream);
+    int n_slots = 0;
     cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, scores,
-                                    stride, bmax, kmin, kmax, status, num_sms(), stream);
+                                    stride, bmax, krange, kr_stride, &n_slots, status, num_sms(), stream);
     if (e != cudaSuccess) return e;
-    // one CTA per kRound positions of the longest selection, up to a cluster of 8
-    const int64_t n_max = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
-    int cs = 1;
-    while (cs < 8 && (int64_t)cs * kRound < n_max) cs <<= 1;
-    const size_t sel_smem = sizeof(SelShared);
-    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(cs, nq, (!reindex && pool_out) ? 2 : 1);
-    lc.blockDim = dim3(kSelThreads);
-    lc.dynamicSmemBytes = sel_smem;
-    lc.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = cs;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    lc.attrs = at;
-    lc.numAttrs = 1;
-    e = cudaLaunchKernelEx(&lc, select_kernel, q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, (int64_t)max_entries,
-                           q_pos, n_entries, pool, (const float*)scores, (const float*)bmax, stride,
-                           (const uint32_t*)kmin, (const uint32_t*)kmax, topk_out, pool_out);
-    if (e != cudaSuccess) return e;
-    e = cudaGetLastError();
+    e = launch_k(select_kernel, dim3(cs, nq, (!reindex && pool_out) ? 2 : 1), dim3(kSelThreads), sel_smem, stream, cs,
+                 q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, (int64_t)max_entries, q_pos, n_entries, pool,
+                 (const float*)scores, (const float*)bmax, stride, (const uint32_t*)krange, kr_stride, n_slots,
+                 topk_out, pool_out);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -17,7 +17,7 @@
 //    (f16 / bf16) from shared memory;
 //  - the epilogue reads D back (one row per thread), forms the ReLU-weighted
 //    head sums, writes the scores, the 8-entry block maxima for HSI and folds
-//    the per-query key range used by the top-k selection.
+//    this CTA's key range per query (one slot each) for the top-k selection.
 // A warpgroup decodes its next tile while its previous MMA runs, and the two
 // warpgroups interleave on the tensor core.  Every wait is bounded.
 #include <algorithm>
@@ -62,8 +62,8 @@ struct ScoreArgs {
   float* scores;        // [chunk][stride]
   int64_t stride;
   float* bmax;          // [chunk][ceil(max_entries/8)] or null
-  uint32_t* kmin;       // [chunk] key range of each query's scores
-  uint32_t* kmax;
+  uint32_t* krange;     // [chunk][kr_stride][2]: key range of each CTA's scores of each query
+  int kr_stride;
   int32_t* status;
 };
 
@@ -116,6 +116,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   constexpr bool kBf16 = (kDtype == CSA2_CACHE_BF16);
   constexpr uint32_t kIdesc = tc::idesc_f16(128, kN, kBf16, kBf16, false, false);
   static_assert(!kGather || QPC == 1, "gather mode scores one query per CTA");
+  griddep_wait();  // before any global read or tensor-memory allocation
+  griddep_launch();
 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* qtile = smem;                          // [kN rows][128] K-major, 256*kN B
@@ -124,6 +126,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], mma_bar[kWG];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ uint32_t rng_lo[QPC], rng_hi[QPC];  // this CTA's key range per query
   __shared__ int32_t ptab[kGather ? 1 : 2 * kMaxTilesPerCta];     // page mode: pages of this CTA's tiles
   __shared__ int32_t gtab[kGather ? kMaxGatherTiles * 128 : 1];   // gather mode: page*64+slot or -1
 
@@ -142,7 +145,14 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   const int64_t n_tiles = (npos + 127) / 128;
   const int64_t t_begin = (int64_t)blockIdx.x * a.tiles_per_cta;
   const int64_t t_end = t_begin + a.tiles_per_cta < n_tiles ? t_begin + a.tiles_per_cta : n_tiles;
-  if (t_begin >= t_end) return;  // uniform: the whole CTA leaves before any barrier
+  if (t_begin >= t_end) {  // uniform: the whole CTA leaves before any barrier, its slots empty
+    if (tid < QPC) {
+      uint32_t* kr = a.krange + ((int64_t)(blockIdx.y * QPC + tid) * a.kr_stride + blockIdx.x) * 2;
+      kr[0] = 0xFFFFFFFFu;
+      kr[1] = 0u;
+    }
+    return;
+  }
   const int n_my = (int)(t_end - t_begin);
 
   // ---- set-up: Q_idx (f16 or bf16) into the B tile, head weights, pages, barriers, TMEM
@@ -194,6 +204,10 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     }
     for (int w = 0; w < kWG; ++w) tc::mbar_init(&mma_bar[w], 1);
     abort_flag = 0;
+    for (int q = 0; q < QPC; ++q) {
+      rng_lo[q] = 0xFFFFFFFFu;
+      rng_hi[q] = 0u;
+    }
     tc::fence_mbar_init();
   }
   if (warp == 0) {
@@ -398,8 +412,18 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   }
   if (kGather) cp_wait<0>();  // no copies into this CTA's shared memory outlive it
 #pragma unroll
-  for (int q = 0; q < QPC; ++q)
-    fold_key_range(klo[q], khi[q], a.kmin + blockIdx.y * QPC + q, a.kmax + blockIdx.y * QPC + q);
+  for (int q = 0; q < QPC; ++q) {
+    uint32_t lo = klo[q], hi = khi[q];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if ((tid & 31) == 0 && lo <= hi) {
+      atomicMin(&rng_lo[q], lo);
+      atomicMax(&rng_hi[q], hi);
+    }
+  }
   // after an abort, let the last issued MMA finish before TMEM is released
   if (last_issued > waited) {
     if (!tc::mbar_wait(&mma_bar[g], last_issued & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
@@ -407,6 +431,11 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   tc::fence_before_sync();
   consumers_sync(kConsumers);
   if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
+  if (tid < QPC) {  // one slot per CTA and query: no initialisation of global state needed
+    uint32_t* kr = a.krange + ((int64_t)(blockIdx.y * QPC + tid) * a.kr_stride + blockIdx.x) * 2;
+    kr[0] = rng_lo[tid];
+    kr[1] = rng_hi[tid];
+  }
 }
 
 }  // namespace
@@ -420,14 +449,14 @@ static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaSt
   smem = std::max<size_t>(smem, 116 * 1024);
   auto kern = score_tc_kernel<kDtype, QPC, kGather>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  kern<<<dim3(splits, groups), Sh::kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_k(kern, dim3(splits, groups), dim3(Sh::kThreads), smem, stream, 0, a);
 }
 
 cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
                             const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
                             int64_t max_entries, const int32_t* pool, float* scores, int64_t stride, float* bmax,
-                            uint32_t* kmin, uint32_t* kmax, int32_t* status, int num_sms, cudaStream_t stream) {
+                            uint32_t* krange, int kr_stride, int* n_slots, int32_t* status, int num_sms,
+                            cudaStream_t stream) {
   const bool gather = pool != nullptr;
   const int qpc = (!gather && Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) ? 4 : 1;
   const int groups = nq / qpc;
@@ -437,8 +466,10 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   const int64_t cap = gather ? kMaxGatherTiles : kMaxTilesPerCta;
   const int64_t per = std::min<int64_t>(cap, std::max<int64_t>(4, (tiles + want - 1) / want));
   const int splits = (int)((tiles + per - 1) / per);
+  if (splits > kr_stride) return cudaErrorInvalidValue;
+  *n_slots = splits;
   ScoreArgs a{q0, Tq, cfg.ratio, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
-              pool, cfg.hsi_blocks, scores, stride, bmax, kmin, kmax, status};
+              pool, cfg.hsi_blocks, scores, stride, bmax, krange, kr_stride, status};
   if (cfg.cache_dtype == CSA2_CACHE_FP4) {
     if (gather) return launch_one<CSA2_CACHE_FP4, 1, true>(a, groups, splits, stream);
     return qpc == 4 ? launch_one<CSA2_CACHE_FP4, 4, false>(a, groups, splits, stream)

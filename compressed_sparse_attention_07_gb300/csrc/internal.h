@@ -4,10 +4,41 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/csa2.h"
 #include "csa2_device.cuh"
 
 namespace csa2 {
+
+// Launch with programmatic stream serialization: the grid may be scheduled
+// while the previous kernel on the stream finishes; every kernel of the
+// library waits for its predecessor (griddep_wait) before touching global
+// memory or allocating tensor memory.  cluster_x > 0 adds a cluster shape.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster_x,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster_x > 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster_x;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 inline CacheView view_of(const csa2_cache& c) {
   return CacheView{static_cast<uint8_t*>(c.data), static_cast<uint8_t*>(c.scales), c.block_table,
@@ -27,7 +58,12 @@ int num_sms();
 cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
                             const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
                             int64_t max_entries, const int32_t* pool, float* scores, int64_t stride, float* bmax,
-                            uint32_t* kmin, uint32_t* kmax, int32_t* status, int num_sms, cudaStream_t stream);
+                            uint32_t* krange, int kr_stride, int* n_slots, int32_t* status, int num_sms,
+                            cudaStream_t stream);
+
+// Key-range slots per query in the indexer workspace: one per scoring CTA
+// (at least four 128-entry tiles each).
+inline int score_range_slots(int64_t tiles) { return (int)((tiles + 3) / 4); }
 
 // Per-query workspace bytes of the indexer (scores + HSI block maxima).
 size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex);

@@ -461,8 +461,11 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   const int qpc = (!gather && Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) ? 4 : 1;
   const int groups = nq / qpc;
   const int64_t tiles = gather ? ((int64_t)cfg.hsi_blocks * kHsiBlock + 127) / 128 : (max_entries + 127) / 128;
-  // enough CTAs for a couple of waves, at least 4 tiles each
-  const int64_t want = std::max<int64_t>(1, (int64_t)(qpc == 1 ? 2 : 1) * num_sms / std::max(groups, 1));
+  // CTAs per query group: one wave of one CTA per SM when there are few
+  // groups (latency-bound: every CTA starts at once), else two waves for
+  // balance; at least 4 tiles each
+  const int waves = (qpc == 1 && (int64_t)groups * 8 > num_sms) ? 2 : 1;
+  const int64_t want = std::max<int64_t>(1, (int64_t)waves * num_sms / std::max(groups, 1));
   const int64_t cap = gather ? kMaxGatherTiles : kMaxTilesPerCta;
   const int64_t per = std::min<int64_t>(cap, std::max<int64_t>(4, (tiles + want - 1) / want));
   const int splits = (int)((tiles + per - 1) / per);

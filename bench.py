@@ -49,6 +49,20 @@ IDX_ENTRY_BYTES = {"fp4": 72, "bf16": 256}
 MAIN_ENTRY_BYTES = {"fp4": 288, "bf16": 1024}
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
+# stage's kernels, from one ncu capture of this bench's default command; the
+# summaries under profiles/ name the capture.  A stage with no capture of the
+# current kernels reports null.
+TRAFFIC = {
+    "decode_b8_ctx32768_r2_fp4": {
+        "compress": (180224, "profiles/compress_kernel_decode_b8_ctx32768_r2_fp4.md"),
+        "index_topk": (9554944 + 630528, "profiles/score_tc_kernel_decode_b8_ctx32768_r2_fp4.md + "
+                                         "profiles/select_kernel_decode_b8_ctx32768_r2_fp4.md"),
+        "attend": (3208704, "profiles/attend_rows_kernel_decode_b8_ctx32768_r2_fp4.md"),
+    },
+}
+
+
 def attend_query_bytes(cache, topk=512, window=128):
     return topk * MAIN_ENTRY_BYTES[cache] + window * 1024 + 64 * 512 * 2 + 64 * 512 * 4 + topk * 4
 
@@ -208,7 +222,7 @@ class DecodeStep(StepBase):
                             "index_topk": B * self.N * eb,
                             "attend": B * attend_query_bytes(wl.cache, wl.topk, wl.window)}
         self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_tc_kernel + select_kernel",
-                              "attend": "attend_tc_kernel"}
+                              "attend": "attend_rows_kernel"}
         self.units = B
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N}
 
@@ -265,7 +279,7 @@ class PrefillStep(StepBase):
                             "attend": B * Tq * attend_query_bytes(wl.cache, wl.topk, wl.window)}
         self.stage_flops = {"index_topk": pairs * 8192, "attend": B * Tq * 4 * 64 * 512 * (wl.topk + wl.window)}
         self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_tc_kernel + select_kernel",
-                              "attend": "attend_tc_kernel"}
+                              "attend": "attend_rows_kernel"}
         self.units = B * Tq
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "query_tokens": Tq, "entries": self.N,
                           "index_pairs": pairs}
@@ -319,8 +333,9 @@ class GroupStep(StepBase):
             extra = {"full": B * (self.N * 72 + r * 1024 + 360), "reindex": B * wl.hsi_blocks * 8 * 72,
                      "reuse": 0}[m]
             self.stage_bytes["L%d_%s" % (l, m)] = att + extra
-        self.stage_kernels = {st: {"full": "compress + score_tc + select + attend_tc",
-                                   "reindex": "score_pool + select + attend_tc", "reuse": "attend_tc"}[st.split("_")[1]]
+        self.stage_kernels = {st: {"full": "compress + score_tc + select + attend_rows",
+                                   "reindex": "score_tc (gather) + select + attend_rows",
+                                   "reuse": "attend_rows"}[st.split("_")[1]]
                               for st in self.stages}
         self.units = B
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N, "layers": len(self.layers),
@@ -638,8 +653,9 @@ def main():
                 "algorithmic_flops_per_launch": flops, "launch_ms": stage_ms[dom]}
     else:
         ach = step.stage_bytes[dom] / (stage_ms[dom] / 1e3) / 1e9
+        traffic, traffic_src = TRAFFIC.get(step.wl.name, {}).get(dom, (None, None))
         roof = {"bound": "hbm", "kernel": step.stage_kernels[dom], "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "traffic": None,
+                "frac": ach / hbm, "traffic": traffic, "traffic_source": traffic_src,
                 "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "of fallback",
                 "algorithmic_bytes_per_launch": step.stage_bytes[dom], "launch_ms": stage_ms[dom]}
     cpu = None

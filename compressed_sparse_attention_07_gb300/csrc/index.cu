@@ -527,10 +527,13 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
   }
   uint32_t* krange = reinterpret_cast<uint32_t*>(cur);
   const int kr_stride = score_range_slots(score_tiles(cfg, max_entries, reindex));
-  // one CTA per kRound positions of the longest selection, up to a cluster of 8
+  // one CTA per kRound positions of the longest selection, up to a cluster of
+  // 8, but no more CTAs than one wave holds (one CTA per SM)
   const int64_t n_max = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
+  const int n_sel = (!reindex && pool_out) ? 2 : 1;
+  const int64_t sel_groups = (int64_t)std::min(chunk, Q) * n_sel;
   int cs = 1;
-  while (cs < 8 && (int64_t)cs * kRound < n_max) cs <<= 1;
+  while (cs < 8 && (int64_t)cs * kRound < n_max && 2 * cs * sel_groups <= num_sms()) cs <<= 1;
   const size_t sel_smem = sizeof(SelShared);
   cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
   for (int q0 = 0; q0 < Q; q0 += chunk) {
@@ -539,7 +542,7 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
     cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, scores,
                                     stride, bmax, krange, kr_stride, &n_slots, status, num_sms(), stream);
     if (e != cudaSuccess) return e;
-    e = launch_k(select_kernel, dim3(cs, nq, (!reindex && pool_out) ? 2 : 1), dim3(kSelThreads), sel_smem, stream, cs,
+    e = launch_k(select_kernel, dim3(cs, nq, n_sel), dim3(kSelThreads), sel_smem, stream, cs,
                  q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, (int64_t)max_entries, q_pos, n_entries, pool,
                  (const float*)scores, (const float*)bmax, stride, (const uint32_t*)krange, kr_stride, n_slots,
                  topk_out, pool_out);

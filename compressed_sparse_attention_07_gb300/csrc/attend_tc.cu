@@ -780,7 +780,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t lane_base = 32 * quad;
   const int t = (int)tc::cluster_rank();
   const int qi = blockIdx.y, b = qi / a.Tq;
-  const bool fp4_tile = kMainFp4 && t < a.tiles_main;
+  // this CTA's rows: 8-row groups of the query's slots dealt round-robin over
+  // the cluster (warp w takes slot group w * n + t), so that every CTA gets
+  // about the same share of FP4 top-k rows and bf16 window rows; the softmax
+  // and the merge see the rows as a set
+  const int slot0 = 8 * (warp * n + t);
+  const bool fp4_tile = kMainFp4 && slot0 < a.tiles_main * 128;
 
   // ---- loads, coalesced: warp w fills the 8-row group w of C (and half of
   // the 8-head group w % 8 of Q); lane l takes row 8w + l % 8 and 16-byte
@@ -788,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // store covers whole 128-byte core-matrix rows
   const int rl = lane & 7, uq = lane >> 3;
   const int rho = 8 * warp + rl;
-  const int32_t sidx_l = slot_source(a, qi, b, t * 128 + rho);
+  const int32_t sidx_l = slot_source(a, qi, b, slot0 + rl);
   uint4 qv[8];
   {
     const int h = 8 * (warp & 7) + rl, u0 = 32 * (warp >> 3);

@@ -25,8 +25,10 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
   __shared__ float e_s[kDim];          // the stored (decoded) entry
   __shared__ float kpart[8][kIdxDim];  // projection partial sums, 8 row slices
   const int m = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  griddep_wait();  // every input may be the previous kernel's output
+  griddep_launch();
   // the W_idx rows this thread needs (64 independent 8-byte loads), issued
-  // first: they depend on nothing, so their latency overlaps the merge
+  // first: their latency overlaps the merge
   const int kg = t & 31, rs = t >> 5;
   uint2 wv[64];
   {
@@ -34,8 +36,6 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
 #pragma unroll
     for (int i = 0; i < 64; ++i) wv[i] = __ldg(w2 + (rs * 64 + i) * (kIdxDim / 4));
   }
-  griddep_wait();  // the previous kernel may still read the cache pages written below
-  griddep_launch();
   const int64_t j = pos0[b] / r + m;
   // both block-table lookups early, off the critical path of the projection
   const int64_t page = page_of(mc, b, j, status);

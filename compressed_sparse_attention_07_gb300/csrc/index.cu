@@ -20,6 +20,8 @@ constexpr int kCandMax = 8192;        // keys of the threshold bin listed in sha
 
 // ---------------------------------------------------------------- select ----
 
+constexpr int kMinCtaKeys = kRound;  // positions per CTA of a selection cluster, at least
+                                     // (below that the cluster's merges cost more than they save)
 constexpr int kRankMax = 512;  // threshold-bin candidates ranked directly (else refined by digits)
 
 struct SelShared {
@@ -28,7 +30,7 @@ struct SelShared {
   uint32_t merged[kHistBins];  // the cluster's histogram
   uint32_t cand[kCandMax];     // this CTA's keys of the threshold bin, minus kmin (peers read them)
   uint32_t all[kRankMax];      // the cluster's threshold-bin keys
-  uint32_t part[kSelThreads];  // bin sums per thread (find_cut)
+  uint32_t part[kSelThreads];  // bin sums per thread (find_cut); rank counts per candidate
   uint32_t wsum[kSelWarps + 1];
   uint32_t cut_bin, cut_above, cut_total, cand_n, c_all, t_x, t_krem, carry_eq, carry_gt, grand;
   uint32_t tot_gt, tot_eq;     // this CTA's counts for the compaction (peers read them)
@@ -56,45 +58,37 @@ struct IdMap {
 // The bin, counting down from the top, where the running count reaches
 // `need` (>= 1): s.cut_bin, s.cut_above = keys in higher bins, s.cut_total =
 // all keys (the cut is set only when cut_total >= need).  Every thread sums
-// nbins/kSelThreads bins (thread t from the top); warp 0 then finds the
-// 32-thread group, the thread and the bin with three warp scans.
+// nbins/kSelThreads bins (thread t from the top) and scans them within its
+// warp; warp 0 scans the warp totals; the one thread whose bins hold the
+// cut walks them.
 __device__ void find_cut(const uint32_t* hist, int nbins, uint32_t need, SelShared& s) {
   const int per = nbins / kSelThreads;
-  const int t = threadIdx.x, lane = t & 31;
-  {
-    const int top = nbins - 1 - per * t;
-    uint32_t sum = 0;
-    for (int i = 0; i < per; ++i) sum += hist[top - i];
-    s.part[t] = sum;
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  const int top = nbins - 1 - per * t;
+  uint32_t sum = 0;
+  for (int i = 0; i < per; ++i) sum += hist[top - i];
+  const uint32_t incl = warp_incl_scan(sum);
+  if (lane == 31) s.wsum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t ws = s.wsum[lane], wi = warp_incl_scan(ws);
+    __syncwarp();
+    s.wsum[lane] = wi - ws;
+    if (lane == 31) s.cut_total = wi;
   }
   __syncthreads();
-  if (t < 32) {
-    uint32_t acc = 0;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) acc += s.part[32 * lane + i];
-    const uint32_t incl = warp_incl_scan(acc), excl = incl - acc;
-    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-    const uint32_t g = __ballot_sync(0xffffffffu, excl < need && incl >= need);
-    if (g) {
-      const int G = __ffs(g) - 1;
-      uint32_t above = __shfl_sync(0xffffffffu, excl, G);
-      const uint32_t pv = s.part[32 * G + lane];
-      const uint32_t pi = warp_incl_scan(pv);
-      const uint32_t h = __ballot_sync(0xffffffffu, above + pi - pv < need && above + pi >= need);
-      const int P = __ffs(h) - 1;
-      above += __shfl_sync(0xffffffffu, pi - pv, P);
-      const int top = nbins - 1 - per * (32 * G + P);
-      const uint32_t hv = lane < per ? hist[top - lane] : 0u;
-      const uint32_t hi = warp_incl_scan(hv);
-      const uint32_t hb = __ballot_sync(0xffffffffu, lane < per && above + hi - hv < need && above + hi >= need);
-      const int Bn = __ffs(hb) - 1;
-      const uint32_t ab = __shfl_sync(0xffffffffu, hi - hv, Bn);
-      if (lane == 0) {
-        s.cut_bin = (uint32_t)(top - Bn);
-        s.cut_above = above + ab;
+  const uint32_t excl = s.wsum[wid] + incl - sum;
+  if (excl < need && excl + sum >= need) {
+    uint32_t above = excl;
+    for (int i = 0; i < per; ++i) {
+      const uint32_t h = hist[top - i];
+      if (above + h >= need) {
+        s.cut_bin = (uint32_t)(top - i);
+        s.cut_above = above;
+        break;
       }
+      above += h;
     }
-    if (lane == 0) s.cut_total = total;
   }
   __syncthreads();
 }
@@ -128,7 +122,8 @@ __device__ __forceinline__ float ld_score(const float* p) {
 
 // Shared-memory slot of key i of a round: 16-byte units are XOR-swizzled so
 // that both the coalesced pattern (thread t, key t + 1024j) and one thread
-// reading the 16 consecutive keys of its own range hit distinct banks.
+// reading the 16 consecutive keys of its own range hit distinct banks.  The
+// XOR term depends on bits 5-7 of i only, so kslot(t + 1024 j) = kslot(t) + 1024 j.
 __device__ __forceinline__ int kslot(int i) {
   const int u = i >> 2;
   return ((u ^ ((u >> 3) & 7)) << 2) | (i & 3);
@@ -182,11 +177,12 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
       const int64_t p = lo + base + threadIdx.x + kSelThreads * j;
       v[j] = p < hi ? ld_score(vals + p) : __uint_as_float(kScoreInvalid);
     }
+    const int ks0 = kslot(threadIdx.x);  // kslot(t + 1024 j) = kslot(t) + 1024 j
+    const int64_t f = forced - (lo + base) - threadIdx.x;  // j * 1024 at the forced position
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int i = threadIdx.x + kSelThreads * j;
-      const uint32_t kk = (lo + base + i == forced) ? 0u : order_key(v[j]);
-      s.keys[kslot(i)] = kk;
+      const uint32_t kk = (f == (int64_t)kSelThreads * j) ? 0u : order_key(v[j]);
+      s.keys[ks0 + kSelThreads * j] = kk;
       if (count && kk) atomicAdd(&s.hist[bin_of(kk)], 1u);
     }
   };
@@ -234,7 +230,7 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
           stage(base);
 #pragma unroll 4
           for (int j = 0; j < kPer; ++j) {
-            const uint32_t kk = s.keys[kslot(threadIdx.x + kSelThreads * j)];
+            const uint32_t kk = s.keys[kslot(threadIdx.x) + kSelThreads * j];
             const bool m = kk != 0u && bin_of(kk) == tb;
             const uint32_t bal = __ballot_sync(0xffffffffu, m);
             if (!bal) continue;
@@ -273,17 +269,28 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
             C = s.all;
             __syncthreads();
           }
-          // rank of each candidate among the threshold-bin keys
-          for (uint32_t i = threadIdx.x; i < c_all; i += kSelThreads) {
+          // rank of each candidate among the threshold-bin keys: the c x c
+          // comparisons spread over all threads (tpc threads per candidate,
+          // counts gathered in shared memory: gt in the low 16 bits, eq high)
+          const uint32_t tpc = c_all ? max(1u, (uint32_t)kSelThreads / c_all) : 1u;
+          for (uint32_t i = threadIdx.x; i < c_all; i += kSelThreads) s.part[i] = 0;
+          __syncthreads();
+          if (threadIdx.x < c_all * tpc) {
+            const uint32_t i = threadIdx.x % c_all, part = threadIdx.x / c_all;
             const uint32_t x = C[i];
             uint32_t gt = 0, eq = 0;
-            for (uint32_t j = 0; j < c_all; ++j) {
+            for (uint32_t j = part; j < c_all; j += tpc) {
               const uint32_t y = C[j];
               gt += y > x;
               eq += y == x;
             }
-            if (gt < krem && krem <= gt + eq) {  // the same x and counts for every such i
-              s.t_x = x;
+            atomicAdd(&s.part[i], gt | (eq << 16));
+          }
+          __syncthreads();
+          for (uint32_t i = threadIdx.x; i < c_all; i += kSelThreads) {
+            const uint32_t gt = s.part[i] & 0xFFFFu, eq = s.part[i] >> 16;
+            if (gt < krem && krem <= gt + eq) {  // the same key and counts for every such i
+              s.t_x = C[i];
               s.t_krem = krem - gt;
             }
           }
@@ -346,7 +353,7 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
 #pragma unroll 4
       for (int j = 0; j < kPer; ++j) {
         const int i = threadIdx.x + kSelThreads * j;
-        const uint32_t kk = s.keys[kslot(i)];
+        const uint32_t kk = s.keys[kslot(threadIdx.x) + kSelThreads * j];
         gt += sel_gt(kk, lo + base + i);
         eq += sel_eq(kk);
       }
@@ -527,13 +534,13 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
   }
   uint32_t* krange = reinterpret_cast<uint32_t*>(cur);
   const int kr_stride = score_range_slots(score_tiles(cfg, max_entries, reindex));
-  // one CTA per kRound positions of the longest selection, up to a cluster of
-  // 8, but no more CTAs than one wave holds (one CTA per SM)
+  // a cluster of up to 8 CTAs per selection, each with at least kMinCtaKeys
+  // positions, but no more CTAs than one wave holds (one CTA per SM)
   const int64_t n_max = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
   const int n_sel = (!reindex && pool_out) ? 2 : 1;
   const int64_t sel_groups = (int64_t)std::min(chunk, Q) * n_sel;
   int cs = 1;
-  while (cs < 8 && (int64_t)cs * kRound < n_max && 2 * cs * sel_groups <= num_sms()) cs <<= 1;
+  while (cs < 8 && (int64_t)cs * kMinCtaKeys < n_max && 2 * cs * sel_groups <= num_sms()) cs <<= 1;
   const size_t sel_smem = sizeof(SelShared);
   cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
   for (int q0 = 0; q0 < Q; q0 += chunk) {

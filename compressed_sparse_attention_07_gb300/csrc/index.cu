@@ -438,6 +438,167 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
   }
 }
 
+// The same selection for a single CTA holding all n <= kRound positions:
+// thread t owns positions 16t .. 16t + 15 and keeps their keys in registers
+// from the one read of the scores to the ordered write of the ids
+// (histogram, cut search, threshold-bin keys ranked or refined by digits,
+// then one scan of packed (above, equal) counts).
+__device__ void select_small(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
+                             uint32_t kmin, uint32_t kmax, SelShared& s) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const bool has_forced = forced >= 0 && forced < n;
+  const uint32_t need = (uint32_t)k - (has_forced ? 1u : 0u);
+  const bool any = kmin <= kmax;
+  const uint32_t range = any ? kmax - kmin : 0u;
+  const int nbits = range ? 32 - __clz(range) : 0;
+  const int sh = nbits > 13 ? nbits - 13 : 0;
+  const bool ranked = need > 0 && any;
+  auto bin_of = [&](uint32_t kk) -> uint32_t {
+    const uint32_t x = kk > kmin ? kk - kmin : 0u;
+    return min(x >> sh, (uint32_t)(kHistBins - 1));
+  };
+  const int64_t p0 = (int64_t)kPer * threadIdx.x;
+  float v[kPer];
+  if (((uintptr_t)vals & 15u) == 0 && p0 + kPer <= n) {
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) {
+      float4 f4;
+      asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(f4.x), "=f"(f4.y), "=f"(f4.z), "=f"(f4.w)
+                   : "l"(vals + p0 + 4 * q));
+      v[4 * q] = f4.x;
+      v[4 * q + 1] = f4.y;
+      v[4 * q + 2] = f4.z;
+      v[4 * q + 3] = f4.w;
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) v[m] = p0 + m < n ? ld_score(vals + p0 + m) : __uint_as_float(kScoreInvalid);
+  }
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
+  if (threadIdx.x == 0) s.cand_n = 0;
+  uint32_t kk[kPer];
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) kk[m] = (p0 + m == forced) ? 0u : order_key(v[m]);
+  __syncthreads();
+
+  uint32_t T = 0xFFFFFFFFu, krem = 0;  // select key > T, then the first krem keys == T
+  if (ranked) {
+#pragma unroll
+    for (int m = 0; m < kPer; ++m)
+      if (kk[m]) atomicAdd(&s.hist[bin_of(kk[m])], 1u);
+    __syncthreads();
+    find_cut(s.hist, kHistBins, need, s);
+    if (s.cut_total <= need) {
+      T = 0;  // every valid key
+    } else {
+      const uint32_t tb = s.cut_bin;
+      uint32_t prefix = tb;
+      int rem = sh;
+      krem = need - s.cut_above;
+      if (rem > 0) {
+#pragma unroll
+        for (int m = 0; m < kPer; ++m)
+          if (kk[m] != 0u && bin_of(kk[m]) == tb) {
+            const uint32_t at = atomicAdd(&s.cand_n, 1u);
+            if (at < (uint32_t)kCandMax) s.cand[at] = kk[m] - kmin;
+          }
+        __syncthreads();
+        const uint32_t c = s.cand_n;
+        if (c <= (uint32_t)kRankMax) {
+          // rank of each candidate among the threshold-bin keys (tpc threads each)
+          const uint32_t tpc = max(1u, (uint32_t)kSelThreads / c);
+          for (uint32_t i = threadIdx.x; i < c; i += kSelThreads) s.part[i] = 0;
+          __syncthreads();
+          if (threadIdx.x < c * tpc) {
+            const uint32_t i = threadIdx.x % c, part = threadIdx.x / c;
+            const uint32_t x = s.cand[i];
+            uint32_t gt = 0, eq = 0;
+            for (uint32_t j = part; j < c; j += tpc) {
+              const uint32_t y = s.cand[j];
+              gt += y > x;
+              eq += y == x;
+            }
+            atomicAdd(&s.part[i], gt | (eq << 16));
+          }
+          __syncthreads();
+          for (uint32_t i = threadIdx.x; i < c; i += kSelThreads) {
+            const uint32_t gt = s.part[i] & 0xFFFFu, eq = s.part[i] >> 16;
+            if (gt < krem && krem <= gt + eq) {  // the same key and counts for every such i
+              s.t_x = s.cand[i];
+              s.t_krem = krem - gt;
+            }
+          }
+          __syncthreads();
+          prefix = s.t_x;
+          krem = s.t_krem;
+          rem = 0;
+        }
+        // many keys in the cut bin: 11-bit digits over the list (or the registers)
+        while (rem > 0) {
+          const int w = rem < 11 ? rem : 11;
+          const int s2 = rem - w;
+          const uint32_t dmask = (1u << w) - 1u;
+          for (int i = threadIdx.x; i < kDigitBins; i += kSelThreads) s.hist[i] = 0;
+          __syncthreads();
+          if (c <= (uint32_t)kCandMax) {
+            for (uint32_t i = threadIdx.x; i < c; i += kSelThreads) {
+              const uint32_t x = s.cand[i];
+              if ((x >> rem) == prefix) atomicAdd(&s.hist[(x >> s2) & dmask], 1u);
+            }
+          } else {
+#pragma unroll
+            for (int m = 0; m < kPer; ++m) {
+              const uint32_t x = kk[m] - kmin;
+              if (kk[m] != 0u && kk[m] >= kmin && (x >> rem) == prefix) atomicAdd(&s.hist[(x >> s2) & dmask], 1u);
+            }
+          }
+          __syncthreads();
+          find_cut(s.hist, kDigitBins, krem, s);
+          krem -= s.cut_above;
+          prefix = (prefix << w) | s.cut_bin;
+          rem = s2;
+        }
+      }
+      T = kmin + prefix;
+    }
+  }
+
+  // ---- ordered compaction
+  uint32_t gt = 0, eq = 0;
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) {
+    gt += kk[m] > T || p0 + m == forced;
+    eq += kk[m] == T && T != 0u;
+  }
+  const uint32_t vpk = gt | (eq << 16);
+  const uint32_t incl = warp_incl_scan(vpk);
+  if (lane == 31) s.wsum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t ws = s.wsum[lane], wi = warp_incl_scan(ws);
+    __syncwarp();
+    s.wsum[lane] = wi - ws;
+    if (lane == 31) s.wsum[kSelWarps] = wi;
+  }
+  __syncthreads();
+  const uint32_t before = s.wsum[wid] + incl - vpk;
+  uint32_t E = before >> 16;
+  uint32_t off = (before & 0xFFFFu) + min(krem, E);
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) {
+    bool take = kk[m] > T || p0 + m == forced;
+    if (!take && kk[m] == T && T != 0u) take = E++ < krem;
+    if (take) {
+      if (off < (uint32_t)k) out[off] = idmap(p0 + m);
+      ++off;
+    }
+  }
+  const uint32_t all = s.wsum[kSelWarps];
+  const uint32_t total = (all & 0xFFFFu) + min(krem, all >> 16);
+  for (uint32_t i = total + threadIdx.x; i < (uint32_t)k; i += kSelThreads) out[i] = -1;
+}
+
 // grid (cs, queries, selections), clusters of cs CTAs along x.  Selection 0:
 // entry top-k (Full or Reindex); 1: HSI block pool (Full).
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, int r, int k, int n_blocks,
@@ -481,17 +642,22 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
   }
   __syncthreads();
   const uint32_t lo = r_lo, hi = r_hi;
+  auto run = [&](const float* v, int64_t n, int kk, int64_t forced, IdMap idmap, int32_t* o) {
+    if (cs == 1 && n <= kRound)
+      select_small(v, n, kk, forced, idmap, o, lo, hi, s);
+    else
+      select_topk(v, n, kk, forced, idmap, o, lo, hi, s, cs, rk);
+  };
   if (blockIdx.z == 0) {
     const float* v = scores + (int64_t)qc * score_stride;
     if (pool)
-      select_topk(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks},
-                  topk_out + (int64_t)qi * k, lo, hi, s, cs, rk);
+      run(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks}, topk_out + (int64_t)qi * k);
     else
-      select_topk(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k, lo, hi, s, cs, rk);
+      run(v, nv, k, -1, IdMap{nullptr}, topk_out + (int64_t)qi * k);
   } else {
     const int64_t nb = (nv + kHsiBlock - 1) / kHsiBlock;
     const float* v = bmax + (int64_t)qc * ((max_entries + 7) / 8);
-    select_topk(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks, lo, hi, s, cs, rk);
+    run(v, nb, n_blocks, nb - 1, IdMap{nullptr}, pool_out + (int64_t)qi * n_blocks);
   }
 }
 

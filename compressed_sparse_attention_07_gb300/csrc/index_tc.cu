@@ -102,6 +102,12 @@ __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0
 // Barrier of one warpgroup (ids 1..4) or of all consumers (id 5).
 __device__ __forceinline__ void wg_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
 __device__ __forceinline__ void consumers_sync(int n) { asm volatile("bar.sync 5, %0;" ::"r"(n) : "memory"); }
+// Page table hand-off in page mode: the consumers arrive once their share of
+// the page table is written, the producer warp waits (barrier 6, all threads).
+template <int kThreadsAll>
+__device__ __forceinline__ void pages_arrive_n() { asm volatile("bar.arrive 6, %0;" ::"n"(kThreadsAll) : "memory"); }
+template <int kThreadsAll>
+__device__ __forceinline__ void pages_sync_n() { asm volatile("bar.sync 6, %0;" ::"n"(kThreadsAll) : "memory"); }
 
 template <int kDtype, int QPC, bool kGather>
 __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kernel(ScoreArgs a) {
@@ -110,6 +116,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   constexpr int kConsumers = Shape<kDtype, QPC>::kConsumers;
   constexpr int kThreads = Shape<kDtype, QPC>::kThreads;
   constexpr int kStages = Shape<kDtype, QPC>::kStages;
+  auto pages_arrive = [] { pages_arrive_n<kThreads>(); };
+  auto pages_sync = [] { pages_sync_n<kThreads>(); };
   constexpr int kN = 32 * QPC;                    // MMA N: QPC queries x 32 heads
   constexpr int kAcols = 64;                      // 128 channels of f16 pairs
   constexpr int kTmemCols = (kWG * kAcols + kWG * kN) <= 256 ? 256 : 512;
@@ -155,48 +163,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   }
   const int n_my = (int)(t_end - t_begin);
 
-  // ---- set-up: Q_idx (f16 or bf16) into the B tile, head weights, pages, barriers, TMEM
-  for (int i = tid; i < kN * kIdxDim / 8; i += kThreads) {
-    const int row = (8 * i) / kIdxDim, k = (8 * i) % kIdxDim;  // row = q*32 + h; 8 channels per load
-    uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
-                                                   (row % kIdxHeads) * kIdxDim + k));
-    if (!kBf16) {
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
-        w[j] = *reinterpret_cast<const uint32_t*>(&h2);
-      }
-      v = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = v;
-  }
-  for (int i = tid; i < QPC * kIdxHeads; i += kThreads)
-    hw[i / kIdxHeads][i % kIdxHeads] = a.head_w ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;
-  if (kGather) {
-    for (int i = tid; i < n_my * 128; i += kThreads) {
-      const int64_t p = t_begin * 128 + i;  // pool position
-      int32_t e = -1;
-      if (p < npos) {
-        const int32_t blk = __ldg(a.pool + (int64_t)g0 * a.n_blocks + p / kHsiBlock);
-        if (blk >= 0) {
-          const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
-          if ((int64_t)blk * kHsiBlock >= a.max_entries) {
-            if (p % kHsiBlock == 0) report(a.status, CSA2_ERR_BAD_INDEX);
-          } else if (j < nv[0]) {
-            const int64_t page = page_of(a.ic, b, j, a.status);
-            if (page >= 0) e = (int32_t)(page * kPage + j % kPage);
-          }
-        }
-      }
-      gtab[i] = e;
-    }
-  } else {
-    for (int i = tid; i < 2 * n_my; i += kThreads) {
-      const int64_t p = 2 * t_begin + i;  // logical page
-      ptab[i] = (p * kPage < nv_max) ? (int32_t)page_of(a.ic, b, p * kPage, a.status) : -1;
-    }
-  }
+  // ---- barriers and TMEM first: the producer starts copying pages while the
+  // consumers build the Q tile
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&full_bar[s], 1);
@@ -214,7 +182,6 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     tc::tmem_alloc(&tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
-  tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -222,16 +189,16 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
 
   if (warp == kConsumers / 32) {
     // ------------------------------------------------------------ producer
-    if (!kGather && (tid & 31) == 0) {
-      int issued = 0;
-      for (int i = 0; i < n_my; ++i) {
+    if (!kGather) {
+      const int lane = tid & 31;
+      const int first = n_my < kStages ? n_my : kStages;
+      if (lane < 2 * first) {  // pages of the first pass; the consumers resolve the rest
+        const int64_t p = 2 * t_begin + lane;  // logical page
+        ptab[lane] = (p * kPage < nv_max) ? (int32_t)page_of(a.ic, b, p * kPage, a.status) : -1;
+      }
+      __syncwarp();
+      auto issue = [&](int i) {
         const int s = i % kStages;
-        if (!tc::mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, kSpin)) {
-          report(a.status, CSA2_ERR_TIMEOUT);
-          atomicExch(&abort_flag, 1);
-          break;
-        }
-        if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
         uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
         uint32_t bytes = 0;
         int64_t pages[2];
@@ -249,14 +216,82 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
             tc::bulk_g2s(slot + 2 * F::kPageData + hh * F::kPageScales, a.ic.scales + pages[hh] * F::kPageScales,
                          F::kPageScales, &full_bar[s]);
         }
-        ++issued;
+      };
+      // the first pass over the ring (fresh slots) from one lane per tile, the
+      // rest in order from lane 0 once the consumers release each slot
+      if (lane < first) issue(lane);
+      __syncwarp();
+      pages_sync();  // the consumers' share of the page table is written
+      if (lane == 0) {
+        int issued = first;
+        for (int i = first; i < n_my; ++i) {
+          const int s = i % kStages;
+          if (!tc::mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, kSpin)) {
+            report(a.status, CSA2_ERR_TIMEOUT);
+            atomicExch(&abort_flag, 1);
+            break;
+          }
+          if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+          issue(i);
+          ++issued;
+        }
+        // do not leave while copies into this CTA's shared memory are in flight
+        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+          if (!tc::mbar_wait(&full_bar[i % kStages], (i / kStages) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
       }
-      // do not leave while copies into this CTA's shared memory are in flight
-      for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-        if (!tc::mbar_wait(&full_bar[i % kStages], (i / kStages) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
     }
     return;
   }
+
+  // ---- consumers' set-up: the pages after the producer's first pass (then
+  // release the producer), Q_idx (f16 or bf16) into the B tile, head
+  // weights, gather positions
+  if (!kGather) {
+    const int first = n_my < kStages ? n_my : kStages;
+    for (int i = 2 * first + tid; i < 2 * n_my; i += kConsumers) {
+      const int64_t p = 2 * t_begin + i;  // logical page
+      ptab[i] = (p * kPage < nv_max) ? (int32_t)page_of(a.ic, b, p * kPage, a.status) : -1;
+    }
+    pages_arrive();
+  }
+  for (int i = tid; i < kN * kIdxDim / 8; i += kConsumers) {
+    const int row = (8 * i) / kIdxDim, k = (8 * i) % kIdxDim;  // row = q*32 + h; 8 channels per load
+    uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
+                                                   (row % kIdxHeads) * kIdxDim + k));
+    if (!kBf16) {
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+        w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = v;
+  }
+  for (int i = tid; i < QPC * kIdxHeads; i += kConsumers)
+    hw[i / kIdxHeads][i % kIdxHeads] = a.head_w ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;
+  if (kGather) {
+    for (int i = tid; i < n_my * 128; i += kConsumers) {
+      const int64_t p = t_begin * 128 + i;  // pool position
+      int32_t e = -1;
+      if (p < npos) {
+        const int32_t blk = __ldg(a.pool + (int64_t)g0 * a.n_blocks + p / kHsiBlock);
+        if (blk >= 0) {
+          const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
+          if ((int64_t)blk * kHsiBlock >= a.max_entries) {
+            if (p % kHsiBlock == 0) report(a.status, CSA2_ERR_BAD_INDEX);
+          } else if (j < nv[0]) {
+            const int64_t page = page_of(a.ic, b, j, a.status);
+            if (page >= 0) e = (int32_t)(page * kPage + j % kPage);
+          }
+        }
+      }
+      gtab[i] = e;
+    }
+  }
+  tc::fence_async_smem();  // the Q tile is read by the tensor core
+  consumers_sync(kConsumers);
 
   // -------------------------------------------------------------- consumers
   const int g = warp >> 2;               // warpgroup: tiles g, g + kWG, ...

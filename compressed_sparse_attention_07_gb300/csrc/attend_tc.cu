@@ -718,15 +718,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
 //   S^T[128 rows x 64 heads]  = sum_c C[c] . Q_c^T       (M 128, N 64, K 512)
 //   partial softmax per head over the tile's rows: m_t, l_t, P = 2^(s - m_t)
 //   O_t^T[c] = C[c]^T . P^T                            (M 128, N 64, K 128)
-// and the tiles are merged through distributed shared memory:
-// M = max_t m_t, L = sum_t 2^(m_t - M) l_t, out = sum_t 2^(m_t - M) O_t / L;
-// chunk c of the output is summed, in tile order, by the CTA of rank c % n.
+// and the tiles are merged through distributed shared memory: every CTA
+// keeps its O_t in its own shared memory, and the CTA of rank c % n pulls
+// chunk c of every tile and forms out = sum_t 2^(m_t - M) O_t / L in tile
+// order (M = max_t m_t, L = sum_t 2^(m_t - M) l_t).
 constexpr int kAllHeads = 64;
 constexpr size_t kRowQBytes = (size_t)kAllHeads * kDim * 2;   // 65536
 constexpr size_t kRowCBytes = 4 * (size_t)kCBytes;            // 131072
 constexpr size_t kRowPBytes = (size_t)kAllHeads * 128 * 2;    // 16384
 constexpr size_t kRowSmem = kRowQBytes + kRowCBytes + kRowPBytes + 128 * 4 + 2 * kAllHeads * 4;
-constexpr int kRowMaxTiles = 6;  // receive area n * ceil(4/n) * 32 KB <= 192 KB
+constexpr int kRowMaxTiles = 6;
 
 // Reduce v[16] over the 32 lanes of a warp (op = max or +): afterwards lane l
 // holds the result for entry l >> 1.  Each step hands half of the entries
@@ -773,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tmem_base;
   __shared__ float red_m[4][kAllHeads], red_s[4][kAllHeads];
-  __shared__ float mx[kAllHeads], alpha[kAllHeads];
+  __shared__ float mx[kAllHeads], fac[kRowMaxTiles][kAllHeads];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = tid & 127, p = tid >> 7, quad = warp & 3;
@@ -948,20 +949,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ok = tc::mbar_wait(&bar, 1, kSpin) && ok;
   tc::fence_after_sync();
-  float o[4][16];
+  // ---- this tile's unscaled partial output into its own shared memory (Q and
+  // C are free now), [chunk][head][channel]: a warp's stores are 128
+  // contiguous bytes
+  float* stg = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t w[16];
     tc::tmem_ld16(tc::taddr(tb, lane_base, kAllHeads + kAllHeads * c + 16 * p), w);
     tc::tmem_wait_ld();
+    float* dst = stg + (c * kAllHeads + 16 * p) * 128 + r;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) o[c][j] = __uint_as_float(w[j]);
+    for (int j = 0; j < 16; ++j) dst[128 * j] = __uint_as_float(w[j]);
   }
   tc::fence_before_sync();
-  // every CTA of the cluster: (m, l) written, products finished, shared memory free
+  // every CTA of the cluster: (m, l) and its partial output written
   tc::cluster_sync();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
+  // per-head factor of every tile: 2^(m_t - M) / L, M = max_t m_t, L = sum_t 2^(m_t - M) l_t
   if (tid < kAllHeads) {
     const uint32_t ml_addr = tc::smem_u32(ml);
     float mk[kRowMaxTiles], lk[kRowMaxTiles];
@@ -977,52 +983,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int k2 = 0; k2 < kRowMaxTiles; ++k2)
       if (mk[k2] != -INFINITY) L += exp2f(mk[k2] - M) * lk[k2];
-    const float mt = ml[tid];
-    alpha[tid] = (ok && L > 0.0f && mt != -INFINITY) ? exp2f(mt - M) / L : 0.0f;
+#pragma unroll
+    for (int k2 = 0; k2 < kRowMaxTiles; ++k2)
+      fac[k2][tid] = (ok && L > 0.0f && mk[k2] != -INFINITY) ? exp2f(mk[k2] - M) / L : 0.0f;
     if (t == 0 && a.lse)
       a.lse[(int64_t)qi * kHeads + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
   if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
   __syncthreads();
-  // ---- push the scaled partial output: chunk c goes to rank c % n, slot c / n,
-  // at [sender tile][slot][head][channel] (a warp's stores are 128 contiguous
-  // bytes); the CTA's own chunk is written to its shared memory directly
-  const int spo = (4 + n - 1) / n;
-  const uint32_t recv = tc::smem_u32(smem);
+  // ---- this CTA's chunks c = t, t + n, ...: pull every tile's partial
+  // (16-byte distributed loads, all issued before the sums), weight and sum
+  // in tile order, 16-byte stores along the channels
+  const uint32_t stg_addr = tc::smem_u32(stg);
+  for (int c = t; c < 4; c += n) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int owner = c % n;
-    const uint32_t e0 = (uint32_t)(((t * spo + c / n) * kAllHeads + 16 * p) * 128 + r);
-    if (owner == t) {
-      float* dst = reinterpret_cast<float*>(smem) + e0;
+    for (int it = 0; it < kAllHeads * 32 / kThreads; it += 2) {
+      float4 v[2][kRowMaxTiles];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) dst[128 * j] = o[c][j] * alpha[16 * p + j];
-    } else {
-      const uint32_t dst = tc::map_rank(recv, owner) + 4u * e0;
+      for (int u = 0; u < 2; ++u) {
+        const int e = tid + kThreads * (it + u), h = e >> 5, ch4 = 4 * (e & 31);
+        const uint32_t off = 4u * (uint32_t)((c * kAllHeads + h) * 128 + ch4);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) tc::st_dsmem(dst + 4u * 128u * j, o[c][j] * alpha[16 * p + j]);
-    }
-  }
-  tc::cluster_sync();
-  // ---- this CTA's chunks: sum the tiles' partials in tile order, four
-  // channels per thread, 16-byte stores along the channels
-  const float* rv = reinterpret_cast<const float*>(smem);
-  for (int s2 = 0; s2 < spo; ++s2) {
-    const int c = s2 * n + t;
-    if (c >= 4) break;
-    for (int e = tid; e < kAllHeads * 32; e += kThreads) {
-      const int h = e >> 5, ch4 = 4 * (e & 31);
-      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      for (int k2 = 0; k2 < n; ++k2) {
-        const float4 v4 = *reinterpret_cast<const float4*>(rv + ((k2 * spo + s2) * kAllHeads + h) * 128 + ch4);
-        acc.x += v4.x;
-        acc.y += v4.y;
-        acc.z += v4.z;
-        acc.w += v4.w;
+        for (int k2 = 0; k2 < kRowMaxTiles; ++k2)
+          if (k2 < n) v[u][k2] = tc::ld_dsmem_v4(tc::map_rank(stg_addr + off, k2));
       }
-      *reinterpret_cast<float4*>(a.out + ((int64_t)qi * kHeads + h) * kDim + c * 128 + ch4) = acc;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int e = tid + kThreads * (it + u), h = e >> 5, ch4 = 4 * (e & 31);
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int k2 = 0; k2 < kRowMaxTiles; ++k2)
+          if (k2 < n) {
+            const float f = fac[k2][h];
+            acc.x = fmaf(f, v[u][k2].x, acc.x);
+            acc.y = fmaf(f, v[u][k2].y, acc.y);
+            acc.z = fmaf(f, v[u][k2].z, acc.z);
+            acc.w = fmaf(f, v[u][k2].w, acc.w);
+          }
+        *reinterpret_cast<float4*>(a.out + ((int64_t)qi * kHeads + h) * kDim + c * 128 + ch4) = acc;
+      }
     }
   }
+  tc::cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
 template <int kDtype>

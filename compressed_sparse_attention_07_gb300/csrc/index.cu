@@ -10,10 +10,10 @@
 namespace csa2 {
 namespace {
 
-constexpr int kSelThreads = 1024;   // one CTA selects for one query
+constexpr int kSelThreads = 1024;   // one CTA (or a cluster of them) selects for one query
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kPer = 16;              // keys a lane holds per round
-constexpr int kRound = kSelThreads * kPer;  // positions per round; a warp covers 512 consecutive ones
+constexpr int kPer = 16;              // keys a thread holds per round
+constexpr int kRound = kSelThreads * kPer;  // positions per round
 constexpr int kHistBins = 8192;       // linear bins over a query's key range
 constexpr int kDigitBins = 2048;      // refinement digit: 11 bits
 constexpr int kCandMax = 8192;        // keys of the threshold bin listed in shared memory
@@ -71,9 +71,9 @@ __device__ void find_cut(const uint32_t* hist, int nbins, uint32_t need, SelShar
   if (lane == 31) s.wsum[wid] = incl;
   __syncthreads();
   if (wid == 0) {
-    const uint32_t ws = s.wsum[lane], wi = warp_incl_scan(ws);
+    const uint32_t ws = lane < kSelWarps ? s.wsum[lane] : 0u, wi = warp_incl_scan(ws);
     __syncwarp();
-    s.wsum[lane] = wi - ws;
+    if (lane < kSelWarps) s.wsum[lane] = wi - ws;
     if (lane == 31) s.cut_total = wi;
   }
   __syncthreads();
@@ -143,8 +143,8 @@ __device__ __forceinline__ int kslot(int i) {
 //      (the first krem by position); more are refined 11 bits at a time
 //      (cluster-summed digit histograms);
 //   3. ordered compaction: each CTA starts after the selections of the lower
-//      ranks; thread t owns 16 consecutive positions of a round, offsets from
-//      warp scans and one scan over the warps.
+//      ranks; thread t owns kPer consecutive positions of a round, offsets
+//      from warp scans and one scan over the warps.
 // Keys are staged in shared memory a round of kRound positions at a time; a
 // range of at most kRound positions is read from global memory once.
 __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
@@ -342,7 +342,7 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
     __syncthreads();
   }
 
-  // ---- ordered compaction: in a round, thread t owns keys 16t .. 16t + 15
+  // ---- ordered compaction: in a round, thread t owns keys kPer t .. kPer t + kPer - 1
   auto sel_gt = [&](uint32_t kk, int64_t p) { return kk > T || p == forced; };
   auto sel_eq = [&](uint32_t kk) { return kk == T && T != 0u; };
   if (cs > 1) {
@@ -406,9 +406,9 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
     if (lane == 31) s.wsum[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-      const uint32_t ws = s.wsum[lane], wi = warp_incl_scan(ws);
+      const uint32_t ws = lane < kSelWarps ? s.wsum[lane] : 0u, wi = warp_incl_scan(ws);
       __syncwarp();
-      s.wsum[lane] = wi - ws;
+      if (lane < kSelWarps) s.wsum[lane] = wi - ws;
       if (lane == 31) s.wsum[kSelWarps] = wi;
     }
     __syncthreads();
@@ -439,7 +439,7 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
 }
 
 // The same selection for a single CTA holding all n <= kRound positions:
-// thread t owns positions 16t .. 16t + 15 and keeps their keys in registers
+// thread t owns positions kPer t .. kPer t + kPer - 1 and keeps their keys in registers
 // from the one read of the scores to the ordered write of the ids
 // (histogram, cut search, threshold-bin keys ranked or refined by digits,
 // then one scan of packed (above, equal) counts).
@@ -497,12 +497,23 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
       int rem = sh;
       krem = need - s.cut_above;
       if (rem > 0) {
+        {  // this thread's keys of the cut bin, one shared-memory atomic per warp
+          uint32_t mine = 0;
 #pragma unroll
-        for (int m = 0; m < kPer; ++m)
-          if (kk[m] != 0u && bin_of(kk[m]) == tb) {
-            const uint32_t at = atomicAdd(&s.cand_n, 1u);
-            if (at < (uint32_t)kCandMax) s.cand[at] = kk[m] - kmin;
+          for (int m = 0; m < kPer; ++m) mine += kk[m] != 0u && bin_of(kk[m]) == tb;
+          const uint32_t incl = warp_incl_scan(mine);
+          uint32_t at = 0;
+          if (lane == 31 && incl) at = atomicAdd(&s.cand_n, incl);
+          at = __shfl_sync(0xffffffffu, at, 31) + incl - mine;
+          if (mine) {
+#pragma unroll
+            for (int m = 0; m < kPer; ++m)
+              if (kk[m] != 0u && bin_of(kk[m]) == tb) {
+                if (at < (uint32_t)kCandMax) s.cand[at] = kk[m] - kmin;
+                ++at;
+              }
           }
+        }
         __syncthreads();
         const uint32_t c = s.cand_n;
         if (c <= (uint32_t)kRankMax) {
@@ -576,9 +587,9 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
   if (lane == 31) s.wsum[wid] = incl;
   __syncthreads();
   if (wid == 0) {
-    const uint32_t ws = s.wsum[lane], wi = warp_incl_scan(ws);
+    const uint32_t ws = lane < kSelWarps ? s.wsum[lane] : 0u, wi = warp_incl_scan(ws);
     __syncwarp();
-    s.wsum[lane] = wi - ws;
+    if (lane < kSelWarps) s.wsum[lane] = wi - ws;
     if (lane == 31) s.wsum[kSelWarps] = wi;
   }
   __syncthreads();

@@ -617,21 +617,32 @@ def main():
     eager_ms = statistics.fmean(e[0].elapsed_time(e[nst]) for e in eev)
     warm_ms = statistics.fmean(a.elapsed_time(b) for a, b in wev)
 
-    # end to end through the Python API with host buffers: H2D of the step's
-    # inputs from pinned memory, the step, D2H of the attention output
-    hin = {k: torch.from_numpy(np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory()
-           for k, v in step.inputs_host().items()}
+    # end to end through the Python API with host buffers: the step's inputs
+    # packed in one pinned host buffer and copied in with one H2D copy (the
+    # device tensors the API is called with are views of one staging
+    # buffer), the step, D2H of the attention output
+    host_in = {k: np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)
+               for k, v in step.inputs_host().items()}
+    offs, total = {}, 0
+    for k, v in host_in.items():
+        offs[k] = total
+        total += (v.nbytes + 255) & ~255
+    hpack = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dpack = torch.empty(total, dtype=torch.uint8, device=dev)
+    dbuf = {}
+    for k, v in host_in.items():
+        hv = torch.from_numpy(v)
+        hpack[offs[k]:offs[k] + v.nbytes].copy_(hv.view(-1).view(torch.uint8))
+        dbuf[k] = dpack[offs[k]:offs[k] + v.nbytes].view(hv.dtype).view(hv.shape)
     hout = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    dbuf = {k: torch.empty_like(v, device=dev) for k, v in hin.items()}
-    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    h2d = total
     d2h = hout.numel() * hout.element_size()
     e2e_steps = max(3, min(args.steps, 50))
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     for k in range(e2e_steps):
         flush.fill_(k & 0xFF)
         e2e_ev[k][0].record()
-        for name, t in hin.items():
-            dbuf[name].copy_(t, non_blocking=True)
+        dpack.copy_(hpack, non_blocking=True)
         out = step.step(d=dbuf)
         hout.copy_(out, non_blocking=True)
         e2e_ev[k][1].record()

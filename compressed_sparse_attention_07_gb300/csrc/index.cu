@@ -443,8 +443,12 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
 // from the one read of the scores to the ordered write of the ids
 // (histogram, cut search, threshold-bin keys ranked or refined by digits,
 // then one scan of packed (above, equal) counts).
+// gpool != NULL: position p reads vals[gpool[p / 8] * 8 + p % 8] (a pool of
+// 8-entry blocks written earlier by this CTA; ids >= nv_lim or blocks < 0 are
+// not candidates).
 __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
-                             uint32_t kmin, uint32_t kmax, SelShared& s) {
+                             uint32_t kmin, uint32_t kmax, SelShared& s, const int32_t* gpool = nullptr,
+                             int64_t nv_lim = 0) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const bool has_forced = forced >= 0 && forced < n;
   const uint32_t need = (uint32_t)k - (has_forced ? 1u : 0u);
@@ -459,7 +463,18 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
   };
   const int64_t p0 = (int64_t)kPer * threadIdx.x;
   float v[kPer];
-  if (((uintptr_t)vals & 15u) == 0 && p0 + kPer <= n) {
+  if (gpool) {
+#pragma unroll
+    for (int h = 0; h < kPer / kHsiBlock; ++h) {
+      const int64_t pb = (p0 >> 3) + h;  // pool slot; plain load: written by this CTA
+      const int32_t blk = pb * kHsiBlock < n ? *reinterpret_cast<const volatile int32_t*>(gpool + pb) : -1;
+#pragma unroll
+      for (int i = 0; i < kHsiBlock; ++i) {
+        const int64_t j = (int64_t)blk * kHsiBlock + i;
+        v[kHsiBlock * h + i] = (blk >= 0 && j < nv_lim) ? ld_score(vals + j) : __uint_as_float(kScoreInvalid);
+      }
+    }
+  } else if (((uintptr_t)vals & 15u) == 0 && p0 + kPer <= n) {
 #pragma unroll
     for (int q = 0; q < kPer / 4; ++q) {
       float4 f4;
@@ -619,7 +634,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
                                                                 const int32_t* __restrict__ pool, const float* scores,
                                                                 const float* bmax, int64_t score_stride,
                                                                 const uint32_t* krange, int kr_stride, int n_slots,
-                                                                int32_t* topk_out, int32_t* pool_out) {
+                                                                int32_t* topk_out, int32_t* pool_out, int fused) {
   griddep_wait();  // the scores are the previous kernel's output
   griddep_launch();
   extern __shared__ __align__(16) unsigned char sel_raw[];
@@ -659,7 +674,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
     else
       select_topk(v, n, kk, forced, idmap, o, lo, hi, s, cs, rk);
   };
-  if (blockIdx.z == 0) {
+  if (fused) {
+    // Full with HSI, one CTA: the pool first, then the top-k over the pool's
+    // positions.  Exact when the pool holds k blocks besides the forced one:
+    // every block ranking above a block that holds a top-k entry e (block max
+    // desc, block id asc) contains an entry ranking above e (score desc, id
+    // asc), so at most k - 1 blocks rank above it.
+    const int64_t nb = (nv + kHsiBlock - 1) / kHsiBlock;
+    int32_t* prow = pool_out + (int64_t)qi * n_blocks;
+    run(bmax + (int64_t)qc * ((max_entries + 7) / 8), nb, n_blocks, nb - 1, IdMap{nullptr}, prow);
+    __syncthreads();  // the pool ids are visible to the whole CTA
+    select_small(scores + (int64_t)qc * score_stride, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{prow},
+                 topk_out + (int64_t)qi * k, lo, hi, s, prow, nv);
+  } else if (blockIdx.z == 0) {
     const float* v = scores + (int64_t)qc * score_stride;
     if (pool)
       run(v, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{pool + (int64_t)qi * n_blocks}, topk_out + (int64_t)qi * k);
@@ -714,10 +741,15 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
   // a cluster of up to 8 CTAs per selection, each with at least kMinCtaKeys
   // positions, but no more CTAs than one wave holds (one CTA per SM)
   const int64_t n_max = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
-  const int n_sel = (!reindex && pool_out) ? 2 : 1;
+  // Full with HSI: one CTA selects the pool and then the top-k among the
+  // pool's positions, when they fit one CTA's registers and the pool has at
+  // least k blocks besides the forced one (what makes it exact)
+  const bool fused = !reindex && pool_out && (int64_t)cfg.hsi_blocks * kHsiBlock <= kRound &&
+                     cfg.hsi_blocks >= cfg.topk + 1;
+  const int n_sel = (!reindex && pool_out && !fused) ? 2 : 1;
   const int64_t sel_groups = (int64_t)std::min(chunk, Q) * n_sel;
   int cs = 1;
-  while (cs < 8 && (int64_t)cs * kMinCtaKeys < n_max && 2 * cs * sel_groups <= num_sms()) cs <<= 1;
+  while (!fused && cs < 8 && (int64_t)cs * kMinCtaKeys < n_max && 2 * cs * sel_groups <= num_sms()) cs <<= 1;
   const size_t sel_smem = sizeof(SelShared);
   cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
   for (int q0 = 0; q0 < Q; q0 += chunk) {
@@ -729,7 +761,7 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
     e = launch_k(select_kernel, dim3(cs, nq, n_sel), dim3(kSelThreads), sel_smem, stream, cs,
                  q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, (int64_t)max_entries, q_pos, n_entries, pool,
                  (const float*)scores, (const float*)bmax, stride, (const uint32_t*)krange, kr_stride, n_slots,
-                 topk_out, pool_out);
+                 topk_out, pool_out, fused ? 1 : 0);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -234,6 +234,25 @@ def test_select_threshold_bin_beyond_shared_list_and_single_slots(N):
     assert (v > v[600]).sum() < 512 and v.max() - v.min() >= 1.0  # the case the test is for
 
 
+@pytest.mark.parametrize("nb", [65, 128])
+def test_full_topk_through_the_hsi_pool_is_exact(nb):
+    """With HSI and at least k + 1 pool blocks the selection takes the pool
+    first and the top-k among the pool's positions; on integer scores with
+    many ties (duplicated rows) both must equal the oracle's top-k over all
+    visible entries and its pool, bit for bit, including a pool of exactly
+    k + 1 blocks."""
+    B, N, k = 3, 6000, 64
+    oc, pc = _idx_caches(B, N, "fp4", seed=27, integer=True, dup=True)
+    q_idx = synth.integer_bf16(synth.rng(27, "q"), (B, 2, H, CI), -1, 1)
+    q_pos = np.array([[5999, 3001], [5999, 5999], [777, 5999]], np.int64)
+    n_ent = np.array([6000, 5555, 2000], np.int32)
+    cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=nb)
+    g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+    o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, want_pool=True)
+    np.testing.assert_array_equal(g_top, o_top)
+    np.testing.assert_array_equal(g_pool, o_pool)
+
+
 def test_reindex_over_pool_matches_oracle():
     B, N, k, nb = 2, 4000, 64, 40
     oc, pc = _idx_caches(B, N, "fp4", seed=23, integer=True, dup=True)

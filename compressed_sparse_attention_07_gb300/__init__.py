@@ -18,7 +18,7 @@ from . import build as _build
 __all__ = [
     "Cfg", "PagedCache", "GroupState", "load", "compress", "index_workspace_bytes", "index_topk", "attend",
     "gather_dequant", "layer", "status_string", "CsaError", "CACHE_FP4", "CACHE_BF16", "MODE_FULL",
-    "MODE_REINDEX", "MODE_REUSE", "PAGE", "library_path",
+    "MODE_REINDEX", "MODE_REUSE", "PAGE", "library_path", "capture",
 ]
 
 CACHE_FP4, CACHE_BF16 = 0, 1
@@ -241,3 +241,31 @@ def layer(cfg: Cfg, mode: int, state: GroupState, q_pos, q, swa, swa_len, swa_po
                   _ptr(swa_pos0, torch.int64, "swa_pos0"), 1.0 / math.sqrt(512) if scale is None else float(scale),
                   _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"))
     _check("csa2_layer", load().csa2_layer(C.byref(cfg), int(mode), C.byref(state._c), C.byref(io), _stream(stream)))
+
+
+class Captured:
+    """A sequence of library calls (and the caller's copies) recorded once as
+    a CUDA graph and replayed with one launch: the same kernels on the same
+    buffers, without the host-side cost of issuing them call by call.  Every
+    buffer the calls touch must stay alive and in place; a call's host-side
+    arguments (sizes, configs, pointers) are those of the capture."""
+
+    def __init__(self, fn, warmup: int = 1):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+
+    def __call__(self):
+        self.graph.replay()
+
+
+def capture(fn, warmup: int = 1) -> Captured:
+    """Record ``fn`` (library calls on the current stream) for replay."""
+    return Captured(fn, warmup)
+

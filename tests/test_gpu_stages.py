@@ -386,3 +386,44 @@ def test_index_long_cache_many_tiles_per_cta():
     o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=2048, want_pool=True)
     np.testing.assert_array_equal(g_top, o_top)
     np.testing.assert_array_equal(g_pool, o_pool)
+
+
+# -------------------------------------------------------------- capture ----
+
+def test_captured_index_and_attend_replay_on_new_data():
+    """csa.capture records the library's calls (clusters, programmatic
+    launches) as a graph; replayed after new query data is written into the
+    same buffers, it gives exactly what the calls give when issued again."""
+    B, N, k, W = 4, 5000, 512, 128
+    _, pi = _idx_caches(B, N, "fp4", seed=28)
+    _, pm = _main_caches(B, N, "fp4", 28)
+    cfg = csa.Cfg(ratio=1, topk=k, window=W)
+    g = synth.rng(28, "q")
+    q_idx = _paged.dev(synth.normal_bf16(g, (B, 1, H, CI)))
+    q = _paged.dev(synth.normal_bf16(g, (B, 1, 64, D)))
+    swa = _paged.dev(synth.normal_bf16(g, (B, W, D)))
+    q_pos = _paged.dev(np.full((B, 1), N - 1, np.int64))
+    n_ent = _paged.dev(np.full(B, N, np.int32))
+    swa_len = _paged.dev(np.full(B, W, np.int32))
+    swa_pos0 = _paged.dev(np.full(B, N - W, np.int64))
+    topk = torch.empty((B, 1, k), dtype=torch.int32, device="cuda")
+    out = torch.empty((B, 1, 64, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(csa.index_workspace_bytes(cfg, B, 1, N), dtype=torch.uint8, device="cuda")
+    st = _status()
+
+    def calls():
+        csa.index_topk(cfg, q_idx, q_pos, pi, n_ent, N, topk, ws, status=st)
+        csa.attend(cfg, q, pm, n_ent, topk, swa, swa_len, swa_pos0, q_pos, out, status=st)
+
+    graph = csa.capture(calls)
+    g2 = synth.rng(29, "q")
+    q_idx.copy_(_paged.dev(synth.normal_bf16(g2, (B, 1, H, CI))))
+    q.copy_(_paged.dev(synth.normal_bf16(g2, (B, 1, 64, D))))
+    graph()
+    torch.cuda.synchronize()
+    got_top, got_out = topk.clone(), out.clone()
+    calls()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(got_top, topk)
+    assert torch.equal(got_out, out)

@@ -288,10 +288,11 @@ class PrefillStep(StepBase):
 
 
 class GroupStep(StepBase):
-    """One decode step through a cross-layer group of decoder layers: layer
-    20 Full (compress the new token, full indexing with the HSI pool), layers
-    24/28/32/36 Reindex over the pool, the other fifteen Reuse; every layer
-    has its own query, indexer query and window rows."""
+    """One decode step through a cross-layer group: decoder layers 20-39
+    (layer 20 Full: compress the new token, full indexing with the HSI pool;
+    layers 24/28/32/36 Reindex over the pool; the other fifteen Reuse) or the
+    encoder macro block 2-7 (layer 2 Full without HSI, five Reuse); every
+    layer has its own query, indexer query and window rows."""
 
     def __init__(self, wl, device, seed_offset=0):
         super().__init__(wl, device, seed_offset)
@@ -339,7 +340,7 @@ class GroupStep(StepBase):
                               for st in self.stages}
         self.units = B
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N, "layers": len(self.layers),
-                          "unit": "query token through the 20-layer group"}
+                          "unit": "query token through the %d-layer group" % len(self.layers)}
 
     def calls(self, d):
         csa = self.csa
@@ -443,7 +444,7 @@ class OracleStep:
         for layer, mode, q, swa, q_idx in self.per_layer:
             if mode == "full":
                 topk, pool, _ = o.index_topk(self.idx, self.n_ent, q_idx, self.q_pos, wl.ratio, wl.topk,
-                                             hsi_blocks=wl.hsi_blocks, want_pool=True)
+                                             hsi_blocks=wl.hsi_blocks if wl.hsi else 0, want_pool=wl.hsi)
             elif mode == "reindex":
                 topk, _, _ = o.index_topk(self.idx, self.n_ent, q_idx, self.q_pos, wl.ratio, wl.topk,
                                           hsi_blocks=wl.hsi_blocks, pool=pool)

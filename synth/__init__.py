@@ -15,8 +15,8 @@ import numpy as np
 import torch
 
 __all__ = [
-    "Workload", "WORKLOADS", "rng", "normal_bf16", "merge_weights", "fp4_bytes", "bf16_bits_to_f64",
-    "integer_fp4_bytes", "integer_bf16", "decode_inputs",
+    "Workload", "WORKLOADS", "ENCODER_GROUP", "DECODER_GROUP", "rng", "normal_bf16", "merge_weights", "fp4_bytes",
+    "bf16_bits_to_f64", "integer_fp4_bytes", "integer_bf16", "decode_inputs",
 ]
 
 
@@ -114,6 +114,9 @@ DECODER_GROUP = tuple(
     (l, "full" if l == 20 else "reindex" if l in (24, 28, 32, 36) else "reuse") for l in range(20, 40)
 )
 
+# The encoder's first CSA2 macro block: layer 2 Full, layers 3-7 Reuse (r = 2, no HSI).
+ENCODER_GROUP = tuple((l, "full" if l == 2 else "reuse") for l in range(2, 8))
+
 WORKLOADS = {
     "decode_b1_ctx4096_r2_bf16": Workload(
         "decode_b1_ctx4096_r2_bf16", batch=1, ctx=4096, ratio=2, cache="bf16", theta=1e4, seed=0),
@@ -128,6 +131,9 @@ WORKLOADS = {
     "prefill_4096_on_1m_r2_fp4": Workload(
         "prefill_4096_on_1m_r2_fp4", batch=1, ctx=1048576, ratio=2, cache="fp4", theta=1e4, seed=4,
         tq=4096),
+    "encoder_group6_b8_ctx32768_r2_fp4": Workload(
+        "encoder_group6_b8_ctx32768_r2_fp4", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=5,
+        layers=ENCODER_GROUP),
 }
 
 

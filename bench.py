@@ -239,20 +239,23 @@ class DecodeStep(StepBase):
 
 
 class PrefillStep(StepBase):
-    """One prefill chunk of Tq query tokens appended to a long context: the
-    compressor on the chunk's tokens, causal indexing of every chunk token
-    over the prefix plus the chunk's own entries, attention with the banded
-    window (rows t-W+1..t of the chunk and the prefix tail)."""
+    """One chunk of Tq query tokens per sequence appended to a long context (a
+    prefill chunk, or a multi-query decode block of draft positions): the
+    compressor on the chunk's complete groups of r tokens (a trailing partial
+    group stays in the window rows), causal indexing of every chunk token over
+    the prefix plus the chunk's own entries, attention with the banded window
+    (rows t-W+1..t of the chunk and the prefix tail)."""
 
     def __init__(self, wl, device, seed_offset=0):
         super().__init__(wl, device, seed_offset)
         torch, csa, B, r, s = self.torch, self.csa, self.B, wl.ratio, self.seed
         Tq, ctx, W = wl.tq, wl.ctx, wl.window
+        Tc = Tq - Tq % r  # tokens that complete a compressor group
         self.N = (ctx + Tq) // r
         self.make_caches(self.N)
         S = W - 1 + Tq
         self.h = {
-            "x": synth.normal_bf16(synth.rng(s, "x_chunk"), (B, Tq, 512)),
+            "x": synth.normal_bf16(synth.rng(s, "x_chunk"), (B, Tc, 512)),
             "pos0": np.full(B, ctx, np.int64),
             "q": synth.normal_bf16(synth.rng(s, "q"), (B, Tq, 64, 512)),
             "q_idx": synth.normal_bf16(synth.rng(s, "q_idx"), (B, Tq, 32, 128)),
@@ -395,8 +398,10 @@ class OracleStep:
         self.w = synth.merge_weights(synth.rng(s, "w"), r, 512)
         self.w_idx = synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512))
         if self.prefill:
-            rows = np.array([0, 2047, 2048, wl.tq - 1], np.int64)
-            self.x = synth.normal_bf16(synth.rng(s, "x_chunk"), (1, wl.tq, 512))
+            # every row of a short block, else 4 rows: both ends and both sides of position 2048
+            rows = np.arange(wl.tq) if wl.tq <= 8 else np.array([0, 2047, 2048, wl.tq - 1], np.int64)
+            Tc = wl.tq - wl.tq % r
+            self.x = synth.normal_bf16(synth.rng(s, "x_chunk"), (1, Tc, 512))
             self.pos0 = np.array([ctx], np.int64)
             self.q = synth.normal_bf16(synth.rng(s, "q"), (1, wl.tq, 64, 512))[:, rows]
             self.q_idx = synth.normal_bf16(synth.rng(s, "q_idx"), (1, wl.tq, 32, 128))[:, rows]
@@ -406,7 +411,8 @@ class OracleStep:
             self.q_pos = (ctx + rows).reshape(1, -1)
             self.n_ent = np.array([N], np.int32)
             self.units = len(rows)
-            self.sample = "4 query rows (0, 2047, 2048, last) of the %d-token chunk plus its compressor" % wl.tq
+            self.sample = ("all %d query rows of one sequence's block plus its compressor" % wl.tq if wl.tq <= 8 else
+                           "4 query rows (0, 2047, 2048, last) of the %d-token chunk plus its compressor" % wl.tq)
         else:
             self.x = synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512))
             self.pos0 = np.full(B, ctx - r, np.int64)

@@ -3,7 +3,9 @@
 // s_j = sum_h w_h ReLU(q_h . K_j) (DeepSeek-V4.1 Flash, hn.213312.xyz
 // sec. 2.3.1; 36kr "CSA2") for every visible indexer-K entry (Full) or for the
 // entries of an HSI pool (Reindex, hn.213312.xyz sec. 2.3.4).  Per CTA: a
-// range of 128-entry tiles of one group of QPC queries of one sequence.
+// range of 128-entry tiles of one group of up to QPC queries of one sequence
+// (a multi-query decode block of up to 6 positions shares one group, so every
+// indexer-K tile is read once for all of them).
 //  - page mode (Full): warp 8 (one elected lane) streams whole cache pages,
 //    two per tile, into a shared-memory ring with 1-D bulk copies completing
 //    on mbarriers;
@@ -50,6 +52,7 @@ struct TileFmt {
 
 struct ScoreArgs {
   int q0, Tq, r;
+  int seg, gps;         // query groups: segments of `seg` queries from q0, `gps` groups of QPC each
   const uint16_t* q_idx;
   const float* head_w;
   const int64_t* q_pos;
@@ -139,14 +142,17 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   __shared__ int32_t gtab[kGather ? kMaxGatherTiles * 128 : 1];   // gather mode: page*64+slot or -1
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int g0 = a.q0 + blockIdx.y * QPC;  // first query of the group (same sequence)
+  const int jg = blockIdx.y % a.gps;
+  const int qc0 = (blockIdx.y / a.gps) * a.seg + jg * QPC;  // chunk-local index of the group's first query
+  const int n_act = min(QPC, a.seg - jg * QPC);             // queries of the group; the rest are masked
+  const int g0 = a.q0 + qc0;                                // first query of the group (same sequence)
   const int b = g0 / a.Tq;
   int64_t nv[QPC];
   int64_t nv_max = 0;
 #pragma unroll
   for (int q = 0; q < QPC; ++q) {
     const int64_t ne = a.n_entries[b] < a.max_entries ? a.n_entries[b] : a.max_entries;
-    nv[q] = visible_entries(a.q_pos[g0 + q], a.r, ne);
+    nv[q] = q < n_act ? visible_entries(a.q_pos[g0 + q], a.r, ne) : 0;
     nv_max = nv[q] > nv_max ? nv[q] : nv_max;
   }
   const int64_t npos = kGather ? (int64_t)a.n_blocks * kHsiBlock : nv_max;
@@ -154,8 +160,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   const int64_t t_begin = (int64_t)blockIdx.x * a.tiles_per_cta;
   const int64_t t_end = t_begin + a.tiles_per_cta < n_tiles ? t_begin + a.tiles_per_cta : n_tiles;
   if (t_begin >= t_end) {  // uniform: the whole CTA leaves before any barrier, its slots empty
-    if (tid < QPC) {
-      uint32_t* kr = a.krange + ((int64_t)(blockIdx.y * QPC + tid) * a.kr_stride + blockIdx.x) * 2;
+    if (tid < n_act) {
+      uint32_t* kr = a.krange + ((int64_t)(qc0 + tid) * a.kr_stride + blockIdx.x) * 2;
       kr[0] = 0xFFFFFFFFu;
       kr[1] = 0u;
     }
@@ -256,8 +262,10 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   }
   for (int i = tid; i < kN * kIdxDim / 8; i += kConsumers) {
     const int row = (8 * i) / kIdxDim, k = (8 * i) % kIdxDim;  // row = q*32 + h; 8 channels per load
-    uint4 v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
-                                                   (row % kIdxHeads) * kIdxDim + k));
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);  // masked queries: zero rows
+    if (row / kIdxHeads < n_act)
+      v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
+                                               (row % kIdxHeads) * kIdxDim + k));
     if (!kBf16) {
       uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -270,7 +278,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = v;
   }
   for (int i = tid; i < QPC * kIdxHeads; i += kConsumers)
-    hw[i / kIdxHeads][i % kIdxHeads] = a.head_w ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;
+    hw[i / kIdxHeads][i % kIdxHeads] =
+        (a.head_w && i / kIdxHeads < n_act) ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;
   if (kGather) {
     for (int i = tid; i < n_my * 128; i += kConsumers) {
       const int64_t p = t_begin * 128 + i;  // pool position
@@ -351,6 +360,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
       const int64_t pos = (t_begin + ie) * 128 + lt;  // entry id (page mode) / pool position (gather mode)
 #pragma unroll
       for (int q = 0; q < QPC; ++q) {
+        if (q >= n_act) break;  // uniform over the CTA
         uint32_t d[32];
         tc::tmem_ld32(tc::taddr(tb, lane_base, dcol + 32 * q), d);
         tc::tmem_wait_ld();
@@ -358,7 +368,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
 #pragma unroll
         for (int hh = 0; hh < kIdxHeads; ++hh) sc = fmaf(hw[q][hh], fmaxf(__uint_as_float(d[hh]), 0.0f), sc);
         sc += 0.0f;
-        const int qc = blockIdx.y * QPC + q;
+        const int qc = qc0 + q;
         const bool valid = kGather ? (gtab[ie * 128 + lt] >= 0) : (pos < nv[q]);
         if (!ok) sc = -INFINITY;
         if (kGather) {
@@ -466,8 +476,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   tc::fence_before_sync();
   consumers_sync(kConsumers);
   if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
-  if (tid < QPC) {  // one slot per CTA and query: no initialisation of global state needed
-    uint32_t* kr = a.krange + ((int64_t)(blockIdx.y * QPC + tid) * a.kr_stride + blockIdx.x) * 2;
+  if (tid < n_act) {  // one slot per CTA and query: no initialisation of global state needed
+    uint32_t* kr = a.krange + ((int64_t)(qc0 + tid) * a.kr_stride + blockIdx.x) * 2;
     kr[0] = rng_lo[tid];
     kr[1] = rng_hi[tid];
   }
@@ -493,8 +503,20 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
                             uint32_t* krange, int kr_stride, int* n_slots, int32_t* status, int num_sms,
                             cudaStream_t stream) {
   const bool gather = pool != nullptr;
-  const int qpc = (!gather && Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) ? 4 : 1;
-  const int groups = nq / qpc;
+  // query groups sharing every K tile: runs of 4 queries when the chunk splits
+  // into them without crossing a sequence (prefill chunks); whole sequences of
+  // a chunk of whole sequences otherwise (multi-query decode: up to 6 queries
+  // in one group, longer blocks in groups of 4); single queries else
+  int qpc = 1, seg = 1;
+  if (!gather && Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) {
+    qpc = 4;
+    seg = 4;
+  } else if (!gather && Tq > 1 && q0 % Tq == 0 && nq % Tq == 0) {
+    qpc = Tq <= 6 ? 6 : 4;
+    seg = Tq;
+  }
+  const int gps = (seg + qpc - 1) / qpc;
+  const int groups = nq / seg * gps;
   const int64_t tiles = gather ? ((int64_t)cfg.hsi_blocks * kHsiBlock + 127) / 128 : (max_entries + 127) / 128;
   // CTAs per query group: one wave of one CTA per SM when there are few
   // groups (latency-bound: every CTA starts at once), else two waves for
@@ -506,14 +528,16 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   const int splits = (int)((tiles + per - 1) / per);
   if (splits > kr_stride) return cudaErrorInvalidValue;
   *n_slots = splits;
-  ScoreArgs a{q0, Tq, cfg.ratio, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
+  ScoreArgs a{q0, Tq, cfg.ratio, seg, gps, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
               pool, cfg.hsi_blocks, scores, stride, bmax, krange, kr_stride, status};
   if (cfg.cache_dtype == CSA2_CACHE_FP4) {
     if (gather) return launch_one<CSA2_CACHE_FP4, 1, true>(a, groups, splits, stream);
+    if (qpc == 6) return launch_one<CSA2_CACHE_FP4, 6, false>(a, groups, splits, stream);
     return qpc == 4 ? launch_one<CSA2_CACHE_FP4, 4, false>(a, groups, splits, stream)
                     : launch_one<CSA2_CACHE_FP4, 1, false>(a, groups, splits, stream);
   }
   if (gather) return launch_one<CSA2_CACHE_BF16, 1, true>(a, groups, splits, stream);
+  if (qpc == 6) return launch_one<CSA2_CACHE_BF16, 6, false>(a, groups, splits, stream);
   return qpc == 4 ? launch_one<CSA2_CACHE_BF16, 4, false>(a, groups, splits, stream)
                   : launch_one<CSA2_CACHE_BF16, 1, false>(a, groups, splits, stream);
 }

@@ -131,6 +131,8 @@ WORKLOADS = {
     "prefill_4096_on_1m_r2_fp4": Workload(
         "prefill_4096_on_1m_r2_fp4", batch=1, ctx=1048576, ratio=2, cache="fp4", theta=1e4, seed=4,
         tq=4096),
+    "mqdecode_b8_q5_ctx32768_r2_fp4": Workload(
+        "mqdecode_b8_q5_ctx32768_r2_fp4", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=6, tq=5),
     "encoder_group6_b8_ctx32768_r2_fp4": Workload(
         "encoder_group6_b8_ctx32768_r2_fp4", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=5,
         layers=ENCODER_GROUP),

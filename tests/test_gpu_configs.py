@@ -1,9 +1,9 @@
-"""GPU-vs-oracle parity at the full sizes of the five synthetic workloads,
-in the launch configurations bench.py times.  The GPU runs the whole
-workload; the oracle checks every output where it finishes in seconds and
-sampled sequences / query rows otherwise (decode b32: 3 of 32 sequences;
-decoder group: 2 of 16 sequences through all 20 layers; prefill: 6 of 4096
-query rows).  Each side works from its own cache: the compressor runs on
+"""GPU-vs-oracle parity at the full sizes of the synthetic workloads, in
+the launch configurations bench.py times.  The GPU runs the whole workload;
+the oracle checks every output where it finishes in seconds (decode b1 and
+b8, the multi-query decode block) and sampled sequences / query rows
+otherwise (decode b32: 3 of 32 sequences; decoder group: 2 of 16 sequences
+through all 20 layers; prefill: 6 of 4096 query rows).  Each side works from its own cache: the compressor runs on
 both, the seeded random prefix is shared input."""
 import math
 
@@ -258,4 +258,63 @@ def test_prefill_chunk_sampled_rows():
     o_out = oracle.attend(om, n_arr, q[:, rows], o_top, swa, swa_len, swa_pos0, q_pos[:, rows], W, SCALE)
     err = P.attention_rel_err(out.cpu().numpy()[:, rows], o_out)
     print("prefill: attention max row rel err %.3g on %d sampled rows" % (err, len(rows)))
+    assert err <= P.ATT_TOL
+
+
+def test_multi_query_decode_block_every_row():
+    """Multi-query decode: a block of 5 draft positions per sequence appended
+    to 8 sequences of 32768 tokens, r = 2.  The compressor takes the block's
+    two complete groups (the fifth token stays in the window rows); each
+    sequence's 5 queries share one indexer group; every query row of every
+    sequence is checked against the oracle."""
+    wl = synth.WORKLOADS["mqdecode_b8_q5_ctx32768_r2_fp4"]
+    B, r, Tq, ctx, W = wl.batch, wl.ratio, wl.tq, wl.ctx, wl.window
+    Tc = Tq - Tq % r
+    N, P0 = (ctx + Tq) // r, ctx // r
+    pm, pi = _paged.cache_pair(B, N, D, wl.cache, wl.seed), _paged.cache_pair(B, N, CI, wl.cache, wl.seed + 1)
+    om, oi = oracle.Cache(B, N, D, wl.cache), oracle.Cache(B, N, CI, wl.cache)
+    for b in range(B):
+        m, i = _prefix(wl, b, P0)
+        om.codes[b, :P0], om.scales[b, :P0] = m.codes[0], m.scales[0]
+        oi.codes[b, :P0], oi.scales[b, :P0] = i.codes[0], i.scales[0]
+    _paged.upload(pm, om)
+    _paged.upload(pi, oi)
+    cfg = _cfg(wl)
+    s = wl.seed
+    x = synth.normal_bf16(synth.rng(s, "x_chunk"), (B, Tc, D))
+    w = synth.merge_weights(synth.rng(s, "w"), r, D)
+    w_idx = synth.normal_bf16(synth.rng(s, "w_idx"), (D, CI), std=1 / math.sqrt(D))
+    q = synth.normal_bf16(synth.rng(s, "q"), (B, Tq, 64, D))
+    q_idx = synth.normal_bf16(synth.rng(s, "q_idx"), (B, Tq, 32, CI))
+    S = W - 1 + Tq
+    swa = synth.normal_bf16(synth.rng(s, "swa"), (B, S, D))
+    swa_len, swa_pos0 = np.full(B, S, np.int32), np.full(B, ctx - W + 1, np.int64)
+    q_pos = np.tile(ctx + np.arange(Tq, dtype=np.int64), (B, 1))
+    pos0 = np.full(B, ctx, np.int64)
+    n_ent = torch.full((B,), P0, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device="cuda")
+    ws = torch.empty(csa.index_workspace_bytes(cfg, B, Tq, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, Tq, 64, D), dtype=torch.float32, device="cuda")
+    csa.compress(cfg, _paged.dev(x), _paged.dev(pos0), _paged.dev(w), _paged.dev(w_idx), pm, pi, n_ent, status=st)
+    csa.index_topk(cfg, _paged.dev(q_idx), _paged.dev(q_pos), pi, n_ent, N, topk, ws, status=st)
+    csa.attend(cfg, _paged.dev(q), pm, n_ent, topk, _paged.dev(swa), _paged.dev(swa_len), _paged.dev(swa_pos0),
+               _paged.dev(q_pos), out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert (n_ent.cpu().numpy() == N).all()
+    diag = oracle.compress(x, pos0, w, w_idx, om, oi, r, wl.theta, diagnostics=True)
+    exc = _check_compress(om, oi, pm, pi, diag, pos0, r, Tc // r, wl.cache)
+    print("multi-query block compressor: %d near-boundary codes excused" % exc)
+    n_arr = np.full(B, N, np.int32)
+    o_top, _, sc = oracle.index_topk(oi, n_arr, q_idx, q_pos, r, wl.topk, want_scores=True)
+    g_top = topk.cpu().numpy()
+    assert P.topk_mismatch(g_top.reshape(B * Tq, -1), o_top.reshape(B * Tq, -1), sc.reshape(B * Tq, -1), wl.topk,
+                           exact=False) == 0
+    assert (g_top >= 0).all()  # every query sees far more than k entries: no padding
+    # the block's own entries are visible only from the positions that complete them
+    assert not np.isin(g_top[:, 0], [P0, P0 + 1]).any() and not np.isin(g_top[:, 2], [P0 + 1]).any()
+    o_out = oracle.attend(om, n_arr, q, o_top, swa, swa_len, swa_pos0, q_pos, W, SCALE)
+    err = P.attention_rel_err(out.cpu().numpy(), o_out)
+    print("multi-query block: attention max row rel err %.3g over %d rows" % (err, B * Tq))
     assert err <= P.ATT_TOL

@@ -373,6 +373,29 @@ def test_index_prefill_queries_share_tiles(integer):
                 assert all(abs(bm[b_] - kth) <= P.NEAR_TIE * abs(kth) for b_ in gp ^ op)
 
 
+@pytest.mark.parametrize("dtype,Tq,chunk", [("fp4", 5, None), ("fp4", 2, None), ("bf16", 6, None),
+                                            ("fp4", 7, None), ("fp4", 5, 5), ("bf16", 5, 6)])
+def test_index_multi_query_blocks_share_tiles(dtype, Tq, chunk):
+    """Multi-query decode: Tq consecutive positions of each of 3 sequences.
+    A chunk of whole sequences puts up to 6 queries of a sequence in one
+    group (Tq = 7: a group of 4 and a masked group of 3); a chunk that cuts a
+    sequence (6 queries of 5-query blocks) falls back to one query per group.
+    Integer inputs: top-k and HSI pool bit-exact, with head weights and
+    ragged n_entries."""
+    B, N, k, nb = 3, 4000, 512, 64
+    oc, pc = _idx_caches(B, N, dtype, seed=26 + Tq, integer=True, dup=True)
+    q_idx = synth.integer_bf16(synth.rng(26, "q%d" % Tq), (B, Tq, H, CI), -1, 1)
+    hw = synth.rng(26, "hw").integers(0, 3, size=(B, Tq, H)).astype(np.float32)
+    n_ent = np.array([N, 3100, 700], np.int32)
+    q_pos = np.stack([2 * n - Tq + np.arange(Tq) for n in n_ent]).astype(np.int64)  # the block ends the context
+    cfg = csa.Cfg(ratio=2, cache_dtype=csa.CACHE_FP4 if dtype == "fp4" else csa.CACHE_BF16, topk=k, hsi_blocks=nb)
+    g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, head_w=hw, want_pool=True, ws_queries=chunk)
+    o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=2, k=k, head_w=hw, hsi_blocks=nb,
+                                         want_pool=True)
+    np.testing.assert_array_equal(g_top, o_top)
+    np.testing.assert_array_equal(g_pool, o_pool)
+
+
 def test_index_long_cache_many_tiles_per_cta():
     """One decode query per sequence over 40000 entries: each CTA walks many
     tiles through the shared-memory ring (wrap-around of every stage)."""

@@ -26,6 +26,9 @@ _lib = None
 
 CACHE_FP4 = 0
 CACHE_BF16 = 1
+CACHE_FP4_G32 = 2   # FP4 main cache, indexer entries with one scale per 32 channels (68 B)
+SWA_BF16 = 0
+SWA_MXFP8 = 1
 
 
 def build(force: bool = False) -> str:
@@ -67,6 +70,12 @@ def lib():
             L.orc_e2m1_nearest_code.argtypes = [d, d]
             L.orc_fp4_encode.argtypes = [vp, i, vp, vp]
             L.orc_fp4_decode.argtypes = [vp, vp, i, vp]
+            L.orc_fp4_encode_g.argtypes = [vp, i, i, vp, vp]
+            L.orc_fp4_decode_g.argtypes = [vp, vp, i, i, vp]
+            L.orc_e8m0_value.restype = d
+            L.orc_e8m0_value.argtypes = [i]
+            L.orc_mxfp8_encode.argtypes = [vp, i, vp]
+            L.orc_mxfp8_decode.argtypes = [vp, i, vp]
             L.orc_compress.restype = i
             L.orc_compress.argtypes = [i, i, i, i, i, i, d, i, vp, vp, vp, vp, i,
                                        vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -74,11 +83,11 @@ def lib():
             L.orc_index_topk.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i, i, i,
                                          vp, vp, vp, vp]
             L.orc_attend.restype = i
-            L.orc_attend.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, i, vp, i, vp, vp, vp,
+            L.orc_attend.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, i, vp, i, i, vp, vp, vp,
                                      i, d, vp, vp]
             L.orc_attend_dense.restype = i
-            L.orc_attend_dense.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, i, vp, vp, vp,
-                                           i, d, vp]
+            L.orc_attend_dense.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, i, i, vp, vp,
+                                           vp, i, d, vp]
             L.orc_threads.restype = i
             _lib = L
     return _lib
@@ -118,42 +127,82 @@ def e2m1_nearest_code(x: float, scale: float) -> int:
     return lib().orc_e2m1_nearest_code(float(x), float(scale))
 
 
-def fp4_encode(x: np.ndarray):
-    """x [..., C] fp64 -> (codes [..., C/2] u8, scales [..., C/16] u8)."""
+def fp4_encode(x: np.ndarray, group: int = 16):
+    """x [..., C] fp64 -> (codes [..., C/2] u8, scales [..., C/group] u8)."""
     x = _c(x, np.float64)
     Cn = x.shape[-1]
     rows = x.reshape(-1, Cn)
     codes = np.zeros((rows.shape[0], Cn // 2), np.uint8)
-    scales = np.zeros((rows.shape[0], Cn // 16), np.uint8)
+    scales = np.zeros((rows.shape[0], Cn // group), np.uint8)
     L = lib()
     for n in range(rows.shape[0]):
-        L.orc_fp4_encode(_p(rows[n]), Cn, _p(codes[n]), _p(scales[n]))
-    return codes.reshape(x.shape[:-1] + (Cn // 2,)), scales.reshape(x.shape[:-1] + (Cn // 16,))
+        L.orc_fp4_encode_g(_p(rows[n]), Cn, group, _p(codes[n]), _p(scales[n]))
+    return codes.reshape(x.shape[:-1] + (Cn // 2,)), scales.reshape(x.shape[:-1] + (Cn // group,))
 
 
 def fp4_decode(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Inverse of fp4_encode; the scale group (16 or 32) follows from the shapes."""
     codes = _c(codes, np.uint8)
     scales = _c(scales, np.uint8)
     Cn = codes.shape[-1] * 2
+    group = Cn // scales.shape[-1]
     cr = codes.reshape(-1, Cn // 2)
-    sr = scales.reshape(-1, Cn // 16)
+    sr = scales.reshape(-1, Cn // group)
     out = np.zeros((cr.shape[0], Cn), np.float64)
     L = lib()
     for n in range(cr.shape[0]):
-        L.orc_fp4_decode(_p(cr[n]), _p(sr[n]), Cn, _p(out[n]))
+        L.orc_fp4_decode_g(_p(cr[n]), _p(sr[n]), Cn, group, _p(out[n]))
     return out.reshape(codes.shape[:-1] + (Cn,))
+
+
+def e8m0_value(byte: int) -> float:
+    return lib().orc_e8m0_value(int(byte))
+
+
+def mxfp8_encode(x: np.ndarray) -> np.ndarray:
+    """x [..., C] fp64 -> MXFP8 rows [..., C + C/32] u8 (elements, then scales)."""
+    x = _c(x, np.float64)
+    Cn = x.shape[-1]
+    rows = x.reshape(-1, Cn)
+    out = np.zeros((rows.shape[0], Cn + Cn // 32), np.uint8)
+    L = lib()
+    for n in range(rows.shape[0]):
+        L.orc_mxfp8_encode(_p(rows[n]), Cn, _p(out[n]))
+    return out.reshape(x.shape[:-1] + (Cn + Cn // 32,))
+
+
+def mxfp8_decode(rows: np.ndarray) -> np.ndarray:
+    rows = _c(rows, np.uint8)
+    Cn = rows.shape[-1] * 32 // 33
+    rr = rows.reshape(-1, rows.shape[-1])
+    out = np.zeros((rr.shape[0], Cn), np.float64)
+    L = lib()
+    for n in range(rr.shape[0]):
+        L.orc_mxfp8_decode(_p(rr[n]), Cn, _p(out[n]))
+    return out.reshape(rows.shape[:-1] + (Cn,))
+
+
+def swa_encode(bits: np.ndarray) -> np.ndarray:
+    """bf16 window rows [..., C] (bit patterns) -> MXFP8 rows [..., C + C/32]."""
+    return mxfp8_encode(bf16_bits_to_f64(bits))
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (_c(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 # ------------------------------------------------------------- the path ----
 
 class Cache:
-    """Canonical (unpaged) cache of B sequences x n_cap entries of `channels`."""
+    """Canonical (unpaged) cache of B sequences x n_cap entries of `channels`:
+    "fp4" (one scale per 16 channels), "fp4g32" (one per 32: the 68-byte
+    indexer entry) or "bf16"."""
 
     def __init__(self, B: int, n_cap: int, channels: int, dtype: str):
         self.B, self.n_cap, self.channels, self.dtype = B, n_cap, channels, dtype
-        if dtype == "fp4":
+        if dtype in ("fp4", "fp4g32"):
             self.codes = np.zeros((B, n_cap, channels // 2), np.uint8)
-            self.scales = np.zeros((B, n_cap, channels // 16), np.uint8)
+            self.scales = np.zeros((B, n_cap, channels // (16 if dtype == "fp4" else 32)), np.uint8)
             self.bf16 = None
         elif dtype == "bf16":
             self.codes = self.scales = None
@@ -163,11 +212,11 @@ class Cache:
 
     @property
     def dtype_code(self) -> int:
-        return CACHE_FP4 if self.dtype == "fp4" else CACHE_BF16
+        return {"fp4": CACHE_FP4, "fp4g32": CACHE_FP4_G32, "bf16": CACHE_BF16}[self.dtype]
 
     def values(self) -> np.ndarray:
         """Decoded fp64 entries [B][n_cap][channels]."""
-        if self.dtype == "fp4":
+        if self.dtype != "bf16":
             return fp4_decode(self.codes, self.scales)
         return (self.bf16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
@@ -187,7 +236,10 @@ def compress(x, pos0, w, w_idx, main: Cache, idx: Cache, r: int, theta: float, r
     if diagnostics:
         for k, n in (("pre_main", D), ("mag_main", D), ("pre_idx", Ci), ("mag_idx", Ci)):
             diag[k] = np.zeros((B, M, n), np.float64)
-    rc = lib().orc_compress(B, T, D, Ci, rope_dims, r, float(theta), main.dtype_code,
+    if idx.dtype == "fp4g32" and main.dtype != "fp4":
+        raise ValueError("the 68-byte indexer entry goes with an FP4 main cache")
+    code = idx.dtype_code if idx.dtype == "fp4g32" else main.dtype_code
+    rc = lib().orc_compress(B, T, D, Ci, rope_dims, r, float(theta), code,
                             _p(x), _p(pos0), _p(w), _p(w_idx), main.n_cap,
                             _p(main.codes), _p(main.scales), _p(main.bf16),
                             _p(idx.codes), _p(idx.scales), _p(idx.bf16),
@@ -220,20 +272,27 @@ def index_topk(idx: Cache, n_entries, q_idx, q_pos, r: int, k: int, head_w=None,
     return topk, pool_out, scores
 
 
+def _swa(swa):
+    """Window rows: uint16 [B][S][D] bf16 bits, or uint8 [B][S][D + D/32] MXFP8 rows."""
+    if swa.dtype == np.uint8:
+        return _c(swa, np.uint8), SWA_MXFP8
+    return _c(swa, np.uint16), SWA_BF16
+
+
 def attend(main: Cache, n_entries, q, topk, swa, swa_len, swa_pos0, q_pos, window: int, scale: float,
            want_lse: bool = False):
-    """a7.  q [B][Tq][Hm][D] bf16 bits, topk [B][Tq][k], swa [B][S][D] bf16 bits.
-    Returns out [B][Tq][Hm][D] fp64 (and lse [B][Tq][Hm])."""
+    """a7.  q [B][Tq][Hm][D] bf16 bits, topk [B][Tq][k], swa [B][S][D] bf16 bits (uint16) or
+    [B][S][D + D/32] MXFP8 rows (uint8).  Returns out [B][Tq][Hm][D] fp64 (and lse [B][Tq][Hm])."""
     q = _c(q, np.uint16)
     B, Tq, Hm, D = q.shape
     topk = _c(topk, np.int32)
     k = topk.shape[-1]
-    swa = _c(swa, np.uint16)
+    swa, fmt = _swa(swa)
     S = swa.shape[1]
     out = np.zeros((B, Tq, Hm, D), np.float64)
     lse = np.zeros((B, Tq, Hm), np.float64) if want_lse else None
     rc = lib().orc_attend(B, Tq, Hm, D, main.dtype_code, main.n_cap, _p(main.codes), _p(main.scales),
-                          _p(main.bf16), _p(_c(n_entries, np.int32)), _p(q), _p(topk), k, _p(swa), S,
+                          _p(main.bf16), _p(_c(n_entries, np.int32)), _p(q), _p(topk), k, _p(swa), fmt, S,
                           _p(_c(swa_len, np.int32)), _p(_c(swa_pos0, np.int64)), _p(_c(q_pos, np.int64)),
                           window, float(scale), _p(out), _p(lse))
     if rc != 0:
@@ -245,12 +304,12 @@ def attend_dense(main: Cache, n_entries, q, swa, swa_len, swa_pos0, q_pos, r: in
                  scale: float):
     q = _c(q, np.uint16)
     B, Tq, Hm, D = q.shape
-    swa = _c(swa, np.uint16)
+    swa, fmt = _swa(swa)
     S = swa.shape[1]
     out = np.zeros((B, Tq, Hm, D), np.float64)
     rc = lib().orc_attend_dense(B, Tq, Hm, D, r, main.dtype_code, main.n_cap, _p(main.codes),
                                 _p(main.scales), _p(main.bf16), _p(_c(n_entries, np.int32)), _p(q),
-                                _p(swa), S, _p(_c(swa_len, np.int32)), _p(_c(swa_pos0, np.int64)),
+                                _p(swa), fmt, S, _p(_c(swa_len, np.int32)), _p(_c(swa_pos0, np.int64)),
                                 _p(_c(q_pos, np.int64)), window, float(scale), _p(out))
     if rc != 0:
         raise ValueError("orc_attend_dense rejected its arguments (%d)" % rc)

@@ -96,14 +96,16 @@ int orc_e2m1_nearest_code(double x, double scale) {
   return (x < 0.0) ? (mag | 8) : mag;
 }
 
-/* One E4M3 scale per 16 consecutive channels: scale = RNE_E4M3(amax / 6),
- * i.e. the E4M3 value nearest to amax / 6, decided by comparing amax with
- * 6 * midpoint (exact).  A zero scale gives all-zero codes. */
-void orc_fp4_encode(const double* x, int C, uint8_t* codes, uint8_t* scales) {
-  for (int g = 0; g < C / 16; ++g) {
+/* One E4M3 scale per `group` consecutive channels (16: the main-KV format
+ * of sec. 2.4.4; 32: the 68-byte indexer entry of sec. 3.1): scale =
+ * RNE_E4M3(amax / 6), i.e. the E4M3 value nearest to amax / 6, decided by
+ * comparing amax with 6 * midpoint (exact).  A zero scale gives all-zero
+ * codes. */
+void orc_fp4_encode_g(const double* x, int C, int group, uint8_t* codes, uint8_t* scales) {
+  for (int g = 0; g < C / group; ++g) {
     double amax = 0.0;
-    for (int i = 0; i < 16; ++i) {
-      double a = fabs(x[16 * g + i]);
+    for (int i = 0; i < group; ++i) {
+      double a = fabs(x[group * g + i]);
       if (a > amax) amax = a;
     }
     int sc = 126;
@@ -114,20 +116,71 @@ void orc_fp4_encode(const double* x, int C, uint8_t* codes, uint8_t* scales) {
     }
     scales[g] = (uint8_t)sc;
     double s = orc_e4m3_value(sc);
-    for (int i = 0; i < 16; i += 2) {
-      int c0 = orc_e2m1_nearest_code(x[16 * g + i], s);
-      int c1 = orc_e2m1_nearest_code(x[16 * g + i + 1], s);
-      codes[(16 * g + i) / 2] = (uint8_t)(c0 | (c1 << 4));
+    for (int i = 0; i < group; i += 2) {
+      int c0 = orc_e2m1_nearest_code(x[group * g + i], s);
+      int c1 = orc_e2m1_nearest_code(x[group * g + i + 1], s);
+      codes[(group * g + i) / 2] = (uint8_t)(c0 | (c1 << 4));
     }
   }
 }
 
-void orc_fp4_decode(const uint8_t* codes, const uint8_t* scales, int C, double* out) {
+void orc_fp4_decode_g(const uint8_t* codes, const uint8_t* scales, int C, int group, double* out) {
   for (int i = 0; i < C; ++i) {
     int byte = codes[i / 2];
     int code = (i & 1) ? (byte >> 4) : (byte & 15);
-    out[i] = orc_e2m1_value(code) * orc_e4m3_value(scales[i / 16]);
+    out[i] = orc_e2m1_value(code) * orc_e4m3_value(scales[i / group]);
   }
+}
+
+void orc_fp4_encode(const double* x, int C, uint8_t* codes, uint8_t* scales) {
+  orc_fp4_encode_g(x, C, 16, codes, scales);
+}
+
+void orc_fp4_decode(const uint8_t* codes, const uint8_t* scales, int C, double* out) {
+  orc_fp4_decode_g(codes, scales, C, 16, out);
+}
+
+/* OCP MX E8M0 scale: 2^(byte - 127); 0xFF is NaN. */
+double orc_e8m0_value(int byte) {
+  if (byte == 255) return NAN;
+  return ldexp(1.0, byte - 127);
+}
+
+/* MXFP8 row of C channels (E4M3 elements, one E8M0 scale per 32 channels,
+ * OCP MX): row = C element bytes (channel c at byte c) then C/32 scale
+ * bytes.  Per block: X = 2^(floor(log2 amax) - 8), 8 being the exponent of
+ * E4M3's largest binade, so that amax / X lies in [256, 512); the scale byte
+ * is clamped to 0..254; an all-zero block takes byte 0.  Element = the E4M3
+ * code nearest to |x| / X (exact: X is a power of two), ties to the even
+ * code, saturating at 448, sign bit set for negative values that do not
+ * round to zero. */
+void orc_mxfp8_encode(const double* x, int C, uint8_t* row) {
+  for (int g = 0; g < C / 32; ++g) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      double a = fabs(x[32 * g + i]);
+      if (a > amax) amax = a;
+    }
+    int sb = 0;
+    if (amax > 0.0) {
+      int ex;
+      frexp(amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+      sb = (ex - 1) - 8 + 127;
+      if (sb < 0) sb = 0;
+      if (sb > 254) sb = 254;
+    }
+    row[C + g] = (uint8_t)sb;
+    double X = orc_e8m0_value(sb);
+    for (int i = 0; i < 32; ++i) {
+      double v = x[32 * g + i];
+      int mag = orc_e4m3_nearest_code(fabs(v) / X);
+      row[32 * g + i] = (uint8_t)((v < 0.0 && mag != 0) ? (mag | 0x80) : mag);
+    }
+  }
+}
+
+void orc_mxfp8_decode(const uint8_t* row, int C, double* out) {
+  for (int i = 0; i < C; ++i) out[i] = orc_e4m3_value(row[i]) * orc_e8m0_value(row[C + i / 32]);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -140,7 +193,8 @@ int orc_compress(int B, int T, int D, int Ci, int rope_dims, int r, double theta
                  uint8_t* main_codes, uint8_t* main_scales, uint16_t* main_bf16,
                  uint8_t* idx_codes, uint8_t* idx_scales, uint16_t* idx_bf16,
                  double* pre_main, double* mag_main, double* pre_idx, double* mag_idx) {
-  if (B < 0 || T < 0 || r < 1 || T % r || D % 16 || Ci % 16 || rope_dims % 2 || rope_dims > D)
+  if (B < 0 || T < 0 || r < 1 || T % r || D % 16 || Ci % 16 || (cache_dtype == ORC_CACHE_FP4_G32 && Ci % 32) ||
+      rope_dims % 2 || rope_dims > D)
     return -1;
   int M = T / r;
   for (int b = 0; b < B; ++b)
@@ -185,7 +239,7 @@ int orc_compress(int B, int T, int D, int Ci, int rope_dims, int r, double theta
       if (pre_main) memcpy(pre_main + row * D, v, sizeof(double) * D);
       if (mag_main) memcpy(mag_main + row * D, mag, sizeof(double) * D);
       /* store, then read back the stored entry (indexer K is projected from it) */
-      if (cache_dtype == ORC_CACHE_FP4) {
+      if (cache_dtype != ORC_CACHE_BF16) {
         orc_fp4_encode(v, D, main_codes + slot * (D / 2), main_scales + slot * (D / 16));
         orc_fp4_decode(main_codes + slot * (D / 2), main_scales + slot * (D / 16), D, e);
       } else {
@@ -209,6 +263,8 @@ int orc_compress(int B, int T, int D, int Ci, int rope_dims, int r, double theta
       if (mag_idx) memcpy(mag_idx + row * Ci, kmag, sizeof(double) * Ci);
       if (cache_dtype == ORC_CACHE_FP4) {
         orc_fp4_encode(kv, Ci, idx_codes + slot * (Ci / 2), idx_scales + slot * (Ci / 16));
+      } else if (cache_dtype == ORC_CACHE_FP4_G32) {
+        orc_fp4_encode_g(kv, Ci, 32, idx_codes + slot * (Ci / 2), idx_scales + slot * (Ci / 32));
       } else {
         for (int k = 0; k < Ci; ++k) idx_bf16[slot * Ci + k] = orc_bf16_round(kv[k]);
       }
@@ -254,6 +310,8 @@ static void orc_load_entry(int cache_dtype, int C, size_t slot, const uint8_t* c
                            const uint8_t* scales, const uint16_t* bf, double* out) {
   if (cache_dtype == ORC_CACHE_FP4) {
     orc_fp4_decode(codes + slot * (C / 2), scales + slot * (C / 16), C, out);
+  } else if (cache_dtype == ORC_CACHE_FP4_G32) {
+    orc_fp4_decode_g(codes + slot * (C / 2), scales + slot * (C / 32), C, 32, out);
   } else {
     for (int c = 0; c < C; ++c) out[c] = orc_bf16_value(bf[slot * C + c]);
   }
@@ -384,12 +442,26 @@ static void orc_attend_rows(int Hm, int D, const double* q, double* const* rows,
   free(l);
 }
 
-static int orc_window_rows(int64_t t, int W, const uint16_t* swa_b, int D, int64_t p0,
+/* Bytes of one window row: bf16 (2 per channel) or MXFP8 (1 per channel plus
+ * one scale byte per 32). */
+static size_t orc_swa_row_bytes(int fmt, int D) { return fmt == ORC_SWA_MXFP8 ? (size_t)D + D / 32 : 2 * (size_t)D; }
+
+static int orc_window_rows(int64_t t, int W, const uint8_t* swa_b, int fmt, int D, int64_t p0,
                            int32_t len, double** rows, int n) {
+  const size_t rb = orc_swa_row_bytes(fmt, D);
   for (int64_t pos = t - W + 1; pos <= t; ++pos) {
     if (pos < 0 || pos < p0 || pos >= p0 + len) continue;
     double* rw = (double*)malloc(sizeof(double) * D);
-    for (int c = 0; c < D; ++c) rw[c] = orc_bf16_value(swa_b[(size_t)(pos - p0) * D + c]);
+    const uint8_t* src = swa_b + (size_t)(pos - p0) * rb;
+    if (fmt == ORC_SWA_MXFP8) {
+      orc_mxfp8_decode(src, D, rw);
+    } else {
+      for (int c = 0; c < D; ++c) {
+        uint16_t bits;
+        memcpy(&bits, src + 2 * c, 2);
+        rw[c] = orc_bf16_value(bits);
+      }
+    }
     rows[n++] = rw;
   }
   return n;
@@ -398,9 +470,11 @@ static int orc_window_rows(int64_t t, int W, const uint16_t* swa_b, int D, int64
 int orc_attend(int B, int Tq, int Hm, int D, int cache_dtype, int n_cap,
                const uint8_t* main_codes, const uint8_t* main_scales, const uint16_t* main_bf16,
                const int32_t* n_entries, const uint16_t* q, const int32_t* topk, int k,
-               const uint16_t* swa, int S, const int32_t* swa_len, const int64_t* swa_pos0,
+               const void* swa, int swa_fmt, int S, const int32_t* swa_len, const int64_t* swa_pos0,
                const int64_t* q_pos, int W, double scale, double* out, double* lse) {
-  if (B < 0 || Tq < 0 || k < 0 || D % 16 || W < 0) return -1;
+  if (B < 0 || Tq < 0 || k < 0 || D % 16 || (swa_fmt == ORC_SWA_MXFP8 && D % 32) || W < 0 || (swa_fmt != ORC_SWA_BF16 && swa_fmt != ORC_SWA_MXFP8))
+    return -1;
+  const size_t rb = orc_swa_row_bytes(swa_fmt, D);
   int bad = 0;
 #pragma omp parallel for collapse(2) schedule(dynamic) reduction(| : bad)
   for (int b = 0; b < B; ++b) {
@@ -420,7 +494,8 @@ int orc_attend(int B, int Tq, int Hm, int D, int cache_dtype, int n_cap,
         ++n;
       }
       int32_t len = swa_len[b] < S ? swa_len[b] : S;
-      n = orc_window_rows(q_pos[qi], W, swa + (size_t)b * S * D, D, swa_pos0[b], len, rows, n);
+      n = orc_window_rows(q_pos[qi], W, (const uint8_t*)swa + (size_t)b * S * rb, swa_fmt, D, swa_pos0[b], len,
+                          rows, n);
       orc_attend_rows(Hm, D, qq, rows, n, scale, out + qi * Hm * D, lse ? lse + qi * Hm : NULL);
       for (int i = 0; i < n; ++i) free(rows[i]);
       free(rows);
@@ -433,9 +508,11 @@ int orc_attend(int B, int Tq, int Hm, int D, int cache_dtype, int n_cap,
 int orc_attend_dense(int B, int Tq, int Hm, int D, int r, int cache_dtype, int n_cap,
                      const uint8_t* main_codes, const uint8_t* main_scales,
                      const uint16_t* main_bf16, const int32_t* n_entries, const uint16_t* q,
-                     const uint16_t* swa, int S, const int32_t* swa_len, const int64_t* swa_pos0,
+                     const void* swa, int swa_fmt, int S, const int32_t* swa_len, const int64_t* swa_pos0,
                      const int64_t* q_pos, int W, double scale, double* out) {
-  if (B < 0 || Tq < 0 || D % 16 || W < 0 || r < 1) return -1;
+  if (B < 0 || Tq < 0 || D % 16 || (swa_fmt == ORC_SWA_MXFP8 && D % 32) || W < 0 || r < 1 || (swa_fmt != ORC_SWA_BF16 && swa_fmt != ORC_SWA_MXFP8))
+    return -1;
+  const size_t rb = orc_swa_row_bytes(swa_fmt, D);
 #pragma omp parallel for collapse(2) schedule(dynamic)
   for (int b = 0; b < B; ++b) {
     for (int t = 0; t < Tq; ++t) {
@@ -452,7 +529,8 @@ int orc_attend_dense(int B, int Tq, int Hm, int D, int r, int cache_dtype, int n
         ++n;
       }
       int32_t len = swa_len[b] < S ? swa_len[b] : S;
-      n = orc_window_rows(q_pos[qi], W, swa + (size_t)b * S * D, D, swa_pos0[b], len, rows, n);
+      n = orc_window_rows(q_pos[qi], W, (const uint8_t*)swa + (size_t)b * S * rb, swa_fmt, D, swa_pos0[b], len,
+                          rows, n);
       orc_attend_rows(Hm, D, qq, rows, n, scale, out + qi * Hm * D, NULL);
       for (int i = 0; i < n; ++i) free(rows[i]);
       free(rows);

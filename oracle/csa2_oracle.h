@@ -16,8 +16,11 @@
  *    from main KV, no overlap, no absolute position embedding), sec. 2.3.2
  *    (Full / Reindex / Reuse), sec. 2.3.4 (HSI: block max, top-2048 blocks of
  *    8, forced latest block), sec. 2.4.4 (FP4 main KV: E2M1 with one E4M3
- *    scale per 16 channels, no global scale, quantised after RoPE),
- *    sec. 3.1 (288 B / 68 B per entry, 890 B/token table), sec. 3.2 (mode
+ *    scale per 16 channels, no global scale, quantised after RoPE; the SWA
+ *    KV kept in FP8, read here as OCP MXFP8: E4M3 elements, one E8M0 scale
+ *    per 32 channels),
+ *    sec. 3.1 (288 B / 68 B per entry, 890 B/token table; 68 B read as 64 B
+ *    of codes + one E4M3 scale per 32 channels), sec. 3.2 (mode
  *    access table), sec. 3.3.1 (key = value, convex-combination readout).
  *  - "What black technologies does DeepSeek V4.1 Flash adopt" (36kr),
  *    sections "CSA2" and "FP4 and Bounded Replay".
@@ -36,8 +39,10 @@
  * Canonical (unpaged) layouts used by every oracle function:
  *  - bf16 tensors are uint16 bit patterns, row-major;
  *  - FP4 entries of C channels: codes [N][C/2] bytes (element 2i in the low
- *    nibble of byte i), scales [N][C/16] E4M3 bytes;
- *  - BF16 cache entries: [N][C] uint16.
+ *    nibble of byte i), scales [N][C/16] E4M3 bytes ([N][C/32] for the
+ *    68-byte indexer entry);
+ *  - BF16 cache entries: [N][C] uint16;
+ *  - MXFP8 window rows: [N][C + C/32] bytes (elements, then block scales).
  *
  * parity pins: every function here is pinned by tests/test_oracle_*.py
  * (codebook anchors, brute-force searches, closed forms and invariants).
@@ -51,6 +56,12 @@ extern "C" {
 
 #define ORC_CACHE_FP4 0
 #define ORC_CACHE_BF16 1
+/* FP4 main KV with the 68-byte indexer entry (sec. 3.1): the indexer cache
+ * carries one E4M3 scale per 32 channels (64 B codes + 4 B scales). */
+#define ORC_CACHE_FP4_G32 2
+/* Window-row formats: bf16, or MXFP8 (sec. 2.4.4: the SWA KV stays FP8) */
+#define ORC_SWA_BF16 0
+#define ORC_SWA_MXFP8 1
 
 /* ---- scalar codecs (OCP MX formats named by the pages, sec. 2.4.4) ---- */
 double orc_bf16_value(uint16_t bits);
@@ -63,6 +74,16 @@ int orc_e2m1_nearest_code(double x, double scale); /* code of x/scale, ties even
 /* FP4 encode / decode of one entry of C channels (C multiple of 16). */
 void orc_fp4_encode(const double* x, int C, uint8_t* codes, uint8_t* scales);
 void orc_fp4_decode(const uint8_t* codes, const uint8_t* scales, int C, double* out);
+/* The same with one scale per `group` channels (16 or 32; C multiple of group). */
+void orc_fp4_encode_g(const double* x, int C, int group, uint8_t* codes, uint8_t* scales);
+void orc_fp4_decode_g(const uint8_t* codes, const uint8_t* scales, int C, int group, double* out);
+
+/* OCP MX E8M0 scale value 2^(byte - 127) (NaN for 0xFF). */
+double orc_e8m0_value(int byte);
+/* MXFP8 window row of C channels (C multiple of 32): C E4M3 element bytes,
+ * then C/32 E8M0 scale bytes; scale 2^(floor(log2 amax) - 8) per block. */
+void orc_mxfp8_encode(const double* x, int C, uint8_t* row);
+void orc_mxfp8_decode(const uint8_t* row, int C, double* out);
 
 /* ---- a1: compressor ----
  * x      [B][T][D] bf16 token latents at positions pos0[b] + i (pos0 % r == 0, T % r == 0)
@@ -84,6 +105,8 @@ int orc_compress(int B, int T, int D, int Ci, int rope_dims, int r, double theta
                  uint8_t* main_codes, uint8_t* main_scales, uint16_t* main_bf16,
                  uint8_t* idx_codes, uint8_t* idx_scales, uint16_t* idx_bf16,
                  double* pre_main, double* mag_main, double* pre_idx, double* mag_idx);
+/* (cache_dtype ORC_CACHE_FP4_G32: the main cache as FP4, the indexer cache
+ * with idx_scales [B][n_cap][Ci/32].) */
 
 /* ---- a3/a4/a5/a6: indexer scores, top-k, HSI pool, Reindex over a pool ----
  * q_idx  [B][Tq][H][Ci] bf16; head_w [B][Tq][H] fp32 or NULL (all ones)
@@ -104,13 +127,14 @@ int orc_index_topk(int B, int Tq, int H, int Ci, int r, int cache_dtype, int n_c
 /* ---- a7: sparse attention over top-k entries and the sliding window ----
  * q      [B][Tq][Hm][D] bf16 (already rotated)
  * main cache canonical, capacity n_cap; topk [B][Tq][k] (-1 = empty slot)
- * swa    [B][S][D] bf16 rows at positions swa_pos0[b] + i, i < swa_len[b] <= S
+ * swa    [B][S] rows at positions swa_pos0[b] + i, i < swa_len[b] <= S:
+ *        swa_fmt ORC_SWA_BF16: [D] bf16; ORC_SWA_MXFP8: D + D/32 bytes
  * window W: a query at t reads the rows at positions max(0, t-W+1)..t present
  * out    [B][Tq][Hm][D]; lse [B][Tq][Hm] (natural log) or NULL */
 int orc_attend(int B, int Tq, int Hm, int D, int cache_dtype, int n_cap,
                const uint8_t* main_codes, const uint8_t* main_scales, const uint16_t* main_bf16,
                const int32_t* n_entries, const uint16_t* q, const int32_t* topk, int k,
-               const uint16_t* swa, int S, const int32_t* swa_len, const int64_t* swa_pos0,
+               const void* swa, int swa_fmt, int S, const int32_t* swa_len, const int64_t* swa_pos0,
                const int64_t* q_pos, int W, double scale, double* out, double* lse);
 
 /* Dense attention over every visible entry and the window (no selection):
@@ -118,7 +142,7 @@ int orc_attend(int B, int Tq, int Hm, int D, int cache_dtype, int n_cap,
 int orc_attend_dense(int B, int Tq, int Hm, int D, int r, int cache_dtype, int n_cap,
                      const uint8_t* main_codes, const uint8_t* main_scales,
                      const uint16_t* main_bf16, const int32_t* n_entries, const uint16_t* q,
-                     const uint16_t* swa, int S, const int32_t* swa_len, const int64_t* swa_pos0,
+                     const void* swa, int swa_fmt, int S, const int32_t* swa_len, const int64_t* swa_pos0,
                      const int64_t* q_pos, int W, double scale, double* out);
 
 /* Threads the oracle's parallel loops may use (OpenMP); returns the count. */

@@ -63,8 +63,17 @@ TRAFFIC = {
 }
 
 
-def attend_query_bytes(cache, topk=512, window=128):
-    return topk * MAIN_ENTRY_BYTES[cache] + window * 1024 + 64 * 512 * 2 + 64 * 512 * 4 + topk * 4
+def attend_query_bytes(cache, topk=512, window=128, row_bytes=1024):
+    """Top-k entries + window rows (bf16 1024 B, MXFP8 528 B) + bf16 Q + fp32 out + ids."""
+    return topk * MAIN_ENTRY_BYTES[cache] + window * row_bytes + 64 * 512 * 2 + 64 * 512 * 4 + topk * 4
+
+
+def idx_entry_bytes(wl):
+    return 68 if wl.idx68 else IDX_ENTRY_BYTES[wl.cache]
+
+
+def swa_row_bytes(wl):
+    return 528 if wl.swa_fp8 else 1024
 
 
 def peaks():
@@ -135,7 +144,7 @@ def _fill_cache(c, cd, g, device):
     0x20..0x3C, or N(0,1) bf16 values (same distribution as the tests)."""
     import torch
     import compressed_sparse_attention_07_gb300 as csa
-    if cd == csa.CACHE_FP4:
+    if cd != csa.CACHE_BF16:
         c.data.random_(0, 256, generator=g)
         c.scales.random_(0x20, 0x3D, generator=g)
     else:
@@ -152,8 +161,9 @@ class StepBase:
         import compressed_sparse_attention_07_gb300 as csa
         self.torch, self.csa, self.wl, self.device = torch, csa, wl, device
         self.cd = csa.CACHE_FP4 if wl.cache == "fp4" else csa.CACHE_BF16
+        fmt = (csa.FMT_IDX_68B if wl.idx68 else 0) | (csa.FMT_SWA_FP8 if wl.swa_fp8 else 0)
         self.cfg = csa.Cfg(ratio=wl.ratio, cache_dtype=self.cd, topk=wl.topk, window=wl.window,
-                           hsi_blocks=wl.hsi_blocks if wl.hsi else 0, rope_theta=wl.theta)
+                           hsi_blocks=wl.hsi_blocks if wl.hsi else 0, rope_theta=wl.theta, formats=fmt)
         self.seed = wl.seed + seed_offset
         self.B = wl.batch
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -162,9 +172,9 @@ class StepBase:
         g = self.torch.Generator(device=self.device)
         g.manual_seed(self.seed)
         self.main = self.csa.PagedCache(self.B, capacity, 512, self.cd, device=self.device)
-        self.idx = self.csa.PagedCache(self.B, capacity, 128, self.cd, device=self.device)
+        self.idx = self.csa.PagedCache(self.B, capacity, 128, self.cfg.idx_dtype, device=self.device)
         for c in (self.main, self.idx):
-            _fill_cache(c, self.cd, g, self.device)
+            _fill_cache(c, c.cache_dtype, g, self.device)
 
     def upload(self):
         self.d = {k: _dev(v, self.device) for k, v in self.h.items()}
@@ -189,7 +199,9 @@ class StepBase:
 class DecodeStep(StepBase):
     """One decode step of one CSA2 layer in Full mode: compress the step's r
     new tokens per sequence (one entry), index the whole visible cache (plus
-    the HSI pool on the decoder Full layer), attend over top-k and window."""
+    the HSI pool on the decoder Full layer), attend over top-k and window.
+    With FP8 window rows the step also encodes its newest window row into
+    the resident MXFP8 window (the older rows were encoded by earlier steps)."""
 
     def __init__(self, wl, device, seed_offset=0):
         super().__init__(wl, device, seed_offset)
@@ -207,6 +219,15 @@ class DecodeStep(StepBase):
             "swa_pos0": np.full(B, ctx - wl.window, np.int64),
             "q_pos": np.full((B, 1), ctx - 1, np.int64),
         }
+        if wl.swa_fp8:
+            # resident MXFP8 window: rows ctx-W .. ctx-2 encoded once here; the
+            # step's input is the newest bf16 row, encoded into row W-1
+            older = self.h.pop("swa")
+            self.h["swa_new"] = np.ascontiguousarray(older[:, -1:])
+            self.swa8 = torch.zeros((B, wl.window, csa.SWA_FP8_ROW), dtype=torch.uint8, device=device)
+            csa.swa_encode(_dev(older[:, :-1], device), torch.zeros(B, dtype=torch.int64, device=device), self.swa8,
+                           status=self.status)
+            self.swa_row0 = torch.full((B,), wl.window - 1, dtype=torch.int64, device=device)
         self.upload()
         self.merge_w = _dev(synth.merge_weights(synth.rng(s, "w"), r, 512), device)
         self.w_idx = _dev(synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512)), device)
@@ -217,25 +238,34 @@ class DecodeStep(StepBase):
         self.out = torch.empty((B, 1, 64, 512), dtype=torch.float32, device=device)
         self.stages = ["compress", "index_topk", "attend"]
         self.launches_per_step = 4  # compress, score, select, attend
-        eb = IDX_ENTRY_BYTES[wl.cache]
-        self.stage_bytes = {"compress": B * (r * 1024 + (288 + 72 if wl.cache == "fp4" else 1280)),
+        eb = idx_entry_bytes(wl)
+        self.stage_bytes = {"compress": B * (r * 1024 + (288 + eb if wl.cache == "fp4" else 1280)),
                             "index_topk": B * self.N * eb,
-                            "attend": B * attend_query_bytes(wl.cache, wl.topk, wl.window)}
+                            "attend": B * attend_query_bytes(wl.cache, wl.topk, wl.window, swa_row_bytes(wl))}
         self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_tc_kernel + select_kernel",
                               "attend": "attend_rows_kernel"}
+        if wl.swa_fp8:
+            self.stages.insert(1, "swa_encode")
+            self.launches_per_step += 1
+            self.stage_bytes["swa_encode"] = B * (1024 + 528)
+            self.stage_kernels["swa_encode"] = "swa_encode_kernel"
         self.units = B
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N}
 
     def calls(self, d):
         csa, st = self.csa, self.status
-        return [
+        c = [
             lambda: csa.compress(self.cfg, d["x"], d["pos0"], self.merge_w, self.w_idx, self.main, self.idx,
                                  self.n_entries, status=st),
             lambda: csa.index_topk(self.cfg, d["q_idx"], d["q_pos"], self.idx, self.n_entries, self.N, self.topk,
                                    self.ws, pool_out=self.pool, status=st),
-            lambda: csa.attend(self.cfg, d["q"], self.main, self.n_entries, self.topk, d["swa"], d["swa_len"],
-                               d["swa_pos0"], d["q_pos"], self.out, status=st),
+            lambda: csa.attend(self.cfg, d["q"], self.main, self.n_entries, self.topk,
+                               self.swa8 if self.wl.swa_fp8 else d["swa"], d["swa_len"], d["swa_pos0"], d["q_pos"],
+                               self.out, status=st),
         ]
+        if self.wl.swa_fp8:
+            c.insert(1, lambda: csa.swa_encode(d["swa_new"], self.swa_row0, self.swa8, status=st))
+        return c
 
 
 class PrefillStep(StepBase):
@@ -386,12 +416,12 @@ class OracleStep:
         N = (wl.ctx + wl.tq) // r if self.prefill else wl.ctx // r
         self.N = N
         self.main = oracle.Cache(B, N, 512, wl.cache)
-        self.idx = oracle.Cache(B, N, 128, wl.cache)
+        self.idx = oracle.Cache(B, N, 128, "fp4g32" if wl.idx68 else wl.cache)
         g = synth.rng(wl.seed, "oracle_cache")
         for c in (self.main, self.idx):
-            if wl.cache == "fp4":
+            if c.dtype != "bf16":
                 for b in range(B):
-                    c.codes[b], c.scales[b] = synth.fp4_bytes(g, N, c.channels)
+                    c.codes[b], c.scales[b] = synth.fp4_bytes(g, N, c.channels, group=32 if c.dtype == "fp4g32" else 16)
             else:
                 c.bf16[:] = synth.normal_bf16(g, c.bf16.shape)
         s, ctx = wl.seed, wl.ctx
@@ -433,6 +463,9 @@ class OracleStep:
                 self.q = synth.normal_bf16(synth.rng(s, "q"), (B, 1, 64, 512))
                 self.q_idx = synth.normal_bf16(synth.rng(s, "q_idx"), (B, 1, 32, 128))
                 self.swa = synth.normal_bf16(synth.rng(s, "swa"), (B, wl.window, 512))
+                if wl.swa_fp8:  # resident MXFP8 window; the step encodes the newest row
+                    self.swa_new = np.ascontiguousarray(self.swa[:, -1:])
+                    self.swa = oracle.swa_encode(self.swa)
                 self.units = B
                 self.sample = "%d sequences of the step (compress + index over %d entries + attend)" % (B, N)
         self.cores = min(oracle.threads(), max(self.units, 1))
@@ -441,6 +474,8 @@ class OracleStep:
         o, wl = self.oracle, self.wl
         sc = 1 / math.sqrt(512)
         o.compress(self.x, self.pos0, self.w, self.w_idx, self.main, self.idx, wl.ratio, wl.theta)
+        if wl.swa_fp8:
+            self.swa[:, -1:] = o.swa_encode(self.swa_new)
         if self.prefill or not wl.layers:
             topk, _, _ = o.index_topk(self.idx, self.n_ent, self.q_idx, self.q_pos, wl.ratio, wl.topk,
                                       hsi_blocks=wl.hsi_blocks if wl.hsi else 0, want_pool=wl.hsi)

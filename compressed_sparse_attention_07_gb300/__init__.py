@@ -18,10 +18,13 @@ from . import build as _build
 __all__ = [
     "Cfg", "PagedCache", "GroupState", "load", "compress", "index_workspace_bytes", "index_topk", "attend",
     "gather_dequant", "layer", "status_string", "CsaError", "CACHE_FP4", "CACHE_BF16", "MODE_FULL",
-    "MODE_REINDEX", "MODE_REUSE", "PAGE", "library_path", "capture",
+    "MODE_REINDEX", "MODE_REUSE", "PAGE", "library_path", "capture", "swa_encode", "CACHE_FP4_S32",
+    "FMT_IDX_68B", "FMT_SWA_FP8", "SWA_FP8_ROW",
 ]
 
-CACHE_FP4, CACHE_BF16 = 0, 1
+CACHE_FP4, CACHE_BF16, CACHE_FP4_S32 = 0, 1, 2
+FMT_IDX_68B, FMT_SWA_FP8 = 1, 2
+SWA_FP8_ROW = 528  # bytes of one MXFP8 window row
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 PAGE = 64
 
@@ -34,14 +37,22 @@ class CsaError(RuntimeError):
 
 class Cfg(C.Structure):
     """csa2_cfg: defaults are the model's sizes (64 x 512 latent, 64 RoPE
-    dims, indexer 32 x 128, top-512, window 128, HSI 2048 x 8)."""
+    dims, indexer 32 x 128, top-512, window 128, HSI 2048 x 8); `formats`
+    takes FMT_IDX_68B (indexer entries with one scale per 32 channels) and
+    FMT_SWA_FP8 (MXFP8 window rows)."""
     _fields_ = [("dim", C.c_int32), ("rope_dims", C.c_int32), ("n_heads", C.c_int32), ("idx_heads", C.c_int32),
                 ("idx_dim", C.c_int32), ("topk", C.c_int32), ("window", C.c_int32), ("ratio", C.c_int32),
                 ("hsi_blocks", C.c_int32), ("hsi_block", C.c_int32), ("cache_dtype", C.c_int32),
-                ("reserved", C.c_int32), ("rope_theta", C.c_double)]
+                ("formats", C.c_int32), ("rope_theta", C.c_double)]
 
-    def __init__(self, ratio=2, cache_dtype=CACHE_FP4, topk=512, window=128, hsi_blocks=0, rope_theta=1e4):
-        super().__init__(512, 64, 64, 32, 128, topk, window, ratio, hsi_blocks, 8, cache_dtype, 0, rope_theta)
+    def __init__(self, ratio=2, cache_dtype=CACHE_FP4, topk=512, window=128, hsi_blocks=0, rope_theta=1e4,
+                 formats=0):
+        super().__init__(512, 64, 64, 32, 128, topk, window, ratio, hsi_blocks, 8, cache_dtype, formats, rope_theta)
+
+    @property
+    def idx_dtype(self) -> int:
+        """Format of the indexer cache under this configuration."""
+        return CACHE_FP4_S32 if (self.cache_dtype == CACHE_FP4 and self.formats & FMT_IDX_68B) else self.cache_dtype
 
 
 class _CacheDesc(C.Structure):
@@ -96,6 +107,8 @@ def load():
         L.csa2_gather_dequant.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
         L.csa2_layer.restype = i32
         L.csa2_layer.argtypes = [vp, i32, vp, vp, vp]
+        L.csa2_swa_encode.restype = i32
+        L.csa2_swa_encode.argtypes = [i32, i32, vp, vp, vp, i32, vp, vp]
         _lib = L
         return L
 
@@ -192,16 +205,36 @@ def index_topk(cfg: Cfg, q_idx, q_pos, idx: PagedCache, n_entries, max_entries: 
         workspace.numel() * workspace.element_size(), _ptr(status, torch.int32, "status"), _stream(stream)))
 
 
+def _swa(cfg: Cfg, swa):
+    """Window rows: bf16 [B][S][512], or uint8 MXFP8 rows [B][S][528] under FMT_SWA_FP8."""
+    if swa is None:
+        return None
+    if cfg.formats & FMT_SWA_FP8:
+        if swa.shape[-1] != SWA_FP8_ROW:
+            raise ValueError("MXFP8 window rows must be [B][S][%d] uint8" % SWA_FP8_ROW)
+        return _ptr(swa, torch.uint8, "swa")
+    return _bf16(swa, "swa")
+
+
+def swa_encode(x, row0, rows, status=None, stream=None):
+    """FP8 window rows: x [B][T][512] bf16 -> rows[b][row0[b] + i] of rows [B][S][528] uint8 (MXFP8)."""
+    B, T = x.shape[:2]
+    _check("csa2_swa_encode", load().csa2_swa_encode(
+        B, T, _bf16(x, "x"), _ptr(row0, torch.int64, "row0"), _ptr(rows, torch.uint8, "rows"), rows.shape[1],
+        _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
 def attend(cfg: Cfg, q, main: PagedCache, n_entries, topk, swa, swa_len, swa_pos0, q_pos, out, lse=None,
            scale=None, status=None, stream=None):
-    """a7: q [B][Tq][64][512] bf16, topk [B][Tq][k], swa [B][S][512] bf16 -> out [B][Tq][64][512] fp32."""
+    """a7: q [B][Tq][64][512] bf16, topk [B][Tq][k], swa [B][S][512] bf16 (or [B][S][528] uint8 MXFP8 rows
+    under FMT_SWA_FP8) -> out [B][Tq][64][512] fp32."""
     B, Tq = q.shape[:2]
     S = swa.shape[1] if swa is not None else 0
     d = main.desc()
     scale = 1.0 / math.sqrt(512) if scale is None else float(scale)
     _check("csa2_attend", load().csa2_attend(
         C.byref(cfg), B, Tq, _bf16(q, "q"), C.byref(d), _ptr(n_entries, torch.int32, "n_entries"),
-        _ptr(topk, torch.int32, "topk"), _bf16(swa, "swa"), S, _ptr(swa_len, torch.int32, "swa_len"),
+        _ptr(topk, torch.int32, "topk"), _swa(cfg, swa), S, _ptr(swa_len, torch.int32, "swa_len"),
         _ptr(swa_pos0, torch.int64, "swa_pos0"), _ptr(q_pos, torch.int64, "q_pos"), scale,
         _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(status, torch.int32, "status"),
         _stream(stream)))
@@ -236,7 +269,7 @@ def layer(cfg: Cfg, mode: int, state: GroupState, q_pos, q, swa, swa_len, swa_po
     B, Tq = q.shape[:2]
     io = _LayerIO(B, Tq, _ptr(q_pos, torch.int64, "q_pos"), x.shape[1] if x is not None else 0, _bf16(x, "x"),
                   _ptr(pos0, torch.int64, "pos0"), _ptr(merge_w, torch.float32, "merge_w"), _bf16(w_idx, "w_idx"),
-                  _bf16(q_idx, "q_idx"), _ptr(head_w, torch.float32, "head_w"), _bf16(q, "q"), _bf16(swa, "swa"),
+                  _bf16(q_idx, "q_idx"), _ptr(head_w, torch.float32, "head_w"), _bf16(q, "q"), _swa(cfg, swa),
                   swa.shape[1] if swa is not None else 0, _ptr(swa_len, torch.int32, "swa_len"),
                   _ptr(swa_pos0, torch.int64, "swa_pos0"), 1.0 / math.sqrt(512) if scale is None else float(scale),
                   _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"))

@@ -11,7 +11,9 @@ namespace {
 
 bool cfg_supported(const csa2_cfg* c, int32_t* err) {
   if (!c) { *err = CSA2_ERR_INVALID_ARG; return false; }
-  if (c->reserved != 0 || !(c->rope_theta > 0.0) || (c->cache_dtype != CSA2_CACHE_FP4 && c->cache_dtype != CSA2_CACHE_BF16)) {
+  if ((c->formats & ~(CSA2_FMT_IDX_68B | CSA2_FMT_SWA_FP8)) != 0 || !(c->rope_theta > 0.0) ||
+      (c->cache_dtype != CSA2_CACHE_FP4 && c->cache_dtype != CSA2_CACHE_BF16) ||
+      ((c->formats & CSA2_FMT_IDX_68B) && c->cache_dtype != CSA2_CACHE_FP4)) {
     *err = CSA2_ERR_INVALID_ARG;
     return false;
   }
@@ -27,7 +29,7 @@ bool cfg_supported(const csa2_cfg* c, int32_t* err) {
 bool cache_ok(const csa2_cache* c, int channels, int dtype) {
   if (!c || !c->data || !c->block_table || c->max_pages <= 0 || c->num_pages <= 0 || c->reserved != 0) return false;
   if (c->channels != channels) return false;
-  if (dtype == CSA2_CACHE_FP4 && !c->scales) return false;
+  if (dtype != CSA2_CACHE_BF16 && !c->scales) return false;
   // 16-byte alignment of the page bases (128-bit loads)
   if ((reinterpret_cast<uintptr_t>(c->data) & 15) || (c->scales && (reinterpret_cast<uintptr_t>(c->scales) & 15)))
     return false;
@@ -57,6 +59,8 @@ extern "C" {
 size_t csa2_page_bytes(int32_t channels, int32_t cache_dtype, int32_t which) {
   if (channels <= 0 || channels % 16) return 0;
   if (cache_dtype == CSA2_CACHE_FP4) return which == 0 ? (size_t)kPage * channels / 2 : (size_t)kPage * channels / 16;
+  if (cache_dtype == CSA2_CACHE_FP4_S32)
+    return channels % 32 ? 0 : which == 0 ? (size_t)kPage * channels / 2 : (size_t)kPage * channels / 32;
   if (cache_dtype == CSA2_CACHE_BF16) return which == 0 ? (size_t)kPage * channels * 2 : 0;
   return 0;
 }
@@ -83,7 +87,7 @@ int32_t csa2_compress(const csa2_cfg* cfg, int32_t B, int32_t T, const uint16_t*
   if (B < 0 || T < 0 || T % cfg->ratio) return CSA2_ERR_INVALID_ARG;
   if (B == 0 || T == 0) return CSA2_OK;
   if (!x || !pos0 || !merge_w || !w_idx || !n_entries || !aligned(x, 4)) return CSA2_ERR_INVALID_ARG;
-  if (!cache_ok(main_cache, kDim, cfg->cache_dtype) || !cache_ok(idx_cache, kIdxDim, cfg->cache_dtype))
+  if (!cache_ok(main_cache, kDim, cfg->cache_dtype) || !cache_ok(idx_cache, kIdxDim, idx_dtype(*cfg)))
     return CSA2_ERR_INVALID_ARG;
   return cuda_status(launch_compress(*cfg, B, T, x, pos0, merge_w, w_idx, *main_cache, *idx_cache, n_entries, status,
                                      static_cast<cudaStream_t>(stream)));
@@ -104,7 +108,7 @@ int32_t csa2_index_topk(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16
   if (B < 0 || Tq < 0 || max_entries < 0) return CSA2_ERR_INVALID_ARG;
   if (B == 0 || Tq == 0) return CSA2_OK;
   if (!q_idx || !q_pos || !n_entries || !topk_out || !workspace) return CSA2_ERR_INVALID_ARG;
-  if (!cache_ok(idx_cache, kIdxDim, cfg->cache_dtype)) return CSA2_ERR_INVALID_ARG;
+  if (!cache_ok(idx_cache, kIdxDim, idx_dtype(*cfg))) return CSA2_ERR_INVALID_ARG;
   if ((int64_t)max_entries > (int64_t)idx_cache->max_pages * kPage) return CSA2_ERR_CAPACITY;
   if (pool && pool_out) return CSA2_ERR_INVALID_ARG;
   if ((pool || pool_out) && cfg->hsi_blocks <= 0) return CSA2_ERR_INVALID_ARG;
@@ -116,7 +120,7 @@ int32_t csa2_index_topk(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16
 }
 
 int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q, const csa2_cache* main_cache,
-                    const int32_t* n_entries, const int32_t* topk, const uint16_t* swa, int32_t S,
+                    const int32_t* n_entries, const int32_t* topk, const void* swa, int32_t S,
                     const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos, float scale, float* out,
                     float* lse, int32_t* status, void* stream) {
   int32_t err;
@@ -127,6 +131,7 @@ int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* 
   if (cfg->window > 0 && (!swa || !swa_len || !swa_pos0 || S == 0 || !aligned(swa, 16))) return CSA2_ERR_INVALID_ARG;
   if (!cache_ok(main_cache, kDim, cfg->cache_dtype)) return CSA2_ERR_INVALID_ARG;
   if (!(scale == scale)) return CSA2_ERR_INVALID_ARG;
+  if ((cfg->formats & CSA2_FMT_SWA_FP8) && !attend_rows_path(cfg->topk, cfg->window)) return CSA2_ERR_UNSUPPORTED;
   return cuda_status(launch_attend(*cfg, B, Tq, q, *main_cache, n_entries, topk, swa, S, swa_len, swa_pos0, q_pos,
                                    scale, out, lse, status, static_cast<cudaStream_t>(stream)));
 }
@@ -134,12 +139,22 @@ int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* 
 int32_t csa2_gather_dequant(const csa2_cache* cache, int32_t cache_dtype, int32_t B, int32_t n, const int32_t* ids,
                             float* out, int32_t* status, void* stream) {
   if (!cache || (cache->channels != kDim && cache->channels != kIdxDim)) return CSA2_ERR_INVALID_ARG;
-  if (cache_dtype != CSA2_CACHE_FP4 && cache_dtype != CSA2_CACHE_BF16) return CSA2_ERR_INVALID_ARG;
+  if (cache_dtype != CSA2_CACHE_FP4 && cache_dtype != CSA2_CACHE_BF16 && cache_dtype != CSA2_CACHE_FP4_S32)
+    return CSA2_ERR_INVALID_ARG;
+  if (cache_dtype == CSA2_CACHE_FP4_S32 && cache->channels != kIdxDim) return CSA2_ERR_INVALID_ARG;
   if (!cache_ok(cache, cache->channels, cache_dtype)) return CSA2_ERR_INVALID_ARG;
   if (B < 0 || n < 0) return CSA2_ERR_INVALID_ARG;
   if (B == 0 || n == 0) return CSA2_OK;
   if (!ids || !out) return CSA2_ERR_INVALID_ARG;
   return cuda_status(launch_gather_dequant(*cache, cache_dtype, B, n, ids, out, status, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t csa2_swa_encode(int32_t B, int32_t T, const uint16_t* x, const int64_t* row0, void* rows, int32_t S,
+                        int32_t* status, void* stream) {
+  if (B < 0 || T < 0 || S < 0) return CSA2_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return CSA2_OK;
+  if (!x || !row0 || !rows || !aligned(x, 16) || !aligned(rows, 16) || T > S) return CSA2_ERR_INVALID_ARG;
+  return cuda_status(launch_swa_encode(B, T, x, row0, rows, S, status, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t csa2_layer(const csa2_cfg* cfg, int32_t mode, csa2_group_state* st, const csa2_layer_io* io, void* stream) {

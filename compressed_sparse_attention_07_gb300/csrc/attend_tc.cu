@@ -48,7 +48,8 @@ struct AttArgs {
   const int32_t* n_entries;
   int64_t capacity;
   const int32_t* topk;
-  const uint16_t* swa;
+  const uint16_t* swa;   // bf16 window rows [B][S][512], or
+  const uint8_t* swa8;   // MXFP8 window rows [B][S][528 B] (row-tile kernel only)
   const int32_t* swa_len;
   const int64_t* swa_pos0;
   const int64_t* q_pos;
@@ -76,6 +77,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return f16x2_from_f32(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+
 __device__ __forceinline__ uint32_t f16x2_scale(uint32_t sbyte) {
   uint32_t r;
   uint16_t pair = (uint16_t)(sbyte | (sbyte << 8));
@@ -95,6 +97,35 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
+}
+
+// 16 MXFP8 elements (E4M3, element 2i in the low byte of pair i) with E8M0
+// scale byte `sb` -> 8 f16x2, each the f16 nearest to E4M3 x 2^(sb - 127):
+// the E4M3 -> f16 step is exact; the scale is applied by one f16 multiply
+// when 2^(sb - 127) is an f16 value, else in fp32 (exact) and rounded once.
+__device__ __forceinline__ void mxfp8x16_to_f16x2(uint4 w, uint32_t sb, uint32_t (&o)[8]) {
+  const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint16_t lo = (uint16_t)(wv[i] & 0xFFFFu), hi = (uint16_t)(wv[i] >> 16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * i]) : "h"(lo));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[2 * i + 1]) : "h"(hi));
+  }
+  const int e = (int)sb - 127;
+  if (e >= -24 && e <= 15) {
+    const uint32_t sh = e >= -14 ? (uint32_t)(e + 15) << 10 : 1u << (e + 24);
+    const uint32_t s2 = sh | (sh << 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = hmul2(h[i], s2);
+  } else {
+    const float sf = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << 22);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+      o[i] = f16x2_from_f32(f.x * sf, f.y * sf);
+    }
+  }
 }
 
 // Row source of slot i (tiles padded to 128), page already resolved:
@@ -758,7 +789,7 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16]) {
   return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
 }
 
-template <int kDtype>
+template <int kDtype, bool kSwaFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_rows_kernel(AttArgs a) {
   griddep_wait();  // before any global read or tensor-memory allocation
@@ -787,6 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // and the merge see the rows as a set
   const int slot0 = 8 * (warp * n + t);
   const bool fp4_tile = kMainFp4 && slot0 < a.tiles_main * 128;
+  const bool fp8_win = kSwaFp8 && slot0 >= a.tiles_main * 128;  // an 8-row group of MXFP8 window rows
 
   // ---- loads, coalesced: warp w fills the 8-row group w of C (and half of
   // the 8-head group w % 8 of Q); lane l takes row 8w + l % 8 and 16-byte
@@ -821,9 +853,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 16; ++k) raw[k] = __ldg(g + 4 * k + uq);
     }
   } else if (sidx_l <= -2) {
-    const uint4* g = reinterpret_cast<const uint4*>(a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx_l)) * kDim);
+    if (kSwaFp8) {  // 32 units of 16 elements, lane units 4k + l/8; then the 16 scale bytes
+      const uint4* g =
+          reinterpret_cast<const uint4*>(a.swa8 + ((int64_t)b * a.S + (-2 - (int64_t)sidx_l)) * kSwaFp8Row);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) raw[k] = __ldg(g + 4 * k + uq);
+      for (int k = 0; k < 8; ++k) raw[k] = __ldg(g + 4 * k + uq);
+      raw[8] = __ldg(g + 32);
+    } else {
+      const uint4* g = reinterpret_cast<const uint4*>(a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx_l)) * kDim);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) raw[k] = __ldg(g + 4 * k + uq);
+    }
   }
   if (uq == 0) srcs[rho] = sidx_l;
   if (tid == 0) {
@@ -861,6 +901,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 32 * q + 8 * i, kDim)) = o;
       }
+    }
+  } else if (fp8_win) {
+    // MXFP8 unit u = 4k + l/8: channels 16u..16u+15, scale byte u/2
+    const uint32_t sw[4] = {raw[8].x, raw[8].y, raw[8].z, raw[8].w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int u = 4 * k + uq, blk = u >> 1;
+      uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (sidx_l != -1) mxfp8x16_to_f16x2(raw[k], (sw[blk >> 2] >> (8 * (blk & 3))) & 0xFFu, o);
+      *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 16 * u, kDim)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 16 * u + 8, kDim)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
   } else {
 #pragma unroll
@@ -1027,10 +1078,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
-template <int kDtype>
+template <int kDtype, bool kSwaFp8>
 cudaError_t launch_rows(const AttArgs& a, int Q, cudaStream_t stream) {
   const int n_tiles = a.tiles_main + a.tiles_win;
-  auto kern = attend_rows_kernel<kDtype>;
+  auto kern = attend_rows_kernel<kDtype, kSwaFp8>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRowSmem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_tiles, Q);
@@ -1045,6 +1096,7 @@ cudaError_t launch_rows(const AttArgs& a, int Q, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // whether this cluster shape can be scheduled at all, asked once per shape
+  // (per instantiation: the function-local table is one per template)
   static int schedulable[kRowMaxTiles + 1] = {};  // 0 unknown, 1 yes, -1 no
   if (schedulable[n_tiles] == 0) {
     int clusters = 0;
@@ -1104,28 +1156,37 @@ cudaError_t launch_dtype(const AttArgs& a, int Q, int num_sms, cudaStream_t stre
 
 }  // namespace
 
+bool attend_rows_path(int topk, int window) { return (topk + 127) / 128 + (window + 127) / 128 <= kRowMaxTiles; }
+
 bool attend_tc_supported(int topk, int window) {
   const int nt = (topk + 127) / 128 + (window + 127) / 128;
   return nt * 16 <= 512 && att_smem<CSA2_CACHE_FP4, 16>(nt) <= kSmemLimit;
 }
 
 cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q, const csa2_cache& main_c,
-                          const int32_t* n_entries, const int32_t* topk, const uint16_t* swa, int S,
+                          const int32_t* n_entries, const int32_t* topk, const void* swa, int S,
                           const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos,
                           float scale, float* out, float* lse, int32_t* status, cudaStream_t stream) {
   const int Q = B * Tq;
   if (Q == 0) return cudaSuccess;
+  const bool fp8 = (cfg.formats & CSA2_FMT_SWA_FP8) != 0;
   AttArgs a{Tq, cfg.topk, cfg.window, S, (cfg.topk + 127) / 128, (cfg.window + 127) / 128, q, view_of(main_c),
-            n_entries, (int64_t)main_c.max_pages * kPage, topk, swa, swa_len, swa_pos0, q_pos, scale, out, lse,
-            status};
+            n_entries, (int64_t)main_c.max_pages * kPage, topk,
+            fp8 ? nullptr : static_cast<const uint16_t*>(swa), fp8 ? static_cast<const uint8_t*>(swa) : nullptr,
+            swa_len, swa_pos0, q_pos, scale, out, lse, status};
   // up to six row tiles: one CTA per (query, tile) for every head, the
-  // query's tiles in one cluster; more: split by head groups
+  // query's tiles in one cluster; more: split by head groups (bf16 window
+  // rows only)
   const int n_tiles = a.tiles_main + a.tiles_win;
   if (n_tiles <= kRowMaxTiles) {
-    cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_rows<CSA2_CACHE_FP4>(a, Q, stream)
-                                                      : launch_rows<CSA2_CACHE_BF16>(a, Q, stream);
-    if (e != cudaErrorNotSupported) return e;
+    cudaError_t e;
+    if (cfg.cache_dtype == CSA2_CACHE_FP4)
+      e = fp8 ? launch_rows<CSA2_CACHE_FP4, true>(a, Q, stream) : launch_rows<CSA2_CACHE_FP4, false>(a, Q, stream);
+    else
+      e = fp8 ? launch_rows<CSA2_CACHE_BF16, true>(a, Q, stream) : launch_rows<CSA2_CACHE_BF16, false>(a, Q, stream);
+    if (e != cudaErrorNotSupported || fp8) return e;
   }
+  if (fp8) return cudaErrorNotSupported;
   if ((int64_t)Q * 4 * n_tiles <= 8 * (int64_t)num_sms() && n_tiles <= 16) {
     cudaError_t e = cfg.cache_dtype == CSA2_CACHE_FP4 ? launch_split<CSA2_CACHE_FP4>(a, Q, stream)
                                                       : launch_split<CSA2_CACHE_BF16>(a, Q, stream);

@@ -1,6 +1,8 @@
 // a1 -- CSA2 compressor: merge r tokens per entry with per-channel weights,
 // RoPE at the entry's last covered position, encode into the paged main
-// cache, project the stored entry to indexer K and encode that too.
+// cache, project the stored entry to indexer K and encode that too (FP4
+// with one E4M3 scale per 16 channels, or per 32 for the 68-byte indexer
+// entry of hn.213312.xyz sec. 3.1).
 // (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.3.1 and sec. 2.4.4; 36kr "CSA2",
 // "FP4 and Bounded Replay".)  One CTA per new entry; this step moves a few KB
 // per entry, so it is latency-bound and kept simple.
@@ -16,7 +18,7 @@ struct RopeFreqs {
   double f[kRope / 2];
 };
 
-template <int kDtype>
+template <int kDtype, bool kIdxS32>
 __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs rf, const uint16_t* __restrict__ x,
                                                        const int64_t* __restrict__ pos0,
                                                        const float* __restrict__ merge_w,
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
     if (kDtype == CSA2_CACHE_FP4) {
       float amax = fabsf(kv);
 #pragma unroll
-      for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      for (int o = 1; o < (kIdxS32 ? 32 : 16); o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       int sc = e4m3_scale_code(amax);
       uint32_t code = e2m1_code(kv, e4m3_pos(sc));
       uint32_t hi = __shfl_xor_sync(0xffffffffu, code, 1);
@@ -123,7 +125,11 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
         int bi = t >> 1;  // byte index 0..63 -> 16-byte chunk bi/16
         ic.data[ipage * kIdxFp4Data + ((bi >> 4) * kPage + slot) * 16 + (bi & 15)] = (uint8_t)(code | (hi << 4));
       }
-      if (ipage >= 0 && (t & 15) == 0) ic.scales[ipage * kIdxFp4Scales + slot * (kIdxDim / 16) + (t >> 4)] = (uint8_t)sc;
+      if (kIdxS32) {
+        if (ipage >= 0 && (t & 31) == 0) ic.scales[ipage * kIdxS32Scales + slot * (kIdxDim / 32) + (t >> 5)] = (uint8_t)sc;
+      } else if (ipage >= 0 && (t & 15) == 0) {
+        ic.scales[ipage * kIdxFp4Scales + slot * (kIdxDim / 16) + (t >> 4)] = (uint8_t)sc;
+      }
     } else {
       uint16_t h = __bfloat16_as_ushort(__float2bfloat16_rn(kv));
       if (ipage >= 0) {
@@ -147,10 +153,13 @@ cudaError_t launch_compress(const csa2_cfg& cfg, int B, int T, const uint16_t* x
   dim3 grid(M, B);
   RopeFreqs rf;
   for (int i = 0; i < kRope / 2; ++i) rf.f[i] = std::pow(cfg.rope_theta, -2.0 * i / kRope);
+  if (idx_dtype(cfg) == CSA2_CACHE_FP4_S32)
+    return launch_k(compress_kernel<CSA2_CACHE_FP4, true>, grid, dim3(256), 0, stream, 0, T, cfg.ratio, rf, x, pos0,
+                    merge_w, w_idx, view_of(main_c), view_of(idx_c), n_entries, status);
   if (cfg.cache_dtype == CSA2_CACHE_FP4)
-    return launch_k(compress_kernel<CSA2_CACHE_FP4>, grid, dim3(256), 0, stream, 0, T, cfg.ratio, rf, x, pos0, merge_w,
-                    w_idx, view_of(main_c), view_of(idx_c), n_entries, status);
-  return launch_k(compress_kernel<CSA2_CACHE_BF16>, grid, dim3(256), 0, stream, 0, T, cfg.ratio, rf, x, pos0, merge_w,
+    return launch_k(compress_kernel<CSA2_CACHE_FP4, false>, grid, dim3(256), 0, stream, 0, T, cfg.ratio, rf, x, pos0,
+                    merge_w, w_idx, view_of(main_c), view_of(idx_c), n_entries, status);
+  return launch_k(compress_kernel<CSA2_CACHE_BF16, false>, grid, dim3(256), 0, stream, 0, T, cfg.ratio, rf, x, pos0, merge_w,
                   w_idx, view_of(main_c), view_of(idx_c), n_entries, status);
 }
 

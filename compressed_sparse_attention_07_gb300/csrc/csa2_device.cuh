@@ -24,8 +24,10 @@ constexpr int kMainFp4Data = kPage * kDim / 2;      // 16384
 constexpr int kMainFp4Scales = kPage * kDim / 16;   // 2048
 constexpr int kIdxFp4Data = kPage * kIdxDim / 2;    // 4096
 constexpr int kIdxFp4Scales = kPage * kIdxDim / 16; // 512
+constexpr int kIdxS32Scales = kPage * kIdxDim / 32; // 256 (68-byte indexer entries)
 constexpr int kMainBf16Data = kPage * kDim * 2;     // 65536
 constexpr int kIdxBf16Data = kPage * kIdxDim * 2;   // 16384
+constexpr int kSwaFp8Row = kDim + kDim / 32;        // 528: MXFP8 window row (elements + E8M0 scales)
 
 struct CacheView {
   uint8_t* data;

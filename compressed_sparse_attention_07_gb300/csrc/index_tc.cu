@@ -34,7 +34,7 @@ namespace {
 // and epilogue), two otherwise (TMEM and shared-memory budget).
 template <int kDtype, int QPC>
 struct Shape {
-  static constexpr int kWG = (QPC == 1 && kDtype == CSA2_CACHE_FP4) ? 4 : 2;
+  static constexpr int kWG = (QPC == 1 && kDtype != CSA2_CACHE_BF16) ? 4 : 2;
   static constexpr int kConsumers = 128 * kWG;
   static constexpr int kThreads = kConsumers + 32;  // + one producer warp (page mode)
   static constexpr int kStages = 2 * kWG;           // ring slots; warpgroup g owns slots g, g + kWG
@@ -45,8 +45,9 @@ constexpr int kMaxGatherTiles = 32;        // gather mode: resolved positions he
 
 template <int kDtype>
 struct TileFmt {
-  static constexpr int kPageData = (kDtype == CSA2_CACHE_FP4) ? kIdxFp4Data : kIdxBf16Data;
-  static constexpr int kPageScales = (kDtype == CSA2_CACHE_FP4) ? kIdxFp4Scales : 0;
+  static constexpr int kPageData = (kDtype == CSA2_CACHE_BF16) ? kIdxBf16Data : kIdxFp4Data;
+  static constexpr int kPageScales = (kDtype == CSA2_CACHE_FP4) ? kIdxFp4Scales
+                                     : (kDtype == CSA2_CACHE_FP4_S32) ? kIdxS32Scales : 0;
   static constexpr int kSlotBytes = 2 * (kPageData + kPageScales);
 };
 
@@ -94,6 +95,9 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp8(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
@@ -326,11 +330,14 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
       if (e >= 0) {
         const int64_t page = e / kPage;
         const int es = e % kPage;
-        if (kDtype == CSA2_CACHE_FP4) {
+        if (kDtype != CSA2_CACHE_BF16) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             cp16(slot + h * kIdxFp4Data + (c * kPage + sl) * 16, a.ic.data + page * kIdxFp4Data + (c * kPage + es) * 16);
-          cp8(slot + 2 * kIdxFp4Data + h * kIdxFp4Scales + sl * 8, a.ic.scales + page * kIdxFp4Scales + es * 8);
+          if (kDtype == CSA2_CACHE_FP4)
+            cp8(slot + 2 * kIdxFp4Data + h * kIdxFp4Scales + sl * 8, a.ic.scales + page * kIdxFp4Scales + es * 8);
+          else
+            cp4(slot + 2 * kIdxFp4Data + h * kIdxS32Scales + sl * 4, a.ic.scales + page * kIdxS32Scales + es * 4);
         } else {
 #pragma unroll
           for (int c = 0; c < 16; ++c)
@@ -401,12 +408,17 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
       }
       const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
       const bool present = !kGather || gtab[i * 128 + lt] >= 0;
-      if (kDtype == CSA2_CACHE_FP4) {
+      if (kDtype != CSA2_CACHE_BF16) {
         uint4 cw[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           cw[c] = *reinterpret_cast<const uint4*>(slot + h * kIdxFp4Data + (c * kPage + sl) * 16);
-        const uint2 sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * kIdxFp4Scales + sl * 8);
+        // the entry's scales: 8 bytes (one per 16 channels) or 4 (one per 32)
+        uint2 sc;
+        if (kDtype == CSA2_CACHE_FP4)
+          sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 8);
+        else
+          sc = make_uint2(*reinterpret_cast<const uint32_t*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 4), 0u);
         if (!kGather) tc::mbar_arrive(&empty_bar[s]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // 32 channels -> 16 TMEM columns
@@ -415,7 +427,9 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
-            const uint32_t s2 = f16x2_scale(((gg < 4 ? sc.x : sc.y) >> (8 * (gg & 3))) & 0xFFu);
+            const uint32_t s2 = kDtype == CSA2_CACHE_FP4
+                                    ? f16x2_scale(((gg < 4 ? sc.x : sc.y) >> (8 * (gg & 3))) & 0xFFu)
+                                    : f16x2_scale((sc.x >> (8 * c)) & 0xFFu);  // 32-channel group c
             uint32_t h4[4];
             e2m1x8_to_f16x2(w4[q], h4);
 #pragma unroll
@@ -530,6 +544,12 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   *n_slots = splits;
   ScoreArgs a{q0, Tq, cfg.ratio, seg, gps, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
               pool, cfg.hsi_blocks, scores, stride, bmax, krange, kr_stride, status};
+  if (idx_dtype(cfg) == CSA2_CACHE_FP4_S32) {
+    if (gather) return launch_one<CSA2_CACHE_FP4_S32, 1, true>(a, groups, splits, stream);
+    if (qpc == 6) return launch_one<CSA2_CACHE_FP4_S32, 6, false>(a, groups, splits, stream);
+    return qpc == 4 ? launch_one<CSA2_CACHE_FP4_S32, 4, false>(a, groups, splits, stream)
+                    : launch_one<CSA2_CACHE_FP4_S32, 1, false>(a, groups, splits, stream);
+  }
   if (cfg.cache_dtype == CSA2_CACHE_FP4) {
     if (gather) return launch_one<CSA2_CACHE_FP4, 1, true>(a, groups, splits, stream);
     if (qpc == 6) return launch_one<CSA2_CACHE_FP4, 6, false>(a, groups, splits, stream);

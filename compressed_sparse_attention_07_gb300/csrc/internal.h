@@ -40,6 +40,11 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Format of the indexer cache under a layer configuration.
+inline int idx_dtype(const csa2_cfg& cfg) {
+  return (cfg.cache_dtype == CSA2_CACHE_FP4 && (cfg.formats & CSA2_FMT_IDX_68B)) ? CSA2_CACHE_FP4_S32 : cfg.cache_dtype;
+}
+
 inline CacheView view_of(const csa2_cache& c) {
   return CacheView{static_cast<uint8_t*>(c.data), static_cast<uint8_t*>(c.scales), c.block_table,
                    c.max_pages, c.num_pages};
@@ -75,12 +80,18 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
                               int32_t* status, cudaStream_t stream);
 
 cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q, const csa2_cache& main_c,
-                          const int32_t* n_entries, const int32_t* topk, const uint16_t* swa, int S,
+                          const int32_t* n_entries, const int32_t* topk, const void* swa, int S,
                           const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos,
                           float scale, float* out, float* lse, int32_t* status, cudaStream_t stream);
 
 // Whether the attention kernel fits top-k + window rows (TMEM and shared memory).
 bool attend_tc_supported(int topk, int window);
+
+// Whether csa2_attend takes the row-tile kernel (the one that reads MXFP8 window rows).
+bool attend_rows_path(int topk, int window);
+
+cudaError_t launch_swa_encode(int B, int T, const uint16_t* x, const int64_t* row0, void* rows, int S,
+                              int32_t* status, cudaStream_t stream);
 
 cudaError_t launch_gather_dequant(const csa2_cache& c, int cache_dtype, int B, int n, const int32_t* ids,
                                   float* out, int32_t* status, cudaStream_t stream);

@@ -38,6 +38,15 @@
  *                    scales page 64 x 8 B, slot s at s*8.
  *  BF16: main page 64 x 1024 B row-major; indexer page 64 x 256 B by 16-byte
  *   chunks, chunk c (0..15) of slot s at (c*64 + s)*16; no scales.
+ *  FP4_S32 (indexer only; the 68-byte entry of hn.213312.xyz sec. 3.1: 64 B
+ *   of codes + one E4M3 scale per 32 channels): data page as FP4 indexer;
+ *   scales page 64 x 4 B, slot s at s*4.
+ *
+ * Window rows (the layer's sliding-window KV, passed to csa2_attend): bf16
+ * [B][S][512], or with CSA2_FMT_SWA_FP8 rows of 528 bytes in the OCP MXFP8
+ * layout (hn.213312.xyz sec. 2.4.4: the SWA KV stays in FP8): bytes 0..511
+ * E4M3 elements (channel c at byte c), bytes 512..527 one E8M0 scale
+ * 2^(e - 127) per 32 channels; value = E4M3(element) x scale.
  */
 #ifndef CSA2_H
 #define CSA2_H
@@ -67,7 +76,13 @@ enum {
   CSA2_ERR_TIMEOUT = 18     /* a bounded device-side wait gave up */
 };
 
-enum { CSA2_CACHE_FP4 = 0, CSA2_CACHE_BF16 = 1 };
+enum { CSA2_CACHE_FP4 = 0, CSA2_CACHE_BF16 = 1, CSA2_CACHE_FP4_S32 = 2 };
+/* csa2_cfg.formats flags (0 = FP4 indexer entries with one scale per 16
+ * channels, bf16 window rows) */
+enum {
+  CSA2_FMT_IDX_68B = 1, /* FP4 caches: the indexer cache is CSA2_CACHE_FP4_S32 */
+  CSA2_FMT_SWA_FP8 = 2  /* window rows are 528-byte MXFP8 rows */
+};
 enum { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1, CSA2_MODE_REUSE = 2 };
 
 #define CSA2_PAGE_ENTRIES 64
@@ -87,8 +102,8 @@ typedef struct csa2_cfg {
   int32_t ratio;       /* tokens merged per entry r (2 encoder, 1 decoder) */
   int32_t hsi_blocks;  /* HSI candidate blocks per query (2048); 0 = no HSI */
   int32_t hsi_block;   /* entries per HSI block (8) */
-  int32_t cache_dtype; /* CSA2_CACHE_FP4 or CSA2_CACHE_BF16 */
-  int32_t reserved;    /* must be 0 */
+  int32_t cache_dtype; /* CSA2_CACHE_FP4 or CSA2_CACHE_BF16 (main cache) */
+  int32_t formats;     /* CSA2_FMT_* flags; 0 for the default formats */
   double rope_theta;   /* RoPE base (10000 encoder, 160000 decoder) */
 } csa2_cfg;
 
@@ -103,7 +118,8 @@ typedef struct csa2_cache {
   int32_t reserved;           /* must be 0 */
 } csa2_cache;
 
-/* Bytes of one page of a cache: which = 0 data, 1 scales (0 for BF16). */
+/* Bytes of one page of a cache: which = 0 data, 1 scales (0 for BF16);
+ * cache_dtype CSA2_CACHE_FP4, CSA2_CACHE_BF16 or CSA2_CACHE_FP4_S32. */
 CSA2_API size_t csa2_page_bytes(int32_t channels, int32_t cache_dtype, int32_t which);
 
 /* Human-readable name of a status code (static string). */
@@ -158,13 +174,26 @@ CSA2_API int32_t csa2_index_topk(const csa2_cfg* cfg, int32_t B, int32_t Tq, con
  * the window rows of swa[b] at positions max(0, q_pos-W+1) .. q_pos that lie
  * in [swa_pos0[b], swa_pos0[b] + swa_len[b]); logits l_e = scale * q_h . c_e,
  * p = softmax over E jointly, out_h = sum_e p_e c_e (all 512 channels).
- * q [B][Tq][64][512] bf16; topk [B][Tq][topk]; swa [B][S][512] bf16;
+ * q [B][Tq][64][512] bf16; topk [B][Tq][topk]; swa [B][S][512] bf16, or
+ * [B][S] MXFP8 rows of 528 B with CSA2_FMT_SWA_FP8 (16-byte aligned; only
+ * for topk + window <= 768, else CSA2_ERR_UNSUPPORTED);
  * out [B][Tq][64][512] fp32; lse [B][Tq][64] fp32 natural log, or NULL. */
 CSA2_API int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q,
                     const csa2_cache* main_cache, const int32_t* n_entries, const int32_t* topk,
-                    const uint16_t* swa, int32_t S, const int32_t* swa_len, const int64_t* swa_pos0,
+                    const void* swa, int32_t S, const int32_t* swa_len, const int64_t* swa_pos0,
                     const int64_t* q_pos, float scale, float* out, float* lse, int32_t* status,
                     void* stream);
+
+/* FP8 window rows (hn.213312.xyz sec. 2.4.4: the SWA KV stays FP8), OCP
+ * MXFP8: for each sequence b the T bf16 rows x[b] [T][512] are encoded into
+ * rows[b][row0[b] + i] of a [B][S] array of 528-byte rows (layout above).
+ * Per 32-channel block: scale 2^(floor(log2 amax) - 8) (E8M0, clamped to
+ * 2^-127 .. 2^127; an all-zero block takes 2^-127); element = the E4M3 value
+ * nearest to x / scale, ties to even, saturating at 448, +0 for values that
+ * round to zero.  row0 [B] int64 (device); a sequence whose rows would fall
+ * outside [0, S) is skipped and CSA2_ERR_BAD_INDEX written to *status. */
+CSA2_API int32_t csa2_swa_encode(int32_t B, int32_t T, const uint16_t* x, const int64_t* row0, void* rows,
+                                 int32_t S, int32_t* status, void* stream);
 
 /* csa2_index_topk without a caller-provided workspace, for callers that
  * cannot allocate device memory (a serving engine or plugin host that owns
@@ -227,7 +256,7 @@ typedef struct csa2_layer_io {
   const float* head_w;
   /* attention, every mode */
   const uint16_t* q;
-  const uint16_t* swa;
+  const void* swa;           /* bf16 rows, or MXFP8 rows with CSA2_FMT_SWA_FP8 */
   int32_t S;
   const int32_t* swa_len;
   const int64_t* swa_pos0;

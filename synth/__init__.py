@@ -48,12 +48,13 @@ def merge_weights(g: np.random.Generator, r: int, dim: int) -> np.ndarray:
     return np.stack([np.cos(phi), np.sin(phi)]).astype(np.float32)
 
 
-def fp4_bytes(g: np.random.Generator, n: int, channels: int, scale_lo: int = 0x20, scale_hi: int = 0x3C):
+def fp4_bytes(g: np.random.Generator, n: int, channels: int, scale_lo: int = 0x20, scale_hi: int = 0x3C,
+              group: int = 16):
     """Random FP4 entries in canonical form: codes [n][channels/2] (uniform bytes,
-    i.e. uniform E2M1 codes) and E4M3 scales [n][channels/16] drawn uniformly
+    i.e. uniform E2M1 codes) and E4M3 scales [n][channels/group] drawn uniformly
     from the byte range [scale_lo, scale_hi] (0x20..0x3C = 0.125..0.875 x 2^0)."""
     codes = g.integers(0, 256, size=(n, channels // 2), dtype=np.uint8)
-    scales = g.integers(scale_lo, scale_hi + 1, size=(n, channels // 16), dtype=np.uint8)
+    scales = g.integers(scale_lo, scale_hi + 1, size=(n, channels // group), dtype=np.uint8)
     return codes, scales
 
 
@@ -101,6 +102,8 @@ class Workload:
     window: int = 128
     hsi_blocks: int = 2048
     hsi_block: int = 8
+    idx68: bool = False    # indexer entries of 68 B (one E4M3 scale per 32 channels)
+    swa_fp8: bool = False  # MXFP8 window rows (528 B) instead of bf16
     extra: dict = field(default_factory=dict)
 
     @property
@@ -133,6 +136,9 @@ WORKLOADS = {
         tq=4096),
     "mqdecode_b8_q5_ctx32768_r2_fp4": Workload(
         "mqdecode_b8_q5_ctx32768_r2_fp4", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=6, tq=5),
+    "decode_b8_ctx32768_r2_fp4_idx68_fp8swa": Workload(
+        "decode_b8_ctx32768_r2_fp4_idx68_fp8swa", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=7,
+        idx68=True, swa_fp8=True),
     "encoder_group6_b8_ctx32768_r2_fp4": Workload(
         "encoder_group6_b8_ctx32768_r2_fp4", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=5,
         layers=ENCODER_GROUP),

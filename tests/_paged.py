@@ -36,16 +36,21 @@ def _pad_entries(a: np.ndarray, cap: int) -> np.ndarray:
     return out
 
 
+def _group(cache) -> int:
+    """Channels per FP4 scale: 16, or 32 for the 68-byte indexer entry."""
+    return 32 if cache.cache_dtype == csa.CACHE_FP4_S32 else 16
+
+
 def _page_bytes(cache: csa.PagedCache, canon_codes: np.ndarray, canon_scales):
     """Canonical [B][cap][...] -> per-page byte rows in block-table order."""
     B, mp = cache.batch, cache.max_pages
     C_ = cache.channels
     codes = _pad_entries(canon_codes, cache.capacity)
-    if cache.cache_dtype == csa.CACHE_FP4:
+    if cache.cache_dtype != csa.CACHE_BF16:
         cb = codes.reshape(B, mp, PAGE, C_ // 2)
         if C_ == 128:  # 16-byte chunk c of slot s at (c*64 + s)*16
             cb = cb.reshape(B, mp, PAGE, 4, 16).transpose(0, 1, 3, 2, 4)
-        sb = _pad_entries(canon_scales, cache.capacity).reshape(B, mp, PAGE * (C_ // 16))
+        sb = _pad_entries(canon_scales, cache.capacity).reshape(B, mp, PAGE * (C_ // _group(cache)))
         return cb.reshape(B * mp, -1), sb.reshape(B * mp, -1)
     vb = codes.view(np.uint8).reshape(B, mp, PAGE, C_ * 2)
     if C_ == 128:
@@ -55,7 +60,7 @@ def _page_bytes(cache: csa.PagedCache, canon_codes: np.ndarray, canon_scales):
 
 def upload(cache: csa.PagedCache, ocache) -> None:
     """Copy an oracle.Cache (canonical) into the paged device cache."""
-    if cache.cache_dtype == csa.CACHE_FP4:
+    if cache.cache_dtype != csa.CACHE_BF16:
         d, s = _page_bytes(cache, ocache.codes, ocache.scales)
     else:
         d, s = _page_bytes(cache, ocache.bf16, None)
@@ -71,12 +76,12 @@ def download(cache: csa.PagedCache, n: int):
     B, mp, C_ = cache.batch, cache.max_pages, cache.channels
     bt = cache.block_table.flatten().long()
     d = cache.data[bt].cpu().numpy()
-    if cache.cache_dtype == csa.CACHE_FP4:
+    if cache.cache_dtype != csa.CACHE_BF16:
         cb = d.reshape(B, mp, -1)
         if C_ == 128:
             cb = cb.reshape(B, mp, 4, PAGE, 16).transpose(0, 1, 3, 2, 4)
         codes = np.ascontiguousarray(cb).reshape(B, mp * PAGE, C_ // 2)[:, :n]
-        s = cache.scales[bt].cpu().numpy().reshape(B, mp * PAGE, C_ // 16)[:, :n]
+        s = cache.scales[bt].cpu().numpy().reshape(B, mp * PAGE, C_ // _group(cache))[:, :n]
         return codes, s
     vb = d.reshape(B, mp, -1)
     if C_ == 128:
@@ -86,8 +91,8 @@ def download(cache: csa.PagedCache, n: int):
 
 
 def cache_pair(B, capacity, channels, dtype: str, seed: int):
-    """A paged device cache with a shuffled page table."""
-    cd = csa.CACHE_FP4 if dtype == "fp4" else csa.CACHE_BF16
+    """A paged device cache with a shuffled page table ("fp4", "fp4g32" or "bf16")."""
+    cd = {"fp4": csa.CACHE_FP4, "fp4g32": csa.CACHE_FP4_S32, "bf16": csa.CACHE_BF16}[dtype]
     mp = -(-capacity // PAGE)
     order = page_order(seed, B * mp + 3)[: B * mp]
     return csa.PagedCache(B, capacity, channels, cd, page_order=order, spare_pages=3)
@@ -99,7 +104,7 @@ def upload_seq(cache: csa.PagedCache, b: int, ocache, ob: int = 0) -> None:
     C_ = cache.channels
     n = ocache.n_cap
     one = type(ocache)(1, cache.capacity, C_, ocache.dtype)
-    if ocache.dtype == "fp4":
+    if ocache.dtype != "bf16":
         one.codes[0, :n], one.scales[0, :n] = ocache.codes[ob], ocache.scales[ob]
     else:
         one.bf16[0, :n] = ocache.bf16[ob]
@@ -108,7 +113,7 @@ def upload_seq(cache: csa.PagedCache, b: int, ocache, ob: int = 0) -> None:
     view.max_pages, view.capacity, view.num_pages = mp, cache.capacity, cache.num_pages
     view.data, view.scales = cache.data, cache.scales
     view.block_table = cache.block_table[b:b + 1]
-    if ocache.dtype == "fp4":
+    if ocache.dtype != "bf16":
         d, s = _page_bytes(view, one.codes, one.scales)
     else:
         d, s = _page_bytes(view, one.bf16, None)

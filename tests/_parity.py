@@ -29,12 +29,14 @@ _E2M1_MID = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
 
 
 def fp4_code_mismatches(gpu_codes, gpu_scales, ora_codes, ora_scales, pre, mag, margin):
-    """Returns (n_unexcused, n_excused, bad_entry_mask [..., entries])."""
+    """Returns (n_unexcused, n_excused, bad_entry_mask [..., entries]); the scale
+    group (16 or 32 channels) follows from the shape of the scales."""
     C = pre.shape[-1]
-    G = C // 16
+    G = ora_scales.shape[-1]
+    gs = C // G
     lead = pre.shape[:-1]
-    pre_g = pre.reshape(lead + (G, 16))
-    mag_g = mag.reshape(lead + (G, 16))
+    pre_g = pre.reshape(lead + (G, gs))
+    mag_g = mag.reshape(lead + (G, gs))
     amax = np.abs(pre_g).max(-1)
     tol_a = margin * mag_g.max(-1)
     near_scale = (np.abs(amax[..., None] - _SCALE_T) <= tol_a[..., None]).any(-1)
@@ -45,9 +47,9 @@ def fp4_code_mismatches(gpu_codes, gpu_scales, ora_codes, ora_scales, pre, mag, 
 
     gc, oc = nib(gpu_codes), nib(ora_codes)
     s = _E4_ALL[ora_scales.astype(np.int64)]
-    s_el = np.repeat(s, 16, axis=-1)
+    s_el = np.repeat(s, gs, axis=-1)
     near_code = (np.abs(np.abs(pre)[..., None] - s_el[..., None] * _E2M1_MID) <= (margin * mag)[..., None]).any(-1)
-    near_code |= np.repeat(near_scale, 16, axis=-1)
+    near_code |= np.repeat(near_scale, gs, axis=-1)
     scale_bad = gpu_scales != ora_scales
     code_bad = gc != oc
     unexcused = int((scale_bad & ~near_scale).sum() + (code_bad & ~near_code).sum())

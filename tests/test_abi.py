@@ -143,3 +143,52 @@ def test_paged_round_trip_on_host():
             np.testing.assert_array_equal(got, oc.codes[bj, j])
         else:
             np.testing.assert_array_equal(a, oc.bf16)
+
+
+def test_page_bytes_of_the_68_byte_indexer_entry():
+    lib = csa.load()
+    assert lib.csa2_page_bytes(128, csa.CACHE_FP4_S32, 0) == 64 * 64
+    assert lib.csa2_page_bytes(128, csa.CACHE_FP4_S32, 1) == 64 * 4
+    assert (lib.csa2_page_bytes(128, csa.CACHE_FP4_S32, 0) + lib.csa2_page_bytes(128, csa.CACHE_FP4_S32, 1)) // 64 == 68
+    assert lib.csa2_page_bytes(16, csa.CACHE_FP4_S32, 0) == 0  # channels not a multiple of 32
+
+
+def test_format_flags_are_validated():
+    lib = csa.load()
+    m, i = _fake_cache(512), _fake_cache(128)
+    # an unknown flag, or the 68-byte indexer entry on a bf16 cache
+    for cfg in (csa.Cfg(formats=4), csa.Cfg(cache_dtype=csa.CACHE_BF16, formats=csa.FMT_IDX_68B)):
+        assert lib.csa2_compress(C.byref(cfg), 1, 2, FAKE, FAKE, FAKE, FAKE, C.byref(m), C.byref(i), FAKE, None,
+                                 None) == 1
+    # 68-byte entries need the indexer cache's scale pages
+    cfg = csa.Cfg(formats=csa.FMT_IDX_68B)
+    i_noscale = csa._CacheDesc(FAKE, None, FAKE, 4, 8, 128, 0)
+    assert lib.csa2_index_topk(C.byref(cfg), 1, 1, FAKE, None, FAKE, C.byref(i_noscale), FAKE, 256, None, FAKE,
+                               None, FAKE, 1 << 30, None, None) == 1
+    # MXFP8 window rows go through the row-tile attention only (top-k + window <= 6 tiles of 128)
+    big = csa.Cfg(topk=1024, window=128, formats=csa.FMT_SWA_FP8)
+    assert lib.csa2_attend(C.byref(big), 1, 1, FAKE, C.byref(m), FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 1.0, FAKE,
+                           None, None, None) == 2
+    # swa_encode: rows must be 16-byte aligned and T <= S; empty is a no-op
+    assert lib.csa2_swa_encode(1, 4, FAKE, FAKE, FAKE + 8, 8, None, None) == 1
+    assert lib.csa2_swa_encode(1, 9, FAKE, FAKE, FAKE, 8, None, None) == 1
+    assert lib.csa2_swa_encode(0, 4, None, None, None, 8, None, None) == 0
+
+
+def test_paged_round_trip_of_68_byte_indexer_entries():
+    import oracle
+    import synth
+    from tests import _paged
+
+    order = _paged.page_order(2, 3 * 3 + 2)[:9]
+    pc = csa.PagedCache(3, 150, 128, csa.CACHE_FP4_S32, device="cpu", page_order=order, spare_pages=2)
+    oc = oracle.Cache(3, 150, 128, "fp4g32")
+    g = synth.rng(2, "rt32")
+    oc.codes[:], oc.scales[:] = g.integers(0, 256, oc.codes.shape), g.integers(0, 256, oc.scales.shape)
+    _paged.upload(pc, oc)
+    a, b = _paged.download(pc, 150)
+    np.testing.assert_array_equal(a, oc.codes)
+    np.testing.assert_array_equal(b, oc.scales)
+    bj, j = 1, 77  # documented address of one entry's scales: slot s at s*4
+    page, slot = int(pc.block_table[bj, j // 64]), j % 64
+    np.testing.assert_array_equal(pc.scales[page, slot * 4:slot * 4 + 4].numpy(), oc.scales[bj, j])

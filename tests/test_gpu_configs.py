@@ -25,8 +25,14 @@ SCALE = 1 / math.sqrt(D)
 
 
 def _cfg(wl):
+    fmt = (csa.FMT_IDX_68B if wl.idx68 else 0) | (csa.FMT_SWA_FP8 if wl.swa_fp8 else 0)
     return csa.Cfg(ratio=wl.ratio, cache_dtype=csa.CACHE_FP4 if wl.cache == "fp4" else csa.CACHE_BF16,
-                   topk=wl.topk, window=wl.window, hsi_blocks=wl.hsi_blocks if wl.hsi else 0, rope_theta=wl.theta)
+                   topk=wl.topk, window=wl.window, hsi_blocks=wl.hsi_blocks if wl.hsi else 0, rope_theta=wl.theta,
+                   formats=fmt)
+
+
+def _idx_dtype(wl):
+    return "fp4g32" if wl.idx68 else wl.cache
 
 
 def _prefix(wl, b, n):
@@ -57,10 +63,10 @@ def _compress_full_context(wl):
     N = ctx // r
     x = synth.normal_bf16(synth.rng(wl.seed, "ctx_tokens"), (B, ctx, D))
     w, w_idx, q, q_idx, swa = _step_inputs(wl, B)
-    om, oi = oracle.Cache(B, N, D, wl.cache), oracle.Cache(B, N, CI, wl.cache)
+    om, oi = oracle.Cache(B, N, D, wl.cache), oracle.Cache(B, N, CI, _idx_dtype(wl))
     diag = oracle.compress(x, np.zeros(B, np.int64), w, w_idx, om, oi, r, wl.theta, diagnostics=True)
     cfg = _cfg(wl)
-    pm, pi = _paged.cache_pair(B, N, D, wl.cache, wl.seed), _paged.cache_pair(B, N, CI, wl.cache, wl.seed + 1)
+    pm, pi = _paged.cache_pair(B, N, D, wl.cache, wl.seed), _paged.cache_pair(B, N, CI, _idx_dtype(wl), wl.seed + 1)
     n_ent = torch.zeros(B, dtype=torch.int32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     csa.compress(cfg, _paged.dev(x), _paged.dev(np.zeros(B, np.int64)), _paged.dev(w), _paged.dev(w_idx), pm, pi,
@@ -72,11 +78,26 @@ def _compress_full_context(wl):
     return cfg, om, oi, pm, pi, n_ent, q, q_idx, swa
 
 
-@pytest.mark.parametrize("name", ["decode_b1_ctx4096_r2_bf16", "decode_b8_ctx32768_r2_fp4"])
+@pytest.mark.parametrize("name", ["decode_b1_ctx4096_r2_bf16", "decode_b8_ctx32768_r2_fp4",
+                                  "decode_b8_ctx32768_r2_fp4_idx68_fp8swa"])
 def test_decode_full_context_through_the_compressor(name):
+    """The whole context through the compressor on both sides, then indexing
+    and attention of the last position.  The pages' own formats (68-byte
+    indexer entries, MXFP8 window rows) run the same check; their window rows
+    are encoded on each side and compared bit for bit first."""
     wl = synth.WORKLOADS[name]
     B, N = wl.batch, wl.ctx // wl.ratio
     cfg, om, oi, pm, pi, n_ent, q, q_idx, swa = _compress_full_context(wl)
+    swa_dev = _paged.dev(swa)
+    if wl.swa_fp8:
+        rows = torch.zeros((B, wl.window, csa.SWA_FP8_ROW), dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        csa.swa_encode(swa_dev, torch.zeros(B, dtype=torch.int64, device="cuda"), rows, status=st)
+        swa = oracle.swa_encode(swa)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        np.testing.assert_array_equal(rows.cpu().numpy(), swa)
+        swa_dev = rows
     q_pos = np.full((B, 1), wl.ctx - 1, np.int64)
     swa_len, swa_pos0 = np.full(B, wl.window, np.int32), np.full(B, wl.ctx - wl.window, np.int64)
     topk = torch.empty((B, 1, wl.topk), dtype=torch.int32, device="cuda")
@@ -84,7 +105,7 @@ def test_decode_full_context_through_the_compressor(name):
     out = torch.empty((B, 1, 64, D), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     csa.index_topk(cfg, _paged.dev(q_idx), _paged.dev(q_pos), pi, n_ent, N, topk, ws, status=st)
-    csa.attend(cfg, _paged.dev(q), pm, n_ent, topk, _paged.dev(swa), _paged.dev(swa_len), _paged.dev(swa_pos0),
+    csa.attend(cfg, _paged.dev(q), pm, n_ent, topk, swa_dev, _paged.dev(swa_len), _paged.dev(swa_pos0),
                _paged.dev(q_pos), out, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0

@@ -161,7 +161,8 @@ class StepBase:
         import compressed_sparse_attention_07_gb300 as csa
         self.torch, self.csa, self.wl, self.device = torch, csa, wl, device
         self.cd = csa.CACHE_FP4 if wl.cache == "fp4" else csa.CACHE_BF16
-        fmt = (csa.FMT_IDX_68B if wl.idx68 else 0) | (csa.FMT_SWA_FP8 if wl.swa_fp8 else 0)
+        fmt = ((csa.FMT_IDX_68B if wl.idx68 else 0) | (csa.FMT_SWA_FP8 if wl.swa_fp8 else 0) |
+               (csa.FMT_IDX_QFP4 if wl.q_fp4 else 0))
         self.cfg = csa.Cfg(ratio=wl.ratio, cache_dtype=self.cd, topk=wl.topk, window=wl.window,
                            hsi_blocks=wl.hsi_blocks if wl.hsi else 0, rope_theta=wl.theta, formats=fmt)
         self.seed = wl.seed + seed_offset
@@ -478,7 +479,7 @@ class OracleStep:
             self.swa[:, -1:] = o.swa_encode(self.swa_new)
         if self.prefill or not wl.layers:
             topk, _, _ = o.index_topk(self.idx, self.n_ent, self.q_idx, self.q_pos, wl.ratio, wl.topk,
-                                      hsi_blocks=wl.hsi_blocks if wl.hsi else 0, want_pool=wl.hsi)
+                                      hsi_blocks=wl.hsi_blocks if wl.hsi else 0, want_pool=wl.hsi, q_fp4=wl.q_fp4)
             return o.attend(self.main, self.n_ent, self.q, topk, self.swa, self.swa_len, self.swa_pos0, self.q_pos,
                             wl.window, sc)
         topk = pool = None

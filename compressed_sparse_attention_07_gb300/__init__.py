@@ -19,11 +19,11 @@ __all__ = [
     "Cfg", "PagedCache", "GroupState", "load", "compress", "index_workspace_bytes", "index_topk", "attend",
     "gather_dequant", "layer", "status_string", "CsaError", "CACHE_FP4", "CACHE_BF16", "MODE_FULL",
     "MODE_REINDEX", "MODE_REUSE", "PAGE", "library_path", "capture", "swa_encode", "CACHE_FP4_S32",
-    "FMT_IDX_68B", "FMT_SWA_FP8", "SWA_FP8_ROW",
+    "FMT_IDX_68B", "FMT_SWA_FP8", "FMT_IDX_QFP4", "SWA_FP8_ROW",
 ]
 
 CACHE_FP4, CACHE_BF16, CACHE_FP4_S32 = 0, 1, 2
-FMT_IDX_68B, FMT_SWA_FP8 = 1, 2
+FMT_IDX_68B, FMT_SWA_FP8, FMT_IDX_QFP4 = 1, 2, 4
 SWA_FP8_ROW = 528  # bytes of one MXFP8 window row
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 PAGE = 64
@@ -38,8 +38,8 @@ class CsaError(RuntimeError):
 class Cfg(C.Structure):
     """csa2_cfg: defaults are the model's sizes (64 x 512 latent, 64 RoPE
     dims, indexer 32 x 128, top-512, window 128, HSI 2048 x 8); `formats`
-    takes FMT_IDX_68B (indexer entries with one scale per 32 channels) and
-    FMT_SWA_FP8 (MXFP8 window rows)."""
+    takes FMT_IDX_68B (indexer entries with one scale per 32 channels),
+    FMT_SWA_FP8 (MXFP8 window rows) and FMT_IDX_QFP4 (FP4 indexer queries)."""
     _fields_ = [("dim", C.c_int32), ("rope_dims", C.c_int32), ("n_heads", C.c_int32), ("idx_heads", C.c_int32),
                 ("idx_dim", C.c_int32), ("topk", C.c_int32), ("window", C.c_int32), ("ratio", C.c_int32),
                 ("hsi_blocks", C.c_int32), ("hsi_block", C.c_int32), ("cache_dtype", C.c_int32),

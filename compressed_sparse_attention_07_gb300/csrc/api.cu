@@ -11,7 +11,7 @@ namespace {
 
 bool cfg_supported(const csa2_cfg* c, int32_t* err) {
   if (!c) { *err = CSA2_ERR_INVALID_ARG; return false; }
-  if ((c->formats & ~(CSA2_FMT_IDX_68B | CSA2_FMT_SWA_FP8)) != 0 || !(c->rope_theta > 0.0) ||
+  if ((c->formats & ~(CSA2_FMT_IDX_68B | CSA2_FMT_SWA_FP8 | CSA2_FMT_IDX_QFP4)) != 0 || !(c->rope_theta > 0.0) ||
       (c->cache_dtype != CSA2_CACHE_FP4 && c->cache_dtype != CSA2_CACHE_BF16) ||
       ((c->formats & CSA2_FMT_IDX_68B) && c->cache_dtype != CSA2_CACHE_FP4)) {
     *err = CSA2_ERR_INVALID_ARG;

@@ -54,6 +54,7 @@ struct TileFmt {
 struct ScoreArgs {
   int q0, Tq, r;
   int seg, gps;         // query groups: segments of `seg` queries from q0, `gps` groups of QPC each
+  int q_fp4;            // score with FP4-encoded indexer queries
   const uint16_t* q_idx;
   const float* head_w;
   const int64_t* q_pos;
@@ -270,16 +271,41 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     if (row / kIdxHeads < n_act)
       v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
                                                (row % kIdxHeads) * kIdxDim + k));
-    if (!kBf16) {
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (a.q_fp4) {
+      // FP4 indexer query: this thread's 8 channels and its neighbour lane's
+      // form one 16-channel group; encode (E4M3 scale nearest amax / 6, E2M1
+      // codes, both by exact comparisons) and read back, exactly
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[2 * j] = __uint_as_float(w[j] << 16);
+        f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      const float sc = e4m3_pos(e4m3_scale_code(amax));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = e2m1_to_float(e2m1_code(f[j], sc)) * sc;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (kBf16) {
+          w[j] = (__float_as_uint(f[2 * j]) >> 16) | (__float_as_uint(f[2 * j + 1]) & 0xFFFF0000u);
+        } else {
+          const __half2 h2 = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+          w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+    } else if (!kBf16) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
         w[j] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      v = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = v;
+    *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   for (int i = tid; i < QPC * kIdxHeads; i += kConsumers)
     hw[i / kIdxHeads][i % kIdxHeads] =
@@ -542,7 +568,7 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   const int splits = (int)((tiles + per - 1) / per);
   if (splits > kr_stride) return cudaErrorInvalidValue;
   *n_slots = splits;
-  ScoreArgs a{q0, Tq, cfg.ratio, seg, gps, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
+  ScoreArgs a{q0, Tq, cfg.ratio, seg, gps, (cfg.formats & CSA2_FMT_IDX_QFP4) ? 1 : 0, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
               pool, cfg.hsi_blocks, scores, stride, bmax, krange, kr_stride, status};
   if (idx_dtype(cfg) == CSA2_CACHE_FP4_S32) {
     if (gather) return launch_one<CSA2_CACHE_FP4_S32, 1, true>(a, groups, splits, stream);

@@ -80,8 +80,11 @@ enum { CSA2_CACHE_FP4 = 0, CSA2_CACHE_BF16 = 1, CSA2_CACHE_FP4_S32 = 2 };
 /* csa2_cfg.formats flags (0 = FP4 indexer entries with one scale per 16
  * channels, bf16 window rows) */
 enum {
-  CSA2_FMT_IDX_68B = 1, /* FP4 caches: the indexer cache is CSA2_CACHE_FP4_S32 */
-  CSA2_FMT_SWA_FP8 = 2  /* window rows are 528-byte MXFP8 rows */
+  CSA2_FMT_IDX_68B = 1,  /* FP4 caches: the indexer cache is CSA2_CACHE_FP4_S32 */
+  CSA2_FMT_SWA_FP8 = 2,  /* window rows are 528-byte MXFP8 rows */
+  CSA2_FMT_IDX_QFP4 = 4  /* indexer queries scored in FP4: each head's q_idx is encoded like a
+                            cache entry (E2M1, E4M3 per 16 channels) and read back (the FP4
+                            indexer Q/K of hn.213312.xyz sec. 2.4.4) */
 };
 enum { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1, CSA2_MODE_REUSE = 2 };
 

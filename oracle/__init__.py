@@ -82,6 +82,9 @@ def lib():
             L.orc_index_topk.restype = i
             L.orc_index_topk.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, i, i, i,
                                          vp, vp, vp, vp]
+            L.orc_index_topk_q.restype = i
+            L.orc_index_topk_q.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, i, vp, vp, i, i, i,
+                                           vp, vp, vp, vp]
             L.orc_attend.restype = i
             L.orc_attend.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, i, vp, i, i, vp, vp, vp,
                                      i, d, vp, vp]
@@ -251,8 +254,10 @@ def compress(x, pos0, w, w_idx, main: Cache, idx: Cache, r: int, theta: float, r
 
 
 def index_topk(idx: Cache, n_entries, q_idx, q_pos, r: int, k: int, head_w=None, hsi_blocks: int = 0,
-               hsi_block: int = 8, pool=None, want_pool: bool = False, want_scores: bool = False):
-    """a3-a6.  q_idx [B][Tq][H][Ci] bf16 bits, q_pos [B][Tq] int64.
+               hsi_block: int = 8, pool=None, want_pool: bool = False, want_scores: bool = False,
+               q_fp4: bool = False):
+    """a3-a6.  q_idx [B][Tq][H][Ci] bf16 bits, q_pos [B][Tq] int64; q_fp4: score with
+    each head's query encoded to FP4 (E2M1, E4M3 per 16 channels) and read back.
     Returns (topk [B][Tq][k] int32, pool [B][Tq][hsi_blocks] or None, scores or None)."""
     q_idx = _c(q_idx, np.uint16)
     B, Tq, H, Ci = q_idx.shape
@@ -263,10 +268,10 @@ def index_topk(idx: Cache, n_entries, q_idx, q_pos, r: int, k: int, head_w=None,
     topk = np.zeros((B, Tq, k), np.int32)
     pool_out = np.zeros((B, Tq, hsi_blocks), np.int32) if want_pool else None
     scores = np.zeros((B, Tq, idx.n_cap), np.float64) if want_scores else None
-    rc = lib().orc_index_topk(B, Tq, H, Ci, r, idx.dtype_code, idx.n_cap, _p(idx.codes),
-                              _p(idx.scales), _p(idx.bf16), _p(n_entries), _p(q_idx), _p(hw),
-                              _p(q_pos), k, hsi_blocks, hsi_block, _p(pl), _p(topk), _p(pool_out),
-                              _p(scores))
+    rc = lib().orc_index_topk_q(B, Tq, H, Ci, r, idx.dtype_code, idx.n_cap, _p(idx.codes),
+                                _p(idx.scales), _p(idx.bf16), _p(n_entries), _p(q_idx), int(bool(q_fp4)), _p(hw),
+                                _p(q_pos), k, hsi_blocks, hsi_block, _p(pl), _p(topk), _p(pool_out),
+                                _p(scores))
     if rc != 0:
         raise ValueError("orc_index_topk rejected its arguments (%d)" % rc)
     return topk, pool_out, scores

@@ -329,6 +329,15 @@ int orc_index_topk(int B, int Tq, int H, int Ci, int r, int cache_dtype, int n_c
                    const int32_t* n_entries, const uint16_t* q_idx, const float* head_w,
                    const int64_t* q_pos, int k, int n_blocks, int bs, const int32_t* pool,
                    int32_t* topk_out, int32_t* pool_out, double* scores_out) {
+  return orc_index_topk_q(B, Tq, H, Ci, r, cache_dtype, n_cap, idx_codes, idx_scales, idx_bf16, n_entries, q_idx,
+                          0, head_w, q_pos, k, n_blocks, bs, pool, topk_out, pool_out, scores_out);
+}
+
+int orc_index_topk_q(int B, int Tq, int H, int Ci, int r, int cache_dtype, int n_cap,
+                     const uint8_t* idx_codes, const uint8_t* idx_scales, const uint16_t* idx_bf16,
+                     const int32_t* n_entries, const uint16_t* q_idx, int q_fp4, const float* head_w,
+                     const int64_t* q_pos, int k, int n_blocks, int bs, const int32_t* pool,
+                     int32_t* topk_out, int32_t* pool_out, double* scores_out) {
   if (B < 0 || Tq < 0 || k < 1 || Ci % 16 || r < 1) return -1;
   if ((pool || pool_out) && (n_blocks < 1 || bs < 1)) return -1;
   if (pool && pool_out) return -1;
@@ -341,6 +350,18 @@ int orc_index_topk(int B, int Tq, int H, int Ci, int r, int cache_dtype, int n_c
       double* q = (double*)malloc(sizeof(double) * H * Ci);
       double* kv = (double*)malloc(sizeof(double) * Ci);
       for (int i = 0; i < H * Ci; ++i) q[i] = orc_bf16_value(q_idx[qi * H * Ci + i]);
+      if (q_fp4) {
+        /* FP4 indexer queries: each head's query encoded like a cache entry
+         * (E2M1, one E4M3 scale per 16 channels) and read back */
+        uint8_t* qc = (uint8_t*)malloc((size_t)Ci / 2);
+        uint8_t* qs = (uint8_t*)malloc((size_t)Ci / 16);
+        for (int h = 0; h < H; ++h) {
+          orc_fp4_encode(q + (size_t)h * Ci, Ci, qc, qs);
+          orc_fp4_decode(qc, qs, Ci, q + (size_t)h * Ci);
+        }
+        free(qc);
+        free(qs);
+      }
       /* candidate set: all visible entries, or the visible entries of the pool */
       char* cand = (char*)calloc((size_t)(nv > 0 ? nv : 1), 1);
       if (pool) {

@@ -123,6 +123,15 @@ int orc_index_topk(int B, int Tq, int H, int Ci, int r, int cache_dtype, int n_c
                    const int32_t* n_entries, const uint16_t* q_idx, const float* head_w,
                    const int64_t* q_pos, int k, int n_blocks, int bs, const int32_t* pool,
                    int32_t* topk_out, int32_t* pool_out, double* scores_out);
+/* The same with q_fp4 != 0: every head's indexer query is first encoded to
+ * FP4 like a cache entry (E2M1, one E4M3 scale per 16 channels) and read
+ * back, so the scores are FP4 x FP4 dot products (the FP4 indexer Q/K that
+ * sec. 2.4.4 says V4 already trained with). */
+int orc_index_topk_q(int B, int Tq, int H, int Ci, int r, int cache_dtype, int n_cap,
+                     const uint8_t* idx_codes, const uint8_t* idx_scales, const uint16_t* idx_bf16,
+                     const int32_t* n_entries, const uint16_t* q_idx, int q_fp4, const float* head_w,
+                     const int64_t* q_pos, int k, int n_blocks, int bs, const int32_t* pool,
+                     int32_t* topk_out, int32_t* pool_out, double* scores_out);
 
 /* ---- a7: sparse attention over top-k entries and the sliding window ----
  * q      [B][Tq][Hm][D] bf16 (already rotated)

@@ -104,6 +104,7 @@ class Workload:
     hsi_block: int = 8
     idx68: bool = False    # indexer entries of 68 B (one E4M3 scale per 32 channels)
     swa_fp8: bool = False  # MXFP8 window rows (528 B) instead of bf16
+    q_fp4: bool = False    # indexer queries scored in FP4 (E2M1, E4M3 per 16 channels)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -139,6 +140,8 @@ WORKLOADS = {
     "decode_b8_ctx32768_r2_fp4_idx68_fp8swa": Workload(
         "decode_b8_ctx32768_r2_fp4_idx68_fp8swa", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=7,
         idx68=True, swa_fp8=True),
+    "decode_b8_ctx32768_r2_fp4_qfp4": Workload(
+        "decode_b8_ctx32768_r2_fp4_qfp4", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=8, q_fp4=True),
     "encoder_group6_b8_ctx32768_r2_fp4": Workload(
         "encoder_group6_b8_ctx32768_r2_fp4", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=5,
         layers=ENCODER_GROUP),

@@ -157,7 +157,7 @@ def test_format_flags_are_validated():
     lib = csa.load()
     m, i = _fake_cache(512), _fake_cache(128)
     # an unknown flag, or the 68-byte indexer entry on a bf16 cache
-    for cfg in (csa.Cfg(formats=4), csa.Cfg(cache_dtype=csa.CACHE_BF16, formats=csa.FMT_IDX_68B)):
+    for cfg in (csa.Cfg(formats=8), csa.Cfg(cache_dtype=csa.CACHE_BF16, formats=csa.FMT_IDX_68B)):
         assert lib.csa2_compress(C.byref(cfg), 1, 2, FAKE, FAKE, FAKE, FAKE, C.byref(m), C.byref(i), FAKE, None,
                                  None) == 1
     # 68-byte entries need the indexer cache's scale pages

@@ -25,7 +25,8 @@ SCALE = 1 / math.sqrt(D)
 
 
 def _cfg(wl):
-    fmt = (csa.FMT_IDX_68B if wl.idx68 else 0) | (csa.FMT_SWA_FP8 if wl.swa_fp8 else 0)
+    fmt = ((csa.FMT_IDX_68B if wl.idx68 else 0) | (csa.FMT_SWA_FP8 if wl.swa_fp8 else 0) |
+           (csa.FMT_IDX_QFP4 if wl.q_fp4 else 0))
     return csa.Cfg(ratio=wl.ratio, cache_dtype=csa.CACHE_FP4 if wl.cache == "fp4" else csa.CACHE_BF16,
                    topk=wl.topk, window=wl.window, hsi_blocks=wl.hsi_blocks if wl.hsi else 0, rope_theta=wl.theta,
                    formats=fmt)
@@ -79,7 +80,7 @@ def _compress_full_context(wl):
 
 
 @pytest.mark.parametrize("name", ["decode_b1_ctx4096_r2_bf16", "decode_b8_ctx32768_r2_fp4",
-                                  "decode_b8_ctx32768_r2_fp4_idx68_fp8swa"])
+                                  "decode_b8_ctx32768_r2_fp4_idx68_fp8swa", "decode_b8_ctx32768_r2_fp4_qfp4"])
 def test_decode_full_context_through_the_compressor(name):
     """The whole context through the compressor on both sides, then indexing
     and attention of the last position.  The pages' own formats (68-byte
@@ -110,7 +111,7 @@ def test_decode_full_context_through_the_compressor(name):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     n_arr = np.full(B, N, np.int32)
-    o_top, _, s = oracle.index_topk(oi, n_arr, q_idx, q_pos, wl.ratio, wl.topk, want_scores=True)
+    o_top, _, s = oracle.index_topk(oi, n_arr, q_idx, q_pos, wl.ratio, wl.topk, want_scores=True, q_fp4=wl.q_fp4)
     assert P.topk_mismatch(topk.cpu().numpy().reshape(B, -1), o_top.reshape(B, -1), s.reshape(B, -1), wl.topk,
                            exact=False) == 0
     o_out = oracle.attend(om, n_arr, q, o_top, swa, swa_len, swa_pos0, q_pos, wl.window, SCALE)

@@ -218,3 +218,50 @@ def test_gather_dequant_of_68_byte_entries_bit_exact():
     want = np.stack([vals[b][np.maximum(ids[b], 0)] for b in range(B)])
     want[1, 5] = 0.0
     np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), want)
+
+
+# -------------------------------------------------- FP4 indexer queries ----
+
+@pytest.mark.parametrize("dtype,Tq,mode", [("fp4", 2, "full"), ("fp4", 8, "full"), ("fp4", 5, "full"),
+                                           ("fp4", 2, "reindex"), ("fp4g32", 5, "full"), ("bf16", 3, "full")])
+def test_index_with_fp4_queries_bit_exact(dtype, Tq, mode):
+    """FP4-encoded indexer queries (E2M1, E4M3 per 16 channels) on every
+    scoring path: one query per group (Tq 2), runs of 4 (Tq 8), a multi-query
+    block (Tq 5), Reindex gathers, 68-byte entries, a bf16 cache.  Queries
+    are integers in [-5, 5], whose FP4 encodings are multiples of 1/16 (the
+    group scales 0.8125, 0.6875, ...), and the cache values are multiples of
+    1/4, so every score is exact and top-k and pools must match bit for bit."""
+    B, N, k, nb = 2, 4000, 512, 80
+    if dtype == "fp4g32":
+        oc, pc = _g32_caches(B, N, 60 + Tq)
+    else:
+        oc = oracle.Cache(B, N, CI, dtype)
+        g = synth.rng(60 + Tq, "int")
+        pick = synth.rng(60 + Tq, "dup").integers(0, 50, size=(B, N))
+        for b in range(B):
+            if dtype == "fp4":
+                c, s = synth.integer_fp4_bytes(g, 50, CI)
+                oc.codes[b], oc.scales[b] = c[pick[b]], s[pick[b]]
+            else:
+                oc.bf16[b] = synth.integer_bf16(g, (50, CI), -6, 6)[pick[b]]
+        pc = _paged.cache_pair(B, N, CI, dtype, 60 + Tq)
+        _paged.upload(pc, oc)
+    q_idx = synth.integer_bf16(synth.rng(61, "q%d" % Tq), (B, Tq, H, CI), -5, 5)
+    n_ent = np.array([N, 2900], np.int32)
+    q_pos = np.stack([n - Tq + np.arange(Tq) for n in n_ent]).astype(np.int64)
+    fmt = csa.FMT_IDX_QFP4 | (csa.FMT_IDX_68B if dtype == "fp4g32" else 0)
+    cfg = csa.Cfg(ratio=1, cache_dtype=csa.CACHE_BF16 if dtype == "bf16" else csa.CACHE_FP4, topk=k,
+                  hsi_blocks=nb, formats=fmt)
+    o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, 1, k, hsi_blocks=nb, want_pool=True, q_fp4=True)
+    if mode == "full":
+        g_top, g_pool = _index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+        np.testing.assert_array_equal(g_pool, o_pool)
+        np.testing.assert_array_equal(g_top, o_top)
+    else:
+        q2 = synth.integer_bf16(synth.rng(62, "q%d" % Tq), (B, Tq, H, CI), -5, 5)
+        r_top, _ = _index(cfg, pc, q2, q_pos, n_ent, N, pool=o_pool)
+        o_rtop, _, _ = oracle.index_topk(oc, n_ent, q2, q_pos, 1, k, hsi_blocks=nb, pool=o_pool, q_fp4=True)
+        np.testing.assert_array_equal(r_top, o_rtop)
+    # the FP4 queries change the selection against the bf16 queries
+    b_top, _, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, 1, k)
+    assert not np.array_equal(b_top, o_top)

@@ -1,4 +1,6 @@
-"""Pins of the oracle's two storage variants of the pages' own formats:
+"""Pins of the oracle's variants for the pages' own formats: FP4 indexer
+queries (sec. 2.4.4: V4 already trained its indexer Q/K in FP4), and two
+storage variants:
 the 68-byte indexer entry (FP4 with one E4M3 scale per 32 channels;
 hn.213312.xyz sec. 3.1 prints 68 B per 128-channel indexer entry) and the
 FP8 window rows (sec. 2.4.4: the SWA KV stays FP8), read as OCP MXFP8 --
@@ -220,3 +222,35 @@ def test_attend_on_mxfp8_rows_equals_bf16_rows_of_the_decoded_values():
     d8 = oracle.attend_dense(main, np.array([N], np.int32), q, rows, *args[:3], 1, W, 1 / math.sqrt(D))
     db = oracle.attend_dense(main, np.array([N], np.int32), q, dec_bits, *args[:3], 1, W, 1 / math.sqrt(D))
     np.testing.assert_array_equal(d8, db)
+
+
+# ------------------------------------------------- FP4 indexer queries ----
+
+def test_fp4_queries_equal_bf16_queries_holding_their_fp4_values():
+    """Scoring with FP4 queries equals scoring with bf16 queries that hold the
+    queries' FP4 encodings read back (exact in bf16: at most 6 significant
+    bits), on both cache formats; the FP4 queries are the pinned encoder's."""
+    B, Tq, N, k = 2, 2, 400, 64
+    for dtype in ("fp4", "fp4g32"):
+        c = oracle.Cache(B, N, 128, dtype)
+        g = synth.rng(50, dtype)
+        for b in range(B):
+            c.codes[b], c.scales[b] = synth.fp4_bytes(g, N, 128, group=16 if dtype == "fp4" else 32)
+        q_idx = synth.normal_bf16(synth.rng(50, "q"), (B, Tq, 32, 128))
+        qc, qs = oracle.fp4_encode(oracle.bf16_bits_to_f64(q_idx))
+        qv = oracle.fp4_decode(qc, qs)
+        q_bits = np.vectorize(oracle.bf16_round, otypes=[np.uint16])(qv)
+        np.testing.assert_array_equal(oracle.bf16_bits_to_f64(q_bits), qv)
+        q_pos = np.array([[N - 1, 200], [N - 1, 17]], np.int64)
+        n_ent = np.array([N, N - 3], np.int32)
+        hw = synth.rng(50, "hw").uniform(0, 2, size=(B, Tq, 32)).astype(np.float32)
+        t1, p1, s1 = oracle.index_topk(c, n_ent, q_idx, q_pos, 1, k, head_w=hw, hsi_blocks=8, want_pool=True,
+                                       want_scores=True, q_fp4=True)
+        t2, p2, s2 = oracle.index_topk(c, n_ent, q_bits, q_pos, 1, k, head_w=hw, hsi_blocks=8, want_pool=True,
+                                       want_scores=True)
+        np.testing.assert_array_equal(t1, t2)
+        np.testing.assert_array_equal(p1, p2)
+        np.testing.assert_array_equal(s1, s2)
+        # and the FP4 queries do change the scores
+        _, _, s3 = oracle.index_topk(c, n_ent, q_idx, q_pos, 1, k, head_w=hw, want_scores=True)
+        assert not np.array_equal(s1, s3)

@@ -322,58 +322,71 @@ class PrefillStep(StepBase):
 
 
 class GroupStep(StepBase):
-    """One decode step through a cross-layer group: decoder layers 20-39
-    (layer 20 Full: compress the new token, full indexing with the HSI pool;
-    layers 24/28/32/36 Reindex over the pool; the other fifteen Reuse) or the
-    encoder macro block 2-7 (layer 2 Full without HSI, five Reuse); every
+    """One step through a cross-layer group: decoder layers 20-39 (layer 20
+    Full: compress the new token, full indexing with the HSI pool; layers
+    24/28/32/36 Reindex over the pool; the other fifteen Reuse) or the encoder
+    macro block 2-7 (layer 2 Full without HSI, five Reuse), in decode (one
+    query token per sequence) or on a prefill chunk of Tq tokens (the Full
+    layer compresses the chunk and indexes every chunk token causally); every
     layer has its own query, indexer query and window rows."""
 
     def __init__(self, wl, device, seed_offset=0):
         super().__init__(wl, device, seed_offset)
         torch, csa, B, r, s = self.torch, self.csa, self.B, wl.ratio, self.seed
-        ctx = wl.ctx
-        self.N = ctx // r
+        ctx, Tq, W = wl.ctx, wl.tq, wl.window
+        self.N = (ctx + Tq) // r if Tq > 1 else ctx // r
         self.make_caches(self.N)
         self.layers = list(wl.layers)
-        self.h = {
-            "x": synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512)),
-            "pos0": np.full(B, ctx - r, np.int64),
-            "swa_len": np.full(B, wl.window, np.int32),
-            "swa_pos0": np.full(B, ctx - wl.window, np.int64),
-            "q_pos": np.full((B, 1), ctx - 1, np.int64),
-        }
+        S = W - 1 + Tq if Tq > 1 else W
+        if Tq > 1:
+            self.h = {"x": synth.normal_bf16(synth.rng(s, "x_chunk"), (B, Tq, 512)), "pos0": np.full(B, ctx, np.int64),
+                      "swa_len": np.full(B, S, np.int32), "swa_pos0": np.full(B, ctx - (W - 1), np.int64),
+                      "q_pos": np.tile(ctx + np.arange(Tq, dtype=np.int64), (B, 1))}
+        else:
+            self.h = {"x": synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512)), "pos0": np.full(B, ctx - r, np.int64),
+                      "swa_len": np.full(B, W, np.int32), "swa_pos0": np.full(B, ctx - W, np.int64),
+                      "q_pos": np.full((B, 1), ctx - 1, np.int64)}
         for layer, mode in self.layers:
             ls = s * 1000 + layer
-            self.h["q%d" % layer] = synth.normal_bf16(synth.rng(ls, "q"), (B, 1, 64, 512))
-            self.h["swa%d" % layer] = synth.normal_bf16(synth.rng(ls, "swa"), (B, wl.window, 512))
+            self.h["q%d" % layer] = synth.normal_bf16(synth.rng(ls, "q"), (B, Tq, 64, 512))
+            self.h["swa%d" % layer] = synth.normal_bf16(synth.rng(ls, "swa"), (B, S, 512))
             if mode != "reuse":
-                self.h["q_idx%d" % layer] = synth.normal_bf16(synth.rng(ls, "q_idx"), (B, 1, 32, 128))
+                self.h["q_idx%d" % layer] = synth.normal_bf16(synth.rng(ls, "q_idx"), (B, Tq, 32, 128))
         self.upload()
         self.merge_w = _dev(synth.merge_weights(synth.rng(s, "w"), r, 512), device)
         self.w_idx = _dev(synth.normal_bf16(synth.rng(s, "w_idx"), (512, 128), 1 / math.sqrt(512)), device)
-        self.n_entries = torch.full((B,), self.N - 1, dtype=torch.int32, device=device)
-        topk = torch.empty((B, 1, wl.topk), dtype=torch.int32, device=device)
-        pool = torch.empty((B, 1, wl.hsi_blocks), dtype=torch.int32, device=device)
-        ws = torch.empty(max(csa.index_workspace_bytes(self.cfg, B, 1, self.N),
-                             csa.index_workspace_bytes(self.cfg, B, 1, self.N, reindex=True)),
+        self.n_entries = torch.full((B,), ctx // r if Tq > 1 else self.N - 1, dtype=torch.int32, device=device)
+        topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device=device)
+        pool = torch.empty((B, Tq, wl.hsi_blocks), dtype=torch.int32, device=device) if wl.hsi else None
+        nq = min(B * Tq, 512)  # queries per indexer pass (the library runs longer chunks in passes)
+        ws = torch.empty(max(csa.index_workspace_bytes(self.cfg, 1, nq, self.N),
+                             csa.index_workspace_bytes(self.cfg, 1, nq, self.N, reindex=True)),
                          dtype=torch.uint8, device=device)
         self.state = csa.GroupState(self.main, self.idx, self.n_entries, self.N, topk, pool, ws, self.status)
-        self.outs = {l: torch.empty((B, 1, 64, 512), dtype=torch.float32, device=device) for l, _ in self.layers}
+        self.outs = {l: torch.empty((B, Tq, 64, 512), dtype=torch.float32, device=device) for l, _ in self.layers}
         self.out = self.outs[self.layers[-1][0]]
         self.stages = ["L%d_%s" % (l, m) for l, m in self.layers]
-        self.launches_per_step = sum({"full": 4, "reindex": 3, "reuse": 1}[m] for _, m in self.layers)
-        att = B * attend_query_bytes(wl.cache, wl.topk, wl.window)
-        self.stage_bytes = {}
+        chunks = -(-B * Tq // 512)
+        self.launches_per_step = sum({"full": 2 + 2 * chunks, "reindex": 1 + 2 * chunks, "reuse": 1}[m]
+                                     for _, m in self.layers)
+        att = B * Tq * attend_query_bytes(wl.cache, wl.topk, wl.window)
+        eb = idx_entry_bytes(wl)
+        self.stage_bytes, self.stage_flops = {}, {}
+        pairs = (sum(min((ctx + t - (r - 1)) // r + 1, self.N) for t in range(Tq)) * B if Tq > 1 else B * self.N)
         for l, m in self.layers:
-            extra = {"full": B * (self.N * 72 + r * 1024 + 360), "reindex": B * wl.hsi_blocks * 8 * 72,
-                     "reuse": 0}[m]
+            comp = B * (Tq // r if Tq > 1 else 1) * (r * 1024 + 360)
+            extra = {"full": B * self.N * eb + comp + (B * Tq * (8192 + 2048) if Tq > 1 else 0),
+                     "reindex": B * Tq * wl.hsi_blocks * 8 * eb, "reuse": 0}[m]
             self.stage_bytes["L%d_%s" % (l, m)] = att + extra
+            if Tq > 1 and m == "full":
+                self.stage_flops["L%d_%s" % (l, m)] = pairs * 8192
         self.stage_kernels = {st: {"full": "compress + score_tc + select + attend_rows",
                                    "reindex": "score_tc (gather) + select + attend_rows",
                                    "reuse": "attend_rows"}[st.split("_")[1]]
                               for st in self.stages}
-        self.units = B
+        self.units = B * Tq
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N, "layers": len(self.layers),
+                          "query_tokens": Tq,
                           "unit": "query token through the %d-layer group" % len(self.layers)}
 
     def calls(self, d):
@@ -444,6 +457,15 @@ class OracleStep:
             self.units = len(rows)
             self.sample = ("all %d query rows of one sequence's block plus its compressor" % wl.tq if wl.tq <= 8 else
                            "4 query rows (0, 2047, 2048, last) of the %d-token chunk plus its compressor" % wl.tq)
+            if wl.layers:  # the same rows through every layer of the group, each with its own inputs
+                self.per_layer = []
+                for layer, mode in wl.layers:
+                    ls = s * 1000 + layer
+                    self.per_layer.append((layer, mode,
+                                           synth.normal_bf16(synth.rng(ls, "q"), (1, wl.tq, 64, 512))[:, rows],
+                                           synth.normal_bf16(synth.rng(ls, "swa"), (1, S, 512)),
+                                           synth.normal_bf16(synth.rng(ls, "q_idx"), (1, wl.tq, 32, 128))[:, rows]))
+                self.sample += ", through the %d-layer group" % len(wl.layers)
         else:
             self.x = synth.normal_bf16(synth.rng(s, "x_step"), (B, r, 512))
             self.pos0 = np.full(B, ctx - r, np.int64)
@@ -477,7 +499,7 @@ class OracleStep:
         o.compress(self.x, self.pos0, self.w, self.w_idx, self.main, self.idx, wl.ratio, wl.theta)
         if wl.swa_fp8:
             self.swa[:, -1:] = o.swa_encode(self.swa_new)
-        if self.prefill or not wl.layers:
+        if not wl.layers:
             topk, _, _ = o.index_topk(self.idx, self.n_ent, self.q_idx, self.q_pos, wl.ratio, wl.topk,
                                       hsi_blocks=wl.hsi_blocks if wl.hsi else 0, want_pool=wl.hsi, q_fp4=wl.q_fp4)
             return o.attend(self.main, self.n_ent, self.q, topk, self.swa, self.swa_len, self.swa_pos0, self.q_pos,

@@ -145,6 +145,9 @@ WORKLOADS = {
     "encoder_group6_b8_ctx32768_r2_fp4": Workload(
         "encoder_group6_b8_ctx32768_r2_fp4", batch=8, ctx=32768, ratio=2, cache="fp4", theta=1e4, seed=5,
         layers=ENCODER_GROUP),
+    "encoder_group6_prefill_4096_on_1m_r2_fp4": Workload(
+        "encoder_group6_prefill_4096_on_1m_r2_fp4", batch=1, ctx=1048576, ratio=2, cache="fp4", theta=1e4, seed=9,
+        tq=4096, layers=ENCODER_GROUP),
 }
 
 

@@ -340,3 +340,64 @@ def test_multi_query_decode_block_every_row():
     err = P.attention_rel_err(out.cpu().numpy(), o_out)
     print("multi-query block: attention max row rel err %.3g over %d rows" % (err, B * Tq))
     assert err <= P.ATT_TOL
+
+
+def test_encoder_group_prefill_sampled_rows():
+    """The encoder macro block on a prefill chunk: 4096 tokens appended to a
+    1 M-token context, layer 2 Full (compress the chunk, index all 4096
+    positions causally) and layers 3-7 Reuse, each layer with its own query
+    and banded window; 5 query rows checked through all six layers."""
+    wl = synth.WORKLOADS["encoder_group6_prefill_4096_on_1m_r2_fp4"]
+    B, r, Tq, ctx, W = wl.batch, wl.ratio, wl.tq, wl.ctx, wl.window
+    N, P0 = (ctx + Tq) // r, ctx // r
+    pm, pi = _paged.cache_pair(B, N, D, wl.cache, wl.seed), _paged.cache_pair(B, N, CI, wl.cache, wl.seed + 1)
+    m, i = _prefix(wl, 0, P0)
+    om, oi = oracle.Cache(1, N, D, wl.cache), oracle.Cache(1, N, CI, wl.cache)
+    om.codes[0, :P0], om.scales[0, :P0] = m.codes[0], m.scales[0]
+    oi.codes[0, :P0], oi.scales[0, :P0] = i.codes[0], i.scales[0]
+    _paged.upload(pm, om)
+    _paged.upload(pi, oi)
+    cfg = _cfg(wl)
+    s = wl.seed
+    x = synth.normal_bf16(synth.rng(s, "x_chunk"), (B, Tq, D))
+    w = synth.merge_weights(synth.rng(s, "w"), r, D)
+    w_idx = synth.normal_bf16(synth.rng(s, "w_idx"), (D, CI), std=1 / math.sqrt(D))
+    S = W - 1 + Tq
+    swa_len, swa_pos0 = np.array([S], np.int32), np.array([ctx - W + 1], np.int64)
+    q_pos = (ctx + np.arange(Tq, dtype=np.int64)).reshape(1, Tq)
+    pos0 = np.array([ctx], np.int64)
+    n_ent = torch.full((B,), P0, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device="cuda")
+    ws = torch.empty(csa.index_workspace_bytes(cfg, 1, 512, N), dtype=torch.uint8, device="cuda")
+    state = csa.GroupState(pm, pi, n_ent, N, topk, None, ws, st)
+    rows = np.array([0, 1, 2047, 2048, Tq - 1])
+    n_arr = np.array([N], np.int32)
+    o_top = None
+    for layer, mode in wl.layers:
+        ls = s * 1000 + layer
+        q = synth.normal_bf16(synth.rng(ls, "q"), (B, Tq, 64, D))
+        swa = synth.normal_bf16(synth.rng(ls, "swa"), (B, S, D))
+        q_idx = synth.normal_bf16(synth.rng(ls, "q_idx"), (B, Tq, 32, CI)) if mode != "reuse" else None
+        out = torch.empty((B, Tq, 64, D), dtype=torch.float32, device="cuda")
+        kw = {}
+        if mode == "full":
+            kw = dict(x=_paged.dev(x), pos0=_paged.dev(pos0), merge_w=_paged.dev(w), w_idx=_paged.dev(w_idx))
+        csa.layer(cfg, {"full": csa.MODE_FULL, "reuse": csa.MODE_REUSE}[mode], state, _paged.dev(q_pos),
+                  _paged.dev(q), _paged.dev(swa), _paged.dev(swa_len), _paged.dev(swa_pos0), out,
+                  q_idx=None if q_idx is None else _paged.dev(q_idx), **kw)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        if mode == "full":
+            assert int(n_ent.item()) == N
+            diag = oracle.compress(x, pos0, w, w_idx, om, oi, r, wl.theta, diagnostics=True)
+            exc = _check_compress(om, oi, pm, pi, diag, pos0, r, Tq // r, wl.cache)
+            print("encoder group prefill compressor: %d near-boundary codes excused" % exc)
+            o_top, _, sc = oracle.index_topk(oi, n_arr, q_idx[:, rows], q_pos[:, rows], r, wl.topk, want_scores=True)
+            g_top = topk.cpu().numpy()[:, rows]
+            assert P.topk_mismatch(g_top.reshape(len(rows), -1), o_top.reshape(len(rows), -1),
+                                   sc.reshape(len(rows), -1), wl.topk, exact=False) == 0
+        o_out = oracle.attend(om, n_arr, q[:, rows], o_top, swa, swa_len, swa_pos0, q_pos[:, rows], W, SCALE)
+        err = P.attention_rel_err(out.cpu().numpy()[:, rows], o_out)
+        print("encoder group prefill L%d %s: attention max row rel err %.3g" % (layer, mode, err))
+        assert err <= P.ATT_TOL, (layer, err)

@@ -464,14 +464,30 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
   const int64_t p0 = (int64_t)kPer * threadIdx.x;
   float v[kPer];
   if (gpool) {
+    const bool al = ((uintptr_t)vals & 15u) == 0;
 #pragma unroll
     for (int h = 0; h < kPer / kHsiBlock; ++h) {
       const int64_t pb = (p0 >> 3) + h;  // pool slot; plain load: written by this CTA
       const int32_t blk = pb * kHsiBlock < n ? *reinterpret_cast<const volatile int32_t*>(gpool + pb) : -1;
+      const int64_t j0 = (int64_t)blk * kHsiBlock;
+      if (blk >= 0 && al && j0 + kHsiBlock <= nv_lim) {  // a whole visible block: two 16-byte loads
 #pragma unroll
-      for (int i = 0; i < kHsiBlock; ++i) {
-        const int64_t j = (int64_t)blk * kHsiBlock + i;
-        v[kHsiBlock * h + i] = (blk >= 0 && j < nv_lim) ? ld_score(vals + j) : __uint_as_float(kScoreInvalid);
+        for (int q = 0; q < kHsiBlock / 4; ++q) {
+          float4 f4;
+          asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(f4.x), "=f"(f4.y), "=f"(f4.z), "=f"(f4.w)
+                       : "l"(vals + j0 + 4 * q));
+          v[kHsiBlock * h + 4 * q] = f4.x;
+          v[kHsiBlock * h + 4 * q + 1] = f4.y;
+          v[kHsiBlock * h + 4 * q + 2] = f4.z;
+          v[kHsiBlock * h + 4 * q + 3] = f4.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kHsiBlock; ++i) {
+          const int64_t j = j0 + i;
+          v[kHsiBlock * h + i] = (blk >= 0 && j < nv_lim) ? ld_score(vals + j) : __uint_as_float(kScoreInvalid);
+        }
       }
     }
   } else if (((uintptr_t)vals & 15u) == 0 && p0 + kPer <= n) {

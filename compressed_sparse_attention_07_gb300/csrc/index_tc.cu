@@ -72,11 +72,12 @@ struct ScoreArgs {
   int32_t* status;
 };
 
-__device__ __forceinline__ uint32_t f16x2_scale(uint32_t sbyte) {
-  uint32_t r;
-  uint16_t pair = (uint16_t)(sbyte | (sbyte << 8));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
-  return r;
+// Two E4M3 scale bytes (low byte first) -> each as a broadcast f16x2 (exact).
+__device__ __forceinline__ void e4m3_pair_bcast(uint32_t two, uint32_t& lo2, uint32_t& hi2) {
+  uint32_t f;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f) : "h"((uint16_t)(two & 0xFFFFu)));
+  asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(lo2) : "r"(f));
+  asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(hi2) : "r"(f));
 }
 
 // Four bytes of packed E2M1 pairs -> four f16x2 (element 2i of a byte in the low half).
@@ -397,9 +398,17 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
         uint32_t d[32];
         tc::tmem_ld32(tc::taddr(tb, lane_base, dcol + 32 * q), d);
         tc::tmem_wait_ld();
-        float sc = 0.0f;
+        // four partial sums over heads h = 4i + j, added pairwise
+        float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (a.head_w) {
 #pragma unroll
-        for (int hh = 0; hh < kIdxHeads; ++hh) sc = fmaf(hw[q][hh], fmaxf(__uint_as_float(d[hh]), 0.0f), sc);
+          for (int hh = 0; hh < kIdxHeads; ++hh)
+            ps[hh & 3] = fmaf(hw[q][hh], fmaxf(__uint_as_float(d[hh]), 0.0f), ps[hh & 3]);
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < kIdxHeads; ++hh) ps[hh & 3] += fmaxf(__uint_as_float(d[hh]), 0.0f);
+        }
+        float sc = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         sc += 0.0f;
         const int qc = qc0 + q;
         const bool valid = kGather ? (gtab[ie * 128 + lt] >= 0) : (pos < nv[q]);
@@ -446,6 +455,15 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
         else
           sc = make_uint2(*reinterpret_cast<const uint32_t*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 4), 0u);
         if (!kGather) tc::mbar_arrive(&empty_bar[s]);
+        // the scales as broadcast f16x2: s2g[g] for 16-channel group g (or
+        // 32-channel group g with one scale per 32 channels)
+        uint32_t s2g[8];
+        e4m3_pair_bcast(sc.x, s2g[0], s2g[1]);
+        e4m3_pair_bcast(sc.x >> 16, s2g[2], s2g[3]);
+        if (kDtype == CSA2_CACHE_FP4) {
+          e4m3_pair_bcast(sc.y, s2g[4], s2g[5]);
+          e4m3_pair_bcast(sc.y >> 16, s2g[6], s2g[7]);
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // 32 channels -> 16 TMEM columns
           const uint32_t w4[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
@@ -453,9 +471,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
-            const uint32_t s2 = kDtype == CSA2_CACHE_FP4
-                                    ? f16x2_scale(((gg < 4 ? sc.x : sc.y) >> (8 * (gg & 3))) & 0xFFu)
-                                    : f16x2_scale((sc.x >> (8 * c)) & 0xFFu);  // 32-channel group c
+            const uint32_t s2 = kDtype == CSA2_CACHE_FP4 ? s2g[gg] : s2g[c];
             uint32_t h4[4];
             e2m1x8_to_f16x2(w4[q], h4);
 #pragma unroll

@@ -25,6 +25,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -182,6 +183,12 @@ class StepBase:
 
     def inputs_host(self):
         return self.h
+
+    def late_inputs(self):
+        """(index of the first call that reads them, input names): inputs the
+        first calls of a step do not read, so their upload can overlap them."""
+        calls = len(self.stages)
+        return calls - 1, {k for k in ("q", "swa", "swa_len", "swa_pos0") if k in self.h}
 
     def step(self, events=None, d=None):
         """Run the stages in order, recording events[i] before stage i and
@@ -388,6 +395,16 @@ class GroupStep(StepBase):
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N, "layers": len(self.layers),
                           "query_tokens": Tq,
                           "unit": "query token through the %d-layer group" % len(self.layers)}
+
+    def late_inputs(self):
+        """The per-layer inputs of every layer after the first."""
+        first = self.layers[0][0]
+        late = set()
+        for k in self.h:
+            m = re.fullmatch(r"(q|q_idx|swa)(\d+)", k)
+            if m and int(m.group(2)) != first:
+                late.add(k)
+        return 1, late
 
     def calls(self, d):
         csa = self.csa
@@ -683,32 +700,54 @@ def main():
     warm_ms = statistics.fmean(a.elapsed_time(b) for a, b in wev)
 
     # end to end through the Python API with host buffers: the step's inputs
-    # packed in one pinned host buffer and copied in with one H2D copy (the
-    # device tensors the API is called with are views of one staging
-    # buffer), the step, D2H of the attention output
+    # in two pinned host buffers, each copied in with one H2D copy (the
+    # device tensors the API is called with are views of two staging
+    # buffers): the inputs of the first calls on the step's stream, the rest
+    # (the attention's query and window rows) on a second stream so that
+    # their upload overlaps the first calls; the step; D2H of the output
     host_in = {k: np.ascontiguousarray(v.view(np.int16) if v.dtype == np.uint16 else v)
                for k, v in step.inputs_host().items()}
-    offs, total = {}, 0
-    for k, v in host_in.items():
-        offs[k] = total
-        total += (v.nbytes + 255) & ~255
-    hpack = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dpack = torch.empty(total, dtype=torch.uint8, device=dev)
-    dbuf = {}
-    for k, v in host_in.items():
-        hv = torch.from_numpy(v)
-        hpack[offs[k]:offs[k] + v.nbytes].copy_(hv.view(-1).view(torch.uint8))
-        dbuf[k] = dpack[offs[k]:offs[k] + v.nbytes].view(hv.dtype).view(hv.shape)
+    late_from, late_keys = step.late_inputs()
+    dbuf, packs, total = {}, [], 0
+    for group in ([k for k in host_in if k not in late_keys], [k for k in host_in if k in late_keys]):
+        offs, size = {}, 0
+        for k in group:
+            offs[k] = size
+            size += (host_in[k].nbytes + 255) & ~255
+        if not size:
+            packs.append(None)
+            continue
+        hpack = torch.empty(size, dtype=torch.uint8).pin_memory()
+        dpack = torch.empty(size, dtype=torch.uint8, device=dev)
+        for k in group:
+            hv = torch.from_numpy(host_in[k])
+            hpack[offs[k]:offs[k] + hv.numel() * hv.element_size()].copy_(hv.view(-1).view(torch.uint8))
+            dbuf[k] = dpack[offs[k]:offs[k] + hv.numel() * hv.element_size()].view(hv.dtype).view(hv.shape)
+        packs.append((hpack, dpack))
+        total += size
     hout = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = total
     d2h = hout.numel() * hout.element_size()
+    side = torch.cuda.Stream(device=dev)
+    late_ready = torch.cuda.Event()
+
     def e2e_step():
-        dpack.copy_(hpack, non_blocking=True)
-        o = step.step(d=dbuf)
-        hout.copy_(o, non_blocking=True)
+        main = torch.cuda.current_stream()
+        if packs[1] is not None:
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                packs[1][1].copy_(packs[1][0], non_blocking=True)
+                late_ready.record(side)
+        if packs[0] is not None:
+            packs[0][1].copy_(packs[0][0], non_blocking=True)
+        for i, c in enumerate(step.calls(dbuf)):
+            if i == late_from and packs[1] is not None:
+                main.wait_event(late_ready)
+            c()
+        hout.copy_(step.out, non_blocking=True)
 
     # recorded once through the package's public capture helper: one replay
-    # per step issues the H2D copy, the three library calls and the D2H copy
+    # per step issues the two H2D copies, the library calls and the D2H copy
     e2e = step.csa.capture(e2e_step)
     e2e_steps = max(3, min(args.steps, 50))
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
@@ -767,7 +806,8 @@ def main():
                 "roofline": roof, "cpu_baseline": cpu,
                 "e2e": {"value": ws * step.units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                        "launch": "csa.capture of one H2D copy, the step's API calls and one D2H copy",
+                        "launch": "csa.capture of the step: H2D of the first calls' inputs, the API calls with the "
+                                  "attention inputs' H2D overlapped on a second stream, one D2H copy",
                         "eager_value": ws * step.units / (e2e_eager_ms / 1e3)},
                 "gpu_launches": step.launches_per_step * args.steps, "clocks": clk}
         print(json.dumps(line), flush=True)

@@ -643,6 +643,7 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
 
 // grid (cs, queries, selections), clusters of cs CTAs along x.  Selection 0:
 // entry top-k (Full or Reindex); 1: HSI block pool (Full).
+template <bool kSmall>
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, int r, int k, int n_blocks,
                                                                 int64_t max_entries,
                                                                 const int64_t* __restrict__ q_pos,
@@ -685,7 +686,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
   __syncthreads();
   const uint32_t lo = r_lo, hi = r_hi;
   auto run = [&](const float* v, int64_t n, int kk, int64_t forced, IdMap idmap, int32_t* o) {
-    if (cs == 1 && n <= kRound)
+    if (kSmall)
+      select_small(v, n, kk, forced, idmap, o, lo, hi, s);
+    else if (cs == 1 && n <= kRound)
       select_small(v, n, kk, forced, idmap, o, lo, hi, s);
     else
       select_topk(v, n, kk, forced, idmap, o, lo, hi, s, cs, rk);
@@ -767,14 +770,18 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
   int cs = 1;
   while (!fused && cs < 8 && (int64_t)cs * kMinCtaKeys < n_max && 2 * cs * sel_groups <= num_sms()) cs <<= 1;
   const size_t sel_smem = sizeof(SelShared);
-  cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
+  // one CTA holding every position of each selection: the register-resident
+  // path only, compiled without the general one
+  const bool small = cs == 1 && (fused ? ((int64_t)max_entries + 7) / 8 <= kRound : n_max <= kRound);
+  auto sel = small ? select_kernel<true> : select_kernel<false>;
+  cudaFuncSetAttribute(sel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
   for (int q0 = 0; q0 < Q; q0 += chunk) {
     const int nq = std::min(chunk, Q - q0);
     int n_slots = 0;
     cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, scores,
                                     stride, bmax, krange, kr_stride, &n_slots, status, num_sms(), stream);
     if (e != cudaSuccess) return e;
-    e = launch_k(select_kernel, dim3(cs, nq, n_sel), dim3(kSelThreads), sel_smem, stream, cs,
+    e = launch_k(sel, dim3(cs, nq, n_sel), dim3(kSelThreads), sel_smem, stream, cs,
                  q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, (int64_t)max_entries, q_pos, n_entries, pool,
                  (const float*)scores, (const float*)bmax, stride, (const uint32_t*)krange, kr_stride, n_slots,
                  topk_out, pool_out, fused ? 1 : 0);

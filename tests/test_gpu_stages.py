@@ -450,3 +450,69 @@ def test_captured_index_and_attend_replay_on_new_data():
     assert int(st.item()) == 0
     assert torch.equal(got_top, topk)
     assert torch.equal(got_out, out)
+
+
+# ------------------------------------------------- larger configurations ----
+
+@pytest.mark.parametrize("dtype,k,W,B,Tq", [
+    ("fp4", 1024, 512, 2, 1),    # 12 row tiles: the head-split cluster kernel
+    ("bf16", 1024, 512, 2, 2),
+    ("fp4", 1024, 512, 40, 1),   # too many clusters for one wave: the per-query kernel
+    ("fp4", 768, 0, 3, 2),       # six tiles of top-k rows and no window
+    ("fp4", 640, 256, 3, 2),     # windows clipped at the sequence start
+])
+def test_attend_larger_selections_and_windows(dtype, k, W, B, Tq):
+    """The attention kernels for configurations beyond six row tiles (maximum
+    top-k 1024 and window 512) and without a window, against the oracle."""
+    N = 3000
+    oc, pc = _main_caches(B, N, dtype, seed=70 + k + W)
+    g = synth.rng(70, "ids%d" % k)
+    topk = np.full((B, Tq, k), -1, np.int32)
+    for b in range(B):
+        for t in range(Tq):
+            n = [k, k // 2, 7][(b + t) % 3]
+            topk[b, t, :n] = np.sort(g.choice(N, size=n, replace=False))
+    q = synth.normal_bf16(synth.rng(70, "q%d" % k), (B, Tq, HM, D))
+    S = max(W, 1) + Tq
+    swa = synth.normal_bf16(synth.rng(70, "swa%d" % k), (B, S, D))
+    swa_pos0 = np.zeros(B, np.int64)
+    swa_len = np.full(B, S, np.int32)
+    # positions: the window runs past the buffer start for some queries
+    q_pos = np.array([[min(S - 1, 3 + 200 * b + t * 50) for t in range(Tq)] for b in range(B)], np.int64)
+    n_ent = np.full(B, N, np.int32)
+    cfg = csa.Cfg(ratio=1, cache_dtype=csa.CACHE_FP4 if dtype == "fp4" else csa.CACHE_BF16, topk=k, window=W)
+    out = torch.empty((B, Tq, HM, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, Tq, HM), dtype=torch.float32, device="cuda")
+    st = _status()
+    csa.attend(cfg, _paged.dev(q), pc, _paged.dev(n_ent), _paged.dev(topk), _paged.dev(swa) if W else None,
+               _paged.dev(swa_len), _paged.dev(swa_pos0), _paged.dev(q_pos), out, lse=lse, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_out, o_lse = oracle.attend(oc, n_ent, q, topk, swa, swa_len if W else np.zeros(B, np.int32), swa_pos0, q_pos,
+                                 W, 1 / math.sqrt(D), want_lse=True)
+    err = P.attention_rel_err(out.cpu().numpy(), o_out)
+    assert err <= P.ATT_TOL, err
+    lg = lse.cpu().numpy()
+    fin = np.isfinite(o_lse)
+    assert np.array_equal(np.isfinite(lg), fin)
+    np.testing.assert_allclose(lg[fin], o_lse[fin], rtol=0, atol=1e-3)
+    print("attend %s k=%d W=%d B=%d Tq=%d: max row rel err %.3g" % (dtype, k, W, B, Tq, err))
+
+
+def test_index_maximum_topk_and_hsi_blocks_bit_exact():
+    """top-k 1024 with 4096 HSI blocks (the largest accepted), integer mode,
+    one sequence shorter than the pool, and Reindex over the largest pool."""
+    B, N, k, nb = 2, 40000, 1024, 4096
+    oc, pc = _idx_caches(B, N, "fp4", seed=71, integer=True, dup=True)
+    q_idx = synth.integer_bf16(synth.rng(71, "q"), (B, 1, H, CI), -1, 1)
+    q_pos = np.array([[N - 1], [20000]], np.int64)
+    n_ent = np.array([N, 30000], np.int32)
+    cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=nb)
+    g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+    o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, want_pool=True)
+    np.testing.assert_array_equal(g_top, o_top)
+    np.testing.assert_array_equal(g_pool, o_pool)
+    q2 = synth.integer_bf16(synth.rng(72, "q"), (B, 1, H, CI), -1, 1)
+    r_top, _ = _run_index(cfg, pc, q2, q_pos, n_ent, N, pool=o_pool)
+    o_rtop, _, _ = oracle.index_topk(oc, n_ent, q2, q_pos, r=1, k=k, hsi_blocks=nb, pool=o_pool)
+    np.testing.assert_array_equal(r_top, o_rtop)

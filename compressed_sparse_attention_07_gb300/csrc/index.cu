@@ -23,17 +23,19 @@ constexpr int kCandMax = 8192;        // keys of the threshold bin listed in sha
 constexpr int kMinCtaKeys = kRound;  // positions per CTA of a selection cluster, at least
                                      // (below that the cluster's merges cost more than they save)
 constexpr int kRankMax = 512;  // threshold-bin candidates ranked directly (else refined by digits)
+static_assert(kCandMax <= kHistBins, "one CTA keeps the listed keys' positions in the cluster histogram's space");
 
 struct SelShared {
   uint32_t keys[kRound];       // this CTA's keys of the current round (slots: kslot)
   uint32_t hist[kHistBins];    // this CTA's histogram (the cluster's peers read it)
-  uint32_t merged[kHistBins];  // the cluster's histogram
+  uint32_t merged[kHistBins];  // the cluster's histogram; one CTA: positions of the threshold-bin keys
   uint32_t cand[kCandMax];     // this CTA's keys of the threshold bin, minus kmin (peers read them)
-  uint32_t all[kRankMax];      // the cluster's threshold-bin keys
+  uint32_t all[kRankMax];      // the cluster's threshold-bin keys; one CTA: positions above the bin
   uint32_t part[kSelThreads];  // bin sums per thread (find_cut); rank counts per candidate
   uint32_t wsum[kSelWarps + 1];
   uint32_t cut_bin, cut_above, cut_total, cand_n, c_all, t_x, t_krem, carry_eq, carry_gt, grand;
   uint32_t tot_gt, tot_eq;     // this CTA's counts for the compaction (peers read them)
+  uint32_t above_n;
   uint32_t peer_off[9];
 };
 
@@ -147,6 +149,7 @@ __device__ __forceinline__ int kslot(int i) {
 //      from warp scans and one scan over the warps.
 // Keys are staged in shared memory a round of kRound positions at a time; a
 // range of at most kRound positions is read from global memory once.
+template <bool kOne>  // a single CTA (cs == 1)
 __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
                             uint32_t kmin, uint32_t kmax, SelShared& s, int cs, int rk) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -201,9 +204,15 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
     s.tot_eq = 0;
     s.carry_gt = 0;
     s.carry_eq = 0;
+    s.above_n = 0;
   }
   __syncthreads();
   uint32_t T = 0xFFFFFFFFu, krem = 0;  // select key > T, then the first krem keys == T
+  // one CTA whose threshold bin is listed: the listing pass also keeps the
+  // positions above the bin and of the bin's keys, and the selection is
+  // sorted out of shared memory instead of a compaction pass over the scores
+  bool kept = false;
+  uint32_t kept_x = 0;
   if (ranked) {
     for (int64_t base = 0; base < L; base += kRound) {
       if (base > 0) __syncthreads();
@@ -225,19 +234,35 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
       int rem = sh;
       krem = need - s.cut_above;
       const bool listed = s.hist[tb] <= (uint32_t)kCandMax;  // this CTA's share of the bin
+      kept = kOne && rem > 0 && listed && s.cut_above + (has_forced ? 1u : 0u) <= (uint32_t)kRankMax;
       if (rem > 0 && listed) {
         for (int64_t base = 0; base < L; base += kRound) {
           stage(base);
 #pragma unroll 4
           for (int j = 0; j < kPer; ++j) {
             const uint32_t kk = s.keys[kslot(threadIdx.x) + kSelThreads * j];
-            const bool m = kk != 0u && bin_of(kk) == tb;
+            const int64_t pos = lo + base + threadIdx.x + (int64_t)kSelThreads * j;
+            const uint32_t bn = bin_of(kk);
+            const bool m = kk != 0u && bn == tb;
             const uint32_t bal = __ballot_sync(0xffffffffu, m);
+            if (kOne && kept) {
+              const bool up = (kk != 0u && bn > tb) || pos == forced;
+              const uint32_t bu = __ballot_sync(0xffffffffu, up);
+              if (bu) {
+                uint32_t au = 0;
+                if (lane == 0) au = atomicAdd(&s.above_n, (uint32_t)__popc(bu));
+                au = __shfl_sync(0xffffffffu, au, 0);
+                if (up && au + __popc(bu & lt) < (uint32_t)kRankMax) s.all[au + __popc(bu & lt)] = (uint32_t)pos;
+              }
+            }
             if (!bal) continue;
             uint32_t at = 0;
             if (lane == 0) at = atomicAdd(&s.cand_n, (uint32_t)__popc(bal));
             at = __shfl_sync(0xffffffffu, at, 0);
-            if (m) s.cand[at + __popc(bal & lt)] = kk - kmin;
+            if (m) {
+              s.cand[at + __popc(bal & lt)] = kk - kmin;
+              if (kOne && kept) s.merged[at + __popc(bal & lt)] = (uint32_t)pos;
+            }
           }
         }
       }
@@ -336,10 +361,54 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
         rem = s2;
       }
       T = kmin + prefix;
+      kept_x = prefix;
     }
   } else if (resident) {
     load(0, false);
     __syncthreads();
+  }
+
+  if (kOne && kept) {
+    // every key of the bin equal to T is taken (else the ties straddle the
+    // threshold and the compaction pass orders them by position)
+    __syncthreads();
+    if (threadIdx.x == 0) s.grand = 0;
+    __syncthreads();
+    uint32_t eq = 0;
+    for (uint32_t i = threadIdx.x; i < s.cand_n; i += kSelThreads) eq += s.cand[i] == kept_x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) eq += __shfl_xor_sync(0xffffffffu, eq, o);
+    if (lane == 0 && eq) atomicAdd(&s.grand, eq);
+    __syncthreads();
+    kept = s.grand == krem && s.above_n == s.cut_above + (has_forced ? 1u : 0u);
+    __syncthreads();
+  }
+  if (kOne && kept) {
+    // the selection: the positions above the bin, then the bin's keys >= T,
+    // sorted by position (bitonic sort, one element per thread)
+    const uint32_t na = s.above_n;
+    s.keys[threadIdx.x] = threadIdx.x < na ? s.all[threadIdx.x] : 0xFFFFFFFFu;
+    if (threadIdx.x == 0) s.grand = na;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < s.cand_n; i += kSelThreads)
+      if (s.cand[i] >= kept_x) s.keys[atomicAdd(&s.grand, 1u)] = s.merged[i];
+    __syncthreads();
+    const uint32_t total = s.grand;  // need (+ the forced position) <= k
+    for (int k2 = 2; k2 <= kSelThreads; k2 <<= 1) {
+      for (int j = k2 >> 1; j > 0; j >>= 1) {
+        const int i = threadIdx.x, ixj = i ^ j;
+        if (ixj > i) {
+          const uint32_t x = s.keys[i], y = s.keys[ixj];
+          if ((x > y) == ((i & k2) == 0)) {
+            s.keys[i] = y;
+            s.keys[ixj] = x;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = threadIdx.x; i < k; i += kSelThreads) out[i] = (uint32_t)i < total ? idmap(s.keys[i]) : -1;
+    return;
   }
 
   // ---- ordered compaction: in a round, thread t owns keys kPer t .. kPer t + kPer - 1
@@ -691,7 +760,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
     else if (cs == 1 && n <= kRound)
       select_small(v, n, kk, forced, idmap, o, lo, hi, s);
     else
-      select_topk(v, n, kk, forced, idmap, o, lo, hi, s, cs, rk);
+      cs == 1 ? select_topk<true>(v, n, kk, forced, idmap, o, lo, hi, s, cs, rk)
+              : select_topk<false>(v, n, kk, forced, idmap, o, lo, hi, s, cs, rk);
   };
   if (fused) {
     // Full with HSI, one CTA: the pool first, then the top-k over the pool's

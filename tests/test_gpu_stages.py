@@ -516,3 +516,30 @@ def test_index_maximum_topk_and_hsi_blocks_bit_exact():
     r_top, _ = _run_index(cfg, pc, q2, q_pos, n_ent, N, pool=o_pool)
     o_rtop, _, _ = oracle.index_topk(oc, n_ent, q2, q_pos, r=1, k=k, hsi_blocks=nb, pool=o_pool)
     np.testing.assert_array_equal(r_top, o_rtop)
+
+
+@pytest.mark.parametrize("integer,k", [(True, 512), (False, 512), (True, 1024), (False, 97)])
+def test_select_many_queries_over_long_caches(integer, k):
+    """96 causal queries over 20000 entries: one CTA per selection holding
+    more positions than its registers (the staged path), whose threshold bin
+    is listed with the positions so the selection is sorted out of shared
+    memory; integer inputs with repeated entries make ties straddle the
+    threshold for some queries (then the compaction pass orders them)."""
+    B, N, Tq = 1, 20000, 96
+    oc, pc = _idx_caches(B, N, "fp4", seed=73 + k, integer=integer, dup=integer)
+    g = synth.rng(73, "q%d" % k)
+    q_idx = synth.integer_bf16(g, (B, Tq, H, CI), -1, 1) if integer else synth.normal_bf16(g, (B, Tq, H, CI))
+    q_pos = (N - 2 * Tq + 2 * np.arange(Tq)).reshape(1, Tq).astype(np.int64)  # ragged visibility, all > 16384
+    n_ent = np.array([N], np.int32)
+    cfg = csa.Cfg(ratio=1, topk=k)
+    g_top, _ = _run_index(cfg, pc, q_idx, q_pos, n_ent, N)
+    o_top, _, s = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, want_scores=True)
+    if integer:
+        np.testing.assert_array_equal(g_top, o_top)
+        ties = 0
+        for t in range(Tq):
+            v = np.sort(s[0, t][np.isfinite(s[0, t])])[::-1]
+            ties += v[k - 1] == v[k]
+        assert ties > 0
+    else:
+        assert P.topk_mismatch(g_top.reshape(Tq, k), o_top.reshape(Tq, k), s.reshape(Tq, -1), k, exact=False) == 0

@@ -31,14 +31,19 @@ namespace csa2 {
 namespace {
 
 // Consumer warpgroups: four on single-query FP4 tiles (latency-bound decode
-// and epilogue), two otherwise (TMEM and shared-memory budget).
+// and epilogue, the decoded K tile in TMEM); four on FP4 runs of 4 queries
+// with the decoded K tile in shared memory (TMEM then holds only the
+// accumulators, 4 x 128 columns); two otherwise (TMEM and shared-memory
+// budget).
 template <int kDtype, int QPC>
 struct Shape {
-  static constexpr int kWG = (QPC == 1 && kDtype != CSA2_CACHE_BF16) ? 4 : 2;
+  static constexpr bool kSmemA = QPC == 4 && kDtype != CSA2_CACHE_BF16;
+  static constexpr int kWG = ((QPC == 1 && kDtype != CSA2_CACHE_BF16) || kSmemA) ? 4 : 2;
   static constexpr int kConsumers = 128 * kWG;
   static constexpr int kThreads = kConsumers + 32;  // + one producer warp (page mode)
-  static constexpr int kStages = 2 * kWG;           // ring slots; warpgroup g owns slots g, g + kWG
+  static constexpr int kStages = kSmemA ? 6 : 2 * kWG;  // ring slots, used in tile order
 };
+constexpr int kABytes = 128 * kIdxDim * 2;  // a decoded K tile in shared memory (f16, K-major)
 constexpr uint32_t kSpin = 1u << 26;
 constexpr int kMaxTilesPerCta = 512;
 constexpr int kMaxGatherTiles = 32;        // gather mode: resolved positions held in shared memory
@@ -129,7 +134,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   auto pages_sync = [] { pages_sync_n<kThreads>(); };
   constexpr int kN = 32 * QPC;                    // MMA N: QPC queries x 32 heads
   constexpr int kAcols = 64;                      // 128 channels of f16 pairs
-  constexpr int kTmemCols = (kWG * kAcols + kWG * kN) <= 256 ? 256 : 512;
+  constexpr bool kSmemA = Shape<kDtype, QPC>::kSmemA;
+  constexpr int kTmemCols = ((kSmemA ? 0 : kWG * kAcols) + kWG * kN) <= 256 ? 256 : 512;
   constexpr bool kBf16 = (kDtype == CSA2_CACHE_BF16);
   constexpr uint32_t kIdesc = tc::idesc_f16(128, kN, kBf16, kBf16, false, false);
   static_assert(!kGather || QPC == 1, "gather mode scores one query per CTA");
@@ -139,6 +145,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* qtile = smem;                          // [kN rows][128] K-major, 256*kN B
   uint8_t* ring = smem + 256 * kN;                // kStages slots
+  uint8_t* abuf = ring + kStages * TileFmt<kDtype>::kSlotBytes;  // kSmemA: one K tile per warpgroup
   __shared__ float hw[QPC][kIdxHeads];
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], mma_bar[kWG];
   __shared__ uint32_t tmem_base;
@@ -338,7 +345,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   const int lt = tid & 127;              // entry of the tile, TMEM lane
   const uint32_t lane_base = 32 * (warp & 3);
   const uint32_t acol = (uint32_t)(g * kAcols);
-  const uint32_t dcol = (uint32_t)(kWG * kAcols + g * kN);
+  const uint32_t dcol = (uint32_t)((kSmemA ? 0 : kWG * kAcols) + g * kN);
+  uint8_t* atile = abuf + (size_t)g * kABytes;
   const int n_own = n_my > g ? (n_my - g + kWG - 1) / kWG : 0;
   uint32_t klo[QPC], khi[QPC];
 #pragma unroll
@@ -477,7 +485,14 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
 #pragma unroll
             for (int by = 0; by < 4; ++by) r16[q * 4 + by] = present ? hmul2(h4[by], s2) : 0u;
           }
-          tc::tmem_st16(tc::taddr(tb, lane_base, acol + 16 * c), r16);
+          if (kSmemA) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(atile + tc::kmajor_off(lt, 32 * c + 8 * q, kIdxDim)) =
+                  make_uint4(r16[4 * q], r16[4 * q + 1], r16[4 * q + 2], r16[4 * q + 3]);
+          } else {
+            tc::tmem_st16(tc::taddr(tb, lane_base, acol + 16 * c), r16);
+          }
         }
       } else {
 #pragma unroll
@@ -495,7 +510,10 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
         }
         if (!kGather) tc::mbar_arrive(&empty_bar[s]);
       }
-      tc::tmem_wait_st();
+      if (kSmemA)
+        tc::fence_async_smem();  // the K tile is read by the tensor core
+      else
+        tc::tmem_wait_st();
     }
     tc::fence_before_sync();
     wg_sync(g);
@@ -505,7 +523,11 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
 #pragma unroll
       for (int ks = 0; ks < kIdxDim / 16; ++ks) {
         const uint64_t bdesc = tc::sdesc(tc::smem_u32(qtile) + ks * 256, 128, kIdxDim * 16);
-        tc::mma_ts(tb + dcol, tb + acol + ks * 8, bdesc, kIdesc, ks > 0);
+        if (kSmemA)
+          tc::mma_ss(tb + dcol, tc::sdesc(tc::smem_u32(atile) + ks * 256, 128, kIdxDim * 16), bdesc, kIdesc,
+                     ks > 0);
+        else
+          tc::mma_ts(tb + dcol, tb + acol + ks * 8, bdesc, kIdesc, ks > 0);
       }
       tc::mma_commit(&mma_bar[g]);
     }
@@ -545,7 +567,7 @@ template <int kDtype, int QPC, bool kGather>
 static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaStream_t stream) {
   using F = TileFmt<kDtype>;
   using Sh = Shape<kDtype, QPC>;
-  size_t smem = 256 * 32 * QPC + (size_t)Sh::kStages * F::kSlotBytes;
+  size_t smem = 256 * 32 * QPC + (size_t)Sh::kStages * F::kSlotBytes + (Sh::kSmemA ? (size_t)Sh::kWG * kABytes : 0);
   // one CTA per SM: its TMEM allocation may take all 512 columns
   smem = std::max<size_t>(smem, 116 * 1024);
   auto kern = score_tc_kernel<kDtype, QPC, kGather>;

@@ -4,8 +4,10 @@
 // with one E4M3 scale per 16 channels, or per 32 for the 68-byte indexer
 // entry of hn.213312.xyz sec. 3.1).
 // (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.3.1 and sec. 2.4.4; 36kr "CSA2",
-// "FP4 and Bounded Replay".)  One CTA per new entry; this step moves a few KB
-// per entry, so it is latency-bound and kept simple.
+// "FP4 and Bounded Replay".)  Four CTAs per new entry: each merges, rotates
+// and encodes the entry (the first one stores it) and projects it onto 32 of
+// the 128 indexer channels, so each reads a quarter of W_idx.  The step moves
+// a few KB per entry: latency-bound and kept simple.
 #include <cmath>
 
 #include "internal.h"
@@ -25,18 +27,18 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
                                                        const uint16_t* __restrict__ w_idx, CacheView mc,
                                                        CacheView ic, int32_t* n_entries, int32_t* status) {
   __shared__ float e_s[kDim];          // the stored (decoded) entry
-  __shared__ float kpart[8][kIdxDim];  // projection partial sums, 8 row slices
-  const int m = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  __shared__ float kpart[32][32];  // projection partial sums: 32 row slices x this CTA's 32 columns
+  const int m = blockIdx.x, b = blockIdx.y, sx = blockIdx.z, t = threadIdx.x;
   griddep_wait();  // every input may be the previous kernel's output
   griddep_launch();
-  // the W_idx rows this thread needs (64 independent 8-byte loads), issued
-  // first: their latency overlaps the merge
-  const int kg = t & 31, rs = t >> 5;
-  uint2 wv[64];
+  // the W_idx rows this thread needs (16 independent 8-byte loads of this
+  // CTA's 32 columns), issued first: their latency overlaps the merge
+  const int kg = t & 7, rs = t >> 3;
+  uint2 wv[16];
   {
-    const uint2* w2 = reinterpret_cast<const uint2*>(w_idx) + kg;  // row c at + c * 32
+    const uint2* w2 = reinterpret_cast<const uint2*>(w_idx) + 8 * sx + kg;  // row c at + c * 32
 #pragma unroll
-    for (int i = 0; i < 64; ++i) wv[i] = __ldg(w2 + (rs * 64 + i) * (kIdxDim / 4));
+    for (int i = 0; i < 16; ++i) wv[i] = __ldg(w2 + (rs * 16 + i) * (kIdxDim / 4));
   }
   const int64_t j = pos0[b] / r + m;
   // both block-table lookups early, off the critical path of the projection
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
     int sc = e4m3_scale_code(amax);
     float s = e4m3_pos(sc);
     uint32_t c0 = e2m1_code(v0, s), c1 = e2m1_code(v1, s);
-    if (page >= 0) {
+    if (page >= 0 && sx == 0) {
       mc.data[page * kMainFp4Data + slot * (kDim / 2) + t] = (uint8_t)(c0 | (c1 << 4));
       if ((t & 7) == 0) mc.scales[page * kMainFp4Scales + slot * (kDim / 16) + (t >> 3)] = (uint8_t)sc;
     }
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
   } else {
     __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
     uint32_t packed = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-    if (page >= 0)
+    if (page >= 0 && sx == 0)
       reinterpret_cast<uint32_t*>(mc.data + page * kMainBf16Data + slot * (kDim * 2))[t] = packed;
     e_s[2 * t] = __bfloat162float(h0);
     e_s[2 * t + 1] = __bfloat162float(h1);
@@ -99,8 +101,8 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
   {
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float e = e_s[rs * 64 + i];
+    for (int i = 0; i < 16; ++i) {
+      const float e = e_s[rs * 16 + i];
       acc[0] = fmaf(e, __uint_as_float(wv[i].x << 16), acc[0]);
       acc[1] = fmaf(e, __uint_as_float(wv[i].x & 0xFFFF0000u), acc[1]);
       acc[2] = fmaf(e, __uint_as_float(wv[i].y << 16), acc[2]);
@@ -110,10 +112,11 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
     for (int q = 0; q < 4; ++q) kpart[rs][4 * kg + q] = acc[q];
   }
   __syncthreads();
-  if (t < kIdxDim) {
+  if (t < 32) {
     float kv = kpart[0][t];
 #pragma unroll
-    for (int q = 1; q < 8; ++q) kv += kpart[q][t];
+    for (int q = 1; q < 32; ++q) kv += kpart[q][t];
+    const int col = 32 * sx + t;  // indexer channel
     if (kDtype == CSA2_CACHE_FP4) {
       float amax = fabsf(kv);
 #pragma unroll
@@ -122,24 +125,24 @@ __global__ void __launch_bounds__(256) compress_kernel(int T, int r, RopeFreqs r
       uint32_t code = e2m1_code(kv, e4m3_pos(sc));
       uint32_t hi = __shfl_xor_sync(0xffffffffu, code, 1);
       if (ipage >= 0 && (t & 1) == 0) {
-        int bi = t >> 1;  // byte index 0..63 -> 16-byte chunk bi/16
+        int bi = col >> 1;  // byte index 0..63 -> 16-byte chunk bi/16
         ic.data[ipage * kIdxFp4Data + ((bi >> 4) * kPage + slot) * 16 + (bi & 15)] = (uint8_t)(code | (hi << 4));
       }
       if (kIdxS32) {
-        if (ipage >= 0 && (t & 31) == 0) ic.scales[ipage * kIdxS32Scales + slot * (kIdxDim / 32) + (t >> 5)] = (uint8_t)sc;
-      } else if (ipage >= 0 && (t & 15) == 0) {
-        ic.scales[ipage * kIdxFp4Scales + slot * (kIdxDim / 16) + (t >> 4)] = (uint8_t)sc;
+        if (ipage >= 0 && (col & 31) == 0) ic.scales[ipage * kIdxS32Scales + slot * (kIdxDim / 32) + (col >> 5)] = (uint8_t)sc;
+      } else if (ipage >= 0 && (col & 15) == 0) {
+        ic.scales[ipage * kIdxFp4Scales + slot * (kIdxDim / 16) + (col >> 4)] = (uint8_t)sc;
       }
     } else {
       uint16_t h = __bfloat16_as_ushort(__float2bfloat16_rn(kv));
       if (ipage >= 0) {
-        int byte = 2 * t;  // chunk byte/16
+        int byte = 2 * col;  // chunk byte/16
         *reinterpret_cast<uint16_t*>(ic.data + ipage * kIdxBf16Data + ((byte >> 4) * kPage + slot) * 16 +
                                      (byte & 15)) = h;
       }
     }
   }
-  if (m == gridDim.x - 1 && t == 0) n_entries[b] = (int32_t)(j + 1);
+  if (m == gridDim.x - 1 && t == 0 && sx == 0) n_entries[b] = (int32_t)(j + 1);
 }
 
 }  // namespace
@@ -150,7 +153,7 @@ cudaError_t launch_compress(const csa2_cfg& cfg, int B, int T, const uint16_t* x
                             cudaStream_t stream) {
   const int M = T / cfg.ratio;
   if (M == 0 || B == 0) return cudaSuccess;
-  dim3 grid(M, B);
+  dim3 grid(M, B, 4);  // 4 CTAs per entry: 32 indexer channels each
   RopeFreqs rf;
   for (int i = 0; i < kRope / 2; ++i) rf.f[i] = std::pow(cfg.rope_theta, -2.0 * i / kRope);
   if (idx_dtype(cfg) == CSA2_CACHE_FP4_S32)

@@ -149,6 +149,142 @@ __device__ __forceinline__ int kslot(int i) {
 //      from warp scans and one scan over the warps.
 // Keys are staged in shared memory a round of kRound positions at a time; a
 // range of at most kRound positions is read from global memory once.
+// One CTA over n positions far beyond its registers, with the query's key
+// range known: a 1/16 sample of the keys (one 128-byte block in 16) picks a
+// bin low enough that about twice the needed keys lie at or above it, one
+// pass over the scores lists those keys with their positions, and the
+// selection is finished among them in shared memory: the exact threshold bin
+// by their histogram, the threshold key by ranking the bin's keys, the
+// positions sorted.  Returns false, with nothing written, when the sample
+// missed (too few or too many keys listed), the threshold bin holds too many
+// keys to rank, or ties straddle the threshold; the caller then runs the
+// general passes.  Every decision is taken from shared memory (uniform).
+__device__ bool select_sampled(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
+                               uint32_t kmin, int sh, uint32_t need, SelShared& s) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  auto bin_of = [&](uint32_t kk) -> uint32_t {
+    const uint32_t x = kk > kmin ? kk - kmin : 0u;
+    return min(x >> sh, (uint32_t)(kHistBins - 1));
+  };
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
+  if (threadIdx.x == 0) {
+    s.cand_n = 0;
+    s.above_n = 0;
+  }
+  __syncthreads();
+  // ---- the sample: block b of 32 keys at positions 512 b .. 512 b + 31
+  const int64_t nsb = (n + 511) / 512;
+  for (int64_t b = wid; b < nsb; b += kSelWarps) {
+    const int64_t p = 512 * b + lane;
+    const uint32_t kk = (p < n && p != forced) ? order_key(ld_score(vals + p)) : 0u;
+    if (kk) atomicAdd(&s.hist[bin_of(kk)], 1u);
+  }
+  __syncthreads();
+  const uint32_t target = (2 * need + 1024) / 16 + 32;
+  find_cut(s.hist, kHistBins, target, s);
+  const uint32_t tb_lo = s.cut_total >= target ? s.cut_bin : 0u;
+  __syncthreads();
+  // ---- one pass: every key in a bin >= tb_lo, with its position
+  for (int64_t base = 0; base < n; base += kRound) {
+    float v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int64_t p = base + threadIdx.x + kSelThreads * j;
+      v[j] = p < n ? ld_score(vals + p) : __uint_as_float(kScoreInvalid);
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int64_t p = base + threadIdx.x + kSelThreads * j;
+      const uint32_t kk = p == forced ? 0u : order_key(v[j]);
+      const bool m = kk != 0u && bin_of(kk) >= tb_lo;
+      const uint32_t bal = __ballot_sync(0xffffffffu, m);
+      if (!bal) continue;
+      uint32_t at = 0;
+      if (lane == 0) at = atomicAdd(&s.cand_n, (uint32_t)__popc(bal));
+      at = __shfl_sync(0xffffffffu, at, 0) + __popc(bal & lt);
+      if (m && at < (uint32_t)kCandMax) {
+        s.cand[at] = kk - kmin;
+        s.merged[at] = (uint32_t)p;
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t c = s.cand_n;
+  if (c < need || c > (uint32_t)kCandMax) return false;
+  // ---- the exact threshold bin among the listed keys
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < c; i += kSelThreads) atomicAdd(&s.hist[bin_of(s.cand[i] + kmin)], 1u);
+  __syncthreads();
+  find_cut(s.hist, kHistBins, need, s);
+  uint32_t tx = 0;  // take every listed key x > tx, and the keys x == tx
+  if (s.cut_total > need) {
+    const uint32_t tb = s.cut_bin, krem = need - s.cut_above, cb = s.hist[tb];
+    if (cb > (uint32_t)kRankMax) return false;
+    // the bin's keys into s.all, then each ranked among them (tpc threads each)
+    if (threadIdx.x == 0) s.c_all = 0;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < c; i += kSelThreads) {
+      const uint32_t x = s.cand[i];
+      if (bin_of(x + kmin) == tb) s.all[atomicAdd(&s.c_all, 1u)] = x;
+    }
+    __syncthreads();
+    const uint32_t tpc = max(1u, (uint32_t)kSelThreads / cb);
+    for (uint32_t i = threadIdx.x; i < cb; i += kSelThreads) s.part[i] = 0;
+    __syncthreads();
+    if (threadIdx.x < cb * tpc) {
+      const uint32_t i = threadIdx.x % cb, part = threadIdx.x / cb;
+      const uint32_t x = s.all[i];
+      uint32_t gt = 0, eq = 0;
+      for (uint32_t j = part; j < cb; j += tpc) {
+        const uint32_t y = s.all[j];
+        gt += y > x;
+        eq += y == x;
+      }
+      atomicAdd(&s.part[i], gt | (eq << 16));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s.grand = 0;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < cb; i += kSelThreads) {
+      const uint32_t gt = s.part[i] & 0xFFFFu, eq = s.part[i] >> 16;
+      if (gt < krem && krem <= gt + eq) {  // the same key for every such i
+        s.t_x = s.all[i];
+        s.grand = (gt + eq == krem) ? 1u : 0u;  // every key equal to it is taken
+      }
+    }
+    __syncthreads();
+    if (!s.grand) return false;  // ties straddle the threshold
+    tx = s.t_x;
+  }
+  // ---- the selection (need keys, and the forced position), sorted by position
+  if (threadIdx.x == 0) s.grand = 0;
+  s.keys[threadIdx.x] = 0xFFFFFFFFu;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < c; i += kSelThreads)
+    if (s.cand[i] >= tx) s.keys[atomicAdd(&s.grand, 1u)] = s.merged[i];
+  __syncthreads();
+  if (threadIdx.x == 0 && forced >= 0) s.keys[s.grand++] = (uint32_t)forced;
+  __syncthreads();
+  const uint32_t total = s.grand;
+  for (int k2 = 2; k2 <= kSelThreads; k2 <<= 1) {
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      const int i = threadIdx.x, ixj = i ^ j;
+      if (ixj > i) {
+        const uint32_t x = s.keys[i], y = s.keys[ixj];
+        if ((x > y) == ((i & k2) == 0)) {
+          s.keys[i] = y;
+          s.keys[ixj] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < k; i += kSelThreads) out[i] = (uint32_t)i < total ? idmap(s.keys[i]) : -1;
+  return true;
+}
+
 template <bool kOne>  // a single CTA (cs == 1)
 __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
                             uint32_t kmin, uint32_t kmax, SelShared& s, int cs, int rk) {
@@ -197,6 +333,10 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
     __syncthreads();
   };
 
+  if (kOne && !resident && ranked && n >= 8 * (int64_t)kRound) {
+    if (select_sampled(vals, n, k, forced, idmap, out, kmin, sh, need, s)) return;
+    __syncthreads();  // the general passes reuse the shared memory
+  }
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
   if (threadIdx.x == 0) {
     s.cand_n = 0;

@@ -543,3 +543,25 @@ def test_select_many_queries_over_long_caches(integer, k):
         assert ties > 0
     else:
         assert P.topk_mismatch(g_top.reshape(Tq, k), o_top.reshape(Tq, k), s.reshape(Tq, -1), k, exact=False) == 0
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_select_sampled_pass_over_very_long_caches(integer):
+    """80 causal queries over 140000 entries: one CTA per selection over more
+    than eight rounds of positions, where a 1/16 sample of the keys picks the
+    bin above which the selection is listed in one pass.  Integer inputs with
+    repeated entries make ties straddle the threshold for some queries (the
+    general passes then take over) and must still match bit for bit."""
+    B, N, Tq, k = 1, 140000, 80, 512
+    oc, pc = _idx_caches(B, N, "fp4", seed=77, integer=integer, dup=integer)
+    g = synth.rng(77, "q")
+    q_idx = synth.integer_bf16(g, (B, Tq, H, CI), -1, 1) if integer else synth.normal_bf16(g, (B, Tq, H, CI))
+    q_pos = (N - 3 * Tq + 3 * np.arange(Tq)).reshape(1, Tq).astype(np.int64)
+    n_ent = np.array([N], np.int32)
+    cfg = csa.Cfg(ratio=1, topk=k)
+    g_top, _ = _run_index(cfg, pc, q_idx, q_pos, n_ent, N)
+    o_top, _, s = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, want_scores=True)
+    if integer:
+        np.testing.assert_array_equal(g_top, o_top)
+    else:
+        assert P.topk_mismatch(g_top.reshape(Tq, k), o_top.reshape(Tq, k), s.reshape(Tq, -1), k, exact=False) == 0

@@ -333,7 +333,7 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
     __syncthreads();
   };
 
-  if (kOne && !resident && ranked && n >= 8 * (int64_t)kRound) {
+  if (kOne && !resident && ranked && n >= 2 * (int64_t)kRound && need <= 2048u) {
     if (select_sampled(vals, n, k, forced, idmap, out, kmin, sh, need, s)) return;
     __syncthreads();  // the general passes reuse the shared memory
   }

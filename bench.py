@@ -69,6 +69,12 @@ def attend_query_bytes(cache, topk=512, window=128, row_bytes=1024):
     return topk * MAIN_ENTRY_BYTES[cache] + window * row_bytes + 64 * 512 * 2 + 64 * 512 * 4 + topk * 4
 
 
+def index_chunk(per_query_bytes: int, queries: int, budget: int = 16 << 30) -> int:
+    """Queries per indexer pass: all of them when their workspace fits the
+    budget (one score and one selection launch), else as many as fit."""
+    return max(1, min(queries, budget // max(per_query_bytes, 1)))
+
+
 def idx_entry_bytes(wl):
     return 68 if wl.idx68 else IDX_ENTRY_BYTES[wl.cache]
 
@@ -309,10 +315,11 @@ class PrefillStep(StepBase):
         self.topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device=device)
         self.pool = None
         per_q = csa.index_workspace_bytes(self.cfg, 1, 1, self.N)
-        self.ws = torch.empty(per_q * min(B * Tq, 512), dtype=torch.uint8, device=device)
+        self.chunk = index_chunk(per_q, B * Tq)
+        self.ws = torch.empty(per_q * self.chunk, dtype=torch.uint8, device=device)
         self.out = torch.empty((B, Tq, 64, 512), dtype=torch.float32, device=device)
         self.stages = ["compress", "index_topk", "attend"]
-        chunks = -(-B * Tq // 512)
+        chunks = -(-B * Tq // self.chunk)
         self.launches_per_step = 1 + 2 * chunks + 1
         pairs = sum(min((ctx + t - (r - 1)) // r + 1, self.N) for t in range(Tq)) * B
         self.stage_bytes = {"compress": B * (Tq // r) * (r * 1024 + 360),
@@ -365,7 +372,7 @@ class GroupStep(StepBase):
         self.n_entries = torch.full((B,), ctx // r if Tq > 1 else self.N - 1, dtype=torch.int32, device=device)
         topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device=device)
         pool = torch.empty((B, Tq, wl.hsi_blocks), dtype=torch.int32, device=device) if wl.hsi else None
-        nq = min(B * Tq, 512)  # queries per indexer pass (the library runs longer chunks in passes)
+        nq = index_chunk(csa.index_workspace_bytes(self.cfg, 1, 1, self.N), B * Tq)  # queries per indexer pass
         ws = torch.empty(max(csa.index_workspace_bytes(self.cfg, 1, nq, self.N),
                              csa.index_workspace_bytes(self.cfg, 1, nq, self.N, reindex=True)),
                          dtype=torch.uint8, device=device)
@@ -373,7 +380,7 @@ class GroupStep(StepBase):
         self.outs = {l: torch.empty((B, Tq, 64, 512), dtype=torch.float32, device=device) for l, _ in self.layers}
         self.out = self.outs[self.layers[-1][0]]
         self.stages = ["L%d_%s" % (l, m) for l, m in self.layers]
-        chunks = -(-B * Tq // 512)
+        chunks = -(-B * Tq // nq)
         self.launches_per_step = sum({"full": 2 + 2 * chunks, "reindex": 1 + 2 * chunks, "reuse": 1}[m]
                                      for _, m in self.layers)
         att = B * Tq * attend_query_bytes(wl.cache, wl.topk, wl.window)

@@ -259,7 +259,7 @@ def test_prefill_chunk_sampled_rows():
     n_ent = torch.full((B,), P0, dtype=torch.int32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device="cuda")
-    ws = torch.empty(csa.index_workspace_bytes(cfg, 1, 1, N) * 512, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(csa.index_workspace_bytes(cfg, 1, Tq, N), dtype=torch.uint8, device="cuda")  # one pass, as timed
     out = torch.empty((B, Tq, 64, D), dtype=torch.float32, device="cuda")
     csa.compress(cfg, _paged.dev(x), _paged.dev(pos0), _paged.dev(w), _paged.dev(w_idx), pm, pi, n_ent, status=st)
     csa.index_topk(cfg, _paged.dev(q_idx), _paged.dev(q_pos), pi, n_ent, N, topk, ws, status=st)
@@ -369,7 +369,7 @@ def test_encoder_group_prefill_sampled_rows():
     n_ent = torch.full((B,), P0, dtype=torch.int32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     topk = torch.empty((B, Tq, wl.topk), dtype=torch.int32, device="cuda")
-    ws = torch.empty(csa.index_workspace_bytes(cfg, 1, 512, N), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(csa.index_workspace_bytes(cfg, 1, Tq, N), dtype=torch.uint8, device="cuda")  # one pass, as timed
     state = csa.GroupState(pm, pi, n_ent, N, topk, None, ws, st)
     rows = np.array([0, 1, 2047, 2048, Tq - 1])
     n_arr = np.array([N], np.int32)

@@ -565,3 +565,44 @@ def test_select_sampled_pass_over_very_long_caches(integer):
         np.testing.assert_array_equal(g_top, o_top)
     else:
         assert P.topk_mismatch(g_top.reshape(Tq, k), o_top.reshape(Tq, k), s.reshape(Tq, -1), k, exact=False) == 0
+
+
+def test_degenerate_queries_nothing_visible_and_no_rows():
+    """Queries before the first complete group (nothing visible: the top-k
+    is all -1 and the pool empty), a context shorter than k and than the
+    pool, and attention with neither selected entries nor window rows
+    (output zero, LSE -inf), against the oracle."""
+    B, N, k, nb = 2, 40, 64, 16
+    oc, pc = _idx_caches(B, N, "fp4", seed=79, integer=True, dup=True)
+    q_idx = synth.integer_bf16(synth.rng(79, "q"), (B, 3, H, CI), -1, 1)
+    q_pos = np.array([[0, 1, 2 * N - 1], [0, 5, 30]], np.int64)  # r = 2: position 0 sees nothing
+    n_ent = np.array([N, 17], np.int32)
+    cfg = csa.Cfg(ratio=2, topk=k, hsi_blocks=nb)
+    g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+    o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=2, k=k, hsi_blocks=nb, want_pool=True)
+    np.testing.assert_array_equal(g_top, o_top)
+    np.testing.assert_array_equal(g_pool, o_pool)
+    assert (g_top[:, 0] == -1).all() and (g_pool[:, 0] == -1).all()
+    # attention: query 0 of each sequence has no entry and (swa_len 0) no window row
+    om, pm = _main_caches(B, N, "fp4", seed=79)
+    q = synth.normal_bf16(synth.rng(79, "qa"), (B, 3, HM, D))
+    swa = synth.normal_bf16(synth.rng(79, "swa"), (B, 8, D))
+    swa_len = np.array([0, 8], np.int32)
+    swa_pos0 = np.array([0, 23], np.int64)
+    W = 8
+    acfg = csa.Cfg(ratio=2, topk=k, window=W)
+    out = torch.empty((B, 3, HM, D), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, 3, HM), dtype=torch.float32, device="cuda")
+    st = _status()
+    csa.attend(acfg, _paged.dev(q), pm, _paged.dev(n_ent), _paged.dev(o_top), _paged.dev(swa), _paged.dev(swa_len),
+               _paged.dev(swa_pos0), _paged.dev(q_pos), out, lse=lse, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_out, o_lse = oracle.attend(om, n_ent, q, o_top, swa, swa_len, swa_pos0, q_pos, W, 1 / math.sqrt(D),
+                                 want_lse=True)
+    g_out, g_lse = out.cpu().numpy(), lse.cpu().numpy()
+    assert (g_out[0, 0] == 0).all() and np.isneginf(g_lse[0, 0]).all()  # nothing to attend to
+    assert np.array_equal(np.isfinite(g_lse), np.isfinite(o_lse))
+    fin = np.isfinite(o_lse)
+    np.testing.assert_allclose(g_lse[fin], o_lse[fin], rtol=0, atol=1e-3)
+    assert P.attention_rel_err(g_out[:, 1:], o_out[:, 1:]) <= P.ATT_TOL

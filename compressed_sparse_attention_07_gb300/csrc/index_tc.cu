@@ -6,21 +6,22 @@
 // range of 128-entry tiles of one group of up to QPC queries of one sequence
 // (a multi-query decode block of up to 6 positions shares one group, so every
 // indexer-K tile is read once for all of them).
-//  - page mode (Full): warp 8 (one elected lane) streams whole cache pages,
-//    two per tile, into a shared-memory ring with 1-D bulk copies completing
-//    on mbarriers;
+//  - page mode (Full): the warp after the consumers (one elected lane)
+//    streams whole cache pages, two per tile, into a shared-memory ring with
+//    1-D bulk copies completing on mbarriers;
 //  - gather mode (Reindex): each thread gathers its own entry of the pool
 //    with cp.async into the same ring layout (block ids resolved to pages
 //    once at set-up);
-//  - two consumer warpgroups take alternate tiles; thread t of a warpgroup
-//    owns entry t of the tile and TMEM lane t: it decodes the entry (FP4 ->
-//    f16, exact; bf16 kept), stores it to its warpgroup's TMEM A buffer, and
-//    one thread issues tcgen05.mma D[128 x 32*QPC] = K_tile . Q^T with Q_idx
-//    (f16 / bf16) from shared memory;
+//  - the consumer warpgroups (two to four, see Shape) take tiles in turn;
+//    thread t of a warpgroup owns entry t of the tile and TMEM lane t: it
+//    decodes the entry (FP4 -> f16, exact; bf16 kept) into its warpgroup's
+//    A buffer (TMEM, or shared memory for runs of 4 queries), and one thread
+//    issues tcgen05.mma D[128 x 32*QPC] = K_tile . Q^T with Q_idx (f16 /
+//    bf16) from shared memory;
 //  - the epilogue reads D back (one row per thread), forms the ReLU-weighted
 //    head sums, writes the scores, the 8-entry block maxima for HSI and folds
 //    this CTA's key range per query (one slot each) for the top-k selection.
-// A warpgroup decodes its next tile while its previous MMA runs, and the two
+// A warpgroup decodes its next tile while its previous MMA runs, and the
 // warpgroups interleave on the tensor core.  Every wait is bounded.
 #include <algorithm>
 

@@ -1,13 +1,25 @@
 // a7 -- CSA2 sparse attention on the tensor cores.
 //
-// For one query token and a group of HG heads: rows E = the selected main-KV
-// entries followed by the window rows; logits l = scale * q_h . c_e; one
-// softmax per head over E; out_h = sum_e p_e c_e, the same 512-channel latent
-// serving as key and value (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.2.2 and
-// sec. 3.3.1; 36kr "CSA2").
+// For one query token: rows E = the selected main-KV entries followed by the
+// window rows; logits l = scale * q_h . c_e; one softmax per head over E;
+// out_h = sum_e p_e c_e, the same 512-channel latent serving as key and value
+// (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.2.2 and sec. 3.3.1; 36kr "CSA2").
 //
-// Rows are processed in tiles of 128 (top-k tiles, then window tiles, each
-// padded to 128 rows) and 128-channel chunks:
+// Three kernels, chosen by the number of 128-row tiles (top-k tiles, then
+// window tiles):
+//  - attend_rows_kernel (up to 6 tiles, the model's 512 + 128): one CTA per
+//    (query, tile) for all 64 heads, the query's tiles in one cluster; each
+//    CTA gathers and decodes its rows once, computes S = C.Q^T, a partial
+//    softmax and O = C^T.P^T on the tensor cores, and the partial outputs
+//    are merged through distributed shared memory (the only kernel that
+//    reads MXFP8 window rows);
+//  - attend_split_kernel (up to 16 tiles, few queries): the same with 16
+//    heads per CTA;
+//  - attend_tc_kernel (otherwise): one CTA per (query, group of HG heads)
+//    over all of the query's tiles, described below.
+//
+// attend_tc_kernel processes the rows in tiles of 128 (each padded to 128
+// rows) and 128-channel chunks:
 //  - thread r of the CTA owns row r of every tile: it gathers that row into
 //    a shared-memory staging ring with 16-byte cp.async copies, several units
 //    ahead (whole FP4 rows, 256 B codes + 32 B scales, per top-k tile;

@@ -26,8 +26,15 @@ bool cfg_supported(const csa2_cfg* c, int32_t* err) {
   return true;
 }
 
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Alignment the kernels' loads and stores need of a pointer (null passes:
+// presence is checked separately).
+bool al(const void* p, size_t a) { return !p || aligned(p, a); }
+
 bool cache_ok(const csa2_cache* c, int channels, int dtype) {
   if (!c || !c->data || !c->block_table || c->max_pages <= 0 || c->num_pages <= 0 || c->reserved != 0) return false;
+  if (!al(c->block_table, 4)) return false;
   if (c->channels != channels) return false;
   if (dtype != CSA2_CACHE_BF16 && !c->scales) return false;
   // 16-byte alignment of the page bases (128-bit loads)
@@ -37,8 +44,6 @@ bool cache_ok(const csa2_cache* c, int channels, int dtype) {
 }
 
 int32_t cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
 
@@ -86,7 +91,9 @@ int32_t csa2_compress(const csa2_cfg* cfg, int32_t B, int32_t T, const uint16_t*
   if (!cfg_supported(cfg, &err)) return err;
   if (B < 0 || T < 0 || T % cfg->ratio) return CSA2_ERR_INVALID_ARG;
   if (B == 0 || T == 0) return CSA2_OK;
-  if (!x || !pos0 || !merge_w || !w_idx || !n_entries || !aligned(x, 4)) return CSA2_ERR_INVALID_ARG;
+  if (!x || !pos0 || !merge_w || !w_idx || !n_entries) return CSA2_ERR_INVALID_ARG;
+  if (!al(x, 4) || !al(pos0, 8) || !al(merge_w, 4) || !al(w_idx, 8) || !al(n_entries, 4) || !al(status, 4))
+    return CSA2_ERR_INVALID_ARG;
   if (!cache_ok(main_cache, kDim, cfg->cache_dtype) || !cache_ok(idx_cache, kIdxDim, idx_dtype(*cfg)))
     return CSA2_ERR_INVALID_ARG;
   return cuda_status(launch_compress(*cfg, B, T, x, pos0, merge_w, w_idx, *main_cache, *idx_cache, n_entries, status,
@@ -108,6 +115,9 @@ int32_t csa2_index_topk(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16
   if (B < 0 || Tq < 0 || max_entries < 0) return CSA2_ERR_INVALID_ARG;
   if (B == 0 || Tq == 0) return CSA2_OK;
   if (!q_idx || !q_pos || !n_entries || !topk_out || !workspace) return CSA2_ERR_INVALID_ARG;
+  if (!al(q_idx, 16) || !al(head_w, 4) || !al(q_pos, 8) || !al(n_entries, 4) || !al(pool, 4) || !al(topk_out, 4) ||
+      !al(pool_out, 4) || !al(status, 4))
+    return CSA2_ERR_INVALID_ARG;
   if (!cache_ok(idx_cache, kIdxDim, idx_dtype(*cfg))) return CSA2_ERR_INVALID_ARG;
   if ((int64_t)max_entries > (int64_t)idx_cache->max_pages * kPage) return CSA2_ERR_CAPACITY;
   if (pool && pool_out) return CSA2_ERR_INVALID_ARG;
@@ -128,6 +138,9 @@ int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* 
   if (B < 0 || Tq < 0 || S < 0) return CSA2_ERR_INVALID_ARG;
   if (B == 0 || Tq == 0) return CSA2_OK;
   if (!q || !n_entries || !topk || !q_pos || !out) return CSA2_ERR_INVALID_ARG;
+  if (!al(q, 16) || !al(n_entries, 4) || !al(topk, 4) || !al(swa_len, 4) || !al(swa_pos0, 8) || !al(q_pos, 8) ||
+      !al(out, 16) || !al(lse, 4) || !al(status, 4))
+    return CSA2_ERR_INVALID_ARG;
   if (cfg->window > 0 && (!swa || !swa_len || !swa_pos0 || S == 0 || !aligned(swa, 16))) return CSA2_ERR_INVALID_ARG;
   if (!cache_ok(main_cache, kDim, cfg->cache_dtype)) return CSA2_ERR_INVALID_ARG;
   if (!(scale == scale)) return CSA2_ERR_INVALID_ARG;
@@ -145,7 +158,7 @@ int32_t csa2_gather_dequant(const csa2_cache* cache, int32_t cache_dtype, int32_
   if (!cache_ok(cache, cache->channels, cache_dtype)) return CSA2_ERR_INVALID_ARG;
   if (B < 0 || n < 0) return CSA2_ERR_INVALID_ARG;
   if (B == 0 || n == 0) return CSA2_OK;
-  if (!ids || !out) return CSA2_ERR_INVALID_ARG;
+  if (!ids || !out || !al(ids, 4) || !al(out, 4) || !al(status, 4)) return CSA2_ERR_INVALID_ARG;
   return cuda_status(launch_gather_dequant(*cache, cache_dtype, B, n, ids, out, status, static_cast<cudaStream_t>(stream)));
 }
 
@@ -153,7 +166,8 @@ int32_t csa2_swa_encode(int32_t B, int32_t T, const uint16_t* x, const int64_t* 
                         int32_t* status, void* stream) {
   if (B < 0 || T < 0 || S < 0) return CSA2_ERR_INVALID_ARG;
   if (B == 0 || T == 0) return CSA2_OK;
-  if (!x || !row0 || !rows || !aligned(x, 16) || !aligned(rows, 16) || T > S) return CSA2_ERR_INVALID_ARG;
+  if (!x || !row0 || !rows || !al(x, 16) || !al(rows, 16) || !al(row0, 8) || !al(status, 4) || T > S)
+    return CSA2_ERR_INVALID_ARG;
   return cuda_status(launch_swa_encode(B, T, x, row0, rows, S, status, static_cast<cudaStream_t>(stream)));
 }
 

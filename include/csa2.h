@@ -21,6 +21,13 @@
  *    id or entry id out of range) are written to `*status`, a device int32
  *    that the caller zeroes; the first error wins and the faulty access is
  *    skipped.  No call aborts the process or raises across the ABI.
+ *  - Every pointer has at least its element's natural alignment (2 bytes for
+ *    bf16, 4 for int32 / float, 8 for int64); 16 bytes are required of the
+ *    cache pages, the indexer queries `q_idx`, the attention queries `q`,
+ *    the attention output `out`, window rows and the csa2_swa_encode input;
+ *    8 of the indexer projection `w_idx`; 4 of the compressor input `x`;
+ *    256 of index workspaces.  A pointer short of this is an argument
+ *    error (CSA2_ERR_INVALID_ARG), found before any launch.
  *  - Sizes fixed by the model and accepted only at these values: dim 512,
  *    rope_dims 64, n_heads 64, idx_heads 32, idx_dim 128, hsi_block 8.
  *    topk (1..1024), window (0..512), ratio (1 or 2), hsi_blocks (0..4096)
@@ -66,7 +73,7 @@ extern "C" {
 
 enum {
   CSA2_OK = 0,
-  CSA2_ERR_INVALID_ARG = 1, /* null pointer, bad size or stride */
+  CSA2_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad size or stride */
   CSA2_ERR_UNSUPPORTED = 2, /* a model size other than the ones listed above */
   CSA2_ERR_CUDA = 3,        /* a launch failed (cudaGetLastError) */
   CSA2_ERR_CAPACITY = 4,    /* workspace or cache too small for the request */

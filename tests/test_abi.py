@@ -175,6 +175,42 @@ def test_format_flags_are_validated():
     assert lib.csa2_swa_encode(0, 4, None, None, None, 8, None, None) == 0
 
 
+def test_misaligned_pointers_are_rejected_before_launch():
+    lib = csa.load()
+    cfg = csa.Cfg(ratio=2)
+    m, i = _fake_cache(512), _fake_cache(128)
+    # compressor: x needs 4 bytes, w_idx 8, pos0 8
+    assert lib.csa2_compress(C.byref(cfg), 1, 2, FAKE + 2, FAKE, FAKE, FAKE, C.byref(m), C.byref(i), FAKE, None,
+                             None) == 1
+    assert lib.csa2_compress(C.byref(cfg), 1, 2, FAKE, FAKE, FAKE, FAKE + 4, C.byref(m), C.byref(i), FAKE, None,
+                             None) == 1
+    assert lib.csa2_compress(C.byref(cfg), 1, 2, FAKE, FAKE + 4, FAKE, FAKE, C.byref(m), C.byref(i), FAKE, None,
+                             None) == 1
+    # a block table off its 4-byte boundary
+    bt = csa._CacheDesc(FAKE, FAKE, FAKE + 2, 4, 8, 128, 0)
+    assert lib.csa2_compress(C.byref(cfg), 1, 2, FAKE, FAKE, FAKE, FAKE, C.byref(m), C.byref(bt), FAKE, None,
+                             None) == 1
+    # indexer: q_idx needs 16 bytes, q_pos 8, the outputs 4
+    args = dict(q_idx=FAKE, head_w=None, q_pos=FAKE, topk_out=FAKE, status=None)
+    def index(**kw):
+        a = dict(args, **kw)
+        return lib.csa2_index_topk(C.byref(cfg), 1, 1, a["q_idx"], a["head_w"], a["q_pos"], C.byref(i), FAKE, 256,
+                                   None, a["topk_out"], None, FAKE, 1 << 30, a["status"], None)
+    for kw in (dict(q_idx=FAKE + 8), dict(q_pos=FAKE + 4), dict(head_w=FAKE + 2), dict(topk_out=FAKE + 2),
+               dict(status=FAKE + 1)):
+        assert index(**kw) == 1, kw
+    # attention: q and out need 16 bytes, swa_pos0 8
+    def attend(q=FAKE, out=FAKE, swa_pos0=FAKE):
+        return lib.csa2_attend(C.byref(cfg), 1, 1, q, C.byref(m), FAKE, FAKE, FAKE, 1, FAKE, swa_pos0, FAKE, 1.0,
+                               out, None, None, None)
+    assert attend(q=FAKE + 8) == 1
+    assert attend(out=FAKE + 4) == 1
+    assert attend(swa_pos0=FAKE + 4) == 1
+    # gather: ids and out need 4 bytes
+    assert lib.csa2_gather_dequant(C.byref(m), csa.CACHE_FP4, 1, 1, FAKE + 2, FAKE, None, None) == 1
+    assert lib.csa2_gather_dequant(C.byref(m), csa.CACHE_FP4, 1, 1, FAKE, FAKE + 2, None, None) == 1
+
+
 def test_paged_round_trip_of_68_byte_indexer_entries():
     import oracle
     import synth

@@ -56,10 +56,10 @@ MAIN_ENTRY_BYTES = {"fp4": 288, "bf16": 1024}
 # current kernels reports null.
 TRAFFIC = {
     "decode_b8_ctx32768_r2_fp4": {
-        "compress": (174592, "profiles/compress_kernel_decode_b8_ctx32768_r2_fp4.md"),
-        "index_topk": (9567232 + 623360, "profiles/score_tc_kernel_decode_b8_ctx32768_r2_fp4.md + "
+        "compress": (175104, "profiles/compress_kernel_decode_b8_ctx32768_r2_fp4.md"),
+        "index_topk": (9568512 + 623872, "profiles/score_tc_kernel_decode_b8_ctx32768_r2_fp4.md + "
                                          "profiles/select_kernel_decode_b8_ctx32768_r2_fp4.md"),
-        "attend": (3208960, "profiles/attend_rows_kernel_decode_b8_ctx32768_r2_fp4.md"),
+        "attend": (3213568, "profiles/attend_rows_kernel_decode_b8_ctx32768_r2_fp4.md"),
     },
 }
 

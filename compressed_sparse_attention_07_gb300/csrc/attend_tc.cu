@@ -12,7 +12,9 @@
 //    CTA gathers and decodes its rows once, computes S = C.Q^T, a partial
 //    softmax and O = C^T.P^T on the tensor cores, and the partial outputs
 //    are merged through distributed shared memory (the only kernel that
-//    reads MXFP8 window rows);
+//    reads MXFP8 window rows); launched while the selection still runs, it
+//    first brings the query rows, the window rows and the block table into
+//    L2 (hints only), then waits for the selected ids;
 //  - attend_split_kernel (up to 16 tiles, few queries): the same with 16
 //    heads per CTA;
 //  - attend_tc_kernel (otherwise): one CTA per (query, group of HG heads)
@@ -804,10 +806,40 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16]) {
 template <int kDtype, bool kSwaFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_rows_kernel(AttArgs a) {
-  griddep_wait();  // before any global read or tensor-memory allocation
-  griddep_launch();
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   const int n = a.tiles_main + a.tiles_win;
+  if (threadIdx.x < 32) {
+    // While the previous kernel (the selection) runs, the first warp brings
+    // this query's inputs that do not depend on the selected ids into L2:
+    // the query rows (cluster rank 0), the window rows (rank 1 % n) and, once
+    // per sequence, its main-cache block table (rank n - 1).  Only hints are
+    // issued; the values read to aim them are read again after the wait.
+    const int lane = threadIdx.x, rk = (int)tc::cluster_rank(), qi = blockIdx.y, b = qi / a.Tq;
+    if (rk == 0 && lane < 16)  // 64 x 512 bf16 = 64 KB in 4 KB pieces
+      tc::bulk_prefetch_l2(a.q + (int64_t)qi * kHeads * kDim + lane * 2048, 4096);
+    if (rk == 1 % n && a.W > 0 && a.Tq <= 8) {
+      const int64_t pos = tc::ld_cg_s64(a.q_pos + qi), p0 = tc::ld_cg_s64(a.swa_pos0 + b);
+      int64_t len = tc::ld_cg_s32(a.swa_len + b);
+      len = len < a.S ? len : a.S;
+      const int64_t lo = pos - a.W + 1 > p0 ? pos - a.W + 1 : p0, hi = pos < p0 + len - 1 ? pos : p0 + len - 1;
+      if (lo <= hi) {  // slab rows lo - p0 .. hi - p0, all in [0, S)
+        const int64_t rb = kSwaFp8 ? kSwaFp8Row : kDim * 2;
+        const uint8_t* base =
+            (kSwaFp8 ? a.swa8 : reinterpret_cast<const uint8_t*>(a.swa)) + ((int64_t)b * a.S + (lo - p0)) * rb;
+        const int64_t bytes = (hi - lo + 1) * rb;
+        for (int64_t off = (int64_t)lane * 4096; off < bytes; off += 32 * 4096)
+          tc::bulk_prefetch_l2(base + off, (uint32_t)(bytes - off < 4096 ? bytes - off : 4096));
+      }
+    }
+    if (rk == n - 1 && qi % a.Tq == 0) {
+      int64_t np = (a.capacity + kPage - 1) / kPage;
+      np = np < a.mc.max_pages ? np : a.mc.max_pages;
+      const char* bt = reinterpret_cast<const char*>(a.mc.block_table + (int64_t)b * a.mc.max_pages);
+      for (int64_t off = (int64_t)lane * 128; off < 4 * np; off += 32 * 128) tc::prefetch_l2(bt + off);
+    }
+  }
+  griddep_wait();  // before any other global read or tensor-memory allocation
+  griddep_launch();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* qs = smem;                                     // Q [64 heads x 512] f16, K-major
   uint8_t* ctile = qs + kRowQBytes;                       // C [128 rows x 512 ch] f16, K-major

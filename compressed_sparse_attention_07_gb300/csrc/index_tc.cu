@@ -22,7 +22,9 @@
 //    head sums, writes the scores, the 8-entry block maxima for HSI and folds
 //    this CTA's key range per query (one slot each) for the top-k selection.
 // A warpgroup decodes its next tile while its previous MMA runs, and the
-// warpgroups interleave on the tensor core.  Every wait is bounded.
+// warpgroups interleave on the tensor core.  When the grid is one wave, the
+// producer warp prefetches its first ring pass into L2 while the previous
+// kernel (the compressor) still runs.  Every wait is bounded.
 #include <algorithm>
 
 #include "internal.h"
@@ -61,6 +63,7 @@ struct ScoreArgs {
   int q0, Tq, r;
   int seg, gps;         // query groups: segments of `seg` queries from q0, `gps` groups of QPC each
   int q_fp4;            // score with FP4-encoded indexer queries
+  int prefetch;         // page mode, one wave: warm L2 with the first ring pass before the wait
   const uint16_t* q_idx;
   const float* head_w;
   const int64_t* q_pos;
@@ -140,7 +143,30 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   constexpr bool kBf16 = (kDtype == CSA2_CACHE_BF16);
   constexpr uint32_t kIdesc = tc::idesc_f16(128, kN, kBf16, kBf16, false, false);
   static_assert(!kGather || QPC == 1, "gather mode scores one query per CTA");
-  griddep_wait();  // before any global read or tensor-memory allocation
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int jg = blockIdx.y % a.gps;
+  const int qc0 = (blockIdx.y / a.gps) * a.seg + jg * QPC;  // chunk-local index of the group's first query
+  const int n_act = min(QPC, a.seg - jg * QPC);             // queries of the group; the rest are masked
+  const int g0 = a.q0 + qc0;                                // first query of the group (same sequence)
+  const int b = g0 / a.Tq;
+  if (!kGather && a.prefetch && warp == kConsumers / 32) {
+    // While the previous kernel runs (the grid is one wave, so every CTA is
+    // resident early): the producer warp brings the pages of this CTA's
+    // first ring pass into L2.  Only hints are issued here: the block-table
+    // entries read to aim them are read again after the wait, and every
+    // prefetched page lies in the page pool.
+    const int lane = tid & 31;
+    const int64_t tb0 = (int64_t)blockIdx.x * a.tiles_per_cta;
+    const int64_t pp = 2 * tb0 + lane;  // logical page
+    if (lane < 2 * a.tiles_per_cta && lane < 2 * kStages && pp < a.ic.max_pages && pp * kPage < a.max_entries) {
+      const int32_t pg = tc::ld_cg_s32(a.ic.block_table + (int64_t)b * a.ic.max_pages + pp);
+      if (pg >= 0 && pg < a.ic.num_pages) {
+        tc::bulk_prefetch_l2(a.ic.data + (int64_t)pg * F::kPageData, F::kPageData);
+        if (F::kPageScales) tc::bulk_prefetch_l2(a.ic.scales + (int64_t)pg * F::kPageScales, F::kPageScales);
+      }
+    }
+  }
+  griddep_wait();  // before any other global read or tensor-memory allocation
   griddep_launch();
 
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -155,12 +181,6 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   __shared__ int32_t ptab[kGather ? 1 : 2 * kMaxTilesPerCta];     // page mode: pages of this CTA's tiles
   __shared__ int32_t gtab[kGather ? kMaxGatherTiles * 128 : 1];   // gather mode: page*64+slot or -1
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int jg = blockIdx.y % a.gps;
-  const int qc0 = (blockIdx.y / a.gps) * a.seg + jg * QPC;  // chunk-local index of the group's first query
-  const int n_act = min(QPC, a.seg - jg * QPC);             // queries of the group; the rest are masked
-  const int g0 = a.q0 + qc0;                                // first query of the group (same sequence)
-  const int b = g0 / a.Tq;
   int64_t nv[QPC];
   int64_t nv_max = 0;
 #pragma unroll
@@ -607,8 +627,9 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   const int splits = (int)((tiles + per - 1) / per);
   if (splits > kr_stride) return cudaErrorInvalidValue;
   *n_slots = splits;
-  ScoreArgs a{q0, Tq, cfg.ratio, seg, gps, (cfg.formats & CSA2_FMT_IDX_QFP4) ? 1 : 0, q_idx, head_w, q_pos, view_of(idx_c), n_entries, max_entries, (int)per,
-              pool, cfg.hsi_blocks, scores, stride, bmax, krange, kr_stride, status};
+  ScoreArgs a{q0, Tq, cfg.ratio, seg, gps, (cfg.formats & CSA2_FMT_IDX_QFP4) ? 1 : 0,
+              (!gather && (int64_t)splits * groups <= num_sms) ? 1 : 0, q_idx, head_w, q_pos, view_of(idx_c),
+              n_entries, max_entries, (int)per, pool, cfg.hsi_blocks, scores, stride, bmax, krange, kr_stride, status};
   if (idx_dtype(cfg) == CSA2_CACHE_FP4_S32) {
     if (gather) return launch_one<CSA2_CACHE_FP4_S32, 1, true>(a, groups, splits, stream);
     if (qpc == 6) return launch_one<CSA2_CACHE_FP4_S32, 6, false>(a, groups, splits, stream);

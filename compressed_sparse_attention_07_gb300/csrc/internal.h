@@ -13,8 +13,9 @@ namespace csa2 {
 
 // Launch with programmatic stream serialization: the grid may be scheduled
 // while the previous kernel on the stream finishes; every kernel of the
-// library waits for its predecessor (griddep_wait) before touching global
-// memory or allocating tensor memory.  cluster_x > 0 adds a cluster shape.
+// library waits for its predecessor (griddep_wait) before any global load
+// whose value it uses and before allocating tensor memory (before the wait
+// only L2 prefetch hints are issued).  cluster_x > 0 adds a cluster shape.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster_x,
                      Args&&... args) {

@@ -38,3 +38,21 @@ def test_workloads_are_consistent():
             assert wl.entries == wl.ctx // wl.ratio
         assert not (wl.idx68 and wl.cache != "fp4")
     assert bench.DEFAULT_WORKLOAD in synth.WORKLOADS
+
+
+def test_traffic_figures_match_their_profile_summaries():
+    # every DRAM traffic figure the benchmark reports is the sum of the
+    # dram__bytes_read + dram__bytes_write rows of the summaries it names
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for wl, stages in bench.TRAFFIC.items():
+        assert wl in synth.WORKLOADS
+        for stage, (traffic, sources) in stages.items():
+            total = 0
+            for src in sources.split(" + "):
+                text = open(os.path.join(root, src)).read()
+                m = re.search(r"dram__bytes_read\.sum \+ dram__bytes_write\.sum \| ([\d,]+) B \+ ([\d,]+) B", text)
+                assert m, src
+                total += int(m.group(1).replace(",", "")) + int(m.group(2).replace(",", ""))
+            assert total == traffic, (wl, stage, total, traffic)

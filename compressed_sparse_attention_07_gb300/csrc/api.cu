@@ -84,18 +84,94 @@ const char* csa2_status_string(int32_t code) {
   }
 }
 
-int32_t csa2_compress(const csa2_cfg* cfg, int32_t B, int32_t T, const uint16_t* x, const int64_t* pos0,
-                      const float* merge_w, const uint16_t* w_idx, const csa2_cache* main_cache,
-                      const csa2_cache* idx_cache, int32_t* n_entries, int32_t* status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Host-side argument checks of each entry point (nothing is enqueued).
+// CSA2_OK means the call would launch; a call with nothing to do reports
+// CSA2_OK through *empty.
+int32_t check_compress(const csa2_cfg* cfg, int32_t B, int32_t T, const uint16_t* x, const int64_t* pos0,
+                       const float* merge_w, const uint16_t* w_idx, const csa2_cache* main_cache,
+                       const csa2_cache* idx_cache, const int32_t* n_entries, const int32_t* status, bool* empty) {
   int32_t err;
+  *empty = false;
   if (!cfg_supported(cfg, &err)) return err;
   if (B < 0 || T < 0 || T % cfg->ratio) return CSA2_ERR_INVALID_ARG;
-  if (B == 0 || T == 0) return CSA2_OK;
+  if (B == 0 || T == 0) {
+    *empty = true;
+    return CSA2_OK;
+  }
   if (!x || !pos0 || !merge_w || !w_idx || !n_entries) return CSA2_ERR_INVALID_ARG;
   if (!al(x, 4) || !al(pos0, 8) || !al(merge_w, 4) || !al(w_idx, 8) || !al(n_entries, 4) || !al(status, 4))
     return CSA2_ERR_INVALID_ARG;
   if (!cache_ok(main_cache, kDim, cfg->cache_dtype) || !cache_ok(idx_cache, kIdxDim, idx_dtype(*cfg)))
     return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+}  // namespace
+
+int32_t csa2::check_index(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q_idx, const float* head_w,
+                          const int64_t* q_pos, const csa2_cache* idx_cache, const int32_t* n_entries,
+                          int32_t max_entries, const int32_t* pool, const int32_t* topk_out, const int32_t* pool_out,
+                          const void* workspace, size_t workspace_bytes, const int32_t* status, bool* empty) {
+  int32_t err;
+  *empty = false;
+  if (!cfg_supported(cfg, &err)) return err;
+  if (B < 0 || Tq < 0 || max_entries < 0) return CSA2_ERR_INVALID_ARG;
+  if (B == 0 || Tq == 0) {
+    *empty = true;
+    return CSA2_OK;
+  }
+  if (!q_idx || !q_pos || !n_entries || !topk_out || !workspace) return CSA2_ERR_INVALID_ARG;
+  if (!al(q_idx, 16) || !al(head_w, 4) || !al(q_pos, 8) || !al(n_entries, 4) || !al(pool, 4) || !al(topk_out, 4) ||
+      !al(pool_out, 4) || !al(status, 4))
+    return CSA2_ERR_INVALID_ARG;
+  if (!cache_ok(idx_cache, kIdxDim, idx_dtype(*cfg))) return CSA2_ERR_INVALID_ARG;
+  if ((int64_t)max_entries > (int64_t)idx_cache->max_pages * kPage) return CSA2_ERR_CAPACITY;
+  if (pool && pool_out) return CSA2_ERR_INVALID_ARG;
+  if ((pool || pool_out) && cfg->hsi_blocks <= 0) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return CSA2_ERR_INVALID_ARG;
+  if (workspace_bytes < index_query_ws_bytes(*cfg, max_entries, pool != nullptr)) return CSA2_ERR_CAPACITY;
+  return CSA2_OK;
+}
+
+namespace {
+
+int32_t check_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q, const csa2_cache* main_cache,
+                     const int32_t* n_entries, const int32_t* topk, const void* swa, int32_t S,
+                     const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos, float scale,
+                     const float* out, const float* lse, const int32_t* status, bool* empty) {
+  int32_t err;
+  *empty = false;
+  if (!cfg_supported(cfg, &err)) return err;
+  if (B < 0 || Tq < 0 || S < 0) return CSA2_ERR_INVALID_ARG;
+  if (B == 0 || Tq == 0) {
+    *empty = true;
+    return CSA2_OK;
+  }
+  if (!q || !n_entries || !topk || !q_pos || !out) return CSA2_ERR_INVALID_ARG;
+  if (!al(q, 16) || !al(n_entries, 4) || !al(topk, 4) || !al(swa_len, 4) || !al(swa_pos0, 8) || !al(q_pos, 8) ||
+      !al(out, 16) || !al(lse, 4) || !al(status, 4))
+    return CSA2_ERR_INVALID_ARG;
+  if (cfg->window > 0 && (!swa || !swa_len || !swa_pos0 || S == 0 || !aligned(swa, 16))) return CSA2_ERR_INVALID_ARG;
+  if (!cache_ok(main_cache, kDim, cfg->cache_dtype)) return CSA2_ERR_INVALID_ARG;
+  if (!(scale == scale)) return CSA2_ERR_INVALID_ARG;
+  if ((cfg->formats & CSA2_FMT_SWA_FP8) && !attend_rows_path(cfg->topk, cfg->window)) return CSA2_ERR_UNSUPPORTED;
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t csa2_compress(const csa2_cfg* cfg, int32_t B, int32_t T, const uint16_t* x, const int64_t* pos0,
+                      const float* merge_w, const uint16_t* w_idx, const csa2_cache* main_cache,
+                      const csa2_cache* idx_cache, int32_t* n_entries, int32_t* status, void* stream) {
+  bool empty;
+  const int32_t rc = check_compress(cfg, B, T, x, pos0, merge_w, w_idx, main_cache, idx_cache, n_entries, status, &empty);
+  if (rc != CSA2_OK || empty) return rc;
   return cuda_status(launch_compress(*cfg, B, T, x, pos0, merge_w, w_idx, *main_cache, *idx_cache, n_entries, status,
                                      static_cast<cudaStream_t>(stream)));
 }
@@ -110,20 +186,10 @@ int32_t csa2_index_topk(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16
                         const int64_t* q_pos, const csa2_cache* idx_cache, const int32_t* n_entries,
                         int32_t max_entries, const int32_t* pool, int32_t* topk_out, int32_t* pool_out,
                         void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
-  int32_t err;
-  if (!cfg_supported(cfg, &err)) return err;
-  if (B < 0 || Tq < 0 || max_entries < 0) return CSA2_ERR_INVALID_ARG;
-  if (B == 0 || Tq == 0) return CSA2_OK;
-  if (!q_idx || !q_pos || !n_entries || !topk_out || !workspace) return CSA2_ERR_INVALID_ARG;
-  if (!al(q_idx, 16) || !al(head_w, 4) || !al(q_pos, 8) || !al(n_entries, 4) || !al(pool, 4) || !al(topk_out, 4) ||
-      !al(pool_out, 4) || !al(status, 4))
-    return CSA2_ERR_INVALID_ARG;
-  if (!cache_ok(idx_cache, kIdxDim, idx_dtype(*cfg))) return CSA2_ERR_INVALID_ARG;
-  if ((int64_t)max_entries > (int64_t)idx_cache->max_pages * kPage) return CSA2_ERR_CAPACITY;
-  if (pool && pool_out) return CSA2_ERR_INVALID_ARG;
-  if ((pool || pool_out) && cfg->hsi_blocks <= 0) return CSA2_ERR_INVALID_ARG;
-  if (!aligned(workspace, 256)) return CSA2_ERR_INVALID_ARG;
-  if (workspace_bytes < index_query_ws_bytes(*cfg, max_entries, pool != nullptr)) return CSA2_ERR_CAPACITY;
+  bool empty;
+  const int32_t rc = check_index(cfg, B, Tq, q_idx, head_w, q_pos, idx_cache, n_entries, max_entries, pool, topk_out,
+                                 pool_out, workspace, workspace_bytes, status, &empty);
+  if (rc != CSA2_OK || empty) return rc;
   return cuda_status(launch_index_topk(*cfg, B, Tq, q_idx, head_w, q_pos, *idx_cache, n_entries, max_entries, pool,
                                        topk_out, pool_out, workspace, workspace_bytes, status,
                                        static_cast<cudaStream_t>(stream)));
@@ -133,18 +199,10 @@ int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* 
                     const int32_t* n_entries, const int32_t* topk, const void* swa, int32_t S,
                     const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos, float scale, float* out,
                     float* lse, int32_t* status, void* stream) {
-  int32_t err;
-  if (!cfg_supported(cfg, &err)) return err;
-  if (B < 0 || Tq < 0 || S < 0) return CSA2_ERR_INVALID_ARG;
-  if (B == 0 || Tq == 0) return CSA2_OK;
-  if (!q || !n_entries || !topk || !q_pos || !out) return CSA2_ERR_INVALID_ARG;
-  if (!al(q, 16) || !al(n_entries, 4) || !al(topk, 4) || !al(swa_len, 4) || !al(swa_pos0, 8) || !al(q_pos, 8) ||
-      !al(out, 16) || !al(lse, 4) || !al(status, 4))
-    return CSA2_ERR_INVALID_ARG;
-  if (cfg->window > 0 && (!swa || !swa_len || !swa_pos0 || S == 0 || !aligned(swa, 16))) return CSA2_ERR_INVALID_ARG;
-  if (!cache_ok(main_cache, kDim, cfg->cache_dtype)) return CSA2_ERR_INVALID_ARG;
-  if (!(scale == scale)) return CSA2_ERR_INVALID_ARG;
-  if ((cfg->formats & CSA2_FMT_SWA_FP8) && !attend_rows_path(cfg->topk, cfg->window)) return CSA2_ERR_UNSUPPORTED;
+  bool empty;
+  const int32_t rc = check_attend(cfg, B, Tq, q, main_cache, n_entries, topk, swa, S, swa_len, swa_pos0, q_pos, scale,
+                                  out, lse, status, &empty);
+  if (rc != CSA2_OK || empty) return rc;
   return cuda_status(launch_attend(*cfg, B, Tq, q, *main_cache, n_entries, topk, swa, S, swa_len, swa_pos0, q_pos,
                                    scale, out, lse, status, static_cast<cudaStream_t>(stream)));
 }
@@ -177,26 +235,46 @@ int32_t csa2_layer(const csa2_cfg* cfg, int32_t mode, csa2_group_state* st, cons
   if (!st || !io) return CSA2_ERR_INVALID_ARG;
   if (mode != CSA2_MODE_FULL && mode != CSA2_MODE_REINDEX && mode != CSA2_MODE_REUSE) return CSA2_ERR_INVALID_ARG;
   if (!st->topk) return CSA2_ERR_INVALID_ARG;
-  int32_t rc = CSA2_OK;
-  if (mode == CSA2_MODE_FULL) {
-    if (io->x) {
-      rc = csa2_compress(cfg, io->B, io->T, io->x, io->pos0, io->merge_w, io->w_idx, &st->main_cache, &st->idx_cache,
-                         st->n_entries, st->status, stream);
-      if (rc) return rc;
-    }
-    rc = csa2_index_topk(cfg, io->B, io->Tq, io->q_idx, io->head_w, io->q_pos, &st->idx_cache, st->n_entries,
-                         st->max_entries, nullptr, st->topk, cfg->hsi_blocks > 0 ? st->pool : nullptr, st->workspace,
-                         st->workspace_bytes, st->status, stream);
-    if (rc) return rc;
-  } else if (mode == CSA2_MODE_REINDEX) {
-    if (!st->pool || cfg->hsi_blocks <= 0) return CSA2_ERR_INVALID_ARG;
-    rc = csa2_index_topk(cfg, io->B, io->Tq, io->q_idx, io->head_w, io->q_pos, &st->idx_cache, st->n_entries,
-                         st->max_entries, st->pool, st->topk, nullptr, st->workspace, st->workspace_bytes, st->status,
-                         stream);
+  if (mode == CSA2_MODE_REINDEX && (!st->pool || cfg->hsi_blocks <= 0)) return CSA2_ERR_INVALID_ARG;
+  // every stage's arguments are checked before the first launch, so an
+  // argument error leaves the caches, the published top-k and the pool as
+  // they were
+  const bool comp = mode == CSA2_MODE_FULL && io->x;
+  const bool index = mode != CSA2_MODE_REUSE;
+  const int32_t* pool_in = mode == CSA2_MODE_REINDEX ? st->pool : nullptr;
+  int32_t* pool_out = (mode == CSA2_MODE_FULL && cfg->hsi_blocks > 0) ? st->pool : nullptr;
+  bool e_comp = true, e_index = true, e_att;
+  int32_t rc;
+  if (comp) {
+    rc = check_compress(cfg, io->B, io->T, io->x, io->pos0, io->merge_w, io->w_idx, &st->main_cache, &st->idx_cache,
+                        st->n_entries, st->status, &e_comp);
     if (rc) return rc;
   }
-  return csa2_attend(cfg, io->B, io->Tq, io->q, &st->main_cache, st->n_entries, st->topk, io->swa, io->S, io->swa_len,
-                     io->swa_pos0, io->q_pos, io->scale, io->out, io->lse, st->status, stream);
+  if (index) {
+    rc = check_index(cfg, io->B, io->Tq, io->q_idx, io->head_w, io->q_pos, &st->idx_cache, st->n_entries,
+                     st->max_entries, pool_in, st->topk, pool_out, st->workspace, st->workspace_bytes, st->status,
+                     &e_index);
+    if (rc) return rc;
+  }
+  rc = check_attend(cfg, io->B, io->Tq, io->q, &st->main_cache, st->n_entries, st->topk, io->swa, io->S, io->swa_len,
+                    io->swa_pos0, io->q_pos, io->scale, io->out, io->lse, st->status, &e_att);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!e_comp) {
+    rc = cuda_status(launch_compress(*cfg, io->B, io->T, io->x, io->pos0, io->merge_w, io->w_idx, st->main_cache,
+                                     st->idx_cache, st->n_entries, st->status, s));
+    if (rc) return rc;
+  }
+  if (!e_index) {
+    rc = cuda_status(launch_index_topk(*cfg, io->B, io->Tq, io->q_idx, io->head_w, io->q_pos, st->idx_cache,
+                                       st->n_entries, st->max_entries, pool_in, st->topk, pool_out, st->workspace,
+                                       st->workspace_bytes, st->status, s));
+    if (rc) return rc;
+  }
+  if (e_att) return CSA2_OK;
+  return cuda_status(launch_attend(*cfg, io->B, io->Tq, io->q, st->main_cache, st->n_entries, st->topk, io->swa,
+                                   io->S, io->swa_len, io->swa_pos0, io->q_pos, io->scale, io->out, io->lse,
+                                   st->status, s));
 }
 
 }  // extern "C"

@@ -74,6 +74,13 @@ inline int score_range_slots(int64_t tiles) { return (int)((tiles + 3) / 4); }
 // Per-query workspace bytes of the indexer (scores + HSI block maxima).
 size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex);
 
+// Host-side checks of csa2_index_topk's arguments, in the order that entry
+// point applies them; *empty is set when there is nothing to launch.
+int32_t check_index(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q_idx, const float* head_w,
+                    const int64_t* q_pos, const csa2_cache* idx_cache, const int32_t* n_entries,
+                    int32_t max_entries, const int32_t* pool, const int32_t* topk_out, const int32_t* pool_out,
+                    const void* workspace, size_t workspace_bytes, const int32_t* status, bool* empty);
+
 cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx,
                               const float* head_w, const int64_t* q_pos, const csa2_cache& idx_c,
                               const int32_t* n_entries, int max_entries, const int32_t* pool,

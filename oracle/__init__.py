@@ -339,3 +339,49 @@ def layer_modes(schedule):
         else:
             raise ValueError(mode)
     return out
+
+
+class GroupState:
+    """State shared by the layers of one cross-layer group (hn.213312.xyz
+    sec. 2.3.2 and the access table of sec. 3.2): the main-KV and indexer-K
+    caches the Full layer writes, the entry counts, and the latest published
+    top-k and HSI pool."""
+
+    def __init__(self, main: Cache, idx: Cache, n_entries, r: int, k: int, hsi_blocks: int = 0,
+                 theta: float = 1e4):
+        self.main, self.idx = main, idx
+        self.n_entries = np.array(n_entries, np.int32)
+        self.r, self.k, self.hsi_blocks, self.theta = r, k, hsi_blocks, theta
+        self.topk = None
+        self.pool = None
+
+
+def layer(mode: str, st: GroupState, q_pos, q, swa, swa_len, swa_pos0, window: int, scale: float,
+          q_idx=None, x=None, pos0=None, w=None, w_idx=None):
+    """a8, one layer under its mode, following the access table:
+    full    -- compress the step's tokens (when x is given), index every
+               visible entry, publish top-k (and the HSI pool when the group
+               has one), attend;
+    reindex -- index the published pool's entries with this layer's q_idx,
+               publish top-k, attend; no cache writes;
+    reuse   -- attend with the latest published top-k; reads no indexer and
+               writes nothing.
+    Returns the attention output [B][Tq][Hm][D]."""
+    if mode == "full":
+        if x is not None:
+            compress(x, pos0, w, w_idx, st.main, st.idx, st.r, st.theta)
+            T = np.asarray(x).shape[1]
+            st.n_entries = (np.asarray(pos0, np.int64) // st.r + T // st.r).astype(np.int32)
+        st.topk, st.pool, _ = index_topk(st.idx, st.n_entries, q_idx, q_pos, st.r, st.k,
+                                         hsi_blocks=st.hsi_blocks, want_pool=st.hsi_blocks > 0)
+    elif mode == "reindex":
+        if st.pool is None:
+            raise ValueError("Reindex needs a published HSI pool")
+        st.topk, _, _ = index_topk(st.idx, st.n_entries, q_idx, q_pos, st.r, st.k, hsi_blocks=st.hsi_blocks,
+                                   pool=st.pool)
+    elif mode == "reuse":
+        if st.topk is None:
+            raise ValueError("Reuse needs a published top-k")
+    else:
+        raise ValueError(mode)
+    return attend(st.main, st.n_entries, q, st.topk, swa, swa_len, swa_pos0, q_pos, window, scale)

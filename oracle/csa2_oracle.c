@@ -526,6 +526,28 @@ int orc_attend(int B, int Tq, int Hm, int D, int cache_dtype, int n_cap,
   return bad ? -2 : 0;
 }
 
+/* Dense attention, written out without the selection path's softmax: for
+ * each head the weight of row e is 1 / sum_f exp(scale q.(c_f - c_e)) (the
+ * softmax of the logits in its pairwise form, which needs no running maximum
+ * and never overflows), and the output is sum_e weight_e c_e.  Quadratic in
+ * the rows, so only for the small inputs of the dense-limit pin. */
+static void orc_dense_head(int D, const double* qh, double* const* rows, int n, double scale, double* o) {
+  double* dot = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  for (int e = 0; e < n; ++e) {
+    double acc = 0.0;
+    for (int c = 0; c < D; ++c) acc += rows[e][c] * qh[c];
+    dot[e] = acc;
+  }
+  for (int c = 0; c < D; ++c) o[c] = 0.0;
+  for (int e = 0; e < n; ++e) {
+    double den = 0.0;
+    for (int f = 0; f < n; ++f) den += exp(scale * (dot[f] - dot[e]));
+    const double wgt = 1.0 / den;
+    for (int c = 0; c < D; ++c) o[c] += wgt * rows[e][c];
+  }
+  free(dot);
+}
+
 int orc_attend_dense(int B, int Tq, int Hm, int D, int r, int cache_dtype, int n_cap,
                      const uint8_t* main_codes, const uint8_t* main_scales,
                      const uint16_t* main_bf16, const int32_t* n_entries, const uint16_t* q,
@@ -552,7 +574,7 @@ int orc_attend_dense(int B, int Tq, int Hm, int D, int r, int cache_dtype, int n
       int32_t len = swa_len[b] < S ? swa_len[b] : S;
       n = orc_window_rows(q_pos[qi], W, (const uint8_t*)swa + (size_t)b * S * rb, swa_fmt, D, swa_pos0[b], len,
                           rows, n);
-      orc_attend_rows(Hm, D, qq, rows, n, scale, out + qi * Hm * D, NULL);
+      for (int h = 0; h < Hm; ++h) orc_dense_head(D, qq + (size_t)h * D, rows, n, scale, out + (qi * Hm + h) * D);
       for (int i = 0; i < n; ++i) free(rows[i]);
       free(rows);
       free(qq);

@@ -147,7 +147,9 @@ int orc_attend(int B, int Tq, int Hm, int D, int cache_dtype, int n_cap,
                const int64_t* q_pos, int W, double scale, double* out, double* lse);
 
 /* Dense attention over every visible entry and the window (no selection):
- * the k >= N limit, coded separately for the oracle's own pin. */
+ * the k >= N limit, coded separately for the oracle's own pin -- its own
+ * dot products and the softmax in pairwise form, weight_e =
+ * 1 / sum_f exp(scale q.(c_f - c_e)), sharing nothing with orc_attend. */
 int orc_attend_dense(int B, int Tq, int Hm, int D, int r, int cache_dtype, int n_cap,
                      const uint8_t* main_codes, const uint8_t* main_scales,
                      const uint16_t* main_bf16, const int32_t* n_entries, const uint16_t* q,

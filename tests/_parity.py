@@ -58,16 +58,31 @@ def fp4_code_mismatches(gpu_codes, gpu_scales, ora_codes, ora_scales, pre, mag, 
     return unexcused, excused, bad_entry
 
 
+def _bf16_neighbour(bits, up: bool):
+    """Value of the bf16 next to `bits` toward +inf (up) or -inf.  Between the
+    two zeros the gap is 0: a value of one sign never rounds to the other
+    sign's zero."""
+    b = bits.astype(np.int64)
+    key = np.where(b & 0x8000, 0x7FFF - (b & 0x7FFF), b + 0x8000)   # monotone in the value
+    nk = key + 1 if up else key - 1
+    nb = np.where(nk >= 0x8000, nk - 0x8000, 0x8000 | (0x7FFF - nk)).astype(np.uint32)
+    return (nb << 16).view(np.float32).astype(np.float64)
+
+
 def bf16_mismatches(gpu_vals, ora_vals, pre, mag, margin):
-    """A bf16 code is excused when the GPU value is the rounding of some value
-    within the fp32 evaluation bound of the oracle's pre-rounding value:
-    |g - pre| <= margin * M + ulp(g) (covers sign flips of values that cancel
-    to near zero)."""
+    """A bf16 code g that differs from the oracle's is excused only when g is
+    the round-to-nearest of some value within the fp32 evaluation bound of
+    the oracle's pre-rounding value: g's rounding interval (half the gap to
+    its neighbour on the side of `pre`, so at a binade edge the smaller
+    binade's half-gap below a power of two) must reach to within
+    margin * M of pre.  Equivalently the rounding midpoint between g and
+    the next bf16 toward pre lies within margin * M of pre."""
     g = (gpu_vals.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     diff = gpu_vals != ora_vals
-    ulp = np.ldexp(1.0, np.frexp(np.abs(g))[1] - 8)
-    ulp = np.maximum(ulp, np.ldexp(1.0, -133))
-    near = np.abs(g - pre) <= margin * mag + ulp
+    above = pre > g
+    nb = np.where(above, _bf16_neighbour(gpu_vals, True), _bf16_neighbour(gpu_vals, False))
+    half_gap = np.abs(nb - g) / 2.0
+    near = np.abs(g - pre) <= margin * mag + half_gap
     unexcused = int((diff & ~near).sum())
     excused = int((diff & near).sum())
     return unexcused, excused, diff.any(-1)
@@ -91,6 +106,44 @@ def topk_mismatch(gpu_ids, ora_ids, ora_scores, k, exact: bool):
         s = ora_scores[qi]
         kth = np.sort(s[np.isfinite(s)])[::-1][min(k, np.isfinite(s).sum()) - 1]
         ok = all(abs(s[j] - kth) <= NEAR_TIE * abs(kth) for j in diff)
+        bad += not ok
+    return bad
+
+
+def pool_mismatch(gpu_pool, ora_pool, ora_scores, block=8):
+    """Number of query rows whose HSI pool differs beyond near-ties.  Pools
+    are ascending block ids, -1 padded.  Block score = max of the oracle's
+    scores over the block's visible positions (non-finite = not visible).
+    Both pools must hold the same number of blocks and the oracle's forced
+    block (its latest visible block); every block in the symmetric
+    difference must score within 1e-5 relative of the lowest-scoring
+    non-forced block of the oracle's pool."""
+    bad = 0
+    for qi in range(gpu_pool.shape[0]):
+        g, o = gpu_pool[qi], ora_pool[qi]
+        gs, os_ = set(g[g >= 0].tolist()), set(o[o >= 0].tolist())
+        if len(gs) != len(os_) or (g >= 0).sum() != len(gs) or not np.all(np.diff(g[g >= 0]) > 0):
+            bad += 1
+            continue
+        s = ora_scores[qi]
+        vis = np.nonzero(np.isfinite(s))[0]
+        if len(vis) == 0:
+            bad += len(gs) != 0
+            continue
+        forced = int(vis.max()) // block
+        if forced not in gs:
+            bad += 1
+            continue
+        diff = gs ^ os_
+        if not diff:
+            continue
+        nb = (len(s) + block - 1) // block
+        sp = np.full(nb * block, -np.inf)
+        sp[:len(s)] = np.where(np.isfinite(s), s, -np.inf)
+        bs = sp.reshape(nb, block).max(-1)
+        rest = [bs[j] for j in os_ if j != forced]
+        kth = min(rest) if rest else -np.inf
+        ok = all(j != forced and abs(bs[j] - kth) <= NEAR_TIE * abs(kth) for j in diff)
         bad += not ok
     return bad
 

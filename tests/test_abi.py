@@ -228,3 +228,49 @@ def test_paged_round_trip_of_68_byte_indexer_entries():
     bj, j = 1, 77  # documented address of one entry's scales: slot s at s*4
     page, slot = int(pc.block_table[bj, j // 64]), j % 64
     np.testing.assert_array_equal(pc.scales[page, slot * 4:slot * 4 + 4].numpy(), oc.scales[bj, j])
+
+
+def test_layer_checks_every_stage_before_the_first_launch():
+    """csa2_layer in Full mode: a bad indexer or attention argument is found
+    before the compressor is launched (no GPU here, so a launch would come
+    back as CSA2_ERR_CUDA instead of the argument error)."""
+    lib = csa.load()
+    cfg = csa.Cfg(ratio=1, hsi_blocks=16)
+    m, i = _fake_cache(512), _fake_cache(128)
+    st = csa._GroupState(m, i, FAKE, 256, 0, FAKE, FAKE, FAKE, 1 << 30, None)
+
+    def io(**kw):
+        d = dict(B=1, Tq=1, q_pos=FAKE, T=1, x=FAKE, pos0=FAKE, merge_w=FAKE, w_idx=FAKE, q_idx=FAKE, head_w=None,
+                 q=FAKE, swa=FAKE, S=1, swa_len=FAKE, swa_pos0=FAKE, scale=1.0, out=FAKE, lse=None)
+        d.update(kw)
+        return csa._LayerIO(**d)
+
+    assert lib.csa2_layer(C.byref(cfg), csa.MODE_FULL, C.byref(st), C.byref(io(q_idx=FAKE + 8)), None) == 1
+    assert lib.csa2_layer(C.byref(cfg), csa.MODE_FULL, C.byref(st), C.byref(io(q_idx=None)), None) == 1
+    assert lib.csa2_layer(C.byref(cfg), csa.MODE_FULL, C.byref(st), C.byref(io(out=FAKE + 4)), None) == 1
+    assert lib.csa2_layer(C.byref(cfg), csa.MODE_FULL, C.byref(st), C.byref(io(scale=float("nan"))), None) == 1
+    small = csa._GroupState(m, i, FAKE, 256, 0, FAKE, FAKE, FAKE, 16, None)
+    assert lib.csa2_layer(C.byref(cfg), csa.MODE_FULL, C.byref(small), C.byref(io()), None) == 4
+    # Reindex checks its indexer and attention arguments the same way
+    assert lib.csa2_layer(C.byref(cfg), csa.MODE_REINDEX, C.byref(st), C.byref(io(q_idx=FAKE + 8)), None) == 1
+
+
+def test_static_entry_point_reports_configuration_errors_first():
+    """csa2_index_topk_static applies csa2_index_topk's checks in the same
+    order: an unsupported configuration is reported as such even when the
+    request would also be too large for the static array."""
+    lib = csa.load()
+    lib.csa2_index_topk_static.restype = C.c_int32
+    i = csa._CacheDesc(FAKE, FAKE, FAKE, 1 << 20, 8, 128, 0)
+    big = (64 << 20) // 4
+    bad = csa.Cfg(ratio=3)
+    assert lib.csa2_index_topk_static(C.byref(bad), 1, 1, FAKE, None, FAKE, C.byref(i), FAKE, big, None, FAKE, None,
+                                      None, None) == 2
+    bad = csa.Cfg(topk=0)
+    assert lib.csa2_index_topk_static(C.byref(bad), 1, 1, FAKE, None, FAKE, C.byref(i), FAKE, big, None, FAKE, None,
+                                      None, None) == 2
+    cfg = csa.Cfg(ratio=1)
+    assert lib.csa2_index_topk_static(C.byref(cfg), 1, 1, FAKE + 8, None, FAKE, C.byref(i), FAKE, big, None, FAKE,
+                                      None, None, None) == 1
+    assert lib.csa2_index_topk_static(C.byref(cfg), 1, 1, FAKE, None, FAKE, C.byref(i), FAKE, big, None, FAKE, None,
+                                      None, None) == 4

@@ -210,13 +210,21 @@ def test_decoder_group_sampled_sequences():
         kw = {}
         if mode == "full":
             kw = dict(x=_paged.dev(x), pos0=_paged.dev(pos0), merge_w=_paged.dev(w), w_idx=_paged.dev(w_idx))
+        topk_before, pool_before = topk.clone(), pool.clone()
         csa.layer(cfg, modes[mode], state, _paged.dev(q_pos), _paged.dev(q), _paged.dev(swa), _paged.dev(swa_len),
                   _paged.dev(swa_pos0), out, q_idx=_paged.dev(q_idx) if mode != "reuse" else None, **kw)
         torch.cuda.synchronize()
         assert int(st.item()) == 0, (layer, csa.status_string(int(st.item())))
+        if mode != "full":  # the pool stays the Full layer's; a Reuse layer republishes the source top-k unchanged
+            assert torch.equal(pool, pool_before), (layer, mode)
+        if mode == "reuse":
+            assert torch.equal(topk, topk_before), (layer, mode)
         if mode == "full":
             o_top, o_pool, s = oracle.index_topk(oi, n_arr, q_idx[sm], q_pos[sm], r, wl.topk,
                                                  hsi_blocks=wl.hsi_blocks, want_pool=True, want_scores=True)
+            g_pool = pool.cpu().numpy()[sm]
+            assert P.pool_mismatch(g_pool.reshape(len(sm), -1), o_pool.reshape(len(sm), -1),
+                                   s.reshape(len(sm), -1)) == 0, layer
         elif mode == "reindex":
             o_top, _, s = oracle.index_topk(oi, n_arr, q_idx[sm], q_pos[sm], r, wl.topk, hsi_blocks=wl.hsi_blocks,
                                             pool=o_pool, want_scores=True)

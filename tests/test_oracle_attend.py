@@ -184,21 +184,79 @@ def test_decoder_schedule_reuse_sources():
         oracle.layer_modes([(5, "reuse")])
 
 
-def test_reuse_layer_reproduces_source_layer():
-    """A Reuse layer reads the source layer's top-k unchanged: given the
-    source layer's query and window it reproduces the source output; with
-    its own query it still reads exactly the same rows (convex hull)."""
-    N, W = 300, 128
-    main = _main_cache(8, 1, N)
+def _reuse_group(seed, N=300, W=128, k=64, nb=16):
+    """A decoder-style group state: a seeded FP4 main and indexer cache of N
+    entries (r = 1), a Full layer with HSI run on it."""
+    main = _main_cache(seed, 1, N)
     idx = oracle.Cache(1, N, 128, "fp4")
-    idx.codes[0], idx.scales[0] = synth.fp4_bytes(synth.rng(8, "idx"), N, 128)
-    q_idx = synth.normal_bf16(synth.rng(8, "q_idx"), (1, 1, 32, 128))
+    idx.codes[0], idx.scales[0] = synth.fp4_bytes(synth.rng(seed, "idx"), N, 128)
+    st = oracle.GroupState(main, idx, [N], r=1, k=k, hsi_blocks=nb)
     q_pos = np.array([[N - 1]])
-    topk, _, _ = oracle.index_topk(idx, np.array([N], np.int32), q_idx, q_pos, r=1, k=64)
-    q_src = synth.normal_bf16(synth.rng(8, "q_src"), (1, 1, HM, D))
-    swa = _swa(8, 1, W)
-    a = dict(swa_len=np.array([W], np.int32), swa_pos0=np.array([N - W]), q_pos=q_pos, window=W,
-             scale=SCALE)
-    src = oracle.attend(main, np.array([N], np.int32), q_src, topk, swa, **a)
-    reuse = oracle.attend(main, np.array([N], np.int32), q_src, topk.copy(), swa, **a)
-    np.testing.assert_array_equal(src, reuse)
+    a = dict(swa_len=np.array([W], np.int32), swa_pos0=np.array([N - W]), window=W, scale=SCALE)
+    q_src = synth.normal_bf16(synth.rng(seed, "q_src"), (1, 1, HM, D))
+    swa_src = _swa(seed, 1, W)
+    q_idx = synth.normal_bf16(synth.rng(seed, "q_idx"), (1, 1, 32, 128))
+    src = oracle.layer("full", st, q_pos, q_src, swa_src, q_idx=q_idx, **a)
+    return st, q_pos, a, q_src, swa_src, src
+
+
+def test_reuse_layer_reads_only_the_source_top_k():
+    """Reuse (hn.213312.xyz sec. 2.3.2, access table of sec. 3.2): the layer
+    reads the latest published top-k and writes nothing.  Checked by
+    behaviour, not by restating the attention: (1) the published top-k and
+    pool and both caches are bit-identical after a Reuse layer; (2) a huge
+    row planted at an id outside the source top-k leaves the Reuse output
+    bit-identical; (3) changing a row inside the source top-k changes it;
+    (4) given the source layer's own query and window rows, a Reuse layer
+    reproduces the source layer's output exactly."""
+    st, q_pos, a, q_src, swa_src, src = _reuse_group(8)
+    topk0, pool0 = st.topk.copy(), st.pool.copy()
+    codes0, scales0, icodes0 = st.main.codes.copy(), st.main.scales.copy(), st.idx.codes.copy()
+    q_own = synth.normal_bf16(synth.rng(8, "q_own"), (1, 1, HM, D))
+    swa_own = _swa(9, 1, a["window"])
+    base = oracle.layer("reuse", st, q_pos, q_own, swa_own, **a)
+    # (1) nothing published or cached changed
+    np.testing.assert_array_equal(st.topk, topk0)
+    np.testing.assert_array_equal(st.pool, pool0)
+    np.testing.assert_array_equal(st.main.codes, codes0)
+    np.testing.assert_array_equal(st.main.scales, scales0)
+    np.testing.assert_array_equal(st.idx.codes, icodes0)
+    # (2) an entry outside the source top-k, made huge, is never read
+    sel = set(topk0[0, 0][topk0[0, 0] >= 0].tolist())
+    outside = next(j for j in range(st.main.n_cap) if j not in sel)
+    st.main.codes[0, outside, :] = 0x77    # every element +6
+    st.main.scales[0, outside, :] = 0x7E   # scale 448
+    np.testing.assert_array_equal(oracle.layer("reuse", st, q_pos, q_own, swa_own, **a), base)
+    st.main.codes[0, outside], st.main.scales[0, outside] = codes0[0, outside], scales0[0, outside]
+    # (3) an entry inside the source top-k is read
+    inside = sorted(sel)[len(sel) // 2]
+    st.main.codes[0, inside, :] = 0x77
+    st.main.scales[0, inside, :] = 0x7E
+    changed = oracle.layer("reuse", st, q_pos, q_own, swa_own, **a)
+    assert np.abs(changed - base).max() > 1e-3
+    st.main.codes[0, inside], st.main.scales[0, inside] = codes0[0, inside], scales0[0, inside]
+    # (4) the source layer's query and window rows give the source output
+    np.testing.assert_array_equal(oracle.layer("reuse", st, q_pos, q_src, swa_src, **a), src)
+
+
+def test_reindex_publishes_from_the_pool_and_writes_no_cache():
+    """Reindex (hn.213312.xyz sec. 2.3.2, sec. 2.3.4): its published top-k
+    lies inside the Full layer's pool, the pool and caches are unchanged,
+    and a Reuse layer after it reads the Reindex layer's top-k."""
+    st, q_pos, a, _, _, _ = _reuse_group(10)
+    pool0 = st.pool.copy()
+    codes0, icodes0 = st.main.codes.copy(), st.idx.codes.copy()
+    q = synth.normal_bf16(synth.rng(10, "q_r"), (1, 1, HM, D))
+    swa = _swa(11, 1, a["window"])
+    q_idx = synth.normal_bf16(synth.rng(10, "q_idx_r"), (1, 1, 32, 128))
+    out_r = oracle.layer("reindex", st, q_pos, q, swa, q_idx=q_idx, **a)
+    np.testing.assert_array_equal(st.pool, pool0)
+    np.testing.assert_array_equal(st.main.codes, codes0)
+    np.testing.assert_array_equal(st.idx.codes, icodes0)
+    blocks = set(pool0[0, 0][pool0[0, 0] >= 0].tolist())
+    ids = st.topk[0, 0][st.topk[0, 0] >= 0]
+    assert len(ids) > 0 and all(int(j) // 8 in blocks for j in ids)
+    np.testing.assert_array_equal(oracle.layer("reuse", st, q_pos, q, swa, **a), out_r)
+    with pytest.raises(ValueError):
+        oracle.layer("reindex", oracle.GroupState(st.main, st.idx, [300], 1, 64, 16), q_pos, q, swa,
+                     q_idx=q_idx, **a)

@@ -3,8 +3,9 @@
 A step is one pass of the whole path over one batch: the compressor on the
 step's new tokens, the indexer with top-k (and the HSI pool / Reindex on
 decoder workloads), and sparse attention over top-k plus the window.  The
-default workload is the batch-8 decode step at 32768 tokens of context with
-2:1 compression into an FP4 cache (16384 entries per sequence).
+default workload is the decoder-layer decode step: batch 32, 131072 tokens of
+context at ratio 1 in an FP4 cache, the hierarchical indexer (HSI, 2048
+blocks of 8) and top-512 plus the 128-row window.
 
 Timing: W warm-up steps launched eagerly; then the step is captured once as a
 CUDA graph and K replays are timed, each bracketed by CUDA events on the
@@ -17,11 +18,17 @@ with the inputs copied from pinned host memory and the output copied back.
 Under torchrun every rank runs its own batch (weak scaling, no data-path
 collective); rank 0 prints one JSON line with the max over ranks.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+On one GPU with the default workload the same run also measures the two
+other workloads with a stated target -- the 20-layer decoder group (per
+group time) and the 4096-token prefill chunk (indexer against the tensor
+peak) -- and reports them under "targets".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--batch B] [--impl reference]
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -40,7 +47,11 @@ import synth  # noqa: E402
 
 METRIC = "CSA2 sparse-attention query-tokens/s at 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "query-tokens/s"
-DEFAULT_WORKLOAD = "decode_b8_ctx32768_r2_fp4"
+DEFAULT_WORKLOAD = "decode_b32_ctx131072_r1_fp4_hsi"
+# workloads with a stated target, measured beside the default one: the
+# decoder group's time per group and the prefill indexer's tensor fraction
+TARGETS = {"decoder_group20_b16_ctx262144_fp4": {"ms_per_step": 0.111},
+           "prefill_4096_on_1m_r2_fp4": {"roofline_frac": 0.50}}
 FLUSH_BYTES = 256 << 20
 # algorithmic bytes per unit (hot-path scope table): indexer 72 B per visible
 # FP4 entry per query (256 B per bf16 entry); attention 512 x 288 + 128 x 1024
@@ -54,19 +65,19 @@ MAIN_ENTRY_BYTES = {"fp4": 288, "bf16": 1024}
 # stage's kernels, from one ncu capture of this bench's default command; the
 # summaries under profiles/ name the capture.  A stage with no capture of the
 # current kernels reports null.
-TRAFFIC = {
-    "decode_b8_ctx32768_r2_fp4": {
-        "compress": (175104, "profiles/compress_kernel_decode_b8_ctx32768_r2_fp4.md"),
-        "index_topk": (9568512 + 623872, "profiles/score_tc_kernel_decode_b8_ctx32768_r2_fp4.md + "
-                                         "profiles/select_kernel_decode_b8_ctx32768_r2_fp4.md"),
-        "attend": (3213568, "profiles/attend_rows_kernel_decode_b8_ctx32768_r2_fp4.md"),
-    },
-}
+TRAFFIC = {}
 
 
 def attend_query_bytes(cache, topk=512, window=128, row_bytes=1024):
     """Top-k entries + window rows (bf16 1024 B, MXFP8 528 B) + bf16 Q + fp32 out + ids."""
     return topk * MAIN_ENTRY_BYTES[cache] + window * row_bytes + 64 * 512 * 2 + 64 * 512 * 4 + topk * 4
+
+
+def select_bytes(n_entries: int, wl) -> int:
+    """Workspace bytes one query's selection reads and writes: its fp32
+    scores (and HSI block maxima), the top-k (and pool) ids."""
+    hsi = wl.hsi and not wl.layers
+    return 4 * n_entries + (4 * (-(-n_entries // 8)) + 4 * wl.hsi_blocks if hsi else 0) + 4 * wl.topk
 
 
 def index_chunk(per_query_bytes: int, queries: int, budget: int = 16 << 30) -> int:
@@ -250,14 +261,15 @@ class DecodeStep(StepBase):
         self.pool = torch.empty((B, 1, wl.hsi_blocks), dtype=torch.int32, device=device) if wl.hsi else None
         self.ws = torch.empty(csa.index_workspace_bytes(self.cfg, B, 1, self.N), dtype=torch.uint8, device=device)
         self.out = torch.empty((B, 1, 64, 512), dtype=torch.float32, device=device)
-        self.stages = ["compress", "index_topk", "attend"]
+        self.stages = ["compress", "index_score", "index_select", "attend"]
         self.launches_per_step = 4  # compress, score, select, attend
         eb = idx_entry_bytes(wl)
         self.stage_bytes = {"compress": B * (r * 1024 + (288 + eb if wl.cache == "fp4" else 1280)),
-                            "index_topk": B * self.N * eb,
+                            "index_score": B * self.N * eb,
+                            "index_select": B * select_bytes(self.N, wl),
                             "attend": B * attend_query_bytes(wl.cache, wl.topk, wl.window, swa_row_bytes(wl))}
-        self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_tc_kernel + select_kernel",
-                              "attend": "attend_rows_kernel"}
+        self.stage_kernels = {"compress": "compress_kernel", "index_score": "score_tc_kernel",
+                              "index_select": "select_kernel", "attend": "attend_rows_kernel"}
         if wl.swa_fp8:
             self.stages.insert(1, "swa_encode")
             self.launches_per_step += 1
@@ -271,8 +283,10 @@ class DecodeStep(StepBase):
         c = [
             lambda: csa.compress(self.cfg, d["x"], d["pos0"], self.merge_w, self.w_idx, self.main, self.idx,
                                  self.n_entries, status=st),
-            lambda: csa.index_topk(self.cfg, d["q_idx"], d["q_pos"], self.idx, self.n_entries, self.N, self.topk,
-                                   self.ws, pool_out=self.pool, status=st),
+            lambda: csa.index_score(self.cfg, d["q_idx"], d["q_pos"], self.idx, self.n_entries, self.N, self.ws,
+                                    hsi=self.pool is not None, status=st),
+            lambda: csa.index_select(self.cfg, d["q_pos"], self.idx, self.n_entries, self.N, self.topk, self.ws,
+                                     pool_out=self.pool, status=st),
             lambda: csa.attend(self.cfg, d["q"], self.main, self.n_entries, self.topk,
                                self.swa8 if self.wl.swa_fp8 else d["swa"], d["swa_len"], d["swa_pos0"], d["q_pos"],
                                self.out, status=st),
@@ -318,16 +332,18 @@ class PrefillStep(StepBase):
         self.chunk = index_chunk(per_q, B * Tq)
         self.ws = torch.empty(per_q * self.chunk, dtype=torch.uint8, device=device)
         self.out = torch.empty((B, Tq, 64, 512), dtype=torch.float32, device=device)
-        self.stages = ["compress", "index_topk", "attend"]
-        chunks = -(-B * Tq // self.chunk)
-        self.launches_per_step = 1 + 2 * chunks + 1
+        if self.chunk < B * Tq:
+            raise SystemExit("the indexer workspace of %s does not hold every query in one pass" % wl.name)
+        self.stages = ["compress", "index_score", "index_select", "attend"]
+        self.launches_per_step = 4
         pairs = sum(min((ctx + t - (r - 1)) // r + 1, self.N) for t in range(Tq)) * B
         self.stage_bytes = {"compress": B * (Tq // r) * (r * 1024 + 360),
-                            "index_topk": B * self.N * IDX_ENTRY_BYTES[wl.cache] + B * Tq * (8192 + 2048),
+                            "index_score": B * self.N * IDX_ENTRY_BYTES[wl.cache] + B * Tq * (8192 + 2048),
+                            "index_select": B * Tq * select_bytes(self.N, wl),
                             "attend": B * Tq * attend_query_bytes(wl.cache, wl.topk, wl.window)}
-        self.stage_flops = {"index_topk": pairs * 8192, "attend": B * Tq * 4 * 64 * 512 * (wl.topk + wl.window)}
-        self.stage_kernels = {"compress": "compress_kernel", "index_topk": "score_tc_kernel + select_kernel",
-                              "attend": "attend_rows_kernel"}
+        self.stage_flops = {"index_score": pairs * 8192, "attend": B * Tq * 4 * 64 * 512 * (wl.topk + wl.window)}
+        self.stage_kernels = {"compress": "compress_kernel", "index_score": "score_tc_kernel",
+                              "index_select": "select_kernel", "attend": "attend_rows_kernel"}
         self.units = B * Tq
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "query_tokens": Tq, "entries": self.N,
                           "index_pairs": pairs}
@@ -608,39 +624,18 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--impl", default="own", choices=["own", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
-    ws, rank, local = dist_setup()
-    if args.impl == "reference":
-        run_reference(args, ws, rank)
-        barrier(ws)
-        return
-
+def time_step(step, steps, warmup, flush, ws):
+    """Warm-up, then K graph replays of the whole step (each after an L2
+    flush, bracketed by CUDA events on the launching stream), one graph per
+    stage replayed back to back after the same flush, the eager step through
+    the Python API, and warm-L2 replays."""
     import torch
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    step = make_step(args.workload, dev, seed_offset=rank)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
     nst = len(step.stages)
-
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.fill_(1)
         step.step()
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0, "device status %d" % int(step.status.item())
-
     # the step and each of its stages captured once as CUDA graphs (decode
     # steps are a handful of short kernels: replaying a graph removes the
     # host-side launch gaps between them)
@@ -659,14 +654,11 @@ def main():
         flush.fill_(2)
         g_step.replay()
     torch.cuda.synchronize()
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier(ws)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for k in range(args.steps):
+    for k in range(steps):
         flush.fill_(k & 0xFF)
         evs[k][0].record()
         g_step.replay()
@@ -674,15 +666,10 @@ def main():
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(ws)
-    clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = max_over_ranks(sum(step_ms), ws)
-    ms_per_step = total_ms / args.steps
-    value = ws * step.units * args.steps / (total_ms / 1e3)
-
     # per-stage durations (stage graphs back to back after the flush) and
     # the same step launched eagerly through the Python API
-    n_stage = min(args.steps, 50)
+    n_stage = min(steps, 50)
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(n_stage)]
     for k in range(n_stage):
         flush.fill_(k & 0xFF)
@@ -702,9 +689,102 @@ def main():
         g_step.replay()
         wev[k][1].record()
     torch.cuda.synchronize()
-    stage_ms = {s: statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in sev) for i, s in enumerate(step.stages)}
-    eager_ms = statistics.fmean(e[0].elapsed_time(e[nst]) for e in eev)
-    warm_ms = statistics.fmean(a.elapsed_time(b) for a, b in wev)
+    assert int(step.status.item()) == 0
+    return {"step_ms": step_ms, "wall": wall, "g_step": g_step,
+            "stage_ms": {s: statistics.fmean(e[i].elapsed_time(e[i + 1]) for e in sev)
+                         for i, s in enumerate(step.stages)},
+            "eager_ms": statistics.fmean(e[0].elapsed_time(e[nst]) for e in eev),
+            "warm_ms": statistics.fmean(a.elapsed_time(b) for a, b in wev)}
+
+
+def roofline_of(step, stage_ms):
+    """Roofline of the dominant stage (the longest): its algorithmic FLOPs
+    against the sustained tensor peak where the stage is a contraction with a
+    FLOP count (prefill indexer), else its algorithmic bytes against the
+    measured HBM copy bandwidth; DRAM traffic per launch from the ncu capture
+    named in TRAFFIC, when there is one of the current kernels."""
+    hbm, tflops_sus, src = peaks()
+    dom = max(stage_ms, key=stage_ms.get)
+    flops = getattr(step, "stage_flops", {}).get(dom)
+    traffic, traffic_src = TRAFFIC.get(step.wl.name, {}).get(dom, (None, None))
+    if step.B != step.wl.batch:
+        traffic, traffic_src = None, None  # the captures are of the workload's own batch
+    if flops is not None:
+        # f16 operands run at the bf16 rate; the sustained figure, the kernel
+        # runs inside a long step
+        ach = flops / (stage_ms[dom] / 1e3) / 1e12
+        return {"bound": "tensor", "kernel": step.stage_kernels[dom], "stage": dom, "achieved": ach,
+                "peak": tflops_sus, "unit": "TFLOP/s", "frac": ach / tflops_sus, "traffic": traffic,
+                "traffic_source": traffic_src,
+                "peak_source": ("of measured (MEASURED_PEAKS.json bf16_tflops_sustained, f16 = bf16 rate)"
+                                if src == "measured" else "of fallback"),
+                "algorithmic_flops_per_launch": flops, "launch_ms": stage_ms[dom]}
+    ach = step.stage_bytes[dom] / (stage_ms[dom] / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": step.stage_kernels[dom], "stage": dom, "achieved": ach, "peak": hbm,
+            "unit": "GB/s", "frac": ach / hbm, "traffic": traffic, "traffic_source": traffic_src,
+            "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "of fallback",
+            "algorithmic_bytes_per_launch": step.stage_bytes[dom], "launch_ms": stage_ms[dom]}
+
+
+def measure_target(name, dev, flush, steps, warmup):
+    """One of the workloads with a stated target, measured in the same run:
+    whole-step graph replays after an L2 flush, per-stage times, the
+    roofline of its dominant stage, and the target beside the figure."""
+    import torch
+    step = make_step(name, dev)
+    t = time_step(step, steps, warmup, flush, 1)
+    ms = statistics.fmean(t["step_ms"])
+    out = {"value": step.units / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+           "config": dict({"workload": name}, **step.cfg_extra), "stage_ms": t["stage_ms"],
+           "roofline": roofline_of(step, t["stage_ms"]), "target": TARGETS[name],
+           "gpu_launches": step.launches_per_step * steps}
+    del step, t
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences per GPU instead of the workload's own (smaller profiling captures)")
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-targets", action="store_true",
+                    help="skip the decoder-group and prefill target workloads measured beside the default one")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.batch is not None:
+        wl = synth.WORKLOADS[args.workload]
+        synth.WORKLOADS[args.workload] = dataclasses.replace(wl, batch=args.batch)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        barrier(ws)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    step = make_step(args.workload, dev, seed_offset=rank)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    t = time_step(step, args.steps, args.warmup, flush, ws)
+    clk = clocks.stop()
+    step_ms, stage_ms = t["step_ms"], t["stage_ms"]
+    total_ms = max_over_ranks(sum(step_ms), ws)
+    ms_per_step = total_ms / args.steps
+    value = ws * step.units * args.steps / (total_ms / 1e3)
+    eager_ms, warm_ms, wall = t["eager_ms"], t["warm_ms"], t["wall"]
 
     # end to end through the Python API with host buffers: the step's inputs
     # in two pinned host buffers, each copied in with one H2D copy (the
@@ -775,48 +855,41 @@ def main():
     e2e_eager_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), ws) / e2e_steps
     assert int(step.status.item()) == 0
 
-    hbm, tflops_sus, src = peaks()
-    dom = max(stage_ms, key=stage_ms.get)
-    flops = getattr(step, "stage_flops", {}).get(dom)
-    if flops is not None:
-        # prefill contractions: against the tensor-core peak (f16 operands have
-        # the bf16 rate; the sustained figure, the kernel runs inside a long step)
-        ach = flops / (stage_ms[dom] / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": step.stage_kernels[dom], "achieved": ach, "peak": tflops_sus,
-                "unit": "TFLOP/s", "frac": ach / tflops_sus, "traffic": None,
-                "peak_source": ("of measured (MEASURED_PEAKS.json bf16_tflops_sustained, f16 = bf16 rate)"
-                                if src == "measured" else "of fallback"),
-                "algorithmic_flops_per_launch": flops, "launch_ms": stage_ms[dom]}
-    else:
-        ach = step.stage_bytes[dom] / (stage_ms[dom] / 1e3) / 1e9
-        traffic, traffic_src = TRAFFIC.get(step.wl.name, {}).get(dom, (None, None))
-        roof = {"bound": "hbm", "kernel": step.stage_kernels[dom], "achieved": ach, "peak": hbm, "unit": "GB/s",
-                "frac": ach / hbm, "traffic": traffic, "traffic_source": traffic_src,
-                "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "of fallback",
-                "algorithmic_bytes_per_launch": step.stage_bytes[dom], "launch_ms": stage_ms[dom]}
+    roof = roofline_of(step, stage_ms)
+    wl_name, units, launches, cfg_extra = step.wl.name, step.units, step.launches_per_step, step.cfg_extra
+    wl_obj = step.wl
+    targets = None
+    if ws == 1 and not args.no_targets and args.workload == DEFAULT_WORKLOAD and args.batch is None:
+        del step, e2e, packs, dbuf
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        targets = {name: measure_target(name, dev, flush, steps=max(10, min(args.steps, 40)), warmup=args.warmup)
+                   for name in TARGETS}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(step.wl, args.cpu_seconds)
+        cpu = cpu_baseline(wl_obj, args.cpu_seconds)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-                "config": dict({"workload": step.wl.name}, **step.cfg_extra,
-                               **{"cache": step.wl.cache, "topk": step.wl.topk, "window": step.wl.window,
-                                  "hsi": step.wl.hsi, "operands": "f16 tensor-core operands, fp32 accumulate",
+                "config": dict({"workload": wl_name}, **cfg_extra,
+                               **{"cache": wl_obj.cache, "topk": wl_obj.topk, "window": wl_obj.window,
+                                  "hsi": wl_obj.hsi, "operands": "f16 tensor-core operands, fp32 accumulate",
                                   "l2": "flushed before every step (256 MiB write)",
                                   "launch": "CUDA graph of the step, captured once and replayed per step"}),
                 "stage_ms": stage_ms, "eager_ms_per_step": eager_ms,
-                "warm_l2": {"value": ws * step.units / (max_over_ranks(warm_ms, ws) / 1e3), "unit": UNIT,
+                "warm_l2": {"value": ws * units / (max_over_ranks(warm_ms, ws) / 1e3), "unit": UNIT,
                             "ms_per_step": warm_ms},
                 "median_ms_per_step": statistics.median(step_ms), "wall_s": wall,
                 "roofline": roof, "cpu_baseline": cpu,
-                "e2e": {"value": ws * step.units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "e2e": {"value": ws * units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                         "launch": "csa.capture of the step: H2D of the first calls' inputs, the API calls with the "
                                   "attention inputs' H2D overlapped on a second stream, one D2H copy",
-                        "eager_value": ws * step.units / (e2e_eager_ms / 1e3)},
-                "gpu_launches": step.launches_per_step * args.steps, "clocks": clk}
+                        "eager_value": ws * units / (e2e_eager_ms / 1e3)},
+                "gpu_launches": launches * args.steps, "clocks": clk}
+        if targets is not None:
+            line["targets"] = targets
         print(json.dumps(line), flush=True)
     barrier(ws)
     if ws > 1:

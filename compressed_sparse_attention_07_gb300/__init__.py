@@ -101,6 +101,10 @@ def load():
         L.csa2_index_workspace_bytes.argtypes = [vp, i32, i32, i32, i32]
         L.csa2_index_topk.restype = i32
         L.csa2_index_topk.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp, vp]
+        L.csa2_index_score.restype = i32
+        L.csa2_index_score.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, i32, vp, sz, vp, vp]
+        L.csa2_index_select.restype = i32
+        L.csa2_index_select.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, sz, vp, vp]
         L.csa2_attend.restype = i32
         L.csa2_attend.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, C.c_float, vp, vp, vp, vp]
         L.csa2_gather_dequant.restype = i32
@@ -201,6 +205,30 @@ def index_topk(cfg: Cfg, q_idx, q_pos, idx: PagedCache, n_entries, max_entries: 
         C.byref(cfg), B, Tq, _bf16(q_idx, "q_idx"), _ptr(head_w, torch.float32, "head_w"),
         _ptr(q_pos, torch.int64, "q_pos"), C.byref(d), _ptr(n_entries, torch.int32, "n_entries"), int(max_entries),
         _ptr(pool, torch.int32, "pool"), _ptr(topk_out, torch.int32, "topk_out"),
+        _ptr(pool_out, torch.int32, "pool_out"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def index_score(cfg: Cfg, q_idx, q_pos, idx: PagedCache, n_entries, max_entries: int, workspace, head_w=None,
+                pool=None, hsi=False, status=None, stream=None):
+    """a3/a5/a6 scores of every query into `workspace` (which holds them all), for index_select."""
+    B, Tq = q_idx.shape[:2]
+    d = idx.desc()
+    _check("csa2_index_score", load().csa2_index_score(
+        C.byref(cfg), B, Tq, _bf16(q_idx, "q_idx"), _ptr(head_w, torch.float32, "head_w"),
+        _ptr(q_pos, torch.int64, "q_pos"), C.byref(d), _ptr(n_entries, torch.int32, "n_entries"), int(max_entries),
+        _ptr(pool, torch.int32, "pool"), 1 if hsi else 0, _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def index_select(cfg: Cfg, q_pos, idx: PagedCache, n_entries, max_entries: int, topk_out, workspace, pool=None,
+                 pool_out=None, status=None, stream=None):
+    """a4/a5 from the scores index_score left in `workspace` -> topk_out (and pool_out)."""
+    B, Tq = q_pos.shape[:2]
+    d = idx.desc()
+    _check("csa2_index_select", load().csa2_index_select(
+        C.byref(cfg), B, Tq, _ptr(q_pos, torch.int64, "q_pos"), C.byref(d), _ptr(n_entries, torch.int32, "n_entries"),
+        int(max_entries), _ptr(pool, torch.int32, "pool"), _ptr(topk_out, torch.int32, "topk_out"),
         _ptr(pool_out, torch.int32, "pool_out"), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _ptr(status, torch.int32, "status"), _stream(stream)))
 

@@ -195,6 +195,50 @@ int32_t csa2_index_topk(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16
                                        static_cast<cudaStream_t>(stream)));
 }
 
+// The indexer in two calls: checks of csa2_index_topk, plus a workspace
+// that holds every query (one scoring and one selection launch).
+static int32_t check_split(const csa2_cfg* cfg, int32_t B, int32_t Tq, int32_t max_entries, const int32_t* pool,
+                           size_t workspace_bytes) {
+  const size_t per_q = index_query_ws_bytes(*cfg, max_entries, pool != nullptr);
+  if ((int64_t)B * Tq > 65535) return CSA2_ERR_UNSUPPORTED;
+  if (workspace_bytes / per_q < (size_t)B * Tq) return CSA2_ERR_CAPACITY;
+  return CSA2_OK;
+}
+
+int32_t csa2_index_score(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q_idx, const float* head_w,
+                         const int64_t* q_pos, const csa2_cache* idx_cache, const int32_t* n_entries,
+                         int32_t max_entries, const int32_t* pool, int32_t hsi, void* workspace,
+                         size_t workspace_bytes, int32_t* status, void* stream) {
+  bool empty;
+  if (hsi && pool) return CSA2_ERR_INVALID_ARG;
+  // a stand-in for the outputs (never written here) so that the shared
+  // checks apply; an HSI request is checked as a pool output
+  const int32_t* fake_out = reinterpret_cast<const int32_t*>(uintptr_t{256});
+  int32_t rc = check_index(cfg, B, Tq, q_idx, head_w, q_pos, idx_cache, n_entries, max_entries, pool, fake_out,
+                           hsi ? fake_out : nullptr, workspace, workspace_bytes, status, &empty);
+  if (rc != CSA2_OK || empty) return rc;
+  rc = check_split(cfg, B, Tq, max_entries, pool, workspace_bytes);
+  if (rc != CSA2_OK) return rc;
+  return cuda_status(launch_index_score(*cfg, B, Tq, q_idx, head_w, q_pos, *idx_cache, n_entries, max_entries, pool,
+                                        hsi != 0, workspace, workspace_bytes, status,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int32_t csa2_index_select(const csa2_cfg* cfg, int32_t B, int32_t Tq, const int64_t* q_pos,
+                          const csa2_cache* idx_cache, const int32_t* n_entries, int32_t max_entries,
+                          const int32_t* pool, int32_t* topk_out, int32_t* pool_out, void* workspace,
+                          size_t workspace_bytes, int32_t* status, void* stream) {
+  bool empty;
+  const uint16_t* fake_q = reinterpret_cast<const uint16_t*>(uintptr_t{256});
+  int32_t rc = check_index(cfg, B, Tq, fake_q, nullptr, q_pos, idx_cache, n_entries, max_entries, pool, topk_out,
+                           pool_out, workspace, workspace_bytes, status, &empty);
+  if (rc != CSA2_OK || empty) return rc;
+  rc = check_split(cfg, B, Tq, max_entries, pool, workspace_bytes);
+  if (rc != CSA2_OK) return rc;
+  return cuda_status(launch_index_select(*cfg, B, Tq, q_pos, n_entries, max_entries, pool, topk_out, pool_out,
+                                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream)));
+}
+
 int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q, const csa2_cache* main_cache,
                     const int32_t* n_entries, const int32_t* topk, const void* swa, int32_t S,
                     const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos, float scale, float* out,

@@ -950,58 +950,128 @@ size_t index_query_ws_bytes(const csa2_cfg& cfg, int max_entries, bool reindex) 
   return b + slots;
 }
 
-cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx,
-                              const float* head_w, const int64_t* q_pos, const csa2_cache& idx_c,
-                              const int32_t* n_entries, int max_entries, const int32_t* pool,
-                              int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
-                              int32_t* status, cudaStream_t stream) {
-  const int Q = B * Tq;
-  if (Q == 0) return cudaSuccess;
-  const bool reindex = pool != nullptr;
+namespace {
+
+// Where the indexer's per-query data sits in a workspace, and the shape of
+// the selection launch, for one call over B * Tq queries.  The layout does
+// not depend on whether the HSI pool is asked for: with hsi_blocks > 0 (Full)
+// the block maxima always have their place after the scores.
+struct IndexPlan {
+  int Q, chunk;
+  bool reindex;
+  float* scores;
+  int64_t stride;
+  float* bmax_area;  // block maxima (Full with hsi_blocks > 0), else null
+  uint32_t* krange;
+  int kr_stride;
+  bool fused;
+  int n_sel, cs;
+  bool small;
+};
+
+cudaError_t plan_index(const csa2_cfg& cfg, int B, int Tq, int max_entries, bool reindex, bool hsi_out, void* ws,
+                       size_t ws_bytes, IndexPlan* p) {
+  p->Q = B * Tq;
+  p->reindex = reindex;
   const size_t per_q = index_query_ws_bytes(cfg, max_entries, reindex);
-  const int chunk = (int)std::min<size_t>(std::min<size_t>((size_t)Q, ws_bytes / per_q), 65535);  // grid y
-  if (chunk < 1) return cudaErrorInvalidValue;
-  float* scores = static_cast<float*>(ws);
-  const int64_t stride = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
-  char* cur = static_cast<char*>(ws) + align256((size_t)chunk * stride * sizeof(float));
-  float* bmax = nullptr;
-  if (!reindex && pool_out) {
-    bmax = reinterpret_cast<float*>(cur);
-    cur += align256((size_t)chunk * ((max_entries + 7) / 8) * sizeof(float));
+  p->chunk = (int)std::min<size_t>(std::min<size_t>((size_t)p->Q, ws_bytes / per_q), 65535);  // grid y
+  if (p->chunk < 1) return cudaErrorInvalidValue;
+  p->scores = static_cast<float*>(ws);
+  p->stride = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
+  char* cur = static_cast<char*>(ws) + align256((size_t)p->chunk * p->stride * sizeof(float));
+  p->bmax_area = nullptr;
+  if (!reindex && cfg.hsi_blocks > 0) {
+    p->bmax_area = reinterpret_cast<float*>(cur);
+    cur += align256((size_t)p->chunk * ((max_entries + 7) / 8) * sizeof(float));
   }
-  uint32_t* krange = reinterpret_cast<uint32_t*>(cur);
-  const int kr_stride = score_range_slots(score_tiles(cfg, max_entries, reindex));
+  p->krange = reinterpret_cast<uint32_t*>(cur);
+  p->kr_stride = score_range_slots(score_tiles(cfg, max_entries, reindex));
   // a cluster of up to 8 CTAs per selection, each with at least kMinCtaKeys
   // positions, but no more CTAs than one wave holds (one CTA per SM)
   const int64_t n_max = reindex ? (int64_t)cfg.hsi_blocks * kHsiBlock : (int64_t)max_entries;
   // Full with HSI: one CTA selects the pool and then the top-k among the
   // pool's positions, when they fit one CTA's registers and the pool has at
   // least k blocks besides the forced one (what makes it exact)
-  const bool fused = !reindex && pool_out && (int64_t)cfg.hsi_blocks * kHsiBlock <= kRound &&
-                     cfg.hsi_blocks >= cfg.topk + 1;
-  const int n_sel = (!reindex && pool_out && !fused) ? 2 : 1;
-  const int64_t sel_groups = (int64_t)std::min(chunk, Q) * n_sel;
-  int cs = 1;
-  while (!fused && cs < 8 && (int64_t)cs * kMinCtaKeys < n_max && 2 * cs * sel_groups <= num_sms()) cs <<= 1;
-  const size_t sel_smem = sizeof(SelShared);
+  p->fused = !reindex && hsi_out && (int64_t)cfg.hsi_blocks * kHsiBlock <= kRound && cfg.hsi_blocks >= cfg.topk + 1;
+  p->n_sel = (!reindex && hsi_out && !p->fused) ? 2 : 1;
+  const int64_t sel_groups = (int64_t)std::min(p->chunk, p->Q) * p->n_sel;
+  p->cs = 1;
+  while (!p->fused && p->cs < 8 && (int64_t)p->cs * kMinCtaKeys < n_max && 2 * p->cs * sel_groups <= num_sms())
+    p->cs <<= 1;
   // one CTA holding every position of each selection: the register-resident
   // path only, compiled without the general one
-  const bool small = cs == 1 && (fused ? ((int64_t)max_entries + 7) / 8 <= kRound : n_max <= kRound);
-  auto sel = small ? select_kernel<true> : select_kernel<false>;
+  p->small = p->cs == 1 && (p->fused ? ((int64_t)max_entries + 7) / 8 <= kRound : n_max <= kRound);
+  return cudaSuccess;
+}
+
+cudaError_t run_scores(const IndexPlan& p, const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx,
+                       const float* head_w, const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
+                       int max_entries, const int32_t* pool, bool hsi_out, int* n_slots, int32_t* status,
+                       cudaStream_t stream) {
+  return launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, p.scores,
+                         p.stride, hsi_out ? p.bmax_area : nullptr, p.krange, p.kr_stride, n_slots, status, num_sms(),
+                         stream);
+}
+
+cudaError_t run_select(const IndexPlan& p, const csa2_cfg& cfg, int q0, int nq, int Tq, const int64_t* q_pos,
+                       const int32_t* n_entries, int max_entries, const int32_t* pool, int n_slots,
+                       int32_t* topk_out, int32_t* pool_out, cudaStream_t stream) {
+  const size_t sel_smem = sizeof(SelShared);
+  auto sel = p.small ? select_kernel<true> : select_kernel<false>;
   cudaFuncSetAttribute(sel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel_smem);
-  for (int q0 = 0; q0 < Q; q0 += chunk) {
-    const int nq = std::min(chunk, Q - q0);
+  return launch_k(sel, dim3(p.cs, nq, p.n_sel), dim3(kSelThreads), sel_smem, stream, p.cs, q0, Tq, cfg.ratio,
+                  cfg.topk, cfg.hsi_blocks, (int64_t)max_entries, q_pos, n_entries, pool, (const float*)p.scores,
+                  (const float*)(pool_out ? p.bmax_area : nullptr), p.stride, (const uint32_t*)p.krange, p.kr_stride,
+                  n_slots, topk_out, pool_out, p.fused ? 1 : 0);
+}
+
+}  // namespace
+
+cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx,
+                              const float* head_w, const int64_t* q_pos, const csa2_cache& idx_c,
+                              const int32_t* n_entries, int max_entries, const int32_t* pool,
+                              int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
+                              int32_t* status, cudaStream_t stream) {
+  if (B * Tq == 0) return cudaSuccess;
+  IndexPlan p;
+  cudaError_t e = plan_index(cfg, B, Tq, max_entries, pool != nullptr, pool_out != nullptr, ws, ws_bytes, &p);
+  if (e != cudaSuccess) return e;
+  for (int q0 = 0; q0 < p.Q; q0 += p.chunk) {
+    const int nq = std::min(p.chunk, p.Q - q0);
     int n_slots = 0;
-    cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, scores,
-                                    stride, bmax, krange, kr_stride, &n_slots, status, num_sms(), stream);
+    e = run_scores(p, cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, pool_out != nullptr,
+                   &n_slots, status, stream);
     if (e != cudaSuccess) return e;
-    e = launch_k(sel, dim3(cs, nq, n_sel), dim3(kSelThreads), sel_smem, stream, cs,
-                 q0, Tq, cfg.ratio, cfg.topk, cfg.hsi_blocks, (int64_t)max_entries, q_pos, n_entries, pool,
-                 (const float*)scores, (const float*)bmax, stride, (const uint32_t*)krange, kr_stride, n_slots,
-                 topk_out, pool_out, fused ? 1 : 0);
+    e = run_select(p, cfg, q0, nq, Tq, q_pos, n_entries, max_entries, pool, n_slots, topk_out, pool_out, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_index_score(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx, const float* head_w,
+                               const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
+                               int max_entries, const int32_t* pool, bool hsi_out, void* ws, size_t ws_bytes,
+                               int32_t* status, cudaStream_t stream) {
+  if (B * Tq == 0) return cudaSuccess;
+  IndexPlan p;
+  cudaError_t e = plan_index(cfg, B, Tq, max_entries, pool != nullptr, hsi_out, ws, ws_bytes, &p);
+  if (e != cudaSuccess) return e;
+  if (p.chunk < p.Q) return cudaErrorInvalidValue;  // the workspace holds every query
+  int n_slots = 0;
+  return run_scores(p, cfg, 0, p.Q, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, hsi_out, &n_slots,
+                    status, stream);
+}
+
+cudaError_t launch_index_select(const csa2_cfg& cfg, int B, int Tq, const int64_t* q_pos, const int32_t* n_entries,
+                                int max_entries, const int32_t* pool, int32_t* topk_out, int32_t* pool_out, void* ws,
+                                size_t ws_bytes, cudaStream_t stream) {
+  if (B * Tq == 0) return cudaSuccess;
+  IndexPlan p;
+  cudaError_t e = plan_index(cfg, B, Tq, max_entries, pool != nullptr, pool_out != nullptr, ws, ws_bytes, &p);
+  if (e != cudaSuccess) return e;
+  if (p.chunk < p.Q) return cudaErrorInvalidValue;
+  const int n_slots = score_slots_used(cfg, 0, p.Q, Tq, max_entries, pool != nullptr, num_sms());
+  return run_select(p, cfg, 0, p.Q, Tq, q_pos, n_entries, max_entries, pool, n_slots, topk_out, pool_out, stream);
 }
 
 }  // namespace csa2

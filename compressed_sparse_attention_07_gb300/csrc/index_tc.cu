@@ -596,35 +596,58 @@ static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaSt
   return launch_k(kern, dim3(splits, groups), dim3(Sh::kThreads), smem, stream, 0, a);
 }
 
+namespace {
+
+// Grid of the scorer for queries [q0, q0 + nq): query groups sharing every
+// K tile and the tile ranges (scoring CTAs) per group.
+struct ScoreGrid {
+  int qpc, seg, gps, groups;
+  int64_t per;
+  int splits;
+};
+
+ScoreGrid score_grid(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_entries, bool gather, int num_sms) {
+  // query groups sharing every K tile: runs of 4 queries when the chunk splits
+  // into them without crossing a sequence (prefill chunks); whole sequences of
+  // a chunk of whole sequences otherwise (multi-query decode: up to 6 queries
+  // in one group, longer blocks in groups of 4); single queries else
+  ScoreGrid g{1, 1, 1, 0, 0, 0};
+  if (!gather && Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) {
+    g.qpc = 4;
+    g.seg = 4;
+  } else if (!gather && Tq > 1 && q0 % Tq == 0 && nq % Tq == 0) {
+    g.qpc = Tq <= 6 ? 6 : 4;
+    g.seg = Tq;
+  }
+  g.gps = (g.seg + g.qpc - 1) / g.qpc;
+  g.groups = nq / g.seg * g.gps;
+  const int64_t tiles = gather ? ((int64_t)cfg.hsi_blocks * kHsiBlock + 127) / 128 : (max_entries + 127) / 128;
+  // CTAs per query group: one wave of one CTA per SM when there are few
+  // groups (latency-bound: every CTA starts at once), else two waves for
+  // balance; at least 4 tiles each
+  const int waves = (g.qpc == 1 && (int64_t)g.groups * 8 > num_sms) ? 2 : 1;
+  const int64_t want = std::max<int64_t>(1, (int64_t)waves * num_sms / std::max(g.groups, 1));
+  const int64_t cap = gather ? kMaxGatherTiles : kMaxTilesPerCta;
+  g.per = std::min<int64_t>(cap, std::max<int64_t>(4, (tiles + want - 1) / want));
+  g.splits = (int)((tiles + g.per - 1) / g.per);
+  return g;
+}
+
+}  // namespace
+
+int score_slots_used(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_entries, bool gather, int num_sms) {
+  return score_grid(cfg, q0, nq, Tq, max_entries, gather, num_sms).splits;
+}
+
 cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
                             const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
                             int64_t max_entries, const int32_t* pool, float* scores, int64_t stride, float* bmax,
                             uint32_t* krange, int kr_stride, int* n_slots, int32_t* status, int num_sms,
                             cudaStream_t stream) {
   const bool gather = pool != nullptr;
-  // query groups sharing every K tile: runs of 4 queries when the chunk splits
-  // into them without crossing a sequence (prefill chunks); whole sequences of
-  // a chunk of whole sequences otherwise (multi-query decode: up to 6 queries
-  // in one group, longer blocks in groups of 4); single queries else
-  int qpc = 1, seg = 1;
-  if (!gather && Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) {
-    qpc = 4;
-    seg = 4;
-  } else if (!gather && Tq > 1 && q0 % Tq == 0 && nq % Tq == 0) {
-    qpc = Tq <= 6 ? 6 : 4;
-    seg = Tq;
-  }
-  const int gps = (seg + qpc - 1) / qpc;
-  const int groups = nq / seg * gps;
-  const int64_t tiles = gather ? ((int64_t)cfg.hsi_blocks * kHsiBlock + 127) / 128 : (max_entries + 127) / 128;
-  // CTAs per query group: one wave of one CTA per SM when there are few
-  // groups (latency-bound: every CTA starts at once), else two waves for
-  // balance; at least 4 tiles each
-  const int waves = (qpc == 1 && (int64_t)groups * 8 > num_sms) ? 2 : 1;
-  const int64_t want = std::max<int64_t>(1, (int64_t)waves * num_sms / std::max(groups, 1));
-  const int64_t cap = gather ? kMaxGatherTiles : kMaxTilesPerCta;
-  const int64_t per = std::min<int64_t>(cap, std::max<int64_t>(4, (tiles + want - 1) / want));
-  const int splits = (int)((tiles + per - 1) / per);
+  const ScoreGrid sg = score_grid(cfg, q0, nq, Tq, max_entries, gather, num_sms);
+  const int qpc = sg.qpc, seg = sg.seg, gps = sg.gps, groups = sg.groups, splits = sg.splits;
+  const int64_t per = sg.per;
   if (splits > kr_stride) return cudaErrorInvalidValue;
   *n_slots = splits;
   ScoreArgs a{q0, Tq, cfg.ratio, seg, gps, (cfg.formats & CSA2_FMT_IDX_QFP4) ? 1 : 0,

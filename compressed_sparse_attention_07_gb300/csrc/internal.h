@@ -67,6 +67,10 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
                             uint32_t* krange, int kr_stride, int* n_slots, int32_t* status, int num_sms,
                             cudaStream_t stream);
 
+// Scoring CTAs per query (key-range slots written) of launch_score_tc for
+// the same arguments.
+int score_slots_used(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_entries, bool gather, int num_sms);
+
 // Key-range slots per query in the indexer workspace: one per scoring CTA
 // (at least four 128-entry tiles each).
 inline int score_range_slots(int64_t tiles) { return (int)((tiles + 3) / 4); }
@@ -86,6 +90,17 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
                               const int32_t* n_entries, int max_entries, const int32_t* pool,
                               int32_t* topk_out, int32_t* pool_out, void* ws, size_t ws_bytes,
                               int32_t* status, cudaStream_t stream);
+
+// The two halves of launch_index_topk for a workspace that holds every
+// query: the scores (and HSI block maxima when hsi_out) of all B * Tq
+// queries, then the selection from them.
+cudaError_t launch_index_score(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q_idx, const float* head_w,
+                               const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
+                               int max_entries, const int32_t* pool, bool hsi_out, void* ws, size_t ws_bytes,
+                               int32_t* status, cudaStream_t stream);
+cudaError_t launch_index_select(const csa2_cfg& cfg, int B, int Tq, const int64_t* q_pos, const int32_t* n_entries,
+                                int max_entries, const int32_t* pool, int32_t* topk_out, int32_t* pool_out, void* ws,
+                                size_t ws_bytes, cudaStream_t stream);
 
 cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q, const csa2_cache& main_c,
                           const int32_t* n_entries, const int32_t* topk, const void* swa, int S,

@@ -178,6 +178,29 @@ CSA2_API int32_t csa2_index_topk(const csa2_cfg* cfg, int32_t B, int32_t Tq, con
                         int32_t* topk_out, int32_t* pool_out, void* workspace,
                         size_t workspace_bytes, int32_t* status, void* stream);
 
+/* a3..a6 and a4/a5 as two calls, for a caller that wants the scoring and
+ * the selection on their own (to time or overlap them): csa2_index_score
+ * writes the scores of all B*Tq queries (and, with hsi != 0 on a Full call,
+ * the HSI block maxima) into `workspace`; csa2_index_select then selects
+ * topk_out (and pool_out) from that workspace.  Together they compute what
+ * csa2_index_topk computes with the same arguments.  Arguments and checks
+ * are csa2_index_topk's, plus: the workspace must hold every query
+ * (csa2_index_workspace_bytes(cfg, B, Tq, max_entries, pool != NULL)
+ * bytes, else CSA2_ERR_CAPACITY); B*Tq <= 65535 (else CSA2_ERR_UNSUPPORTED);
+ * hsi != 0 only without `pool` (CSA2_ERR_INVALID_ARG).  The select call
+ * must follow the score call on the same stream with the same cfg, B, Tq,
+ * q_pos, n_entries, max_entries and pool, the same workspace untouched in
+ * between, and pool_out != NULL only if hsi was set; otherwise its output
+ * is unspecified (every access stays inside the workspace). */
+CSA2_API int32_t csa2_index_score(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q_idx,
+                                  const float* head_w, const int64_t* q_pos, const csa2_cache* idx_cache,
+                                  const int32_t* n_entries, int32_t max_entries, const int32_t* pool, int32_t hsi,
+                                  void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+CSA2_API int32_t csa2_index_select(const csa2_cfg* cfg, int32_t B, int32_t Tq, const int64_t* q_pos,
+                                   const csa2_cache* idx_cache, const int32_t* n_entries, int32_t max_entries,
+                                   const int32_t* pool, int32_t* topk_out, int32_t* pool_out, void* workspace,
+                                   size_t workspace_bytes, int32_t* status, void* stream);
+
 /* a7 -- sparse attention (hn.213312.xyz sec. 2.2.2 "global KV and local KV
  * concatenated and scored with Q", sec. 3.3.1 "key = value"; 36kr "CSA2").
  * For query (b, t) and head h: rows E = {main entries topk[b][t][i] >= 0} and

@@ -606,3 +606,44 @@ def test_degenerate_queries_nothing_visible_and_no_rows():
     fin = np.isfinite(o_lse)
     np.testing.assert_allclose(g_lse[fin], o_lse[fin], rtol=0, atol=1e-3)
     assert P.attention_rel_err(g_out[:, 1:], o_out[:, 1:]) <= P.ATT_TOL
+
+
+@pytest.mark.parametrize("mode", ["full_hsi", "full", "reindex", "multi_query"])
+def test_index_in_two_calls_equals_index_topk(mode):
+    """csa2_index_score followed by csa2_index_select gives what
+    csa2_index_topk gives, bit for bit, on integer inputs (exact scores, ties
+    broken by id): Full with and without the HSI pool, Reindex over a pool,
+    and a multi-query block of 5 positions per sequence."""
+    B, N, k, nb = 3, 9000, 128, 200
+    oc, pc = _idx_caches(B, N, "fp4", seed=31, integer=True, dup=True)
+    Tq = 5 if mode == "multi_query" else 1
+    q_idx = synth.integer_bf16(synth.rng(31, "q"), (B, Tq, H, CI), -1, 1)
+    q_pos = np.array([[8995 + t for t in range(Tq)], [7000 + t for t in range(Tq)], [4000 + t for t in range(Tq)]],
+                     np.int64)
+    n_ent = np.array([9000, 8000, 9000], np.int32)
+    cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=nb if mode != "full" else 0)
+    pool = None
+    if mode == "reindex":
+        _, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, want_pool=True)
+        pool = _paged.dev(o_pool)
+    want_pool = mode == "full_hsi"
+    ref_top, ref_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, pool=None if pool is None else o_pool,
+                                   want_pool=want_pool)
+    ws = torch.empty(csa.index_workspace_bytes(cfg, B, Tq, N, reindex=pool is not None), dtype=torch.uint8,
+                     device="cuda")
+    ws.fill_(0xAB)  # no state carried in from elsewhere
+    topk = torch.full((B, Tq, k), -7, dtype=torch.int32, device="cuda")
+    pool_out = torch.full((B, Tq, nb), -7, dtype=torch.int32, device="cuda") if want_pool else None
+    st = _status()
+    qp, ne = _paged.dev(q_pos), _paged.dev(n_ent)
+    csa.index_score(cfg, _paged.dev(q_idx), qp, pc, ne, N, ws, pool=pool, hsi=want_pool, status=st)
+    csa.index_select(cfg, qp, pc, ne, N, topk, ws, pool=pool, pool_out=pool_out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(topk.cpu().numpy(), ref_top)
+    if want_pool:
+        np.testing.assert_array_equal(pool_out.cpu().numpy(), ref_pool)
+    # a workspace short of one query's worth for all of them is refused
+    small = torch.empty(ws.numel() - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(csa.CsaError):
+        csa.index_score(cfg, _paged.dev(q_idx), qp, pc, ne, N, small, pool=pool, hsi=want_pool, status=st)

@@ -135,6 +135,30 @@ __device__ __forceinline__ int kslot(int i) {
   return ((u ^ ((u >> 3) & 7)) << 2) | (i & 3);
 }
 
+// Sort keys[0, total) ascending (total <= 4096, the largest pool of blocks)
+// with a bitonic network over the next power of two >= total, at least
+// kSelThreads; the slots from total on take 0xFFFFFFFF and end up last.
+// Every thread of the CTA calls it; keys[] has room for 4096 entries.
+__device__ void sort_positions(uint32_t* keys, uint32_t total) {
+  uint32_t n = kSelThreads;
+  while (n < total) n <<= 1;
+  for (uint32_t i = total + threadIdx.x; i < n; i += kSelThreads) keys[i] = 0xFFFFFFFFu;
+  __syncthreads();
+  for (uint32_t k2 = 2; k2 <= n; k2 <<= 1) {
+    for (uint32_t j = k2 >> 1; j > 0; j >>= 1) {
+      for (uint32_t p = threadIdx.x; p < n / 2; p += kSelThreads) {
+        const uint32_t i = 2 * j * (p / j) + (p % j), ixj = i + j;  // the pair (i, i + j), bit j of i clear
+        const uint32_t x = keys[i], y = keys[ixj];
+        if ((x > y) == ((i & k2) == 0)) {
+          keys[i] = y;
+          keys[ixj] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 // Select the k largest keys among n positions of `vals` by (key desc,
 // position asc); `forced` (>= 0) always takes a slot.  Writes the chosen ids
 // in ascending position order to out[k], -1 padded.  The cs CTAs of a
@@ -264,7 +288,6 @@ __device__ bool select_sampled(const float* vals, int64_t n, int k, int64_t forc
   }
   // ---- the selection (need keys, and the forced position), sorted by position
   if (threadIdx.x == 0) s.grand = 0;
-  s.keys[threadIdx.x] = 0xFFFFFFFFu;
   __syncthreads();
   for (uint32_t i = threadIdx.x; i < c; i += kSelThreads)
     if (s.cand[i] >= tx) s.keys[atomicAdd(&s.grand, 1u)] = s.merged[i];
@@ -272,19 +295,7 @@ __device__ bool select_sampled(const float* vals, int64_t n, int k, int64_t forc
   if (threadIdx.x == 0 && forced >= 0) s.keys[s.grand++] = (uint32_t)forced;
   __syncthreads();
   const uint32_t total = s.grand;
-  for (int k2 = 2; k2 <= kSelThreads; k2 <<= 1) {
-    for (int j = k2 >> 1; j > 0; j >>= 1) {
-      const int i = threadIdx.x, ixj = i ^ j;
-      if (ixj > i) {
-        const uint32_t x = s.keys[i], y = s.keys[ixj];
-        if ((x > y) == ((i & k2) == 0)) {
-          s.keys[i] = y;
-          s.keys[ixj] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  sort_positions(s.keys, total);
   for (int i = threadIdx.x; i < k; i += kSelThreads) out[i] = (uint32_t)i < total ? idmap(s.keys[i]) : -1;
   return true;
 }
@@ -529,7 +540,7 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
   }
   if (kOne && kept) {
     // the selection: the positions above the bin, then the bin's keys >= T,
-    // sorted by position (bitonic sort, one element per thread)
+    // sorted by position
     const uint32_t na = s.above_n;
     s.keys[threadIdx.x] = threadIdx.x < na ? s.all[threadIdx.x] : 0xFFFFFFFFu;
     if (threadIdx.x == 0) s.grand = na;
@@ -538,19 +549,7 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
       if (s.cand[i] >= kept_x) s.keys[atomicAdd(&s.grand, 1u)] = s.merged[i];
     __syncthreads();
     const uint32_t total = s.grand;  // need (+ the forced position) <= k
-    for (int k2 = 2; k2 <= kSelThreads; k2 <<= 1) {
-      for (int j = k2 >> 1; j > 0; j >>= 1) {
-        const int i = threadIdx.x, ixj = i ^ j;
-        if (ixj > i) {
-          const uint32_t x = s.keys[i], y = s.keys[ixj];
-          if ((x > y) == ((i & k2) == 0)) {
-            s.keys[i] = y;
-            s.keys[ixj] = x;
-          }
-        }
-        __syncthreads();
-      }
-    }
+    sort_positions(s.keys, total);
     for (int i = threadIdx.x; i < k; i += kSelThreads) out[i] = (uint32_t)i < total ? idmap(s.keys[i]) : -1;
     return;
   }
@@ -864,6 +863,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
                                                                 const int32_t* __restrict__ pool, const float* scores,
                                                                 const float* bmax, int64_t score_stride,
                                                                 const uint32_t* krange, int kr_stride, int n_slots,
+                                                                int64_t part_tq, int64_t part_total, int part_grid,
                                                                 int32_t* topk_out, int32_t* pool_out, int fused) {
   griddep_wait();  // the scores are the previous kernel's output
   griddep_launch();
@@ -882,7 +882,15 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
   {
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
     const uint32_t* kr = krange + (int64_t)qc * kr_stride * 2;
-    for (int i = threadIdx.x; i < n_slots; i += kSelThreads) {
+    int ns = n_slots;
+    if (part_grid > 0) {
+      // the scorer shared a flattened range of part_total tiles among
+      // part_grid CTAs: this query's slots belong to the CTAs whose ranges
+      // meet its tiles [qc tq, (qc + 1) tq)
+      auto cta_of = [&](int64_t x) { return ((x + 1) * part_grid - 1) / part_total; };
+      ns = (int)(cta_of((int64_t)(qc + 1) * part_tq - 1) - cta_of((int64_t)qc * part_tq) + 1);
+    }
+    for (int i = threadIdx.x; i < ns; i += kSelThreads) {
       lo = min(lo, kr[2 * i]);
       hi = max(hi, kr[2 * i + 1]);
     }
@@ -1004,17 +1012,48 @@ cudaError_t plan_index(const csa2_cfg& cfg, int B, int Tq, int max_entries, bool
   return cudaSuccess;
 }
 
+// How the scoring CTAs of a chunk map to key-range slots: n_slots per query
+// (one per CTA of the query's tile ranges), or the flattened partition of the
+// warp-specialized scorer (grid > 0).
+struct SlotMap {
+  int n_slots;
+  int64_t tq, total;
+  int grid;
+};
+
+// Which scorer a chunk uses and its slot map (decided the same way for the
+// score and the selection launches).
+SlotMap slot_map(const csa2_cfg& cfg, int q0, int nq, int Tq, int max_entries, bool reindex, bool* ws) {
+  int g = 0;
+  // single-query groups over FP4 pages (the decode scans): the warp-specialized scorer
+  const bool single = reindex || !((Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) || (Tq > 1 && q0 % Tq == 0 && nq % Tq == 0));
+  *ws = !reindex && single && score_ws_usable(cfg, nq, max_entries, num_sms(), &g);
+  if (*ws) {
+    const int64_t tq = ((int64_t)max_entries + 127) / 128;
+    return SlotMap{0, tq, (int64_t)nq * tq, g};
+  }
+  return SlotMap{score_slots_used(cfg, q0, nq, Tq, max_entries, reindex, num_sms()), 0, 0, 0};
+}
+
 cudaError_t run_scores(const IndexPlan& p, const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx,
                        const float* head_w, const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
-                       int max_entries, const int32_t* pool, bool hsi_out, int* n_slots, int32_t* status,
+                       int max_entries, const int32_t* pool, bool hsi_out, SlotMap* sm, int32_t* status,
                        cudaStream_t stream) {
-  return launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, p.scores,
-                         p.stride, hsi_out ? p.bmax_area : nullptr, p.krange, p.kr_stride, n_slots, status, num_sms(),
-                         stream);
+  bool ws = false;
+  *sm = slot_map(cfg, q0, nq, Tq, max_entries, pool != nullptr, &ws);
+  if (ws)
+    return launch_score_ws(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, p.scores, p.stride,
+                           hsi_out ? p.bmax_area : nullptr, p.krange, p.kr_stride, sm->grid, status, stream);
+  int n_slots = 0;
+  const cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool,
+                                        p.scores, p.stride, hsi_out ? p.bmax_area : nullptr, p.krange, p.kr_stride,
+                                        &n_slots, status, num_sms(), stream);
+  sm->n_slots = n_slots;
+  return e;
 }
 
 cudaError_t run_select(const IndexPlan& p, const csa2_cfg& cfg, int q0, int nq, int Tq, const int64_t* q_pos,
-                       const int32_t* n_entries, int max_entries, const int32_t* pool, int n_slots,
+                       const int32_t* n_entries, int max_entries, const int32_t* pool, const SlotMap& sm,
                        int32_t* topk_out, int32_t* pool_out, cudaStream_t stream) {
   const size_t sel_smem = sizeof(SelShared);
   auto sel = p.small ? select_kernel<true> : select_kernel<false>;
@@ -1022,7 +1061,7 @@ cudaError_t run_select(const IndexPlan& p, const csa2_cfg& cfg, int q0, int nq, 
   return launch_k(sel, dim3(p.cs, nq, p.n_sel), dim3(kSelThreads), sel_smem, stream, p.cs, q0, Tq, cfg.ratio,
                   cfg.topk, cfg.hsi_blocks, (int64_t)max_entries, q_pos, n_entries, pool, (const float*)p.scores,
                   (const float*)(pool_out ? p.bmax_area : nullptr), p.stride, (const uint32_t*)p.krange, p.kr_stride,
-                  n_slots, topk_out, pool_out, p.fused ? 1 : 0);
+                  sm.n_slots, sm.tq, sm.total, sm.grid, topk_out, pool_out, p.fused ? 1 : 0);
 }
 
 }  // namespace
@@ -1038,11 +1077,11 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
   if (e != cudaSuccess) return e;
   for (int q0 = 0; q0 < p.Q; q0 += p.chunk) {
     const int nq = std::min(p.chunk, p.Q - q0);
-    int n_slots = 0;
+    SlotMap sm;
     e = run_scores(p, cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, pool_out != nullptr,
-                   &n_slots, status, stream);
+                   &sm, status, stream);
     if (e != cudaSuccess) return e;
-    e = run_select(p, cfg, q0, nq, Tq, q_pos, n_entries, max_entries, pool, n_slots, topk_out, pool_out, stream);
+    e = run_select(p, cfg, q0, nq, Tq, q_pos, n_entries, max_entries, pool, sm, topk_out, pool_out, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -1057,8 +1096,8 @@ cudaError_t launch_index_score(const csa2_cfg& cfg, int B, int Tq, const uint16_
   cudaError_t e = plan_index(cfg, B, Tq, max_entries, pool != nullptr, hsi_out, ws, ws_bytes, &p);
   if (e != cudaSuccess) return e;
   if (p.chunk < p.Q) return cudaErrorInvalidValue;  // the workspace holds every query
-  int n_slots = 0;
-  return run_scores(p, cfg, 0, p.Q, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, hsi_out, &n_slots,
+  SlotMap sm;
+  return run_scores(p, cfg, 0, p.Q, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, hsi_out, &sm,
                     status, stream);
 }
 
@@ -1070,8 +1109,9 @@ cudaError_t launch_index_select(const csa2_cfg& cfg, int B, int Tq, const int64_
   cudaError_t e = plan_index(cfg, B, Tq, max_entries, pool != nullptr, pool_out != nullptr, ws, ws_bytes, &p);
   if (e != cudaSuccess) return e;
   if (p.chunk < p.Q) return cudaErrorInvalidValue;
-  const int n_slots = score_slots_used(cfg, 0, p.Q, Tq, max_entries, pool != nullptr, num_sms());
-  return run_select(p, cfg, 0, p.Q, Tq, q_pos, n_entries, max_entries, pool, n_slots, topk_out, pool_out, stream);
+  bool use_ws = false;
+  const SlotMap sm = slot_map(cfg, 0, p.Q, Tq, max_entries, pool != nullptr, &use_ws);
+  return run_select(p, cfg, 0, p.Q, Tq, q_pos, n_entries, max_entries, pool, sm, topk_out, pool_out, stream);
 }
 
 }  // namespace csa2

@@ -28,6 +28,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "score_common.cuh"
 #include "tc.cuh"
 
 namespace csa2 {
@@ -81,28 +82,9 @@ struct ScoreArgs {
   int32_t* status;
 };
 
-// Two E4M3 scale bytes (low byte first) -> each as a broadcast f16x2 (exact).
-__device__ __forceinline__ void e4m3_pair_bcast(uint32_t two, uint32_t& lo2, uint32_t& hi2) {
-  uint32_t f;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f) : "h"((uint16_t)(two & 0xFFFFu)));
-  asm("prmt.b32 %0, %1, 0, 0x1010;" : "=r"(lo2) : "r"(f));
-  asm("prmt.b32 %0, %1, 0, 0x3232;" : "=r"(hi2) : "r"(f));
-}
-
-// Four bytes of packed E2M1 pairs -> four f16x2 (element 2i of a byte in the low half).
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-      : "r"(w));
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
+using score::e2m1x8_to_f16x2;
+using score::e4m3_pair_bcast;
+using score::hmul2;
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
@@ -301,39 +283,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
       v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
                                                (row % kIdxHeads) * kIdxDim + k));
     uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    if (a.q_fp4) {
-      // FP4 indexer query: this thread's 8 channels and its neighbour lane's
-      // form one 16-channel group; encode (E4M3 scale nearest amax / 6, E2M1
-      // codes, both by exact comparisons) and read back, exactly
-      float f[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        f[2 * j] = __uint_as_float(w[j] << 16);
-        f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-      float amax = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      const float sc = e4m3_pos(e4m3_scale_code(amax));
-#pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] = e2m1_to_float(e2m1_code(f[j], sc)) * sc;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (kBf16) {
-          w[j] = (__float_as_uint(f[2 * j]) >> 16) | (__float_as_uint(f[2 * j + 1]) & 0xFFFF0000u);
-        } else {
-          const __half2 h2 = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
-          w[j] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-      }
-    } else if (!kBf16) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
-        w[j] = *reinterpret_cast<const uint32_t*>(&h2);
-      }
-    }
+    score::q_operand8<kBf16>(w, a.q_fp4 != 0);
     *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   for (int i = tid; i < QPC * kIdxHeads; i += kConsumers)

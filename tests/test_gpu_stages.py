@@ -647,3 +647,33 @@ def test_index_in_two_calls_equals_index_topk(mode):
     small = torch.empty(ws.numel() - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(csa.CsaError):
         csa.index_score(cfg, _paged.dev(q_idx), qp, pc, ne, N, small, pool=pool, hsi=want_pool, status=st)
+
+
+@pytest.mark.parametrize("nb", [2048, 4096])
+def test_large_pools_over_many_blocks_are_ascending_and_exact(nb):
+    """A Full layer with HSI over more than 32768 blocks (the decoder group's
+    262144 entries hold 32768): the pool selection runs over rows longer
+    than one CTA's registers, through the sampled one-pass selection (pool
+    of 2048) or the staged passes (pool of 4096), and its ids must come out
+    ascending.  Random inputs (few ties: the sampled path) compared up to
+    near-ties; integer inputs with ties compared bit for bit."""
+    B, N, k = 1, 280000, 512
+    for integer in (False, True):
+        oc, pc = _idx_caches(B, N, "fp4", seed=32 + integer, integer=integer, dup=integer)
+        q_idx = (synth.integer_bf16(synth.rng(32, "q"), (B, 1, H, CI), -1, 1) if integer else
+                 synth.normal_bf16(synth.rng(32, "q"), (B, 1, H, CI)))
+        q_pos = np.array([[N - 1]], np.int64)
+        n_ent = np.array([N], np.int32)
+        cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=nb)
+        g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+        o_top, o_pool, s = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, want_pool=True,
+                                             want_scores=True)
+        gp = g_pool.reshape(B, nb)
+        assert np.all(np.diff(gp[0][gp[0] >= 0]) > 0), "pool ids not ascending"
+        assert np.all(np.diff(g_top[0, 0][g_top[0, 0] >= 0]) > 0), "top-k ids not ascending"
+        if integer:
+            np.testing.assert_array_equal(g_top, o_top)
+            np.testing.assert_array_equal(g_pool, o_pool)
+        else:
+            assert P.pool_mismatch(gp, o_pool.reshape(B, nb), s.reshape(B, -1)) == 0
+            assert P.topk_mismatch(g_top.reshape(B, k), o_top.reshape(B, k), s.reshape(B, -1), k, exact=False) == 0

@@ -72,8 +72,10 @@ namespace {
 __global__ void __launch_bounds__(128) swa_encode_kernel(int T, int S, const uint16_t* __restrict__ x,
                                                          const int64_t* __restrict__ row0, uint8_t* rows,
                                                          int32_t* status) {
+  // no early launch of the next kernel: the attention reads window rows
+  // before it waits for its predecessor, so a kernel that writes them lets
+  // its successor start only when it has completed
   griddep_wait();
-  griddep_launch();
   const int i = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
   const int64_t r0 = __ldg(row0 + b);
   if (r0 < 0 || r0 + T > S) {

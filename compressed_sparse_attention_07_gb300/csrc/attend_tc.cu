@@ -47,7 +47,6 @@ namespace csa2 {
 namespace {
 
 constexpr int kThreads = 512;  // four threads per row of a 128-row tile
-constexpr uint32_t kSpin = 1u << 26;
 constexpr int kStageRow = 304;                 // staged FP4 row: 256 codes + 32 scales + pad (bank spread)
 constexpr int kStageRowChunk = 272;            // staged bf16 row chunk: 256 + pad
 constexpr int kStageBytes = 128 * kStageRow;   // 38912
@@ -289,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
     if (ph == 1 && n == n_chunks) {
       // ---------------- softmax over all rows (phase A complete)
       const int e = n - 1;
-      const bool ok = tc::mbar_wait(&cdone[e & 1], (e >> 1) & 1, kSpin);
+      const bool ok = tc::mbar_wait(&cdone[e & 1], (e >> 1) & 1);
       waited = e;
       if (!ok) atomicExch(&abort_flag, 1);
       tc::fence_after_sync();
@@ -368,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
     if (n >= 2) {  // the MMAs that read this C tile two chunks ago must be done
       const int e = n - 2;
       if (e > waited) {
-        if (!tc::mbar_wait(&cdone[e & 1], (e >> 1) & 1, kSpin)) atomicExch(&abort_flag, 1);
+        if (!tc::mbar_wait(&cdone[e & 1], (e >> 1) & 1)) atomicExch(&abort_flag, 1);
         waited = e;
       }
     }
@@ -444,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
   // ---------------- epilogue: O^T -> out
   cp_wait<0>();  // no copies into this CTA's shared memory outlive it
   if (last_issued > waited) {
-    const bool ok = tc::mbar_wait(&cdone[last_issued & 1], (last_issued >> 1) & 1, kSpin);
+    const bool ok = tc::mbar_wait(&cdone[last_issued & 1], (last_issued >> 1) & 1);
     if (!ok) aborted = true;
   }
   tc::fence_after_sync();
@@ -625,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
     }
   }
   cp_wait<0>();
-  bool ok = tc::mbar_wait(&cdone, 0, kSpin);
+  bool ok = tc::mbar_wait(&cdone, 0);
   tc::fence_after_sync();
 
   // ---- partial softmax over this tile's rows
@@ -714,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
     if (t == 0 && a.lse)
       a.lse[(int64_t)qi * kHeads + hg * HG + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
-  ok = tc::mbar_wait(&cdone, 1, kSpin) && ok;
+  ok = tc::mbar_wait(&cdone, 1) && ok;
   tc::fence_after_sync();
   __syncthreads();
   // ---- push the scaled partial output to the CTA owning each output slice:
@@ -986,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (tid == 0) tc::mma_commit(&bar);
-  ok = tc::mbar_wait(&bar, 0, kSpin) && ok;
+  ok = tc::mbar_wait(&bar, 0) && ok;
   tc::fence_after_sync();
 
   // ---- partial softmax over the tile's rows (thread: row r, heads 16p..16p+15)
@@ -1042,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mma_commit(&bar);
   }
-  ok = tc::mbar_wait(&bar, 1, kSpin) && ok;
+  ok = tc::mbar_wait(&bar, 1) && ok;
   tc::fence_after_sync();
   // ---- this tile's unscaled partial output into its own shared memory (Q and
   // C are free now), [chunk][head][channel]: a warp's stores are 128
@@ -1122,6 +1121,375 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
+// ---------------------------------------------------------------------------
+// Query-cluster variant for decode (top-k + window <= 640 rows): NC = 4 or 5
+// CTAs per query token, each holding R = 160 or 128 of the query's rows for
+// all 64 heads, the query's CTAs forming a cluster.  Chosen over the
+// row-tile kernel so that every query's cluster fits in one wave of CTAs
+// (NC = 4 when five CTAs per query would not).  Per CTA:
+//  - before waiting for the selection (the kernel is launched while it
+//    runs): the query rows (bf16 -> f16) and this CTA's window rows, which
+//    no kernel of the step writes, are loaded into shared memory;
+//  - after it: this CTA's selected entries are gathered (id, block table,
+//    row) and decoded into the K-major row tile C;
+//  - S^T = C . Q^T on the tensor cores (M = 128 rows; with R = 160 a second
+//    block covers rows 32..159 and only its last 32 lanes are read), a
+//    partial softmax per head over the CTA's rows, O^T = C^T . P^T;
+//  - the merge: after one cluster barrier every CTA pushes its unscaled
+//    partial output, in 16 pieces of 128 channels x 16 heads, into the
+//    owner of each piece (piece i -> CTA i mod NC) with 16-byte
+//    distributed-shared-memory stores, together with its (max, sum) per
+//    head; after a second barrier each owner forms
+//    out = sum_t 2^(m_t - M) O_t / L in tile order, M = max_t m_t,
+//    L = sum_t 2^(m_t - M) l_t, and writes its pieces.
+constexpr int kQcMaxRows = 160;
+constexpr size_t kQcQBytes = (size_t)kAllHeads * kDim * 2;   // 65536; after S: P^T and scratch
+constexpr size_t kQcSmem = kQcQBytes + (size_t)kQcMaxRows * kDim * 2;   // 229376
+constexpr int kQcPieceFloats = 128 * 16;                                // 128 channels x 16 heads
+
+template <int kDtype, bool kSwaFp8, int NC>
+__global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
+  constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
+  constexpr int R = NC == 4 ? 160 : 128;  // rows of this CTA: 8-row groups t, t + NC, ...
+  constexpr int NG = R / 8;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* qs = smem;                                    // Q [64 heads x 512] f16, K-major
+  uint8_t* pt = smem;                                    // after S: P^T [64 heads x R rows] f16, K-major
+  float* scr = reinterpret_cast<float*>(smem + kAllHeads * R * 2);  // after S: reduction scratch
+  uint8_t* ctile = smem + kQcQBytes;                     // C [R rows x 512] f16, K-major
+  float* recv = reinterpret_cast<float*>(smem);          // after O: received pieces [slot][tile][128 ch][16 h]
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ uint32_t vmask[NG / 4 + 1];                 // valid rows of the tile
+  __shared__ float m_all[NC][kAllHeads], l_all[NC][kAllHeads];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & 127, p = tid >> 7, quad = warp & 3;
+  const uint32_t lane_base = 32 * quad;
+  const int t = (int)tc::cluster_rank();
+  const int qi = blockIdx.y, b = qi / a.Tq;
+  const int n_slots = (a.tiles_main + a.tiles_win) * 128;
+  const int rl = lane & 7, uq = lane >> 3;
+  // global slot of local row i
+  auto slot_of = [&](int i) { return 8 * ((i >> 3) * NC + t) + (i & 7); };
+
+  // loads of one 8-row group (this lane: row rl, 16-byte units 4k + uq) and
+  // its decode into C
+  struct Raw {
+    uint4 v[16];
+    uint32_t s[4];
+  };
+  auto load_group = [&](int32_t sidx, Raw& w) {
+    if (sidx >= 0) {
+      const int64_t page = sidx / kPage;
+      const int sl = sidx % kPage;
+      if (kMainFp4) {
+        const uint4* g = reinterpret_cast<const uint4*>(a.mc.data + page * kMainFp4Data + sl * (kDim / 2));
+        const uint16_t* gs = reinterpret_cast<const uint16_t*>(a.mc.scales + page * kMainFp4Scales + sl * (kDim / 16));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          w.v[k] = __ldg(g + 4 * k + uq);
+          w.s[k] = __ldg(gs + 4 * k + uq);
+        }
+      } else {
+        const uint4* g = reinterpret_cast<const uint4*>(a.mc.data + page * kMainBf16Data + sl * (kDim * 2));
+#pragma unroll
+        for (int k = 0; k < 16; ++k) w.v[k] = __ldg(g + 4 * k + uq);
+      }
+    } else if (sidx <= -2) {
+      if (kSwaFp8) {
+        const uint4* g =
+            reinterpret_cast<const uint4*>(a.swa8 + ((int64_t)b * a.S + (-2 - (int64_t)sidx)) * kSwaFp8Row);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w.v[k] = __ldg(g + 4 * k + uq);
+        w.v[8] = __ldg(g + 32);
+      } else {
+        const uint4* g = reinterpret_cast<const uint4*>(a.swa + ((int64_t)b * a.S + (-2 - (int64_t)sidx)) * kDim);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) w.v[k] = __ldg(g + 4 * k + uq);
+      }
+    }
+  };
+  auto store_group = [&](int gi, int32_t sidx, const Raw& w, bool main_row) {
+    const int rho = 8 * gi + rl;
+    if (main_row && kMainFp4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int q = 4 * k + uq;
+        const uint32_t s_lo = f16x2_scale(w.s[k] & 0xFFu), s_hi = f16x2_scale((w.s[k] >> 8) & 0xFFu);
+        const uint32_t w4[4] = {w.v[k].x, w.v[k].y, w.v[k].z, w.v[k].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (sidx >= 0) {
+            uint32_t h4[4];
+            e2m1x8_to_f16x2(w4[i], h4);
+            const uint32_t s2 = i < 2 ? s_lo : s_hi;
+            o = make_uint4(hmul2(h4[0], s2), hmul2(h4[1], s2), hmul2(h4[2], s2), hmul2(h4[3], s2));
+          }
+          *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 32 * q + 8 * i, kDim)) = o;
+        }
+      }
+    } else if (!main_row && kSwaFp8) {
+      const uint32_t sw[4] = {w.v[8].x, w.v[8].y, w.v[8].z, w.v[8].w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int u = 4 * k + uq, blk = u >> 1;
+        uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (sidx != -1) mxfp8x16_to_f16x2(w.v[k], (sw[blk >> 2] >> (8 * (blk & 3))) & 0xFFu, o);
+        *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 16 * u, kDim)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 16 * u + 8, kDim)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint4 o = sidx == -1 ? make_uint4(0, 0, 0, 0)
+                                   : make_uint4(bf16x2_to_f16x2(w.v[k].x), bf16x2_to_f16x2(w.v[k].y),
+                                                bf16x2_to_f16x2(w.v[k].z), bf16x2_to_f16x2(w.v[k].w));
+        *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 8 * (4 * k + uq), kDim)) = o;
+      }
+    }
+    if (uq == 0 && sidx != -1) atomicOr(&vmask[rho >> 5], 1u << (rho & 31));
+  };
+  // this warp's groups: w and (when R = 160) w + 16 for warps 0..3
+  const int g0 = warp, g1 = warp + 16;
+  const bool has1 = g1 < NG;
+  const bool win0 = slot_of(8 * g0) >= a.tiles_main * 128;
+  const bool win1 = has1 && slot_of(8 * g1) >= a.tiles_main * 128;
+
+  // ---------------- before the selection has finished: Q, window rows
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (tid < NG / 4 + 1) vmask[tid] = 0u;
+  {
+    const int h = 8 * (warp & 7) + rl, u0 = 32 * (warp >> 3);
+    const uint4* g = reinterpret_cast<const uint4*>(a.q + ((int64_t)qi * kHeads + h) * kDim);
+    uint4 qv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) qv[k] = __ldg(g + u0 + 4 * k + uq);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<uint4*>(qs + tc::kmajor_off(h, 8 * (u0 + 4 * k + uq), kDim)) =
+          make_uint4(bf16x2_to_f16x2(qv[k].x), bf16x2_to_f16x2(qv[k].y), bf16x2_to_f16x2(qv[k].z),
+                     bf16x2_to_f16x2(qv[k].w));
+  }
+  __syncthreads();  // vmask cleared
+  Raw w0, w1;
+  int32_t s0 = -1, s1 = -1;
+  if (win0) {
+    s0 = slot_source(a, qi, b, slot_of(8 * g0 + rl));
+    load_group(s0, w0);
+    store_group(g0, s0, w0, false);
+  }
+  if (win1) {
+    s1 = slot_source(a, qi, b, slot_of(8 * g1 + rl));
+    load_group(s1, w1);
+    store_group(g1, s1, w1, false);
+  }
+
+  griddep_wait();  // the selected ids are the previous kernel's output
+  griddep_launch();
+  if (warp == 0) {
+    tc::tmem_alloc(&tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  // ---------------- the selected entries
+  if (!win0) s0 = slot_source(a, qi, b, slot_of(8 * g0 + rl));
+  if (has1 && !win1) s1 = slot_source(a, qi, b, slot_of(8 * g1 + rl));
+  if (kMainFp4) {  // both groups' rows in flight at once (20 registers each)
+    if (!win0) load_group(s0, w0);
+    if (has1 && !win1) load_group(s1, w1);
+    if (!win0) store_group(g0, s0, w0, true);
+    if (has1 && !win1) store_group(g1, s1, w1, true);
+  } else {         // 1 KB bf16 rows: one group at a time
+    if (!win0) {
+      load_group(s0, w0);
+      store_group(g0, s0, w0, true);
+    }
+    if (has1 && !win1) {
+      load_group(s1, w1);
+      store_group(g1, s1, w1, true);
+    }
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = tmem_base;
+  bool ok = true;
+
+  // ---- S^T = C . Q^T: block 0 rows 0..127 -> columns 0..63; with R = 160
+  // block 1 rows 32..159 -> columns 64..127 (lanes 96..127 hold rows 128..159)
+  constexpr uint32_t kIdescS = tc::idesc_f16(128, kAllHeads, false, false, false, false);
+  constexpr uint32_t kIdescO = tc::idesc_f16(128, kAllHeads, false, false, true, false);
+  if (tid == 0) {
+#pragma unroll 1
+    for (int blk = 0; blk < (R > 128 ? 2 : 1); ++blk) {
+      const uint32_t cb = tc::smem_u32(ctile) + (blk ? 4 * kDim * 16 : 0);  // row group 4 = row 32
+#pragma unroll 4
+      for (int ks = 0; ks < kDim / 16; ++ks) {
+        const uint64_t ad = tc::sdesc(cb + ks * 256, 128, kDim * 16);
+        const uint64_t bd = tc::sdesc(tc::smem_u32(qs) + ks * 256, 128, kDim * 16);
+        tc::mma_ss(tb + 64 * blk, ad, bd, kIdescS, ks > 0 ? 1u : 0u);
+      }
+    }
+    tc::mma_commit(&bar);
+  }
+  ok = tc::mbar_wait(&bar, 0) && ok;
+  tc::fence_after_sync();
+
+  // ---- partial softmax over the CTA's rows: thread (r, p) holds row r of
+  // block 0 and, in lane quarter 3 with R = 160, row 128 + (r - 96), for
+  // heads 16p .. 16p + 15
+  const float sc2 = a.scale * kLog2e;
+  const bool extra = R > 128 && quad == 3;
+  const bool valid0 = (vmask[r >> 5] >> (r & 31)) & 1u;
+  const int r1 = 128 + (r - 96);
+  const bool valid1 = extra && ((vmask[r1 >> 5] >> (r1 & 31)) & 1u);
+  float v[16], v1[16];
+  {
+    uint32_t wv[16];
+    tc::tmem_ld16(tc::taddr(tb, lane_base, 16 * p), wv);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = valid0 ? __uint_as_float(wv[j]) * sc2 : -INFINITY;
+    if (R > 128) {
+      tc::tmem_ld16(tc::taddr(tb, lane_base, 64 + 16 * p), wv);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v1[j] = valid1 ? __uint_as_float(wv[j]) * sc2 : -INFINITY;
+    }
+  }
+  float* red_m = scr;                    // [4][64]
+  float* red_s = scr + 4 * kAllHeads;    // [4][64]
+  float* mx = scr + 8 * kAllHeads;       // [64]
+  tc::fence_before_sync();
+  __syncthreads();  // every S read from tensor memory: Q's space becomes P^T and scratch
+  tc::fence_after_sync();
+  {
+    float vm[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) vm[j] = R > 128 ? fmaxf(v[j], v1[j]) : v[j];
+    const float wm = warp_reduce16<true>(vm);
+    if ((lane & 1) == 0) red_m[quad * kAllHeads + 16 * p + (lane >> 1)] = wm;
+  }
+  __syncthreads();
+  if (tid < kAllHeads)
+    mx[tid] = fmaxf(fmaxf(red_m[tid], red_m[kAllHeads + tid]), fmaxf(red_m[2 * kAllHeads + tid], red_m[3 * kAllHeads + tid]));
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float mh = mx[16 * p + j];
+    v[j] = (valid0 && mh != -INFINITY) ? exp2f(v[j] - mh) : 0.0f;
+    *reinterpret_cast<__half*>(pt + tc::kmajor_off(16 * p + j, r, R)) = __float2half_rn(v[j]);
+    if (R > 128) {
+      v1[j] = (valid1 && mh != -INFINITY) ? exp2f(v1[j] - mh) : 0.0f;
+      if (extra) *reinterpret_cast<__half*>(pt + tc::kmajor_off(16 * p + j, r1, R)) = __float2half_rn(v1[j]);
+      v[j] += v1[j];
+    }
+  }
+  {
+    const float ws = warp_reduce16<false>(v);
+    if ((lane & 1) == 0) red_s[quad * kAllHeads + 16 * p + (lane >> 1)] = ws;
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  float m_own = 0.0f, l_own = 0.0f;
+  if (tid < kAllHeads) {
+    m_own = mx[tid];
+    l_own = (red_s[tid] + red_s[kAllHeads + tid]) + (red_s[2 * kAllHeads + tid] + red_s[3 * kAllHeads + tid]);
+  }
+
+  // ---- O^T[c] = C[:, chunk c]^T . P^T (C read MN-major)
+  if (tid == 0) {
+    if (ok) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t cbase = tc::smem_u32(ctile) + c * 16 * 128;
+#pragma unroll 2
+        for (int ks = 0; ks < R / 16; ++ks) {
+          const uint64_t ad = tc::sdesc(cbase + ks * 2 * (kDim * 16), kDim * 16, 128);
+          const uint64_t bd = tc::sdesc(tc::smem_u32(pt) + ks * 256, 128, (R / 8) * 128);
+          tc::mma_ss(tb + 128 + 64 * c, ad, bd, kIdescO, ks > 0 ? 1u : 0u);
+        }
+      }
+    }
+    tc::mma_commit(&bar);
+  }
+  ok = tc::mbar_wait(&bar, 1) && ok;
+  tc::fence_after_sync();
+  // every CTA of the cluster has finished reading its Q, P^T and C: their
+  // space receives the pieces
+  tc::fence_before_sync();
+  tc::cluster_sync();
+  tc::fence_after_sync();
+
+  // ---- push: piece (c, p) = channels 128c.., heads 16p..; owner (4c + p) mod NC
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t wv[16];
+    tc::tmem_ld16(tc::taddr(tb, lane_base, 128 + 64 * c + 16 * p), wv);
+    tc::tmem_wait_ld();
+    const int piece = 4 * c + p, owner = piece % NC, ps = piece / NC;
+    const uint32_t dst = tc::map_rank(tc::smem_u32(recv + ((size_t)(ps * NC + t) * 128 + r) * 16), owner);
+#pragma unroll
+    for (int j = 0; j < 16; j += 4)
+      tc::st_dsmem_v4(dst + 4 * j, __uint_as_float(wv[j]), __uint_as_float(wv[j + 1]), __uint_as_float(wv[j + 2]),
+                      __uint_as_float(wv[j + 3]));
+  }
+  if (tid < kAllHeads) {
+#pragma unroll
+    for (int o = 0; o < NC; ++o) {
+      tc::st_dsmem(tc::map_rank(tc::smem_u32(&m_all[t][tid]), o), m_own);
+      tc::st_dsmem(tc::map_rank(tc::smem_u32(&l_all[t][tid]), o), l_own);
+    }
+  }
+  tc::fence_before_sync();
+  tc::cluster_sync();  // every piece and (max, sum) has arrived
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tb, 512);
+  if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
+
+  // ---- the owned pieces: per-head factors 2^(m_t - M) / L, then the sums
+  constexpr int kSlotsOwned = (16 + NC - 1) / NC;
+  float* fac = recv + (size_t)kSlotsOwned * NC * kQcPieceFloats;  // [NC][64]
+  if (tid < kAllHeads) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int k2 = 0; k2 < NC; ++k2) M = fmaxf(M, m_all[k2][tid]);
+    float L = 0.0f;
+#pragma unroll
+    for (int k2 = 0; k2 < NC; ++k2)
+      if (m_all[k2][tid] != -INFINITY) L += exp2f(m_all[k2][tid] - M) * l_all[k2][tid];
+#pragma unroll
+    for (int k2 = 0; k2 < NC; ++k2)
+      fac[k2 * kAllHeads + tid] = (ok && L > 0.0f && m_all[k2][tid] != -INFINITY) ? exp2f(m_all[k2][tid] - M) / L : 0.0f;
+    if (t == 0 && a.lse)
+      a.lse[(int64_t)qi * kHeads + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  }
+  __syncthreads();
+  for (int ps = 0; ps * NC + t < 16; ++ps) {
+    const int piece = ps * NC + t, c = piece >> 2, pp = piece & 3;
+    const int hl = tid & 15, ch4 = tid >> 4;  // 16 heads x 32 runs of 4 channels
+    const int h = 16 * pp + hl;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int k2 = 0; k2 < NC; ++k2) {
+      const float f = fac[k2 * kAllHeads + h];
+      const float* src = recv + ((size_t)(ps * NC + k2) * 128 + 4 * ch4) * 16 + hl;
+      acc.x = fmaf(f, src[0], acc.x);
+      acc.y = fmaf(f, src[16], acc.y);
+      acc.z = fmaf(f, src[32], acc.z);
+      acc.w = fmaf(f, src[48], acc.w);
+    }
+    *reinterpret_cast<float4*>(a.out + ((int64_t)qi * kHeads + h) * kDim + 128 * c + 4 * ch4) = acc;
+  }
+}
+
 template <int kDtype, bool kSwaFp8>
 cudaError_t launch_rows(const AttArgs& a, int Q, cudaStream_t stream) {
   const int n_tiles = a.tiles_main + a.tiles_win;
@@ -1150,6 +1518,49 @@ cudaError_t launch_rows(const AttArgs& a, int Q, cudaStream_t stream) {
   }
   if (schedulable[n_tiles] < 0) return cudaErrorNotSupported;
   return launch_k(kern, cfg.gridDim, cfg.blockDim, kRowSmem, stream, n_tiles, a);
+}
+
+// Clusters of the query-cluster kernel that fit on the device at once (0:
+// not schedulable), asked once per instantiation.
+template <int kDtype, bool kSwaFp8, int NC>
+int qc_clusters() {
+  static int cached = -1;
+  if (cached < 0) {
+    auto kern = attend_qc_kernel<kDtype, kSwaFp8, NC>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQcSmem);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(NC, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kQcSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = NC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) clusters = 0;
+    (void)cudaGetLastError();
+    cached = clusters;
+  }
+  return cached;
+}
+
+// Query-cluster attention for 4 or 5 row tiles: five CTAs of 128 rows per
+// query when the batch fits one wave that way, else four of 160 rows when
+// that saves a wave.  cudaErrorNotSupported when neither shape can run.
+template <int kDtype, bool kSwaFp8>
+cudaError_t launch_qc(const AttArgs& a, int Q, cudaStream_t stream) {
+  const int c5 = qc_clusters<kDtype, kSwaFp8, 5>(), c4 = qc_clusters<kDtype, kSwaFp8, 4>();
+  if (c5 < 1 && c4 < 1) return cudaErrorNotSupported;
+  const int64_t w5 = c5 > 0 ? (Q + c5 - 1) / c5 : INT64_MAX, w4 = c4 > 0 ? (Q + c4 - 1) / c4 : INT64_MAX;
+  if (w4 < w5) {
+    auto kern = attend_qc_kernel<kDtype, kSwaFp8, 4>;
+    return launch_k(kern, dim3(4, Q), dim3(kThreads), kQcSmem, stream, 4, a);
+  }
+  auto kern = attend_qc_kernel<kDtype, kSwaFp8, 5>;
+  return launch_k(kern, dim3(5, Q), dim3(kThreads), kQcSmem, stream, 5, a);
 }
 
 template <int kDtype>
@@ -1222,6 +1633,14 @@ cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q,
   // query's tiles in one cluster; more: split by head groups (bf16 window
   // rows only)
   const int n_tiles = a.tiles_main + a.tiles_win;
+  if (n_tiles == 4 || n_tiles == 5) {
+    cudaError_t e;
+    if (cfg.cache_dtype == CSA2_CACHE_FP4)
+      e = fp8 ? launch_qc<CSA2_CACHE_FP4, true>(a, Q, stream) : launch_qc<CSA2_CACHE_FP4, false>(a, Q, stream);
+    else
+      e = fp8 ? launch_qc<CSA2_CACHE_BF16, true>(a, Q, stream) : launch_qc<CSA2_CACHE_BF16, false>(a, Q, stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (n_tiles <= kRowMaxTiles) {
     cudaError_t e;
     if (cfg.cache_dtype == CSA2_CACHE_FP4)

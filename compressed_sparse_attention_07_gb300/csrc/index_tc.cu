@@ -48,7 +48,6 @@ struct Shape {
   static constexpr int kStages = kSmemA ? 6 : 2 * kWG;  // ring slots, used in tile order
 };
 constexpr int kABytes = 128 * kIdxDim * 2;  // a decoded K tile in shared memory (f16, K-major)
-constexpr uint32_t kSpin = 1u << 26;
 constexpr int kMaxTilesPerCta = 512;
 constexpr int kMaxGatherTiles = 32;        // gather mode: resolved positions held in shared memory
 
@@ -248,7 +247,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
         int issued = first;
         for (int i = first; i < n_my; ++i) {
           const int s = i % kStages;
-          if (!tc::mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1, kSpin)) {
+          if (!tc::mbar_wait(&empty_bar[s], ((i / kStages) & 1) ^ 1)) {
             report(a.status, CSA2_ERR_TIMEOUT);
             atomicExch(&abort_flag, 1);
             break;
@@ -259,7 +258,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
         }
         // do not leave while copies into this CTA's shared memory are in flight
         for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-          if (!tc::mbar_wait(&full_bar[i % kStages], (i / kStages) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
+          if (!tc::mbar_wait(&full_bar[i % kStages], (i / kStages) & 1)) report(a.status, CSA2_ERR_TIMEOUT);
       }
     }
     return;
@@ -363,7 +362,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     if (u >= 1) {
       // ---- epilogue of own tile u-1; afterwards the A and D buffers are free
       const int e = u - 1, ie = g + kWG * e;
-      const bool ok = tc::mbar_wait(&mma_bar[g], e & 1, kSpin);
+      const bool ok = tc::mbar_wait(&mma_bar[g], e & 1);
       waited = e;
       if (!ok) {
         report(a.status, CSA2_ERR_TIMEOUT);
@@ -417,7 +416,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
       if (kGather) {
         gather(u + 1);
         cp_wait<1>();
-      } else if (!tc::mbar_wait(&full_bar[s], (i / kStages) & 1, kSpin)) {
+      } else if (!tc::mbar_wait(&full_bar[s], (i / kStages) & 1)) {
         atomicExch(&abort_flag, 1);
       }
       const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
@@ -520,7 +519,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   }
   // after an abort, let the last issued MMA finish before TMEM is released
   if (last_issued > waited) {
-    if (!tc::mbar_wait(&mma_bar[g], last_issued & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
+    if (!tc::mbar_wait(&mma_bar[g], last_issued & 1)) report(a.status, CSA2_ERR_TIMEOUT);
   }
   tc::fence_before_sync();
   consumers_sync(kConsumers);

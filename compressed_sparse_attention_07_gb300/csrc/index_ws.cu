@@ -46,7 +46,6 @@ constexpr int kTmemCols = 512;
 static_assert(kDecWG * kASlots * kAcols + kDSlots * kDcols <= kTmemCols, "tensor-memory budget");
 constexpr int kStages = 16;                             // ring slots (one tile = two pages each)
 constexpr int kMaxTiles = 1024;                         // tiles of one CTA (page table in shared memory)
-constexpr uint32_t kSpin = 1u << 26;
 constexpr int kQBytes = kIdxHeads * kIdxDim * 2;        // one query's f16 tile, 8 KB
 
 template <int kDtype>
@@ -206,13 +205,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
     atomicExch(&abort_flag, 1);
   };
 
+  // roles: decode warpgroups (warps 0..11), epilogue warpgroups (12..19), the
+  // producer and MMA warps; the control warpgroup's last two warps only join
+  // the final barrier
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int issued = 0;
       for (int k = 0; k < n_act; ++k) {
         const int s = k % kStages;
-        if (k >= kStages && !tc::mbar_wait(&empty_bar[s], ((k / kStages) & 1) ^ 1, kSpin)) {
+        if (k >= kStages && !tc::mbar_wait(&empty_bar[s], ((k / kStages) & 1) ^ 1)) {
           fail();
           break;
         }
@@ -235,8 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
       }
       // no copy into this CTA's shared memory outlives it
       for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
-        if (!tc::mbar_wait(&full_bar[k % kStages], (k / kStages) & 1, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
+        if (!tc::mbar_wait(&full_bar[k % kStages], (k / kStages) & 1)) report(a.status, CSA2_ERR_TIMEOUT);
     }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     constexpr uint32_t kIdesc = tc::idesc_f16(128, kDcols, false, false, false, false);
@@ -244,11 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
     if (lane == 0) {
       for (int k = 0; k < n_act; ++k) {
         const int g = k % kDecWG, u = k / kDecWG, j = u % kASlots, d = k % kDSlots;
-        if (!tc::mbar_wait(&afull[g][j], (u / kASlots) & 1, kSpin)) {
+        if (!tc::mbar_wait(&afull[g][j], (u / kASlots) & 1)) {
           fail();
           break;
         }
-        if (k >= kDSlots && !tc::mbar_wait(&dempty[d], ((k / kDSlots) & 1) ^ 1, kSpin)) {
+        if (k >= kDSlots && !tc::mbar_wait(&dempty[d], ((k / kDSlots) & 1) ^ 1)) {
           fail();
           break;
         }
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
       }
       // every issued MMA has completed before tensor memory is released
       tc::mma_commit(&drain_bar);
-      if (!tc::mbar_wait(&drain_bar, 0, kSpin)) report(a.status, CSA2_ERR_TIMEOUT);
+      if (!tc::mbar_wait(&drain_bar, 0)) report(a.status, CSA2_ERR_TIMEOUT);
     }
     __syncwarp();
   } else if (warp < 4 * kDecWG) {
@@ -277,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
     const uint32_t lane_base = 32u * (warp & 3);
     for (int k = g, u = 0; k < n_act; k += kDecWG, ++u) {
       const int s = k % kStages, j = u % kASlots;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&full_bar[s], (k / kStages) & 1, kSpin)) && lane == 0) fail();
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&full_bar[s], (k / kStages) & 1)) && lane == 0) fail();
       if (__any_sync(0xffffffffu, aborted())) break;  // uniform in the warp: tcgen05.st is warp-wide
       const uint8_t* slot = ring + (size_t)s * F::kSlot;
       uint4 cw[4];
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
         score::e4m3_pair_bcast(sc.y >> 16, s2g[6], s2g[7]);
       }
       // the A slot is free once the MMA that read it two tiles ago is done
-      if (u >= kASlots && !__all_sync(0xffffffffu, tc::mbar_wait(&aempty[g][j], ((u / kASlots) & 1) ^ 1, kSpin))) {
+      if (u >= kASlots && !__all_sync(0xffffffffu, tc::mbar_wait(&aempty[g][j], ((u / kASlots) & 1) ^ 1))) {
         if (lane == 0) fail();
         break;
       }
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
       tc::fence_before_sync();
       tc::mbar_arrive(&afull[g][j]);
     }
-  } else {
+  } else if (warp < kCtlWarp0) {
     // ------------------------------------------------------------ epilogue
     const int e = (warp >> 2) - kDecWG;
     const int lt = 32 * (warp & 3) + lane;
@@ -333,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
     const bool weighted = a.head_w != nullptr;
     for (int k = e; k < n_act; k += kEpiWG) {
       const int d = k % kDSlots;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&dfull[d], (k / kDSlots) & 1, kSpin)) && lane == 0) fail();
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&dfull[d], (k / kDSlots) & 1)) && lane == 0) fail();
       if (__any_sync(0xffffffffu, aborted())) break;  // uniform in the warp: tcgen05.ld is warp-wide
       tc::fence_after_sync();
       uint32_t v[32];

@@ -13,9 +13,12 @@ namespace csa2 {
 
 // Launch with programmatic stream serialization: the grid may be scheduled
 // while the previous kernel on the stream finishes; every kernel of the
-// library waits for its predecessor (griddep_wait) before any global load
-// whose value it uses and before allocating tensor memory (before the wait
-// only L2 prefetch hints are issued).  cluster_x > 0 adds a cluster shape.
+// library waits for its predecessor (griddep_wait) before allocating tensor
+// memory and before any global load whose value a kernel of the library may
+// write -- before the wait a kernel issues L2 prefetch hints and reads only
+// the attention's query and window rows, which only csa2_swa_encode writes,
+// and that kernel lets its successor start only at its completion.
+// cluster_x > 0 adds a cluster shape.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster_x,
                      Args&&... args) {

@@ -80,6 +80,7 @@ const char* csa2_status_string(int32_t code) {
     case CSA2_ERR_BAD_PAGE: return "block table entry outside the page pool";
     case CSA2_ERR_BAD_INDEX: return "entry id outside the sequence";
     case CSA2_ERR_TIMEOUT: return "device wait timed out";
+    case CSA2_ERR_RANGE: return "input beyond the f16 operand range";
     default: return "unknown status";
   }
 }

@@ -90,6 +90,21 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return f16x2_from_f32(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// Bit 15 / 31 set when the low / high f16 half is an infinity or NaN: the
+// bf16 or MXFP8 value it came from lies outside the f16 range (|x| > 65504)
+// or was not finite.  Kernels OR these bits over their conversions and
+// report CSA2_ERR_RANGE.
+__device__ __forceinline__ uint32_t f16x2_nonfinite(uint32_t h) {
+  return ((h & 0x7C007C00u) + 0x04000400u) & 0x80008000u;
+}
+
+// bf16 pair -> f16 pair, recording an out-of-range value in `flag`.
+__device__ __forceinline__ uint32_t to_f16x2(uint32_t w, uint32_t& flag) {
+  const uint32_t h = bf16x2_to_f16x2(w);
+  flag |= f16x2_nonfinite(h);
+  return h;
+}
+
 
 __device__ __forceinline__ uint32_t f16x2_scale(uint32_t sbyte) {
   uint32_t r;
@@ -173,6 +188,7 @@ template <int kDtype, int HG, int kStages>
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
   griddep_wait();  // before any global read or tensor-memory allocation
   griddep_launch();
+  uint32_t rflag = 0;  // an f16 operand out of range (CSA2_ERR_RANGE)
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   constexpr int CPT = HG / 4;  // TMEM columns (heads) per thread in softmax / epilogue
   const int n_tiles = a.tiles_main + a.tiles_win;
@@ -212,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
     const int h = (8 * i) / kDim, kk = (8 * i) % kDim;
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)qi * kHeads + hg * HG + h) * kDim + kk));
     *reinterpret_cast<uint4*>(qp + tc::kmajor_off(h, kk, kDim)) =
-        make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+        make_uint4(to_f16x2(w.x, rflag), to_f16x2(w.y, rflag), to_f16x2(w.z, rflag), to_f16x2(w.w, rflag));
   }
   if (tid == 0) {
     tc::mbar_init(&cdone[0], 1);
@@ -397,10 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * j);
-          av[4 * j] = bf16x2_to_f16x2(v.x);
-          av[4 * j + 1] = bf16x2_to_f16x2(v.y);
-          av[4 * j + 2] = bf16x2_to_f16x2(v.z);
-          av[4 * j + 3] = bf16x2_to_f16x2(v.w);
+          av[4 * j] = to_f16x2(v.x, rflag);
+          av[4 * j + 1] = to_f16x2(v.y, rflag);
+          av[4 * j + 2] = to_f16x2(v.z, rflag);
+          av[4 * j + 3] = to_f16x2(v.w, rflag);
         }
       }
 #pragma unroll
@@ -462,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttArgs a) {
   } else if (tid == 0) {
     report(a.status, CSA2_ERR_TIMEOUT);
   }
+  if (rflag) report(a.status, CSA2_ERR_RANGE);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, tmem_cols);
@@ -486,6 +503,7 @@ template <int kDtype>
 __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
   griddep_wait();  // before any global read or tensor-memory allocation
   griddep_launch();
+  uint32_t rflag = 0;  // an f16 operand out of range (CSA2_ERR_RANGE)
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   constexpr int HG = kSplitHG, CPT = kSplitCPT;
   const int n_tiles = a.tiles_main + a.tiles_win;
@@ -515,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
     const int h = (8 * i) / kDim, kk = (8 * i) % kDim;
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(a.q + ((int64_t)qi * kHeads + hg * HG + h) * kDim + kk));
     *reinterpret_cast<uint4*>(qs + tc::kmajor_off(h, kk, kDim)) =
-        make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z), bf16x2_to_f16x2(w.w));
+        make_uint4(to_f16x2(w.x, rflag), to_f16x2(w.y, rflag), to_f16x2(w.z, rflag), to_f16x2(w.w, rflag));
   }
   if (tid == 0) {
     tc::mbar_init(&cdone, 1);
@@ -596,10 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * j);
-        av[4 * j] = bf16x2_to_f16x2(v.x);
-        av[4 * j + 1] = bf16x2_to_f16x2(v.y);
-        av[4 * j + 2] = bf16x2_to_f16x2(v.z);
-        av[4 * j + 3] = bf16x2_to_f16x2(v.w);
+        av[4 * j] = to_f16x2(v.x, rflag);
+        av[4 * j + 1] = to_f16x2(v.y, rflag);
+        av[4 * j + 2] = to_f16x2(v.z, rflag);
+        av[4 * j + 3] = to_f16x2(v.w, rflag);
       }
     }
     uint8_t* ct = ctile + c * kCBytes;
@@ -736,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_split_kernel(AttArgs a) {
     }
   }
   if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
+  if (rflag) report(a.status, CSA2_ERR_RANGE);
   tc::fence_before_sync();
   tc::cluster_sync();
   // ---- this CTA's slice: sum the tiles' partials in tile order
@@ -807,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attend_rows_kernel(AttArgs a) {
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
   const int n = a.tiles_main + a.tiles_win;
+  uint32_t rflag = 0;  // an f16 operand out of range (CSA2_ERR_RANGE)
   if (threadIdx.x < 32) {
     // While the previous kernel (the selection) runs, the first warp brings
     // this query's inputs that do not depend on the selected ids into L2:
@@ -922,8 +942,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       *reinterpret_cast<uint4*>(qs + tc::kmajor_off(h, 8 * (u0 + 4 * k + uq), kDim)) =
-          make_uint4(bf16x2_to_f16x2(qv[k].x), bf16x2_to_f16x2(qv[k].y), bf16x2_to_f16x2(qv[k].z),
-                     bf16x2_to_f16x2(qv[k].w));
+          make_uint4(to_f16x2(qv[k].x, rflag), to_f16x2(qv[k].y, rflag), to_f16x2(qv[k].z, rflag),
+                     to_f16x2(qv[k].w, rflag));
   }
   // ---- decode into C: FP4 code chunk q = 4k + l/8 (32 channels, two scale
   // groups) -> units 4q..4q+3; bf16 unit u = 4k + l/8 -> unit u
@@ -953,6 +973,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = 4 * k + uq, blk = u >> 1;
       uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
       if (sidx_l != -1) mxfp8x16_to_f16x2(raw[k], (sw[blk >> 2] >> (8 * (blk & 3))) & 0xFFu, o);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rflag |= f16x2_nonfinite(o[i]);
       *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 16 * u, kDim)) = make_uint4(o[0], o[1], o[2], o[3]);
       *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 16 * u + 8, kDim)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
@@ -960,8 +982,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       const uint4 o = sidx_l == -1 ? make_uint4(0, 0, 0, 0)
-                                   : make_uint4(bf16x2_to_f16x2(raw[k].x), bf16x2_to_f16x2(raw[k].y),
-                                                bf16x2_to_f16x2(raw[k].z), bf16x2_to_f16x2(raw[k].w));
+                                   : make_uint4(to_f16x2(raw[k].x, rflag), to_f16x2(raw[k].y, rflag),
+                                                to_f16x2(raw[k].z, rflag), to_f16x2(raw[k].w, rflag));
       *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 8 * (4 * k + uq), kDim)) = o;
     }
   }
@@ -1084,6 +1106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       a.lse[(int64_t)qi * kHeads + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
   if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
+  if (rflag) report(a.status, CSA2_ERR_RANGE);
   __syncthreads();
   // ---- this CTA's chunks c = t, t + n, ...: pull every tile's partial
   // (16-byte distributed loads, all issued before the sums), weight and sum
@@ -1150,6 +1173,7 @@ constexpr int kQcPieceFloats = 128 * 16;                                // 128 c
 template <int kDtype, bool kSwaFp8, int NC>
 __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
   constexpr bool kMainFp4 = (kDtype == CSA2_CACHE_FP4);
+  uint32_t rflag = 0;  // an f16 operand out of range (CSA2_ERR_RANGE)
   constexpr int R = NC == 4 ? 160 : 128;  // rows of this CTA: 8-row groups t, t + NC, ...
   constexpr int NG = R / 8;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -1237,6 +1261,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
         const int u = 4 * k + uq, blk = u >> 1;
         uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         if (sidx != -1) mxfp8x16_to_f16x2(w.v[k], (sw[blk >> 2] >> (8 * (blk & 3))) & 0xFFu, o);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rflag |= f16x2_nonfinite(o[i]);
         *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 16 * u, kDim)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 16 * u + 8, kDim)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
@@ -1244,8 +1270,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const uint4 o = sidx == -1 ? make_uint4(0, 0, 0, 0)
-                                   : make_uint4(bf16x2_to_f16x2(w.v[k].x), bf16x2_to_f16x2(w.v[k].y),
-                                                bf16x2_to_f16x2(w.v[k].z), bf16x2_to_f16x2(w.v[k].w));
+                                   : make_uint4(to_f16x2(w.v[k].x, rflag), to_f16x2(w.v[k].y, rflag),
+                                                to_f16x2(w.v[k].z, rflag), to_f16x2(w.v[k].w, rflag));
         *reinterpret_cast<uint4*>(ctile + tc::kmajor_off(rho, 8 * (4 * k + uq), kDim)) = o;
       }
     }
@@ -1272,8 +1298,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       *reinterpret_cast<uint4*>(qs + tc::kmajor_off(h, 8 * (u0 + 4 * k + uq), kDim)) =
-          make_uint4(bf16x2_to_f16x2(qv[k].x), bf16x2_to_f16x2(qv[k].y), bf16x2_to_f16x2(qv[k].z),
-                     bf16x2_to_f16x2(qv[k].w));
+          make_uint4(to_f16x2(qv[k].x, rflag), to_f16x2(qv[k].y, rflag), to_f16x2(qv[k].z, rflag),
+                     to_f16x2(qv[k].w, rflag));
   }
   __syncthreads();  // vmask cleared
   Raw w0, w1;
@@ -1453,6 +1479,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
   if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
+  if (rflag) report(a.status, CSA2_ERR_RANGE);
 
   // ---- the owned pieces: per-head factors 2^(m_t - M) / L, then the sums
   constexpr int kSlotsOwned = (16 + NC - 1) / NC;

@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
       v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + (int64_t)(g0 + row / kIdxHeads) * kIdxHeads * kIdxDim +
                                                (row % kIdxHeads) * kIdxDim + k));
     uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    score::q_operand8<kBf16>(w, a.q_fp4 != 0);
+    if (score::q_operand8<kBf16>(w, a.q_fp4 != 0)) report(a.status, CSA2_ERR_RANGE);
     *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   for (int i = tid; i < QPC * kIdxHeads; i += kConsumers)

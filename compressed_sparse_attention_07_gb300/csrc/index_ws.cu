@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_ws_kernel(WsArgs a) {
       if (have)
         v = __ldg(reinterpret_cast<const uint4*>(a.q_idx + ((int64_t)(a.q0 + qa + j) * kIdxHeads + row) * kIdxDim + kk));
       uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      score::q_operand8<false>(w, a.q_fp4 != 0);
+      if (score::q_operand8<false>(w, a.q_fp4 != 0) && have) report(a.status, CSA2_ERR_RANGE);
       if (i < kPieces)
         *reinterpret_cast<uint4*>(qtile + j * kQBytes + tc::kmajor_off(row, kk, kIdxDim)) =
             make_uint4(w[0], w[1], w[2], w[3]);

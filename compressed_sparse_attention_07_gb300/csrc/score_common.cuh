@@ -39,9 +39,12 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 // q_fp4 the row is first encoded like a cache entry (E4M3 scale nearest
 // amax / 6 per 16 channels, E2M1 codes, both by exact comparisons) and read
 // back; the 16-channel group is this lane's 8 channels and its neighbour
-// lane's (lane ^ 1), whose maximum is shared by one shuffle.
+// lane's (lane ^ 1), whose maximum is shared by one shuffle.  Returns
+// nonzero when a bf16 value made into f16 was outside the f16 range (or not
+// finite): the caller reports CSA2_ERR_RANGE.
 template <bool kBf16>
-__device__ __forceinline__ void q_operand8(uint32_t (&w)[4], bool q_fp4) {
+__device__ __forceinline__ uint32_t q_operand8(uint32_t (&w)[4], bool q_fp4) {
+  uint32_t bad = 0;
   if (q_fp4) {
     float f[8];
 #pragma unroll
@@ -70,8 +73,10 @@ __device__ __forceinline__ void q_operand8(uint32_t (&w)[4], bool q_fp4) {
     for (int j = 0; j < 4; ++j) {
       const __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
       w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      bad |= ((w[j] & 0x7C007C00u) + 0x04000400u) & 0x80008000u;  // an infinite or NaN half
     }
   }
+  return bad;
 }
 
 }  // namespace score

@@ -32,6 +32,14 @@
  *    rope_dims 64, n_heads 64, idx_heads 32, idx_dim 128, hsi_block 8.
  *    topk (1..1024), window (0..512), ratio (1 or 2), hsi_blocks (0..4096)
  *    and rope_theta are free.
+ *  - f16 operands: the tensor cores multiply in f16 with fp32 accumulation.
+ *    FP4 and MXFP8 values and FP4-encoded queries are exact in f16; bf16
+ *    inputs made into f16 -- the attention queries `q`, bf16 window rows,
+ *    the rows of a bf16 main cache, and the indexer queries `q_idx` over an
+ *    FP4 cache -- keep their value for |x| in [2^-14, 65504] (below that an
+ *    absolute error of at most 2^-25).  Such an input beyond 65504 in
+ *    magnitude, or not finite, sets CSA2_ERR_RANGE in *status (the query's
+ *    results are then unspecified); the call still completes.
  *
  * Paged cache layout (a build choice; the pages never mention paging).  A
  * page holds 64 consecutive entries of one sequence; entry j of sequence b
@@ -80,7 +88,10 @@ enum {
   /* device-side status codes (written to *status) */
   CSA2_ERR_BAD_PAGE = 16,   /* block_table entry outside [0, num_pages) */
   CSA2_ERR_BAD_INDEX = 17,  /* top-k / pool id outside the sequence's entries */
-  CSA2_ERR_TIMEOUT = 18     /* a bounded device-side wait gave up */
+  CSA2_ERR_TIMEOUT = 18,    /* a bounded device-side wait gave up */
+  CSA2_ERR_RANGE = 19       /* an input that becomes an f16 tensor-core operand is not finite
+                               or beyond the f16 range (|x| > 65504); the affected query's
+                               results are unspecified (see "f16 operands" below) */
 };
 
 enum { CSA2_CACHE_FP4 = 0, CSA2_CACHE_BF16 = 1, CSA2_CACHE_FP4_S32 = 2 };

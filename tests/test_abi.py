@@ -46,7 +46,7 @@ def test_page_bytes_follow_layout():
 
 
 def test_status_strings():
-    for code in (0, 1, 2, 3, 4, 16, 17, 18):
+    for code in (0, 1, 2, 3, 4, 16, 17, 18, 19):
         assert csa.status_string(code) != "unknown status"
     assert csa.status_string(999) == "unknown status"
 

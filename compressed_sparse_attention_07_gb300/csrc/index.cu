@@ -863,7 +863,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
                                                                 const int32_t* __restrict__ pool, const float* scores,
                                                                 const float* bmax, int64_t score_stride,
                                                                 const uint32_t* krange, int kr_stride, int n_slots,
-                                                                int64_t part_tq, int64_t part_total, int part_grid,
                                                                 int32_t* topk_out, int32_t* pool_out, int fused) {
   griddep_wait();  // the scores are the previous kernel's output
   griddep_launch();
@@ -882,15 +881,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
   {
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
     const uint32_t* kr = krange + (int64_t)qc * kr_stride * 2;
-    int ns = n_slots;
-    if (part_grid > 0) {
-      // the scorer shared a flattened range of part_total tiles among
-      // part_grid CTAs: this query's slots belong to the CTAs whose ranges
-      // meet its tiles [qc tq, (qc + 1) tq)
-      auto cta_of = [&](int64_t x) { return ((x + 1) * part_grid - 1) / part_total; };
-      ns = (int)(cta_of((int64_t)(qc + 1) * part_tq - 1) - cta_of((int64_t)qc * part_tq) + 1);
-    }
-    for (int i = threadIdx.x; i < ns; i += kSelThreads) {
+    for (int i = threadIdx.x; i < n_slots; i += kSelThreads) {
       lo = min(lo, kr[2 * i]);
       hi = max(hi, kr[2 * i + 1]);
     }
@@ -1012,48 +1003,17 @@ cudaError_t plan_index(const csa2_cfg& cfg, int B, int Tq, int max_entries, bool
   return cudaSuccess;
 }
 
-// How the scoring CTAs of a chunk map to key-range slots: n_slots per query
-// (one per CTA of the query's tile ranges), or the flattened partition of the
-// warp-specialized scorer (grid > 0).
-struct SlotMap {
-  int n_slots;
-  int64_t tq, total;
-  int grid;
-};
-
-// Which scorer a chunk uses and its slot map (decided the same way for the
-// score and the selection launches).
-SlotMap slot_map(const csa2_cfg& cfg, int q0, int nq, int Tq, int max_entries, bool reindex, bool* ws) {
-  int g = 0;
-  // single-query groups over FP4 pages (the decode scans): the warp-specialized scorer
-  const bool single = reindex || !((Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) || (Tq > 1 && q0 % Tq == 0 && nq % Tq == 0));
-  *ws = !reindex && single && score_ws_usable(cfg, nq, max_entries, num_sms(), &g);
-  if (*ws) {
-    const int64_t tq = ((int64_t)max_entries + 127) / 128;
-    return SlotMap{0, tq, (int64_t)nq * tq, g};
-  }
-  return SlotMap{score_slots_used(cfg, q0, nq, Tq, max_entries, reindex, num_sms()), 0, 0, 0};
-}
-
 cudaError_t run_scores(const IndexPlan& p, const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx,
                        const float* head_w, const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
-                       int max_entries, const int32_t* pool, bool hsi_out, SlotMap* sm, int32_t* status,
+                       int max_entries, const int32_t* pool, bool hsi_out, int* n_slots, int32_t* status,
                        cudaStream_t stream) {
-  bool ws = false;
-  *sm = slot_map(cfg, q0, nq, Tq, max_entries, pool != nullptr, &ws);
-  if (ws)
-    return launch_score_ws(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, p.scores, p.stride,
-                           hsi_out ? p.bmax_area : nullptr, p.krange, p.kr_stride, sm->grid, status, stream);
-  int n_slots = 0;
-  const cudaError_t e = launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool,
-                                        p.scores, p.stride, hsi_out ? p.bmax_area : nullptr, p.krange, p.kr_stride,
-                                        &n_slots, status, num_sms(), stream);
-  sm->n_slots = n_slots;
-  return e;
+  return launch_score_tc(cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, p.scores,
+                         p.stride, hsi_out ? p.bmax_area : nullptr, p.krange, p.kr_stride, n_slots, status, num_sms(),
+                         stream);
 }
 
 cudaError_t run_select(const IndexPlan& p, const csa2_cfg& cfg, int q0, int nq, int Tq, const int64_t* q_pos,
-                       const int32_t* n_entries, int max_entries, const int32_t* pool, const SlotMap& sm,
+                       const int32_t* n_entries, int max_entries, const int32_t* pool, int n_slots,
                        int32_t* topk_out, int32_t* pool_out, cudaStream_t stream) {
   const size_t sel_smem = sizeof(SelShared);
   auto sel = p.small ? select_kernel<true> : select_kernel<false>;
@@ -1061,7 +1021,7 @@ cudaError_t run_select(const IndexPlan& p, const csa2_cfg& cfg, int q0, int nq, 
   return launch_k(sel, dim3(p.cs, nq, p.n_sel), dim3(kSelThreads), sel_smem, stream, p.cs, q0, Tq, cfg.ratio,
                   cfg.topk, cfg.hsi_blocks, (int64_t)max_entries, q_pos, n_entries, pool, (const float*)p.scores,
                   (const float*)(pool_out ? p.bmax_area : nullptr), p.stride, (const uint32_t*)p.krange, p.kr_stride,
-                  sm.n_slots, sm.tq, sm.total, sm.grid, topk_out, pool_out, p.fused ? 1 : 0);
+                  n_slots, topk_out, pool_out, p.fused ? 1 : 0);
 }
 
 }  // namespace
@@ -1077,11 +1037,11 @@ cudaError_t launch_index_topk(const csa2_cfg& cfg, int B, int Tq, const uint16_t
   if (e != cudaSuccess) return e;
   for (int q0 = 0; q0 < p.Q; q0 += p.chunk) {
     const int nq = std::min(p.chunk, p.Q - q0);
-    SlotMap sm;
+    int n_slots = 0;
     e = run_scores(p, cfg, q0, nq, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, pool_out != nullptr,
-                   &sm, status, stream);
+                   &n_slots, status, stream);
     if (e != cudaSuccess) return e;
-    e = run_select(p, cfg, q0, nq, Tq, q_pos, n_entries, max_entries, pool, sm, topk_out, pool_out, stream);
+    e = run_select(p, cfg, q0, nq, Tq, q_pos, n_entries, max_entries, pool, n_slots, topk_out, pool_out, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -1096,8 +1056,8 @@ cudaError_t launch_index_score(const csa2_cfg& cfg, int B, int Tq, const uint16_
   cudaError_t e = plan_index(cfg, B, Tq, max_entries, pool != nullptr, hsi_out, ws, ws_bytes, &p);
   if (e != cudaSuccess) return e;
   if (p.chunk < p.Q) return cudaErrorInvalidValue;  // the workspace holds every query
-  SlotMap sm;
-  return run_scores(p, cfg, 0, p.Q, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, hsi_out, &sm,
+  int n_slots = 0;
+  return run_scores(p, cfg, 0, p.Q, Tq, q_idx, head_w, q_pos, idx_c, n_entries, max_entries, pool, hsi_out, &n_slots,
                     status, stream);
 }
 
@@ -1109,9 +1069,8 @@ cudaError_t launch_index_select(const csa2_cfg& cfg, int B, int Tq, const int64_
   cudaError_t e = plan_index(cfg, B, Tq, max_entries, pool != nullptr, pool_out != nullptr, ws, ws_bytes, &p);
   if (e != cudaSuccess) return e;
   if (p.chunk < p.Q) return cudaErrorInvalidValue;
-  bool use_ws = false;
-  const SlotMap sm = slot_map(cfg, 0, p.Q, Tq, max_entries, pool != nullptr, &use_ws);
-  return run_select(p, cfg, 0, p.Q, Tq, q_pos, n_entries, max_entries, pool, sm, topk_out, pool_out, stream);
+  const int n_slots = score_slots_used(cfg, 0, p.Q, Tq, max_entries, pool != nullptr, num_sms());
+  return run_select(p, cfg, 0, p.Q, Tq, q_pos, n_entries, max_entries, pool, n_slots, topk_out, pool_out, stream);
 }
 
 }  // namespace csa2

@@ -120,7 +120,10 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   constexpr int kN = 32 * QPC;                    // MMA N: QPC queries x 32 heads
   constexpr int kAcols = 64;                      // 128 channels of f16 pairs
   constexpr bool kSmemA = Shape<kDtype, QPC>::kSmemA;
-  constexpr int kTmemCols = ((kSmemA ? 0 : kWG * kAcols) + kWG * kN) <= 256 ? 256 : 512;
+  // D double-buffered per warpgroup when tensor memory holds it (the MMA of
+  // tile u runs while the epilogue of tile u-1 reads the other buffer)
+  constexpr int kDBuf = (!kSmemA && kWG * kAcols + 2 * kWG * kN <= 512) ? 2 : 1;
+  constexpr int kTmemCols = ((kSmemA ? 0 : kWG * kAcols) + kDBuf * kWG * kN) <= 256 ? 256 : 512;
   constexpr bool kBf16 = (kDtype == CSA2_CACHE_BF16);
   constexpr uint32_t kIdesc = tc::idesc_f16(128, kN, kBf16, kBf16, false, false);
   static_assert(!kGather || QPC == 1, "gather mode scores one query per CTA");
@@ -315,7 +318,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   const int lt = tid & 127;              // entry of the tile, TMEM lane
   const uint32_t lane_base = 32 * (warp & 3);
   const uint32_t acol = (uint32_t)(g * kAcols);
-  const uint32_t dcol = (uint32_t)((kSmemA ? 0 : kWG * kAcols) + g * kN);
+  const uint32_t dcol0 = (uint32_t)((kSmemA ? 0 : kWG * kAcols) + g * kDBuf * kN);
+  auto dcol_of = [&](int uu) { return dcol0 + (uint32_t)((uu % kDBuf) * kN); };
   uint8_t* atile = abuf + (size_t)g * kABytes;
   const int n_own = n_my > g ? (n_my - g + kWG - 1) / kWG : 0;
   uint32_t klo[QPC], khi[QPC];
@@ -355,153 +359,182 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   gather(0);
 
   int last_issued = -1, waited = -1;  // own tile counters
-  int u = 0;
-  for (; u <= n_own; ++u) {
-    const int i = g + kWG * u;  // CTA-local tile index
+
+  // epilogue of own tile e (its MMA has completed): ReLU-weighted head sums,
+  // scores, HSI block maxima, key ranges
+  auto epilogue = [&](int e, bool ok) {
+    const int ie = g + kWG * e;
+    const int64_t pos = (t_begin + ie) * 128 + lt;  // entry id (page mode) / pool position (gather mode)
+#pragma unroll
+    for (int q = 0; q < QPC; ++q) {
+      if (q >= n_act) break;  // uniform over the CTA
+      uint32_t d[32];
+      tc::tmem_ld32(tc::taddr(tb, lane_base, dcol_of(e) + 32 * q), d);
+      tc::tmem_wait_ld();
+      // four partial sums over heads h = 4i + j, added pairwise
+      float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (a.head_w) {
+#pragma unroll
+        for (int hh = 0; hh < kIdxHeads; ++hh)
+          ps[hh & 3] = fmaf(hw[q][hh], fmaxf(__uint_as_float(d[hh]), 0.0f), ps[hh & 3]);
+      } else {
+#pragma unroll
+        for (int hh = 0; hh < kIdxHeads; ++hh) ps[hh & 3] += fmaxf(__uint_as_float(d[hh]), 0.0f);
+      }
+      float sc = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      sc += 0.0f;
+      const int qc = qc0 + q;
+      const bool valid = kGather ? (gtab[ie * 128 + lt] >= 0) : (pos < nv[q]);
+      if (!ok) sc = -INFINITY;
+      if (kGather) {
+        if (pos < npos) a.scores[(int64_t)qc * a.stride + pos] = valid ? sc : __uint_as_float(kScoreInvalid);
+      } else if (valid) {
+        a.scores[(int64_t)qc * a.stride + pos] = sc;
+      }
+      if (valid) {
+        const uint32_t kk = order_key(sc);
+        klo[q] = min(klo[q], kk);
+        khi[q] = max(khi[q], kk);
+      }
+      if (!kGather && a.bmax) {
+        float m = valid ? sc : -INFINITY;
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        if ((lt & 7) == 0 && valid) a.bmax[(int64_t)qc * ((a.max_entries + 7) / 8) + pos / 8] = m;
+      }
+    }
+  };
+
+  // own tile u's entry (this thread's) from the ring, decoded into 64
+  // registers of f16 (or bf16) pairs; the ring slot is released
+  auto decode = [&](int u, uint32_t (&r)[64]) {
+    const int i = g + kWG * u;
+    const int s = i % kStages;
+    if (kGather) {
+      gather(u + 1);
+      cp_wait<1>();
+    } else if (!tc::mbar_wait(&full_bar[s], (i / kStages) & 1)) {
+      atomicExch(&abort_flag, 1);
+    }
+    const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
+    const bool present = !kGather || gtab[i * 128 + lt] >= 0;
+    if (kDtype != CSA2_CACHE_BF16) {
+      uint4 cw[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        cw[c] = *reinterpret_cast<const uint4*>(slot + h * kIdxFp4Data + (c * kPage + sl) * 16);
+      // the entry's scales: 8 bytes (one per 16 channels) or 4 (one per 32)
+      uint2 sc;
+      if (kDtype == CSA2_CACHE_FP4)
+        sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 8);
+      else
+        sc = make_uint2(*reinterpret_cast<const uint32_t*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 4), 0u);
+      if (!kGather) tc::mbar_arrive(&empty_bar[s]);
+      // the scales as broadcast f16x2: s2g[g] for 16-channel group g (or
+      // 32-channel group g with one scale per 32 channels)
+      uint32_t s2g[8];
+      e4m3_pair_bcast(sc.x, s2g[0], s2g[1]);
+      e4m3_pair_bcast(sc.x >> 16, s2g[2], s2g[3]);
+      if (kDtype == CSA2_CACHE_FP4) {
+        e4m3_pair_bcast(sc.y, s2g[4], s2g[5]);
+        e4m3_pair_bcast(sc.y >> 16, s2g[6], s2g[7]);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {  // 32 channels -> 16 registers
+        const uint32_t w4[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
+          const uint32_t s2 = kDtype == CSA2_CACHE_FP4 ? s2g[gg] : s2g[c];
+          uint32_t h4[4];
+          e2m1x8_to_f16x2(w4[q], h4);
+#pragma unroll
+          for (int by = 0; by < 4; ++by) r[16 * c + q * 4 + by] = present ? hmul2(h4[by], s2) : 0u;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(slot + h * kIdxBf16Data + (c * kPage + sl) * 16);
+        r[4 * c] = present ? v.x : 0u;
+        r[4 * c + 1] = present ? v.y : 0u;
+        r[4 * c + 2] = present ? v.z : 0u;
+        r[4 * c + 3] = present ? v.w : 0u;
+      }
+      if (!kGather) tc::mbar_arrive(&empty_bar[s]);
+    }
+  };
+
+  // the decoded tile into the A buffer (shared or tensor memory)
+  auto store_a = [&](const uint32_t (&r)[64]) {
+    if (kSmemA) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(atile + tc::kmajor_off(lt, 8 * c, kIdxDim)) =
+            make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+      tc::fence_async_smem();  // the K tile is read by the tensor core
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r16[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) r16[x] = r[16 * c + x];
+        tc::tmem_st16(tc::taddr(tb, lane_base, acol + 16 * c), r16);
+      }
+      tc::tmem_wait_st();
+    }
+  };
+
+  auto issue = [&](int u) {
+    if (lt == 0) {
+#pragma unroll
+      for (int ks = 0; ks < kIdxDim / 16; ++ks) {
+        const uint64_t bdesc = tc::sdesc(tc::smem_u32(qtile) + ks * 256, 128, kIdxDim * 16);
+        if (kSmemA)
+          tc::mma_ss(tb + dcol_of(u), tc::sdesc(tc::smem_u32(atile) + ks * 256, 128, kIdxDim * 16), bdesc, kIdesc,
+                     ks > 0);
+        else
+          tc::mma_ts(tb + dcol_of(u), tb + acol + ks * 8, bdesc, kIdesc, ks > 0);
+      }
+      tc::mma_commit(&mma_bar[g]);
+    }
+  };
+
+  // Per own tile u: decode u into registers (while MMA u-1 runs), wait for
+  // MMA u-1 (the A buffer is free and D(u-1) holds its products), store A,
+  // issue MMA u; then the epilogue of u-1 while MMA u runs (with one D
+  // buffer the epilogue of u-1 comes before MMA u instead).
+  // (with the decoded K tile in shared memory, the tile is decoded after the
+  // wait instead, straight into the A buffer: that instantiation has no
+  // registers to spare for it)
+  constexpr bool kEarly = !kSmemA;
+  for (int u = 0; u <= n_own; ++u) {
     const bool have = u < n_own;
+    uint32_t r[64];
+    if (kEarly && have) decode(u, r);
+    bool ok = true;
     if (u >= 1) {
-      // ---- epilogue of own tile u-1; afterwards the A and D buffers are free
-      const int e = u - 1, ie = g + kWG * e;
-      const bool ok = tc::mbar_wait(&mma_bar[g], e & 1);
-      waited = e;
+      ok = tc::mbar_wait(&mma_bar[g], (u - 1) & 1);
+      waited = u - 1;
       if (!ok) {
         report(a.status, CSA2_ERR_TIMEOUT);
         atomicExch(&abort_flag, 1);
       }
       tc::fence_after_sync();
-      const int64_t pos = (t_begin + ie) * 128 + lt;  // entry id (page mode) / pool position (gather mode)
-#pragma unroll
-      for (int q = 0; q < QPC; ++q) {
-        if (q >= n_act) break;  // uniform over the CTA
-        uint32_t d[32];
-        tc::tmem_ld32(tc::taddr(tb, lane_base, dcol + 32 * q), d);
-        tc::tmem_wait_ld();
-        // four partial sums over heads h = 4i + j, added pairwise
-        float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (a.head_w) {
-#pragma unroll
-          for (int hh = 0; hh < kIdxHeads; ++hh)
-            ps[hh & 3] = fmaf(hw[q][hh], fmaxf(__uint_as_float(d[hh]), 0.0f), ps[hh & 3]);
-        } else {
-#pragma unroll
-          for (int hh = 0; hh < kIdxHeads; ++hh) ps[hh & 3] += fmaxf(__uint_as_float(d[hh]), 0.0f);
-        }
-        float sc = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        sc += 0.0f;
-        const int qc = qc0 + q;
-        const bool valid = kGather ? (gtab[ie * 128 + lt] >= 0) : (pos < nv[q]);
-        if (!ok) sc = -INFINITY;
-        if (kGather) {
-          if (pos < npos) a.scores[(int64_t)qc * a.stride + pos] = valid ? sc : __uint_as_float(kScoreInvalid);
-        } else if (valid) {
-          a.scores[(int64_t)qc * a.stride + pos] = sc;
-        }
-        if (valid) {
-          const uint32_t kk = order_key(sc);
-          klo[q] = min(klo[q], kk);
-          khi[q] = max(khi[q], kk);
-        }
-        if (!kGather && a.bmax) {
-          float m = valid ? sc : -INFINITY;
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-          if ((lt & 7) == 0 && valid) a.bmax[(int64_t)qc * ((a.max_entries + 7) / 8) + pos / 8] = m;
-        }
-      }
+      if (kDBuf == 1) epilogue(u - 1, ok);
     }
-    if (have) {
-      // ---- fetch own tile i and decode this thread's entry straight into TMEM
-      const int s = i % kStages;
-      if (kGather) {
-        gather(u + 1);
-        cp_wait<1>();
-      } else if (!tc::mbar_wait(&full_bar[s], (i / kStages) & 1)) {
-        atomicExch(&abort_flag, 1);
-      }
-      const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
-      const bool present = !kGather || gtab[i * 128 + lt] >= 0;
-      if (kDtype != CSA2_CACHE_BF16) {
-        uint4 cw[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          cw[c] = *reinterpret_cast<const uint4*>(slot + h * kIdxFp4Data + (c * kPage + sl) * 16);
-        // the entry's scales: 8 bytes (one per 16 channels) or 4 (one per 32)
-        uint2 sc;
-        if (kDtype == CSA2_CACHE_FP4)
-          sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 8);
-        else
-          sc = make_uint2(*reinterpret_cast<const uint32_t*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 4), 0u);
-        if (!kGather) tc::mbar_arrive(&empty_bar[s]);
-        // the scales as broadcast f16x2: s2g[g] for 16-channel group g (or
-        // 32-channel group g with one scale per 32 channels)
-        uint32_t s2g[8];
-        e4m3_pair_bcast(sc.x, s2g[0], s2g[1]);
-        e4m3_pair_bcast(sc.x >> 16, s2g[2], s2g[3]);
-        if (kDtype == CSA2_CACHE_FP4) {
-          e4m3_pair_bcast(sc.y, s2g[4], s2g[5]);
-          e4m3_pair_bcast(sc.y >> 16, s2g[6], s2g[7]);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // 32 channels -> 16 TMEM columns
-          const uint32_t w4[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
-          uint32_t r16[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
-            const uint32_t s2 = kDtype == CSA2_CACHE_FP4 ? s2g[gg] : s2g[c];
-            uint32_t h4[4];
-            e2m1x8_to_f16x2(w4[q], h4);
-#pragma unroll
-            for (int by = 0; by < 4; ++by) r16[q * 4 + by] = present ? hmul2(h4[by], s2) : 0u;
-          }
-          if (kSmemA) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(atile + tc::kmajor_off(lt, 32 * c + 8 * q, kIdxDim)) =
-                  make_uint4(r16[4 * q], r16[4 * q + 1], r16[4 * q + 2], r16[4 * q + 3]);
-          } else {
-            tc::tmem_st16(tc::taddr(tb, lane_base, acol + 16 * c), r16);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t r16[16];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(slot + h * kIdxBf16Data + ((4 * c4 + c) * kPage + sl) * 16);
-            r16[4 * c] = present ? v.x : 0u;
-            r16[4 * c + 1] = present ? v.y : 0u;
-            r16[4 * c + 2] = present ? v.z : 0u;
-            r16[4 * c + 3] = present ? v.w : 0u;
-          }
-          tc::tmem_st16(tc::taddr(tb, lane_base, acol + 16 * c4), r16);
-        }
-        if (!kGather) tc::mbar_arrive(&empty_bar[s]);
-      }
-      if (kSmemA)
-        tc::fence_async_smem();  // the K tile is read by the tensor core
-      else
-        tc::tmem_wait_st();
-    }
+    if (!kEarly && have) decode(u, r);
+    if (have) store_a(r);
     tc::fence_before_sync();
     wg_sync(g);
     tc::fence_after_sync();
     if (*reinterpret_cast<volatile int*>(&abort_flag)) break;  // uniform within the warpgroup
-    if (have && lt == 0) {
-#pragma unroll
-      for (int ks = 0; ks < kIdxDim / 16; ++ks) {
-        const uint64_t bdesc = tc::sdesc(tc::smem_u32(qtile) + ks * 256, 128, kIdxDim * 16);
-        if (kSmemA)
-          tc::mma_ss(tb + dcol, tc::sdesc(tc::smem_u32(atile) + ks * 256, 128, kIdxDim * 16), bdesc, kIdesc,
-                     ks > 0);
-        else
-          tc::mma_ts(tb + dcol, tb + acol + ks * 8, bdesc, kIdesc, ks > 0);
-      }
-      tc::mma_commit(&mma_bar[g]);
+    if (have) {
+      issue(u);
+      last_issued = u;
     }
-    if (have) last_issued = u;
+    if (kDBuf == 2 && u >= 1) epilogue(u - 1, ok);
   }
   if (kGather) cp_wait<0>();  // no copies into this CTA's shared memory outlive it
 #pragma unroll

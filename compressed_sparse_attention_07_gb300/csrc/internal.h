@@ -70,15 +70,6 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
                             uint32_t* krange, int kr_stride, int* n_slots, int32_t* status, int num_sms,
                             cudaStream_t stream);
 
-// The warp-specialized scorer (single queries over FP4 indexer pages, one
-// wave sharing the flattened (query, tile) range): whether it takes a chunk
-// of nq queries, and its grid.
-bool score_ws_usable(const csa2_cfg& cfg, int nq, int64_t max_entries, int num_sms, int* grid);
-cudaError_t launch_score_ws(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
-                            const int64_t* q_pos, const csa2_cache& idx_c, const int32_t* n_entries,
-                            int64_t max_entries, float* scores, int64_t stride, float* bmax, uint32_t* krange,
-                            int kr_stride, int grid, int32_t* status, cudaStream_t stream);
-
 // Scoring CTAs per query (key-range slots written) of launch_score_tc for
 // the same arguments.
 int score_slots_used(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_entries, bool gather, int num_sms);

@@ -78,3 +78,42 @@ def test_static_scratch_rejects_oversized_requests():
     rc = lib.csa2_index_topk_static(C.byref(cfg), 1, 1, fake, None, fake, C.byref(d), fake, too_many, None, fake,
                                     fake, None, None)
     assert rc == 4  # CSA2_ERR_CAPACITY
+
+
+def test_static_scratch_at_its_largest_accepted_size():
+    """The largest sequence length whose per-query scratch (scores, HSI block
+    maxima, key-range slots) fits the static array exactly: two queries run
+    one after the other through the array and give the workspace entry
+    point's results; one entry more is refused before any launch."""
+    lib = csa.load()
+    lib.csa2_index_topk_static.restype = C.c_int32
+    cap = lib.csa2_index_static_scratch_bytes()
+    cfg = csa.Cfg(ratio=1, topk=512, hsi_blocks=2048)
+    lo, hi = 1, 4 << 20  # largest N with a per-query scratch of at most the array's size
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if csa.index_workspace_bytes(cfg, 1, 1, mid) <= cap:
+            lo = mid
+        else:
+            hi = mid - 1
+    N = lo
+    assert csa.index_workspace_bytes(cfg, 1, 1, N) <= cap < csa.index_workspace_bytes(cfg, 1, 1, N + 1)
+    B = 2
+    pc, q_idx, q_pos, n_ent = _case(44, B, N, integer=False)
+    q_idx, q_pos = q_idx[:, :1].contiguous(), q_pos[:, :1].contiguous()
+    want_top = torch.full((B, 1, cfg.topk), -9, dtype=torch.int32, device="cuda")
+    want_pool = torch.full((B, 1, cfg.hsi_blocks), -9, dtype=torch.int32, device="cuda")
+    ws = torch.empty(csa.index_workspace_bytes(cfg, B, 1, N), dtype=torch.uint8, device="cuda")
+    csa.index_topk(cfg, q_idx, q_pos, pc, n_ent, N, want_top, ws, pool_out=want_pool)
+    got_top = torch.full_like(want_top, -5)
+    got_pool = torch.full_like(want_pool, -5)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = _static(cfg, q_idx, q_pos, pc, n_ent, N, got_top, got_pool, st)
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st.item()) == 0
+    assert torch.equal(got_top, want_top) and torch.equal(got_pool, want_pool)
+    fake = C.c_void_p(0x10000)  # never dereferenced: the size check fails first
+    d = csa._CacheDesc(0x10000, 0x10000, 0x10000, 1 << 16, 1 << 16, 128, 0)
+    rc = lib.csa2_index_topk_static(C.byref(cfg), B, 1, fake, None, fake, C.byref(d), fake, N + 1, None, fake, fake,
+                                    None, None)
+    assert rc == 4  # CSA2_ERR_CAPACITY

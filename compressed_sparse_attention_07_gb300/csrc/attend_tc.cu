@@ -1158,17 +1158,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 //  - S^T = C . Q^T on the tensor cores (M = 128 rows; with R = 160 a second
 //    block covers rows 32..159 and only its last 32 lanes are read), a
 //    partial softmax per head over the CTA's rows, O^T = C^T . P^T;
-//  - the merge: after one cluster barrier every CTA pushes its unscaled
-//    partial output, in 16 pieces of 128 channels x 16 heads, into the
-//    owner of each piece (piece i -> CTA i mod NC) with 16-byte
-//    distributed-shared-memory stores, together with its (max, sum) per
-//    head; after a second barrier each owner forms
-//    out = sum_t 2^(m_t - M) O_t / L in tile order, M = max_t m_t,
-//    L = sum_t 2^(m_t - M) l_t, and writes its pieces.
+//  - the merge: every CTA stages its unscaled partial output in its own
+//    shared memory; after one cluster barrier the output's 16 pieces of 128
+//    channels x 16 heads are shared out (piece i -> CTA i mod NC), and each
+//    owner pulls its pieces of every tile with 16-byte distributed-shared-
+//    memory loads and forms out = sum_t 2^(m_t - M) O_t / L in tile order,
+//    M = max_t m_t, L = sum_t 2^(m_t - M) l_t (pushing the pieces with
+//    remote stores was measured slower).
 constexpr int kQcMaxRows = 160;
 constexpr size_t kQcQBytes = (size_t)kAllHeads * kDim * 2;   // 65536; after S: P^T and scratch
 constexpr size_t kQcSmem = kQcQBytes + (size_t)kQcMaxRows * kDim * 2;   // 229376
-constexpr int kQcPieceFloats = 128 * 16;                                // 128 channels x 16 heads
 
 template <int kDtype, bool kSwaFp8, int NC>
 __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
@@ -1181,18 +1180,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
   uint8_t* pt = smem;                                    // after S: P^T [64 heads x R rows] f16, K-major
   float* scr = reinterpret_cast<float*>(smem + kAllHeads * R * 2);  // after S: reduction scratch
   uint8_t* ctile = smem + kQcQBytes;                     // C [R rows x 512] f16, K-major
-  float* recv = reinterpret_cast<float*>(smem);          // after O: received pieces [slot][tile][128 ch][16 h]
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tmem_base;
   __shared__ uint32_t vmask[NG / 4 + 1];                 // valid rows of the tile
-  __shared__ float m_all[NC][kAllHeads], l_all[NC][kAllHeads];
+  __shared__ float m_all[1][kAllHeads], l_all[1][kAllHeads];  // this CTA's (max, sum) per head
+  __shared__ float fac_s[NC][kAllHeads];                       // factor of every tile per head
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = tid & 127, p = tid >> 7, quad = warp & 3;
   const uint32_t lane_base = 32 * quad;
   const int t = (int)tc::cluster_rank();
   const int qi = blockIdx.y, b = qi / a.Tq;
-  const int n_slots = (a.tiles_main + a.tiles_win) * 128;
   const int rl = lane & 7, uq = lane >> 3;
   // global slot of local row i
   auto slot_of = [&](int i) { return 8 * ((i >> 3) * NC + t) + (i & 7); };
@@ -1287,6 +1285,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
     tc::fence_mbar_init();
+  }
+  if (warp == kThreads / 32 - 1 && t == NC - 1 && qi % a.Tq == 0) {
+    // once per sequence, its main-cache block table into L2 (hints only)
+    int64_t np = (a.capacity + kPage - 1) / kPage;
+    np = np < a.mc.max_pages ? np : a.mc.max_pages;
+    const char* bt = reinterpret_cast<const char*>(a.mc.block_table + (int64_t)b * a.mc.max_pages);
+    for (int64_t off = (int64_t)lane * 128; off < 4 * np; off += 32 * 128) tc::prefetch_l2(bt + off);
   }
   if (tid < NG / 4 + 1) vmask[tid] = 0u;
   {
@@ -1448,73 +1453,74 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
   }
   ok = tc::mbar_wait(&bar, 1) && ok;
   tc::fence_after_sync();
-  // every CTA of the cluster has finished reading its Q, P^T and C: their
-  // space receives the pieces
-  tc::fence_before_sync();
-  tc::cluster_sync();
-  tc::fence_after_sync();
-
-  // ---- push: piece (c, p) = channels 128c.., heads 16p..; owner (4c + p) mod NC
+  // ---- this tile's unscaled partial output into its own shared memory (Q,
+  // P^T and C are free once its MMAs are done), [chunk][head][channel]: a
+  // warp's stores are 128 contiguous bytes
+  float* stg = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t wv[16];
     tc::tmem_ld16(tc::taddr(tb, lane_base, 128 + 64 * c + 16 * p), wv);
     tc::tmem_wait_ld();
-    const int piece = 4 * c + p, owner = piece % NC, ps = piece / NC;
-    const uint32_t dst = tc::map_rank(tc::smem_u32(recv + ((size_t)(ps * NC + t) * 128 + r) * 16), owner);
+    float* dst = stg + (c * kAllHeads + 16 * p) * 128 + r;
 #pragma unroll
-    for (int j = 0; j < 16; j += 4)
-      tc::st_dsmem_v4(dst + 4 * j, __uint_as_float(wv[j]), __uint_as_float(wv[j + 1]), __uint_as_float(wv[j + 2]),
-                      __uint_as_float(wv[j + 3]));
+    for (int j = 0; j < 16; ++j) dst[128 * j] = __uint_as_float(wv[j]);
   }
   if (tid < kAllHeads) {
-#pragma unroll
-    for (int o = 0; o < NC; ++o) {
-      tc::st_dsmem(tc::map_rank(tc::smem_u32(&m_all[t][tid]), o), m_own);
-      tc::st_dsmem(tc::map_rank(tc::smem_u32(&l_all[t][tid]), o), l_own);
-    }
+    m_all[0][tid] = m_own;  // this CTA's (max, sum) per head, read by the cluster below
+    l_all[0][tid] = l_own;
   }
   tc::fence_before_sync();
-  tc::cluster_sync();  // every piece and (max, sum) has arrived
+  tc::cluster_sync();  // every CTA's partial output and (max, sum) are in place
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
   if (!ok && tid == 0) report(a.status, CSA2_ERR_TIMEOUT);
   if (rflag) report(a.status, CSA2_ERR_RANGE);
 
-  // ---- the owned pieces: per-head factors 2^(m_t - M) / L, then the sums
-  constexpr int kSlotsOwned = (16 + NC - 1) / NC;
-  float* fac = recv + (size_t)kSlotsOwned * NC * kQcPieceFloats;  // [NC][64]
+  // ---- per-head factors of every tile: 2^(m_t - M) / L
   if (tid < kAllHeads) {
+    float mk[NC], lk[NC];
+#pragma unroll
+    for (int k2 = 0; k2 < NC; ++k2) {
+      mk[k2] = tc::ld_dsmem(tc::map_rank(tc::smem_u32(&m_all[0][tid]), k2));
+      lk[k2] = tc::ld_dsmem(tc::map_rank(tc::smem_u32(&l_all[0][tid]), k2));
+    }
     float M = -INFINITY;
 #pragma unroll
-    for (int k2 = 0; k2 < NC; ++k2) M = fmaxf(M, m_all[k2][tid]);
+    for (int k2 = 0; k2 < NC; ++k2) M = fmaxf(M, mk[k2]);
     float L = 0.0f;
 #pragma unroll
     for (int k2 = 0; k2 < NC; ++k2)
-      if (m_all[k2][tid] != -INFINITY) L += exp2f(m_all[k2][tid] - M) * l_all[k2][tid];
+      if (mk[k2] != -INFINITY) L += exp2f(mk[k2] - M) * lk[k2];
 #pragma unroll
     for (int k2 = 0; k2 < NC; ++k2)
-      fac[k2 * kAllHeads + tid] = (ok && L > 0.0f && m_all[k2][tid] != -INFINITY) ? exp2f(m_all[k2][tid] - M) / L : 0.0f;
+      fac_s[k2][tid] = (ok && L > 0.0f && mk[k2] != -INFINITY) ? exp2f(mk[k2] - M) / L : 0.0f;
     if (t == 0 && a.lse)
       a.lse[(int64_t)qi * kHeads + tid] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
   __syncthreads();
-  for (int ps = 0; ps * NC + t < 16; ++ps) {
-    const int piece = ps * NC + t, c = piece >> 2, pp = piece & 3;
-    const int hl = tid & 15, ch4 = tid >> 4;  // 16 heads x 32 runs of 4 channels
-    const int h = 16 * pp + hl;
+  // ---- the pieces this CTA owns (piece i = chunk i / 4, heads 16 (i % 4)..;
+  // owner i mod NC): every tile's part pulled with 16-byte distributed loads,
+  // all issued before the sums, weighted and summed in tile order
+  const uint32_t stg_addr = tc::smem_u32(stg);
+  for (int piece = t; piece < 16; piece += NC) {
+    const int c = piece >> 2, h = 16 * (piece & 3) + (tid >> 5), ch4 = 4 * (tid & 31);
+    const uint32_t off = 4u * (uint32_t)((c * kAllHeads + h) * 128 + ch4);
+    float4 v[NC];
+#pragma unroll
+    for (int k2 = 0; k2 < NC; ++k2) v[k2] = tc::ld_dsmem_v4(tc::map_rank(stg_addr + off, k2));
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
     for (int k2 = 0; k2 < NC; ++k2) {
-      const float f = fac[k2 * kAllHeads + h];
-      const float* src = recv + ((size_t)(ps * NC + k2) * 128 + 4 * ch4) * 16 + hl;
-      acc.x = fmaf(f, src[0], acc.x);
-      acc.y = fmaf(f, src[16], acc.y);
-      acc.z = fmaf(f, src[32], acc.z);
-      acc.w = fmaf(f, src[48], acc.w);
+      const float f = fac_s[k2][h];
+      acc.x = fmaf(f, v[k2].x, acc.x);
+      acc.y = fmaf(f, v[k2].y, acc.y);
+      acc.z = fmaf(f, v[k2].z, acc.z);
+      acc.w = fmaf(f, v[k2].w, acc.w);
     }
-    *reinterpret_cast<float4*>(a.out + ((int64_t)qi * kHeads + h) * kDim + 128 * c + 4 * ch4) = acc;
+    *reinterpret_cast<float4*>(a.out + ((int64_t)qi * kHeads + h) * kDim + 128 * c + ch4) = acc;
   }
+  tc::cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
 template <int kDtype, bool kSwaFp8>

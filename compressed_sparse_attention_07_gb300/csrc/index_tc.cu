@@ -501,14 +501,14 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     }
   };
 
-  // Per own tile u: decode u into registers (while MMA u-1 runs), wait for
-  // MMA u-1 (the A buffer is free and D(u-1) holds its products), store A,
-  // issue MMA u; then the epilogue of u-1 while MMA u runs (with one D
-  // buffer the epilogue of u-1 comes before MMA u instead).
-  // (with the decoded K tile in shared memory, the tile is decoded after the
-  // wait instead, straight into the A buffer: that instantiation has no
-  // registers to spare for it)
-  constexpr bool kEarly = !kSmemA;
+  // Per own tile u: wait for MMA u-1 (the A buffer is free and D(u-1) holds
+  // its products), decode and store A, issue MMA u; then the epilogue of u-1
+  // while MMA u runs (with one D buffer the epilogue of u-1 comes before the
+  // decode of u instead).
+  // The tile is decoded after the wait, straight into the A buffer: decoding
+  // it into registers before the wait (kEarly) was measured slower on the
+  // single-query scans, whose 544-thread CTAs then spill.
+  constexpr bool kEarly = false;
   for (int u = 0; u <= n_own; ++u) {
     const bool have = u < n_own;
     uint32_t r[64];

@@ -65,7 +65,13 @@ MAIN_ENTRY_BYTES = {"fp4": 288, "bf16": 1024}
 # stage's kernels, from one ncu capture of this bench's default command; the
 # summaries under profiles/ name the capture.  A stage with no capture of the
 # current kernels reports null.
-TRAFFIC = {}
+TRAFFIC = {
+    "decode_b32_ctx131072_r1_fp4_hsi": {
+        "index_score": (302601472 + 16808192, "profiles/score_tc_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
+        "index_select": (9127936, "profiles/select_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
+        "attend": (12978176, "profiles/attend_qc_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
+    },
+}
 
 
 def attend_query_bytes(cache, topk=512, window=128, row_bytes=1024):

@@ -659,19 +659,16 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
 // 8-entry blocks written earlier by this CTA; ids >= nv_lim or blocks < 0 are
 // not candidates).
 __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
-                             uint32_t kmin_q, uint32_t kmax_q, SelShared& s, const int32_t* gpool = nullptr,
+                             uint32_t kmin, uint32_t kmax, SelShared& s, const int32_t* gpool = nullptr,
                              int64_t nv_lim = 0) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const bool has_forced = forced >= 0 && forced < n;
   const uint32_t need = (uint32_t)k - (has_forced ? 1u : 0u);
-  // the histogram's bins span the range of these keys themselves (found
-  // below), which for a pool's positions or for block maxima is a narrow
-  // top part of the query's range kmin_q .. kmax_q
-  (void)kmin_q;
-  (void)kmax_q;
-  uint32_t kmin = 0, kmax = 0;
-  int sh = 0;
-  bool ranked = false;
+  const bool any = kmin <= kmax;
+  const uint32_t range = any ? kmax - kmin : 0u;
+  const int nbits = range ? 32 - __clz(range) : 0;
+  const int sh = nbits > 13 ? nbits - 13 : 0;
+  const bool ranked = need > 0 && any;
   auto bin_of = [&](uint32_t kk) -> uint32_t {
     const uint32_t x = kk > kmin ? kk - kmin : 0u;
     return min(x >> sh, (uint32_t)(kHistBins - 1));
@@ -731,42 +728,11 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
     for (int m = 0; m < kPer; ++m) v[m] = p0 + m < n ? ld_score(vals + p0 + m) : __uint_as_float(kScoreInvalid);
   }
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
-  if (threadIdx.x == 0) {
-    s.cand_n = 0;
-    s.t_x = 0xFFFFFFFFu;  // the keys' minimum and maximum, reduced below
-    s.t_krem = 0u;
-  }
+  if (threadIdx.x == 0) s.cand_n = 0;
   uint32_t kk[kPer];
-  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
-  for (int m = 0; m < kPer; ++m) {
-    kk[m] = (p0 + m == forced) ? 0u : order_key(v[m]);
-    if (kk[m]) {
-      lo = min(lo, kk[m]);
-      hi = max(hi, kk[m]);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-  }
-  __syncthreads();  // the counters above are initialised
-  if (lane == 0 && lo <= hi) {
-    atomicMin(&s.t_x, lo);
-    atomicMax(&s.t_krem, hi);
-  }
+  for (int m = 0; m < kPer; ++m) kk[m] = (p0 + m == forced) ? 0u : order_key(v[m]);
   __syncthreads();
-  {
-    kmin = s.t_x;
-    kmax = s.t_krem;
-    const bool any = kmin <= kmax;
-    const uint32_t range = any ? kmax - kmin : 0u;
-    const int nbits = range ? 32 - __clz(range) : 0;
-    sh = nbits > 13 ? nbits - 13 : 0;
-    ranked = need > 0 && any;
-  }
-  __syncthreads();  // s.t_x / s.t_krem are reused by the ranking below
 
   uint32_t T = 0xFFFFFFFFu, krem = 0;  // select key > T, then the first krem keys == T
   if (ranked) {

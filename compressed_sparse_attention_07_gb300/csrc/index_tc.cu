@@ -79,7 +79,20 @@ struct ScoreArgs {
   uint32_t* krange;     // [chunk][kr_stride][2]: key range of each CTA's scores of each query
   int kr_stride;
   int32_t* status;
+  // single-query page scans in one wave (flat != 0): CTA c takes tiles
+  // [c total / G, (c + 1) total / G) of the flattened sequence of the chunk's
+  // queries' tiles (tq per query, total = queries x tq), at most two queries
+  int flat;
+  int64_t tq, total;
+  int kr_pad;  // flat mode: key-range slots read per query (unused ones are written empty)
 };
+
+// First flattened tile of CTA c, and the CTA holding flattened tile x (the
+// largest c with flat_first(c) <= x).
+__host__ __device__ inline int64_t flat_first(int64_t c, int64_t total, int64_t grid) { return c * total / grid; }
+__host__ __device__ inline int64_t flat_cta_of(int64_t x, int64_t total, int64_t grid) {
+  return ((x + 1) * grid - 1) / total;
+}
 
 using score::e2m1x8_to_f16x2;
 using score::e4m3_pair_bcast;
@@ -127,11 +140,25 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   constexpr bool kBf16 = (kDtype == CSA2_CACHE_BF16);
   constexpr uint32_t kIdesc = tc::idesc_f16(128, kN, kBf16, kBf16, false, false);
   static_assert(!kGather || QPC == 1, "gather mode scores one query per CTA");
+  // query slots of a CTA: the group's QPC queries, or in the flat mode the
+  // (at most) two queries its tile range touches
+  constexpr bool kFlatable = QPC == 1 && !kGather;
+  constexpr int kQS = kFlatable ? 2 : QPC;
+  const bool flat = kFlatable && a.flat;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int jg = blockIdx.y % a.gps;
-  const int qc0 = (blockIdx.y / a.gps) * a.seg + jg * QPC;  // chunk-local index of the group's first query
-  const int n_act = min(QPC, a.seg - jg * QPC);             // queries of the group; the rest are masked
-  const int g0 = a.q0 + qc0;                                // first query of the group (same sequence)
+  int qc0 = (blockIdx.y / a.gps) * a.seg + jg * QPC;  // chunk-local index of the first query
+  int n_act = min(QPC, a.seg - jg * QPC);             // queries of the group; the rest are masked
+  int64_t gt0 = 0, gt1 = 0;
+  bool two = false;
+  if (flat) {
+    gt0 = flat_first(blockIdx.x, a.total, gridDim.x);
+    gt1 = flat_first(blockIdx.x + 1, a.total, gridDim.x);
+    qc0 = (int)(gt0 / a.tq);
+    two = gt1 > (int64_t)(qc0 + 1) * a.tq;
+    n_act = two ? 2 : 1;
+  }
+  const int g0 = a.q0 + qc0;                          // first query of the CTA
   const int b = g0 / a.Tq;
   if (!kGather && a.prefetch && warp == kConsumers / 32) {
     // While the previous kernel runs (the grid is one wave, so every CTA is
@@ -140,9 +167,11 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     // entries read to aim them are read again after the wait, and every
     // prefetched page lies in the page pool.
     const int lane = tid & 31;
-    const int64_t tb0 = (int64_t)blockIdx.x * a.tiles_per_cta;
-    const int64_t pp = 2 * tb0 + lane;  // logical page
-    if (lane < 2 * a.tiles_per_cta && lane < 2 * kStages && pp < a.ic.max_pages && pp * kPage < a.max_entries) {
+    const int64_t tb0 = flat ? gt0 - (int64_t)qc0 * a.tq : (int64_t)blockIdx.x * a.tiles_per_cta;
+    const int64_t pp = 2 * tb0 + lane;  // logical page (of the CTA's first query)
+    const int64_t qend = (int64_t)(qc0 + 1) * a.tq;
+    const int64_t lim = flat ? 2 * ((gt1 < qend ? gt1 : qend) - gt0) : 2 * a.tiles_per_cta;
+    if (lane < lim && lane < 2 * kStages && pp < a.ic.max_pages && pp * kPage < a.max_entries) {
       const int32_t pg = tc::ld_cg_s32(a.ic.block_table + (int64_t)b * a.ic.max_pages + pp);
       if (pg >= 0 && pg < a.ic.num_pages) {
         tc::bulk_prefetch_l2(a.ic.data + (int64_t)pg * F::kPageData, F::kPageData);
@@ -154,38 +183,76 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   griddep_launch();
 
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* qtile = smem;                          // [kN rows][128] K-major, 256*kN B
-  uint8_t* ring = smem + 256 * kN;                // kStages slots
+  uint8_t* qtile = smem;                          // [kQS*32 rows][128] K-major: query slot j at j * 256 * 32
+  uint8_t* ring = smem + 256 * 32 * kQS;          // kStages slots
   uint8_t* abuf = ring + kStages * TileFmt<kDtype>::kSlotBytes;  // kSmemA: one K tile per warpgroup
-  __shared__ float hw[QPC][kIdxHeads];
+  __shared__ float hw[kQS][kIdxHeads];
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], mma_bar[kWG];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ uint32_t rng_lo[QPC], rng_hi[QPC];  // this CTA's key range per query
+  __shared__ uint32_t rng_lo[kQS], rng_hi[kQS];  // this CTA's key range per query slot
   __shared__ int32_t ptab[kGather ? 1 : 2 * kMaxTilesPerCta];     // page mode: pages of this CTA's tiles
   __shared__ int32_t gtab[kGather ? kMaxGatherTiles * 128 : 1];   // gather mode: page*64+slot or -1
 
-  int64_t nv[QPC];
+  int64_t nv[kQS];
   int64_t nv_max = 0;
 #pragma unroll
-  for (int q = 0; q < QPC; ++q) {
-    const int64_t ne = a.n_entries[b] < a.max_entries ? a.n_entries[b] : a.max_entries;
+  for (int q = 0; q < kQS; ++q) {
+    const int bq = (g0 + q) / a.Tq;
+    const int64_t ne = q < n_act ? (a.n_entries[bq] < a.max_entries ? a.n_entries[bq] : a.max_entries) : 0;
     nv[q] = q < n_act ? visible_entries(a.q_pos[g0 + q], a.r, ne) : 0;
     nv_max = nv[q] > nv_max ? nv[q] : nv_max;
   }
   const int64_t npos = kGather ? (int64_t)a.n_blocks * kHsiBlock : nv_max;
   const int64_t n_tiles = (npos + 127) / 128;
-  const int64_t t_begin = (int64_t)blockIdx.x * a.tiles_per_cta;
-  const int64_t t_end = t_begin + a.tiles_per_cta < n_tiles ? t_begin + a.tiles_per_cta : n_tiles;
+  int64_t t_begin = (int64_t)blockIdx.x * a.tiles_per_cta;
+  int64_t t_end = t_begin + a.tiles_per_cta < n_tiles ? t_begin + a.tiles_per_cta : n_tiles;
+  // flat mode: the active tiles are slot 0's tiles ta0 .. ta0 + ka - 1, then
+  // slot 1's tiles 0 .. kb - 1 (tiles past a query's visible entries skipped)
+  int64_t ta0 = 0;
+  int ka = 0;
+  if (flat) {
+    ta0 = gt0 - (int64_t)qc0 * a.tq;
+    const int64_t na = (two ? (int64_t)(qc0 + 1) * a.tq : gt1) - gt0;
+    const int64_t nb = two ? gt1 - (int64_t)(qc0 + 1) * a.tq : 0;
+    const int64_t ra = (nv[0] + 127) / 128 - ta0, rb = (nv[1] + 127) / 128;  // visible tiles left
+    ka = (int)(ra < 0 ? 0 : (ra < na ? ra : na));
+    const int kb = (int)(rb < nb ? rb : nb);
+    t_begin = 0;
+    t_end = ka + kb;
+  }
+  // query slot and tile (within its query) of CTA-local tile i
+  auto tile_slot = [&](int64_t i) -> int { return flat ? (i < ka ? 0 : 1) : 0; };
+  auto tile_of = [&](int64_t i) -> int64_t { return flat ? (i < ka ? ta0 + i : i - ka) : t_begin + i; };
+  // key-range slot of query slot j: one per CTA of the query's tiles
+  auto kr_slot = [&](int j) -> int64_t {
+    return flat ? blockIdx.x - flat_cta_of((int64_t)(qc0 + j) * a.tq, a.total, gridDim.x) : (int64_t)blockIdx.x;
+  };
+  // this CTA's key range of query slot j; in the flat mode the CTA holding a
+  // query's last tile also empties the query's slots past its own
+  auto put_range = [&](int j, uint32_t lo, uint32_t hi) {
+    uint32_t* kr = a.krange + (int64_t)(qc0 + j) * a.kr_stride * 2;
+    const int64_t s = kr_slot(j);
+    kr[2 * s] = lo;
+    kr[2 * s + 1] = hi;
+    if (flat && (int64_t)(qc0 + j + 1) * a.tq <= gt1)
+      for (int64_t x = s + 1; x < a.kr_pad; ++x) {
+        kr[2 * x] = 0xFFFFFFFFu;
+        kr[2 * x + 1] = 0u;
+      }
+  };
   if (t_begin >= t_end) {  // uniform: the whole CTA leaves before any barrier, its slots empty
-    if (tid < n_act) {
-      uint32_t* kr = a.krange + ((int64_t)(qc0 + tid) * a.kr_stride + blockIdx.x) * 2;
-      kr[0] = 0xFFFFFFFFu;
-      kr[1] = 0u;
-    }
+    if (tid < n_act) put_range(tid, 0xFFFFFFFFu, 0u);
     return;
   }
   const int n_my = (int)(t_end - t_begin);
+  // logical page h of CTA-local tile i and the sequence it belongs to
+  auto page_id = [&](int i, int h) -> int32_t {
+    const int j = tile_slot(i);
+    const int64_t p = 2 * tile_of(i) + h;
+    const int64_t lim = flat ? nv[j] : nv_max;  // a group's tiles serve every query of the group
+    return (p * kPage < lim) ? (int32_t)page_of(a.ic, (g0 + j) / a.Tq, p * kPage, a.status) : -1;
+  };
 
   // ---- barriers and TMEM first: the producer starts copying pages while the
   // consumers build the Q tile
@@ -196,7 +263,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     }
     for (int w = 0; w < kWG; ++w) tc::mbar_init(&mma_bar[w], 1);
     abort_flag = 0;
-    for (int q = 0; q < QPC; ++q) {
+    for (int q = 0; q < kQS; ++q) {
       rng_lo[q] = 0xFFFFFFFFu;
       rng_hi[q] = 0u;
     }
@@ -216,10 +283,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     if (!kGather) {
       const int lane = tid & 31;
       const int first = n_my < kStages ? n_my : kStages;
-      if (lane < 2 * first) {  // pages of the first pass; the consumers resolve the rest
-        const int64_t p = 2 * t_begin + lane;  // logical page
-        ptab[lane] = (p * kPage < nv_max) ? (int32_t)page_of(a.ic, b, p * kPage, a.status) : -1;
-      }
+      if (lane < 2 * first) ptab[lane] = page_id(lane >> 1, lane & 1);  // the first pass; the consumers resolve the rest
       __syncwarp();
       auto issue = [&](int i) {
         const int s = i % kStages;
@@ -272,13 +336,10 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   // weights, gather positions
   if (!kGather) {
     const int first = n_my < kStages ? n_my : kStages;
-    for (int i = 2 * first + tid; i < 2 * n_my; i += kConsumers) {
-      const int64_t p = 2 * t_begin + i;  // logical page
-      ptab[i] = (p * kPage < nv_max) ? (int32_t)page_of(a.ic, b, p * kPage, a.status) : -1;
-    }
+    for (int i = 2 * first + tid; i < 2 * n_my; i += kConsumers) ptab[i] = page_id(i >> 1, i & 1);
     pages_arrive();
   }
-  for (int i = tid; i < kN * kIdxDim / 8; i += kConsumers) {
+  for (int i = tid; i < kQS * 32 * kIdxDim / 8; i += kConsumers) {
     const int row = (8 * i) / kIdxDim, k = (8 * i) % kIdxDim;  // row = q*32 + h; 8 channels per load
     uint4 v = make_uint4(0u, 0u, 0u, 0u);  // masked queries: zero rows
     if (row / kIdxHeads < n_act)
@@ -288,7 +349,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     if (score::q_operand8<kBf16>(w, a.q_fp4 != 0)) report(a.status, CSA2_ERR_RANGE);
     *reinterpret_cast<uint4*>(qtile + tc::kmajor_off(row, k, kIdxDim)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  for (int i = tid; i < QPC * kIdxHeads; i += kConsumers)
+  for (int i = tid; i < kQS * kIdxHeads; i += kConsumers)
     hw[i / kIdxHeads][i % kIdxHeads] =
         (a.head_w && i / kIdxHeads < n_act) ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;
   if (kGather) {
@@ -322,9 +383,9 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   auto dcol_of = [&](int uu) { return dcol0 + (uint32_t)((uu % kDBuf) * kN); };
   uint8_t* atile = abuf + (size_t)g * kABytes;
   const int n_own = n_my > g ? (n_my - g + kWG - 1) / kWG : 0;
-  uint32_t klo[QPC], khi[QPC];
+  uint32_t klo[kQS], khi[kQS];
 #pragma unroll
-  for (int q = 0; q < QPC; ++q) {
+  for (int q = 0; q < kQS; ++q) {
     klo[q] = 0xFFFFFFFFu;
     khi[q] = 0u;
   }
@@ -364,12 +425,14 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   // scores, HSI block maxima, key ranges
   auto epilogue = [&](int e, bool ok) {
     const int ie = g + kWG * e;
-    const int64_t pos = (t_begin + ie) * 128 + lt;  // entry id (page mode) / pool position (gather mode)
+    const int64_t pos = tile_of(ie) * 128 + lt;  // entry id (page mode) / pool position (gather mode)
+    const int qs = tile_slot(ie);
 #pragma unroll
-    for (int q = 0; q < QPC; ++q) {
-      if (q >= n_act) break;  // uniform over the CTA
+    for (int q = 0; q < kQS; ++q) {
+      if (q >= n_act) break;      // uniform over the CTA
+      if (flat && q != qs) continue;  // flat mode: a tile scores one query slot, in D's first 32 columns
       uint32_t d[32];
-      tc::tmem_ld32(tc::taddr(tb, lane_base, dcol_of(e) + 32 * q), d);
+      tc::tmem_ld32(tc::taddr(tb, lane_base, dcol_of(e) + 32 * (flat ? 0 : q)), d);
       tc::tmem_wait_ld();
       // four partial sums over heads h = 4i + j, added pairwise
       float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -490,7 +553,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     if (lt == 0) {
 #pragma unroll
       for (int ks = 0; ks < kIdxDim / 16; ++ks) {
-        const uint64_t bdesc = tc::sdesc(tc::smem_u32(qtile) + ks * 256, 128, kIdxDim * 16);
+        const uint64_t bdesc =
+            tc::sdesc(tc::smem_u32(qtile) + tile_slot(g + kWG * u) * 256 * 32 + ks * 256, 128, kIdxDim * 16);
         if (kSmemA)
           tc::mma_ss(tb + dcol_of(u), tc::sdesc(tc::smem_u32(atile) + ks * 256, 128, kIdxDim * 16), bdesc, kIdesc,
                      ks > 0);
@@ -501,13 +565,27 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     }
   };
 
+  // wait for MMA u (its A buffer is free again and its D holds the products)
+  auto wait_mma = [&](int u) {
+    const bool ok = tc::mbar_wait(&mma_bar[g], u & 1);
+    waited = u;
+    if (!ok) {
+      report(a.status, CSA2_ERR_TIMEOUT);
+      atomicExch(&abort_flag, 1);
+    }
+    tc::fence_after_sync();
+    return ok;
+  };
+
   // Per own tile u: wait for MMA u-1 (the A buffer is free and D(u-1) holds
   // its products), decode and store A, issue MMA u; then the epilogue of u-1
   // while MMA u runs (with one D buffer the epilogue of u-1 comes before the
   // decode of u instead).
   // The tile is decoded after the wait, straight into the A buffer: decoding
   // it into registers before the wait (kEarly) was measured slower on the
-  // single-query scans, whose 544-thread CTAs then spill.
+  // single-query scans, whose 544-thread CTAs then spill, and so was a second
+  // A buffer per warpgroup in shared memory (odd tiles) that let the MMA of
+  // one tile run under the decode of the next.
   constexpr bool kEarly = false;
   for (int u = 0; u <= n_own; ++u) {
     const bool have = u < n_own;
@@ -515,13 +593,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     if (kEarly && have) decode(u, r);
     bool ok = true;
     if (u >= 1) {
-      ok = tc::mbar_wait(&mma_bar[g], (u - 1) & 1);
-      waited = u - 1;
-      if (!ok) {
-        report(a.status, CSA2_ERR_TIMEOUT);
-        atomicExch(&abort_flag, 1);
-      }
-      tc::fence_after_sync();
+      ok = wait_mma(u - 1);
       if (kDBuf == 1) epilogue(u - 1, ok);
     }
     if (!kEarly && have) decode(u, r);
@@ -538,7 +610,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   }
   if (kGather) cp_wait<0>();  // no copies into this CTA's shared memory outlive it
 #pragma unroll
-  for (int q = 0; q < QPC; ++q) {
+  for (int q = 0; q < kQS; ++q) {
     uint32_t lo = klo[q], hi = khi[q];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -557,11 +629,8 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   tc::fence_before_sync();
   consumers_sync(kConsumers);
   if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
-  if (tid < n_act) {  // one slot per CTA and query: no initialisation of global state needed
-    uint32_t* kr = a.krange + ((int64_t)(qc0 + tid) * a.kr_stride + blockIdx.x) * 2;
-    kr[0] = rng_lo[tid];
-    kr[1] = rng_hi[tid];
-  }
+  // one slot per CTA and query: no initialisation of global state needed
+  if (tid < n_act) put_range(tid, rng_lo[tid], rng_hi[tid]);
 }
 
 }  // namespace
@@ -570,7 +639,8 @@ template <int kDtype, int QPC, bool kGather>
 static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaStream_t stream) {
   using F = TileFmt<kDtype>;
   using Sh = Shape<kDtype, QPC>;
-  size_t smem = 256 * 32 * QPC + (size_t)Sh::kStages * F::kSlotBytes + (Sh::kSmemA ? (size_t)Sh::kWG * kABytes : 0);
+  constexpr int kQS = (QPC == 1 && !kGather) ? 2 : QPC;  // query tiles held
+  size_t smem = 256 * 32 * kQS + (size_t)Sh::kStages * F::kSlotBytes + (Sh::kSmemA ? (size_t)Sh::kWG * kABytes : 0);
   // one CTA per SM: its TMEM allocation may take all 512 columns
   smem = std::max<size_t>(smem, 116 * 1024);
   auto kern = score_tc_kernel<kDtype, QPC, kGather>;
@@ -586,6 +656,11 @@ struct ScoreGrid {
   int qpc, seg, gps, groups;
   int64_t per;
   int splits;
+  // one-wave flattened partition of single-query page scans: `splits` CTAs
+  // over nq x tq tiles, kr_pad key-range slots per query
+  bool flat;
+  int64_t tq, total;
+  int kr_pad;
 };
 
 ScoreGrid score_grid(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_entries, bool gather, int num_sms) {
@@ -593,7 +668,7 @@ ScoreGrid score_grid(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_en
   // into them without crossing a sequence (prefill chunks); whole sequences of
   // a chunk of whole sequences otherwise (multi-query decode: up to 6 queries
   // in one group, longer blocks in groups of 4); single queries else
-  ScoreGrid g{1, 1, 1, 0, 0, 0};
+  ScoreGrid g{1, 1, 1, 0, 0, 0, false, 0, 0, 0};
   if (!gather && Tq % 4 == 0 && q0 % 4 == 0 && nq % 4 == 0) {
     g.qpc = 4;
     g.seg = 4;
@@ -612,13 +687,36 @@ ScoreGrid score_grid(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_en
   const int64_t cap = gather ? kMaxGatherTiles : kMaxTilesPerCta;
   g.per = std::min<int64_t>(cap, std::max<int64_t>(4, (tiles + want - 1) / want));
   g.splits = (int)((tiles + g.per - 1) / g.per);
+  g.kr_pad = g.splits;
+  // Single queries over more than one wave: one CTA per SM over the queries'
+  // tiles laid end to end instead.  With at most as many queries as CTAs a
+  // CTA's range (at most tq tiles) touches at most two queries; each query's
+  // key-range slots are those of the CTAs over its tiles, padded to the most
+  // any query has.
+  const int64_t total = (int64_t)nq * tiles;
+  if (g.qpc == 1 && !gather && (int64_t)g.groups * g.splits > num_sms && nq <= num_sms &&
+      total >= 4 * (int64_t)num_sms && (total + num_sms - 1) / num_sms <= kMaxTilesPerCta) {
+    int64_t pad = 0;
+    for (int q = 0; q < nq; ++q)
+      pad = std::max<int64_t>(pad, flat_cta_of((int64_t)(q + 1) * tiles - 1, total, num_sms) -
+                                       flat_cta_of((int64_t)q * tiles, total, num_sms) + 1);
+    if (pad <= score_range_slots(tiles)) {
+      g.flat = true;
+      g.tq = tiles;
+      g.total = total;
+      g.splits = num_sms;
+      g.groups = 1;
+      g.per = (total + num_sms - 1) / num_sms;
+      g.kr_pad = (int)pad;
+    }
+  }
   return g;
 }
 
 }  // namespace
 
 int score_slots_used(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_entries, bool gather, int num_sms) {
-  return score_grid(cfg, q0, nq, Tq, max_entries, gather, num_sms).splits;
+  return score_grid(cfg, q0, nq, Tq, max_entries, gather, num_sms).kr_pad;
 }
 
 cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const uint16_t* q_idx, const float* head_w,
@@ -630,11 +728,12 @@ cudaError_t launch_score_tc(const csa2_cfg& cfg, int q0, int nq, int Tq, const u
   const ScoreGrid sg = score_grid(cfg, q0, nq, Tq, max_entries, gather, num_sms);
   const int qpc = sg.qpc, seg = sg.seg, gps = sg.gps, groups = sg.groups, splits = sg.splits;
   const int64_t per = sg.per;
-  if (splits > kr_stride) return cudaErrorInvalidValue;
-  *n_slots = splits;
+  if (sg.kr_pad > kr_stride) return cudaErrorInvalidValue;
+  *n_slots = sg.kr_pad;
   ScoreArgs a{q0, Tq, cfg.ratio, seg, gps, (cfg.formats & CSA2_FMT_IDX_QFP4) ? 1 : 0,
               (!gather && (int64_t)splits * groups <= num_sms) ? 1 : 0, q_idx, head_w, q_pos, view_of(idx_c),
-              n_entries, max_entries, (int)per, pool, cfg.hsi_blocks, scores, stride, bmax, krange, kr_stride, status};
+              n_entries, max_entries, (int)per, pool, cfg.hsi_blocks, scores, stride, bmax, krange, kr_stride, status,
+              sg.flat ? 1 : 0, sg.tq, sg.total, sg.kr_pad};
   if (idx_dtype(cfg) == CSA2_CACHE_FP4_S32) {
     if (gather) return launch_one<CSA2_CACHE_FP4_S32, 1, true>(a, groups, splits, stream);
     if (qpc == 6) return launch_one<CSA2_CACHE_FP4_S32, 6, false>(a, groups, splits, stream);

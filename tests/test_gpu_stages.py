@@ -679,31 +679,52 @@ def test_large_pools_over_many_blocks_are_ascending_and_exact(nb):
             assert P.topk_mismatch(g_top.reshape(B, k), o_top.reshape(B, k), s.reshape(B, -1), k, exact=False) == 0
 
 
-@pytest.mark.parametrize("fmt", ["fp4", "fp4g32"])
-def test_single_query_scan_many_tiles_per_cta_exact(fmt):
-    """The single-query scan over many pages: 8 sequences of up to 50000
-    entries share one wave of CTAs, so every CTA streams about 20 tiles (its
-    shared-memory ring of 16 slots wraps around) and most CTAs' ranges cross
-    from one query into the next; ragged entry counts and query positions
-    leave inactive tiles at the ends of some ranges.  Integer inputs: the
-    top-k and the HSI pool must equal the oracle's bit for bit; the 68-byte
-    entries run the same path."""
-    B, N, k, nb = 8, 50000, 512, 1024
+def _single_query_scan(fmt, seed, N, n_ent, q_pos, nb=1024, k=512):
+    """Integer-valued single-query scans of B sequences (repeated rows make
+    ties at the k-th place): top-k and HSI pool against the oracle, bit for
+    bit."""
+    B = len(n_ent)
     oc = oracle.Cache(B, N, CI, fmt)
-    g = synth.rng(33, "idx")
+    g = synth.rng(seed, "idx")
     for b in range(B):
         codes, scales = synth.integer_fp4_bytes(g, N, CI)  # every scale 1.0
         oc.codes[b], oc.scales[b] = codes, scales[:, :oc.scales.shape[-1]]
-    pick = synth.rng(33, "dup").integers(0, 3000, size=(B, N))  # repeated rows: ties at the k-th place
+    pick = synth.rng(seed, "dup").integers(0, 3000, size=(B, N))
     for b in range(B):
         oc.codes[b], oc.scales[b] = oc.codes[b][pick[b]], oc.scales[b][pick[b]]
-    pc = _paged.cache_pair(B, N, CI, "fp4" if fmt == "fp4" else "fp4g32", 33)
+    pc = _paged.cache_pair(B, N, CI, "fp4" if fmt == "fp4" else "fp4g32", seed)
     _paged.upload(pc, oc)
-    q_idx = synth.integer_bf16(synth.rng(33, "q"), (B, 1, H, CI), -1, 1)
-    n_ent = np.array([50000, 49999, 31000, 50000, 12345, 50000, 40000, 50000], np.int32)
-    q_pos = np.array([[49999], [49999], [30999], [20000], [12344], [49999], [39999], [777]], np.int64)
+    q_idx = synth.integer_bf16(synth.rng(seed, "q"), (B, 1, H, CI), -1, 1)
+    n_ent = np.asarray(n_ent, np.int32)
+    q_pos = np.asarray(q_pos, np.int64).reshape(B, 1)
     cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=nb, formats=csa.FMT_IDX_68B if fmt == "fp4g32" else 0)
     g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
     o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, want_pool=True)
     np.testing.assert_array_equal(g_top, o_top)
     np.testing.assert_array_equal(g_pool, o_pool)
+
+
+@pytest.mark.parametrize("fmt", ["fp4", "fp4g32"])
+def test_single_query_scan_many_tiles_per_cta_exact(fmt):
+    """The single-query scan over many pages: 8 sequences of up to 50000
+    entries share one wave of CTAs, so every CTA streams about 20 tiles (its
+    shared-memory ring of 16 slots wraps around); ragged entry counts and
+    query positions leave inactive tiles at the ends of some ranges.  The
+    68-byte entries run the same path."""
+    _single_query_scan(fmt, 33, 50000, [50000, 49999, 31000, 50000, 12345, 50000, 40000, 50000],
+                       [49999, 49999, 30999, 20000, 12344, 49999, 39999, 777])
+
+
+@pytest.mark.parametrize("fmt", ["fp4", "fp4g32"])
+def test_single_query_scan_flattened_over_one_wave_exact(fmt):
+    """24 single queries, too many for one wave of per-query CTA ranges: the
+    scorer lays the queries' tiles end to end over one CTA per SM, so most
+    CTAs' ranges cross from one query into the next (two query tiles, two
+    key-range slots) and the selection reads each query's slots by the
+    partition.  Ragged lengths: a sequence of one entry, short sequences whose
+    CTAs have no visible tile, a query that sees a few entries only."""
+    n_ent = [20000, 1, 19999, 300, 20000, 12345, 20000, 129, 20000, 20000, 7000, 20000,
+             20000, 18000, 20000, 128, 20000, 20000, 20000, 5000, 20000, 19000, 20000, 20000]
+    q_pos = [19999, 0, 19998, 299, 100, 12344, 19999, 128, 19999, 3, 6999, 19999,
+             19999, 17999, 10000, 127, 19999, 19999, 19999, 4999, 19999, 18999, 19999, 640]
+    _single_query_scan(fmt, 34, 20000, n_ent, q_pos)

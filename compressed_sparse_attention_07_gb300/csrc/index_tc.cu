@@ -39,12 +39,15 @@ namespace {
 // with the decoded K tile in shared memory (TMEM then holds only the
 // accumulators, 4 x 128 columns); two otherwise (TMEM and shared-memory
 // budget).
-template <int kDtype, int QPC>
+template <int kDtype, int QPC, bool kGather>
 struct Shape {
   static constexpr bool kSmemA = QPC == 4 && kDtype != CSA2_CACHE_BF16;
   static constexpr int kWG = ((QPC == 1 && kDtype != CSA2_CACHE_BF16) || kSmemA) ? 4 : 2;
   static constexpr int kConsumers = 128 * kWG;
-  static constexpr int kThreads = kConsumers + 32;  // + one producer warp (page mode)
+  // single-query FP4 page scans: one issuer warp per consumer warpgroup
+  // (copies of its tiles, its MMAs) instead of one producer warp
+  static constexpr bool kIss = QPC == 1 && kDtype != CSA2_CACHE_BF16 && !kGather;
+  static constexpr int kThreads = kConsumers + (kIss ? 32 * kWG : 32);
   static constexpr int kStages = kSmemA ? 6 : 2 * kWG;  // ring slots, used in tile order
 };
 constexpr int kABytes = 128 * kIdxDim * 2;  // a decoded K tile in shared memory (f16, K-major)
@@ -120,19 +123,24 @@ template <int kThreadsAll>
 __device__ __forceinline__ void pages_arrive_n() { asm volatile("bar.arrive 6, %0;" ::"n"(kThreadsAll) : "memory"); }
 template <int kThreadsAll>
 __device__ __forceinline__ void pages_sync_n() { asm volatile("bar.sync 6, %0;" ::"n"(kThreadsAll) : "memory"); }
+// End of a CTA with issuer warps (barrier 7, all threads).
+template <int kThreadsAll>
+__device__ __forceinline__ void all_sync_n() { asm volatile("bar.sync 7, %0;" ::"n"(kThreadsAll) : "memory"); }
 
 template <int kDtype, int QPC, bool kGather>
-__global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) score_tc_kernel(ScoreArgs a) {
   using F = TileFmt<kDtype>;
-  constexpr int kWG = Shape<kDtype, QPC>::kWG;
-  constexpr int kConsumers = Shape<kDtype, QPC>::kConsumers;
-  constexpr int kThreads = Shape<kDtype, QPC>::kThreads;
-  constexpr int kStages = Shape<kDtype, QPC>::kStages;
+  using Sh = Shape<kDtype, QPC, kGather>;
+  constexpr int kWG = Sh::kWG;
+  constexpr int kConsumers = Sh::kConsumers;
+  constexpr int kThreads = Sh::kThreads;
+  constexpr int kStages = Sh::kStages;
+  constexpr bool kIss = Sh::kIss;
   auto pages_arrive = [] { pages_arrive_n<kThreads>(); };
   auto pages_sync = [] { pages_sync_n<kThreads>(); };
   constexpr int kN = 32 * QPC;                    // MMA N: QPC queries x 32 heads
   constexpr int kAcols = 64;                      // 128 channels of f16 pairs
-  constexpr bool kSmemA = Shape<kDtype, QPC>::kSmemA;
+  constexpr bool kSmemA = Sh::kSmemA;
   // D double-buffered per warpgroup when tensor memory holds it (the MMA of
   // tile u runs while the epilogue of tile u-1 reads the other buffer)
   constexpr int kDBuf = (!kSmemA && kWG * kAcols + 2 * kWG * kN <= 512) ? 2 : 1;
@@ -188,6 +196,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   uint8_t* abuf = ring + kStages * TileFmt<kDtype>::kSlotBytes;  // kSmemA: one K tile per warpgroup
   __shared__ float hw[kQS][kIdxHeads];
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], mma_bar[kWG];
+  __shared__ __align__(8) uint64_t a_full[kWG];  // kIss: warpgroup g has stored its A tile
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ uint32_t rng_lo[kQS], rng_hi[kQS];  // this CTA's key range per query slot
@@ -261,7 +270,10 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
       tc::mbar_init(&full_bar[s], 1);
       tc::mbar_init(&empty_bar[s], 128);
     }
-    for (int w = 0; w < kWG; ++w) tc::mbar_init(&mma_bar[w], 1);
+    for (int w = 0; w < kWG; ++w) {
+      tc::mbar_init(&mma_bar[w], 1);
+      tc::mbar_init(&a_full[w], 128);
+    }
     abort_flag = 0;
     for (int q = 0; q < kQS; ++q) {
       rng_lo[q] = 0xFFFFFFFFu;
@@ -278,6 +290,86 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   tc::fence_after_sync();
   const uint32_t tb = tmem_base;
 
+  // the copy of CTA-local tile i into its ring slot (page mode)
+  auto copy_tile = [&](int i) {
+    const int s = i % kStages;
+    uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
+    uint32_t bytes = 0;
+    int64_t pages[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      pages[hh] = ptab[2 * i + hh];
+      if (pages[hh] >= 0) bytes += F::kPageData + F::kPageScales;
+    }
+    tc::mbar_arrive_expect_tx(&full_bar[s], bytes);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      if (pages[hh] < 0) continue;
+      tc::bulk_g2s(slot + hh * F::kPageData, a.ic.data + pages[hh] * F::kPageData, F::kPageData, &full_bar[s]);
+      if (F::kPageScales)
+        tc::bulk_g2s(slot + 2 * F::kPageData + hh * F::kPageScales, a.ic.scales + pages[hh] * F::kPageScales,
+                     F::kPageScales, &full_bar[s]);
+    }
+  };
+
+  if (kIss && warp >= kConsumers / 32) {
+    // ------------------------------------------------------------- issuers
+    // Issuer warp k serves warpgroup k, whose tiles k, k + kWG, ... use ring
+    // slots k and k + kWG in turn: it copies the warpgroup's next tile into a
+    // slot once the warpgroup has decoded the slot's tile and stored it as A
+    // (a_full), and issues that tile's MMA.  The MMA issue, which holds its
+    // thread for about a thousand cycles per tile, so stays off the
+    // warpgroup's own path.
+    const int k = warp - kConsumers / 32;
+    const int lane = tid & 31;
+    const int n_k = n_my > k ? (n_my - k + kWG - 1) / kWG : 0;
+    const int first = n_k < 2 ? n_k : 2;
+    if (lane < 2 * first) {
+      const int i = k + kWG * (lane >> 1);
+      ptab[2 * i + (lane & 1)] = page_id(i, lane & 1);
+    }
+    __syncwarp();
+    if (lane < first) copy_tile(k + kWG * lane);
+    __syncwarp();
+    pages_sync();  // the consumers' share of the page table is written
+    if (lane == 0) {
+      const uint32_t acol_k = (uint32_t)(k * kAcols);
+      const uint32_t dcol_k = (uint32_t)(kWG * kAcols + k * kDBuf * kN);
+      int issued = -1, copied = first;
+      for (int u = 0; u < n_k; ++u) {
+        if (!tc::mbar_wait(&a_full[k], u & 1)) {
+          report(a.status, CSA2_ERR_TIMEOUT);
+          atomicExch(&abort_flag, 1);
+          break;
+        }
+        if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+        tc::fence_after_sync();
+        const int i = k + kWG * u;
+        const uint32_t qaddr = tc::smem_u32(qtile) + tile_slot(i) * 256 * 32;
+#pragma unroll
+        for (int ks = 0; ks < kIdxDim / 16; ++ks)
+          tc::mma_ts(tb + dcol_k + (uint32_t)((u % kDBuf) * kN), tb + acol_k + ks * 8,
+                     tc::sdesc(qaddr + ks * 256, 128, kIdxDim * 16), kIdesc, ks > 0);
+        tc::mma_commit(&mma_bar[k]);
+        issued = u;
+        if (u + 2 < n_k) {
+          copy_tile(k + kWG * (u + 2));
+          copied = u + 3;
+        }
+      }
+      // no copy into this CTA's shared memory and no MMA in flight at its end
+      for (int v = copied > 2 ? copied - 2 : 0; v < copied; ++v) {
+        const int i = k + kWG * v;
+        if (!tc::mbar_wait(&full_bar[i % kStages], (i / kStages) & 1)) report(a.status, CSA2_ERR_TIMEOUT);
+      }
+      if (issued >= 0 && !tc::mbar_wait(&mma_bar[k], issued & 1)) report(a.status, CSA2_ERR_TIMEOUT);
+    }
+    __syncwarp();
+    tc::fence_before_sync();
+    all_sync_n<kThreads>();  // then the consumers release tensor memory
+    return;
+  }
+
   if (warp == kConsumers / 32) {
     // ------------------------------------------------------------ producer
     if (!kGather) {
@@ -285,26 +377,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
       const int first = n_my < kStages ? n_my : kStages;
       if (lane < 2 * first) ptab[lane] = page_id(lane >> 1, lane & 1);  // the first pass; the consumers resolve the rest
       __syncwarp();
-      auto issue = [&](int i) {
-        const int s = i % kStages;
-        uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
-        uint32_t bytes = 0;
-        int64_t pages[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          pages[hh] = ptab[2 * i + hh];
-          if (pages[hh] >= 0) bytes += F::kPageData + F::kPageScales;
-        }
-        tc::mbar_arrive_expect_tx(&full_bar[s], bytes);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if (pages[hh] < 0) continue;
-          tc::bulk_g2s(slot + hh * F::kPageData, a.ic.data + pages[hh] * F::kPageData, F::kPageData, &full_bar[s]);
-          if (F::kPageScales)
-            tc::bulk_g2s(slot + 2 * F::kPageData + hh * F::kPageScales, a.ic.scales + pages[hh] * F::kPageScales,
-                         F::kPageScales, &full_bar[s]);
-        }
-      };
+      auto issue = copy_tile;
       // the first pass over the ring (fresh slots) from one lane per tile, the
       // rest in order from lane 0 once the consumers release each slot
       if (lane < first) issue(lane);
@@ -471,7 +544,70 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
 
   // own tile u's entry (this thread's) from the ring, decoded into 64
   // registers of f16 (or bf16) pairs; the ring slot is released
+  // An FP4 entry as read from the ring: 64 bytes of codes and its scales
+  struct Fp4Entry {
+    uint4 cw[4];
+    uint2 sc;
+    bool present;
+  };
+  // own tile u's entry (this thread's) read from the ring, whose slot is
+  // then released
+  auto fetch = [&](int u, Fp4Entry& e) {
+    const int i = g + kWG * u;
+    const int s = i % kStages;
+    if (kGather) {
+      gather(u + 1);
+      cp_wait<1>();
+    } else if (!tc::mbar_wait(&full_bar[s], (i / kStages) & 1)) {
+      atomicExch(&abort_flag, 1);
+    }
+    const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
+    e.present = !kGather || gtab[i * 128 + lt] >= 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      e.cw[c] = *reinterpret_cast<const uint4*>(slot + h * kIdxFp4Data + (c * kPage + sl) * 16);
+    // the entry's scales: 8 bytes (one per 16 channels) or 4 (one per 32)
+    if (kDtype == CSA2_CACHE_FP4)
+      e.sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 8);
+    else
+      e.sc = make_uint2(*reinterpret_cast<const uint32_t*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 4), 0u);
+    if (!kGather && !kIss) tc::mbar_arrive(&empty_bar[s]);
+  };
+  // the entry decoded into 64 registers of f16 pairs
+  auto convert = [&](const Fp4Entry& e, uint32_t (&r)[64]) {
+    // the scales as broadcast f16x2: s2g[g] for 16-channel group g (or
+    // 32-channel group g with one scale per 32 channels)
+    uint32_t s2g[8];
+    e4m3_pair_bcast(e.sc.x, s2g[0], s2g[1]);
+    e4m3_pair_bcast(e.sc.x >> 16, s2g[2], s2g[3]);
+    if (kDtype == CSA2_CACHE_FP4) {
+      e4m3_pair_bcast(e.sc.y, s2g[4], s2g[5]);
+      e4m3_pair_bcast(e.sc.y >> 16, s2g[6], s2g[7]);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {  // 32 channels -> 16 registers
+      const uint32_t w4[4] = {e.cw[c].x, e.cw[c].y, e.cw[c].z, e.cw[c].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
+        const uint32_t s2 = kDtype == CSA2_CACHE_FP4 ? s2g[gg] : s2g[c];
+        uint32_t h4[4];
+        e2m1x8_to_f16x2(w4[q], h4);
+#pragma unroll
+        for (int by = 0; by < 4; ++by) r[16 * c + q * 4 + by] = e.present ? hmul2(h4[by], s2) : 0u;
+      }
+    }
+  };
+
+  // own tile u's entry (this thread's) from the ring, decoded into 64
+  // registers of f16 (or bf16) pairs; the ring slot is released
   auto decode = [&](int u, uint32_t (&r)[64]) {
+    if (kDtype != CSA2_CACHE_BF16) {
+      Fp4Entry e;
+      fetch(u, e);
+      convert(e, r);
+      return;
+    }
     const int i = g + kWG * u;
     const int s = i % kStages;
     if (kGather) {
@@ -482,51 +618,15 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     }
     const uint8_t* slot = ring + (size_t)s * F::kSlotBytes;
     const bool present = !kGather || gtab[i * 128 + lt] >= 0;
-    if (kDtype != CSA2_CACHE_BF16) {
-      uint4 cw[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        cw[c] = *reinterpret_cast<const uint4*>(slot + h * kIdxFp4Data + (c * kPage + sl) * 16);
-      // the entry's scales: 8 bytes (one per 16 channels) or 4 (one per 32)
-      uint2 sc;
-      if (kDtype == CSA2_CACHE_FP4)
-        sc = *reinterpret_cast<const uint2*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 8);
-      else
-        sc = make_uint2(*reinterpret_cast<const uint32_t*>(slot + 2 * kIdxFp4Data + h * F::kPageScales + sl * 4), 0u);
-      if (!kGather) tc::mbar_arrive(&empty_bar[s]);
-      // the scales as broadcast f16x2: s2g[g] for 16-channel group g (or
-      // 32-channel group g with one scale per 32 channels)
-      uint32_t s2g[8];
-      e4m3_pair_bcast(sc.x, s2g[0], s2g[1]);
-      e4m3_pair_bcast(sc.x >> 16, s2g[2], s2g[3]);
-      if (kDtype == CSA2_CACHE_FP4) {
-        e4m3_pair_bcast(sc.y, s2g[4], s2g[5]);
-        e4m3_pair_bcast(sc.y >> 16, s2g[6], s2g[7]);
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {  // 32 channels -> 16 registers
-        const uint32_t w4[4] = {cw[c].x, cw[c].y, cw[c].z, cw[c].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
-          const uint32_t s2 = kDtype == CSA2_CACHE_FP4 ? s2g[gg] : s2g[c];
-          uint32_t h4[4];
-          e2m1x8_to_f16x2(w4[q], h4);
-#pragma unroll
-          for (int by = 0; by < 4; ++by) r[16 * c + q * 4 + by] = present ? hmul2(h4[by], s2) : 0u;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(slot + h * kIdxBf16Data + (c * kPage + sl) * 16);
-        r[4 * c] = present ? v.x : 0u;
-        r[4 * c + 1] = present ? v.y : 0u;
-        r[4 * c + 2] = present ? v.z : 0u;
-        r[4 * c + 3] = present ? v.w : 0u;
-      }
-      if (!kGather) tc::mbar_arrive(&empty_bar[s]);
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(slot + h * kIdxBf16Data + (c * kPage + sl) * 16);
+      r[4 * c] = present ? v.x : 0u;
+      r[4 * c + 1] = present ? v.y : 0u;
+      r[4 * c + 2] = present ? v.z : 0u;
+      r[4 * c + 3] = present ? v.w : 0u;
     }
+    if (!kGather && !kIss) tc::mbar_arrive(&empty_bar[s]);
   };
 
   // the decoded tile into the A buffer (shared or tensor memory)
@@ -587,7 +687,27 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
   // A buffer per warpgroup in shared memory (odd tiles) that let the MMA of
   // one tile run under the decode of the next.
   constexpr bool kEarly = false;
-  for (int u = 0; u <= n_own; ++u) {
+  if (kIss) {
+    // With an issuer warp: wait for MMA u-1 (A free again), decode and store
+    // A and signal the issuer, then the epilogue of u-1 while MMA u is issued
+    // and runs.  The warps of the warpgroup do not wait for one another.
+    // Reading the next tile's entry from the ring before the wait was
+    // measured slower (the registers it holds across the wait spill).
+    for (int u = 0; u <= n_own; ++u) {
+      bool ok = true;
+      if (u >= 1) ok = wait_mma(u - 1);
+      if (u < n_own) {
+        uint32_t r[64];
+        decode(u, r);
+        store_a(r);
+        tc::fence_before_sync();
+        tc::mbar_arrive(&a_full[g]);
+      }
+      if (u >= 1) epilogue(u - 1, ok);
+      if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+    }
+  }
+  for (int u = 0; !kIss && u <= n_own; ++u) {
     const bool have = u < n_own;
     uint32_t r[64];
     if (kEarly && have) decode(u, r);
@@ -627,7 +747,10 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
     if (!tc::mbar_wait(&mma_bar[g], last_issued & 1)) report(a.status, CSA2_ERR_TIMEOUT);
   }
   tc::fence_before_sync();
-  consumers_sync(kConsumers);
+  if (kIss)
+    all_sync_n<kThreads>();  // the issuers' MMAs have completed
+  else
+    consumers_sync(kConsumers);
   if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
   // one slot per CTA and query: no initialisation of global state needed
   if (tid < n_act) put_range(tid, rng_lo[tid], rng_hi[tid]);
@@ -638,7 +761,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC>::kThreads, 1) score_tc_kern
 template <int kDtype, int QPC, bool kGather>
 static cudaError_t launch_one(const ScoreArgs& a, int groups, int splits, cudaStream_t stream) {
   using F = TileFmt<kDtype>;
-  using Sh = Shape<kDtype, QPC>;
+  using Sh = Shape<kDtype, QPC, kGather>;
   constexpr int kQS = (QPC == 1 && !kGather) ? 2 : QPC;  // query tiles held
   size_t smem = 256 * 32 * kQS + (size_t)Sh::kStages * F::kSlotBytes + (Sh::kSmemA ? (size_t)Sh::kWG * kABytes : 0);
   // one CTA per SM: its TMEM allocation may take all 512 columns

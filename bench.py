@@ -23,7 +23,7 @@ other workloads with a stated target -- the 20-layer decoder group (per
 group time) and the 4096-token prefill chunk (indexer against the tensor
 peak) -- and reports them under "targets".
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--batch B] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--batch B] [--tq T] [--impl reference]
 """
 from __future__ import annotations
 
@@ -758,6 +758,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per GPU instead of the workload's own (smaller profiling captures)")
+    ap.add_argument("--tq", type=int, default=None,
+                    help="query tokens per sequence instead of the workload's own (smaller prefill captures)")
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -768,6 +770,9 @@ def main():
     if args.batch is not None:
         wl = synth.WORKLOADS[args.workload]
         synth.WORKLOADS[args.workload] = dataclasses.replace(wl, batch=args.batch)
+    if args.tq is not None:
+        wl = synth.WORKLOADS[args.workload]
+        synth.WORKLOADS[args.workload] = dataclasses.replace(wl, tq=args.tq)
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
@@ -865,7 +870,7 @@ def main():
     wl_name, units, launches, cfg_extra = step.wl.name, step.units, step.launches_per_step, step.cfg_extra
     wl_obj = step.wl
     targets = None
-    if ws == 1 and not args.no_targets and args.workload == DEFAULT_WORKLOAD and args.batch is None:
+    if ws == 1 and not args.no_targets and args.workload == DEFAULT_WORKLOAD and args.batch is None and args.tq is None:
         del step, e2e, packs, dbuf
         torch.cuda.synchronize()
         torch.cuda.empty_cache()

@@ -811,13 +811,16 @@ ScoreGrid score_grid(const csa2_cfg& cfg, int q0, int nq, int Tq, int64_t max_en
   g.per = std::min<int64_t>(cap, std::max<int64_t>(4, (tiles + want - 1) / want));
   g.splits = (int)((tiles + g.per - 1) / g.per);
   g.kr_pad = g.splits;
-  // Single queries over more than one wave: one CTA per SM over the queries'
-  // tiles laid end to end instead.  With at most as many queries as CTAs a
-  // CTA's range (at most tq tiles) touches at most two queries; each query's
-  // key-range slots are those of the CTAs over its tiles, padded to the most
-  // any query has.
+  // Single queries: one CTA per SM over the queries' tiles laid end to end
+  // instead, when that gives an SM fewer tiles (more than one wave of
+  // per-query ranges, or ranges that leave SMs idle).  With at most as many
+  // queries as CTAs a CTA's range (at most tq tiles) touches at most two
+  // queries; each query's key-range slots are those of the CTAs over its
+  // tiles, padded to the most any query has.
   const int64_t total = (int64_t)nq * tiles;
-  if (g.qpc == 1 && !gather && (int64_t)g.groups * g.splits > num_sms && nq <= num_sms &&
+  const int64_t ctas = (int64_t)g.groups * g.splits;
+  const int64_t per_sm = g.per * ((ctas + num_sms - 1) / num_sms);  // tiles of the busiest SM
+  if (g.qpc == 1 && !gather && (total + num_sms - 1) / num_sms < per_sm && nq <= num_sms &&
       total >= 4 * (int64_t)num_sms && (total + num_sms - 1) / num_sms <= kMaxTilesPerCta) {
     int64_t pad = 0;
     for (int q = 0; q < nq; ++q)

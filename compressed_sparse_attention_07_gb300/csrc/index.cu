@@ -650,17 +650,23 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
   }
 }
 
-// The same selection for a single CTA holding all n <= kRound positions:
+// The same selection for a single CTA holding all n <= kRound positions
+// (one copy of its code shared by every call site: when the code is not
+// cached its instructions are fetched once, which was measured faster than
+// inlining it into each caller):
 // thread t owns positions kPer t .. kPer t + kPer - 1 and keeps their keys in registers
 // from the one read of the scores to the ordered write of the ids
 // (histogram, cut search, threshold-bin keys ranked or refined by digits,
 // then one scan of packed (above, equal) counts).
 // gpool != NULL: position p reads vals[gpool[p / 8] * 8 + p % 8] (a pool of
 // 8-entry blocks written earlier by this CTA; ids >= nv_lim or blocks < 0 are
-// not candidates).
-__device__ void select_small(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
+// not candidates).  Keys below kmin are not candidates either (the caller
+// knows at least k keys lie at or above it).  out_copy: the ids also written
+// there (shared memory); t_out: the threshold key (every selected key but the
+// forced one is at or above it).
+__device__ __noinline__ void select_small(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
                              uint32_t kmin, uint32_t kmax, SelShared& s, const int32_t* gpool = nullptr,
-                             int64_t nv_lim = 0) {
+                             int64_t nv_lim = 0, int32_t* out_copy = nullptr, uint32_t* t_out = nullptr) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const bool has_forced = forced >= 0 && forced < n;
   const uint32_t need = (uint32_t)k - (has_forced ? 1u : 0u);
@@ -738,11 +744,11 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
   if (ranked) {
 #pragma unroll
     for (int m = 0; m < kPer; ++m)
-      if (kk[m]) atomicAdd(&s.hist[bin_of(kk[m])], 1u);
+      if (kk[m] && kk[m] >= kmin) atomicAdd(&s.hist[bin_of(kk[m])], 1u);
     __syncthreads();
     find_cut(s.hist, kHistBins, need, s);
     if (s.cut_total <= need) {
-      T = 0;  // every valid key
+      T = kmin > 0u ? kmin - 1u : 0u;  // every candidate key
     } else {
       const uint32_t tb = s.cut_bin;
       uint32_t prefix = tb;
@@ -752,7 +758,7 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
         {  // this thread's keys of the cut bin, one shared-memory atomic per warp
           uint32_t mine = 0;
 #pragma unroll
-          for (int m = 0; m < kPer; ++m) mine += kk[m] != 0u && bin_of(kk[m]) == tb;
+          for (int m = 0; m < kPer; ++m) mine += kk[m] != 0u && kk[m] >= kmin && bin_of(kk[m]) == tb;
           const uint32_t incl = warp_incl_scan(mine);
           uint32_t at = 0;
           if (lane == 31 && incl) at = atomicAdd(&s.cand_n, incl);
@@ -760,7 +766,7 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
           if (mine) {
 #pragma unroll
             for (int m = 0; m < kPer; ++m)
-              if (kk[m] != 0u && bin_of(kk[m]) == tb) {
+              if (kk[m] != 0u && kk[m] >= kmin && bin_of(kk[m]) == tb) {
                 if (at < (uint32_t)kCandMax) s.cand[at] = kk[m] - kmin;
                 ++at;
               }
@@ -853,14 +859,21 @@ __device__ void select_small(const float* vals, int64_t n, int k, int64_t forced
     bool take = kk[m] > T || p0 + m == forced;
     if (!take && kk[m] == T && T != 0u) take = E++ < krem;
     if (take) {
-      if (off < (uint32_t)k)
-        out[off] = pmap ? blkr[m / kHsiBlock] * kHsiBlock + (int32_t)(m % kHsiBlock) : (int32_t)(p0 + m);
+      if (off < (uint32_t)k) {
+        const int32_t id = pmap ? blkr[m / kHsiBlock] * kHsiBlock + (int32_t)(m % kHsiBlock) : (int32_t)(p0 + m);
+        out[off] = id;
+        if (out_copy) out_copy[off] = id;
+      }
       ++off;
     }
   }
   const uint32_t all = s.wsum[kSelWarps];
   const uint32_t total = (all & 0xFFFFu) + min(krem, all >> 16);
-  for (uint32_t i = total + threadIdx.x; i < (uint32_t)k; i += kSelThreads) out[i] = -1;
+  for (uint32_t i = total + threadIdx.x; i < (uint32_t)k; i += kSelThreads) {
+    out[i] = -1;
+    if (out_copy) out_copy[i] = -1;
+  }
+  if (t_out && threadIdx.x == 0) *t_out = T;
 }
 
 // grid (cs, queries, selections), clusters of cs CTAs along x.  Selection 0:
@@ -922,12 +935,27 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
     // every block ranking above a block that holds a top-k entry e (block max
     // desc, block id asc) contains an entry ranking above e (score desc, id
     // asc), so at most k - 1 blocks rank above it.
+    // The pool also goes to shared memory (the second selection reads its
+    // block ids from there), and its threshold key bounds the second one from
+    // below: each of the pool's blocks but the forced one has its maximum at
+    // or above it, so at least k of the pool's positions do (n_blocks > k).
     const int64_t nb = (nv + kHsiBlock - 1) / kHsiBlock;
     int32_t* prow = pool_out + (int64_t)qi * n_blocks;
-    run(bmax + (int64_t)qc * ((max_entries + 7) / 8), nb, n_blocks, nb - 1, IdMap{nullptr}, prow);
-    __syncthreads();  // the pool ids are visible to the whole CTA
-    select_small(scores + (int64_t)qc * score_stride, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{prow},
-                 topk_out + (int64_t)qi * k, lo, hi, s, prow, nv);
+    const float* bm = bmax + (int64_t)qc * ((max_entries + 7) / 8);
+    __shared__ uint32_t t_pool;
+    if (kSmall || (cs == 1 && nb <= kRound)) {
+      int32_t* pool_s = reinterpret_cast<int32_t*>(s.keys);  // unused by the register-resident selection
+      select_small(bm, nb, n_blocks, nb - 1, IdMap{nullptr}, prow, lo, hi, s, nullptr, 0, pool_s, &t_pool);
+      __syncthreads();  // the pool ids and its threshold are visible to the whole CTA
+      const uint32_t lo2 = (t_pool != 0xFFFFFFFFu && t_pool > lo) ? t_pool : lo;
+      select_small(scores + (int64_t)qc * score_stride, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{prow},
+                   topk_out + (int64_t)qi * k, lo2, hi, s, pool_s, nv);
+    } else {
+      run(bm, nb, n_blocks, nb - 1, IdMap{nullptr}, prow);
+      __syncthreads();  // the pool ids are visible to the whole CTA
+      select_small(scores + (int64_t)qc * score_stride, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{prow},
+                   topk_out + (int64_t)qi * k, lo, hi, s, prow, nv);
+    }
   } else if (blockIdx.z == 0) {
     const float* v = scores + (int64_t)qc * score_stride;
     if (pool)

@@ -21,10 +21,14 @@
 //  - the epilogue reads D back (one row per thread), forms the ReLU-weighted
 //    head sums, writes the scores, the 8-entry block maxima for HSI and folds
 //    this CTA's key range per query (one slot each) for the top-k selection.
-// A warpgroup decodes its next tile while its previous MMA runs, and the
-// warpgroups interleave on the tensor core.  When the grid is one wave, the
-// producer warp prefetches its first ring pass into L2 while the previous
-// kernel (the compressor) still runs.  Every wait is bounded.
+// The epilogue of a warpgroup's previous tile runs while its next MMA
+// executes, and the warpgroups interleave on the tensor core.  Single-query
+// FP4 page scans (every decode Full layer) replace the producer warp by one
+// issuer warp per warpgroup, which copies that warpgroup's tiles and issues
+// its MMAs, and lay the queries' tiles end to end over one wave of CTAs
+// (one per SM).  When the grid is one wave, the first copying warp
+// prefetches its first ring pass into L2 while the previous kernel (the
+// compressor) still runs.  Every wait is bounded.
 #include <algorithm>
 
 #include "internal.h"

@@ -689,7 +689,7 @@ def _single_query_scan(fmt, seed, N, n_ent, q_pos, nb=1024, k=512):
     for b in range(B):
         codes, scales = synth.integer_fp4_bytes(g, N, CI)  # every scale 1.0
         oc.codes[b], oc.scales[b] = codes, scales[:, :oc.scales.shape[-1]]
-    pick = synth.rng(seed, "dup").integers(0, 3000, size=(B, N))
+    pick = synth.rng(seed, "dup").integers(0, min(3000, N), size=(B, N))
     for b in range(B):
         oc.codes[b], oc.scales[b] = oc.codes[b][pick[b]], oc.scales[b][pick[b]]
     pc = _paged.cache_pair(B, N, CI, "fp4" if fmt == "fp4" else "fp4g32", seed)
@@ -728,3 +728,17 @@ def test_single_query_scan_flattened_over_one_wave_exact(fmt):
     q_pos = [19999, 0, 19998, 299, 100, 12344, 19999, 128, 19999, 3, 6999, 19999,
              19999, 17999, 10000, 127, 19999, 19999, 19999, 4999, 19999, 18999, 19999, 640]
     _single_query_scan(fmt, 34, 20000, n_ent, q_pos)
+
+
+def test_single_query_scan_flattened_across_nearly_every_cta_exact():
+    """151 single queries of up to 700 entries (6 tiles each) over one wave
+    of 152 CTAs of about 6 tiles: nearly every CTA's range crosses from one
+    query into the next, and each query's key range is spread over two
+    slots.  A pool of 40 blocks with k = 32 takes the fused selection (the
+    pool, then the top-k among its positions, bounded below by the pool's
+    threshold key).  Short sequences and queries that see a few entries
+    only."""
+    B, N = 151, 700
+    n_ent = [N if b % 5 else 1 + (37 * b) % N for b in range(B)]
+    q_pos = [(n - 1) if b % 3 else (53 * b) % N for b, n in enumerate(n_ent)]
+    _single_query_scan("fp4", 35, N, n_ent, q_pos, nb=40, k=32)

@@ -730,7 +730,8 @@ def test_single_query_scan_flattened_over_one_wave_exact(fmt):
     _single_query_scan(fmt, 34, 20000, n_ent, q_pos)
 
 
-def test_single_query_scan_flattened_across_nearly_every_cta_exact():
+@pytest.mark.parametrize("fmt", ["fp4", "fp4g32"])
+def test_single_query_scan_flattened_across_nearly_every_cta_exact(fmt):
     """151 single queries of up to 700 entries (6 tiles each) over one wave
     of 152 CTAs of about 6 tiles: nearly every CTA's range crosses from one
     query into the next, and each query's key range is spread over two
@@ -741,4 +742,4 @@ def test_single_query_scan_flattened_across_nearly_every_cta_exact():
     B, N = 151, 700
     n_ent = [N if b % 5 else 1 + (37 * b) % N for b in range(B)]
     q_pos = [(n - 1) if b % 3 else (53 * b) % N for b, n in enumerate(n_ent)]
-    _single_query_scan("fp4", 35, N, n_ent, q_pos, nb=40, k=32)
+    _single_query_scan(fmt, 35, N, n_ent, q_pos, nb=40, k=32)

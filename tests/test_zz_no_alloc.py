@@ -117,3 +117,28 @@ def test_static_scratch_at_its_largest_accepted_size():
     rc = lib.csa2_index_topk_static(C.byref(cfg), B, 1, fake, None, fake, C.byref(d), fake, N + 1, None, fake, fake,
                                     None, None)
     assert rc == 4  # CSA2_ERR_CAPACITY
+
+
+def test_static_scratch_with_single_queries_laid_end_to_end():
+    """24 single queries of 20000 entries: the scorer lays their tiles end to
+    end over one wave (CTA ranges crossing from one query into the next) in
+    both entry points; the static one, whose array holds all 24 queries'
+    scratch, gives the workspace entry point's results."""
+    lib = csa.load()
+    lib.csa2_index_topk_static.restype = C.c_int32
+    cfg = csa.Cfg(ratio=1, topk=512, hsi_blocks=1024)
+    B, N = 24, 20000
+    assert csa.index_workspace_bytes(cfg, B, 1, N) <= lib.csa2_index_static_scratch_bytes()
+    pc, q_idx, q_pos, n_ent = _case(45, B, N, integer=True)
+    q_idx, q_pos = q_idx[:, :1].contiguous(), q_pos[:, :1].contiguous()
+    want_top = torch.full((B, 1, cfg.topk), -9, dtype=torch.int32, device="cuda")
+    want_pool = torch.full((B, 1, cfg.hsi_blocks), -9, dtype=torch.int32, device="cuda")
+    ws = torch.empty(csa.index_workspace_bytes(cfg, B, 1, N), dtype=torch.uint8, device="cuda")
+    csa.index_topk(cfg, q_idx, q_pos, pc, n_ent, N, want_top, ws, pool_out=want_pool)
+    got_top = torch.full_like(want_top, -5)
+    got_pool = torch.full_like(want_pool, -5)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = _static(cfg, q_idx, q_pos, pc, n_ent, N, got_top, got_pool, st)
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st.item()) == 0
+    assert torch.equal(got_top, want_top) and torch.equal(got_pool, want_pool)

@@ -103,6 +103,8 @@ __host__ __device__ inline int64_t flat_cta_of(int64_t x, int64_t total, int64_t
 
 using score::e2m1x8_to_f16x2;
 using score::e4m3_pair_bcast;
+using score::fadd2;
+using score::ffma2;
 using score::hmul2;
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) scor
   uint8_t* qtile = smem;                          // [kQS*32 rows][128] K-major: query slot j at j * 256 * 32
   uint8_t* ring = smem + 256 * 32 * kQS;          // kStages slots
   uint8_t* abuf = ring + kStages * TileFmt<kDtype>::kSlotBytes;  // kSmemA: one K tile per warpgroup
-  __shared__ float hw[kQS][kIdxHeads];
+  __shared__ float hw[kQS][kIdxHeads];  // half the head weights (see the epilogue)
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], mma_bar[kWG];
   __shared__ __align__(8) uint64_t a_full[kWG];  // kIss: warpgroup g has stored its A tile
   __shared__ uint32_t tmem_base;
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) scor
   }
   for (int i = tid; i < kQS * kIdxHeads; i += kConsumers)
     hw[i / kIdxHeads][i % kIdxHeads] =
-        (a.head_w && i / kIdxHeads < n_act) ? __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 1.0f;
+        (a.head_w && i / kIdxHeads < n_act) ? 0.5f * __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 0.5f;
   if (kGather) {
     for (int i = tid; i < n_my * 128; i += kConsumers) {
       const int64_t p = t_begin * 128 + i;  // pool position
@@ -511,18 +513,32 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) scor
       uint32_t d[32];
       tc::tmem_ld32(tc::taddr(tb, lane_base, dcol_of(e) + 32 * (flat ? 0 : q)), d);
       tc::tmem_wait_ld();
-      // four partial sums over heads h = 4i + j, added pairwise
-      float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // four partial sums over heads h = 4i + j (two f32x2 accumulators),
+      // added pairwise.  ReLU(x) is taken as (x + |x|) / 2, exactly: the
+      // sums run over x + |x| (an add with an absolute-value operand, on the
+      // FMA pipe like the packed adds, rather than a max on the ALU pipe) and
+      // the half comes with the weights or at the end, both exact scalings
+      // by two, so every partial sum is bit for bit the ReLU sum's.
+      float2 p01 = make_float2(0.0f, 0.0f), p23 = make_float2(0.0f, 0.0f);
+      auto relu2x = [&](int hh, int j) {  // 2 ReLU(x), exactly
+        const float x = __uint_as_float(d[hh + j]);
+        return x + fabsf(x);
+      };
       if (a.head_w) {
 #pragma unroll
-        for (int hh = 0; hh < kIdxHeads; ++hh)
-          ps[hh & 3] = fmaf(hw[q][hh], fmaxf(__uint_as_float(d[hh]), 0.0f), ps[hh & 3]);
+        for (int hh = 0; hh < kIdxHeads; hh += 4) {
+          p01 = ffma2(make_float2(hw[q][hh], hw[q][hh + 1]), make_float2(relu2x(hh, 0), relu2x(hh, 1)), p01);
+          p23 = ffma2(make_float2(hw[q][hh + 2], hw[q][hh + 3]), make_float2(relu2x(hh, 2), relu2x(hh, 3)), p23);
+        }
       } else {
 #pragma unroll
-        for (int hh = 0; hh < kIdxHeads; ++hh) ps[hh & 3] += fmaxf(__uint_as_float(d[hh]), 0.0f);
+        for (int hh = 0; hh < kIdxHeads; hh += 4) {
+          p01 = fadd2(p01, make_float2(relu2x(hh, 0), relu2x(hh, 1)));
+          p23 = fadd2(p23, make_float2(relu2x(hh, 2), relu2x(hh, 3)));
+        }
       }
-      float sc = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      sc += 0.0f;
+      float sc = (p01.x + p01.y) + (p23.x + p23.y);
+      sc = a.head_w ? sc + 0.0f : 0.5f * sc;
       const int qc = qc0 + q;
       const bool valid = kGather ? (gtab[ie * 128 + lt] >= 0) : (pos < nv[q]);
       if (!ok) sc = -INFINITY;

@@ -102,10 +102,8 @@ __host__ __device__ inline int64_t flat_cta_of(int64_t x, int64_t total, int64_t
 }
 
 using score::e2m1x8_to_f16x2;
-using score::e4m3_pair_bcast;
 using score::fadd2;
 using score::ffma2;
-using score::hmul2;
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
@@ -595,26 +593,32 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) scor
   };
   // the entry decoded into 64 registers of f16 pairs
   auto convert = [&](const Fp4Entry& e, uint32_t (&r)[64]) {
-    // the scales as broadcast f16x2: s2g[g] for 16-channel group g (or
-    // 32-channel group g with one scale per 32 channels)
-    uint32_t s2g[8];
-    e4m3_pair_bcast(e.sc.x, s2g[0], s2g[1]);
-    e4m3_pair_bcast(e.sc.x >> 16, s2g[2], s2g[3]);
+    // the scales, two per f16 pair as decoded (exact); each product takes
+    // its scale as the pair's low or high half, which the f16 multiply reads
+    // as an operand selection rather than a separate broadcast
+    uint32_t sraw[4];
+    sraw[0] = score::e4m3_pair(e.sc.x);
+    sraw[1] = score::e4m3_pair(e.sc.x >> 16);
     if (kDtype == CSA2_CACHE_FP4) {
-      e4m3_pair_bcast(e.sc.y, s2g[4], s2g[5]);
-      e4m3_pair_bcast(e.sc.y >> 16, s2g[6], s2g[7]);
+      sraw[2] = score::e4m3_pair(e.sc.y);
+      sraw[3] = score::e4m3_pair(e.sc.y >> 16);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {  // 32 channels -> 16 registers
       const uint32_t w4[4] = {e.cw[c].x, e.cw[c].y, e.cw[c].z, e.cw[c].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int gg = 2 * c + (q >> 1);  // 16-channel group of these 8 channels
-        const uint32_t s2 = kDtype == CSA2_CACHE_FP4 ? s2g[gg] : s2g[c];
+        // scale group of these 8 channels: 16-channel groups, or 32-channel ones
+        const int gg = kDtype == CSA2_CACHE_FP4 ? 2 * c + (q >> 1) : c;
+        const __half2 sp = *reinterpret_cast<const __half2*>(&sraw[gg >> 1]);
+        const __half2 s2 = (gg & 1) ? __high2half2(sp) : __low2half2(sp);
         uint32_t h4[4];
         e2m1x8_to_f16x2(w4[q], h4);
 #pragma unroll
-        for (int by = 0; by < 4; ++by) r[16 * c + q * 4 + by] = e.present ? hmul2(h4[by], s2) : 0u;
+        for (int by = 0; by < 4; ++by) {
+          const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&h4[by]), s2);  // exact
+          r[16 * c + q * 4 + by] = e.present ? *reinterpret_cast<const uint32_t*>(&prod) : 0u;
+        }
       }
     }
   };

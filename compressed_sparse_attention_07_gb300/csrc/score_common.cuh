@@ -10,6 +10,13 @@
 namespace csa2 {
 namespace score {
 
+// Two E4M3 scale bytes (low byte first) -> one f16 pair (exact).
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t two) {
+  uint32_t f;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f) : "h"((uint16_t)(two & 0xFFFFu)));
+  return f;
+}
+
 // Two E4M3 scale bytes (low byte first) -> each as a broadcast f16x2 (exact).
 __device__ __forceinline__ void e4m3_pair_bcast(uint32_t two, uint32_t& lo2, uint32_t& hi2) {
   uint32_t f;

@@ -497,12 +497,25 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) scor
   gather(0);
 
   int last_issued = -1, waited = -1;  // own tile counters
+  // each query slot's score and block-maximum rows, and its visible entries
+  constexpr bool kRows = kQS <= 2;
+  float* srow_q[kRows ? kQS : 1];
+  float* brow_q[kRows ? kQS : 1];
+  int nv32[kQS];
+#pragma unroll
+  for (int q = 0; q < kQS; ++q) {
+    nv32[q] = (int)nv[q];
+    if (kRows) {
+      srow_q[q] = a.scores + (int64_t)(qc0 + q) * a.stride;
+      brow_q[q] = a.bmax ? a.bmax + (int64_t)(qc0 + q) * ((a.max_entries + 7) / 8) : nullptr;
+    }
+  }
 
   // epilogue of own tile e (its MMA has completed): ReLU-weighted head sums,
   // scores, HSI block maxima, key ranges
   auto epilogue = [&](int e, bool ok) {
     const int ie = g + kWG * e;
-    const int64_t pos = tile_of(ie) * 128 + lt;  // entry id (page mode) / pool position (gather mode)
+    const int pos = (int)tile_of(ie) * 128 + lt;  // entry id (page mode) / pool position (gather mode)
     const int qs = tile_slot(ie);
 #pragma unroll
     for (int q = 0; q < kQS; ++q) {
@@ -538,12 +551,13 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) scor
       float sc = (p01.x + p01.y) + (p23.x + p23.y);
       sc = a.head_w ? sc + 0.0f : 0.5f * sc;
       const int qc = qc0 + q;
-      const bool valid = kGather ? (gtab[ie * 128 + lt] >= 0) : (pos < nv[q]);
+      const bool valid = kGather ? (gtab[ie * 128 + lt] >= 0) : (pos < nv32[q]);
       if (!ok) sc = -INFINITY;
+      float* srow = kRows ? srow_q[q] : a.scores + (int64_t)qc * a.stride;
       if (kGather) {
-        if (pos < npos) a.scores[(int64_t)qc * a.stride + pos] = valid ? sc : __uint_as_float(kScoreInvalid);
+        if (pos < npos) srow[pos] = valid ? sc : __uint_as_float(kScoreInvalid);
       } else if (valid) {
-        a.scores[(int64_t)qc * a.stride + pos] = sc;
+        srow[pos] = sc;
       }
       if (valid) {
         const uint32_t kk = order_key(sc);
@@ -555,7 +569,7 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) scor
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        if ((lt & 7) == 0 && valid) a.bmax[(int64_t)qc * ((a.max_entries + 7) / 8) + pos / 8] = m;
+        if ((lt & 7) == 0 && valid) (kRows ? brow_q[q] : a.bmax + (int64_t)qc * ((a.max_entries + 7) / 8))[pos >> 3] = m;
       }
     }
   };

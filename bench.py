@@ -67,7 +67,7 @@ MAIN_ENTRY_BYTES = {"fp4": 288, "bf16": 1024}
 # current kernels reports null.
 TRAFFIC = {
     "decode_b32_ctx131072_r1_fp4_hsi": {
-        "index_score": (302601472 + 18103552, "profiles/score_tc_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
+        "index_score": (302600704 + 17805056, "profiles/score_tc_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
         "index_select": (9110528, "profiles/select_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
         "attend": (12978944, "profiles/attend_qc_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
     },

@@ -675,10 +675,6 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
   const int nbits = range ? 32 - __clz(range) : 0;
   const int sh = nbits > 13 ? nbits - 13 : 0;
   const bool ranked = need > 0 && any;
-  auto bin_of = [&](uint32_t kk) -> uint32_t {
-    const uint32_t x = kk > kmin ? kk - kmin : 0u;
-    return min(x >> sh, (uint32_t)(kHistBins - 1));
-  };
   const int64_t p0 = (int64_t)kPer * threadIdx.x;
   float v[kPer];
   // the ids this thread may emit come from two 8-position pool blocks (a
@@ -735,16 +731,19 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
   }
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
   if (threadIdx.x == 0) s.cand_n = 0;
+  // this thread's positions as bits of 16-bit masks (bit m: position p0 + m)
+  const uint32_t fm = (has_forced && forced >= p0 && forced < p0 + kPer) ? 1u << (int)(forced - p0) : 0u;
   uint32_t kk[kPer];
 #pragma unroll
-  for (int m = 0; m < kPer; ++m) kk[m] = (p0 + m == forced) ? 0u : order_key(v[m]);
+  for (int m = 0; m < kPer; ++m) kk[m] = ((fm >> m) & 1u) ? 0u : order_key(v[m]);
   __syncthreads();
 
+  const uint32_t kmin1 = kmin > 0u ? kmin : 1u;  // candidates: keys >= kmin (key 0: none)
   uint32_t T = 0xFFFFFFFFu, krem = 0;  // select key > T, then the first krem keys == T
   if (ranked) {
 #pragma unroll
     for (int m = 0; m < kPer; ++m)
-      if (kk[m] && kk[m] >= kmin) atomicAdd(&s.hist[bin_of(kk[m])], 1u);
+      if (kk[m] >= kmin1) atomicAdd(&s.hist[min((kk[m] - kmin) >> sh, (uint32_t)(kHistBins - 1))], 1u);
     __syncthreads();
     find_cut(s.hist, kHistBins, need, s);
     if (s.cut_total <= need) {
@@ -756,17 +755,23 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
       krem = need - s.cut_above;
       if (rem > 0) {
         {  // this thread's keys of the cut bin, one shared-memory atomic per warp
-          uint32_t mine = 0;
+          // the bin's keys: kmin + [tb << sh, (tb + 1) << sh), the top bin open above
+          const uint32_t klo = kmin + (tb << sh);
+          const uint32_t span = (1u << sh) - 1u;
+          const uint32_t khi = (tb == (uint32_t)(kHistBins - 1) || klo > 0xFFFFFFFFu - span) ? 0xFFFFFFFFu : klo + span;
+          const uint32_t klo1 = klo > kmin1 ? klo : kmin1;
+          uint32_t cutm = 0;
 #pragma unroll
-          for (int m = 0; m < kPer; ++m) mine += kk[m] != 0u && kk[m] >= kmin && bin_of(kk[m]) == tb;
+          for (int m = 0; m < kPer; ++m) cutm |= (kk[m] >= klo1 && kk[m] <= khi) ? 1u << m : 0u;
+          const uint32_t mine = __popc(cutm);
           const uint32_t incl = warp_incl_scan(mine);
           uint32_t at = 0;
           if (lane == 31 && incl) at = atomicAdd(&s.cand_n, incl);
           at = __shfl_sync(0xffffffffu, at, 31) + incl - mine;
-          if (mine) {
+          if (cutm) {
 #pragma unroll
             for (int m = 0; m < kPer; ++m)
-              if (kk[m] != 0u && kk[m] >= kmin && bin_of(kk[m]) == tb) {
+              if ((cutm >> m) & 1u) {
                 if (at < (uint32_t)kCandMax) s.cand[at] = kk[m] - kmin;
                 ++at;
               }
@@ -834,13 +839,13 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
   }
 
   // ---- ordered compaction
-  uint32_t gt = 0, eq = 0;
+  uint32_t gtm = fm, eqm = 0;  // keys above T (and the forced position); keys equal to T
 #pragma unroll
   for (int m = 0; m < kPer; ++m) {
-    gt += kk[m] > T || p0 + m == forced;
-    eq += kk[m] == T && T != 0u;
+    gtm |= kk[m] > T ? 1u << m : 0u;
+    eqm |= (kk[m] == T && T != 0u) ? 1u << m : 0u;
   }
-  const uint32_t vpk = gt | (eq << 16);
+  const uint32_t vpk = __popc(gtm) | (__popc(eqm) << 16);
   const uint32_t incl = warp_incl_scan(vpk);
   if (lane == 31) s.wsum[wid] = incl;
   __syncthreads();
@@ -852,20 +857,26 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
   }
   __syncthreads();
   const uint32_t before = s.wsum[wid] + incl - vpk;
-  uint32_t E = before >> 16;
+  const uint32_t E = before >> 16;
   uint32_t off = (before & 0xFFFFu) + min(krem, E);
-#pragma unroll
-  for (int m = 0; m < kPer; ++m) {
-    bool take = kk[m] > T || p0 + m == forced;
-    if (!take && kk[m] == T && T != 0u) take = E++ < krem;
-    if (take) {
-      if (off < (uint32_t)k) {
-        const int32_t id = pmap ? blkr[m / kHsiBlock] * kHsiBlock + (int32_t)(m % kHsiBlock) : (int32_t)(p0 + m);
-        out[off] = id;
-        if (out_copy) out_copy[off] = id;
-      }
-      ++off;
+  // taken: every key above T, and the first krem - E of this thread's keys
+  // equal to T (by position); written in position order
+  uint32_t takem = gtm;
+  for (uint32_t em = eqm, left = krem > E ? krem - E : 0u; em && left; --left) {
+    takem |= em & (0u - em);
+    em &= em - 1u;
+  }
+  static_assert(kPer == 2 * kHsiBlock, "a thread's positions span two pool blocks");
+  while (takem) {
+    const int m = __ffs(takem) - 1;
+    takem &= takem - 1u;
+    if (off < (uint32_t)k) {
+      const int32_t id = pmap ? (m >= kHsiBlock ? blkr[1] : blkr[0]) * kHsiBlock + (m & (kHsiBlock - 1))
+                              : (int32_t)(p0 + m);
+      out[off] = id;
+      if (out_copy) out_copy[off] = id;
     }
+    ++off;
   }
   const uint32_t all = s.wsum[kSelWarps];
   const uint32_t total = (all & 0xFFFFu) + min(krem, all >> 16);

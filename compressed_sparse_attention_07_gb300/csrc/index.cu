@@ -780,28 +780,28 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
         __syncthreads();
         const uint32_t c = s.cand_n;
         if (c <= (uint32_t)kRankMax) {
-          // rank of each candidate among the threshold-bin keys (tpc threads each)
-          const uint32_t tpc = max(1u, (uint32_t)kSelThreads / c);
-          for (uint32_t i = threadIdx.x; i < c; i += kSelThreads) s.part[i] = 0;
-          __syncthreads();
-          if (threadIdx.x < c * tpc) {
-            const uint32_t i = threadIdx.x % c, part = threadIdx.x / c;
-            const uint32_t x = s.cand[i];
-            uint32_t gt = 0, eq = 0;
-            for (uint32_t j = part; j < c; j += tpc) {
+          // rank of each candidate among the threshold-bin keys: 2^lg adjacent
+          // lanes per candidate (one while there are fewer than 32, at most 8),
+          // their counts summed by shuffles
+          int lg = 0;
+          while ((c << (lg + 1)) <= (uint32_t)kSelThreads && (2u << lg) <= c / 16u) ++lg;
+          const uint32_t i = threadIdx.x >> lg, part = threadIdx.x & ((1u << lg) - 1u);
+          uint32_t gt = 0, eq = 0, x = 0;
+          if (i < c) {
+            x = s.cand[i];
+            for (uint32_t j = part; j < c; j += 1u << lg) {
               const uint32_t y = s.cand[j];
               gt += y > x;
               eq += y == x;
             }
-            atomicAdd(&s.part[i], gt | (eq << 16));
           }
-          __syncthreads();
-          for (uint32_t i = threadIdx.x; i < c; i += kSelThreads) {
-            const uint32_t gt = s.part[i] & 0xFFFFu, eq = s.part[i] >> 16;
-            if (gt < krem && krem <= gt + eq) {  // the same key and counts for every such i
-              s.t_x = s.cand[i];
-              s.t_krem = krem - gt;
-            }
+          for (int o = 1; o < (1 << lg); o <<= 1) {
+            gt += __shfl_xor_sync(0xffffffffu, gt, o);
+            eq += __shfl_xor_sync(0xffffffffu, eq, o);
+          }
+          if (i < c && part == 0 && gt < krem && krem <= gt + eq) {  // the same key and counts for every such i
+            s.t_x = x;
+            s.t_krem = krem - gt;
           }
           __syncthreads();
           prefix = s.t_x;

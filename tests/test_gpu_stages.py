@@ -235,13 +235,16 @@ def test_select_threshold_bin_beyond_shared_list_and_single_slots(N):
 
 
 @pytest.mark.parametrize("nb", [65, 128])
-def test_full_topk_through_the_hsi_pool_is_exact(nb):
+@pytest.mark.parametrize("N", [6000, 6003])
+def test_full_topk_through_the_hsi_pool_is_exact(nb, N):
     """With HSI and at least k + 1 pool blocks the selection takes the pool
     first and the top-k among the pool's positions; on integer scores with
     many ties (duplicated rows) both must equal the oracle's top-k over all
     visible entries and its pool, bit for bit, including a pool of exactly
-    k + 1 blocks."""
-    B, N, k = 3, 6000, 64
+    k + 1 blocks.  With 6003 entries per row most queries' score and
+    block-maximum rows start off a 16-byte boundary (read without vector
+    loads)."""
+    B, k = 3, 64
     oc, pc = _idx_caches(B, N, "fp4", seed=27, integer=True, dup=True)
     q_idx = synth.integer_bf16(synth.rng(27, "q"), (B, 2, H, CI), -1, 1)
     q_pos = np.array([[5999, 3001], [5999, 5999], [777, 5999]], np.int64)

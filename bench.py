@@ -68,8 +68,8 @@ MAIN_ENTRY_BYTES = {"fp4": 288, "bf16": 1024}
 TRAFFIC = {
     "decode_b32_ctx131072_r1_fp4_hsi": {
         "index_score": (302600704 + 17805056, "profiles/score_tc_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
-        "index_select": (9110528, "profiles/select_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
-        "attend": (12978944, "profiles/attend_qc_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
+        "index_select": (9095936, "profiles/select_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
+        "attend": (12979456, "profiles/attend_qc_kernel_decode_b32_ctx131072_r1_fp4_hsi.md"),
     },
 }
 

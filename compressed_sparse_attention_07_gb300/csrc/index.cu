@@ -650,11 +650,11 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
   }
 }
 
-// The same selection for a single CTA holding all n <= kRound positions
+// The same selection for a single CTA holding all n <= kSelThreads * kP positions
 // (one copy of its code shared by every call site: when the code is not
 // cached its instructions are fetched once, which was measured faster than
 // inlining it into each caller):
-// thread t owns positions kPer t .. kPer t + kPer - 1 and keeps their keys in registers
+// thread t owns positions kP t .. kP t + kP - 1 (kP = 16 or 32) and keeps their keys in registers
 // from the one read of the scores to the ordered write of the ids
 // (histogram, cut search, threshold-bin keys ranked or refined by digits,
 // then one scan of packed (above, equal) counts).
@@ -664,6 +664,7 @@ __device__ void select_topk(const float* vals, int64_t n, int k, int64_t forced,
 // knows at least k keys lie at or above it).  out_copy: the ids also written
 // there (shared memory); t_out: the threshold key (every selected key but the
 // forced one is at or above it).
+template <int kP>
 __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, int64_t forced, IdMap idmap, int32_t* out,
                              uint32_t kmin, uint32_t kmax, SelShared& s, const int32_t* gpool = nullptr,
                              int64_t nv_lim = 0, int32_t* out_copy = nullptr, uint32_t* t_out = nullptr) {
@@ -675,22 +676,22 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
   const int nbits = range ? 32 - __clz(range) : 0;
   const int sh = nbits > 13 ? nbits - 13 : 0;
   const bool ranked = need > 0 && any;
-  const int64_t p0 = (int64_t)kPer * threadIdx.x;
-  float v[kPer];
+  const int64_t p0 = (int64_t)kP * threadIdx.x;
+  float v[kP];
   // the ids this thread may emit come from two 8-position pool blocks (a
   // pool-mapped selection): their block ids are kept in registers, so the
   // ordered writes below need no dependent load per selected position
   const int32_t* pmap = gpool ? gpool : idmap.pool;
-  int32_t blkr[kPer / kHsiBlock];
+  int32_t blkr[kP / kHsiBlock];
 #pragma unroll
-  for (int h = 0; h < kPer / kHsiBlock; ++h) {
+  for (int h = 0; h < kP / kHsiBlock; ++h) {
     const int64_t pb = (p0 >> 3) + h;
     blkr[h] = (pmap && pb * kHsiBlock < n) ? *reinterpret_cast<const volatile int32_t*>(pmap + pb) : -1;
   }
   if (gpool) {
     const bool al = ((uintptr_t)vals & 15u) == 0;
 #pragma unroll
-    for (int h = 0; h < kPer / kHsiBlock; ++h) {
+    for (int h = 0; h < kP / kHsiBlock; ++h) {
       const int32_t blk = blkr[h];  // pool slot's block (written by this CTA just before)
       const int64_t j0 = (int64_t)blk * kHsiBlock;
       if (blk >= 0 && al && j0 + kHsiBlock <= nv_lim) {  // a whole visible block: two 16-byte loads
@@ -713,9 +714,9 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
         }
       }
     }
-  } else if (((uintptr_t)vals & 15u) == 0 && p0 + kPer <= n) {
+  } else if (((uintptr_t)vals & 15u) == 0 && p0 + kP <= n) {
 #pragma unroll
-    for (int q = 0; q < kPer / 4; ++q) {
+    for (int q = 0; q < kP / 4; ++q) {
       float4 f4;
       asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
                    : "=f"(f4.x), "=f"(f4.y), "=f"(f4.z), "=f"(f4.w)
@@ -727,22 +728,22 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
     }
   } else {
 #pragma unroll
-    for (int m = 0; m < kPer; ++m) v[m] = p0 + m < n ? ld_score(vals + p0 + m) : __uint_as_float(kScoreInvalid);
+    for (int m = 0; m < kP; ++m) v[m] = p0 + m < n ? ld_score(vals + p0 + m) : __uint_as_float(kScoreInvalid);
   }
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
   if (threadIdx.x == 0) s.cand_n = 0;
   // this thread's positions as bits of 16-bit masks (bit m: position p0 + m)
-  const uint32_t fm = (has_forced && forced >= p0 && forced < p0 + kPer) ? 1u << (int)(forced - p0) : 0u;
-  uint32_t kk[kPer];
+  const uint32_t fm = (has_forced && forced >= p0 && forced < p0 + kP) ? 1u << (int)(forced - p0) : 0u;
+  uint32_t kk[kP];
 #pragma unroll
-  for (int m = 0; m < kPer; ++m) kk[m] = ((fm >> m) & 1u) ? 0u : order_key(v[m]);
+  for (int m = 0; m < kP; ++m) kk[m] = ((fm >> m) & 1u) ? 0u : order_key(v[m]);
   __syncthreads();
 
   const uint32_t kmin1 = kmin > 0u ? kmin : 1u;  // candidates: keys >= kmin (key 0: none)
   uint32_t T = 0xFFFFFFFFu, krem = 0;  // select key > T, then the first krem keys == T
   if (ranked) {
 #pragma unroll
-    for (int m = 0; m < kPer; ++m)
+    for (int m = 0; m < kP; ++m)
       if (kk[m] >= kmin1) atomicAdd(&s.hist[min((kk[m] - kmin) >> sh, (uint32_t)(kHistBins - 1))], 1u);
     __syncthreads();
     find_cut(s.hist, kHistBins, need, s);
@@ -762,7 +763,7 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
           const uint32_t klo1 = klo > kmin1 ? klo : kmin1;
           uint32_t cutm = 0;
 #pragma unroll
-          for (int m = 0; m < kPer; ++m) cutm |= (kk[m] >= klo1 && kk[m] <= khi) ? 1u << m : 0u;
+          for (int m = 0; m < kP; ++m) cutm |= (kk[m] >= klo1 && kk[m] <= khi) ? 1u << m : 0u;
           const uint32_t mine = __popc(cutm);
           const uint32_t incl = warp_incl_scan(mine);
           uint32_t at = 0;
@@ -770,7 +771,7 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
           at = __shfl_sync(0xffffffffu, at, 31) + incl - mine;
           if (cutm) {
 #pragma unroll
-            for (int m = 0; m < kPer; ++m)
+            for (int m = 0; m < kP; ++m)
               if ((cutm >> m) & 1u) {
                 if (at < (uint32_t)kCandMax) s.cand[at] = kk[m] - kmin;
                 ++at;
@@ -822,7 +823,7 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
             }
           } else {
 #pragma unroll
-            for (int m = 0; m < kPer; ++m) {
+            for (int m = 0; m < kP; ++m) {
               const uint32_t x = kk[m] - kmin;
               if (kk[m] != 0u && kk[m] >= kmin && (x >> rem) == prefix) atomicAdd(&s.hist[(x >> s2) & dmask], 1u);
             }
@@ -841,7 +842,7 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
   // ---- ordered compaction
   uint32_t gtm = fm, eqm = 0;  // keys above T (and the forced position); keys equal to T
 #pragma unroll
-  for (int m = 0; m < kPer; ++m) {
+  for (int m = 0; m < kP; ++m) {
     gtm |= kk[m] > T ? 1u << m : 0u;
     eqm |= (kk[m] == T && T != 0u) ? 1u << m : 0u;
   }
@@ -866,13 +867,15 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
     takem |= em & (0u - em);
     em &= em - 1u;
   }
-  static_assert(kPer == 2 * kHsiBlock, "a thread's positions span two pool blocks");
+  static_assert(kP <= 32 && kP % kHsiBlock == 0, "a thread's positions: bits of one mask, whole pool blocks");
   while (takem) {
     const int m = __ffs(takem) - 1;
     takem &= takem - 1u;
     if (off < (uint32_t)k) {
-      const int32_t id = pmap ? (m >= kHsiBlock ? blkr[1] : blkr[0]) * kHsiBlock + (m & (kHsiBlock - 1))
-                              : (int32_t)(p0 + m);
+      int32_t blk = blkr[0];
+#pragma unroll
+      for (int h = 1; h < kP / kHsiBlock; ++h) blk = (m >> 3) == h ? blkr[h] : blk;
+      const int32_t id = pmap ? blk * kHsiBlock + (m & (kHsiBlock - 1)) : (int32_t)(p0 + m);
       out[off] = id;
       if (out_copy) out_copy[off] = id;
     }
@@ -933,9 +936,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
   const uint32_t lo = r_lo, hi = r_hi;
   auto run = [&](const float* v, int64_t n, int kk, int64_t forced, IdMap idmap, int32_t* o) {
     if (kSmall)
-      select_small(v, n, kk, forced, idmap, o, lo, hi, s);
+      select_small<kPer>(v, n, kk, forced, idmap, o, lo, hi, s);
     else if (cs == 1 && n <= kRound)
-      select_small(v, n, kk, forced, idmap, o, lo, hi, s);
+      select_small<kPer>(v, n, kk, forced, idmap, o, lo, hi, s);
+    else if (cs == 1 && n <= 2 * kRound)
+      select_small<2 * kPer>(v, n, kk, forced, idmap, o, lo, hi, s);
     else
       cs == 1 ? select_topk<true>(v, n, kk, forced, idmap, o, lo, hi, s, cs, rk)
               : select_topk<false>(v, n, kk, forced, idmap, o, lo, hi, s, cs, rk);
@@ -954,18 +959,24 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
     int32_t* prow = pool_out + (int64_t)qi * n_blocks;
     const float* bm = bmax + (int64_t)qc * ((max_entries + 7) / 8);
     __shared__ uint32_t t_pool;
-    if (kSmall || (cs == 1 && nb <= kRound)) {
+    if (kSmall || (cs == 1 && nb <= 2 * kRound)) {
+      // the pool over up to 2 kRound blocks held in registers (16 or 32 keys
+      // a thread), then the top-k over its positions
       int32_t* pool_s = reinterpret_cast<int32_t*>(s.keys);  // unused by the register-resident selection
-      select_small(bm, nb, n_blocks, nb - 1, IdMap{nullptr}, prow, lo, hi, s, nullptr, 0, pool_s, &t_pool);
+      if (!kSmall && nb > kRound)
+        select_small<2 * kPer>(bm, nb, n_blocks, nb - 1, IdMap{nullptr}, prow, lo, hi, s, nullptr, 0, pool_s,
+                               &t_pool);
+      else
+        select_small<kPer>(bm, nb, n_blocks, nb - 1, IdMap{nullptr}, prow, lo, hi, s, nullptr, 0, pool_s, &t_pool);
       __syncthreads();  // the pool ids and its threshold are visible to the whole CTA
       const uint32_t lo2 = (t_pool != 0xFFFFFFFFu && t_pool > lo) ? t_pool : lo;
-      select_small(scores + (int64_t)qc * score_stride, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{prow},
-                   topk_out + (int64_t)qi * k, lo2, hi, s, pool_s, nv);
+      select_small<kPer>(scores + (int64_t)qc * score_stride, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{prow},
+                         topk_out + (int64_t)qi * k, lo2, hi, s, pool_s, nv);
     } else {
       run(bm, nb, n_blocks, nb - 1, IdMap{nullptr}, prow);
       __syncthreads();  // the pool ids are visible to the whole CTA
-      select_small(scores + (int64_t)qc * score_stride, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{prow},
-                   topk_out + (int64_t)qi * k, lo, hi, s, prow, nv);
+      select_small<kPer>(scores + (int64_t)qc * score_stride, (int64_t)n_blocks * kHsiBlock, k, -1, IdMap{prow},
+                         topk_out + (int64_t)qi * k, lo, hi, s, prow, nv);
     }
   } else if (blockIdx.z == 0) {
     const float* v = scores + (int64_t)qc * score_stride;

@@ -256,6 +256,25 @@ def test_full_topk_through_the_hsi_pool_is_exact(nb, N):
     np.testing.assert_array_equal(g_pool, o_pool)
 
 
+@pytest.mark.parametrize("dup", [True, False])
+def test_full_topk_through_a_pool_over_more_blocks_than_one_round(dup):
+    """The HSI pool chosen among 16385..32768 blocks (more than 16 keys a
+    thread hold): the pool selection holds 32 keys a thread in registers,
+    then the top-k among the pool's positions; integer scores (with 40
+    distinct entries repeated, or not), bit for bit against the oracle's
+    pool and top-k."""
+    B, N, k, nb = 2, 262000, 64, 128
+    oc, pc = _idx_caches(B, N, "fp4", seed=29, integer=True, dup=dup)
+    q_idx = synth.integer_bf16(synth.rng(29, "q"), (B, 1, H, CI), -1, 1)
+    q_pos = np.array([[261999], [140000]], np.int64)  # 32750 and 17501 blocks visible
+    n_ent = np.array([262000, 200000], np.int32)
+    cfg = csa.Cfg(ratio=1, topk=k, hsi_blocks=nb)
+    g_top, g_pool = _run_index(cfg, pc, q_idx, q_pos, n_ent, N, want_pool=True)
+    o_top, o_pool, _ = oracle.index_topk(oc, n_ent, q_idx, q_pos, r=1, k=k, hsi_blocks=nb, want_pool=True)
+    np.testing.assert_array_equal(g_pool, o_pool)
+    np.testing.assert_array_equal(g_top, o_top)
+
+
 def test_reindex_over_pool_matches_oracle():
     B, N, k, nb = 2, 4000, 64, 40
     oc, pc = _idx_caches(B, N, "fp4", seed=23, integer=True, dup=True)
@@ -524,10 +543,9 @@ def test_index_maximum_topk_and_hsi_blocks_bit_exact():
 @pytest.mark.parametrize("integer,k", [(True, 512), (False, 512), (True, 1024), (False, 97)])
 def test_select_many_queries_over_long_caches(integer, k):
     """96 causal queries over 20000 entries: one CTA per selection holding
-    more positions than its registers (the staged path), whose threshold bin
-    is listed with the positions so the selection is sorted out of shared
-    memory; integer inputs with repeated entries make ties straddle the
-    threshold for some queries (then the compaction pass orders them)."""
+    twice the positions of the 16-keys-a-thread selection, 32 keys in each
+    thread's registers; integer inputs with repeated entries make ties
+    straddle the threshold for some queries."""
     B, N, Tq = 1, 20000, 96
     oc, pc = _idx_caches(B, N, "fp4", seed=73 + k, integer=integer, dup=integer)
     g = synth.rng(73, "q%d" % k)

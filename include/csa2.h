@@ -14,6 +14,15 @@
  *  - All pointers are DEVICE pointers unless stated, owned by the caller; the
  *    library allocates nothing and never synchronises.  Calls are enqueued on
  *    `stream` (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *  - Every kernel is launched as a programmatic dependent launch: it may
+ *    start while the kernel enqueued just before it on the stream finishes.
+ *    Each kernel of this library waits for that kernel's completion (and
+ *    the visibility of its writes) before reading any argument, with one
+ *    exception, named at csa2_attend and csa2_layer: the decode attention
+ *    reads q, the window rows and their positions before that wait.
+ *    Because every kernel of this library waits before it lets its own
+ *    successor start, placing any call of this library between the kernel
+ *    that writes those inputs and the attention satisfies the rule.
  *  - bf16 tensors are passed as uint16_t bit patterns, row-major.
  *  - The return value reports argument errors found on the host before any
  *    launch (CSA2_ERR_INVALID_ARG / CSA2_ERR_UNSUPPORTED / CSA2_ERR_CAPACITY)
@@ -221,7 +230,14 @@ CSA2_API int32_t csa2_index_select(const csa2_cfg* cfg, int32_t B, int32_t Tq, c
  * q [B][Tq][64][512] bf16; topk [B][Tq][topk]; swa [B][S][512] bf16, or
  * [B][S] MXFP8 rows of 528 B with CSA2_FMT_SWA_FP8 (16-byte aligned; only
  * for topk + window <= 768, else CSA2_ERR_UNSUPPORTED);
- * out [B][Tq][64][512] fp32; lse [B][Tq][64] fp32 natural log, or NULL. */
+ * out [B][Tq][64][512] fp32; lse [B][Tq][64] fp32 natural log, or NULL.
+ * Read before the wait on the previous kernel (so that the loads overlap a
+ * preceding selection): q, swa, swa_len, swa_pos0 and q_pos.  They must not
+ * be written by the kernel enqueued immediately before this call on the
+ * stream; of this library's calls only csa2_swa_encode writes any of them,
+ * so enqueue another call (the indexer of a decode step) between the two.
+ * topk, n_entries and the main cache are read after that kernel has
+ * completed. */
 CSA2_API int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* q,
                     const csa2_cache* main_cache, const int32_t* n_entries, const int32_t* topk,
                     const void* swa, int32_t S, const int32_t* swa_len, const int64_t* swa_pos0,
@@ -235,7 +251,9 @@ CSA2_API int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const u
  * 2^-127 .. 2^127; an all-zero block takes 2^-127); element = the E4M3 value
  * nearest to x / scale, ties to even, saturating at 448, +0 for values that
  * round to zero.  row0 [B] int64 (device); a sequence whose rows would fall
- * outside [0, S) is skipped and CSA2_ERR_BAD_INDEX written to *status. */
+ * outside [0, S) is skipped and CSA2_ERR_BAD_INDEX written to *status.
+ * A csa2_attend that reads these rows must not be the next call enqueued
+ * on the stream (it reads window rows before waiting for its predecessor). */
 CSA2_API int32_t csa2_swa_encode(int32_t B, int32_t T, const uint16_t* x, const int64_t* row0, void* rows,
                                  int32_t S, int32_t* status, void* stream);
 
@@ -315,7 +333,10 @@ typedef struct csa2_layer_io {
  *          (and the HSI pool when cfg->hsi_blocks > 0), attend;
  *  REINDEX index only the pool's entries with this layer's q_idx, publish
  *          top-k, attend (no cache writes);
- *  REUSE   attend with the latest published top-k (no indexer, no writes). */
+ *  REUSE   attend with the latest published top-k (no indexer, no writes).
+ * The attention reads io's query and window arrays before it waits for the
+ * kernel enqueued just before it (see csa2_attend): in REUSE mode that is
+ * the kernel enqueued before this call, which therefore must not write them. */
 CSA2_API int32_t csa2_layer(const csa2_cfg* cfg, int32_t mode, csa2_group_state* state,
                    const csa2_layer_io* io, void* stream);
 

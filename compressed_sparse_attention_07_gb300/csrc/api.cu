@@ -249,7 +249,7 @@ int32_t csa2_attend(const csa2_cfg* cfg, int32_t B, int32_t Tq, const uint16_t* 
                                   out, lse, status, &empty);
   if (rc != CSA2_OK || empty) return rc;
   return cuda_status(launch_attend(*cfg, B, Tq, q, *main_cache, n_entries, topk, swa, S, swa_len, swa_pos0, q_pos,
-                                   scale, out, lse, status, static_cast<cudaStream_t>(stream)));
+                                   scale, out, lse, status, false, static_cast<cudaStream_t>(stream)));
 }
 
 int32_t csa2_gather_dequant(const csa2_cache* cache, int32_t cache_dtype, int32_t B, int32_t n, const int32_t* ids,
@@ -317,9 +317,11 @@ int32_t csa2_layer(const csa2_cfg* cfg, int32_t mode, csa2_group_state* st, cons
     if (rc) return rc;
   }
   if (e_att) return CSA2_OK;
+  // a Reuse layer's attention gathers its rows before it waits for the
+  // kernel enqueued just before it (that kernel writes no top-k or cache)
   return cuda_status(launch_attend(*cfg, io->B, io->Tq, io->q, st->main_cache, st->n_entries, st->topk, io->swa,
                                    io->S, io->swa_len, io->swa_pos0, io->q_pos, io->scale, io->out, io->lse,
-                                   st->status, s));
+                                   st->status, mode == CSA2_MODE_REUSE, s));
 }
 
 }  // extern "C"

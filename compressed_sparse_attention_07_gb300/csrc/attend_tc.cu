@@ -70,6 +70,10 @@ struct AttArgs {
   float* out;
   float* lse;
   int32_t* status;
+  // the query-cluster kernel may read topk, n_entries and the main cache
+  // before it waits for the previous kernel (a Reuse layer: the kernel
+  // enqueued just before wrote none of them)
+  int early;
 };
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
@@ -1320,11 +1324,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
     store_group(g1, s1, w1, false);
   }
 
-  griddep_wait();  // the selected ids are the previous kernel's output
-  griddep_launch();
-  if (warp == 0) {
-    tc::tmem_alloc(&tmem_base, 512);
-    tc::tmem_relinquish();
+  const bool early = a.early != 0;
+  if (!early) {
+    griddep_wait();  // the selected ids are the previous kernel's output
+    griddep_launch();
+    if (warp == 0) {
+      tc::tmem_alloc(&tmem_base, 512);
+      tc::tmem_relinquish();
+    }
   }
   // ---------------- the selected entries
   if (!win0) s0 = slot_source(a, qi, b, slot_of(8 * g0 + rl));
@@ -1342,6 +1349,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_qc_kernel(AttArgs a) {
     if (has1 && !win1) {
       load_group(s1, w1);
       store_group(g1, s1, w1, true);
+    }
+  }
+  if (early) {  // the rows are gathered: now the previous kernel's completion
+    griddep_wait();
+    griddep_launch();
+    if (warp == 0) {
+      tc::tmem_alloc(&tmem_base, 512);
+      tc::tmem_relinquish();
     }
   }
   tc::fence_async_smem();
@@ -1654,14 +1669,15 @@ bool attend_tc_supported(int topk, int window) {
 cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q, const csa2_cache& main_c,
                           const int32_t* n_entries, const int32_t* topk, const void* swa, int S,
                           const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos,
-                          float scale, float* out, float* lse, int32_t* status, cudaStream_t stream) {
+                          float scale, float* out, float* lse, int32_t* status, bool ids_early,
+                          cudaStream_t stream) {
   const int Q = B * Tq;
   if (Q == 0) return cudaSuccess;
   const bool fp8 = (cfg.formats & CSA2_FMT_SWA_FP8) != 0;
   AttArgs a{Tq, cfg.topk, cfg.window, S, (cfg.topk + 127) / 128, (cfg.window + 127) / 128, q, view_of(main_c),
             n_entries, (int64_t)main_c.max_pages * kPage, topk,
             fp8 ? nullptr : static_cast<const uint16_t*>(swa), fp8 ? static_cast<const uint8_t*>(swa) : nullptr,
-            swa_len, swa_pos0, q_pos, scale, out, lse, status};
+            swa_len, swa_pos0, q_pos, scale, out, lse, status, ids_early ? 1 : 0};
   // up to six row tiles: one CTA per (query, tile) for every head, the
   // query's tiles in one cluster; more: split by head groups (bf16 window
   // rows only)

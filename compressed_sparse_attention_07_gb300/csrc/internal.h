@@ -108,7 +108,7 @@ cudaError_t launch_index_select(const csa2_cfg& cfg, int B, int Tq, const int64_
 cudaError_t launch_attend(const csa2_cfg& cfg, int B, int Tq, const uint16_t* q, const csa2_cache& main_c,
                           const int32_t* n_entries, const int32_t* topk, const void* swa, int S,
                           const int32_t* swa_len, const int64_t* swa_pos0, const int64_t* q_pos,
-                          float scale, float* out, float* lse, int32_t* status, cudaStream_t stream);
+                          float scale, float* out, float* lse, int32_t* status, bool ids_early, cudaStream_t stream);
 
 // Whether the attention kernel fits top-k + window rows (TMEM and shared memory).
 bool attend_tc_supported(int topk, int window);

@@ -335,8 +335,12 @@ typedef struct csa2_layer_io {
  *          top-k, attend (no cache writes);
  *  REUSE   attend with the latest published top-k (no indexer, no writes).
  * The attention reads io's query and window arrays before it waits for the
- * kernel enqueued just before it (see csa2_attend): in REUSE mode that is
- * the kernel enqueued before this call, which therefore must not write them. */
+ * kernel enqueued just before it (see csa2_attend); in REUSE mode it also
+ * gathers its rows before that wait, reading the published top-k,
+ * state->n_entries and the main cache.  In REUSE mode that kernel is the one
+ * enqueued before this call, which therefore must write none of these (a
+ * preceding csa2_layer call of the group writes none of them with its last
+ * kernel). */
 CSA2_API int32_t csa2_layer(const csa2_cfg* cfg, int32_t mode, csa2_group_state* state,
                    const csa2_layer_io* io, void* stream);
 

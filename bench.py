@@ -74,6 +74,13 @@ TRAFFIC = {
 }
 
 
+def attend_kernel(topk, window):
+    """The decode attention kernel the library launches for this many row
+    tiles of 128 (a query cluster of 4-5 CTAs, else one CTA per tile)."""
+    tiles = (topk + 127) // 128 + (window + 127) // 128
+    return "attend_qc_kernel" if tiles in (4, 5) else "attend_rows_kernel" if tiles <= 6 else "attend_split_kernel"
+
+
 def attend_query_bytes(cache, topk=512, window=128, row_bytes=1024):
     """Top-k entries + window rows (bf16 1024 B, MXFP8 528 B) + bf16 Q + fp32 out + ids."""
     return topk * MAIN_ENTRY_BYTES[cache] + window * row_bytes + 64 * 512 * 2 + 64 * 512 * 4 + topk * 4
@@ -275,7 +282,7 @@ class DecodeStep(StepBase):
                             "index_select": B * select_bytes(self.N, wl),
                             "attend": B * attend_query_bytes(wl.cache, wl.topk, wl.window, swa_row_bytes(wl))}
         self.stage_kernels = {"compress": "compress_kernel", "index_score": "score_tc_kernel",
-                              "index_select": "select_kernel", "attend": "attend_rows_kernel"}
+                              "index_select": "select_kernel", "attend": attend_kernel(wl.topk, wl.window)}
         if wl.swa_fp8:
             self.stages.insert(1, "swa_encode")
             self.launches_per_step += 1
@@ -349,7 +356,7 @@ class PrefillStep(StepBase):
                             "attend": B * Tq * attend_query_bytes(wl.cache, wl.topk, wl.window)}
         self.stage_flops = {"index_score": pairs * 8192, "attend": B * Tq * 4 * 64 * 512 * (wl.topk + wl.window)}
         self.stage_kernels = {"compress": "compress_kernel", "index_score": "score_tc_kernel",
-                              "index_select": "select_kernel", "attend": "attend_rows_kernel"}
+                              "index_select": "select_kernel", "attend": attend_kernel(wl.topk, wl.window)}
         self.units = B * Tq
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "query_tokens": Tq, "entries": self.N,
                           "index_pairs": pairs}
@@ -416,9 +423,10 @@ class GroupStep(StepBase):
             self.stage_bytes["L%d_%s" % (l, m)] = att + extra
             if Tq > 1 and m == "full":
                 self.stage_flops["L%d_%s" % (l, m)] = pairs * 8192
-        self.stage_kernels = {st: {"full": "compress + score_tc + select + attend_rows",
-                                   "reindex": "score_tc (gather) + select + attend_rows",
-                                   "reuse": "attend_rows"}[st.split("_")[1]]
+        att_k = attend_kernel(wl.topk, wl.window).replace("_kernel", "")
+        self.stage_kernels = {st: {"full": "compress + score_tc + select + " + att_k,
+                                   "reindex": "score_tc (gather) + select + " + att_k,
+                                   "reuse": att_k}[st.split("_")[1]]
                               for st in self.stages}
         self.units = B * Tq
         self.cfg_extra = {"batch_per_gpu": B, "ctx": ctx, "entries": self.N, "layers": len(self.layers),

@@ -901,19 +901,24 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(int q0, int Tq, 
                                                                 const float* bmax, int64_t score_stride,
                                                                 const uint32_t* krange, int kr_stride, int n_slots,
                                                                 int32_t* topk_out, int32_t* pool_out, int fused) {
-  griddep_wait();  // the scores are the previous kernel's output
-  griddep_launch();
   extern __shared__ __align__(16) unsigned char sel_raw[];
   SelShared& s = *reinterpret_cast<SelShared*>(sel_raw);
   __shared__ uint32_t r_lo, r_hi;
   const int cs = (int)tc::cluster_size(), rk = (int)tc::cluster_rank();
   const int qc = blockIdx.y, qi = q0 + qc, b = qi / Tq;
-  const int64_t nv = visible_entries(q_pos[qi], r, n_entries[b] < max_entries ? n_entries[b] : max_entries);
-  // the query's key range: the scoring CTAs' slots reduced
+  // the query's position and entry count are read before the wait: the
+  // previous kernel is always the scoring kernel of the same call, which
+  // writes neither and waited itself for whatever wrote them
+  const int64_t qp = q_pos[qi];
+  const int32_t ne = n_entries[b];
   if (threadIdx.x == 0) {
     r_lo = 0xFFFFFFFFu;
     r_hi = 0u;
   }
+  griddep_wait();  // the scores are the previous kernel's output
+  griddep_launch();
+  const int64_t nv = visible_entries(qp, r, ne < max_entries ? ne : (int32_t)max_entries);
+  // the query's key range: the scoring CTAs' slots reduced
   __syncthreads();
   {
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;

@@ -1058,9 +1058,12 @@ cudaError_t plan_index(const csa2_cfg& cfg, int B, int Tq, int max_entries, bool
   // least k blocks besides the forced one (what makes it exact)
   p->fused = !reindex && hsi_out && (int64_t)cfg.hsi_blocks * kHsiBlock <= kRound && cfg.hsi_blocks >= cfg.topk + 1;
   p->n_sel = (!reindex && hsi_out && !p->fused) ? 2 : 1;
+  // (a selection one CTA holds in registers, up to 2 kRound positions at 32
+  // keys a thread, stays on one CTA)
   const int64_t sel_groups = (int64_t)std::min(p->chunk, p->Q) * p->n_sel;
   p->cs = 1;
-  while (!p->fused && p->cs < 8 && (int64_t)p->cs * kMinCtaKeys < n_max && 2 * p->cs * sel_groups <= num_sms())
+  while (!p->fused && n_max > 2 * kRound && p->cs < 8 && (int64_t)p->cs * kMinCtaKeys < n_max &&
+         2 * p->cs * sel_groups <= num_sms())
     p->cs <<= 1;
   // one CTA holding every position of each selection: the register-resident
   // path only, compiled without the general one

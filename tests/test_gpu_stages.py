@@ -206,14 +206,14 @@ def test_index_topk_random_fp4_with_head_weights_and_ratio2():
     assert (g_top[0, 2] >= 0).sum() == 1 and g_top[0, 2, 0] == 0  # t = 1 sees entry 0 only
 
 
-@pytest.mark.parametrize("N", [20000, 16000])
+@pytest.mark.parametrize("N", [40000, 20000, 16000])
 def test_select_threshold_bin_beyond_shared_list_and_single_slots(N):
     """N - 500 copies of one indexer row among 500 random rows: fewer than k
     keys lie above the copies' key, so the k-th place falls inside a bin of
     more than 8192 equal keys (refined over the scores themselves, the first
-    ids win); N = 20000 selects over a two-CTA cluster, N = 16000 within one
-    CTA.  hsi_blocks = 1 keeps only the forced latest block and topk = 1 the
-    single best entry."""
+    ids win); N = 40000 selects over a cluster of CTAs, N = 20000 within one
+    CTA at 32 keys a thread, N = 16000 at 16.  hsi_blocks = 1 keeps only the
+    forced latest block and topk = 1 the single best entry."""
     B = 1
     oc = oracle.Cache(B, N, CI, "fp4")
     oc.codes[0], oc.scales[0] = synth.integer_fp4_bytes(synth.rng(26, "idx"), N, CI)

@@ -1596,13 +1596,17 @@ int qc_clusters() {
 }
 
 // Query-cluster attention for 4 or 5 row tiles: five CTAs of 128 rows per
-// query when the batch fits one wave that way, else four of 160 rows when
-// that saves a wave.  cudaErrorNotSupported when neither shape can run.
+// query when the batch fits one wave that way beside one more CTA per query
+// (the selection that precedes a decode attention holds one SM per query
+// while this kernel's CTAs start), else four of 160 rows when those fit one
+// wave, else whichever shape takes fewer waves.  cudaErrorNotSupported when
+// neither shape can run.
 template <int kDtype, bool kSwaFp8>
 cudaError_t launch_qc(const AttArgs& a, int Q, cudaStream_t stream) {
   const int c5 = qc_clusters<kDtype, kSwaFp8, 5>(), c4 = qc_clusters<kDtype, kSwaFp8, 4>();
   if (c5 < 1 && c4 < 1) return cudaErrorNotSupported;
-  const int64_t w5 = c5 > 0 ? (Q + c5 - 1) / c5 : INT64_MAX, w4 = c4 > 0 ? (Q + c4 - 1) / c4 : INT64_MAX;
+  int64_t w5 = c5 > 0 ? (Q + c5 - 1) / c5 : INT64_MAX, w4 = c4 > 0 ? (Q + c4 - 1) / c4 : INT64_MAX;
+  if (w5 == 1 && w4 == 1 && 6 * (int64_t)Q > num_sms()) w5 = 2;  // five beside the selection do not fit
   if (w4 < w5) {
     auto kern = attend_qc_kernel<kDtype, kSwaFp8, 4>;
     return launch_k(kern, dim3(4, Q), dim3(kThreads), kQcSmem, stream, 4, a);

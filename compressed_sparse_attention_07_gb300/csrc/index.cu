@@ -201,31 +201,48 @@ __device__ bool select_sampled(const float* vals, int64_t n, int k, int64_t forc
     s.above_n = 0;
   }
   __syncthreads();
-  // ---- the sample: block b of 32 keys at positions 512 b .. 512 b + 31
+  // ---- the sample: block b of 32 keys at positions 512 b .. 512 b + 31,
+  // eight blocks a warp in flight at once
   const int64_t nsb = (n + 511) / 512;
-  for (int64_t b = wid; b < nsb; b += kSelWarps) {
-    const int64_t p = 512 * b + lane;
-    const uint32_t kk = (p < n && p != forced) ? order_key(ld_score(vals + p)) : 0u;
-    if (kk) atomicAdd(&s.hist[bin_of(kk)], 1u);
+  constexpr int kSampleBatch = 8;
+  for (int64_t b0 = wid; b0 < nsb; b0 += (int64_t)kSelWarps * kSampleBatch) {
+    float sv[kSampleBatch];
+#pragma unroll
+    for (int u = 0; u < kSampleBatch; ++u) {
+      const int64_t p = 512 * (b0 + (int64_t)kSelWarps * u) + lane;
+      sv[u] = p < n ? ld_score(vals + p) : __uint_as_float(kScoreInvalid);
+    }
+#pragma unroll
+    for (int u = 0; u < kSampleBatch; ++u) {
+      const int64_t p = 512 * (b0 + (int64_t)kSelWarps * u) + lane;
+      const uint32_t kk = p != forced ? order_key(sv[u]) : 0u;
+      if (kk) atomicAdd(&s.hist[bin_of(kk)], 1u);
+    }
   }
   __syncthreads();
   const uint32_t target = (2 * need + 1024) / 16 + 32;
   find_cut(s.hist, kHistBins, target, s);
   const uint32_t tb_lo = s.cut_total >= target ? s.cut_bin : 0u;
   __syncthreads();
-  // ---- one pass: every key in a bin >= tb_lo, with its position
-  for (int64_t base = 0; base < n; base += kRound) {
-    float v[kPer];
+  // ---- one pass: every key in a bin >= tb_lo (key >= klo1; bin 0 takes
+  // every key, those below kmin too), with its position.  Rounds of kRound
+  // positions, the next round's loads in flight while this one is listed.
+  const uint32_t klo1 = tb_lo == 0u ? 1u : kmin + (tb_lo << sh);
+  auto load_round = [&](float (&v)[kPer], int64_t base) {
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int64_t p = base + threadIdx.x + kSelThreads * j;
       v[j] = p < n ? ld_score(vals + p) : __uint_as_float(kScoreInvalid);
     }
+  };
+  auto list_round = [&](const float (&v)[kPer], int64_t base) {
+    // j of this thread's forced position in the round, else -1
+    const int64_t fo = forced - base - threadIdx.x;
+    const int jf = (forced >= 0 && fo >= 0 && fo < (int64_t)kRound && fo % kSelThreads == 0) ? (int)(fo / kSelThreads) : -1;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int64_t p = base + threadIdx.x + kSelThreads * j;
-      const uint32_t kk = p == forced ? 0u : order_key(v[j]);
-      const bool m = kk != 0u && bin_of(kk) >= tb_lo;
+      const uint32_t kk = order_key(v[j]);
+      const bool m = kk >= klo1 && j != jf;
       const uint32_t bal = __ballot_sync(0xffffffffu, m);
       if (!bal) continue;
       uint32_t at = 0;
@@ -233,8 +250,19 @@ __device__ bool select_sampled(const float* vals, int64_t n, int k, int64_t forc
       at = __shfl_sync(0xffffffffu, at, 0) + __popc(bal & lt);
       if (m && at < (uint32_t)kCandMax) {
         s.cand[at] = kk - kmin;
-        s.merged[at] = (uint32_t)p;
+        s.merged[at] = (uint32_t)(base + threadIdx.x + kSelThreads * j);
       }
+    }
+  };
+  {
+    float va[kPer], vb[kPer];
+    load_round(va, 0);
+    for (int64_t base = 0; base < n; base += 2 * (int64_t)kRound) {
+      if (base + kRound < n) load_round(vb, base + kRound);
+      list_round(va, base);
+      if (base + kRound >= n) break;
+      if (base + 2 * kRound < n) load_round(va, base + 2 * kRound);
+      list_round(vb, base + kRound);
     }
   }
   __syncthreads();

@@ -760,7 +760,7 @@ __device__ __noinline__ void select_small(const float* vals, int64_t n, int k, i
   }
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) s.hist[i] = 0;
   if (threadIdx.x == 0) s.cand_n = 0;
-  // this thread's positions as bits of 16-bit masks (bit m: position p0 + m)
+  // this thread's positions as bits of kP-bit masks (bit m: position p0 + m)
   const uint32_t fm = (has_forced && forced >= p0 && forced < p0 + kP) ? 1u << (int)(forced - p0) : 0u;
   uint32_t kk[kP];
 #pragma unroll

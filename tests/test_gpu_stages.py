@@ -482,10 +482,13 @@ def test_captured_index_and_attend_replay_on_new_data():
     ("fp4", 1024, 512, 40, 1),   # too many clusters for one wave: the per-query kernel
     ("fp4", 768, 0, 3, 2),       # six tiles of top-k rows and no window
     ("fp4", 640, 256, 3, 2),     # windows clipped at the sequence start
+    ("fp4", 512, 128, 24, 1),    # the model's five row tiles: clusters of five beside the selection
+    ("fp4", 512, 128, 28, 1),    # ... clusters of four (five would not fit beside the selection)
 ])
 def test_attend_larger_selections_and_windows(dtype, k, W, B, Tq):
     """The attention kernels for configurations beyond six row tiles (maximum
-    top-k 1024 and window 512) and without a window, against the oracle."""
+    top-k 1024 and window 512) and without a window, and the query-cluster
+    kernel in both of its cluster shapes, against the oracle."""
     N = 3000
     oc, pc = _main_caches(B, N, dtype, seed=70 + k + W)
     g = synth.rng(70, "ids%d" % k)

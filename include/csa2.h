@@ -17,9 +17,13 @@
  *  - Every kernel is launched as a programmatic dependent launch: it may
  *    start while the kernel enqueued just before it on the stream finishes.
  *    Each kernel of this library waits for that kernel's completion (and
- *    the visibility of its writes) before reading any argument, with one
- *    exception, named at csa2_attend and csa2_layer: the decode attention
- *    reads q, the window rows and their positions before that wait.
+ *    the visibility of its writes) before reading any argument, with two
+ *    exceptions: the selection reads q_pos and n_entries before that wait
+ *    (its predecessor is the scoring kernel of the same indexer call, which
+ *    writes neither; csa2_index_select follows csa2_index_score with the
+ *    same q_pos and n_entries), and the decode attention reads q, the
+ *    window rows and their positions before it (named at csa2_attend and
+ *    csa2_layer).
  *    Because every kernel of this library waits before it lets its own
  *    successor start, placing any call of this library between the kernel
  *    that writes those inputs and the attention satisfies the rule.

@@ -430,22 +430,33 @@ __global__ void __launch_bounds__(Shape<kDtype, QPC, kGather>::kThreads, 1) scor
     hw[i / kIdxHeads][i % kIdxHeads] =
         (a.head_w && i / kIdxHeads < n_act) ? 0.5f * __ldg(a.head_w + (int64_t)g0 * kIdxHeads + i) : 0.5f;
   if (kGather) {
-    for (int i = tid; i < n_my * 128; i += kConsumers) {
+    // this thread's positions i = tid + kConsumers * u: every pool entry
+    // loaded first, then every block-table entry, so that the loads of its
+    // positions are in flight together rather than one pair after another
+    constexpr int kIt = (kMaxGatherTiles * 128 + kConsumers - 1) / kConsumers;
+    int32_t blkv[kIt];
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      const int i = tid + kConsumers * u;
       const int64_t p = t_begin * 128 + i;  // pool position
+      blkv[u] = (i < n_my * 128 && p < npos) ? __ldg(a.pool + (int64_t)g0 * a.n_blocks + p / kHsiBlock) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      const int i = tid + kConsumers * u;
+      const int64_t p = t_begin * 128 + i;
+      const int32_t blk = blkv[u];
       int32_t e = -1;
-      if (p < npos) {
-        const int32_t blk = __ldg(a.pool + (int64_t)g0 * a.n_blocks + p / kHsiBlock);
-        if (blk >= 0) {
-          const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
-          if ((int64_t)blk * kHsiBlock >= a.max_entries) {
-            if (p % kHsiBlock == 0) report(a.status, CSA2_ERR_BAD_INDEX);
-          } else if (j < nv[0]) {
-            const int64_t page = page_of(a.ic, b, j, a.status);
-            if (page >= 0) e = (int32_t)(page * kPage + j % kPage);
-          }
+      if (blk >= 0) {
+        const int64_t j = (int64_t)blk * kHsiBlock + p % kHsiBlock;
+        if ((int64_t)blk * kHsiBlock >= a.max_entries) {
+          if (p % kHsiBlock == 0) report(a.status, CSA2_ERR_BAD_INDEX);
+        } else if (j < nv[0]) {
+          const int64_t page = page_of(a.ic, b, j, a.status);
+          if (page >= 0) e = (int32_t)(page * kPage + j % kPage);
         }
       }
-      gtab[i] = e;
+      if (i < n_my * 128) gtab[i] = e;
     }
   }
   tc::fence_async_smem();  // the Q tile is read by the tensor core

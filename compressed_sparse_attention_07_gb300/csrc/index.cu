@@ -3,9 +3,10 @@
 // top-k selection with the (score desc, id asc) order.
 // (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.3.1, 2.3.2, 2.3.4; 36kr "CSA2".)
 // The selection kernel holds a query's keys in registers when they fit one
-// CTA (decode), stages them through shared memory in rounds otherwise, with
-// a sampled one-pass variant for very long rows and clusters of CTAs when
-// few queries leave SMs idle; every variant gives the same exact result.
+// CTA (up to 32768 positions, 16 or 32 keys a thread), stages them through
+// shared memory in rounds otherwise, with a sampled one-pass variant for
+// very long rows and clusters of CTAs when few queries leave SMs idle;
+// every variant gives the same exact result.
 #include <algorithm>
 
 #include "internal.h"

@@ -5,16 +5,19 @@
 // out_h = sum_e p_e c_e, the same 512-channel latent serving as key and value
 // (DeepSeek-V4.1 Flash, hn.213312.xyz sec. 2.2.2 and sec. 3.3.1; 36kr "CSA2").
 //
-// Three kernels, chosen by the number of 128-row tiles (top-k tiles, then
+// Four kernels, chosen by the number of 128-row tiles (top-k tiles, then
 // window tiles):
-//  - attend_rows_kernel (up to 6 tiles, the model's 512 + 128): one CTA per
-//    (query, tile) for all 64 heads, the query's tiles in one cluster; each
-//    CTA gathers and decodes its rows once, computes S = C.Q^T, a partial
-//    softmax and O = C^T.P^T on the tensor cores, and the partial outputs
-//    are merged through distributed shared memory (the only kernel that
-//    reads MXFP8 window rows); launched while the selection still runs, it
-//    first brings the query rows, the window rows and the block table into
-//    L2 (hints only), then waits for the selected ids;
+//  - attend_qc_kernel (4 or 5 tiles, the model's 512 + 128): a cluster of 4
+//    or 5 CTAs per query, each holding 160 or 128 of its rows for all 64
+//    heads; each CTA gathers and decodes its rows once, computes S = C.Q^T,
+//    a partial softmax and O = C^T.P^T on the tensor cores, and the partial
+//    outputs are merged through distributed shared memory; launched while
+//    the selection still runs, it loads the query and window rows and
+//    brings the block table into L2 before it waits for the selected ids
+//    (in a Reuse layer it gathers its selected rows before the wait too);
+//  - attend_rows_kernel (other counts up to 6 tiles): one CTA per (query,
+//    tile), the query's tiles in one cluster, otherwise the same (these two
+//    read MXFP8 window rows);
 //  - attend_split_kernel (up to 16 tiles, few queries): the same with 16
 //    heads per CTA;
 //  - attend_tc_kernel (otherwise): one CTA per (query, group of HG heads)
